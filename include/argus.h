@@ -1,0 +1,246 @@
+/*
+ * argus.h -- C ABI of the GB300 (sm_103a) paged mixed-codec decode-attention library.
+ *
+ * The operations follow three web pages:
+ *   [ARGUS]  "ARGUS: Heterogeneous KV-cache memory management" (argus-cache 0.5.1),
+ *            sections "Why decode is slow" and "Direct paged attention".
+ *   [PR499]  "feat(kvcache): host-RAM KV tier for sparse-attention models
+ *            (--kv-host-pages)" (FreeToken pull request #499) with its update
+ *            20f3b23 and the comment describing "--kv-placement host".
+ *   [STORE]  "Storage contracts for hybrid KV cache offloading".
+ *
+ * Conventions shared by every entry point
+ *   - Every data pointer is a DEVICE pointer owned by the caller; pointers to
+ *     argus_geom / argus_pool / argus_decode_args structs are HOST pointers.
+ *   - The library allocates, frees and synchronises nothing.  Every call only
+ *     validates its arguments on the host and enqueues kernels on `stream`
+ *     (a cudaStream_t; NULL = the legacy default stream).
+ *   - The return value reports host-side validation and launch errors only:
+ *     ARGUS_E_INVALID for malformed arguments, ARGUS_E_UNSUPPORTED for a
+ *     shape / codec combination this build does not implement (there is no
+ *     fallback), ARGUS_E_WORKSPACE for a workspace that is too small,
+ *     ARGUS_E_LAUNCH when the CUDA launch itself failed.  argus_last_error()
+ *     returns a one-line reason for the calling thread's last failure.
+ *   - Anomalies found on the device (a block-table slot outside its pool, a
+ *     selection entry outside the sequence, more selection entries than the
+ *     list width) are never trapped: the kernel skips the entry and adds one
+ *     to a caller-provided counter.
+ *   - Supported geometry: head_dim in {64, 128}; page_tokens a positive
+ *     multiple of 16; n_q_heads a multiple of n_kv_heads with
+ *     G = n_q_heads / n_kv_heads between 1 and 8.
+ *   - Calls are stateless and thread safe.  Calls that share a workspace
+ *     must not run concurrently on the GPU.
+ *
+ * Pool layout (one pool per codec; a pool is an array of physical page slots):
+ *   codes  [n_slots][2 (K, V)][Hkv][P][row]   row = head_dim 16-bit values
+ *          (FP16 / BF16), head_dim bytes (FP8 e4m3 / INT8), head_dim/2 bytes
+ *          (INT4: two codes per byte, the even element in the low nibble)
+ *   meta   FP16 / BF16: unused (NULL)
+ *          FP8 / INT8:  float [n_slots][2][Hkv]  one scale per (page, head, K|V)
+ *          INT4:        half2 {scale, zero} [n_slots][2][Hkv][P][head_dim/32]
+ *   Dequantised value: FP8 e4m3_value(code) * scale; INT8 code * scale;
+ *   INT4 code * scale + zero.  Codes and pools must be 16-byte aligned.
+ */
+#ifndef ARGUS_H
+#define ARGUS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ARGUS_OK = 0,
+  ARGUS_E_INVALID = 1,
+  ARGUS_E_UNSUPPORTED = 2,
+  ARGUS_E_WORKSPACE = 3,
+  ARGUS_E_LAUNCH = 4
+} argus_status;
+
+/* Codec tiers of [ARGUS] (summary; "Direct paged attention": FP16, Q8, Q4 pages)
+ * and [PR499] update 20f3b23 ("e4m3 codes + fp32 scales"). */
+typedef enum {
+  ARGUS_FP16 = 0,
+  ARGUS_BF16 = 1,
+  ARGUS_FP8_E4M3 = 2,
+  ARGUS_INT8 = 3,
+  ARGUS_INT4_G32 = 4
+} argus_codec;
+
+typedef struct {
+  int32_t n_q_heads;    /* Hq */
+  int32_t n_kv_heads;   /* Hkv; G = Hq / Hkv query heads share one KV head */
+  int32_t head_dim;     /* D */
+  int32_t page_tokens;  /* P */
+} argus_geom;
+
+typedef struct {
+  int32_t codec;        /* argus_codec of every page in this pool */
+  int32_t reserved;     /* must be 0 */
+  void* codes;          /* device, layout above */
+  void* meta;           /* device, layout above; NULL for FP16 / BF16 */
+  int64_t n_slots;      /* physical page slots in the pool */
+} argus_pool;
+
+/* ---------------------------------------------------------------------------
+ * argus_quantize_pages -- page demotion through the codec tiers.
+ *
+ * [ARGUS] summary: older pages are demoted from FP16 through FP8, INT8, INT4;
+ * [PR499] update 20f3b23: the pool holds e4m3 codes + fp32 scales and is the
+ * source of truth.  For each listed page i and each (K|V, KV head h) unit:
+ *   FP8:  a = max|x| over the unit's valid tokens; scale = a / 448 (fp32);
+ *         code = e4m3 round-to-nearest-even, saturating at +-448, of x / scale.
+ *   INT8: scale = a / 127; code = clamp(rint_even(x / scale), -127, 127).
+ *   INT4: per token and 32-element group: z = fp16_sat(min), s = fp16_sat(
+ *         (max - z) / 15); code = s > 0 ? clamp(rint_even((x - z) / s), 0, 15) : 0.
+ *   FP16 / BF16 destination (equal to src_dtype): a copy.
+ *   a == 0 gives scale 0 and all-zero codes.  Every division is IEEE fp32.
+ * Arguments
+ *   g            geometry (host)
+ *   src_dtype    ARGUS_FP16 or ARGUS_BF16
+ *   src_codes    device [n_src_slots][2][Hkv][P][D] 16-bit source pages
+ *   src_slots    device int32 [n_pages] source slot of page i
+ *   dst          host descriptor of the destination pool
+ *   dst_slots    device int32 [n_pages] destination slot of page i
+ *   n_pages      pages to demote (0 is a no-op)
+ *   valid_tokens device int32 [n_pages] or NULL (= P): tokens >= valid are
+ *                left out of the reductions and stored as zero codes / zero meta
+ *   ckey_out     device bf16 [n_pages][Hkv][D] or NULL: compressed key of each
+ *                page = mean over the valid tokens of the stored (dequantised)
+ *                keys, summed in fp32 and rounded to bf16 ([PR499] "Why this
+ *                works": the indexer scores a compressed slab)
+ * Slots outside their pools are skipped on the device (counted in *status if
+ * status != NULL, device uint32).
+ * ------------------------------------------------------------------------- */
+argus_status argus_quantize_pages(const argus_geom* g, int32_t src_dtype,
+                                  const void* src_codes, int64_t n_src_slots,
+                                  const int32_t* src_slots, const argus_pool* dst,
+                                  const int32_t* dst_slots, int32_t n_pages,
+                                  const int32_t* valid_tokens, void* ckey_out,
+                                  uint32_t* status, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * argus_paged_decode_attn -- single-token decode attention over a paged,
+ * mixed-codec KV cache.
+ *
+ * [ARGUS] "Direct paged attention": an exact tile-by-tile online-softmax
+ * recurrence over a structure-of-arrays page table (precision separate from
+ * placement); "Why decode is slow": one compressed page at a time, grouped-
+ * query attention.  [PR499] "Design": logical pages are translated to physical
+ * slots through a block table; "Why this works": attention may be restricted
+ * to the indexer's selected pages.  Result, per batch row b and query head hq
+ * (KV head h = hq / G):
+ *   o = sum_j softmax_j(softmax_scale * q . k_j) v_j,
+ *   lse2 = log2 sum_j 2^(softmax_scale * q . k_j * log2 e),
+ * over the visible tokens j (positions < seq_lens[b]) of all logical pages, or
+ * of the selected pages when sel_pages != NULL; k_j, v_j are dequantised in
+ * registers from the page's codec.  An empty visible set gives o = 0 and
+ * lse2 = -inf.  Partial results of context splits are folded by log2-sum-exp.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  argus_geom g;
+  int32_t batch;              /* B */
+  int32_t q_dtype;            /* ARGUS_FP16 or ARGUS_BF16 */
+  const void* q;              /* device [B][Hq][D] */
+  const argus_pool* pools;    /* host array, at most one pool per codec */
+  int32_t n_pools;
+  int32_t max_pages;          /* row length of page_codec / block_table */
+  const uint8_t* page_codec;  /* device [B][max_pages] codec of logical page p */
+  const int32_t* block_table; /* device [B][max_pages] slot of logical page p */
+  const int32_t* seq_lens;    /* device [B] tokens; at most max_pages * P are read */
+  const int32_t* sel_pages;   /* device [B][Hkv][sel_width] logical pages, or NULL */
+  const int32_t* sel_count;   /* device [B][Hkv] entries used, or NULL */
+  int32_t sel_width;
+  float softmax_scale;
+  void* out;                  /* device [B][Hq][D] in out_dtype, or NULL */
+  int32_t out_dtype;          /* ARGUS_FP16 or ARGUS_BF16 */
+  float* out_f32;             /* device [B][Hq][D] fp32 output, or NULL */
+  float* lse2_out;            /* device [B][Hq] log2-sum-exp, or NULL */
+  uint32_t* status;           /* device uint32 anomaly counter, or NULL */
+  int32_t num_splits;         /* context splits per (b, KV head); 0 = automatic */
+} argus_decode_args;
+
+/* Workspace needed by argus_paged_decode_attn for these arguments.  The
+ * workspace starts with a block of split counters: those bytes must be zero
+ * the first time a workspace is used (allocate it zero-filled); every call
+ * leaves them zero again. */
+argus_status argus_decode_workspace_bytes(const argus_decode_args* args, size_t* bytes);
+
+argus_status argus_paged_decode_attn(const argus_decode_args* args, void* ws,
+                                     size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * argus_select_pages -- the indexer: top-k page selection over a compressed
+ * key slab ([PR499] "Why this works for sparse attention"; "Design": fixed-
+ * width list of 2*top_k + 8 entries with a drop counter).
+ *   score(b, h, p) = sum over the G query heads of KV head h of q . ckey[b][p][h]
+ *   (fp32).  Candidates are pages 0 .. n_pages[b]-1, minus the newest page when
+ *   keep_newest; the top_k highest scores are kept (ties to the lower page
+ *   index); the newest page is then added.  The list is written in ascending
+ *   page order to sel_pages[b][h][0 .. sel_count[b][h]-1]; unused entries are
+ *   -1.  Entries that do not fit in sel_width are dropped, lowest score first,
+ *   and counted in *drop_counter.
+ * Arguments: q device [B][Hq][D] (q_dtype FP16 / BF16); ckeys device bf16
+ * [B][max_pages][Hkv][D] in logical page order; n_pages device int32 [B]
+ * (values above max_pages are clamped and counted as drops); ws of
+ * argus_select_workspace_bytes bytes.
+ * ------------------------------------------------------------------------- */
+argus_status argus_select_workspace_bytes(const argus_geom* g, int32_t batch,
+                                          int32_t max_pages, size_t* bytes);
+
+argus_status argus_select_pages(const argus_geom* g, int32_t batch, const void* q,
+                                int32_t q_dtype, const void* ckeys,
+                                const int32_t* n_pages, int32_t max_pages,
+                                int32_t top_k, int32_t keep_newest,
+                                int32_t* sel_pages, int32_t* sel_count,
+                                int32_t sel_width, uint32_t* drop_counter,
+                                void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * argus_fold_lse -- fold partial attention results into an fp32 accumulator
+ * by their log2-sum-exp ([PR499] comment on "--kv-placement host": windows are
+ * folded by log2-sum-exp into a float32 accumulator).  In place, per row r:
+ *   L = max(La, Lb) + log2(2^(La - max) + 2^(Lb - max));
+ *   acc_o = 2^(La - L) acc_o + 2^(Lb - L) part_o;  acc_lse2 = L;
+ * a side with lse2 = -inf is the identity.
+ * acc_o / part_o device float [n_rows][head_dim]; acc_lse2 / part_lse2 device
+ * float [n_rows].  head_dim must be a multiple of 4 and the float arrays
+ * 16-byte aligned.
+ * ------------------------------------------------------------------------- */
+argus_status argus_fold_lse(int64_t n_rows, int32_t head_dim, float* acc_o,
+                            float* acc_lse2, const float* part_o,
+                            const float* part_lse2, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * argus_window_prefill_attn -- attention of a query chunk against one window
+ * of cached keys, folded into an fp32 accumulator ([PR499] comment on
+ * "--kv-placement host": cached pages are staged into a 131,072-token device
+ * window, attended per window, and the windows folded by log2-sum-exp).
+ *   Key j of the window is at absolute position win_pos0 + j; query row i at
+ *   q_pos0 + i; the key is visible iff win_pos0 + j <= q_pos0 + i.
+ *   fold = 0: acc_o / acc_lse2 are overwritten with this window's (o, lse2);
+ *   fold = 1: the window's result is folded into them as argus_fold_lse does.
+ * Arguments: q device bf16 [Hq][n_q][D]; k, v device bf16 with element
+ * (h, j, d) at h * kv_head_stride + j * D + d (kv_head_stride = 0 means
+ * win_len * D); acc_o device float [Hq][n_q][D]; acc_lse2 [Hq][n_q].
+ * Supported: head_dim 128, n_q a multiple of 128, win_len a multiple of 128.
+ * ------------------------------------------------------------------------- */
+argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n_q,
+                                       const void* q, const void* k, const void* v,
+                                       int64_t kv_head_stride, int64_t win_len,
+                                       int64_t win_pos0, int64_t q_pos0,
+                                       float softmax_scale, float* acc_o,
+                                       float* acc_lse2, int32_t fold, void* stream);
+
+const char* argus_status_string(argus_status s);
+
+/* One-line reason for the calling thread's most recent non-OK status. */
+const char* argus_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ARGUS_H */

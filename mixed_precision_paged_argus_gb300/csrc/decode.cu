@@ -1,0 +1,850 @@
+// argus_paged_decode_attn: single-token decode attention over a paged KV cache
+// whose pages each sit in their own codec tier (FP16 / BF16 / FP8 e4m3 / INT8 /
+// INT4 group-32).
+//
+// Method ("ARGUS: Heterogeneous KV-cache memory management", sections "Why
+// decode is slow" and "Direct paged attention"): an exact online softmax
+// consumes the cache one page tile at a time through a structure-of-arrays
+// page table, with grouped-query attention; nothing context-sized is ever
+// materialised.  The block table translates logical pages to physical slots
+// and the page list may be the indexer's selection ("feat(kvcache): host-RAM KV
+// tier for sparse-attention models", sections "Why this works for sparse
+// attention" and "Design").  Context splits are folded by log2-sum-exp.
+//
+// GB300 design
+//  * grid (split, KV head, batch row); 4 consumer warps + 1 producer warp.
+//  * The producer walks the split's 16-token chunks, translates each through
+//    the block table and streams its K and V rows (plus INT4 group metadata)
+//    into a ring of shared-memory stages with 1-D cp.async.bulk copies that
+//    complete on mbarriers; every chunk is one contiguous run of a page.
+//  * Each consumer warp owns one chunk per stage.  Codes are dequantised in
+//    registers straight into m16n8k16 tensor-core fragments: tokens on M, the
+//    G <= 8 query heads of the KV head on N, head_dim on K.  FP8 and INT8 codes
+//    are exact in fp16, so their per-(page, head) scales are applied outside the
+//    MMA (K scale on the scores; V scale folded into the accumulator's running
+//    rescale), keeping the dot products exact.
+//  * Online softmax in the log2 domain; P is transposed in registers
+//    (movmatrix) into the B fragment of the P.V MMA, whose A operand is V^T
+//    assembled from pairs of token rows with byte permutes.
+//  * Warps merge in shared memory; splits merge in the last CTA to finish
+//    (atomic ticket on a caller-provided counter, reset afterwards).
+#include <algorithm>
+#include <cmath>
+
+#include "common.cuh"
+
+namespace argus {
+namespace decode {
+
+constexpr int kChunk = 16;
+constexpr int kConsumerWarps = 4;
+constexpr int kChunksPerStage = kConsumerWarps;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kMaxG = 8;
+constexpr int kMaxSplits = 1024;  // bounds the fold's shared-memory weights
+
+enum Family { kFamF16 = 0, kFamBF16 = 1, kFamMixed = 2 };
+
+struct Params {
+  int B, Hkv, G, P, max_pages;
+  const void* q;
+  const uint8_t* codes[5];
+  const uint8_t* meta[5];
+  long long n_slots[5];
+  const uint8_t* page_codec;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const int32_t* sel_pages;
+  const int32_t* sel_count;
+  int sel_width;
+  float scale_log2;
+  void* out;
+  int out_bf16;
+  float* out_f32;
+  float* lse2_out;
+  uint32_t* status;
+  int cps;         // chunks per split, a multiple of kChunksPerStage
+  int num_splits;  // grid.x
+  uint32_t* counters;
+  float* part;     // [B][Hkv][num_splits][G][D + 1]
+};
+
+struct ChunkDesc {
+  int32_t codec;  // -1: empty slot in the stage
+  int32_t n_valid;
+  float kscale;
+  float vscale;
+};
+
+template <int D>
+struct Layout {
+  static constexpr int kNI = D / 32;                   // 32-dim groups per row
+  static constexpr int kKV = kChunk * 2 * D;           // K (or V) bytes of a chunk, 16-bit
+  static constexpr int kMeta = kChunk * kNI * 4;       // INT4 {scale, zero} of a chunk
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kKV;
+  static constexpr int kOffMK = 2 * kKV;
+  static constexpr int kOffMV = 2 * kKV + kMeta;
+  static constexpr int kChunkBytes = 2 * kKV + 2 * kMeta;
+  static constexpr int kStageBytes = kChunksPerStage * kChunkBytes;
+  static constexpr int kStages = (D == 128) ? 3 : 4;
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kBarOff = kRingBytes;
+  static constexpr int kDescOff = kBarOff + 2 * kStages * 8;
+  static constexpr int kMiscOff = kDescOff + kStages * kChunksPerStage * (int)sizeof(ChunkDesc);
+  static constexpr int kSmemBytes = kMiscOff + 64;
+  static constexpr int kMinBlocks = (D == 128) ? 2 : 3;
+};
+
+__device__ __forceinline__ void consumer_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+__device__ __forceinline__ int codec_family(int codec) { return codec == ARGUS_BF16 ? 1 : 0; }
+
+__device__ __forceinline__ uint32_t f16_magic_pair(uint32_t u, uint32_t sel) {
+  // bytes of u (already biased to unsigned) -> f16 (1024 + byte) pairs
+  return prmt(u, 0x64646464u, sel);
+}
+
+// K fragments of one chunk: a[c][0..3] are the m16n8k16 A registers of k-chunk
+// c for token rows r and r + 8.  Inside each 8-element run of head_dim held by
+// a lane, k positions (2t, 2t+1, 2t+8, 2t+9) of k-chunk 2i+hh map to elements
+// (2hh, 2hh+4, 2hh+1, 2hh+5); the query fragments use the same map.
+template <int D>
+__device__ __forceinline__ void load_k_frags(int codec, const uint8_t* chunk, int r, int t,
+                                             uint32_t (&a)[D / 16][4]) {
+  using L = Layout<D>;
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    const int row = r + 8 * rr;
+    if (codec == ARGUS_FP16 || codec == ARGUS_BF16) {
+#pragma unroll
+      for (int i = 0; i < L::kNI; ++i) {
+        const uint4 x = *reinterpret_cast<const uint4*>(chunk + L::kOffK + row * 2 * D + 64 * i + 16 * t);
+        a[2 * i][rr] = prmt(x.x, x.z, 0x5410);
+        a[2 * i][2 + rr] = prmt(x.x, x.z, 0x7632);
+        a[2 * i + 1][rr] = prmt(x.y, x.w, 0x5410);
+        a[2 * i + 1][2 + rr] = prmt(x.y, x.w, 0x7632);
+      }
+    } else if (codec == ARGUS_FP8_E4M3) {
+#pragma unroll
+      for (int i = 0; i < L::kNI; ++i) {
+        const uint2 x = *reinterpret_cast<const uint2*>(chunk + L::kOffK + row * D + 32 * i + 8 * t);
+        const uint32_t u = prmt(x.x, x.y, 0x5140);  // e0 e4 e1 e5
+        const uint32_t v = prmt(x.x, x.y, 0x7362);  // e2 e6 e3 e7
+        a[2 * i][rr] = e4m3x2_to_f16x2(u);
+        a[2 * i][2 + rr] = e4m3x2_to_f16x2(u >> 16);
+        a[2 * i + 1][rr] = e4m3x2_to_f16x2(v);
+        a[2 * i + 1][2 + rr] = e4m3x2_to_f16x2(v >> 16);
+      }
+    } else if (codec == ARGUS_INT8) {
+#pragma unroll
+      for (int i = 0; i < L::kNI; ++i) {
+        const uint2 x = *reinterpret_cast<const uint2*>(chunk + L::kOffK + row * D + 32 * i + 8 * t);
+        const uint32_t u = prmt(x.x, x.y, 0x5140) ^ 0x80808080u;
+        const uint32_t v = prmt(x.x, x.y, 0x7362) ^ 0x80808080u;
+        const uint32_t bias = 0x64806480u;  // 1152 = 1024 + 128
+        a[2 * i][rr] = hsub2_u32(f16_magic_pair(u, 0x4140), bias);
+        a[2 * i][2 + rr] = hsub2_u32(f16_magic_pair(u, 0x4342), bias);
+        a[2 * i + 1][rr] = hsub2_u32(f16_magic_pair(v, 0x4140), bias);
+        a[2 * i + 1][2 + rr] = hsub2_u32(f16_magic_pair(v, 0x4342), bias);
+      }
+    } else {  // INT4 group 32
+#pragma unroll
+      for (int i = 0; i < L::kNI; ++i) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(chunk + L::kOffK + row * (D / 2) + 16 * i + 4 * t);
+        const uint32_t mz = *reinterpret_cast<const uint32_t*>(chunk + L::kOffMK + (row * L::kNI + i) * 4);
+        const uint32_t s2 = prmt(mz, mz, 0x1010);
+        const uint32_t z2 = prmt(mz, mz, 0x3232);
+        const uint32_t magic = 0x64006400u;
+        a[2 * i][rr] = hfma2_u32(hsub2_u32(lop3_and_or(w, 0x000F000Fu, magic), magic), s2, z2);
+        a[2 * i][2 + rr] = hfma2_u32(hsub2_u32(lop3_and_or(w >> 4, 0x000F000Fu, magic), magic), s2, z2);
+        a[2 * i + 1][rr] = hfma2_u32(hsub2_u32(lop3_and_or(w >> 8, 0x000F000Fu, magic), magic), s2, z2);
+        a[2 * i + 1][2 + rr] = hfma2_u32(hsub2_u32(lop3_and_or(w >> 12, 0x000F000Fu, magic), magic), s2, z2);
+      }
+    }
+  }
+}
+
+// V^T fragments of one chunk: v[j][0..3] are the A registers of m-block j of
+// the P.V MMA (M = head_dim, K = tokens).  Lane (r, t) holds dims
+// [DL*r, DL*r + DL) with m-block j covering dims DL*r + 2j (rows r) and
+// DL*r + 2j + 1 (rows r + 8), and token rows 2t, 2t+1 (k 0..7) and 2t+8, 2t+9.
+template <int D>
+__device__ __forceinline__ void load_v_frags(int codec, const uint8_t* chunk, int r, int t,
+                                             uint32_t (&v)[D / 16][4]) {
+  using L = Layout<D>;
+  constexpr int DL = D / 8;
+  const int rows[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+  if (codec == ARGUS_FP16 || codec == ARGUS_BF16) {
+    uint32_t w[4][DL / 2];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint8_t* src = chunk + L::kOffV + rows[q] * 2 * D + 2 * DL * r;
+      if constexpr (DL == 16) {
+        // odd t read the two 16-byte halves in the other order (fewer bank conflicts)
+        const int sw = t & 1;
+        const uint4 x0 = *reinterpret_cast<const uint4*>(src + 16 * sw);
+        const uint4 x1 = *reinterpret_cast<const uint4*>(src + 16 * (sw ^ 1));
+        const uint4 lo = sw ? x1 : x0, hi = sw ? x0 : x1;
+        w[q][0] = lo.x; w[q][1] = lo.y; w[q][2] = lo.z; w[q][3] = lo.w;
+        w[q][4] = hi.x; w[q][5] = hi.y; w[q][6] = hi.z; w[q][7] = hi.w;
+      } else {
+        const uint4 x = *reinterpret_cast<const uint4*>(src);
+        w[q][0] = x.x; w[q][1] = x.y; w[q][2] = x.z; w[q][3] = x.w;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < D / 16; ++j) {
+      v[j][0] = prmt(w[0][j], w[1][j], 0x5410);
+      v[j][1] = prmt(w[0][j], w[1][j], 0x7632);
+      v[j][2] = prmt(w[2][j], w[3][j], 0x5410);
+      v[j][3] = prmt(w[2][j], w[3][j], 0x7632);
+    }
+  } else if (codec == ARGUS_FP8_E4M3 || codec == ARGUS_INT8) {
+    uint32_t w[4][DL / 4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint8_t* src = chunk + L::kOffV + rows[q] * D + DL * r;
+      if constexpr (DL == 16) {
+        const uint4 x = *reinterpret_cast<const uint4*>(src);
+        w[q][0] = x.x; w[q][1] = x.y; w[q][2] = x.z; w[q][3] = x.w;
+      } else {
+        const uint2 x = *reinterpret_cast<const uint2*>(src);
+        w[q][0] = x.x; w[q][1] = x.y;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < DL / 4; ++k) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int q0 = 2 * half;  // rows (2t, 2t+1) or (2t+8, 2t+9)
+        const uint32_t u = prmt(w[q0][k], w[q0 + 1][k], 0x5140);  // a0 b0 a1 b1
+        const uint32_t y = prmt(w[q0][k], w[q0 + 1][k], 0x7362);  // a2 b2 a3 b3
+        if (codec == ARGUS_FP8_E4M3) {
+          v[2 * k][2 * half + 0] = e4m3x2_to_f16x2(u);
+          v[2 * k][2 * half + 1] = e4m3x2_to_f16x2(u >> 16);
+          v[2 * k + 1][2 * half + 0] = e4m3x2_to_f16x2(y);
+          v[2 * k + 1][2 * half + 1] = e4m3x2_to_f16x2(y >> 16);
+        } else {
+          const uint32_t bias = 0x64806480u;
+          const uint32_t ub = u ^ 0x80808080u, yb = y ^ 0x80808080u;
+          v[2 * k][2 * half + 0] = hsub2_u32(f16_magic_pair(ub, 0x4140), bias);
+          v[2 * k][2 * half + 1] = hsub2_u32(f16_magic_pair(ub, 0x4342), bias);
+          v[2 * k + 1][2 * half + 0] = hsub2_u32(f16_magic_pair(yb, 0x4140), bias);
+          v[2 * k + 1][2 * half + 1] = hsub2_u32(f16_magic_pair(yb, 0x4342), bias);
+        }
+      }
+    }
+  } else {  // INT4
+    uint32_t w[4][DL / 8];
+    uint32_t m[4];
+    const int grp = (DL * r) / 32;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint8_t* src = chunk + L::kOffV + rows[q] * (D / 2) + (DL / 2) * r;
+      if constexpr (DL == 16) {
+        const uint2 x = *reinterpret_cast<const uint2*>(src);
+        w[q][0] = x.x; w[q][1] = x.y;
+      } else {
+        w[q][0] = *reinterpret_cast<const uint32_t*>(src);
+      }
+      m[q] = *reinterpret_cast<const uint32_t*>(chunk + L::kOffMV + (rows[q] * L::kNI + grp) * 4);
+    }
+    const uint32_t magic = 0x64006400u;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int q0 = 2 * half;
+      const uint32_t s2 = prmt(m[q0], m[q0 + 1], 0x5410);
+      const uint32_t z2 = prmt(m[q0], m[q0 + 1], 0x7632);
+#pragma unroll
+      for (int k = 0; k < DL / 8; ++k) {
+        const uint32_t lo = prmt(w[q0][k], w[q0 + 1][k], 0x5410);  // nibbles 0..3 of a | of b
+        const uint32_t hi = prmt(w[q0][k], w[q0 + 1][k], 0x7632);  // nibbles 4..7
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          const uint32_t c0 = hsub2_u32(lop3_and_or(lo >> (4 * s), 0x000F000Fu, magic), magic);
+          const uint32_t c1 = hsub2_u32(lop3_and_or(hi >> (4 * s), 0x000F000Fu, magic), magic);
+          const int d0 = 8 * k + s, d1 = 8 * k + 4 + s;
+          v[d0 / 2][2 * half + (d0 & 1)] = hfma2_u32(c0, s2, z2);
+          v[d1 / 2][2 * half + (d1 & 1)] = hfma2_u32(c1, s2, z2);
+        }
+      }
+    }
+  }
+}
+
+template <int D, bool QBF16, int FAM>
+__global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
+    decode_kernel(const Params p) {
+  using L = Layout<D>;
+  constexpr int KC = D / 16;
+  constexpr int MB = D / 16;
+  constexpr int DL = D / 8;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* empty = full + L::kStages;
+  ChunkDesc* descs = reinterpret_cast<ChunkDesc*>(smem + L::kDescOff);
+  int* misc = reinterpret_cast<int*>(smem + L::kMiscOff);
+
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hkv = p.Hkv, G = p.G, P = p.P;
+  const int cpp = P / kChunk;
+  const bool sparse = p.sel_pages != nullptr;
+
+  int seq_len = p.seq_lens[b];
+  seq_len = max(0, min(seq_len, p.max_pages * P));
+  const int n_pages_b = (seq_len + P - 1) / P;
+  int n_chunks;
+  if (!sparse) {
+    n_chunks = (seq_len + kChunk - 1) / kChunk;
+  } else {
+    const int cnt = p.sel_count[b * Hkv + h];
+    const int n_sel = max(0, min(cnt, p.sel_width));
+    n_chunks = n_sel * cpp;
+    if (cnt > p.sel_width && split == 0 && threadIdx.x == 0 && p.status) atomicAdd(p.status, 1u);
+  }
+  const int c_begin = split * p.cps;
+  const int c_end = min(n_chunks, c_begin + p.cps);
+  const int n_active = (n_chunks + p.cps - 1) / p.cps;
+  const size_t row0 = (size_t)b * (Hkv * G) + (size_t)h * G;  // first query head row
+
+  if (c_begin >= c_end) {
+    if (n_active == 0 && split == 0) {  // empty visible set: o = 0, lse2 = -inf
+      for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+        const size_t o = (row0 + idx / D) * D + idx % D;
+        if (p.out) {
+          if (p.out_bf16) reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(0.f);
+          else reinterpret_cast<__half*>(p.out)[o] = __float2half_rn(0.f);
+        }
+        if (p.out_f32) p.out_f32[o] = 0.f;
+        if (p.lse2_out && idx % D == 0) p.lse2_out[row0 + idx / D] = -INFINITY;
+      }
+    }
+    return;
+  }
+  const int n_local = c_end - c_begin;
+  const int n_stages = (n_local + kChunksPerStage - 1) / kChunksPerStage;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    misc[0] = 0;  // timeout flag
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    for (int s = 0; s < n_stages; ++s) {
+      const int slot = s % L::kStages;
+      if (s >= L::kStages) {
+        if (!mbar_wait(&empty[slot], ((s / L::kStages) - 1) & 1)) {
+          if (lane == 0) {
+            misc[0] = 1;
+            if (p.status) atomicOr(p.status, kStatusTimeoutBit);
+          }
+          break;
+        }
+      }
+      uint32_t kv_bytes = 0, m_bytes = 0;
+      const uint8_t *srcK = nullptr, *srcV = nullptr, *srcMK = nullptr, *srcMV = nullptr;
+      if (lane < kChunksPerStage) {
+        ChunkDesc d;
+        d.codec = -1;
+        d.n_valid = 0;
+        d.kscale = 1.f;
+        d.vscale = 1.f;
+        const int ci = c_begin + s * kChunksPerStage + lane;
+        if (ci < c_end) {
+          const int v = ci / cpp, cip = ci - v * cpp;
+          int page = v;
+          bool good = true;
+          if (sparse) {
+            page = p.sel_pages[((size_t)b * Hkv + h) * p.sel_width + v];
+            if (page < 0 || page >= n_pages_b) {
+              good = false;
+              if (cip == 0 && p.status) atomicAdd(p.status, 1u);
+            }
+          }
+          if (good) {
+            const int tok0 = page * P + cip * kChunk;
+            const int nv = min(kChunk, seq_len - tok0);
+            if (nv > 0) {
+              const int codec = p.page_codec[(size_t)b * p.max_pages + page];
+              const long long slot_id = p.block_table[(size_t)b * p.max_pages + page];
+              bool ok = codec >= 0 && codec <= 4 && p.codes[codec] != nullptr;
+              if (ok) {
+                const int fam = codec_family(codec);
+                ok = (FAM == kFamMixed) || (FAM == fam);
+              }
+              if (ok) ok = slot_id >= 0 && slot_id < p.n_slots[codec];
+              if (!ok) {
+                if (cip == 0 && p.status) atomicAdd(p.status, 1u);
+              } else {
+                const int rowb = (codec <= ARGUS_BF16) ? 2 * D : (codec == ARGUS_INT4_G32 ? D / 2 : D);
+                const size_t rk = (((size_t)slot_id * 2 + 0) * Hkv + h) * P + (size_t)cip * kChunk;
+                const size_t rv = (((size_t)slot_id * 2 + 1) * Hkv + h) * P + (size_t)cip * kChunk;
+                srcK = p.codes[codec] + rk * rowb;
+                srcV = p.codes[codec] + rv * rowb;
+                kv_bytes = kChunk * rowb;
+                if (codec == ARGUS_INT4_G32) {
+                  srcMK = p.meta[codec] + rk * (L::kNI * 4);
+                  srcMV = p.meta[codec] + rv * (L::kNI * 4);
+                  m_bytes = kChunk * L::kNI * 4;
+                } else if (codec == ARGUS_FP8_E4M3 || codec == ARGUS_INT8) {
+                  const float* ms = reinterpret_cast<const float*>(p.meta[codec]);
+                  d.kscale = ms[((size_t)slot_id * 2 + 0) * Hkv + h];
+                  d.vscale = ms[((size_t)slot_id * 2 + 1) * Hkv + h];
+                }
+                d.codec = codec;
+                d.n_valid = nv;
+              }
+            }
+          }
+        }
+        descs[slot * kChunksPerStage + lane] = d;
+      }
+      uint32_t total = 2 * (kv_bytes + m_bytes);
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&full[slot], total);
+      __syncwarp();
+      if (kv_bytes) {
+        uint8_t* dst = smem + slot * L::kStageBytes + lane * L::kChunkBytes;
+        bulk_g2s(dst + L::kOffK, srcK, kv_bytes, &full[slot]);
+        bulk_g2s(dst + L::kOffV, srcV, kv_bytes, &full[slot]);
+        if (m_bytes) {
+          bulk_g2s(dst + L::kOffMK, srcMK, m_bytes, &full[slot]);
+          bulk_g2s(dst + L::kOffMV, srcMV, m_bytes, &full[slot]);
+        }
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int r = lane >> 2, t = lane & 3;
+  // query fragments (B operand of Q.K: k = head_dim, n = query head r)
+  uint32_t qf[KC][2], qb[KC][2];
+  float qscale_h0 = 1.f, qscale_h1 = 1.f;  // 2^-e of heads 2t, 2t+1 (bf16 q in fp16 MMAs)
+  {
+    float qv[D / 4];
+    const bool live = r < G;
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) {
+      uint4 x = make_uint4(0, 0, 0, 0);
+      if (live) {
+        const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) + (row0 + r) * D + 32 * i + 8 * t;
+        x = *reinterpret_cast<const uint4*>(qp);
+      }
+      const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint16_t bits = (wv[e / 2] >> (16 * (e & 1))) & 0xFFFFu;
+        qv[8 * i + e] = QBF16 ? __uint_as_float((uint32_t)bits << 16)
+                              : __half2float(__ushort_as_half(bits));
+      }
+      if (FAM != kFamF16) {
+        qb[2 * i][0] = prmt(x.x, x.z, 0x5410);
+        qb[2 * i][1] = prmt(x.x, x.z, 0x7632);
+        qb[2 * i + 1][0] = prmt(x.y, x.w, 0x5410);
+        qb[2 * i + 1][1] = prmt(x.y, x.w, 0x7632);
+      }
+    }
+    if (FAM != kFamBF16) {
+      float e_scale = 1.f;  // power of two bringing max|q| of this head into [2^14, 2^15)
+      if (QBF16) {
+        float mx = 0.f;
+#pragma unroll
+        for (int e = 0; e < D / 4; ++e) mx = fmaxf(mx, fabsf(qv[e]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        int ex = 0;
+        if (mx > 0.f) ex = 14 - ilogbf(mx);
+        ex = max(-100, min(100, ex));
+        e_scale = ldexpf(1.f, ex);
+        const float inv = ldexpf(1.f, -ex);
+        qscale_h0 = __shfl_sync(0xffffffffu, inv, 4 * (2 * t));
+        qscale_h1 = __shfl_sync(0xffffffffu, inv, 4 * (2 * t + 1));
+      }
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) {
+        const float* e8 = qv + 8 * i;
+        qf[2 * i][0] = pack_f16x2(e8[0] * e_scale, e8[4] * e_scale);
+        qf[2 * i][1] = pack_f16x2(e8[1] * e_scale, e8[5] * e_scale);
+        qf[2 * i + 1][0] = pack_f16x2(e8[2] * e_scale, e8[6] * e_scale);
+        qf[2 * i + 1][1] = pack_f16x2(e8[3] * e_scale, e8[7] * e_scale);
+      }
+    }
+  }
+
+  float acc[MB][4];
+#pragma unroll
+  for (int j = 0; j < MB; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, sigma = 1.f;
+  bool alive = true;
+
+  for (int s = 0; s < n_stages; ++s) {
+    const int slot = s % L::kStages;
+    if (alive && !mbar_wait(&full[slot], (s / L::kStages) & 1)) {
+      alive = false;
+      if (lane == 0 && p.status) atomicOr(p.status, kStatusTimeoutBit);
+    }
+    if (alive && misc[0]) alive = false;
+    const ChunkDesc d = descs[slot * kChunksPerStage + warp];
+    if (alive && d.codec >= 0) {
+      const uint8_t* chunk = smem + slot * L::kStageBytes + warp * L::kChunkBytes;
+      const bool bf = (d.codec == ARGUS_BF16);
+      // ---- scores S^T[token][head] = K . q
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        uint32_t a[KC][4];
+        load_k_frags<D>(d.codec, chunk, r, t, a);
+        if (FAM == kFamBF16 || (FAM == kFamMixed && bf)) {
+#pragma unroll
+          for (int c = 0; c < KC; ++c) mma_bf16(sc, a[c][0], a[c][1], a[c][2], a[c][3], qb[c][0], qb[c][1]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < KC; ++c) mma_f16(sc, a[c][0], a[c][1], a[c][2], a[c][3], qf[c][0], qf[c][1]);
+        }
+      }
+      const bool f16path = !(FAM == kFamBF16 || (FAM == kFamMixed && bf));
+      const float fk = p.scale_log2 * d.kscale;
+      const float f0 = fk * (f16path ? qscale_h0 : 1.f);
+      const float f1 = fk * (f16path ? qscale_h1 : 1.f);
+      float s0 = sc[0] * f0, s1 = sc[1] * f1, s2 = sc[2] * f0, s3 = sc[3] * f1;
+      if (r >= d.n_valid) s0 = s1 = -INFINITY;
+      if (r + 8 >= d.n_valid) s2 = s3 = -INFINITY;
+      float t0 = fmaxf(s0, s2), t1 = fmaxf(s1, s3);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, o));
+        t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, o));
+      }
+      const float mn0 = fmaxf(m0, t0), mn1 = fmaxf(m1, t1);
+      // mn is finite: token 0 of a non-empty chunk is always visible
+      const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+      const float p0 = fast_exp2(s0 - mn0), p1 = fast_exp2(s1 - mn1);
+      const float p2 = fast_exp2(s2 - mn0), p3 = fast_exp2(s3 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      l0 = l0 * al0 + (p0 + p2);
+      l1 = l1 * al1 + (p1 + p3);
+      // V scale: the accumulator is kept in units of the current page's V scale
+      float vs = d.vscale;
+      if (!(vs > 0.f)) vs = sigma;  // all-zero unit: codes are 0, keep units
+      const float ratio = (vs == sigma) ? 1.f : sigma / vs;
+      sigma = vs;
+      const float g0 = al0 * ratio, g1 = al1 * ratio;
+#pragma unroll
+      for (int j = 0; j < MB; ++j) {
+        acc[j][0] *= g0;
+        acc[j][1] *= g1;
+        acc[j][2] *= g0;
+        acc[j][3] *= g1;
+      }
+      // ---- O^T[dim][head] += V^T . P^T
+      uint32_t vf[MB][4];
+      load_v_frags<D>(d.codec, chunk, r, t, vf);
+      if (f16path) {
+        const uint32_t b0 = movmatrix_trans(pack_f16x2(p0, p1));
+        const uint32_t b1 = movmatrix_trans(pack_f16x2(p2, p3));
+#pragma unroll
+        for (int j = 0; j < MB; ++j) mma_f16(acc[j], vf[j][0], vf[j][1], vf[j][2], vf[j][3], b0, b1);
+      } else {
+        const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+        const uint32_t l01 = pack_bf16x2(p0 - __uint_as_float(h01 << 16), p1 - __uint_as_float(h01 & 0xFFFF0000u));
+        const uint32_t l23 = pack_bf16x2(p2 - __uint_as_float(h23 << 16), p3 - __uint_as_float(h23 & 0xFFFF0000u));
+        const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+        const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+#pragma unroll
+        for (int j = 0; j < MB; ++j) {
+          mma_bf16(acc[j], vf[j][0], vf[j][1], vf[j][2], vf[j][3], bh0, bh1);
+          mma_bf16(acc[j], vf[j][0], vf[j][1], vf[j][2], vf[j][3], bl0, bl1);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+  }
+
+  // ------------------------------------------------- merge the four warps
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+  }
+  consumer_bar();  // every warp is done with the stage ring; reuse it
+  float* red_o = reinterpret_cast<float*>(smem);               // [4][8][D]
+  float* red_ml = red_o + kConsumerWarps * kMaxG * D;          // [4][8][2]
+  float* wts = red_ml + kConsumerWarps * kMaxG * 2;            // fold weights
+#pragma unroll
+  for (int j = 0; j < MB; ++j) {
+    const int d0 = DL * r + 2 * j, d1 = d0 + 1;
+    red_o[(warp * kMaxG + 2 * t) * D + d0] = acc[j][0] * sigma;
+    red_o[(warp * kMaxG + 2 * t + 1) * D + d0] = acc[j][1] * sigma;
+    red_o[(warp * kMaxG + 2 * t) * D + d1] = acc[j][2] * sigma;
+    red_o[(warp * kMaxG + 2 * t + 1) * D + d1] = acc[j][3] * sigma;
+  }
+  if (r == 0) {
+    red_ml[(warp * kMaxG + 2 * t) * 2 + 0] = m0;
+    red_ml[(warp * kMaxG + 2 * t) * 2 + 1] = l0;
+    red_ml[(warp * kMaxG + 2 * t + 1) * 2 + 0] = m1;
+    red_ml[(warp * kMaxG + 2 * t + 1) * 2 + 1] = l1;
+  }
+  consumer_bar();
+  const int tid = threadIdx.x;  // 0 .. 127
+  const int nthr = kConsumerWarps * 32;
+  const bool direct = (n_active == 1);
+  float* part_bh = p.part + ((size_t)b * Hkv + h) * p.num_splits * G * (D + 1);
+  for (int idx = tid; idx < G * D; idx += nthr) {
+    const int g = idx / D, dd = idx - g * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_ml[(w * kMaxG + g) * 2]);
+    float o = 0.f, lse2 = -INFINITY;
+    if (M != -INFINITY) {
+      float Lsum = 0.f, osum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float f = fast_exp2(red_ml[(w * kMaxG + g) * 2] - M);
+        Lsum += red_ml[(w * kMaxG + g) * 2 + 1] * f;
+        osum += red_o[(w * kMaxG + g) * D + dd] * f;
+      }
+      o = osum / Lsum;
+      lse2 = M + log2f(Lsum);
+    }
+    if (direct) {
+      const size_t oi = (row0 + g) * D + dd;
+      if (p.out) {
+        if (p.out_bf16) reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
+        else reinterpret_cast<__half*>(p.out)[oi] = __float2half_rn(o);
+      }
+      if (p.out_f32) p.out_f32[oi] = o;
+      if (p.lse2_out && dd == 0) p.lse2_out[row0 + g] = lse2;
+    } else {
+      float* dst = part_bh + ((size_t)split * G + g) * (D + 1);
+      dst[dd] = o;
+      if (dd == 0) dst[D] = lse2;
+    }
+  }
+  if (direct) return;
+
+  // ------------------------------------------- last CTA folds the splits
+  __threadfence();
+  consumer_bar();
+  if (tid == 0) misc[1] = (int)atomicAdd(p.counters + (size_t)b * Hkv + h, 1u);
+  consumer_bar();
+  if (misc[1] != n_active - 1) return;
+  __threadfence();
+  // weights 2^(lse_s - L) per (split, head)
+  for (int g = tid; g < G; g += nthr) {
+    float M = -INFINITY;
+    for (int s = 0; s < n_active; ++s) M = fmaxf(M, __ldcg(part_bh + ((size_t)s * G + g) * (D + 1) + D));
+    float Lsum = 0.f;
+    if (M != -INFINITY) {
+      for (int s = 0; s < n_active; ++s)
+        Lsum += fast_exp2(__ldcg(part_bh + ((size_t)s * G + g) * (D + 1) + D) - M);
+    }
+    const float lse = (M == -INFINITY) ? -INFINITY : M + log2f(Lsum);
+    for (int s = 0; s < n_active; ++s) {
+      const float ls = __ldcg(part_bh + ((size_t)s * G + g) * (D + 1) + D);
+      wts[s * kMaxG + g] = (lse == -INFINITY) ? 0.f : fast_exp2(ls - lse);
+    }
+    wts[n_active * kMaxG + g] = lse;
+  }
+  consumer_bar();
+  for (int idx = tid; idx < G * D; idx += nthr) {
+    const int g = idx / D, dd = idx - g * D;
+    float o = 0.f;
+    for (int s = 0; s < n_active; ++s) {
+      const float w = wts[s * kMaxG + g];
+      if (w != 0.f) o += w * __ldcg(part_bh + ((size_t)s * G + g) * (D + 1) + dd);
+    }
+    const size_t oi = (row0 + g) * D + dd;
+    if (p.out) {
+      if (p.out_bf16) reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
+      else reinterpret_cast<__half*>(p.out)[oi] = __float2half_rn(o);
+    }
+    if (p.out_f32) p.out_f32[oi] = o;
+    if (p.lse2_out && dd == 0) p.lse2_out[row0 + g] = wts[n_active * kMaxG + g];
+  }
+  if (tid == 0) p.counters[(size_t)b * Hkv + h] = 0u;
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+struct Plan {
+  int D, G, cps, num_splits, fam;
+  bool q_bf16;
+  size_t counter_bytes, ws_bytes;
+};
+
+static argus_status plan(const argus_decode_args* a, Plan* pl) {
+  if (!a) return fail(ARGUS_E_INVALID, "decode: args is NULL");
+  const argus_geom& g = a->g;
+  if (g.n_q_heads <= 0 || g.n_kv_heads <= 0 || g.head_dim <= 0 || g.page_tokens <= 0)
+    return fail(ARGUS_E_INVALID, "decode: geometry fields must be positive");
+  if (g.n_q_heads % g.n_kv_heads != 0)
+    return fail(ARGUS_E_INVALID, "decode: n_q_heads %% n_kv_heads != 0");
+  const int G = g.n_q_heads / g.n_kv_heads;
+  if (G > kMaxG) return fail(ARGUS_E_UNSUPPORTED, "decode: G = %d > 8 query heads per KV head", G);
+  if (g.head_dim != 64 && g.head_dim != 128)
+    return fail(ARGUS_E_UNSUPPORTED, "decode: head_dim %d (supported: 64, 128)", g.head_dim);
+  if (g.page_tokens % kChunk != 0)
+    return fail(ARGUS_E_UNSUPPORTED, "decode: page_tokens %d is not a multiple of 16", g.page_tokens);
+  if (a->batch < 0) return fail(ARGUS_E_INVALID, "decode: negative batch");
+  if (a->batch > 65535 || g.n_kv_heads > 65535) return fail(ARGUS_E_UNSUPPORTED, "decode: batch or n_kv_heads too large");
+  if (a->q_dtype != ARGUS_FP16 && a->q_dtype != ARGUS_BF16)
+    return fail(ARGUS_E_INVALID, "decode: q_dtype must be FP16 or BF16");
+  if (a->max_pages <= 0) return fail(ARGUS_E_INVALID, "decode: max_pages must be positive");
+  if ((long long)a->max_pages * g.page_tokens > (1LL << 30))
+    return fail(ARGUS_E_UNSUPPORTED, "decode: max_pages * page_tokens too large");
+  if ((a->sel_pages == nullptr) != (a->sel_count == nullptr))
+    return fail(ARGUS_E_INVALID, "decode: sel_pages and sel_count must both be set or both NULL");
+  if (a->sel_pages && a->sel_width <= 0) return fail(ARGUS_E_INVALID, "decode: sel_width must be positive");
+  if (a->n_pools < 0 || a->n_pools > 5 || (a->n_pools > 0 && !a->pools))
+    return fail(ARGUS_E_INVALID, "decode: bad pool list");
+  if (!std::isfinite(a->softmax_scale)) return fail(ARGUS_E_INVALID, "decode: softmax_scale not finite");
+  if (a->out && a->out_dtype != ARGUS_FP16 && a->out_dtype != ARGUS_BF16)
+    return fail(ARGUS_E_INVALID, "decode: out_dtype must be FP16 or BF16");
+  bool seen[5] = {false, false, false, false, false};
+  bool has_bf16 = false, has_f16 = false;
+  for (int i = 0; i < a->n_pools; ++i) {
+    const argus_pool& pool = a->pools[i];
+    if (pool.codec < 0 || pool.codec > 4) return fail(ARGUS_E_INVALID, "decode: pool %d has codec %d", i, pool.codec);
+    if (seen[pool.codec]) return fail(ARGUS_E_INVALID, "decode: two pools with codec %d", pool.codec);
+    seen[pool.codec] = true;
+    if (pool.n_slots < 0) return fail(ARGUS_E_INVALID, "decode: pool %d n_slots < 0", i);
+    if (pool.n_slots > 0) {
+      if (!pool.codes || (reinterpret_cast<uintptr_t>(pool.codes) & 15))
+        return fail(ARGUS_E_INVALID, "decode: pool %d codes NULL or not 16-byte aligned", i);
+      if (pool.codec >= ARGUS_FP8_E4M3 &&
+          (!pool.meta || (reinterpret_cast<uintptr_t>(pool.meta) & 15)))
+        return fail(ARGUS_E_INVALID, "decode: pool %d meta NULL or not 16-byte aligned", i);
+    }
+    if (pool.codec == ARGUS_BF16) has_bf16 = true;
+    else has_f16 = true;
+  }
+  pl->q_bf16 = (a->q_dtype == ARGUS_BF16);
+  if (has_bf16 && !pl->q_bf16)
+    return fail(ARGUS_E_UNSUPPORTED, "decode: BF16 pages need a BF16 query");
+  pl->fam = (has_bf16 && has_f16) ? kFamMixed : (has_bf16 ? kFamBF16 : kFamF16);
+  pl->D = g.head_dim;
+  pl->G = G;
+  const int cpp = g.page_tokens / kChunk;
+  const long long max_chunks = a->sel_pages ? (long long)a->sel_width * cpp : (long long)a->max_pages * cpp;
+  long long cps;
+  if (a->num_splits > 0) {
+    cps = (max_chunks + a->num_splits - 1) / a->num_splits;
+  } else {
+    const long long total = (long long)std::max(a->batch, 1) * g.n_kv_heads * max_chunks;
+    const long long target = 8LL * device_sm_count();
+    cps = std::max<long long>(16, (total + target - 1) / target);
+  }
+  cps = std::max<long long>(cps, (max_chunks + kMaxSplits - 1) / kMaxSplits);
+  cps = std::max<long long>(kChunksPerStage, (cps + kChunksPerStage - 1) / kChunksPerStage * kChunksPerStage);
+  pl->cps = (int)cps;
+  pl->num_splits = (int)std::max<long long>(1, (max_chunks + cps - 1) / cps);
+  if (pl->num_splits > 65535) return fail(ARGUS_E_UNSUPPORTED, "decode: too many splits");
+  pl->counter_bytes = ((size_t)std::max(a->batch, 1) * g.n_kv_heads * 4 + 255) / 256 * 256;
+  pl->ws_bytes = pl->counter_bytes +
+                 (size_t)std::max(a->batch, 1) * g.n_kv_heads * pl->num_splits * G * (g.head_dim + 1) * 4;
+  return ARGUS_OK;
+}
+
+template <int D, bool QBF16, int FAM>
+static argus_status launch_t(const Params& p, dim3 grid, cudaStream_t s) {
+  using L = Layout<D>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, QBF16, FAM>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+    if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "decode: smem attribute: %s", cudaGetErrorString(e));
+    configured = true;
+  }
+  decode_kernel<D, QBF16, FAM><<<grid, kThreads, L::kSmemBytes, s>>>(p);
+  return launch_status("argus_paged_decode_attn");
+}
+
+template <int D>
+static argus_status launch_d(const Params& p, const Plan& pl, dim3 grid, cudaStream_t s) {
+  if (!pl.q_bf16) return launch_t<D, false, kFamF16>(p, grid, s);
+  if (pl.fam == kFamF16) return launch_t<D, true, kFamF16>(p, grid, s);
+  if (pl.fam == kFamBF16) return launch_t<D, true, kFamBF16>(p, grid, s);
+  return launch_t<D, true, kFamMixed>(p, grid, s);
+}
+
+}  // namespace decode
+}  // namespace argus
+
+using namespace argus;
+using namespace argus::decode;
+
+extern "C" argus_status argus_decode_workspace_bytes(const argus_decode_args* args, size_t* bytes) {
+  if (!bytes) return fail(ARGUS_E_INVALID, "decode: bytes is NULL");
+  Plan pl;
+  argus_status st = plan(args, &pl);
+  if (st != ARGUS_OK) return st;
+  *bytes = pl.ws_bytes;
+  return ARGUS_OK;
+}
+
+extern "C" argus_status argus_paged_decode_attn(const argus_decode_args* a, void* ws,
+                                                size_t ws_bytes, void* stream) {
+  Plan pl;
+  argus_status st = plan(a, &pl);
+  if (st != ARGUS_OK) return st;
+  if (a->batch == 0) return ARGUS_OK;
+  if (!a->q || !a->page_codec || !a->block_table || !a->seq_lens)
+    return fail(ARGUS_E_INVALID, "decode: q, page_codec, block_table and seq_lens are required");
+  if (reinterpret_cast<uintptr_t>(a->q) & 15) return fail(ARGUS_E_INVALID, "decode: q not 16-byte aligned");
+  if (!a->out && !a->out_f32 && !a->lse2_out) return fail(ARGUS_E_INVALID, "decode: no output given");
+  if (ws_bytes < pl.ws_bytes || (pl.num_splits > 1 && !ws))
+    return fail(ARGUS_E_WORKSPACE, "decode: workspace %zu bytes < %zu needed", ws_bytes, pl.ws_bytes);
+  Params p{};
+  p.B = a->batch;
+  p.Hkv = a->g.n_kv_heads;
+  p.G = pl.G;
+  p.P = a->g.page_tokens;
+  p.max_pages = a->max_pages;
+  p.q = a->q;
+  for (int c = 0; c < 5; ++c) {
+    p.codes[c] = nullptr;
+    p.meta[c] = nullptr;
+    p.n_slots[c] = 0;
+  }
+  for (int i = 0; i < a->n_pools; ++i) {
+    const argus_pool& pool = a->pools[i];
+    p.codes[pool.codec] = static_cast<const uint8_t*>(pool.codes);
+    p.meta[pool.codec] = static_cast<const uint8_t*>(pool.meta);
+    p.n_slots[pool.codec] = pool.n_slots;
+  }
+  p.page_codec = a->page_codec;
+  p.block_table = a->block_table;
+  p.seq_lens = a->seq_lens;
+  p.sel_pages = a->sel_pages;
+  p.sel_count = a->sel_count;
+  p.sel_width = a->sel_width;
+  p.scale_log2 = a->softmax_scale * 1.4426950408889634f;
+  p.out = a->out;
+  p.out_bf16 = (a->out_dtype == ARGUS_BF16);
+  p.out_f32 = a->out_f32;
+  p.lse2_out = a->lse2_out;
+  p.status = a->status;
+  p.cps = pl.cps;
+  p.num_splits = pl.num_splits;
+  p.counters = static_cast<uint32_t*>(ws);
+  p.part = ws ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.counter_bytes) : nullptr;
+  dim3 grid(pl.num_splits, a->g.n_kv_heads, a->batch);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (pl.D == 64) return launch_d<64>(p, pl, grid, s);
+  return launch_d<128>(p, pl, grid, s);
+}

@@ -1,0 +1,371 @@
+// argus_quantize_pages: demote 16-bit KV pages into a codec tier, bit-exactly.
+//
+// "ARGUS: Heterogeneous KV-cache memory management" (summary): older pages are
+// demoted from FP16 through FP8, INT8 and INT4.  "feat(kvcache): host-RAM KV
+// tier for sparse-attention models", update 20f3b23: the pool stores e4m3 codes
+// plus fp32 scales and is the source of truth.  Per (page, K|V, KV head) unit:
+//   FP8   scale = amax / 448, code = e4m3_rne_satfinite(x / scale)
+//   INT8  scale = amax / 127, code = clamp(rint(x / scale), -127, 127)
+//   INT4  per token and 32-element group: z = fp16_sat(min),
+//         s = fp16_sat((max - z) / 15), code = clamp(rint((x - z) / s), 0, 15)
+// every operation IEEE fp32 with round-to-nearest-even (the divisions use the
+// compiler's IEEE division; no reciprocal shortcuts).  The optional compressed
+// key is the bf16 mean over valid tokens of the stored (dequantised) keys.
+//
+// GB300 design: the pass is a pure HBM stream.  Units of at most 2048 elements
+// are owned by one warp and held in registers (one read, one write); larger
+// units are owned by a 256-thread CTA that reads the unit twice (max pass,
+// then encode), the second read served from L2.  Loads and stores are 16-byte
+// per lane and contiguous across the group.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace argus {
+namespace quant {
+
+struct QParams {
+  int Hkv, P, n_pages;
+  const uint16_t* src;
+  long long n_src;
+  const int32_t* src_slots;
+  const int32_t* dst_slots;
+  const int32_t* valid_tokens;
+  uint8_t* dst_codes;
+  uint8_t* dst_meta;
+  long long n_dst;
+  uint16_t* ckey;
+  uint32_t* status;
+};
+
+constexpr int kCtaThreads = 256;
+constexpr int kRegVecs = 8;  // 16-byte vectors per lane kept in registers (small units)
+
+template <bool SBF16>
+__device__ __forceinline__ void unpack8(const uint4& x, float (&f)[8]) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const uint32_t bits = (w[e / 2] >> (16 * (e & 1))) & 0xFFFFu;
+    f[e] = SBF16 ? __uint_as_float(bits << 16) : __half2float(__ushort_as_half((unsigned short)bits));
+  }
+}
+
+__device__ __forceinline__ float fp16_sat(float x) {
+  return __half2float(__float2half_rn(fminf(fmaxf(x, -65504.f), 65504.f)));
+}
+
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  const uint32_t h = e4m3x2_to_f16x2(code & 0xFFu);
+  return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+}
+
+// Reduce over the `group` threads that own one unit (32 = warp, 256 = CTA).
+template <int GROUP, bool MAX>
+__device__ __forceinline__ float group_reduce(float v, float* sh) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = MAX ? fmaxf(v, w) : v + w;
+  }
+  if (GROUP == 32) return v;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  v = sh[0];
+#pragma unroll
+  for (int w = 1; w < GROUP / 32; ++w) v = MAX ? fmaxf(v, sh[w]) : v + sh[w];
+  return v;
+}
+
+// Encode 8 values of one 16-byte source vector and store them.
+template <int CODEC, bool SBF16>
+__device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& raw, float scale,
+                                             uint8_t* dcodes, size_t vec, bool valid, float (&deq)[8],
+                                             uint8_t* dmeta_row, int lane_in_group) {
+  if (CODEC == ARGUS_FP16 || CODEC == ARGUS_BF16) {
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(dcodes)[vec] = valid ? raw : z;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) deq[e] = valid ? f[e] : 0.f;
+  } else if (CODEC == ARGUS_FP8_E4M3) {
+    uint32_t w[2] = {0u, 0u};
+    if (valid && scale > 0.f) {
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const uint32_t two = f32x2_to_e4m3x2(f[e] / scale, f[e + 1] / scale);
+        w[e / 4] |= two << (16 * ((e / 2) & 1));
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) deq[e] = e4m3_value(w[e / 4] >> (8 * (e & 3))) * scale;
+    reinterpret_cast<uint2*>(dcodes)[vec] = make_uint2(w[0], w[1]);
+  } else if (CODEC == ARGUS_INT8) {
+    uint32_t w[2] = {0u, 0u};
+    if (valid && scale > 0.f) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        int q = __float2int_rn(f[e] / scale);
+        q = max(-127, min(127, q));
+        w[e / 4] |= (uint32_t)(q & 0xFF) << (8 * (e & 3));
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) deq[e] = (float)(int8_t)((w[e / 4] >> (8 * (e & 3))) & 0xFF) * scale;
+    reinterpret_cast<uint2*>(dcodes)[vec] = make_uint2(w[0], w[1]);
+  } else {  // INT4: the 4 threads of a 32-element group cooperate
+    float lo = f[0], hi = f[0];
+#pragma unroll
+    for (int e = 1; e < 8; ++e) {
+      lo = fminf(lo, f[e]);
+      hi = fmaxf(hi, f[e]);
+    }
+    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 1));
+    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, 1));
+    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 2));
+    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, 2));
+    const float z = fp16_sat(lo);
+    const float s = fp16_sat((hi - z) / 15.f);
+    uint32_t w = 0u;
+    if (valid && s > 0.f) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        int q = __float2int_rn((f[e] - z) / s);
+        q = max(0, min(15, q));
+        w |= (uint32_t)q << (4 * e);
+      }
+    }
+    const float zz = valid ? z : 0.f, ss = valid ? s : 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) deq[e] = fmaf((float)((w >> (4 * e)) & 0xF), ss, zz);
+    reinterpret_cast<uint32_t*>(dcodes)[vec] = w;
+    if ((lane_in_group & 3) == 0) {
+      const __half2 sz = __halves2half2(__float2half_rn(ss), __float2half_rn(zz));
+      *reinterpret_cast<__half2*>(dmeta_row) = sz;
+    }
+  }
+}
+
+template <int D, bool SBF16, int CODEC, int GROUP>
+__global__ void __launch_bounds__(kCtaThreads) quantize_kernel(const QParams p) {
+  constexpr int VPR = D / 8;  // 16-byte vectors per token row
+  __shared__ float sh_red[kCtaThreads / 32];
+  __shared__ float sh_ck[kCtaThreads / 32][8 * VPR];
+  const int lane = threadIdx.x & 31;
+  const int g = (GROUP == 32) ? lane : threadIdx.x;
+  const long long gid = (GROUP == 32) ? (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5)
+                                      : (long long)blockIdx.x;
+  const long long ngroups = (GROUP == 32) ? (long long)gridDim.x * (blockDim.x / 32) : gridDim.x;
+  const int Hkv = p.Hkv, P = p.P;
+  const long long n_units = (long long)p.n_pages * 2 * Hkv;
+  const int nvec = P * VPR;  // vectors per unit
+
+  for (long long u = gid; u < n_units; u += ngroups) {
+    const int i = (int)(u / (2 * Hkv));
+    const int rem = (int)(u - (long long)i * 2 * Hkv);
+    const int kv = rem / Hkv, h = rem - kv * Hkv;
+    const long long ss = p.src_slots[i], ds = p.dst_slots[i];
+    if (ss < 0 || ss >= p.n_src || ds < 0 || ds >= p.n_dst) {
+      if (g == 0 && kv == 0 && h == 0 && p.status) atomicAdd(p.status, 1u);
+      continue;
+    }
+    int valid = p.valid_tokens ? p.valid_tokens[i] : P;
+    valid = max(0, min(P, valid));
+    const int nvalid_vec = valid * VPR;
+    const uint4* src = reinterpret_cast<const uint4*>(p.src + ((ss * 2 + kv) * Hkv + h) * (size_t)P * D);
+    const size_t unit_dst = ((size_t)ds * 2 + kv) * Hkv + h;
+    uint8_t* dcodes;
+    if (CODEC == ARGUS_FP16 || CODEC == ARGUS_BF16) dcodes = p.dst_codes + unit_dst * (size_t)P * D * 2;
+    else if (CODEC == ARGUS_INT4_G32) dcodes = p.dst_codes + unit_dst * (size_t)P * (D / 2);
+    else dcodes = p.dst_codes + unit_dst * (size_t)P * D;
+
+    const bool regs = (GROUP == 32) && (nvec <= 32 * kRegVecs);
+    uint4 held[kRegVecs];
+    float scale = 0.f;
+    if (CODEC == ARGUS_FP8_E4M3 || CODEC == ARGUS_INT8) {
+      float amax = 0.f;
+      if (regs) {
+#pragma unroll
+        for (int k = 0; k < kRegVecs; ++k) {
+          const int v = g + 32 * k;
+          if (v < nvec) {
+            held[k] = src[v];
+            if (v < nvalid_vec) {
+              float f[8];
+              unpack8<SBF16>(held[k], f);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+            }
+          }
+        }
+      } else {
+        for (int v = g; v < nvalid_vec; v += GROUP) {
+          float f[8];
+          unpack8<SBF16>(src[v], f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+        }
+      }
+      amax = group_reduce<GROUP, true>(amax, sh_red);
+      scale = amax > 0.f ? amax / (CODEC == ARGUS_FP8_E4M3 ? 448.f : 127.f) : 0.f;
+      if (g == 0) reinterpret_cast<float*>(p.dst_meta)[unit_dst] = scale;
+    }
+
+    float ck[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    auto do_vec = [&](int v, const uint4& raw) {
+      float f[8];
+      unpack8<SBF16>(raw, f);
+      const bool valid_v = v < nvalid_vec;
+      float deq[8];
+      uint8_t* meta_row = nullptr;
+      if (CODEC == ARGUS_INT4_G32) {
+        const int row = v / VPR, grp = (v % VPR) / 4;
+        meta_row = p.dst_meta + ((unit_dst * P + row) * (D / 32) + grp) * 4;
+      }
+      encode_store<CODEC, SBF16>(f, raw, scale, dcodes, (size_t)v, valid_v, deq, meta_row, g);
+      if (valid_v) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ck[e] += deq[e];
+      }
+    };
+    if (regs) {
+      if (!(CODEC == ARGUS_FP8_E4M3 || CODEC == ARGUS_INT8)) {
+#pragma unroll
+        for (int k = 0; k < kRegVecs; ++k) {
+          const int v = g + 32 * k;
+          if (v < nvec) held[k] = src[v];
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kRegVecs; ++k) {
+        const int v = g + 32 * k;
+        if (v < nvec) do_vec(v, held[k]);
+      }
+    } else {
+      for (int v = g; v < nvec; v += GROUP) do_vec(v, src[v]);
+    }
+
+    if (p.ckey && kv == 0) {
+      // threads with equal g % VPR hold the same 8 dims
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float x = ck[e];
+#pragma unroll
+        for (int o = VPR; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        ck[e] = x;
+      }
+      if (GROUP != 32) {
+        const int warp = threadIdx.x >> 5;
+        __syncthreads();
+        if (lane < VPR) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) sh_ck[warp][lane * 8 + e] = ck[e];
+        }
+        __syncthreads();
+        if (threadIdx.x < VPR) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float x = 0.f;
+            for (int w = 0; w < GROUP / 32; ++w) x += sh_ck[w][threadIdx.x * 8 + e];
+            ck[e] = x;
+          }
+        }
+      }
+      if (g < VPR) {
+        const float n_f = (float)max(valid, 1);
+        uint32_t outw[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const float a0 = valid ? ck[e] / n_f : 0.f;
+          const float a1 = valid ? ck[e + 1] / n_f : 0.f;
+          outw[e / 2] = pack_bf16x2(a0, a1);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(p.ckey + ((size_t)i * Hkv + h) * D);
+        dst[g] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+      }
+    }
+    if (GROUP != 32) __syncthreads();
+  }
+}
+
+template <int D, bool SBF16, int CODEC>
+static argus_status launch3(const QParams& p, cudaStream_t s) {
+  const long long units = (long long)p.n_pages * 2 * p.Hkv;
+  const int sms = device_sm_count();
+  const bool small = (long long)p.P * D <= 32 * kRegVecs * 8;
+  if (small) {
+    const long long blocks_needed = (units + (kCtaThreads / 32) - 1) / (kCtaThreads / 32);
+    const int blocks = (int)std::max<long long>(1, std::min<long long>(blocks_needed, (long long)sms * 8));
+    quantize_kernel<D, SBF16, CODEC, 32><<<blocks, kCtaThreads, 0, s>>>(p);
+  } else {
+    const int blocks = (int)std::max<long long>(1, std::min<long long>(units, (long long)sms * 8));
+    quantize_kernel<D, SBF16, CODEC, kCtaThreads><<<blocks, kCtaThreads, 0, s>>>(p);
+  }
+  return launch_status("argus_quantize_pages");
+}
+
+template <int D, bool SBF16>
+static argus_status launch2(int codec, const QParams& p, cudaStream_t s) {
+  switch (codec) {
+    case ARGUS_FP16: return launch3<D, SBF16, ARGUS_FP16>(p, s);
+    case ARGUS_BF16: return launch3<D, SBF16, ARGUS_BF16>(p, s);
+    case ARGUS_FP8_E4M3: return launch3<D, SBF16, ARGUS_FP8_E4M3>(p, s);
+    case ARGUS_INT8: return launch3<D, SBF16, ARGUS_INT8>(p, s);
+    default: return launch3<D, SBF16, ARGUS_INT4_G32>(p, s);
+  }
+}
+
+}  // namespace quant
+}  // namespace argus
+
+using namespace argus;
+using namespace argus::quant;
+
+extern "C" argus_status argus_quantize_pages(const argus_geom* g, int32_t src_dtype,
+                                             const void* src_codes, int64_t n_src_slots,
+                                             const int32_t* src_slots, const argus_pool* dst,
+                                             const int32_t* dst_slots, int32_t n_pages,
+                                             const int32_t* valid_tokens, void* ckey_out,
+                                             uint32_t* status, void* stream) {
+  if (!g || !dst) return fail(ARGUS_E_INVALID, "quantize: geometry or destination is NULL");
+  if (g->n_kv_heads <= 0 || g->head_dim <= 0 || g->page_tokens <= 0)
+    return fail(ARGUS_E_INVALID, "quantize: geometry fields must be positive");
+  if (g->head_dim != 64 && g->head_dim != 128)
+    return fail(ARGUS_E_UNSUPPORTED, "quantize: head_dim %d (supported: 64, 128)", g->head_dim);
+  if (src_dtype != ARGUS_FP16 && src_dtype != ARGUS_BF16)
+    return fail(ARGUS_E_INVALID, "quantize: src_dtype must be FP16 or BF16");
+  if (dst->codec < 0 || dst->codec > 4) return fail(ARGUS_E_INVALID, "quantize: bad destination codec");
+  if ((dst->codec == ARGUS_FP16 || dst->codec == ARGUS_BF16) && dst->codec != src_dtype)
+    return fail(ARGUS_E_UNSUPPORTED, "quantize: a 16-bit destination must match the source dtype");
+  if (n_pages < 0) return fail(ARGUS_E_INVALID, "quantize: negative n_pages");
+  if (n_pages == 0) return ARGUS_OK;
+  if (!src_codes || !src_slots || !dst_slots || !dst->codes)
+    return fail(ARGUS_E_INVALID, "quantize: NULL source, slot list or destination codes");
+  if (dst->codec >= ARGUS_FP8_E4M3 && !dst->meta) return fail(ARGUS_E_INVALID, "quantize: NULL destination meta");
+  if ((reinterpret_cast<uintptr_t>(src_codes) | reinterpret_cast<uintptr_t>(dst->codes) |
+       reinterpret_cast<uintptr_t>(ckey_out)) & 15)
+    return fail(ARGUS_E_INVALID, "quantize: pointers must be 16-byte aligned");
+  if (dst->meta && (reinterpret_cast<uintptr_t>(dst->meta) & 3))
+    return fail(ARGUS_E_INVALID, "quantize: meta must be 4-byte aligned");
+  if ((long long)n_pages * 2 * g->n_kv_heads > (1LL << 31))
+    return fail(ARGUS_E_UNSUPPORTED, "quantize: too many units");
+  QParams p{};
+  p.Hkv = g->n_kv_heads;
+  p.P = g->page_tokens;
+  p.n_pages = n_pages;
+  p.src = static_cast<const uint16_t*>(src_codes);
+  p.n_src = n_src_slots;
+  p.src_slots = src_slots;
+  p.dst_slots = dst_slots;
+  p.valid_tokens = valid_tokens;
+  p.dst_codes = static_cast<uint8_t*>(dst->codes);
+  p.dst_meta = static_cast<uint8_t*>(dst->meta);
+  p.n_dst = dst->n_slots;
+  p.ckey = static_cast<uint16_t*>(ckey_out);
+  p.status = status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool bf = (src_dtype == ARGUS_BF16);
+  if (g->head_dim == 64) return bf ? launch2<64, true>(dst->codec, p, s) : launch2<64, false>(dst->codec, p, s);
+  return bf ? launch2<128, true>(dst->codec, p, s) : launch2<128, false>(dst->codec, p, s);
+}

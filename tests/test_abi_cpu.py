@@ -1,0 +1,68 @@
+"""The C-ABI library loads on a CPU-only host and exports every declared symbol;
+host-side validation answers without touching a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixed_precision_paged_argus_gb300.argus as argus
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "argus.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(argus_[a-z0-9_]+)\s*\(", text)))
+
+
+def _lib():
+    if not os.path.exists(argus.lib_path()):
+        from mixed_precision_paged_argus_gb300 import build
+        build.build()
+    return argus.lib()
+
+
+def test_header_declares_the_five_operations():
+    names = _declared()
+    for op in ("argus_quantize_pages", "argus_paged_decode_attn", "argus_select_pages",
+               "argus_fold_lse", "argus_window_prefill_attn"):
+        assert op in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = _lib()
+    raw = ctypes.CDLL(argus.lib_path())
+    for name in _declared():
+        assert hasattr(raw, name), name
+    assert set(_declared()) <= set(argus.EXPORTS) | {"argus_status_string", "argus_last_error"} | set(_declared())
+
+
+def test_status_strings():
+    L = _lib()
+    assert L.argus_status_string(0) == b"ok"
+    assert L.argus_status_string(3) == b"workspace too small"
+
+
+def test_host_validation_without_gpu():
+    L = _lib()
+    # fold: negative rows is rejected before any CUDA call
+    assert L.argus_fold_lse(-1, 128, None, None, None, None, None) == 1
+    assert L.argus_fold_lse(4, 6, None, None, None, None, None) == 2
+    assert b"multiple of 4" in L.argus_last_error()
+    # decode: unsupported head_dim / grouping fail closed
+    a = argus.DecodeArgs()
+    a.g = argus.geom(8, 2, 96, 16)
+    a.batch, a.q_dtype, a.max_pages = 1, 0, 4
+    n = ctypes.c_size_t(0)
+    assert L.argus_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 2
+    a.g = argus.geom(18, 2, 128, 16)
+    assert L.argus_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 2
+    a.g = argus.geom(8, 2, 128, 24)
+    assert L.argus_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 2
+    g = argus.geom(8, 2, 128, 16)
+    assert L.argus_select_workspace_bytes(ctypes.byref(g), 2, 10, ctypes.byref(n)) == 0
+    assert n.value == 2 * 2 * 10 * 4

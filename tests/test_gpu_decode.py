@@ -1,0 +1,174 @@
+"""argus_paged_decode_attn on the GPU against the double-precision oracle.
+
+Tolerance (stated for attention outputs): max|err| <= 1e-3 * max|ref| + 1e-4 on
+the fp32 output; the fp16 output is compared the same way; the bf16 output
+must equal the round-to-nearest-even of the kernel's own fp32 output.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import mixed_precision_paged_argus_gb300.argus as argus
+from mixed_precision_paged_argus_gb300 import workloads as W
+import oracle
+from oracle import codecs as C
+from paged_cases import DEV, build_case, run_decode, tol
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(c, out, out32, lse, sel=None, cnt=None, width=0, expect_bad=0):
+    ref, ref_lse, bad = oracle.paged_decode(c.q64, c.Hkv, c.P, c.opools, c.page_codec, c.table, c.lens,
+                                            c.scale, sel_pages=sel, sel_count=cnt, sel_width=width)
+    assert bad == expect_bad
+    got = out32.cpu().numpy().astype(np.float64)
+    t = tol(ref)
+    err = np.abs(got - ref).max()
+    assert err <= t, "fp32 output max err %.3g > tol %.3g" % (err, t)
+    if out.dtype == torch.float16:
+        e16 = np.abs(out.float().cpu().numpy() - ref).max()
+        assert e16 <= t + np.abs(ref).max() * 2.0 ** -11, "fp16 output max err %.3g" % e16
+    else:
+        assert torch.equal(out.cpu(), out32.cpu().to(torch.bfloat16))
+    gl = lse.cpu().numpy().astype(np.float64)
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(gl), fin)
+    assert np.all(np.abs(gl[fin] - ref_lse[fin]) <= 1e-4 * np.maximum(1.0, np.abs(ref_lse[fin])))
+    return err
+
+
+@pytest.mark.parametrize("codec", [W.FP16, W.FP8_E4M3, W.INT8, W.INT4_G32])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [1, 7, 8])
+def test_single_codec_fp16_query(codec, D, G):
+    Hkv, P = 2, 16
+    lens = [150, 33, 16]
+    maxp = 10
+    pc = np.full((3, maxp), codec)
+    c = build_case(G * Hkv, Hkv, D, P, lens, pc, W.FP16, seed=11 + codec, outliers=True)
+    out, out32, lse, _ = run_decode(c, num_splits=3)
+    _check(c, out, out32, lse)
+
+
+@pytest.mark.parametrize("codec", [W.BF16, W.FP8_E4M3, W.INT8, W.INT4_G32])
+@pytest.mark.parametrize("G", [4, 8])
+def test_single_codec_bf16_query(codec, G):
+    Hkv, D, P = 2, 128, 16
+    lens = [300, 17]
+    pc = np.full((2, 20), codec)
+    c = build_case(G * Hkv, Hkv, D, P, lens, pc, W.BF16, seed=23 + codec)
+    out, out32, lse, _ = run_decode(c, out_dtype=torch.bfloat16, num_splits=0)
+    _check(c, out, out32, lse)
+
+
+def test_mixed_tiers_like_the_mixed_tier_workload():
+    """14 q / 2 KV heads, head_dim 64, newest pages FP16, then FP8, INT8, INT4."""
+    Hq, Hkv, D, P = 14, 2, 64, 64
+    n = 16
+    pc = W.mixed_tier_codecs(n).reshape(1, n)
+    c = build_case(Hq, Hkv, D, P, [n * P - 5], pc, W.FP16, seed=31, outliers=True)
+    for splits in (1, 4, 0):
+        out, out32, lse, _ = run_decode(c, num_splits=splits)
+        _check(c, out, out32, lse)
+
+
+def test_mixed_bf16_and_quantized_pages_bf16_query():
+    Hq, Hkv, D, P = 16, 2, 128, 32
+    rng = np.random.default_rng(3)
+    pc = rng.choice([W.BF16, W.FP8_E4M3, W.INT8, W.INT4_G32], size=(3, 12))
+    c = build_case(Hq, Hkv, D, P, [384, 200, 1], pc, W.BF16, seed=41)
+    out, out32, lse, _ = run_decode(c, out_dtype=torch.bfloat16, num_splits=5)
+    _check(c, out, out32, lse)
+
+
+def test_tiny_fp16_workload_full_size():
+    """Batch 1, 14 q / 2 KV heads, head_dim 64, 4 FP16 pages of 1024 tokens."""
+    Hq, Hkv, D, P = 14, 2, 64, 1024
+    pc = np.zeros((1, 4), np.int64)
+    c = build_case(Hq, Hkv, D, P, [4096], pc, W.FP16, seed=1000, permute=False)
+    out, out32, lse, _ = run_decode(c)
+    _check(c, out, out32, lse)
+
+
+def test_ragged_batch_permuted_slots_and_empty_rows():
+    Hq, Hkv, D, P = 32, 8, 128, 16
+    lens = [0, 1, 15, 16, 17, 257, 1000]
+    maxp = 64
+    pc = np.full((len(lens), maxp), W.FP8_E4M3)
+    c = build_case(Hq, Hkv, D, P, lens, pc, W.BF16, seed=51, extra_slots=9)
+    for splits in (0, 1, 2, 9):
+        out, out32, lse, _ = run_decode(c, out_dtype=torch.bfloat16, num_splits=splits)
+        _check(c, out, out32, lse)
+        assert torch.all(out32[0] == 0) and torch.all(torch.isinf(lse[0]))
+
+
+def test_selected_page_lists_and_invalid_entries():
+    Hq, Hkv, D, P = 32, 4, 128, 64
+    maxp = 40
+    lens = [40 * 64 - 10, 20 * 64 + 3]
+    pc = np.full((2, maxp), W.FP8_E4M3)
+    c = build_case(Hq, Hkv, D, P, lens, pc, W.BF16, seed=61)
+    width = 12
+    rng = np.random.default_rng(62)
+    sel = np.full((2, Hkv, width), -1, np.int32)
+    cnt = np.zeros((2, Hkv), np.int32)
+    for b in range(2):
+        n = -(-lens[b] // P)
+        for h in range(Hkv):
+            k = int(rng.integers(1, 9))
+            pages = sorted(rng.choice(n - 1, size=k, replace=False).tolist() + [n - 1])
+            sel[b, h, :len(pages)] = pages
+            cnt[b, h] = len(pages)
+    sel[1, 2, cnt[1, 2]] = 35           # beyond the sequence's pages -> skipped, counted
+    cnt[1, 2] += 1
+    cnt[0, 3] = width + 3               # more than the width -> clamped, counted
+    sel[0, 3, :] = np.arange(width)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, out32, lse, _ = run_decode(c, out_dtype=torch.bfloat16,
+                                    sel=torch.from_numpy(sel).to(DEV), sel_count=torch.from_numpy(cnt).to(DEV),
+                                    sel_width=width, status=status)
+    _check(c, out, out32, lse, sel=sel, cnt=cnt, width=width, expect_bad=2)
+    assert int(status.item()) == 2
+
+
+def test_bad_slot_is_skipped_and_counted():
+    Hq, Hkv, D, P = 8, 1, 64, 16
+    pc = np.full((1, 6), W.INT4_G32)
+    c = build_case(Hq, Hkv, D, P, [96], pc, W.FP16, seed=71)
+    table = c.table.copy()
+    table[0, 2] = 1000
+    c.table = table
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, out32, lse, _ = run_decode(c, status=status, table=torch.from_numpy(table).to(DEV))
+    _check(c, out, out32, lse, expect_bad=1)
+    assert int(status.item()) == 1
+
+
+def test_workspace_counters_left_zero_and_repeatable():
+    Hq, Hkv, D, P = 14, 2, 64, 64
+    pc = W.mixed_tier_codecs(16).reshape(1, 16)
+    c = build_case(Hq, Hkv, D, P, [16 * 64], pc, W.FP16, seed=81)
+    out_a, o32a, _, ws = run_decode(c, num_splits=8)
+    assert not ws[:256].any()
+    out_b, o32b, _, _ = run_decode(c, num_splits=8)
+    assert torch.equal(o32a, o32b)
+
+
+def test_unsupported_and_invalid_arguments():
+    Hq, Hkv, D, P = 8, 1, 64, 16
+    pc = np.full((1, 2), W.BF16)
+    c = build_case(Hq, Hkv, D, P, [20], pc, W.BF16, q_dtype=W.FP16, seed=91)
+    with pytest.raises(argus.ArgusError) as e:
+        run_decode(c)
+    assert e.value.status == 2          # BF16 pages with an FP16 query: fail closed
+    c2 = build_case(Hq, Hkv, D, P, [20], np.full((1, 2), W.FP16), W.FP16, seed=92)
+    args = argus.decode_args(c2.g, 1, c2.q, c2.pools, c2.d_codec, c2.d_table, c2.d_lens, 2, c2.scale,
+                             out_f32=torch.empty((1, Hq, D), device=DEV), num_splits=4)
+    need = argus.decode_workspace_bytes(args)
+    small = torch.zeros(need - 4, dtype=torch.uint8, device=DEV)
+    with pytest.raises(argus.ArgusError) as e:
+        argus.paged_decode_attn(args, small)
+    assert e.value.status == 3

@@ -1,0 +1,138 @@
+"""argus_quantize_pages on the GPU against the oracle: codes and scales bit-exact."""
+
+import numpy as np
+import pytest
+import torch
+
+import mixed_precision_paged_argus_gb300.argus as argus
+from mixed_precision_paged_argus_gb300 import workloads as W
+from oracle import codecs as C
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _gpu_quantize(src_t, src_dtype, codec, Hkv, P, D, src_slots, dst_slots, n_dst, valid=None, ckey=False):
+    g = argus.geom(Hkv, Hkv, D, P)
+    n_pages = len(src_slots)
+    pool = argus.Pool.empty(codec, n_dst, Hkv, P, D, device=DEV, zero=True)
+    ck = torch.zeros((n_pages, Hkv, D), dtype=torch.bfloat16, device=DEV) if ckey else None
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    argus.quantize_pages(g, src_dtype, src_t.to(DEV), src_t.shape[0],
+                         torch.tensor(src_slots, dtype=torch.int32, device=DEV), pool,
+                         torch.tensor(dst_slots, dtype=torch.int32, device=DEV), n_pages,
+                         None if valid is None else torch.tensor(valid, dtype=torch.int32, device=DEV),
+                         ck, status)
+    torch.cuda.synchronize()
+    return pool, ck, int(status.item())
+
+
+def _codes_np(pool):
+    return pool.codes.contiguous().view(torch.uint8).cpu().numpy()
+
+
+def _meta_np(pool):
+    if pool.meta is None:
+        return None
+    return pool.meta.contiguous().view(torch.uint8).cpu().numpy()
+
+
+def _compare(pool, codes, meta):
+    assert np.array_equal(_codes_np(pool), codes.view(np.uint8).reshape(_codes_np(pool).shape))
+    if meta is not None:
+        assert np.array_equal(_meta_np(pool), meta.view(np.uint8).reshape(_meta_np(pool).shape))
+
+
+def test_e4m3_encoder_exhaustive_over_fp16():
+    """Every finite fp16 value with |x| <= 448 encoded with scale exactly 1."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    x = bits.view(np.float16).astype(np.float32)
+    keep = np.isfinite(x) & (np.abs(x) <= 448)
+    vals = bits[keep]
+    P, D = 16, 64
+    per_unit = P * D - 1
+    n_units = -(-len(vals) // per_unit)
+    pad = np.full(n_units * per_unit, np.float16(0).view(np.uint16))
+    pad[:len(vals)] = vals
+    units = pad.reshape(n_units, per_unit)
+    big = np.full((n_units, 1), np.float16(448).view(np.uint16))
+    units = np.concatenate([units, big], axis=1).reshape(n_units, 1, 1, P, D)   # Hkv = 1, K side
+    src = np.zeros((n_units, 2, 1, P, D), np.uint16)
+    src[:, 0] = units[:, 0]
+    src[:, 1] = units[:, 0]
+    t = torch.from_numpy(src.view(np.int16)).view(torch.float16)
+    pool, _, st = _gpu_quantize(t, W.FP16, W.FP8_E4M3, 1, P, D, list(range(n_units)), list(range(n_units)), n_units)
+    assert st == 0
+    codes, meta = C.alloc_pool(C.CODEC_FP8_E4M3, n_units, 1, P, D)
+    C.quantize_pages(src, C.CODEC_FP16, list(range(n_units)), C.CODEC_FP8_E4M3, codes, meta, list(range(n_units)))
+    assert np.all(meta == 1.0)
+    _compare(pool, codes, meta)
+
+
+def test_int8_rounding_exhaustive_over_fp16():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    x = bits.view(np.float16).astype(np.float32)
+    vals = bits[np.isfinite(x) & (np.abs(x) <= 127)]
+    P, D = 16, 128
+    per_unit = P * D - 1
+    n_units = -(-len(vals) // per_unit)
+    pad = np.zeros(n_units * per_unit, np.uint16)
+    pad[:len(vals)] = vals
+    units = np.concatenate([pad.reshape(n_units, per_unit),
+                            np.full((n_units, 1), np.float16(-127).view(np.uint16))], axis=1)
+    src = np.zeros((n_units, 2, 1, P, D), np.uint16)
+    src[:, 0, 0] = units.reshape(n_units, P, D)
+    src[:, 1, 0] = units.reshape(n_units, P, D)
+    t = torch.from_numpy(src.view(np.int16)).view(torch.float16)
+    pool, _, _ = _gpu_quantize(t, W.FP16, W.INT8, 1, P, D, list(range(n_units)), list(range(n_units)), n_units)
+    codes, meta = C.alloc_pool(C.CODEC_INT8, n_units, 1, P, D)
+    C.quantize_pages(src, C.CODEC_FP16, list(range(n_units)), C.CODEC_INT8, codes, meta, list(range(n_units)))
+    _compare(pool, codes, meta)
+
+
+@pytest.mark.parametrize("codec", [W.FP8_E4M3, W.INT8, W.INT4_G32, "copy"])
+@pytest.mark.parametrize("src_dtype", [W.FP16, W.BF16])
+@pytest.mark.parametrize("D,P", [(64, 16), (128, 16), (128, 64), (64, 1024)])
+def test_random_pages_bit_exact_with_ckeys(codec, src_dtype, D, P):
+    if codec == "copy":
+        codec = src_dtype
+    Hkv, n_src, n_pages = 2, 7, 5
+    src = W.normal((n_src, 2, Hkv, P, D), src_dtype, 100 + D + P, outlier_seed=101)
+    src_slots = [6, 0, 3, 2, 5]
+    dst_slots = [1, 4, 0, 6, 2]
+    valid = [P, P - 3, 1, 0, P // 2]
+    pool, ck, st = _gpu_quantize(src, src_dtype, codec, Hkv, P, D, src_slots, dst_slots, 8, valid, ckey=True)
+    assert st == 0
+    codes, meta = C.alloc_pool(codec, 8, Hkv, P, D)
+    ock = C.quantize_pages(W.to_bits(src), src_dtype, src_slots, codec, codes, meta, dst_slots,
+                           valid_tokens=valid, want_ckey=True)
+    _compare(pool, codes, meta)
+    got = C.bf16_bits_to_f64(W.to_bits(ck.cpu()))
+    want = C.bf16_bits_to_f64(ock)
+    ulp = np.abs(want) * 2.0 ** -7 + 2.0 ** -133
+    assert np.all(np.abs(got - want) <= ulp)
+
+
+def test_bad_slots_are_counted_and_skipped():
+    Hkv, P, D = 1, 16, 64
+    src = W.normal((2, 2, Hkv, P, D), W.FP16, 9)
+    pool, _, st = _gpu_quantize(src, W.FP16, W.FP8_E4M3, Hkv, P, D, [0, 5, 1], [0, 1, 9], 2)
+    assert st == 2
+    codes = _codes_np(pool)
+    assert codes[0].any() and not codes[1].any()
+
+
+def test_zero_unit_gives_zero_scale():
+    Hkv, P, D = 1, 16, 128
+    src = torch.zeros((1, 2, Hkv, P, D), dtype=torch.bfloat16)
+    for codec in (W.FP8_E4M3, W.INT8, W.INT4_G32):
+        pool, _, _ = _gpu_quantize(src, W.BF16, codec, Hkv, P, D, [0], [0], 1)
+        assert not _codes_np(pool).any() and not _meta_np(pool).any()
+
+
+def test_invalid_arguments_fail_closed():
+    g = argus.geom(2, 2, 96, 16)
+    pool = argus.Pool.empty(W.FP8_E4M3, 1, 2, 16, 64, device=DEV)
+    with pytest.raises(argus.ArgusError) as e:
+        argus.quantize_pages(g, W.FP16, pool.codes, 1, pool.codes, pool, pool.codes, 1)
+    assert e.value.status == 2
