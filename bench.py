@@ -1,0 +1,376 @@
+"""Benchmark: paged mixed-codec decode attention on one GB300.
+
+Default workload (the mixed-tier decode the metric is quoted on): batch 1, 24
+layers, 14 query / 2 KV heads, head_dim 64, a 16,384-token context in 1024-token
+pages -- newest 4 pages FP16, next 4 FP8 e4m3 (fp32 scale per page and KV
+head), next 4 INT8, oldest 4 INT4 group-32 -- K/V ~ N(0,1) with 1% of elements
+x8.  One step = one decoded token through all 24 layers: 24 calls of
+argus_paged_decode_attn replayed as one CUDA graph; L2 is flushed (a 2 x L2
+write) before every timed step, outside the timed region.
+
+Printed value: decode attention microseconds per token per layer (lower is
+better), plus the effective KV bandwidth against the HBM roofline.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--legs]
+
+--impl reference times the CPU oracle (double precision, one process per host
+core) on a bounded sample of the same workload.  Under torchrun every rank
+runs an independent replica (the path has no exchange step); rank 0 prints.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode attn µs/token/layer & effective KV GB/s (% of GB300 HBM peak)"
+WORKLOAD = ("mixed_tier_decode: batch 1, 24 layers, 14 q / 2 kv heads, head_dim 64, 16384 tokens in "
+            "1024-token pages (4 FP16 newest, 4 FP8 e4m3, 4 INT8, 4 INT4 g32 oldest), N(0,1) with 1% x8")
+LAYERS, HQ, HKV, D, P, NPAGES = 24, 14, 2, 64, 1024, 16
+CTX = NPAGES * P
+
+
+def kv_bytes_per_layer():
+    from mixed_precision_paged_argus_gb300 import accounting as A
+    tiers = [A.FP16, A.FP8_E4M3, A.INT8, A.INT4_G32]
+    return sum(A.kv_bytes(c, 4 * P, HKV, D, 4) for c in tiers)
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def source_hash(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "mixed_precision_paged_argus_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key, src_files):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)[kernel_key]
+        if t.get("source_hash") == source_hash(src_files):
+            return float(t["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- workload
+
+def build_mixed_tier(dev):
+    """Device pools for all 24 layers (one pool per codec, 4 slots per layer),
+    per-layer block tables and queries.  Setup only: quantisation by the
+    library's own kernel, not timed."""
+    import torch
+    import mixed_precision_paged_argus_gb300.argus as argus
+    from mixed_precision_paged_argus_gb300 import workloads as W
+    g = argus.geom(HQ, HKV, D, P)
+    tiers = W.mixed_tier_codecs(NPAGES)
+    pools = {c: argus.Pool.empty(c, 4 * LAYERS, HKV, P, D, device=dev, zero=True)
+             for c in (W.FP16, W.FP8_E4M3, W.INT8, W.INT4_G32)}
+    tables, qs = [], []
+    for layer in range(LAYERS):
+        src = W.normal((NPAGES, 2, HKV, P, D), W.FP16, W.seed_of("mixed_tier", layer, 1), device=dev,
+                       outlier_seed=W.seed_of("mixed_tier", layer, 5))
+        perm = W.permutation(4, W.seed_of("mixed_tier", layer, 4))
+        table = np.zeros(NPAGES, np.int32)
+        for codec, pool in pools.items():
+            pages = [p for p in range(NPAGES) if tiers[p] == codec]
+            slots = [4 * layer + int(perm[i]) for i in range(4)]
+            argus.quantize_pages(g, W.FP16, src, NPAGES, torch.tensor(pages, dtype=torch.int32, device=dev),
+                                 pool, torch.tensor(slots, dtype=torch.int32, device=dev), len(pages))
+            table[pages] = slots
+        tables.append(torch.from_numpy(table.reshape(1, NPAGES)).to(dev))
+        qs.append(W.normal((1, HQ, D), W.FP16, W.seed_of("mixed_tier", layer, 0), device=dev))
+        del src
+    torch.cuda.synchronize()
+    codec_row = torch.from_numpy(tiers.reshape(1, NPAGES).astype(np.uint8)).to(dev)
+    lens = torch.tensor([CTX], dtype=torch.int32, device=dev)
+    return g, [pools[c] for c in sorted(pools)], tables, qs, codec_row, lens
+
+
+def run_gpu(args, rank, world):
+    import torch
+    import mixed_precision_paged_argus_gb300.argus as argus
+    from mixed_precision_paged_argus_gb300 import workloads as W
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    argus.lib()
+    g, pools, tables, qs, codec_row, lens = build_mixed_tier(dev)
+    scale = W.softmax_scale(D)
+    outs = [torch.empty((1, HQ, D), dtype=torch.float16, device=dev) for _ in range(LAYERS)]
+    arg_list = [argus.decode_args(g, 1, qs[l], pools, codec_row, tables[l], lens, NPAGES, scale, out=outs[l])
+                for l in range(LAYERS)]
+    ws_bytes = max(argus.decode_workspace_bytes(a) for a in arg_list)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
+
+    def step_layers():
+        for a in arg_list:
+            argus.paged_decode_attn(a, ws, ws_bytes, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step_layers()                       # first calls set kernel attributes (outside capture)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step_layers()
+    torch.cuda.synchronize()
+
+    def timed(n, fn):
+        times = []
+        for _ in range(n):
+            with torch.cuda.stream(stream):
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        return times
+
+    timed(args.warmup, graph.replay)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_wall0 = time.perf_counter()
+    times = timed(args.steps, graph.replay)
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    torch.cuda.synchronize()
+    ms_step = sum(times) / len(times)
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+        torch.distributed.barrier()
+
+    # ---- end to end through the public API with host buffers
+    q_host = torch.empty((LAYERS, 1, HQ, D), dtype=torch.float16).pin_memory()
+    for l in range(LAYERS):
+        q_host[l].copy_(qs[l].cpu())
+    out_host = torch.empty((LAYERS, 1, HQ, D), dtype=torch.float16).pin_memory()
+    q_dev = torch.empty((LAYERS, 1, HQ, D), dtype=torch.float16, device=dev)
+    out_dev = torch.empty((LAYERS, 1, HQ, D), dtype=torch.float16, device=dev)
+    e2e_args = [argus.decode_args(g, 1, q_dev[l], pools, codec_row, tables[l], lens, NPAGES, scale,
+                                  out=out_dev[l]) for l in range(LAYERS)]
+
+    def e2e_step():
+        q_dev.copy_(q_host, non_blocking=True)
+        for a in e2e_args:
+            argus.paged_decode_attn(a, ws, ws_bytes, stream=stream)
+        out_host.copy_(out_dev, non_blocking=True)
+
+    timed(args.warmup, e2e_step)
+    e2e_times = timed(args.steps, e2e_step)
+    ms_e2e = sum(e2e_times) / len(e2e_times)
+    if world > 1:
+        t = torch.tensor([ms_e2e], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    return ms_step, ms_e2e, clocks, t_wall, q_host.numel() * 2, out_host.numel() * 2
+
+
+# ---------------------------------------------------------------- oracle leg
+
+def _oracle_layer(layer):
+    """One layer of the mixed-tier workload in the oracle: generate, demote
+    (oracle), then time the decode alone.  Returns seconds of decode."""
+    import oracle
+    from oracle import codecs as C
+    from mixed_precision_paged_argus_gb300 import workloads as W
+    tiers = W.mixed_tier_codecs(NPAGES)
+    src = W.to_bits(W.normal((NPAGES, 2, HKV, P, D), W.FP16, W.seed_of("mixed_tier", layer, 1),
+                             outlier_seed=W.seed_of("mixed_tier", layer, 5)))
+    q64 = C.f16_bits_to_f64(W.to_bits(W.normal((1, HQ, D), W.FP16, W.seed_of("mixed_tier", layer, 0))))
+    pools, table = {}, np.zeros((1, NPAGES), np.int32)
+    for codec in (0, 2, 3, 4):
+        pages = [p for p in range(NPAGES) if tiers[p] == codec]
+        codes, meta = C.alloc_pool(codec, 4, HKV, P, D)
+        C.quantize_pages(src, C.CODEC_FP16, pages, codec, codes, meta, [0, 1, 2, 3])
+        pools[codec] = (codes, meta)
+        table[0, pages] = [0, 1, 2, 3]
+    t0 = time.perf_counter()
+    oracle.paged_decode(q64, HKV, P, pools, tiers.reshape(1, -1).astype(np.uint8), table,
+                        np.array([CTX]), float(np.float32(1 / math.sqrt(D))))
+    return time.perf_counter() - t0
+
+
+def oracle_leg(budget_s=15.0, max_layers=None):
+    """Oracle throughput on the host cores: layers decoded in parallel, one
+    process per core (spawn), until about budget_s of work."""
+    import multiprocessing as mp
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    cores = os.cpu_count() or 1
+    t_one = _oracle_layer(0)                       # calibrate (also warms imports)
+    per_core = max(1, int(budget_s / max(t_one, 1e-3) / 2))
+    n_layers = min(LAYERS * 4, cores * per_core) if max_layers is None else max_layers
+    ctx = mp.get_context("spawn")
+    t0 = time.perf_counter()
+    with ctx.Pool(cores) as pool:
+        decode_s = pool.map(_oracle_layer, [l % LAYERS for l in range(n_layers)])
+    wall = time.perf_counter() - t0
+    # decode-only time per layer per core; throughput across cores
+    per_layer = sum(decode_s) / len(decode_s)
+    us_per_token_layer = per_layer / cores * 1e6
+    return {"value": us_per_token_layer, "unit": "us/token/layer", "cores": cores, "kind": "oracle",
+            "sample": "%d layer-decodes of the mixed-tier workload (one token, 16384-token context each) on "
+                      "%d processes; decode time only, %.1f s wall incl. oracle demotion" % (n_layers, cores, wall),
+            "single_core_us_per_token_layer": per_layer * 1e6}
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="argus", choices=["argus", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    n_gpus = max(args.gpus, world)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        cb = oracle_leg()
+        line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "us/token/layer",
+                "n_gpus": n_gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step":
+                cb["value"] * LAYERS / 1000.0, "higher_is_better": False, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "batch": 1, "layers": LAYERS},
+                "cpu_baseline": {"value": cb["value"], "unit": cb["unit"], "cores": cb["cores"],
+                                 "kind": "oracle", "sample": cb["sample"]},
+                "e2e": {"value": cb["value"], "unit": "us/token/layer", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_leg()                         # before the first GPU call (spawned pool)
+    ms_step, ms_e2e, clocks, t_wall, h2d, d2h = run_gpu(args, rank, world)
+    if rank != 0:
+        return
+    hbm, _, peak_kind = peaks()
+    bytes_layer = kv_bytes_per_layer()
+    launch_ms = ms_step / LAYERS
+    achieved = bytes_layer / (launch_ms * 1e-3) / 1e9
+    us_tl = ms_step * 1000.0 / (LAYERS * world)
+    traffic = profiled_traffic("decode_mixed_tier", ["decode.cu", "common.cuh"])
+    line = {
+        "metric": METRIC, "value": us_tl, "unit": "us/token/layer", "n_gpus": n_gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16 mma / f32 accumulate (fp16, fp8, int8, int4 pages)",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": 1, "layers": LAYERS, "context": CTX, "page_tokens": P,
+                   "l2": "flushed (2x L2 write) before every timed step, outside the timed region",
+                   "replay": "24 decode launches as one CUDA graph",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "kv_bytes_per_layer": bytes_layer,
+        "kv_gbs": achieved,
+        "kv_frac_of_8tbs": achieved / 8000.0,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": traffic, "peak_kind": peak_kind + " (hbm_gbs)",
+                     "kernel": "argus decode_kernel<64,f16 query,f16 family>",
+                     "per_launch_bytes": bytes_layer},
+        "e2e": {"value": ms_e2e * 1000.0 / LAYERS, "unit": "us/token/layer", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "how": "per step: pinned q for 24 layers copied H2D, 24 argus_paged_decode_attn calls through "
+                       "the ctypes binding, outputs copied D2H; CUDA events on the stream"},
+        "gpu_launches": LAYERS * args.steps,
+        "clocks": clocks,
+        "wall_s_timed": t_wall,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

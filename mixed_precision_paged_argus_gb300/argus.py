@@ -183,7 +183,9 @@ def decode_args(g, batch, q, pools, page_codec, block_table, seq_lens, max_pages
     a.lse2_out = _ptr(lse2_out)
     a.status = _ptr(status)
     a.num_splits = int(num_splits)
-    a._keep = arr
+    # the struct holds raw pointers: keep every tensor it points to alive with it
+    a._keep = (arr, list(pools), q, page_codec, block_table, seq_lens, sel_pages, sel_count, out,
+               out_f32, lse2_out, status)
     return a
 
 

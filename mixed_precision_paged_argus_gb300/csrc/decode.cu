@@ -111,9 +111,12 @@ __device__ __forceinline__ uint32_t f16_magic_pair(uint32_t u, uint32_t sel) {
 // c for token rows r and r + 8.  Inside each 8-element run of head_dim held by
 // a lane, k positions (2t, 2t+1, 2t+8, 2t+9) of k-chunk 2i+hh map to elements
 // (2hh, 2hh+4, 2hh+1, 2hh+5); the query fragments use the same map.
+// INT4 pages give the raw codes (exact in fp16) and each row's per-group
+// {scale, zero} in kz, so that the scores can be formed exactly as
+// sum_g scale_g * (q_g . c_g) + zero_g * sum(q_g).
 template <int D>
 __device__ __forceinline__ void load_k_frags(int codec, const uint8_t* chunk, int r, int t,
-                                             uint32_t (&a)[D / 16][4]) {
+                                             uint32_t (&a)[D / 16][4], float (&kz)[2][D / 32][2]) {
   using L = Layout<D>;
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
@@ -154,14 +157,14 @@ __device__ __forceinline__ void load_k_frags(int codec, const uint8_t* chunk, in
 #pragma unroll
       for (int i = 0; i < L::kNI; ++i) {
         const uint32_t w = *reinterpret_cast<const uint32_t*>(chunk + L::kOffK + row * (D / 2) + 16 * i + 4 * t);
-        const uint32_t mz = *reinterpret_cast<const uint32_t*>(chunk + L::kOffMK + (row * L::kNI + i) * 4);
-        const uint32_t s2 = prmt(mz, mz, 0x1010);
-        const uint32_t z2 = prmt(mz, mz, 0x3232);
+        const __half2 mz = *reinterpret_cast<const __half2*>(chunk + L::kOffMK + (row * L::kNI + i) * 4);
+        kz[rr][i][0] = __low2float(mz);
+        kz[rr][i][1] = __high2float(mz);
         const uint32_t magic = 0x64006400u;
-        a[2 * i][rr] = hfma2_u32(hsub2_u32(lop3_and_or(w, 0x000F000Fu, magic), magic), s2, z2);
-        a[2 * i][2 + rr] = hfma2_u32(hsub2_u32(lop3_and_or(w >> 4, 0x000F000Fu, magic), magic), s2, z2);
-        a[2 * i + 1][rr] = hfma2_u32(hsub2_u32(lop3_and_or(w >> 8, 0x000F000Fu, magic), magic), s2, z2);
-        a[2 * i + 1][2 + rr] = hfma2_u32(hsub2_u32(lop3_and_or(w >> 12, 0x000F000Fu, magic), magic), s2, z2);
+        a[2 * i][rr] = hsub2_u32(lop3_and_or(w, 0x000F000Fu, magic), magic);
+        a[2 * i][2 + rr] = hsub2_u32(lop3_and_or(w >> 4, 0x000F000Fu, magic), magic);
+        a[2 * i + 1][rr] = hsub2_u32(lop3_and_or(w >> 8, 0x000F000Fu, magic), magic);
+        a[2 * i + 1][2 + rr] = hsub2_u32(lop3_and_or(w >> 12, 0x000F000Fu, magic), magic);
       }
     }
   }
@@ -432,6 +435,7 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
   const int r = lane >> 2, t = lane & 3;
   // query fragments (B operand of Q.K: k = head_dim, n = query head r)
   uint32_t qf[KC][2], qb[KC][2];
+  float qgs[D / 32][2];  // per-group query sums of heads 2t, 2t+1 (fp16 domain)
   float qscale_h0 = 1.f, qscale_h1 = 1.f;  // 2^-e of heads 2t, 2t+1 (bf16 q in fp16 MMAs)
   {
     float qv[D / 4];
@@ -480,6 +484,14 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
         qf[2 * i][1] = pack_f16x2(e8[1] * e_scale, e8[5] * e_scale);
         qf[2 * i + 1][0] = pack_f16x2(e8[2] * e_scale, e8[6] * e_scale);
         qf[2 * i + 1][1] = pack_f16x2(e8[3] * e_scale, e8[7] * e_scale);
+        // sum of this head's fp16 query values over 32-dim group i (INT4 zero-points)
+        float part = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) part += __half2float(__float2half_rn(e8[e] * e_scale));
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        qgs[i][0] = __shfl_sync(0xffffffffu, part, 4 * (2 * t));
+        qgs[i][1] = __shfl_sync(0xffffffffu, part, 4 * (2 * t + 1));
       }
     }
   }
@@ -505,10 +517,24 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
       {
         uint32_t a[KC][4];
-        load_k_frags<D>(d.codec, chunk, r, t, a);
+        float kz[2][D / 32][2];
+        load_k_frags<D>(d.codec, chunk, r, t, a, kz);
         if (FAM == kFamBF16 || (FAM == kFamMixed && bf)) {
 #pragma unroll
           for (int c = 0; c < KC; ++c) mma_bf16(sc, a[c][0], a[c][1], a[c][2], a[c][3], qb[c][0], qb[c][1]);
+        } else if (FAM != kFamBF16 && d.codec == ARGUS_INT4_G32) {
+          float sg[D / 32][4];
+#pragma unroll
+          for (int i = 0; i < D / 32; ++i) sg[i][0] = sg[i][1] = sg[i][2] = sg[i][3] = 0.f;
+#pragma unroll
+          for (int c = 0; c < KC; ++c) mma_f16(sg[c / 2], a[c][0], a[c][1], a[c][2], a[c][3], qf[c][0], qf[c][1]);
+#pragma unroll
+          for (int i = 0; i < D / 32; ++i) {
+            sc[0] += kz[0][i][0] * sg[i][0] + kz[0][i][1] * qgs[i][0];
+            sc[1] += kz[0][i][0] * sg[i][1] + kz[0][i][1] * qgs[i][1];
+            sc[2] += kz[1][i][0] * sg[i][2] + kz[1][i][1] * qgs[i][0];
+            sc[3] += kz[1][i][0] * sg[i][3] + kz[1][i][1] * qgs[i][1];
+          }
         } else {
 #pragma unroll
           for (int c = 0; c < KC; ++c) mma_f16(sc, a[c][0], a[c][1], a[c][2], a[c][3], qf[c][0], qf[c][1]);
