@@ -41,7 +41,7 @@ constexpr int kConsumerWarps = 4;
 constexpr int kChunksPerStage = kConsumerWarps;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kMaxG = 8;
-constexpr int kMaxSplits = 1024;  // bounds the fold's shared-memory weights
+constexpr int kMaxSplits = 512;  // bounds the fold's shared-memory weights
 
 enum Family { kFamF16 = 0, kFamBF16 = 1, kFamMixed = 2 };
 
@@ -66,7 +66,8 @@ struct Params {
   int cps;         // chunks per split, a multiple of kChunksPerStage
   int num_splits;  // grid.x
   uint32_t* counters;
-  float* part;     // [B][Hkv][num_splits][G][D + 1]
+  float* part_o;   // [B][Hkv][num_splits][G][D]
+  float* part_lse; // [B][Hkv][num_splits][G]
 };
 
 struct ChunkDesc {
@@ -291,6 +292,11 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
   ChunkDesc* descs = reinterpret_cast<ChunkDesc*>(smem + L::kDescOff);
   int* misc = reinterpret_cast<int*>(smem + L::kMiscOff);
 
+  // Programmatic dependent launch: the next kernel on the stream may start its
+  // prologue (block-table walk and K/V prefetch) while this grid finishes; every
+  // read of data a predecessor may write (q) and every global write below
+  // happens after griddepcontrol.wait.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hkv = p.Hkv, G = p.G, P = p.P;
@@ -316,6 +322,7 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
 
   if (c_begin >= c_end) {
     if (n_active == 0 && split == 0) {  // empty visible set: o = 0, lse2 = -inf
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
         const size_t o = (row0 + idx / D) * D + idx % D;
         if (p.out) {
@@ -333,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 2);  // producer: expect_tx arrival + descriptor arrival
       mbar_init(&empty[s], kConsumerWarps);
     }
     misc[0] = 0;  // timeout flag
@@ -354,14 +361,18 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
           break;
         }
       }
+      // Two arrivals complete a stage: the first announces the transaction
+      // bytes before any copy is issued, the second publishes the descriptors
+      // (written after the copies are in flight, overlapping the scale loads).
       uint32_t kv_bytes = 0, m_bytes = 0;
       const uint8_t *srcK = nullptr, *srcV = nullptr, *srcMK = nullptr, *srcMV = nullptr;
+      ChunkDesc d;
+      d.codec = -1;
+      d.n_valid = 0;
+      d.kscale = 1.f;
+      d.vscale = 1.f;
+      long long slot_id = 0;
       if (lane < kChunksPerStage) {
-        ChunkDesc d;
-        d.codec = -1;
-        d.n_valid = 0;
-        d.kscale = 1.f;
-        d.vscale = 1.f;
         const int ci = c_begin + s * kChunksPerStage + lane;
         if (ci < c_end) {
           const int v = ci / cpp, cip = ci - v * cpp;
@@ -379,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
             const int nv = min(kChunk, seq_len - tok0);
             if (nv > 0) {
               const int codec = p.page_codec[(size_t)b * p.max_pages + page];
-              const long long slot_id = p.block_table[(size_t)b * p.max_pages + page];
+              slot_id = p.block_table[(size_t)b * p.max_pages + page];
               bool ok = codec >= 0 && codec <= 4 && p.codes[codec] != nullptr;
               if (ok) {
                 const int fam = codec_family(codec);
@@ -399,10 +410,6 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
                   srcMK = p.meta[codec] + rk * (L::kNI * 4);
                   srcMV = p.meta[codec] + rv * (L::kNI * 4);
                   m_bytes = kChunk * L::kNI * 4;
-                } else if (codec == ARGUS_FP8_E4M3 || codec == ARGUS_INT8) {
-                  const float* ms = reinterpret_cast<const float*>(p.meta[codec]);
-                  d.kscale = ms[((size_t)slot_id * 2 + 0) * Hkv + h];
-                  d.vscale = ms[((size_t)slot_id * 2 + 1) * Hkv + h];
                 }
                 d.codec = codec;
                 d.n_valid = nv;
@@ -410,12 +417,10 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
             }
           }
         }
-        descs[slot * kChunksPerStage + lane] = d;
       }
       uint32_t total = 2 * (kv_bytes + m_bytes);
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
-      __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(&full[slot], total);
       __syncwarp();
       if (kv_bytes) {
@@ -427,11 +432,22 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
           bulk_g2s(dst + L::kOffMV, srcMV, m_bytes, &full[slot]);
         }
       }
+      if (lane < kChunksPerStage) {
+        if (d.codec == ARGUS_FP8_E4M3 || d.codec == ARGUS_INT8) {
+          const float* ms = reinterpret_cast<const float*>(p.meta[d.codec]);
+          d.kscale = ms[((size_t)slot_id * 2 + 0) * Hkv + h];
+          d.vscale = ms[((size_t)slot_id * 2 + 1) * Hkv + h];
+        }
+        descs[slot * kChunksPerStage + lane] = d;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[slot]);
     }
     return;
   }
 
   // -------------------------------------------------------------- consumers
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int r = lane >> 2, t = lane & 3;
   // query fragments (B operand of Q.K: k = head_dim, n = query head r)
   uint32_t qf[KC][2], qb[KC][2];
@@ -628,7 +644,9 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
   const int tid = threadIdx.x;  // 0 .. 127
   const int nthr = kConsumerWarps * 32;
   const bool direct = (n_active == 1);
-  float* part_bh = p.part + ((size_t)b * Hkv + h) * p.num_splits * G * (D + 1);
+  const size_t bh = (size_t)b * Hkv + h;
+  float* po_bh = p.part_o + bh * p.num_splits * G * D;
+  float* pl_bh = p.part_lse + bh * p.num_splits * G;
   for (int idx = tid; idx < G * D; idx += nthr) {
     const int g = idx / D, dd = idx - g * D;
     float M = -INFINITY;
@@ -655,9 +673,8 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
       if (p.out_f32) p.out_f32[oi] = o;
       if (p.lse2_out && dd == 0) p.lse2_out[row0 + g] = lse2;
     } else {
-      float* dst = part_bh + ((size_t)split * G + g) * (D + 1);
-      dst[dd] = o;
-      if (dd == 0) dst[D] = lse2;
+      po_bh[((size_t)split * G + g) * D + dd] = o;
+      if (dd == 0) pl_bh[(size_t)split * G + g] = lse2;
     }
   }
   if (direct) return;
@@ -665,41 +682,57 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
   // ------------------------------------------- last CTA folds the splits
   __threadfence();
   consumer_bar();
-  if (tid == 0) misc[1] = (int)atomicAdd(p.counters + (size_t)b * Hkv + h, 1u);
+  if (tid == 0) misc[1] = (int)atomicAdd(p.counters + bh, 1u);
   consumer_bar();
   if (misc[1] != n_active - 1) return;
   __threadfence();
-  // weights 2^(lse_s - L) per (split, head)
-  for (int g = tid; g < G; g += nthr) {
+  float* wl = wts;                                  // [n_active][G] partial lse
+  float* ww = wts + n_active * G;                   // [n_active][G] fold weights
+  float* wlse = ww + n_active * G;                  // [G] folded lse
+  for (int i = tid; i < n_active * G; i += nthr) wl[i] = __ldcg(pl_bh + i);
+  consumer_bar();
+  const int cw = tid >> 5, cl = tid & 31;
+  for (int g = cw; g < G; g += kConsumerWarps) {
     float M = -INFINITY;
-    for (int s = 0; s < n_active; ++s) M = fmaxf(M, __ldcg(part_bh + ((size_t)s * G + g) * (D + 1) + D));
+    for (int s2 = cl; s2 < n_active; s2 += 32) M = fmaxf(M, wl[s2 * G + g]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float Lsum = 0.f;
-    if (M != -INFINITY) {
-      for (int s = 0; s < n_active; ++s)
-        Lsum += fast_exp2(__ldcg(part_bh + ((size_t)s * G + g) * (D + 1) + D) - M);
-    }
+    if (M != -INFINITY)
+      for (int s2 = cl; s2 < n_active; s2 += 32) Lsum += fast_exp2(wl[s2 * G + g] - M);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
     const float lse = (M == -INFINITY) ? -INFINITY : M + log2f(Lsum);
-    for (int s = 0; s < n_active; ++s) {
-      const float ls = __ldcg(part_bh + ((size_t)s * G + g) * (D + 1) + D);
-      wts[s * kMaxG + g] = (lse == -INFINITY) ? 0.f : fast_exp2(ls - lse);
-    }
-    wts[n_active * kMaxG + g] = lse;
+    for (int s2 = cl; s2 < n_active; s2 += 32)
+      ww[s2 * G + g] = (lse == -INFINITY) ? 0.f : fast_exp2(wl[s2 * G + g] - lse);
+    if (cl == 0) wlse[g] = lse;
   }
   consumer_bar();
-  for (int idx = tid; idx < G * D; idx += nthr) {
-    const int g = idx / D, dd = idx - g * D;
-    float o = 0.f;
-    for (int s = 0; s < n_active; ++s) {
-      const float w = wts[s * kMaxG + g];
-      if (w != 0.f) o += w * __ldcg(part_bh + ((size_t)s * G + g) * (D + 1) + dd);
+  constexpr int D4 = D / 4;
+  for (int idx = tid; idx < G * D4; idx += nthr) {
+    const int g = idx / D4, d4 = idx - g * D4;
+    float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4* src = reinterpret_cast<const float4*>(po_bh + (size_t)g * D) + d4;
+#pragma unroll 8
+    for (int s2 = 0; s2 < n_active; ++s2) {
+      const float w = ww[s2 * G + g];
+      const float4 x = __ldcg(src + (size_t)s2 * G * D4);
+      acc4.x += w * x.x;
+      acc4.y += w * x.y;
+      acc4.z += w * x.z;
+      acc4.w += w * x.w;
     }
-    const size_t oi = (row0 + g) * D + dd;
-    if (p.out) {
-      if (p.out_bf16) reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
-      else reinterpret_cast<__half*>(p.out)[oi] = __float2half_rn(o);
+    const float ov[4] = {acc4.x, acc4.y, acc4.z, acc4.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const size_t oi = (row0 + g) * D + 4 * d4 + e;
+      if (p.out) {
+        if (p.out_bf16) reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(ov[e]);
+        else reinterpret_cast<__half*>(p.out)[oi] = __float2half_rn(ov[e]);
+      }
+      if (p.out_f32) p.out_f32[oi] = ov[e];
     }
-    if (p.out_f32) p.out_f32[oi] = o;
-    if (p.lse2_out && dd == 0) p.lse2_out[row0 + g] = wts[n_active * kMaxG + g];
+    if (p.lse2_out && d4 == 0) p.lse2_out[row0 + g] = wlse[g];
   }
   if (tid == 0) p.counters[(size_t)b * Hkv + h] = 0u;
 }
@@ -710,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
 struct Plan {
   int D, G, cps, num_splits, fam;
   bool q_bf16;
-  size_t counter_bytes, ws_bytes;
+  size_t counter_bytes, part_o_bytes, ws_bytes;
 };
 
 static argus_status plan(const argus_decode_args* a, Plan* pl) {
@@ -781,8 +814,9 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
   pl->num_splits = (int)std::max<long long>(1, (max_chunks + cps - 1) / cps);
   if (pl->num_splits > 65535) return fail(ARGUS_E_UNSUPPORTED, "decode: too many splits");
   pl->counter_bytes = ((size_t)std::max(a->batch, 1) * g.n_kv_heads * 4 + 255) / 256 * 256;
-  pl->ws_bytes = pl->counter_bytes +
-                 (size_t)std::max(a->batch, 1) * g.n_kv_heads * pl->num_splits * G * (g.head_dim + 1) * 4;
+  pl->part_o_bytes = (size_t)std::max(a->batch, 1) * g.n_kv_heads * pl->num_splits * G * g.head_dim * 4;
+  pl->ws_bytes = pl->counter_bytes + pl->part_o_bytes +
+                 (size_t)std::max(a->batch, 1) * g.n_kv_heads * pl->num_splits * G * 4;
   return ARGUS_OK;
 }
 
@@ -796,7 +830,18 @@ static argus_status launch_t(const Params& p, dim3 grid, cudaStream_t s) {
     if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "decode: smem attribute: %s", cudaGetErrorString(e));
     configured = true;
   }
-  decode_kernel<D, QBF16, FAM><<<grid, kThreads, L::kSmemBytes, s>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<D, QBF16, FAM>, p);
+  if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "argus_paged_decode_attn: %s", cudaGetErrorString(e));
   return launch_status("argus_paged_decode_attn");
 }
 
@@ -868,7 +913,9 @@ extern "C" argus_status argus_paged_decode_attn(const argus_decode_args* a, void
   p.cps = pl.cps;
   p.num_splits = pl.num_splits;
   p.counters = static_cast<uint32_t*>(ws);
-  p.part = ws ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.counter_bytes) : nullptr;
+  p.part_o = ws ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.counter_bytes) : nullptr;
+  p.part_lse = ws ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.counter_bytes + pl.part_o_bytes)
+                  : nullptr;
   dim3 grid(pl.num_splits, a->g.n_kv_heads, a->batch);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (pl.D == 64) return launch_d<64>(p, pl, grid, s);
