@@ -350,103 +350,114 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    for (int s = 0; s < n_stages; ++s) {
-      const int slot = s % L::kStages;
-      if (s >= L::kStages) {
-        if (!mbar_wait(&empty[slot], ((s / L::kStages) - 1) & 1)) {
-          if (lane == 0) {
-            misc[0] = 1;
-            if (p.status) atomicOr(p.status, kStatusTimeoutBit);
-          }
-          break;
-        }
-      }
-      // Two arrivals complete a stage: the first announces the transaction
-      // bytes before any copy is issued, the second publishes the descriptors
-      // (written after the copies are in flight, overlapping the scale loads).
-      uint32_t kv_bytes = 0, m_bytes = 0;
-      const uint8_t *srcK = nullptr, *srcV = nullptr, *srcMK = nullptr, *srcMV = nullptr;
+    // Chunks are translated 32 at a time, one per lane, so that the block-table
+    // and scale lookups of eight stages cost two dependent round trips; the
+    // lanes then issue their chunk's bulk copies stage by stage.
+    bool stop = false;
+    for (int base = 0; base < n_local && !stop; base += 32) {
       ChunkDesc d;
       d.codec = -1;
       d.n_valid = 0;
       d.kscale = 1.f;
       d.vscale = 1.f;
-      long long slot_id = 0;
-      if (lane < kChunksPerStage) {
-        const int ci = c_begin + s * kChunksPerStage + lane;
-        if (ci < c_end) {
-          const int v = ci / cpp, cip = ci - v * cpp;
-          int page = v;
-          bool good = true;
-          if (sparse) {
-            page = p.sel_pages[((size_t)b * Hkv + h) * p.sel_width + v];
-            if (page < 0 || page >= n_pages_b) {
-              good = false;
+      uint32_t kv_bytes = 0, m_bytes = 0;
+      const uint8_t *srcK = nullptr, *srcV = nullptr, *srcMK = nullptr, *srcMV = nullptr;
+      const int ci = c_begin + base + lane;
+      if (base + lane < n_local) {
+        const int v = ci / cpp, cip = ci - v * cpp;
+        int page = v;
+        bool good = true;
+        if (sparse) {
+          page = p.sel_pages[((size_t)b * Hkv + h) * p.sel_width + v];
+          if (page < 0 || page >= n_pages_b) {
+            good = false;
+            if (cip == 0 && p.status) atomicAdd(p.status, 1u);
+          }
+        }
+        if (good) {
+          const int tok0 = page * P + cip * kChunk;
+          const int nv = min(kChunk, seq_len - tok0);
+          if (nv > 0) {
+            const int codec = p.page_codec[(size_t)b * p.max_pages + page];
+            const long long slot_id = p.block_table[(size_t)b * p.max_pages + page];
+            bool ok = codec >= 0 && codec <= 4 && p.codes[codec] != nullptr;
+            if (ok) {
+              const int fam = codec_family(codec);
+              ok = (FAM == kFamMixed) || (FAM == fam);
+            }
+            if (ok) ok = slot_id >= 0 && slot_id < p.n_slots[codec];
+            if (!ok) {
               if (cip == 0 && p.status) atomicAdd(p.status, 1u);
-            }
-          }
-          if (good) {
-            const int tok0 = page * P + cip * kChunk;
-            const int nv = min(kChunk, seq_len - tok0);
-            if (nv > 0) {
-              const int codec = p.page_codec[(size_t)b * p.max_pages + page];
-              slot_id = p.block_table[(size_t)b * p.max_pages + page];
-              bool ok = codec >= 0 && codec <= 4 && p.codes[codec] != nullptr;
-              if (ok) {
-                const int fam = codec_family(codec);
-                ok = (FAM == kFamMixed) || (FAM == fam);
+            } else {
+              const int rowb = (codec <= ARGUS_BF16) ? 2 * D : (codec == ARGUS_INT4_G32 ? D / 2 : D);
+              const size_t rk = (((size_t)slot_id * 2 + 0) * Hkv + h) * P + (size_t)cip * kChunk;
+              const size_t rv = (((size_t)slot_id * 2 + 1) * Hkv + h) * P + (size_t)cip * kChunk;
+              srcK = p.codes[codec] + rk * rowb;
+              srcV = p.codes[codec] + rv * rowb;
+              kv_bytes = kChunk * rowb;
+              if (codec == ARGUS_INT4_G32) {
+                srcMK = p.meta[codec] + rk * (L::kNI * 4);
+                srcMV = p.meta[codec] + rv * (L::kNI * 4);
+                m_bytes = kChunk * L::kNI * 4;
+              } else if (codec == ARGUS_FP8_E4M3 || codec == ARGUS_INT8) {
+                const float* ms = reinterpret_cast<const float*>(p.meta[codec]);
+                d.kscale = ms[((size_t)slot_id * 2 + 0) * Hkv + h];
+                d.vscale = ms[((size_t)slot_id * 2 + 1) * Hkv + h];
               }
-              if (ok) ok = slot_id >= 0 && slot_id < p.n_slots[codec];
-              if (!ok) {
-                if (cip == 0 && p.status) atomicAdd(p.status, 1u);
-              } else {
-                const int rowb = (codec <= ARGUS_BF16) ? 2 * D : (codec == ARGUS_INT4_G32 ? D / 2 : D);
-                const size_t rk = (((size_t)slot_id * 2 + 0) * Hkv + h) * P + (size_t)cip * kChunk;
-                const size_t rv = (((size_t)slot_id * 2 + 1) * Hkv + h) * P + (size_t)cip * kChunk;
-                srcK = p.codes[codec] + rk * rowb;
-                srcV = p.codes[codec] + rv * rowb;
-                kv_bytes = kChunk * rowb;
-                if (codec == ARGUS_INT4_G32) {
-                  srcMK = p.meta[codec] + rk * (L::kNI * 4);
-                  srcMV = p.meta[codec] + rv * (L::kNI * 4);
-                  m_bytes = kChunk * L::kNI * 4;
-                }
-                d.codec = codec;
-                d.n_valid = nv;
-              }
+              d.codec = codec;
+              d.n_valid = nv;
             }
           }
         }
       }
-      uint32_t total = 2 * (kv_bytes + m_bytes);
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
-      if (lane == 0) mbar_arrive_expect_tx(&full[slot], total);
-      __syncwarp();
-      if (kv_bytes) {
-        uint8_t* dst = smem + slot * L::kStageBytes + lane * L::kChunkBytes;
-        bulk_g2s(dst + L::kOffK, srcK, kv_bytes, &full[slot]);
-        bulk_g2s(dst + L::kOffV, srcV, kv_bytes, &full[slot]);
-        if (m_bytes) {
-          bulk_g2s(dst + L::kOffMK, srcMK, m_bytes, &full[slot]);
-          bulk_g2s(dst + L::kOffMV, srcMV, m_bytes, &full[slot]);
+      const uint32_t my_bytes = 2 * (kv_bytes + m_bytes);
+      const int n_batch_stages = min(8, (n_local - base + kChunksPerStage - 1) / kChunksPerStage);
+      for (int st = 0; st < n_batch_stages; ++st) {
+        const int s = base / kChunksPerStage + st;
+        const int slot = s % L::kStages;
+        if (s >= L::kStages) {
+          if (!mbar_wait(&empty[slot], ((s / L::kStages) - 1) & 1)) {
+            if (lane == 0) {
+              misc[0] = 1;
+              if (p.status) atomicOr(p.status, kStatusTimeoutBit);
+            }
+            stop = true;
+            break;
+          }
         }
-      }
-      if (lane < kChunksPerStage) {
-        if (d.codec == ARGUS_FP8_E4M3 || d.codec == ARGUS_INT8) {
-          const float* ms = reinterpret_cast<const float*>(p.meta[d.codec]);
-          d.kscale = ms[((size_t)slot_id * 2 + 0) * Hkv + h];
-          d.vscale = ms[((size_t)slot_id * 2 + 1) * Hkv + h];
+        const bool mine = (lane >> 2) == st;  // lanes 4st .. 4st+3 own this stage
+        uint32_t total = mine ? my_bytes : 0u;
+        total += __shfl_xor_sync(0xffffffffu, total, 1);
+        total += __shfl_xor_sync(0xffffffffu, total, 2);
+        total = __shfl_sync(0xffffffffu, total, 4 * st);
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], total);
+        __syncwarp();
+        if (mine) {
+          const int j = lane & 3;
+          if (kv_bytes) {
+            uint8_t* dst = smem + slot * L::kStageBytes + j * L::kChunkBytes;
+            bulk_g2s(dst + L::kOffK, srcK, kv_bytes, &full[slot]);
+            bulk_g2s(dst + L::kOffV, srcV, kv_bytes, &full[slot]);
+            if (m_bytes) {
+              bulk_g2s(dst + L::kOffMK, srcMK, m_bytes, &full[slot]);
+              bulk_g2s(dst + L::kOffMV, srcMV, m_bytes, &full[slot]);
+            }
+          }
+          descs[slot * kChunksPerStage + j] = d;
         }
-        descs[slot * kChunksPerStage + lane] = d;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[slot]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&full[slot]);
     }
     return;
   }
 
   // -------------------------------------------------------------- consumers
+  if (warp == 0 && lane < G) {
+    // pull this CTA's query rows toward L2 while the predecessor finishes
+    const char* qrow = reinterpret_cast<const char*>(p.q) + ((row0 + lane) * D) * 2;
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow));
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int r = lane >> 2, t = lane & 3;
   // query fragments (B operand of Q.K: k = head_dim, n = query head r)
