@@ -834,12 +834,14 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
 template <int D, bool QBF16, int FAM>
 static argus_status launch_t(const Params& p, dim3 grid, cudaStream_t s) {
   using L = Layout<D>;
-  static bool configured = false;
-  if (!configured) {
+  static bool configured[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(ARGUS_E_LAUNCH, "decode: no device");
+  if (!configured[dev]) {
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, QBF16, FAM>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "decode: smem attribute: %s", cudaGetErrorString(e));
-    configured = true;
+    configured[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -879,18 +881,17 @@ extern "C" argus_status argus_decode_workspace_bytes(const argus_decode_args* ar
   return ARGUS_OK;
 }
 
-extern "C" argus_status argus_paged_decode_attn(const argus_decode_args* a, void* ws,
-                                                size_t ws_bytes, void* stream) {
-  Plan pl;
-  argus_status st = plan(a, &pl);
-  if (st != ARGUS_OK) return st;
-  if (a->batch == 0) return ARGUS_OK;
+static argus_status check_io(const argus_decode_args* a) {
   if (!a->q || !a->page_codec || !a->block_table || !a->seq_lens)
     return fail(ARGUS_E_INVALID, "decode: q, page_codec, block_table and seq_lens are required");
   if (reinterpret_cast<uintptr_t>(a->q) & 15) return fail(ARGUS_E_INVALID, "decode: q not 16-byte aligned");
   if (!a->out && !a->out_f32 && !a->lse2_out) return fail(ARGUS_E_INVALID, "decode: no output given");
-  if (ws_bytes < pl.ws_bytes || (pl.num_splits > 1 && !ws))
-    return fail(ARGUS_E_WORKSPACE, "decode: workspace %zu bytes < %zu needed", ws_bytes, pl.ws_bytes);
+  return ARGUS_OK;
+}
+
+// Fill the kernel parameters and launch; ws holds pl.ws_bytes bytes whose
+// counter block is zero.
+static argus_status run(const argus_decode_args* a, const Plan& pl, void* ws, void* stream) {
   Params p{};
   p.B = a->batch;
   p.Hkv = a->g.n_kv_heads;
@@ -932,3 +933,16 @@ extern "C" argus_status argus_paged_decode_attn(const argus_decode_args* a, void
   if (pl.D == 64) return launch_d<64>(p, pl, grid, s);
   return launch_d<128>(p, pl, grid, s);
 }
+
+extern "C" argus_status argus_paged_decode_attn(const argus_decode_args* a, void* ws,
+                                                size_t ws_bytes, void* stream) {
+  Plan pl;
+  argus_status st = plan(a, &pl);
+  if (st != ARGUS_OK) return st;
+  if (a->batch == 0) return ARGUS_OK;
+  if ((st = check_io(a)) != ARGUS_OK) return st;
+  if (ws_bytes < pl.ws_bytes || (pl.num_splits > 1 && !ws))
+    return fail(ARGUS_E_WORKSPACE, "decode: workspace %zu bytes < %zu needed", ws_bytes, pl.ws_bytes);
+  return run(a, pl, ws, stream);
+}
+
