@@ -172,6 +172,36 @@ argus_status argus_paged_decode_attn(const argus_decode_args* args, void* ws,
                                      size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * argus_paged_decode_attn_noalloc -- the same decode attention, for callers
+ * that cannot allocate device memory.  (The source pages have no counterpart:
+ * it is an interface addition of this library.)
+ *
+ * Who needs it: runtimes whose memory planner hands out all device memory
+ * before decoding starts, and host code that may not call cudaMalloc on the
+ * decode path (cudaMalloc can synchronise the device).  Such callers cannot
+ * provide the workspace argus_paged_decode_attn wants.
+ *
+ * How it works: the split-combine scratch is a fixed file-scope device array
+ * of ARGUS_NOALLOC_SCRATCH_BYTES bytes inside the library; every GPU that
+ * loads the library holds it until the process exits.  The caller still
+ * passes every input and output in args.  The call allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *   - The first call on a device resolves the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call clears the array's counter block on `stream` before its
+ *     kernel, since the array keeps the previous call's contents.
+ *   - All calls share the one array: calls that overlap on the GPU (different
+ *     streams, or different host threads on the same device) race.  Serialise
+ *     them on one stream.
+ *   - Arguments whose scratch need (argus_decode_workspace_bytes) exceeds
+ *     ARGUS_NOALLOC_SCRATCH_BYTES are rejected with ARGUS_E_WORKSPACE; a
+ *     smaller num_splits lowers the need.
+ * ------------------------------------------------------------------------- */
+#define ARGUS_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+argus_status argus_paged_decode_attn_noalloc(const argus_decode_args* args, void* stream);
+
+/* ---------------------------------------------------------------------------
  * argus_select_pages -- the indexer: top-k page selection over a compressed
  * key slab ([PR499] "Why this works for sparse attention"; "Design": fixed-
  * width list of 2*top_k + 8 entries with a drop counter).

@@ -51,6 +51,7 @@ class DecodeArgs(ctypes.Structure):
 
 
 EXPORTS = ["argus_quantize_pages", "argus_decode_workspace_bytes", "argus_paged_decode_attn",
+           "argus_paged_decode_attn_noalloc",
            "argus_select_workspace_bytes", "argus_select_pages", "argus_fold_lse",
            "argus_window_prefill_attn", "argus_status_string", "argus_last_error"]
 
@@ -80,6 +81,8 @@ def lib():
     L.argus_decode_workspace_bytes.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.POINTER(sz)]
     L.argus_paged_decode_attn.restype = ctypes.c_int
     L.argus_paged_decode_attn.argtypes = [ctypes.POINTER(DecodeArgs), vp, sz, vp]
+    L.argus_paged_decode_attn_noalloc.restype = ctypes.c_int
+    L.argus_paged_decode_attn_noalloc.argtypes = [ctypes.POINTER(DecodeArgs), vp]
     L.argus_select_workspace_bytes.restype = ctypes.c_int
     L.argus_select_workspace_bytes.argtypes = [ctypes.POINTER(Geom), i32, i32, ctypes.POINTER(sz)]
     L.argus_select_pages.restype = ctypes.c_int
@@ -199,6 +202,15 @@ def paged_decode_attn(args, ws, ws_bytes=None, stream=None):
     if ws_bytes is None:
         ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(lib().argus_paged_decode_attn(ctypes.byref(args), _ptr(ws), int(ws_bytes), _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def paged_decode_attn_noalloc(args, stream=None):
+    """Decode with the library's fixed device scratch instead of a workspace
+    (for callers that cannot allocate; calls must not overlap on the GPU)."""
+    _check(lib().argus_paged_decode_attn_noalloc(ctypes.byref(args), _stream(stream)))
 
 
 def select_workspace_bytes(g, batch, max_pages):

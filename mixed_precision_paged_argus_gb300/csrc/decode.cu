@@ -30,6 +30,7 @@
 //    (atomic ticket on a caller-provided counter, reset afterwards).
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -946,3 +947,60 @@ extern "C" argus_status argus_paged_decode_attn(const argus_decode_args* a, void
   return run(a, pl, ws, stream);
 }
 
+// ---------------------------------------------------------------------------
+// Decode without a caller-provided workspace.
+//
+// Some callers cannot hand the library any device memory: runtimes whose
+// memory planner has already given out the device memory before decoding
+// starts, and host code that must not call cudaMalloc on the decode path
+// (cudaMalloc can synchronise the device, and a planner-owned heap has no
+// room to spare).  For them the split-combine scratch lives in a fixed
+// file-scope device array of ARGUS_NOALLOC_SCRATCH_BYTES bytes, which every
+// GPU that loads this library keeps until the process exits.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) uint8_t g_noalloc_scratch[ARGUS_NOALLOC_SCRATCH_BYTES];
+
+namespace argus {
+namespace decode {
+
+// Device address of g_noalloc_scratch, resolved once per device with that
+// device current (the host-side name is only a stand-in for the symbol).
+static argus_status noalloc_scratch(void** out) {
+  static void* addr[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    return fail(ARGUS_E_LAUNCH, "decode (no-alloc): no current device");
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr)
+      return fail(ARGUS_E_LAUNCH, "decode (no-alloc): cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
+    addr[dev] = ptr;
+  }
+  *out = addr[dev];
+  return ARGUS_OK;
+}
+
+}  // namespace decode
+}  // namespace argus
+
+extern "C" argus_status argus_paged_decode_attn_noalloc(const argus_decode_args* a, void* stream) {
+  Plan pl;
+  argus_status st = plan(a, &pl);
+  if (st != ARGUS_OK) return st;
+  if (a->batch == 0) return ARGUS_OK;
+  if ((st = check_io(a)) != ARGUS_OK) return st;
+  if (pl.ws_bytes > (size_t)ARGUS_NOALLOC_SCRATCH_BYTES)
+    return fail(ARGUS_E_WORKSPACE,
+                "decode (no-alloc): these arguments need %zu bytes of scratch, more than the fixed %zu; "
+                "lower num_splits or use argus_paged_decode_attn with a workspace",
+                pl.ws_bytes, (size_t)ARGUS_NOALLOC_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != ARGUS_OK) return st;
+  // the array keeps whatever the previous call left: clear the split counters
+  cudaError_t e = cudaMemsetAsync(scratch, 0, pl.counter_bytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "decode (no-alloc): clearing counters: %s", cudaGetErrorString(e));
+  return run(a, pl, scratch, stream);
+}
