@@ -350,7 +350,8 @@ def main():
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "batch": 1, "layers": LAYERS, "context": CTX, "page_tokens": P,
                    "l2": "flushed (2x L2 write) before every timed step, outside the timed region",
-                   "replay": "24 decode launches as one CUDA graph",
+                   "replay": "24 x (decode + split-combine) launches as one CUDA graph, chained by "
+                             "programmatic dependent launch",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "kv_bytes_per_layer": bytes_layer,
         "kv_gbs": achieved,
@@ -363,7 +364,7 @@ def main():
                 "d2h_bytes_per_step": d2h,
                 "how": "per step: pinned q for 24 layers copied H2D, 24 argus_paged_decode_attn calls through "
                        "the ctypes binding, outputs copied D2H; CUDA events on the stream"},
-        "gpu_launches": LAYERS * args.steps,
+        "gpu_launches": 2 * LAYERS * args.steps,
         "clocks": clocks,
         "wall_s_timed": t_wall,
     }

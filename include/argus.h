@@ -162,10 +162,10 @@ typedef struct {
   int32_t num_splits;         /* context splits per (b, KV head); 0 = automatic */
 } argus_decode_args;
 
-/* Workspace needed by argus_paged_decode_attn for these arguments.  The
- * workspace starts with a block of split counters: those bytes must be zero
- * the first time a workspace is used (allocate it zero-filled); every call
- * leaves them zero again. */
+/* Workspace needed by argus_paged_decode_attn for these arguments: fp32
+ * partial outputs and log2-sum-exp values of the context splits.  Its contents
+ * need no initialisation; calls that share a workspace must not overlap on the
+ * GPU. */
 argus_status argus_decode_workspace_bytes(const argus_decode_args* args, size_t* bytes);
 
 argus_status argus_paged_decode_attn(const argus_decode_args* args, void* ws,
@@ -188,8 +188,8 @@ argus_status argus_paged_decode_attn(const argus_decode_args* args, void* ws,
  * cudaMalloc, no cudaFree, no allocating library routine.
  *   - The first call on a device resolves the array's device address (with
  *     that device current); make that first call before any stream capture.
- *   - Every call clears the array's counter block on `stream` before its
- *     kernel, since the array keeps the previous call's contents.
+ *   - The array keeps the previous call's contents; nothing in it needs to
+ *     start at zero (every partial result is written before it is read).
  *   - All calls share the one array: calls that overlap on the GPU (different
  *     streams, or different host threads on the same device) race.  Serialise
  *     them on one stream.

@@ -26,8 +26,8 @@
 //  * Online softmax in the log2 domain; P is transposed in registers
 //    (movmatrix) into the B fragment of the P.V MMA, whose A operand is V^T
 //    assembled from pairs of token rows with byte permutes.
-//  * Warps merge in shared memory; splits merge in the last CTA to finish
-//    (atomic ticket on a caller-provided counter, reset afterwards).
+//  * Warps merge in shared memory; context splits are folded by a second,
+//    fully parallel kernel chained with programmatic dependent launch.
 #include <algorithm>
 #include <cmath>
 #include <mutex>
@@ -39,10 +39,12 @@ namespace decode {
 
 constexpr int kChunk = 16;
 constexpr int kConsumerWarps = 4;
-constexpr int kChunksPerStage = kConsumerWarps;
+constexpr int kNC = 2;  // chunks a consumer warp processes together per stage
+constexpr int kChunksPerStage = kConsumerWarps * kNC;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kMaxG = 8;
-constexpr int kMaxSplits = 512;  // bounds the fold's shared-memory weights
+constexpr int kMaxSplits = 512;  // bounds the split combine's per-thread loads
+constexpr int kFoldThreads = 256;
 
 enum Family { kFamF16 = 0, kFamBF16 = 1, kFamMixed = 2 };
 
@@ -66,7 +68,6 @@ struct Params {
   uint32_t* status;
   int cps;         // chunks per split, a multiple of kChunksPerStage
   int num_splits;  // grid.x
-  uint32_t* counters;
   float* part_o;   // [B][Hkv][num_splits][G][D]
   float* part_lse; // [B][Hkv][num_splits][G]
 };
@@ -89,13 +90,13 @@ struct Layout {
   static constexpr int kOffMV = 2 * kKV + kMeta;
   static constexpr int kChunkBytes = 2 * kKV + 2 * kMeta;
   static constexpr int kStageBytes = kChunksPerStage * kChunkBytes;
-  static constexpr int kStages = (D == 128) ? 3 : 4;
+  static constexpr int kStages = 3;
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kBarOff = kRingBytes;
   static constexpr int kDescOff = kBarOff + 2 * kStages * 8;
   static constexpr int kMiscOff = kDescOff + kStages * kChunksPerStage * (int)sizeof(ChunkDesc);
   static constexpr int kSmemBytes = kMiscOff + 64;
-  static constexpr int kMinBlocks = (D == 128) ? 2 : 3;
+  static constexpr int kMinBlocks = (D == 128) ? 1 : 2;  // by shared memory
 };
 
 __device__ __forceinline__ void consumer_bar() {
@@ -280,6 +281,114 @@ __device__ __forceinline__ void load_v_frags(int codec, const uint8_t* chunk, in
   }
 }
 
+// Scores of NCG chunks of one codec: every fragment load and MMA of the
+// group is issued before any result is consumed (the m16n8k16 MMA latency is
+// long), with two accumulator chains per chunk.  sv is masked and scaled to
+// the log2 domain; kscale and the query exponent are applied here.
+template <int D, int CODEC, int NCG, bool BF>
+__device__ __forceinline__ void group_scores(const uint8_t* const* cptr, const ChunkDesc* dsc, int r, int t,
+                                             const uint32_t (&qf)[D / 16][2], const uint32_t (&qb)[D / 16][2],
+                                             const float (&qgs)[D / 32][2], float f0h, float f1h,
+                                             float scale_log2, float (&sv)[kNC][4], int c0) {
+  constexpr int KC = D / 16;
+  uint32_t a[NCG][KC][4];
+  float kz[NCG][2][D / 32][2];
+#pragma unroll
+  for (int c = 0; c < NCG; ++c) load_k_frags<D>(CODEC, cptr[c], r, t, a[c], kz[c]);
+  if constexpr (CODEC == ARGUS_INT4_G32) {
+    float sg[NCG][D / 32][4];
+#pragma unroll
+    for (int c = 0; c < NCG; ++c)
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) sg[c][i][0] = sg[c][i][1] = sg[c][i][2] = sg[c][i][3] = 0.f;
+#pragma unroll
+    for (int k = 0; k < KC; ++k)
+#pragma unroll
+      for (int c = 0; c < NCG; ++c) mma_f16(sg[c][k / 2], a[c][k][0], a[c][k][1], a[c][k][2], a[c][k][3], qf[k][0], qf[k][1]);
+#pragma unroll
+    for (int c = 0; c < NCG; ++c) {
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) {
+        sc[0] += kz[c][0][i][0] * sg[c][i][0] + kz[c][0][i][1] * qgs[i][0];
+        sc[1] += kz[c][0][i][0] * sg[c][i][1] + kz[c][0][i][1] * qgs[i][1];
+        sc[2] += kz[c][1][i][0] * sg[c][i][2] + kz[c][1][i][1] * qgs[i][0];
+        sc[3] += kz[c][1][i][0] * sg[c][i][3] + kz[c][1][i][1] * qgs[i][1];
+      }
+      const float f0 = scale_log2 * f0h, f1 = scale_log2 * f1h;
+      const int nv = dsc[c].n_valid;
+      sv[c0 + c][0] = (r < nv) ? sc[0] * f0 : -INFINITY;
+      sv[c0 + c][1] = (r < nv) ? sc[1] * f1 : -INFINITY;
+      sv[c0 + c][2] = (r + 8 < nv) ? sc[2] * f0 : -INFINITY;
+      sv[c0 + c][3] = (r + 8 < nv) ? sc[3] * f1 : -INFINITY;
+    }
+  } else {
+    float sc[NCG][2][4];
+#pragma unroll
+    for (int c = 0; c < NCG; ++c)
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) sc[c][h2][0] = sc[c][h2][1] = sc[c][h2][2] = sc[c][h2][3] = 0.f;
+#pragma unroll
+    for (int k = 0; k < KC; ++k)
+#pragma unroll
+      for (int c = 0; c < NCG; ++c) {
+        if constexpr (BF) mma_bf16(sc[c][k & 1], a[c][k][0], a[c][k][1], a[c][k][2], a[c][k][3], qb[k][0], qb[k][1]);
+        else mma_f16(sc[c][k & 1], a[c][k][0], a[c][k][1], a[c][k][2], a[c][k][3], qf[k][0], qf[k][1]);
+      }
+#pragma unroll
+    for (int c = 0; c < NCG; ++c) {
+      const float fk = scale_log2 * dsc[c].kscale;
+      const float f0 = fk * f0h, f1 = fk * f1h;
+      const int nv = dsc[c].n_valid;
+      sv[c0 + c][0] = (r < nv) ? (sc[c][0][0] + sc[c][1][0]) * f0 : -INFINITY;
+      sv[c0 + c][1] = (r < nv) ? (sc[c][0][1] + sc[c][1][1]) * f1 : -INFINITY;
+      sv[c0 + c][2] = (r + 8 < nv) ? (sc[c][0][2] + sc[c][1][2]) * f0 : -INFINITY;
+      sv[c0 + c][3] = (r + 8 < nv) ? (sc[c][0][3] + sc[c][1][3]) * f1 : -INFINITY;
+    }
+  }
+}
+
+// O^T += V^T . (w P)^T for NCG chunks of one codec; all V fragments and P
+// transposes are formed before the MMAs.  pw[c] = {p0, p1, p2, p3} already
+// multiplied by the chunk's V-scale weight; chunks with skip[c] contribute nothing.
+template <int D, int CODEC, int NCG, bool BF>
+__device__ __forceinline__ void group_pv(const uint8_t* const* cptr, int r, int t, const float (*pw)[4],
+                                         const bool* skip, float (&acc)[D / 16][4]) {
+  constexpr int MB = D / 16;
+  uint32_t vf[NCG][MB][4];
+  uint32_t bh[NCG][2], bl[NCG][2];
+#pragma unroll
+  for (int c = 0; c < NCG; ++c) {
+    load_v_frags<D>(CODEC, cptr[c], r, t, vf[c]);
+    if constexpr (BF) {
+      const float* q = pw[c];
+      const uint32_t h01 = pack_bf16x2(q[0], q[1]), h23 = pack_bf16x2(q[2], q[3]);
+      const uint32_t l01 = pack_bf16x2(q[0] - __uint_as_float(h01 << 16), q[1] - __uint_as_float(h01 & 0xFFFF0000u));
+      const uint32_t l23 = pack_bf16x2(q[2] - __uint_as_float(h23 << 16), q[3] - __uint_as_float(h23 & 0xFFFF0000u));
+      bh[c][0] = movmatrix_trans(h01);
+      bh[c][1] = movmatrix_trans(h23);
+      bl[c][0] = movmatrix_trans(l01);
+      bl[c][1] = movmatrix_trans(l23);
+    } else {
+      bh[c][0] = movmatrix_trans(pack_f16x2(pw[c][0], pw[c][1]));
+      bh[c][1] = movmatrix_trans(pack_f16x2(pw[c][2], pw[c][3]));
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < NCG; ++c) {
+    if (skip[c]) continue;
+#pragma unroll
+    for (int j = 0; j < MB; ++j) {
+      if constexpr (BF) {
+        mma_bf16(acc[j], vf[c][j][0], vf[c][j][1], vf[c][j][2], vf[c][j][3], bh[c][0], bh[c][1]);
+        mma_bf16(acc[j], vf[c][j][0], vf[c][j][1], vf[c][j][2], vf[c][j][3], bl[c][0], bl[c][1]);
+      } else {
+        mma_f16(acc[j], vf[c][j][0], vf[c][j][1], vf[c][j][2], vf[c][j][3], bh[c][0], bh[c][1]);
+      }
+    }
+  }
+}
+
 template <int D, bool QBF16, int FAM>
 __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
     decode_kernel(const Params p) {
@@ -412,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
         }
       }
       const uint32_t my_bytes = 2 * (kv_bytes + m_bytes);
-      const int n_batch_stages = min(8, (n_local - base + kChunksPerStage - 1) / kChunksPerStage);
+      const int n_batch_stages = min(32 / kChunksPerStage, (n_local - base + kChunksPerStage - 1) / kChunksPerStage);
       for (int st = 0; st < n_batch_stages; ++st) {
         const int s = base / kChunksPerStage + st;
         const int slot = s % L::kStages;
@@ -426,15 +535,15 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
             break;
           }
         }
-        const bool mine = (lane >> 2) == st;  // lanes 4st .. 4st+3 own this stage
+        const bool mine = (lane / kChunksPerStage) == st;  // these lanes own this stage's chunks
         uint32_t total = mine ? my_bytes : 0u;
-        total += __shfl_xor_sync(0xffffffffu, total, 1);
-        total += __shfl_xor_sync(0xffffffffu, total, 2);
-        total = __shfl_sync(0xffffffffu, total, 4 * st);
+#pragma unroll
+        for (int o = 1; o < kChunksPerStage; o <<= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+        total = __shfl_sync(0xffffffffu, total, kChunksPerStage * st);
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], total);
         __syncwarp();
         if (mine) {
-          const int j = lane & 3;
+          const int j = lane % kChunksPerStage;
           if (kv_bytes) {
             uint8_t* dst = smem + slot * L::kStageBytes + j * L::kChunkBytes;
             bulk_g2s(dst + L::kOffK, srcK, kv_bytes, &full[slot]);
@@ -527,7 +636,9 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
   float acc[MB][4];
 #pragma unroll
   for (int j = 0; j < MB; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, sigma = 1.f;
+  // running max (log2 domain) and lane-partial sums of heads 2t, 2t+1; the
+  // accumulator is kept in units of sigma (the largest V scale seen so far)
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, sigma = 0.f;
   bool alive = true;
 
   for (int s = 0; s < n_stages; ++s) {
@@ -537,65 +648,80 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
       if (lane == 0 && p.status) atomicOr(p.status, kStatusTimeoutBit);
     }
     if (alive && misc[0]) alive = false;
-    const ChunkDesc d = descs[slot * kChunksPerStage + warp];
-    if (alive && d.codec >= 0) {
-      const uint8_t* chunk = smem + slot * L::kStageBytes + warp * L::kChunkBytes;
-      const bool bf = (d.codec == ARGUS_BF16);
-      // ---- scores S^T[token][head] = K . q
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
-      {
-        uint32_t a[KC][4];
-        float kz[2][D / 32][2];
-        load_k_frags<D>(d.codec, chunk, r, t, a, kz);
-        if (FAM == kFamBF16 || (FAM == kFamMixed && bf)) {
+    ChunkDesc dsc[kNC];
+    const uint8_t* cptr[kNC];
+    bool any = false;
 #pragma unroll
-          for (int c = 0; c < KC; ++c) mma_bf16(sc, a[c][0], a[c][1], a[c][2], a[c][3], qb[c][0], qb[c][1]);
-        } else if (FAM != kFamBF16 && d.codec == ARGUS_INT4_G32) {
-          float sg[D / 32][4];
-#pragma unroll
-          for (int i = 0; i < D / 32; ++i) sg[i][0] = sg[i][1] = sg[i][2] = sg[i][3] = 0.f;
-#pragma unroll
-          for (int c = 0; c < KC; ++c) mma_f16(sg[c / 2], a[c][0], a[c][1], a[c][2], a[c][3], qf[c][0], qf[c][1]);
-#pragma unroll
-          for (int i = 0; i < D / 32; ++i) {
-            sc[0] += kz[0][i][0] * sg[i][0] + kz[0][i][1] * qgs[i][0];
-            sc[1] += kz[0][i][0] * sg[i][1] + kz[0][i][1] * qgs[i][1];
-            sc[2] += kz[1][i][0] * sg[i][2] + kz[1][i][1] * qgs[i][0];
-            sc[3] += kz[1][i][0] * sg[i][3] + kz[1][i][1] * qgs[i][1];
+    for (int c = 0; c < kNC; ++c) {
+      dsc[c] = descs[slot * kChunksPerStage + warp * kNC + c];
+      cptr[c] = smem + slot * L::kStageBytes + (warp * kNC + c) * L::kChunkBytes;
+      any |= dsc[c].codec >= 0;
+    }
+    if (alive && any) {
+      // ---- scores S^T[token][head] = K . q; a group whose chunks share one
+      // codec runs as straight-line code so that all MMAs overlap
+      float sv[kNC][4];
+      const bool same = (dsc[0].codec >= 0) && (dsc[1].codec == dsc[0].codec);
+      const float fq0 = qscale_h0, fq1 = qscale_h1;
+      auto scores = [&](int codec, int c0, int ncg) {
+        const uint8_t* const* cp = cptr + c0;
+        const ChunkDesc* dd = dsc + c0;
+        if (ncg == 2) {
+          switch (codec) {
+            case ARGUS_FP16: group_scores<D, ARGUS_FP16, 2, false>(cp, dd, r, t, qf, qb, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+            case ARGUS_BF16: group_scores<D, ARGUS_BF16, 2, true>(cp, dd, r, t, qf, qb, qgs, 1.f, 1.f, p.scale_log2, sv, c0); break;
+            case ARGUS_FP8_E4M3: group_scores<D, ARGUS_FP8_E4M3, 2, false>(cp, dd, r, t, qf, qb, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+            case ARGUS_INT8: group_scores<D, ARGUS_INT8, 2, false>(cp, dd, r, t, qf, qb, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+            default: group_scores<D, ARGUS_INT4_G32, 2, false>(cp, dd, r, t, qf, qb, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
           }
         } else {
+          switch (codec) {
+            case ARGUS_FP16: group_scores<D, ARGUS_FP16, 1, false>(cp, dd, r, t, qf, qb, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+            case ARGUS_BF16: group_scores<D, ARGUS_BF16, 1, true>(cp, dd, r, t, qf, qb, qgs, 1.f, 1.f, p.scale_log2, sv, c0); break;
+            case ARGUS_FP8_E4M3: group_scores<D, ARGUS_FP8_E4M3, 1, false>(cp, dd, r, t, qf, qb, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+            case ARGUS_INT8: group_scores<D, ARGUS_INT8, 1, false>(cp, dd, r, t, qf, qb, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+            default: group_scores<D, ARGUS_INT4_G32, 1, false>(cp, dd, r, t, qf, qb, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+          }
+        }
+      };
+      if (same) {
+        scores(dsc[0].codec, 0, 2);
+      } else {
 #pragma unroll
-          for (int c = 0; c < KC; ++c) mma_f16(sc, a[c][0], a[c][1], a[c][2], a[c][3], qf[c][0], qf[c][1]);
+        for (int c = 0; c < kNC; ++c) {
+          sv[c][0] = sv[c][1] = sv[c][2] = sv[c][3] = -INFINITY;
+          if (dsc[c].codec >= 0) scores(dsc[c].codec, c, 1);
         }
       }
-      const bool f16path = !(FAM == kFamBF16 || (FAM == kFamMixed && bf));
-      const float fk = p.scale_log2 * d.kscale;
-      const float f0 = fk * (f16path ? qscale_h0 : 1.f);
-      const float f1 = fk * (f16path ? qscale_h1 : 1.f);
-      float s0 = sc[0] * f0, s1 = sc[1] * f1, s2 = sc[2] * f0, s3 = sc[3] * f1;
-      if (r >= d.n_valid) s0 = s1 = -INFINITY;
-      if (r + 8 >= d.n_valid) s2 = s3 = -INFINITY;
-      float t0 = fmaxf(s0, s2), t1 = fmaxf(s1, s3);
+      // ---- one online-softmax update for all chunks of the group
+      float t0 = -INFINITY, t1 = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kNC; ++c) {
+        t0 = fmaxf(t0, fmaxf(sv[c][0], sv[c][2]));
+        t1 = fmaxf(t1, fmaxf(sv[c][1], sv[c][3]));
+      }
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
         t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, o));
         t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, o));
       }
+      // the new maxima are finite: token 0 of a non-empty chunk is visible
       const float mn0 = fmaxf(m0, t0), mn1 = fmaxf(m1, t1);
-      // mn is finite: token 0 of a non-empty chunk is always visible
       const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
-      const float p0 = fast_exp2(s0 - mn0), p1 = fast_exp2(s1 - mn1);
-      const float p2 = fast_exp2(s2 - mn0), p3 = fast_exp2(s3 - mn1);
       m0 = mn0;
       m1 = mn1;
-      l0 = l0 * al0 + (p0 + p2);
-      l1 = l1 * al1 + (p1 + p3);
-      // V scale: the accumulator is kept in units of the current page's V scale
-      float vs = d.vscale;
-      if (!(vs > 0.f)) vs = sigma;  // all-zero unit: codes are 0, keep units
-      const float ratio = (vs == sigma) ? 1.f : sigma / vs;
-      sigma = vs;
-      const float g0 = al0 * ratio, g1 = al1 * ratio;
+      // V scales: codecs without one count as 1; sigma only grows, so every
+      // chunk's weight vs / sigma is <= 1 and P stays in [0, 1] before the MMA
+      float vmax = sigma;
+#pragma unroll
+      for (int c = 0; c < kNC; ++c)
+        if (dsc[c].codec >= 0 && dsc[c].vscale > 0.f) vmax = fmaxf(vmax, dsc[c].vscale);
+      float gs = 1.f;
+      if (vmax > sigma) {
+        gs = (sigma > 0.f) ? sigma / vmax : 0.f;
+        sigma = vmax;
+      }
+      const float g0 = al0 * gs, g1 = al1 * gs;
 #pragma unroll
       for (int j = 0; j < MB; ++j) {
         acc[j][0] *= g0;
@@ -603,41 +729,69 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
         acc[j][2] *= g0;
         acc[j][3] *= g1;
       }
-      // ---- O^T[dim][head] += V^T . P^T
-      uint32_t vf[MB][4];
-      load_v_frags<D>(d.codec, chunk, r, t, vf);
-      if (f16path) {
-        const uint32_t b0 = movmatrix_trans(pack_f16x2(p0, p1));
-        const uint32_t b1 = movmatrix_trans(pack_f16x2(p2, p3));
+      float pw[kNC][4];
+      bool skip[kNC];
+      l0 *= al0;
+      l1 *= al1;
 #pragma unroll
-        for (int j = 0; j < MB; ++j) mma_f16(acc[j], vf[j][0], vf[j][1], vf[j][2], vf[j][3], b0, b1);
-      } else {
-        const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
-        const uint32_t l01 = pack_bf16x2(p0 - __uint_as_float(h01 << 16), p1 - __uint_as_float(h01 & 0xFFFF0000u));
-        const uint32_t l23 = pack_bf16x2(p2 - __uint_as_float(h23 << 16), p3 - __uint_as_float(h23 & 0xFFFF0000u));
-        const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-        const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
-#pragma unroll
-        for (int j = 0; j < MB; ++j) {
-          mma_bf16(acc[j], vf[j][0], vf[j][1], vf[j][2], vf[j][3], bh0, bh1);
-          mma_bf16(acc[j], vf[j][0], vf[j][1], vf[j][2], vf[j][3], bl0, bl1);
+      for (int c = 0; c < kNC; ++c) {
+        const float p0 = fast_exp2(sv[c][0] - mn0), p1 = fast_exp2(sv[c][1] - mn1);
+        const float p2 = fast_exp2(sv[c][2] - mn0), p3 = fast_exp2(sv[c][3] - mn1);
+        l0 += p0 + p2;
+        l1 += p1 + p3;
+        // all-zero V codes (scale 0) and empty slots contribute nothing
+        skip[c] = !(dsc[c].codec >= 0 && dsc[c].vscale > 0.f);
+        const float w = skip[c] ? 0.f : dsc[c].vscale / sigma;
+        pw[c][0] = p0 * w;
+        pw[c][1] = p1 * w;
+        pw[c][2] = p2 * w;
+        pw[c][3] = p3 * w;
+      }
+      // ---- O^T[dim][head] += V^T . (w P)^T
+      auto pv = [&](int codec, int c0, int ncg) {
+        const uint8_t* const* cp = cptr + c0;
+        if (ncg == 2) {
+          switch (codec) {
+            case ARGUS_FP16: group_pv<D, ARGUS_FP16, 2, false>(cp, r, t, pw + c0, skip + c0, acc); break;
+            case ARGUS_BF16: group_pv<D, ARGUS_BF16, 2, true>(cp, r, t, pw + c0, skip + c0, acc); break;
+            case ARGUS_FP8_E4M3: group_pv<D, ARGUS_FP8_E4M3, 2, false>(cp, r, t, pw + c0, skip + c0, acc); break;
+            case ARGUS_INT8: group_pv<D, ARGUS_INT8, 2, false>(cp, r, t, pw + c0, skip + c0, acc); break;
+            default: group_pv<D, ARGUS_INT4_G32, 2, false>(cp, r, t, pw + c0, skip + c0, acc); break;
+          }
+        } else {
+          switch (codec) {
+            case ARGUS_FP16: group_pv<D, ARGUS_FP16, 1, false>(cp, r, t, pw + c0, skip + c0, acc); break;
+            case ARGUS_BF16: group_pv<D, ARGUS_BF16, 1, true>(cp, r, t, pw + c0, skip + c0, acc); break;
+            case ARGUS_FP8_E4M3: group_pv<D, ARGUS_FP8_E4M3, 1, false>(cp, r, t, pw + c0, skip + c0, acc); break;
+            case ARGUS_INT8: group_pv<D, ARGUS_INT8, 1, false>(cp, r, t, pw + c0, skip + c0, acc); break;
+            default: group_pv<D, ARGUS_INT4_G32, 1, false>(cp, r, t, pw + c0, skip + c0, acc); break;
+          }
         }
+      };
+      if (same) {
+        pv(dsc[0].codec, 0, 2);
+      } else {
+#pragma unroll
+        for (int c = 0; c < kNC; ++c)
+          if (!skip[c]) pv(dsc[c].codec, c, 1);
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
   }
 
-  // ------------------------------------------------- merge the four warps
+  // ------------------------------------------------- merge the consumer warps
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, o);
     l1 += __shfl_xor_sync(0xffffffffu, l1, o);
   }
+  if (sigma == 0.f) sigma = 1.f;  // nothing accumulated
   consumer_bar();  // every warp is done with the stage ring; reuse it
-  float* red_o = reinterpret_cast<float*>(smem);               // [4][8][D]
-  float* red_ml = red_o + kConsumerWarps * kMaxG * D;          // [4][8][2]
-  float* wts = red_ml + kConsumerWarps * kMaxG * 2;            // fold weights
+  float* red_o = reinterpret_cast<float*>(smem);               // [warps][8][D]
+  float* red_ml = red_o + kConsumerWarps * kMaxG * D;          // [warps][8][2]
+  float* red_w = red_ml + kConsumerWarps * kMaxG * 2;          // [warps][8] merge weights
+  float* red_lse = red_w + kConsumerWarps * kMaxG;             // [8]
 #pragma unroll
   for (int j = 0; j < MB; ++j) {
     const int d0 = DL * r + 2 * j, d1 = d0 + 1;
@@ -653,29 +807,36 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
     red_ml[(warp * kMaxG + 2 * t + 1) * 2 + 1] = l1;
   }
   consumer_bar();
-  const int tid = threadIdx.x;  // 0 .. 127
+  const int tid = threadIdx.x;
   const int nthr = kConsumerWarps * 32;
+  if (tid < G) {  // per head: weight of each warp's partial, and the CTA's lse
+    const int g = tid;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_ml[(w * kMaxG + g) * 2]);
+    float Lsum = 0.f;
+    float f[kConsumerWarps];
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      f[w] = (M == -INFINITY) ? 0.f : fast_exp2(red_ml[(w * kMaxG + g) * 2] - M);
+      Lsum += red_ml[(w * kMaxG + g) * 2 + 1] * f[w];
+    }
+    const float inv = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) red_w[w * kMaxG + g] = f[w] * inv;
+    red_lse[g] = (Lsum > 0.f) ? M + log2f(Lsum) : -INFINITY;
+  }
+  consumer_bar();
   const bool direct = (n_active == 1);
   const size_t bh = (size_t)b * Hkv + h;
   float* po_bh = p.part_o + bh * p.num_splits * G * D;
   float* pl_bh = p.part_lse + bh * p.num_splits * G;
   for (int idx = tid; idx < G * D; idx += nthr) {
     const int g = idx / D, dd = idx - g * D;
-    float M = -INFINITY;
+    float o = 0.f;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_ml[(w * kMaxG + g) * 2]);
-    float o = 0.f, lse2 = -INFINITY;
-    if (M != -INFINITY) {
-      float Lsum = 0.f, osum = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float f = fast_exp2(red_ml[(w * kMaxG + g) * 2] - M);
-        Lsum += red_ml[(w * kMaxG + g) * 2 + 1] * f;
-        osum += red_o[(w * kMaxG + g) * D + dd] * f;
-      }
-      o = osum / Lsum;
-      lse2 = M + log2f(Lsum);
-    }
+    for (int w = 0; w < kConsumerWarps; ++w) o += red_w[w * kMaxG + g] * red_o[(w * kMaxG + g) * D + dd];
+    const float lse2 = red_lse[g];
     if (direct) {
       const size_t oi = (row0 + g) * D + dd;
       if (p.out) {
@@ -689,64 +850,112 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
       if (dd == 0) pl_bh[(size_t)split * G + g] = lse2;
     }
   }
-  if (direct) return;
+}
 
-  // ------------------------------------------- last CTA folds the splits
-  __threadfence();
-  consumer_bar();
-  if (tid == 0) misc[1] = (int)atomicAdd(p.counters + bh, 1u);
-  consumer_bar();
-  if (misc[1] != n_active - 1) return;
-  __threadfence();
-  float* wl = wts;                                  // [n_active][G] partial lse
-  float* ww = wts + n_active * G;                   // [n_active][G] fold weights
-  float* wlse = ww + n_active * G;                  // [G] folded lse
-  for (int i = tid; i < n_active * G; i += nthr) wl[i] = __ldcg(pl_bh + i);
-  consumer_bar();
-  const int cw = tid >> 5, cl = tid & 31;
-  for (int g = cw; g < G; g += kConsumerWarps) {
-    float M = -INFINITY;
-    for (int s2 = cl; s2 < n_active; s2 += 32) M = fmaxf(M, wl[s2 * G + g]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float Lsum = 0.f;
-    if (M != -INFINITY)
-      for (int s2 = cl; s2 < n_active; s2 += 32) Lsum += fast_exp2(wl[s2 * G + g] - M);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
-    const float lse = (M == -INFINITY) ? -INFINITY : M + log2f(Lsum);
-    for (int s2 = cl; s2 < n_active; s2 += 32)
-      ww[s2 * G + g] = (lse == -INFINITY) ? 0.f : fast_exp2(wl[s2 * G + g] - lse);
-    if (cl == 0) wlse[g] = lse;
-  }
-  consumer_bar();
+// Split combine: one CTA per (batch row, query head).  Launched after the
+// decode grid with programmatic dependent launch, it waits for the partials,
+// then every thread loads its share of (split, 16-byte column) partials at once
+// and the CTA folds them by log2-sum-exp.  Rows with at most one active split
+// were written by the decode kernel itself.
+template <int D>
+__global__ void __launch_bounds__(kFoldThreads) decode_fold_kernel(const Params p) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int D4 = D / 4;
-  for (int idx = tid; idx < G * D4; idx += nthr) {
-    const int g = idx / D4, d4 = idx - g * D4;
-    float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4* src = reinterpret_cast<const float4*>(po_bh + (size_t)g * D) + d4;
-#pragma unroll 8
-    for (int s2 = 0; s2 < n_active; ++s2) {
-      const float w = ww[s2 * G + g];
-      const float4 x = __ldcg(src + (size_t)s2 * G * D4);
-      acc4.x += w * x.x;
-      acc4.y += w * x.y;
-      acc4.z += w * x.z;
-      acc4.w += w * x.w;
+  constexpr int GROUPS = kFoldThreads / D4;     // split groups per column
+  __shared__ float4 sh_acc[GROUPS][D4];
+  const int hq = blockIdx.x, b = blockIdx.y;
+  const int G = p.G, Hkv = p.Hkv;
+  const int h = hq / G, g = hq - h * G;
+  const int cpp = p.P / kChunk;
+  int seq_len = p.seq_lens[b];
+  seq_len = max(0, min(seq_len, p.max_pages * p.P));
+  int n_chunks;
+  if (!p.sel_pages) n_chunks = (seq_len + kChunk - 1) / kChunk;
+  else n_chunks = max(0, min(p.sel_count[b * Hkv + h], p.sel_width)) * cpp;
+  const int n_active = (n_chunks + p.cps - 1) / p.cps;
+  if (n_active <= 1) return;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const size_t bh = (size_t)b * Hkv + h;
+  const float* po = p.part_o + bh * p.num_splits * G * D + (size_t)g * D;
+  const float* pl = p.part_lse + bh * p.num_splits * G + g;
+  const int tid = threadIdx.x;
+  const int col = tid % D4, grp = tid / D4;
+  // each thread folds splits grp, grp + GROUPS, ... of one 16-byte column,
+  // kKPT of them per batch with every load of the batch issued first, keeping
+  // its own running (max, sum, vector) in the log2 domain
+  constexpr int kKPT = 8;
+  float m = -INFINITY, l = 0.f;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int base = 0; base < n_active; base += kKPT * GROUPS) {
+    float4 x[kKPT];
+    float ls[kKPT];
+#pragma unroll
+    for (int k = 0; k < kKPT; ++k) {
+      const int s2 = base + grp + k * GROUPS;
+      if (s2 < n_active) {
+        x[k] = __ldcg(reinterpret_cast<const float4*>(po + (size_t)s2 * G * D) + col);
+        ls[k] = __ldcg(pl + (size_t)s2 * G);
+      } else {
+        x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        ls[k] = -INFINITY;
+      }
     }
-    const float ov[4] = {acc4.x, acc4.y, acc4.z, acc4.w};
+    float bm = m;
+#pragma unroll
+    for (int k = 0; k < kKPT; ++k) bm = fmaxf(bm, ls[k]);
+    if (bm == -INFINITY) continue;
+    const float r0 = fast_exp2(m - bm);
+    a.x *= r0; a.y *= r0; a.z *= r0; a.w *= r0;
+    l *= r0;
+#pragma unroll
+    for (int k = 0; k < kKPT; ++k) {
+      const float w = fast_exp2(ls[k] - bm);
+      a.x += w * x[k].x;
+      a.y += w * x[k].y;
+      a.z += w * x[k].z;
+      a.w += w * x[k].w;
+      l += w;
+    }
+    m = bm;
+  }
+  // combine the GROUPS partial folds of each column
+  __shared__ float sh_m[GROUPS][D4];
+  __shared__ float sh_l[GROUPS][D4];
+  sh_m[grp][col] = m;
+  sh_l[grp][col] = l;
+  sh_acc[grp][col] = a;
+  __syncthreads();
+  if (grp == 0) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < GROUPS; ++q) M = fmaxf(M, sh_m[q][col]);
+    float L = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int q = 0; q < GROUPS; ++q) {
+        const float w = fast_exp2(sh_m[q][col] - M);
+        L += w * sh_l[q][col];
+        o.x += w * sh_acc[q][col].x;
+        o.y += w * sh_acc[q][col].y;
+        o.z += w * sh_acc[q][col].z;
+        o.w += w * sh_acc[q][col].w;
+      }
+    }
+    const float inv = (L > 0.f) ? 1.f / L : 0.f;
+    const float ov[4] = {o.x * inv, o.y * inv, o.z * inv, o.w * inv};
+    const size_t row = (size_t)b * Hkv * G + hq;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const size_t oi = (row0 + g) * D + 4 * d4 + e;
+      const size_t oi = row * D + 4 * col + e;
       if (p.out) {
         if (p.out_bf16) reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(ov[e]);
         else reinterpret_cast<__half*>(p.out)[oi] = __float2half_rn(ov[e]);
       }
       if (p.out_f32) p.out_f32[oi] = ov[e];
     }
-    if (p.lse2_out && d4 == 0) p.lse2_out[row0 + g] = wlse[g];
+    if (p.lse2_out && col == 0) p.lse2_out[row] = (L > 0.f) ? M + log2f(L) : -INFINITY;
   }
-  if (tid == 0) p.counters[(size_t)b * Hkv + h] = 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -755,7 +964,7 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
 struct Plan {
   int D, G, cps, num_splits, fam;
   bool q_bf16;
-  size_t counter_bytes, part_o_bytes, ws_bytes;
+  size_t part_o_bytes, ws_bytes;
 };
 
 static argus_status plan(const argus_decode_args* a, Plan* pl) {
@@ -818,16 +1027,15 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
   } else {
     const long long total = (long long)std::max(a->batch, 1) * g.n_kv_heads * max_chunks;
     const long long target = 8LL * device_sm_count();
-    cps = std::max<long long>(16, (total + target - 1) / target);
+    cps = std::max<long long>(kChunksPerStage, (total + target - 1) / target);
   }
   cps = std::max<long long>(cps, (max_chunks + kMaxSplits - 1) / kMaxSplits);
   cps = std::max<long long>(kChunksPerStage, (cps + kChunksPerStage - 1) / kChunksPerStage * kChunksPerStage);
   pl->cps = (int)cps;
   pl->num_splits = (int)std::max<long long>(1, (max_chunks + cps - 1) / cps);
   if (pl->num_splits > 65535) return fail(ARGUS_E_UNSUPPORTED, "decode: too many splits");
-  pl->counter_bytes = ((size_t)std::max(a->batch, 1) * g.n_kv_heads * 4 + 255) / 256 * 256;
   pl->part_o_bytes = (size_t)std::max(a->batch, 1) * g.n_kv_heads * pl->num_splits * G * g.head_dim * 4;
-  pl->ws_bytes = pl->counter_bytes + pl->part_o_bytes +
+  pl->ws_bytes = pl->part_o_bytes +
                  (size_t)std::max(a->batch, 1) * g.n_kv_heads * pl->num_splits * G * 4;
   return ARGUS_OK;
 }
@@ -856,6 +1064,14 @@ static argus_status launch_t(const Params& p, dim3 grid, cudaStream_t s) {
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<D, QBF16, FAM>, p);
   if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "argus_paged_decode_attn: %s", cudaGetErrorString(e));
+  if (p.num_splits > 1) {
+    cudaLaunchConfig_t fc = cfg;
+    fc.gridDim = dim3(p.Hkv * p.G, p.B);
+    fc.blockDim = dim3(kFoldThreads);
+    fc.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelEx(&fc, decode_fold_kernel<D>, p);
+    if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "argus_paged_decode_attn (combine): %s", cudaGetErrorString(e));
+  }
   return launch_status("argus_paged_decode_attn");
 }
 
@@ -890,8 +1106,7 @@ static argus_status check_io(const argus_decode_args* a) {
   return ARGUS_OK;
 }
 
-// Fill the kernel parameters and launch; ws holds pl.ws_bytes bytes whose
-// counter block is zero.
+// Fill the kernel parameters and launch; ws holds pl.ws_bytes bytes.
 static argus_status run(const argus_decode_args* a, const Plan& pl, void* ws, void* stream) {
   Params p{};
   p.B = a->batch;
@@ -925,10 +1140,8 @@ static argus_status run(const argus_decode_args* a, const Plan& pl, void* ws, vo
   p.status = a->status;
   p.cps = pl.cps;
   p.num_splits = pl.num_splits;
-  p.counters = static_cast<uint32_t*>(ws);
-  p.part_o = ws ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.counter_bytes) : nullptr;
-  p.part_lse = ws ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.counter_bytes + pl.part_o_bytes)
-                  : nullptr;
+  p.part_o = static_cast<float*>(ws);
+  p.part_lse = ws ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.part_o_bytes) : nullptr;
   dim3 grid(pl.num_splits, a->g.n_kv_heads, a->batch);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (pl.D == 64) return launch_d<64>(p, pl, grid, s);
@@ -999,8 +1212,7 @@ extern "C" argus_status argus_paged_decode_attn_noalloc(const argus_decode_args*
                 pl.ws_bytes, (size_t)ARGUS_NOALLOC_SCRATCH_BYTES);
   void* scratch = nullptr;
   if ((st = noalloc_scratch(&scratch)) != ARGUS_OK) return st;
-  // the array keeps whatever the previous call left: clear the split counters
-  cudaError_t e = cudaMemsetAsync(scratch, 0, pl.counter_bytes, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "decode (no-alloc): clearing counters: %s", cudaGetErrorString(e));
+  // the array keeps whatever the previous call left; nothing in it has to
+  // start at zero (every partial is written before it is read)
   return run(a, pl, scratch, stream);
 }

@@ -147,14 +147,19 @@ def test_bad_slot_is_skipped_and_counted():
     assert int(status.item()) == 1
 
 
-def test_workspace_counters_left_zero_and_repeatable():
+def test_workspace_needs_no_initialisation_and_is_repeatable():
     Hq, Hkv, D, P = 14, 2, 64, 64
     pc = W.mixed_tier_codecs(16).reshape(1, 16)
     c = build_case(Hq, Hkv, D, P, [16 * 64], pc, W.FP16, seed=81)
-    out_a, o32a, _, ws = run_decode(c, num_splits=8)
-    assert not ws[:256].any()
-    out_b, o32b, _, _ = run_decode(c, num_splits=8)
-    assert torch.equal(o32a, o32b)
+    out_a, o32a, lse, _ = run_decode(c, num_splits=8)
+    _check(c, out_a, o32a, lse)
+    args = argus.decode_args(c.g, c.B, c.q, c.pools, c.d_codec, c.d_table, c.d_lens, c.max_pages, c.scale,
+                             out_f32=torch.empty_like(o32a), num_splits=8)
+    ws = torch.full((argus.decode_workspace_bytes(args),), 0xFF, dtype=torch.uint8, device=DEV)  # NaN-filled
+    for _ in range(2):
+        argus.paged_decode_attn(args, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(args._keep[9], o32a)
 
 
 def test_unsupported_and_invalid_arguments():
