@@ -2,20 +2,498 @@
 // cached keys, folded into an fp32 accumulator by log2-sum-exp.
 //
 // "feat(kvcache): host-RAM KV tier for sparse-attention models", comment on
-// "--kv-placement host": cached pages are staged into a 131,072-token device
-// window, attended per window, and the windows folded by their log2-sum-exp
-// into a float32 accumulator allocated up front.
+// "--kv-placement host": when a prefill's rows would together read more than
+// the cache, the cached pages are staged into a 131,072-token device window,
+// attended per window, and the windows folded by their log2-sum-exp into a
+// float32 accumulator allocated up front (fold_attention_pass).
+//
+// GB300 design: this is the one dense contraction of the library, so it runs
+// on the 5th-generation tensor cores.
+//  * A CTA owns 128 query rows of one KV head: the G query heads sharing the KV
+//    head are stacked along M, so every K/V tile loaded is used by all of them.
+//  * TMA (cp.async.bulk.tensor, 128-byte swizzle) streams the Q tile once and
+//    128-key K/V tiles through a two-stage ring.
+//  * One elected thread issues tcgen05.mma: S = Q K^T (M=128, N=128, K=16 steps)
+//    into one of two TMEM score buffers while the softmax warps work on the
+//    other, then O += P V with P read straight from TMEM (it overwrites the
+//    consumed scores, as a bf16 hi + lo pair) and V from shared memory
+//    (MN-major operand).
+//  * Four softmax warps own one query row per thread (TMEM lane = row): scores
+//    are read with tcgen05.ld, the running max is only moved when it grows by
+//    more than 2^8 (the exact result does not depend on the reference), and the
+//    rare rescale of O goes through TMEM.
+//  * The epilogue normalises O, forms lse2 = m + log2(l) and folds the window
+//    into the caller's fp32 accumulator.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
 #include "common.cuh"
 
+namespace argus {
+namespace prefill {
+
+constexpr int kBM = 128;          // query rows per CTA (TMEM lanes)
+constexpr int kBN = 128;          // keys per block
+constexpr int kD = 128;           // head_dim
+constexpr int kStages = 2;        // K/V ring depth
+constexpr int kSoftmaxWarps = 4;
+constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
+constexpr int kTile = kBM * kD * 2;   // 32 KB: a 128 x 128 bf16 tile as two 16 KB swizzled halves
+constexpr int kHalf = kTile / 2;
+constexpr int kTmemCols = 512;        // S0 [0,128) S1 [128,256) O [256,384)
+constexpr float kRescaleThreshold = 8.f;
+
+// shared memory map (offsets from a 1024-byte aligned base)
+constexpr int kOffQ = 0;
+constexpr int kOffK = kTile;
+constexpr int kOffV = kOffK + kStages * kTile;
+constexpr int kOffBar = kOffV + kStages * kTile;
+// barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], s_free[2], o_done
+constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+// The CTA owns the SM anyway; allocating most of the shared memory keeps every
+// descriptor read well inside the CTA's window.
+constexpr int kSmemBytes = 224 * 1024;
+static_assert(kOffMisc + 64 + 1024 <= kSmemBytes, "shared memory map too large");
+
+struct PParams {
+  int G, n_q, n_tiles;              // tiles per KV head = G * n_q / 128
+  long long win_len, win_pos0, q_pos0;
+  float scale_log2;
+  float* acc_o;
+  float* acc_lse2;
+  int fold;
+};
+
+// ---------------------------------------------------------------- PTX
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+          "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// shared-memory matrix descriptor, 128-byte swizzle (sm_100 layout code 2, version 1)
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// instruction descriptor, kind::f16: bf16 x bf16 -> f32, M = 128, N = 128
+__host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(kBN >> 3) << 17) |
+         ((uint32_t)(kBM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+      "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+      "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------- kernel
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const PParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + kStages;
+  uint64_t* s_full = kv_empty + kStages;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* s_free = p_full + 2;
+  uint64_t* o_done = s_free + 2;
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc);  // [0] tmem base, [1] error
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x, h = blockIdx.y;
+  const long long row0 = (long long)h * p.G * p.n_q + (long long)tile * kBM;   // first row of [Hq*n_q]
+  const int hq = (int)(row0 / p.n_q);
+  const long long i0 = row0 - (long long)hq * p.n_q;                              // first query index
+  // keys j < n_keys can be visible to some row of the tile
+  const long long last_visible = p.q_pos0 + i0 + kBM - 1 - p.win_pos0;
+  long long n_keys = last_visible + 1;
+  if (n_keys < 0) n_keys = 0;
+  if (n_keys > p.win_len) n_keys = p.win_len;
+  const int nb = (int)((n_keys + kBN - 1) / kBN);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_full[b], kSoftmaxWarps * 32);
+      mbar_init(&s_free[b], 1);
+    }
+    mbar_init(o_done, 1);
+    misc[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == kSoftmaxWarps + 1) {  // the MMA warp owns the TMEM allocation
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32((const void*)&misc[0])),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const uint32_t tS[2] = {tmem, tmem + 128};
+  const uint32_t tO = tmem + 256;
+
+  if (warp == kSoftmaxWarps) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0 && nb > 0) {
+      mbar_arrive_expect_tx(q_full, kTile);
+      tma_load_2d(smem + kOffQ, &tmQ, 0, (int)row0, q_full);
+      tma_load_2d(smem + kOffQ + kHalf, &tmQ, 64, (int)row0, q_full);
+      for (int j = 0; j < nb; ++j) {
+        const int st = j % kStages;
+        if (j >= kStages && !mbar_wait(&kv_empty[st], ((j / kStages) - 1) & 1)) {
+          misc[1] = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&kv_full[st], 2 * kTile);
+        uint8_t* kd = smem + kOffK + st * kTile;
+        uint8_t* vd = smem + kOffV + st * kTile;
+        tma_load_3d(kd, &tmK, 0, j * kBN, h, &kv_full[st]);
+        tma_load_3d(kd + kHalf, &tmK, 64, j * kBN, h, &kv_full[st]);
+        tma_load_3d(vd, &tmV, 0, j * kBN, h, &kv_full[st]);
+        tma_load_3d(vd + kHalf, &tmV, 64, j * kBN, h, &kv_full[st]);
+      }
+    }
+  } else if (warp == kSoftmaxWarps + 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0 && nb > 0) {
+      constexpr uint32_t idQK = idesc_bf16(false);
+      constexpr uint32_t idPV = idesc_bf16(true);
+      const uint32_t q_s = smem_u32(smem + kOffQ);
+      bool ok = mbar_wait(q_full, 0);
+      auto issue_pv = [&](int i) {
+        const int b = i & 1, st = i % kStages;
+        if (!mbar_wait(&p_full[b], (i >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t v_s = smem_u32(smem + kOffV + st * kTile);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          // P: 16 keys = 8 packed bf16x2 columns (high part at column 0, low part
+          // at column 64); V: 16 key rows = two 8-row swizzle atoms
+          const uint64_t vd = sdesc(v_s + kk * 2048, kHalf, 1024);
+          mma_ts(tO, tS[b] + kk * 8, vd, idPV, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tO, tS[b] + 64 + kk * 8, vd, idPV, 1u);
+        }
+        mma_commit(o_done);
+        mma_commit(&kv_empty[st]);
+        mma_commit(&s_free[b]);
+        return true;
+      };
+      for (int j = 0; j < nb && ok; ++j) {
+        const int st = j % kStages, b = j & 1;
+        if (!mbar_wait(&kv_full[st], (j / kStages) & 1)) { ok = false; break; }
+        if (j >= 2 && !mbar_wait(&s_free[b], ((j >> 1) - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t k_s = smem_u32(smem + kOffK + st * kTile);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          mma_ss(tS[b], sdesc(q_s + off, kHalf, 1024), sdesc(k_s + off, kHalf, 1024), idQK, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[b]);
+        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+      }
+      if (ok) ok = issue_pv(nb - 1);
+      if (!ok) misc[1] = 1;
+    }
+  } else {
+    // ---------------------------------------------------------- softmax rows
+    const int row = warp * 32 + lane;                  // TMEM lane = tile row
+    const long long qi = i0 + row;                     // query index within the chunk
+    const long long vis_last = p.q_pos0 + qi - p.win_pos0;   // last visible key index
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    float m = -INFINITY, l = 0.f;
+    bool alive = nb > 0;
+    for (int j = 0; j < nb && alive; ++j) {
+      const int b = j & 1;
+      if (!mbar_wait(&s_full[b], (j >> 1) & 1)) { alive = false; misc[1] = 1; break; }
+      tc_fence_after();
+      float s[kBN];
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tS[b] + lane_off + c * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(v[e]) * p.scale_log2;
+      }
+      const long long k0 = (long long)j * kBN;
+      if (k0 + kBN - 1 > vis_last) {   // block crosses the causal edge (or the window end)
+#pragma unroll
+        for (int e = 0; e < kBN; ++e)
+          if (k0 + e > vis_last) s[e] = -INFINITY;
+      }
+      float mj = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < kBN; ++e) mj = fmaxf(mj, s[e]);
+      if (mj > m + kRescaleThreshold || (m == -INFINITY && mj != -INFINITY)) {
+        if (m != -INFINITY) {
+          const float r = fast_exp2(m - mj);
+          l *= r;
+          // O holds blocks < j: wait for their last P.V, rescale it in TMEM
+          if (!mbar_wait(o_done, (j - 1) & 1)) { alive = false; misc[1] = 1; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < kD / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tO + lane_off + c * 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * r);
+            tmem_st32(tO + lane_off + c * 32, v);
+          }
+          tmem_wait_st();
+        }
+        m = mj;
+      }
+      // P over the consumed scores as a bf16 pair hi + lo (P.V then carries
+      // about 16 significant bits of P); l sums the represented values
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t vh[16], vl[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = (m == -INFINITY) ? 0.f : fast_exp2(s[c * 32 + 2 * e] - m);
+          const float p1 = (m == -INFINITY) ? 0.f : fast_exp2(s[c * 32 + 2 * e + 1] - m);
+          const uint32_t hi = pack_bf16x2(p0, p1);
+          const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xFFFF0000u);
+          const uint32_t lo = pack_bf16x2(p0 - h0, p1 - h1);
+          l += (h0 + __uint_as_float(lo << 16)) + (h1 + __uint_as_float(lo & 0xFFFF0000u));
+          vh[e] = hi;
+          vl[e] = lo;
+        }
+        tmem_st16(tS[b] + lane_off + c * 16, vh);
+        tmem_st16(tS[b] + lane_off + 64 + c * 16, vl);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&p_full[b]);
+    }
+    // ---- epilogue: this window's (o, lse2), folded into the accumulator
+    const long long orow = (long long)hq * p.n_q + qi;
+    float* ao = p.acc_o + orow * kD;
+    const bool have = alive && nb > 0 && l > 0.f;
+    if (alive && nb > 0) {
+      // the last score block seen implies P.V of block nb-3 is done; wait for
+      // nb-2 and then nb-1 so that each parity wait is unambiguous
+      if (nb >= 2 && !mbar_wait(o_done, (nb - 2) & 1)) misc[1] = 1;
+      if (!mbar_wait(o_done, (nb - 1) & 1)) misc[1] = 1;
+      tc_fence_after();
+    }
+    const float lse = have ? m + log2f(l) : -INFINITY;
+    const float La = p.fold ? p.acc_lse2[orow] : -INFINITY;
+    float wa = 0.f, wb = 0.f, L = -INFINITY;
+    if (have) {
+      if (La == -INFINITY) {
+        wb = 1.f / l;
+        L = lse;
+      } else {
+        const float M = fmaxf(La, lse);
+        L = M + log2f(exp2f(La - M) + exp2f(lse - M));
+        wa = exp2f(La - L);
+        wb = exp2f(lse - L) / l;
+      }
+    } else {
+      wa = 1.f;
+      L = La;
+    }
+#pragma unroll
+    for (int c = 0; c < kD / 32; ++c) {
+      uint32_t v[32];
+      if (have) {
+        tmem_ld32(tO + lane_off + c * 32, v);
+        tmem_wait_ld();
+      }
+#pragma unroll
+      for (int e = 0; e < 32; e += 4) {
+        float4 a = (p.fold && wa != 0.f) ? *reinterpret_cast<const float4*>(ao + c * 32 + e)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 o;
+        o.x = wa * a.x + (have ? wb * __uint_as_float(v[e + 0]) : 0.f);
+        o.y = wa * a.y + (have ? wb * __uint_as_float(v[e + 1]) : 0.f);
+        o.z = wa * a.z + (have ? wb * __uint_as_float(v[e + 2]) : 0.f);
+        o.w = wa * a.w + (have ? wb * __uint_as_float(v[e + 3]) : 0.f);
+        if (have || !p.fold) *reinterpret_cast<float4*>(ao + c * 32 + e) = o;
+      }
+    }
+    if (have || !p.fold) p.acc_lse2[orow] = L;
+  }
+
+  // ---- teardown: every tcgen05 op of the CTA has completed (the softmax warps
+  // waited for the last P.V); the allocating warp frees TMEM
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kSoftmaxWarps + 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------- host
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+static bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint32_t box[3] = {64, (cuuint32_t)kBM, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace prefill
+}  // namespace argus
+
 using namespace argus;
+using namespace argus::prefill;
 
 extern "C" argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n_q, const void* q,
                                                   const void* k, const void* v, int64_t kv_head_stride,
                                                   int64_t win_len, int64_t win_pos0, int64_t q_pos0,
                                                   float softmax_scale, float* acc_o, float* acc_lse2,
                                                   int32_t fold, void* stream) {
-  (void)g; (void)n_q; (void)q; (void)k; (void)v; (void)kv_head_stride; (void)win_len;
-  (void)win_pos0; (void)q_pos0; (void)softmax_scale; (void)acc_o; (void)acc_lse2; (void)fold;
-  (void)stream;
-  return fail(ARGUS_E_UNSUPPORTED, "window prefill: not implemented in this build");
+  if (!g) return fail(ARGUS_E_INVALID, "prefill: geometry is NULL");
+  if (g->n_q_heads <= 0 || g->n_kv_heads <= 0 || g->n_q_heads % g->n_kv_heads)
+    return fail(ARGUS_E_INVALID, "prefill: bad head counts");
+  if (g->head_dim != kD) return fail(ARGUS_E_UNSUPPORTED, "prefill: head_dim %d (supported: 128)", g->head_dim);
+  if (n_q < 0 || win_len < 0) return fail(ARGUS_E_INVALID, "prefill: negative n_q or win_len");
+  if (n_q % kBM != 0 || win_len % kBN != 0)
+    return fail(ARGUS_E_UNSUPPORTED, "prefill: n_q (%d) and win_len (%lld) must be multiples of 128", n_q,
+                (long long)win_len);
+  if (fold != 0 && fold != 1) return fail(ARGUS_E_INVALID, "prefill: fold must be 0 or 1");
+  if (!std::isfinite(softmax_scale)) return fail(ARGUS_E_INVALID, "prefill: softmax_scale not finite");
+  if (n_q == 0) return ARGUS_OK;
+  if (!q || !acc_o || !acc_lse2 || (win_len > 0 && (!k || !v)))
+    return fail(ARGUS_E_INVALID, "prefill: NULL pointer");
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+       reinterpret_cast<uintptr_t>(acc_o)) & 15)
+    return fail(ARGUS_E_INVALID, "prefill: pointers must be 16-byte aligned");
+  const long long stride = kv_head_stride ? kv_head_stride : win_len * kD;
+  if (stride % 8 != 0 || stride < win_len * kD)
+    return fail(ARGUS_E_INVALID, "prefill: kv_head_stride must be >= win_len*head_dim and a multiple of 8");
+  if ((long long)g->n_q_heads * n_q > (1LL << 31) || win_len > (1LL << 31))
+    return fail(ARGUS_E_UNSUPPORTED, "prefill: sizes beyond 2^31 rows");
+  const int G = g->n_q_heads / g->n_kv_heads;
+  PParams p{};
+  p.G = G;
+  p.n_q = n_q;
+  p.n_tiles = G * n_q / kBM;
+  p.win_len = win_len;
+  p.win_pos0 = win_pos0;
+  p.q_pos0 = q_pos0;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.acc_o = acc_o;
+  p.acc_lse2 = acc_lse2;
+  p.fold = fold;
+  CUtensorMap mq, mk, mv;
+  const cuuint64_t qd[2] = {(cuuint64_t)kD, (cuuint64_t)g->n_q_heads * n_q};
+  const cuuint64_t qs[1] = {(cuuint64_t)kD * 2};
+  const long long wl = std::max<long long>(win_len, kBN);
+  const cuuint64_t kd[3] = {(cuuint64_t)kD, (cuuint64_t)wl, (cuuint64_t)g->n_kv_heads};
+  const cuuint64_t ks[2] = {(cuuint64_t)kD * 2, (cuuint64_t)stride * 2};
+  if (!make_map(&mq, q, 2, qd, qs)) return fail(ARGUS_E_LAUNCH, "prefill: tensor map for q failed");
+  if (!make_map(&mk, win_len > 0 ? k : q, 3, kd, ks)) return fail(ARGUS_E_LAUNCH, "prefill: tensor map for k failed");
+  if (!make_map(&mv, win_len > 0 ? v : q, 3, kd, ks)) return fail(ARGUS_E_LAUNCH, "prefill: tensor map for v failed");
+  static bool configured[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(ARGUS_E_LAUNCH, "prefill: no device");
+  if (!configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "prefill: smem attribute: %s", cudaGetErrorString(e));
+    configured[dev] = true;
+  }
+  dim3 grid(p.n_tiles, g->n_kv_heads);
+  prefill_kernel<<<grid, kThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(mq, mk, mv, p);
+  return launch_status("argus_window_prefill_attn");
 }

@@ -1,0 +1,105 @@
+"""argus_window_prefill_attn (tcgen05) on the GPU against the oracle.
+
+Windows are slices of one cache (kv_head_stride), attended with causal
+visibility by absolute position and folded by log2-sum-exp; the folded result
+must equal single-pass attention over everything visible.  Tolerance on the
+fp32 accumulator: max|err| <= 1e-3 * max|ref| + 1e-4.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import mixed_precision_paged_argus_gb300.argus as argus
+from mixed_precision_paged_argus_gb300 import workloads as W
+import oracle
+from oracle import codecs as C
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _data(Hq, Hkv, n_q, ctx, seed):
+    q = W.normal((Hq, n_q, 128), W.BF16, seed)
+    kv_len = ctx + n_q
+    k = W.normal((Hkv, kv_len, 128), W.BF16, seed + 1)
+    v = W.normal((Hkv, kv_len, 128), W.BF16, seed + 2)
+    f = lambda t: C.bf16_bits_to_f64(W.to_bits(t))
+    return q, k, v, f(q), f(k), f(v)
+
+
+def _run_windows(Hq, Hkv, n_q, ctx, windows, seed, scale=None):
+    q, k, v, q64, k64, v64 = _data(Hq, Hkv, n_q, ctx, seed)
+    scale = W.softmax_scale(128) if scale is None else scale
+    g = argus.geom(Hq, Hkv, 128, 16)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    kv_len = ctx + n_q
+    acc_o = torch.zeros((Hq, n_q, 128), dtype=torch.float32, device=DEV)
+    acc_l = torch.full((Hq, n_q), float("-inf"), dtype=torch.float32, device=DEV)
+    for wi, (w0, w1) in enumerate(windows):
+        argus.window_prefill_attn(g, n_q, qd, kd[:, w0:], vd[:, w0:], kv_len * 128, w1 - w0, w0, ctx, scale,
+                                  acc_o, acc_l, 1 if wi > 0 else 0)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.window_attention(q64, k64, v64, 0, ctx, scale)
+    return acc_o.cpu().numpy(), acc_l.cpu().numpy(), ref_o, ref_l
+
+
+def _check(go, gl, ro, rl):
+    t = 1e-3 * np.abs(ro).max() + 1e-4
+    err = np.abs(go - ro).max()
+    assert err <= t, "max err %.3g > tol %.3g" % (err, t)
+    assert np.abs(gl - rl).max() <= 1e-4 * np.abs(rl).max() + 1e-5
+
+
+def test_single_window_full_view_small():
+    go, gl, ro, rl = _run_windows(1, 1, 128, 128, [(0, 128)], seed=501)
+    # the chunk itself is not part of this window: compare against the cache-only oracle
+    q, k, v, q64, k64, v64 = _data(1, 1, 128, 128, 501)
+    ro, rl = oracle.window_attention(q64, k64[:, :128], v64[:, :128], 0, 128, W.softmax_scale(128))
+    _check(go, gl, ro, rl)
+
+
+def test_causal_chunk_window_only():
+    # a 256-row chunk attending only to itself: causal inside the chunk
+    q, k, v, q64, k64, v64 = _data(2, 1, 256, 0, 503)
+    g = argus.geom(2, 1, 128, 16)
+    acc_o = torch.empty((2, 256, 128), dtype=torch.float32, device=DEV)
+    acc_l = torch.empty((2, 256), dtype=torch.float32, device=DEV)
+    argus.window_prefill_attn(g, 256, q.to(DEV), k.to(DEV), v.to(DEV), 0, 256, 1000, 1000,
+                              W.softmax_scale(128), acc_o, acc_l, 0)
+    torch.cuda.synchronize()
+    ro, rl = oracle.window_attention(q64, k64, v64, 1000, 1000, W.softmax_scale(128))
+    _check(acc_o.cpu().numpy(), acc_l.cpu().numpy(), ro, rl)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(2, 1), (16, 2)])
+def test_windows_folded_equal_single_pass(Hq, Hkv):
+    n_q, ctx = 256, 768
+    windows = [(0, 256), (256, 768), (768, 1024)]      # two cache windows, then the chunk
+    go, gl, ro, rl = _run_windows(Hq, Hkv, n_q, ctx, windows, seed=505 + Hq)
+    _check(go, gl, ro, rl)
+
+
+def test_window_beyond_every_query_is_identity():
+    q, k, v, q64, k64, v64 = _data(2, 1, 128, 256, 509)
+    g = argus.geom(2, 1, 128, 16)
+    acc_o = torch.randn((2, 128, 128), device=DEV)
+    acc_l = torch.randn((2, 128), device=DEV)
+    o0, l0 = acc_o.clone(), acc_l.clone()
+    # keys at positions 10_000.. are after every query (positions 256..383)
+    argus.window_prefill_attn(g, 128, q.to(DEV), k.to(DEV), v.to(DEV), 0, 128, 10_000, 256,
+                              W.softmax_scale(128), acc_o, acc_l, 1)
+    torch.cuda.synchronize()
+    assert torch.equal(acc_o, o0) and torch.equal(acc_l, l0)
+
+
+def test_rejects_unsupported_shapes():
+    g = argus.geom(2, 1, 64, 16)
+    t = torch.zeros((2, 128, 64), dtype=torch.bfloat16, device=DEV)
+    o = torch.zeros((2, 128, 64), device=DEV)
+    l = torch.zeros((2, 128), device=DEV)
+    with pytest.raises(argus.ArgusError) as e:
+        argus.window_prefill_attn(g, 128, t, t, t, 0, 128, 0, 0, 0.1, o, l, 0)
+    assert e.value.status == 2
