@@ -11,7 +11,11 @@ write) before every timed step, outside the timed region.
 Printed value: decode attention microseconds per token per layer (lower is
 better), plus the effective KV bandwidth against the HBM roofline.
 
-  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--legs]
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--no-legs]
+
+The same line also carries "legs": the other four workloads (tiny FP16 decode,
+batched BF16/FP8 decode and demotion, sparse selected-page decode, windowed
+prefill), each timed with L2 flushed and reported against its roofline.
 
 --impl reference times the CPU oracle (double precision, one process per host
 core) on a bounded sample of the same workload.  Under torchrun every rank
@@ -249,6 +253,240 @@ def run_gpu(args, rank, world):
     return ms_step, ms_e2e, clocks, t_wall, q_host.numel() * 2, out_host.numel() * 2
 
 
+# ---------------------------------------------------------------- other workloads
+# Each leg builds one of the other four synthetic workloads on the device, times
+# it as a CUDA graph with L2 flushed before every timed replay, and reports
+# absolute numbers plus the fraction of the roofline.  Legs never change the
+# headline value above.
+
+class Timer:
+    def __init__(self, dev):
+        import torch
+        self.torch = torch
+        self.stream = torch.cuda.Stream(device=dev)
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
+
+    def graph(self, fn):
+        torch = self.torch
+        with torch.cuda.stream(self.stream):
+            fn()
+            fn()
+            self.stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                fn()
+        torch.cuda.synchronize()
+        return g
+
+    def time(self, replay, n, warm):
+        torch = self.torch
+        out = []
+        for i in range(warm + n):
+            with torch.cuda.stream(self.stream):
+                self.flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(self.stream)
+                replay()
+                e1.record(self.stream)
+            e1.synchronize()
+            if i >= warm:
+                out.append(e0.elapsed_time(e1))
+        return sum(out) / len(out)
+
+
+def leg_tiny(dev, timer, steps, warm, hbm):
+    """Batch 1, 1 layer, 14 q / 2 KV heads, head_dim 64, 4 FP16 pages of 1024."""
+    import torch
+    import mixed_precision_paged_argus_gb300.argus as argus
+    from mixed_precision_paged_argus_gb300 import workloads as W, accounting as A
+    Hq, Hkv, D_, P_ = 14, 2, 64, 1024
+    g = argus.geom(Hq, Hkv, D_, P_)
+    pool = argus.Pool(W.FP16, W.normal((4, 2, Hkv, P_, D_), W.FP16, W.seed_of("tiny_fp16", 0, 1), device=dev),
+                      None, 4)
+    q = W.normal((1, Hq, D_), W.FP16, W.seed_of("tiny_fp16", 0, 0), device=dev)
+    out = torch.empty((1, Hq, D_), dtype=torch.float16, device=dev)
+    a = argus.decode_args(g, 1, q, [pool], torch.zeros((1, 4), dtype=torch.uint8, device=dev),
+                          torch.arange(4, dtype=torch.int32, device=dev).reshape(1, 4),
+                          torch.tensor([4096], dtype=torch.int32, device=dev), 4, W.softmax_scale(D_), out=out)
+    ws = torch.empty(max(1, argus.decode_workspace_bytes(a)), dtype=torch.uint8, device=dev)
+    gr = timer.graph(lambda: argus.paged_decode_attn(a, ws, stream=timer.stream))
+    ms = timer.time(gr.replay, steps, warm)
+    nbytes = A.kv_bytes(A.FP16, 4096, Hkv, D_, 4) + 2 * Hq * D_ * 2
+    return {"workload": "tiny_fp16_decode: batch 1, 14 q / 2 kv, head_dim 64, 4 x 1024-token FP16 pages",
+            "us_per_step": ms * 1e3, "us_per_token_layer": ms * 1e3, "bytes": nbytes,
+            "gbs": nbytes / (ms * 1e-3) / 1e9, "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm,
+            "note": "2 MiB per step: launch-latency bound, the HBM fraction is not meaningful"}
+
+
+def leg_batched(dev, timer, steps, warm, hbm):
+    """Batch 32, 32 q / 8 KV heads, head_dim 128, 16-token pages, lengths
+    U[8192, 32768], random physical slots; BF16 and FP8 decode, and demotion
+    of the BF16 pages to FP8 / INT8 / INT4."""
+    import torch
+    import mixed_precision_paged_argus_gb300.argus as argus
+    from mixed_precision_paged_argus_gb300 import workloads as W, accounting as A
+    B, Hq, Hkv, D_, P_, MAXP = 32, 32, 8, 128, 16, 2048
+    lens = W.uniform_ints(B, 8192, 32768, W.seed_of("batched", 0, 3))
+    table, n_slots = W.paged_block_table(lens, P_, MAXP, W.seed_of("batched", 0, 4))
+    g = argus.geom(Hq, Hkv, D_, P_)
+    bf = argus.Pool(W.BF16, W.normal((n_slots, 2, Hkv, P_, D_), W.BF16, W.seed_of("batched", 0, 1), device=dev),
+                    None, n_slots)
+    q = W.normal((B, Hq, D_), W.BF16, W.seed_of("batched", 0, 0), device=dev)
+    d_table = torch.from_numpy(table).to(dev)
+    d_lens = torch.from_numpy(lens.astype(np.int32)).to(dev)
+    ids = torch.arange(n_slots, dtype=torch.int32, device=dev)
+    res = {"workload": "batched_decode: batch 32, 32 q / 8 kv, head_dim 128, 16-token pages, lengths U[8192,32768] "
+                       "(sum %d tokens), slots a random permutation" % int(lens.sum())}
+    tokens = int(lens.sum())
+    pages = int(sum((L + P_ - 1) // P_ for L in lens))
+    # demotion of every BF16 page
+    for name, codec in (("fp8", W.FP8_E4M3), ("int8", W.INT8), ("int4", W.INT4_G32)):
+        dst = argus.Pool.empty(codec, n_slots, Hkv, P_, D_, device=dev)
+        gr = timer.graph(lambda: argus.quantize_pages(g, W.BF16, bf.codes, n_slots, ids, dst, ids, n_slots,
+                                                      stream=timer.stream))
+        ms = timer.time(gr.replay, max(3, steps // 5), warm)
+        nb = A.quantize_bytes(codec, 2, n_slots * 2 * Hkv, P_, D_)
+        res["quantize_" + name] = {"us": ms * 1e3, "bytes": nb, "gbs": nb / (ms * 1e-3) / 1e9,
+                                   "frac_of_hbm": nb / (ms * 1e-3) / 1e9 / hbm}
+        if codec == W.FP8_E4M3:
+            fp8 = dst
+        else:
+            del dst
+        torch.cuda.synchronize()
+    for name, pool, codec in (("bf16", bf, W.BF16), ("fp8", fp8, W.FP8_E4M3)):
+        out = torch.empty((B, Hq, D_), dtype=torch.bfloat16, device=dev)
+        a = argus.decode_args(g, B, q, [pool], torch.full((B, MAXP), codec, dtype=torch.uint8, device=dev),
+                              d_table, d_lens, MAXP, W.softmax_scale(D_), out=out)
+        ws = torch.empty(max(1, argus.decode_workspace_bytes(a)), dtype=torch.uint8, device=dev)
+        gr = timer.graph(lambda: argus.paged_decode_attn(a, ws, stream=timer.stream))
+        ms = timer.time(gr.replay, steps, warm)
+        nb = A.kv_bytes(codec, tokens, Hkv, D_, pages) + 2 * B * Hq * D_ * 2
+        res["decode_" + name] = {"us_per_step": ms * 1e3, "us_per_token_layer": ms * 1e3 / B, "bytes": nb,
+                                 "gbs": nb / (ms * 1e-3) / 1e9, "frac_of_hbm": nb / (ms * 1e-3) / 1e9 / hbm}
+    del bf, fp8
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def leg_sparse(dev, timer, steps, warm, hbm):
+    """Batch 8, 12 layers, 32 q / 4 KV heads, head_dim 128, 262144 tokens in
+    64-token FP8 pages with bf16 compressed keys; per layer the indexer picks
+    the top 32 pages plus the newest one per KV head, then decode reads only
+    those."""
+    import torch
+    import mixed_precision_paged_argus_gb300.argus as argus
+    from mixed_precision_paged_argus_gb300 import workloads as W, accounting as A
+    B, L_, Hq, Hkv, D_, P_, NP, K_ = 8, 12, 32, 4, 128, 64, 4096, 32
+    width = 2 * K_ + 8
+    g = argus.geom(Hq, Hkv, D_, P_)
+    pools, ckeys, qs = [], [], []
+    ids = torch.arange(NP, dtype=torch.int32, device=dev)
+    for layer in range(L_):
+        pool = argus.Pool.empty(W.FP8_E4M3, B * NP, Hkv, P_, D_, device=dev)
+        ck = torch.empty((B, NP, Hkv, D_), dtype=torch.bfloat16, device=dev)
+        for b in range(B):
+            src = W.normal((NP, 2, Hkv, P_, D_), W.BF16, W.seed_of("sparse", layer, 1) * 16 + b, device=dev)
+            argus.quantize_pages(g, W.BF16, src, NP, ids, pool, ids + b * NP, NP, ckey_out=ck[b])
+            del src
+        pools.append(pool)
+        ckeys.append(ck)
+        qs.append(W.normal((B, Hq, D_), W.BF16, W.seed_of("sparse", layer, 0), device=dev))
+    torch.cuda.synchronize()
+    table = (torch.arange(B * NP, dtype=torch.int32, device=dev)).reshape(B, NP)
+    codec = torch.full((B, NP), W.FP8_E4M3, dtype=torch.uint8, device=dev)
+    lens = torch.full((B,), NP * P_, dtype=torch.int32, device=dev)
+    npages = torch.full((B,), NP, dtype=torch.int32, device=dev)
+    sel = torch.empty((B, Hkv, width), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B, Hkv), dtype=torch.int32, device=dev)
+    drops = torch.zeros(1, dtype=torch.int32, device=dev)
+    sws = torch.empty(argus.select_workspace_bytes(g, B, NP), dtype=torch.uint8, device=dev)
+    outs = [torch.empty((B, Hq, D_), dtype=torch.bfloat16, device=dev) for _ in range(L_)]
+    args = [argus.decode_args(g, B, qs[l], [pools[l]], codec, table, lens, NP, W.softmax_scale(D_), out=outs[l],
+                              sel_pages=sel, sel_count=cnt, sel_width=width) for l in range(L_)]
+    dws = torch.empty(max(argus.decode_workspace_bytes(a) for a in args), dtype=torch.uint8, device=dev)
+
+    def step(select=True, decode=True):
+        for l in range(L_):
+            if select:
+                argus.select_pages(g, B, qs[l], ckeys[l], npages, NP, K_, True, sel, cnt, width, drops, sws,
+                                   stream=timer.stream)
+            if decode:
+                argus.paged_decode_attn(args[l], dws, stream=timer.stream)
+
+    ms = timer.time(timer.graph(step).replay, steps, warm)
+    ms_sel = timer.time(timer.graph(lambda: step(decode=False)).replay, steps, warm)
+    ms_dec = timer.time(timer.graph(lambda: step(select=False)).replay, steps, warm)
+    slab = B * NP * Hkv * D_ * 2
+    sel_bytes = B * Hkv * (K_ + 1) * (2 * P_ * D_ + 8)
+    per_layer = slab + sel_bytes + 2 * B * Hq * D_ * 2
+    nb = L_ * per_layer
+    res = {"workload": "sparse_decode: batch 8, 12 layers, 32 q / 4 kv, head_dim 128, 262144 tokens in 64-token "
+                       "FP8 pages, top-32 + newest page per kv head",
+           "us_per_step": ms * 1e3, "us_per_step_layer": ms * 1e3 / L_, "bytes_per_step": nb,
+           "gbs": nb / (ms * 1e-3) / 1e9, "frac_of_hbm": nb / (ms * 1e-3) / 1e9 / hbm,
+           "select_us_per_step": ms_sel * 1e3, "select_gbs": L_ * slab / (ms_sel * 1e-3) / 1e9,
+           "decode_us_per_step": ms_dec * 1e3, "decode_gbs": L_ * sel_bytes / (ms_dec * 1e-3) / 1e9,
+           "drops": int(drops.item())}
+    del pools, ckeys
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def leg_prefill(dev, timer, steps, warm, tflops_peak):
+    """16 q / 2 KV heads, head_dim 128, 1048576 cached BF16 tokens and a
+    1024-token causal chunk; eight 131072-token windows plus the chunk window,
+    folded by log2-sum-exp into an fp32 accumulator."""
+    import torch
+    import mixed_precision_paged_argus_gb300.argus as argus
+    from mixed_precision_paged_argus_gb300 import workloads as W, accounting as A
+    Hq, Hkv, D_, NQ, CTX, WIN = 16, 2, 128, 1024, 1 << 20, 131072
+    kv_len = CTX + NQ
+    q = W.normal((Hq, NQ, D_), W.BF16, W.seed_of("prefill", 0, 0), device=dev)
+    k = W.normal((Hkv, kv_len, D_), W.BF16, W.seed_of("prefill", 0, 1), device=dev)
+    v = W.normal((Hkv, kv_len, D_), W.BF16, W.seed_of("prefill", 0, 2), device=dev)
+    g = argus.geom(Hq, Hkv, D_, 16)
+    acc_o = torch.empty((Hq, NQ, D_), dtype=torch.float32, device=dev)
+    acc_l = torch.empty((Hq, NQ), dtype=torch.float32, device=dev)
+    wins = [(w, w + WIN) for w in range(0, CTX, WIN)] + [(CTX, CTX + NQ)]
+
+    def run():
+        for i, (w0, w1) in enumerate(wins):
+            argus.window_prefill_attn(g, NQ, q, k[:, w0:], v[:, w0:], kv_len * D_, w1 - w0, w0, CTX,
+                                      W.softmax_scale(D_), acc_o, acc_l, 1 if i else 0, stream=timer.stream)
+
+    ms = timer.time(timer.graph(run).replay, max(3, steps // 10), warm)
+    flops = A.prefill_flops(Hq, D_, NQ, NQ * CTX + NQ * (NQ + 1) // 2)
+    res = {"workload": "windowed_prefill: 16 q / 2 kv, head_dim 128, 1048576 cached bf16 tokens + 1024-token "
+                       "causal chunk, 131072-token windows folded by log2-sum-exp",
+           "ms": ms, "flops": flops, "tflops": flops / (ms * 1e-3) / 1e12,
+           "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / tflops_peak,
+           "note": "useful FLOPs 4*D*Hq*visible pairs; the P.V product runs twice (bf16 hi + lo of P)"}
+    del q, k, v
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_legs(steps, warm):
+    import torch
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    timer = Timer(dev)
+    hbm, tf, _ = peaks()
+    out = {}
+    for name, fn, arg in (("tiny_fp16", leg_tiny, hbm), ("batched", leg_batched, hbm),
+                          ("sparse", leg_sparse, hbm), ("prefill", leg_prefill, tf)):
+        t0 = time.perf_counter()
+        try:
+            out[name] = fn(dev, timer, steps, warm, arg)
+        except Exception as e:  # a leg failure is reported, never hidden
+            out[name] = {"error": "%s: %s" % (type(e).__name__, e)}
+        out[name]["wall_s"] = time.perf_counter() - t0
+    return out
+
+
 # ---------------------------------------------------------------- oracle leg
 
 def _oracle_layer(layer):
@@ -307,6 +545,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="argus", choices=["argus", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-legs", action="store_true", help="skip the other four workloads")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -335,6 +574,9 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_leg()                         # before the first GPU call (spawned pool)
     ms_step, ms_e2e, clocks, t_wall, h2d, d2h = run_gpu(args, rank, world)
+    legs = None
+    if rank == 0 and not args.no_legs:
+        legs = run_legs(max(5, args.steps // 2), args.warmup)
     if rank != 0:
         return
     hbm, _, peak_kind = peaks()
@@ -370,6 +612,8 @@ def main():
     }
     if cpu is not None:
         line["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    if legs is not None:
+        line["legs"] = legs
     print(json.dumps(line))
 
 
