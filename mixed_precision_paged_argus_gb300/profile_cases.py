@@ -1,0 +1,144 @@
+"""Small, self-contained cases of each kernel, sized for Nsight Compute.
+
+  python -m mixed_precision_paged_argus_gb300.profile_cases <case> [--reps N]
+
+Every case builds its inputs with the seeded generators, runs the library
+call `reps` times and synchronises.  Cases keep a few GB at most on the device
+and use inputs larger than L2 where the kernel streams HBM.
+
+  decode_mixed    one layer of the mixed-tier decode (14/2 heads, D 64, 16 pages x 1024)
+  decode_bf16     batched BF16 decode, batch 8 of the batched workload's shape
+  decode_fp8      the same pages demoted to FP8
+  quantize_fp8    demote 64 Ki 16x128 BF16 units to FP8 (256 MB read)
+  quantize_int4   the same to INT4
+  select          indexer scores + top-k for one layer of the sparse workload
+  prefill         one 131072-token window of the windowed prefill
+  fold            fold a 16 x 1024 x 128 fp32 partial into an accumulator
+"""
+
+import argparse
+import sys
+
+import numpy as np
+import torch
+
+from . import argus
+from . import workloads as W
+
+
+def _decode_mixed(dev):
+    Hq, Hkv, D, P, NP = 14, 2, 64, 1024, 16
+    g = argus.geom(Hq, Hkv, D, P)
+    tiers = W.mixed_tier_codecs(NP)
+    src = W.normal((NP, 2, Hkv, P, D), W.FP16, W.seed_of("mixed_tier", 0, 1), device=dev,
+                   outlier_seed=W.seed_of("mixed_tier", 0, 5))
+    pools, table = [], np.zeros(NP, np.int32)
+    for codec in (W.FP16, W.FP8_E4M3, W.INT8, W.INT4_G32):
+        pages = [p for p in range(NP) if tiers[p] == codec]
+        pool = argus.Pool.empty(codec, 4, Hkv, P, D, device=dev)
+        argus.quantize_pages(g, W.FP16, src, NP, torch.tensor(pages, dtype=torch.int32, device=dev), pool,
+                             torch.arange(4, dtype=torch.int32, device=dev), 4)
+        table[pages] = np.arange(4)
+        pools.append(pool)
+    q = W.normal((1, Hq, D), W.FP16, W.seed_of("mixed_tier", 0, 0), device=dev)
+    out = torch.empty((1, Hq, D), dtype=torch.float16, device=dev)
+    a = argus.decode_args(g, 1, q, pools, torch.from_numpy(tiers.reshape(1, NP).astype(np.uint8)).to(dev),
+                          torch.from_numpy(table.reshape(1, NP)).to(dev),
+                          torch.tensor([NP * P], dtype=torch.int32, device=dev), NP, W.softmax_scale(D), out=out)
+    ws = torch.empty(max(1, argus.decode_workspace_bytes(a)), dtype=torch.uint8, device=dev)
+    return lambda: argus.paged_decode_attn(a, ws)
+
+
+def _decode_batched(dev, fp8):
+    B, Hq, Hkv, D, P, MAXP = 8, 32, 8, 128, 16, 2048
+    lens = W.uniform_ints(B, 8192, 32768, W.seed_of("batched", 0, 3))
+    table, n_slots = W.paged_block_table(lens, P, MAXP, W.seed_of("batched", 0, 4))
+    g = argus.geom(Hq, Hkv, D, P)
+    pool = argus.Pool(W.BF16, W.normal((n_slots, 2, Hkv, P, D), W.BF16, W.seed_of("batched", 0, 1), device=dev),
+                      None, n_slots)
+    codec = W.BF16
+    if fp8:
+        ids = torch.arange(n_slots, dtype=torch.int32, device=dev)
+        dst = argus.Pool.empty(W.FP8_E4M3, n_slots, Hkv, P, D, device=dev)
+        argus.quantize_pages(g, W.BF16, pool.codes, n_slots, ids, dst, ids, n_slots)
+        pool, codec = dst, W.FP8_E4M3
+    q = W.normal((B, Hq, D), W.BF16, W.seed_of("batched", 0, 0), device=dev)
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    a = argus.decode_args(g, B, q, [pool], torch.full((B, MAXP), codec, dtype=torch.uint8, device=dev),
+                          torch.from_numpy(table).to(dev), torch.from_numpy(lens.astype(np.int32)).to(dev), MAXP,
+                          W.softmax_scale(D), out=out)
+    ws = torch.empty(max(1, argus.decode_workspace_bytes(a)), dtype=torch.uint8, device=dev)
+    return lambda: argus.paged_decode_attn(a, ws)
+
+
+def _quantize(dev, codec):
+    Hkv, P, D, n = 8, 16, 128, 8192
+    g = argus.geom(Hkv, Hkv, D, P)
+    src = W.normal((n, 2, Hkv, P, D), W.BF16, 77, device=dev)
+    ids = torch.arange(n, dtype=torch.int32, device=dev)
+    dst = argus.Pool.empty(codec, n, Hkv, P, D, device=dev)
+    return lambda: argus.quantize_pages(g, W.BF16, src, n, ids, dst, ids, n)
+
+
+def _select(dev):
+    B, Hq, Hkv, D, NP, K = 8, 32, 4, 128, 4096, 32
+    g = argus.geom(Hq, Hkv, D, 64)
+    q = W.normal((B, Hq, D), W.BF16, W.seed_of("sparse", 0, 0), device=dev)
+    ck = W.normal((B, NP, Hkv, D), W.BF16, W.seed_of("sparse", 0, 6), device=dev)
+    npg = torch.full((B,), NP, dtype=torch.int32, device=dev)
+    sel = torch.empty((B, Hkv, 2 * K + 8), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B, Hkv), dtype=torch.int32, device=dev)
+    drops = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(argus.select_workspace_bytes(g, B, NP), dtype=torch.uint8, device=dev)
+    return lambda: argus.select_pages(g, B, q, ck, npg, NP, K, True, sel, cnt, 2 * K + 8, drops, ws)
+
+
+def _prefill(dev):
+    Hq, Hkv, D, NQ, WIN = 16, 2, 128, 1024, 131072
+    q = W.normal((Hq, NQ, D), W.BF16, W.seed_of("prefill", 0, 0), device=dev)
+    k = W.normal((Hkv, WIN, D), W.BF16, W.seed_of("prefill", 0, 1), device=dev)
+    v = W.normal((Hkv, WIN, D), W.BF16, W.seed_of("prefill", 0, 2), device=dev)
+    g = argus.geom(Hq, Hkv, D, 16)
+    acc_o = torch.zeros((Hq, NQ, D), dtype=torch.float32, device=dev)
+    acc_l = torch.full((Hq, NQ), float("-inf"), device=dev)
+    return lambda: argus.window_prefill_attn(g, NQ, q, k, v, 0, WIN, 0, 1 << 20, W.softmax_scale(D), acc_o,
+                                             acc_l, 1)
+
+
+def _fold(dev):
+    n, D = 16 * 1024, 128
+    ao = torch.randn((n, D), device=dev)
+    al = torch.randn((n,), device=dev)
+    po = torch.randn((n, D), device=dev)
+    pl = torch.randn((n,), device=dev)
+    return lambda: argus.fold_lse(ao, al, po, pl)
+
+
+CASES = {
+    "decode_mixed": _decode_mixed,
+    "decode_bf16": lambda d: _decode_batched(d, False),
+    "decode_fp8": lambda d: _decode_batched(d, True),
+    "quantize_fp8": lambda d: _quantize(d, W.FP8_E4M3),
+    "quantize_int4": lambda d: _quantize(d, W.INT4_G32),
+    "select": _select,
+    "prefill": _prefill,
+    "fold": _fold,
+}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=sorted(CASES))
+    ap.add_argument("--reps", type=int, default=3)
+    a = ap.parse_args(argv)
+    dev = torch.device("cuda", 0)
+    fn = CASES[a.case](dev)
+    torch.cuda.synchronize()
+    for _ in range(a.reps):
+        fn()
+    torch.cuda.synchronize()
+    print("ok", a.case)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
