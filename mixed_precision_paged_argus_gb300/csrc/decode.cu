@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
         const int s = base / kChunksPerStage + st;
         const int slot = s % L::kStages;
         if (s >= L::kStages) {
-          if (!mbar_wait(&empty[slot], ((s / L::kStages) - 1) & 1)) {
+          if (!mbar_wait(&empty[slot], ((s / L::kStages) - 1) & 1, reinterpret_cast<volatile uint32_t*>(misc))) {
             if (lane == 0) {
               misc[0] = 1;
               if (p.status) atomicOr(p.status, kStatusTimeoutBit);
@@ -643,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
 
   for (int s = 0; s < n_stages; ++s) {
     const int slot = s % L::kStages;
-    if (alive && !mbar_wait(&full[slot], (s / L::kStages) & 1)) {
+    if (alive && !mbar_wait(&full[slot], (s / L::kStages) & 1, reinterpret_cast<volatile uint32_t*>(misc))) {
       alive = false;
       if (lane == 0 && p.status) atomicOr(p.status, kStatusTimeoutBit);
     }

@@ -39,12 +39,13 @@ namespace prefill {
 constexpr int kBM = 128;          // query rows per CTA (TMEM lanes)
 constexpr int kBN = 128;          // keys per block
 constexpr int kD = 128;           // head_dim
-constexpr int kStages = 2;        // K/V ring depth
-constexpr int kSoftmaxWarps = 4;
+constexpr int kStages = 3;        // K/V ring depth
+constexpr int kGroupWarps = 4;    // one softmax warpgroup: a thread per row
+constexpr int kSoftmaxWarps = 2 * kGroupWarps;   // two groups take alternate key blocks
 constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
 constexpr int kTile = kBM * kD * 2;   // 32 KB: a 128 x 128 bf16 tile as two 16 KB swizzled halves
 constexpr int kHalf = kTile / 2;
-constexpr int kTmemCols = 512;        // S0 [0,128) S1 [128,256) O [256,384)
+constexpr int kTmemCols = 512;        // S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512)
 constexpr float kRescaleThreshold = 8.f;
 
 // shared memory map (offsets from a 1024-byte aligned base)
@@ -52,13 +53,11 @@ constexpr int kOffQ = 0;
 constexpr int kOffK = kTile;
 constexpr int kOffV = kOffK + kStages * kTile;
 constexpr int kOffBar = kOffV + kStages * kTile;
-// barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], s_free[2], o_done
-constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 1;
+// barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], s_free[2], o_done[2]
+constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 2;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-// The CTA owns the SM anyway; allocating most of the shared memory keeps every
-// descriptor read well inside the CTA's window.
-constexpr int kSmemBytes = 224 * 1024;
-static_assert(kOffMisc + 64 + 1024 <= kSmemBytes, "shared memory map too large");
+constexpr int kOffML = kOffMisc + 64;                 // group 1's (m, l) per row
+constexpr int kSmemBytes = kOffML + kBM * 8 + 1024;   // + alignment slack
 
 struct PParams {
   int G, n_q, n_tiles;              // tiles per KV head = G * n_q / 128
@@ -143,6 +142,20 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
@@ -155,6 +168,10 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------- kernel
+__device__ __forceinline__ void group_bar(int id) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kSoftmaxWarps * 32) : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PParams p) {
@@ -169,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_free = p_full + 2;
   uint64_t* o_done = s_free + 2;
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc);  // [0] tmem base, [1] error
+  float2* ml1 = reinterpret_cast<float2*>(smem + kOffML);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x, h = blockIdx.y;
@@ -190,10 +208,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], kSoftmaxWarps * 32);
+      mbar_init(&p_full[b], kGroupWarps * 32);
       mbar_init(&s_free[b], 1);
+      mbar_init(&o_done[b], 1);
     }
-    mbar_init(o_done, 1);
     misc[1] = 0;
     fence_mbar_init();
   }
@@ -208,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = misc[0];
   const uint32_t tS[2] = {tmem, tmem + 128};
-  const uint32_t tO = tmem + 256;
+  const uint32_t tO[2] = {tmem + 256, tmem + 384};
 
   if (warp == kSoftmaxWarps) {
     // ---------------------------------------------------------- TMA producer
@@ -218,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_2d(smem + kOffQ + kHalf, &tmQ, 64, (int)row0, q_full);
       for (int j = 0; j < nb; ++j) {
         const int st = j % kStages;
-        if (j >= kStages && !mbar_wait(&kv_empty[st], ((j / kStages) - 1) & 1)) {
+        if (j >= kStages && !mbar_wait(&kv_empty[st], ((j / kStages) - 1) & 1, &misc[1])) {
           misc[1] = 1;
           break;
         }
@@ -233,33 +251,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kSoftmaxWarps + 1) {
     // ---------------------------------------------------------- MMA issuer
+    // order: S0, S1, then per block i: P.V of i, S of i+2 (into the buffer
+    // P.V of i reads; the MMA pipe keeps the two in order)
     if (lane == 0 && nb > 0) {
       constexpr uint32_t idQK = idesc_bf16(false);
       constexpr uint32_t idPV = idesc_bf16(true);
       const uint32_t q_s = smem_u32(smem + kOffQ);
-      bool ok = mbar_wait(q_full, 0);
-      auto issue_pv = [&](int i) {
-        const int b = i & 1, st = i % kStages;
-        if (!mbar_wait(&p_full[b], (i >> 1) & 1)) return false;
-        tc_fence_after();
-        const uint32_t v_s = smem_u32(smem + kOffV + st * kTile);
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          // P: 16 keys = 8 packed bf16x2 columns (high part at column 0, low part
-          // at column 64); V: 16 key rows = two 8-row swizzle atoms
-          const uint64_t vd = sdesc(v_s + kk * 2048, kHalf, 1024);
-          mma_ts(tO, tS[b] + kk * 8, vd, idPV, (i > 0 || kk > 0) ? 1u : 0u);
-          mma_ts(tO, tS[b] + 64 + kk * 8, vd, idPV, 1u);
-        }
-        mma_commit(o_done);
-        mma_commit(&kv_empty[st]);
-        mma_commit(&s_free[b]);
-        return true;
-      };
-      for (int j = 0; j < nb && ok; ++j) {
+      bool ok = mbar_wait(q_full, 0, &misc[1]);
+      auto issue_s = [&](int j) {
         const int st = j % kStages, b = j & 1;
-        if (!mbar_wait(&kv_full[st], (j / kStages) & 1)) { ok = false; break; }
-        if (j >= 2 && !mbar_wait(&s_free[b], ((j >> 1) - 1) & 1)) { ok = false; break; }
+        if (!mbar_wait(&kv_full[st], (j / kStages) & 1, &misc[1])) return false;
+        // no wait for the P.V that last read this buffer: tcgen05.mma from one
+        // thread execute in issue order, so these writes follow its reads
         tc_fence_after();
         const uint32_t k_s = smem_u32(smem + kOffK + st * kTile);
 #pragma unroll
@@ -268,136 +271,210 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(tS[b], sdesc(q_s + off, kHalf, 1024), sdesc(k_s + off, kHalf, 1024), idQK, kk > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[b]);
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        return true;
+      };
+      auto issue_pv = [&](int i) {
+        const int b = i & 1, st = i % kStages;
+        if (!mbar_wait(&p_full[b], (i >> 1) & 1, &misc[1])) return false;
+        tc_fence_after();
+        const uint32_t v_s = smem_u32(smem + kOffV + st * kTile);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          // P: 16 keys = 8 packed bf16x2 columns, high part at 16kk, low part at
+          // 16kk + 8; V: 16 key rows = two 8-row swizzle atoms
+          const uint64_t vd = sdesc(v_s + kk * 2048, kHalf, 1024);
+          mma_ts(tO[b], tS[b] + kk * 16, vd, idPV, (i >= 2 || kk > 0) ? 1u : 0u);
+          mma_ts(tO[b], tS[b] + kk * 16 + 8, vd, idPV, 1u);
+        }
+        mma_commit(&o_done[b]);
+        mma_commit(&kv_empty[st]);
+        mma_commit(&s_free[b]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok && nb > 1) ok = issue_s(1);
+      for (int i = 0; i < nb && ok; ++i) {
+        ok = issue_pv(i);
+        if (ok && i + 2 < nb) ok = issue_s(i + 2);
       }
-      if (ok) ok = issue_pv(nb - 1);
       if (!ok) misc[1] = 1;
     }
   } else {
     // ---------------------------------------------------------- softmax rows
-    const int row = warp * 32 + lane;                  // TMEM lane = tile row
+    const int grp = warp / kGroupWarps;                // this group takes blocks grp, grp+2, ...
+    const int wq = warp % kGroupWarps;                 // TMEM lane quarter
+    const int row = wq * 32 + lane;                    // TMEM lane = tile row
     const long long qi = i0 + row;                     // query index within the chunk
     const long long vis_last = p.q_pos0 + qi - p.win_pos0;   // last visible key index
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t sS = tS[grp] + lane_off, sO = tO[grp] + lane_off;
     float m = -INFINITY, l = 0.f;
-    bool alive = nb > 0;
-    for (int j = 0; j < nb && alive; ++j) {
-      const int b = j & 1;
-      if (!mbar_wait(&s_full[b], (j >> 1) & 1)) { alive = false; misc[1] = 1; break; }
+    bool alive = true;
+    int k = 0;
+    for (int j = grp; j < nb && alive; j += 2, ++k) {
+      // keep the warp together: tcgen05.ld below is warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[grp], k & 1, &misc[1]))) { alive = false; misc[1] = 1; break; }
       tc_fence_after();
-      float s[kBN];
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS[b] + lane_off + c * 32, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(v[e]) * p.scale_log2;
-      }
       const long long k0 = (long long)j * kBN;
-      if (k0 + kBN - 1 > vis_last) {   // block crosses the causal edge (or the window end)
-#pragma unroll
-        for (int e = 0; e < kBN; ++e)
-          if (k0 + e > vis_last) s[e] = -INFINITY;
-      }
+      // tcgen05.ld / st are warp-collective: every branch around them below is
+      // uniform across the warp (per-row conditions only select values)
+      const bool edge = __any_sync(0xffffffffu, k0 + kBN - 1 > vis_last);   // some row crosses the edge
+      // pass 1: block maximum (masking only on a block that crosses the edge)
       float mj = -INFINITY;
+      if (!edge) {
 #pragma unroll
-      for (int e = 0; e < kBN; ++e) mj = fmaxf(mj, s[e]);
-      if (mj > m + kRescaleThreshold || (m == -INFINITY && mj != -INFINITY)) {
-        if (m != -INFINITY) {
-          const float r = fast_exp2(m - mj);
-          l *= r;
-          // O holds blocks < j: wait for their last P.V, rescale it in TMEM
-          if (!mbar_wait(o_done, (j - 1) & 1)) { alive = false; misc[1] = 1; break; }
-          tc_fence_after();
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(sS + c * 32, v);
+          tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < kD / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tO + lane_off + c * 32, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * r);
-            tmem_st32(tO + lane_off + c * 32, v);
-          }
-          tmem_wait_st();
+          for (int e = 0; e < 32; e += 2) mj = fmaxf(mj, fmaxf(__uint_as_float(v[e]), __uint_as_float(v[e + 1])));
         }
-        m = mj;
+      } else {
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(sS + c * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (k0 + c * 32 + e <= vis_last) mj = fmaxf(mj, __uint_as_float(v[e]));
+        }
       }
-      // P over the consumed scores as a bf16 pair hi + lo (P.V then carries
-      // about 16 significant bits of P); l sums the represented values
+      mj *= p.scale_log2;
+      const bool move = mj > m + kRescaleThreshold || (m == -INFINITY && mj != -INFINITY);
+      const bool scale_o = move && m != -INFINITY;
+      if (__any_sync(0xffffffffu, scale_o)) {
+        // the scores of this block being complete implies this group's
+        // previous P.V is complete too (all earlier MMAs were committed)
+        const float r = scale_o ? fast_exp2(m - mj) : 1.f;
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t vh[16], vl[16];
+        for (int c = 0; c < kD / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(sO + c * 32, v);
+          tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = (m == -INFINITY) ? 0.f : fast_exp2(s[c * 32 + 2 * e] - m);
-          const float p1 = (m == -INFINITY) ? 0.f : fast_exp2(s[c * 32 + 2 * e + 1] - m);
-          const uint32_t hi = pack_bf16x2(p0, p1);
-          const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xFFFF0000u);
-          const uint32_t lo = pack_bf16x2(p0 - h0, p1 - h1);
-          l += (h0 + __uint_as_float(lo << 16)) + (h1 + __uint_as_float(lo & 0xFFFF0000u));
-          vh[e] = hi;
-          vl[e] = lo;
+          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * r);
+          tmem_st32(sO + c * 32, v);
         }
-        tmem_st16(tS[b] + lane_off + c * 16, vh);
-        tmem_st16(tS[b] + lane_off + 64 + c * 16, vl);
+        tmem_wait_st();
+        l *= r;
+      }
+      if (move) m = mj;
+      // pass 2: P over the consumed scores as a bf16 pair hi + lo (P.V then
+      // carries about 16 significant bits of P).  A fully masked block has
+      // m = -inf and yields P = 0 through the mask below.
+      const float sc = p.scale_log2;
+      const float mm = (m == -INFINITY) ? 0.f : m;
+      const long long lim = edge ? vis_last - k0 : (long long)kBN;   // keys e <= lim are visible
+#pragma unroll 2
+      for (int c = 0; c < kBN / 16; ++c) {
+        uint32_t v[16];
+        tmem_ld16(sS + c * 16, v);
+        tmem_wait_ld();
+        uint32_t vh[8], vl[8];
+        if (!edge && m != -INFINITY) {   // per-row branch: math only
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e]), sc, -mm));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), sc, -mm));
+            const uint32_t hi = pack_bf16x2(p0, p1);
+            vh[e] = hi;
+            vl[e] = pack_bf16x2(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xFFFF0000u));
+            l += p0 + p1;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const bool ok0 = (m != -INFINITY) && (c * 16 + 2 * e <= lim);
+            const bool ok1 = (m != -INFINITY) && (c * 16 + 2 * e + 1 <= lim);
+            const float p0 = ok0 ? fast_exp2(fmaf(__uint_as_float(v[2 * e]), sc, -mm)) : 0.f;
+            const float p1 = ok1 ? fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), sc, -mm)) : 0.f;
+            const uint32_t hi = pack_bf16x2(p0, p1);
+            vh[e] = hi;
+            vl[e] = pack_bf16x2(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xFFFF0000u));
+            l += p0 + p1;
+          }
+        }
+        // keys 16c .. 16c+15: high part in columns 16c .. 16c+7, low part in
+        // 16c+8 .. 16c+15 -- exactly the columns just read, never unread ones
+        tmem_st8(sS + c * 16, vh);
+        tmem_st8(sS + c * 16 + 8, vl);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[b]);
+      mbar_arrive(&p_full[grp]);
     }
-    // ---- epilogue: this window's (o, lse2), folded into the accumulator
-    const long long orow = (long long)hq * p.n_q + qi;
-    float* ao = p.acc_o + orow * kD;
-    const bool have = alive && nb > 0 && l > 0.f;
-    if (alive && nb > 0) {
-      // the last score block seen implies P.V of block nb-3 is done; wait for
-      // nb-2 and then nb-1 so that each parity wait is unambiguous
-      if (nb >= 2 && !mbar_wait(o_done, (nb - 2) & 1)) misc[1] = 1;
-      if (!mbar_wait(o_done, (nb - 1) & 1)) misc[1] = 1;
+    // ---- this group's last P.V
+    const int nk = (nb > grp) ? (nb - grp + 1) / 2 : 0;   // blocks this group owned
+    if (alive && nk > 0) {
+      if (!mbar_wait(&o_done[grp], (nk - 1) & 1, &misc[1])) misc[1] = 1;
       tc_fence_after();
     }
-    const float lse = have ? m + log2f(l) : -INFINITY;
-    const float La = p.fold ? p.acc_lse2[orow] : -INFINITY;
-    float wa = 0.f, wb = 0.f, L = -INFINITY;
-    if (have) {
-      if (La == -INFINITY) {
-        wb = 1.f / l;
-        L = lse;
-      } else {
-        const float M = fmaxf(La, lse);
-        L = M + log2f(exp2f(La - M) + exp2f(lse - M));
-        wa = exp2f(La - L);
-        wb = exp2f(lse - L) / l;
-      }
-    } else {
-      wa = 1.f;
-      L = La;
-    }
-#pragma unroll
-    for (int c = 0; c < kD / 32; ++c) {
-      uint32_t v[32];
+    if (grp == 1) ml1[row] = make_float2(nk > 0 ? m : -INFINITY, nk > 0 ? l : 0.f);
+    tc_fence_before();
+    group_bar(1);
+    if (grp == 0) {
+      // ---- epilogue: combine both groups, fold this window into the accumulator
+      tc_fence_after();
+      const float2 o1ml = ml1[row];
+      const int nk1 = (nb > 1) ? nb / 2 : 0;
+      const float m0v = nk > 0 ? m : -INFINITY, l0v = nk > 0 ? l : 0.f;
+      const float M = fmaxf(m0v, o1ml.x);
+      const float w0 = (m0v == -INFINITY) ? 0.f : fast_exp2(m0v - M);
+      const float w1 = (o1ml.x == -INFINITY) ? 0.f : fast_exp2(o1ml.x - M);
+      const float lt = l0v * w0 + o1ml.y * w1;
+      const bool have = alive && lt > 0.f;
+      const long long orow = (long long)hq * p.n_q + qi;
+      float* ao = p.acc_o + orow * kD;
+      const float lse = have ? M + log2f(lt) : -INFINITY;
+      const float La = p.fold ? p.acc_lse2[orow] : -INFINITY;
+      float wa = 0.f, wb = 0.f, L = -INFINITY;
       if (have) {
-        tmem_ld32(tO + lane_off + c * 32, v);
+        if (La == -INFINITY) {
+          wb = 1.f / lt;
+          L = lse;
+        } else {
+          const float Mx = fmaxf(La, lse);
+          L = Mx + log2f(exp2f(La - Mx) + exp2f(lse - Mx));
+          wa = exp2f(La - L);
+          wb = exp2f(lse - L) / lt;
+        }
+      } else {
+        wa = 1.f;
+        L = La;
+      }
+      const uint32_t o0a = tO[0] + lane_off, o1a = tO[1] + lane_off;
+#pragma unroll 1
+      for (int c = 0; c < kD / 16; ++c) {
+        uint32_t v0[16], v1[16];
+        if (nk > 0) tmem_ld16(o0a + c * 16, v0);     // nk, nk1 are uniform across the CTA
+        if (nk1 > 0) tmem_ld16(o1a + c * 16, v1);
         tmem_wait_ld();
-      }
 #pragma unroll
-      for (int e = 0; e < 32; e += 4) {
-        float4 a = (p.fold && wa != 0.f) ? *reinterpret_cast<const float4*>(ao + c * 32 + e)
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
-        float4 o;
-        o.x = wa * a.x + (have ? wb * __uint_as_float(v[e + 0]) : 0.f);
-        o.y = wa * a.y + (have ? wb * __uint_as_float(v[e + 1]) : 0.f);
-        o.z = wa * a.z + (have ? wb * __uint_as_float(v[e + 2]) : 0.f);
-        o.w = wa * a.w + (have ? wb * __uint_as_float(v[e + 3]) : 0.f);
-        if (have || !p.fold) *reinterpret_cast<float4*>(ao + c * 32 + e) = o;
+        for (int e = 0; e < 16; e += 4) {
+          float ov[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float x = 0.f;
+            if (have) {
+              if (nk > 0) x += w0 * __uint_as_float(v0[e + u]);
+              if (nk1 > 0) x += w1 * __uint_as_float(v1[e + u]);
+            }
+            ov[u] = x * wb;
+          }
+          float4 a = (p.fold && wa != 0.f) ? *reinterpret_cast<const float4*>(ao + c * 16 + e)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+          float4 o = make_float4(wa * a.x + ov[0], wa * a.y + ov[1], wa * a.z + ov[2], wa * a.w + ov[3]);
+          if (have || !p.fold) *reinterpret_cast<float4*>(ao + c * 16 + e) = o;
+        }
       }
+      if (have || !p.fold) p.acc_lse2[orow] = L;
     }
-    if (have || !p.fold) p.acc_lse2[orow] = L;
   }
 
-  // ---- teardown: every tcgen05 op of the CTA has completed (the softmax warps
-  // waited for the last P.V); the allocating warp frees TMEM
+  // ---- teardown: every tcgen05 op of the CTA has completed (both groups
+  // waited for their last P.V); the allocating warp frees TMEM
   tc_fence_before();
   __syncthreads();
   if (warp == kSoftmaxWarps + 1) {
