@@ -8,8 +8,9 @@
 //   INT8  scale = amax / 127, code = clamp(rint(x / scale), -127, 127)
 //   INT4  per token and 32-element group: z = fp16_sat(min),
 //         s = fp16_sat((max - z) / 15), code = clamp(rint((x - z) / s), 0, 15)
-// every operation IEEE fp32 with round-to-nearest-even (the divisions use the
-// compiler's IEEE division; no reciprocal shortcuts).  The optional compressed
+// every operation IEEE fp32 with round-to-nearest-even.  The quotients are
+// formed with a reciprocal product that provably selects the same code as the
+// IEEE division, falling back to the division near rounding boundaries.  The optional compressed
 // key is the bf16 mean over valid tokens of the stored (dequantised) keys.
 //
 // GB300 design: the pass is a pure HBM stream.  Units of at most 2048 elements
@@ -79,6 +80,30 @@ __device__ __forceinline__ float group_reduce(float v, float* sh) {
   return v;
 }
 
+// Quotients for the encoders.  The codes are defined on RN(x / s) (IEEE fp32
+// division).  x * RN(1/s) is within 1.5 ulp of RN(x / s), so it selects the
+// same code unless it lies within a few ulps of a rounding boundary of the
+// target format; those rare elements (and e4m3's subnormal range) take the
+// IEEE division itself.  The codes are therefore identical to dividing every
+// element.
+//  e4m3 (normal range): boundaries are the midpoints between neighbouring
+//  codes, i.e. fp32 mantissas whose 20 bits below the 3 kept bits equal 0x80000.
+__device__ __forceinline__ float quot_e4m3(float x, float s, float r) {
+  const float y = x * r;
+  const uint32_t low = __float_as_uint(y) & 0xFFFFFu;
+  const bool near = (low - 0x80000u + 8u) <= 16u;
+  const bool small = fabsf(y) < 0.0157f;   // e4m3 subnormals start below 2^-6
+  return (near || small) ? x / s : y;
+}
+
+//  integer codes: boundaries are the half-integers; |y| <= 128 keeps the
+//  quotient's ulp <= 2^-17, far inside the 2^-12 guard band.
+__device__ __forceinline__ float quot_rint(float x, float s, float r) {
+  const float y = x * r;
+  const float f = y - floorf(y);
+  return (fabsf(f - 0.5f) < 0x1p-12f) ? x / s : y;
+}
+
 // Encode 8 values of one 16-byte source vector and store them.
 template <int CODEC, bool SBF16>
 __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& raw, float scale,
@@ -92,9 +117,10 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
   } else if (CODEC == ARGUS_FP8_E4M3) {
     uint32_t w[2] = {0u, 0u};
     if (valid && scale > 0.f) {
+      const float r = 1.f / scale;
 #pragma unroll
       for (int e = 0; e < 8; e += 2) {
-        const uint32_t two = f32x2_to_e4m3x2(f[e] / scale, f[e + 1] / scale);
+        const uint32_t two = f32x2_to_e4m3x2(quot_e4m3(f[e], scale, r), quot_e4m3(f[e + 1], scale, r));
         w[e / 4] |= two << (16 * ((e / 2) & 1));
       }
     }
@@ -104,9 +130,10 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
   } else if (CODEC == ARGUS_INT8) {
     uint32_t w[2] = {0u, 0u};
     if (valid && scale > 0.f) {
+      const float r = 1.f / scale;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        int q = __float2int_rn(f[e] / scale);
+        int q = __float2int_rn(quot_rint(f[e], scale, r));
         q = max(-127, min(127, q));
         w[e / 4] |= (uint32_t)(q & 0xFF) << (8 * (e & 3));
       }
@@ -129,9 +156,10 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
     const float s = fp16_sat((hi - z) / 15.f);
     uint32_t w = 0u;
     if (valid && s > 0.f) {
+      const float r = 1.f / s;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        int q = __float2int_rn((f[e] - z) / s);
+        int q = __float2int_rn(quot_rint(f[e] - z, s, r));
         q = max(0, min(15, q));
         w |= (uint32_t)q << (4 * e);
       }
@@ -289,6 +317,135 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_kernel(const QParams p) 
   }
 }
 
+// Units of at most 2048 elements: one warp per unit, held in registers,
+// software-pipelined so that the next unit's loads are in flight while the
+// current one is reduced, encoded and stored.
+template <int D, bool SBF16, int CODEC>
+__global__ void __launch_bounds__(kCtaThreads) quantize_small_kernel(const QParams p) {
+  constexpr int VPR = D / 8;
+  const int lane = threadIdx.x & 31;
+  const long long wid = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const long long nw = (long long)gridDim.x * (blockDim.x / 32);
+  const int Hkv = p.Hkv, P = p.P;
+  const long long n_units = (long long)p.n_pages * 2 * Hkv;
+  const int nvec = P * VPR;
+  const bool want_ck = p.ckey != nullptr;
+
+  struct Unit {
+    const uint4* src;
+    size_t dst;
+    int page, kv, h, valid;
+    bool ok;
+  };
+  auto describe = [&](long long u) {
+    Unit d;
+    d.page = (int)(u / (2 * Hkv));
+    const int rem = (int)(u - (long long)d.page * 2 * Hkv);
+    d.kv = rem / Hkv;
+    d.h = rem - d.kv * Hkv;
+    const long long ss = p.src_slots[d.page], ds = p.dst_slots[d.page];
+    d.ok = !(ss < 0 || ss >= p.n_src || ds < 0 || ds >= p.n_dst);
+    int valid = p.valid_tokens ? p.valid_tokens[d.page] : P;
+    d.valid = max(0, min(P, valid));
+    d.src = reinterpret_cast<const uint4*>(p.src + ((ss * 2 + d.kv) * Hkv + d.h) * (size_t)P * D);
+    d.dst = ((size_t)ds * 2 + d.kv) * Hkv + d.h;
+    return d;
+  };
+  auto load = [&](const Unit& d, uint4 (&buf)[kRegVecs]) {
+#pragma unroll
+    for (int k = 0; k < kRegVecs; ++k) {
+      const int v = lane + 32 * k;
+      if (d.ok && v < nvec) buf[k] = __ldcs(d.src + v);   // streamed once: evict first
+    }
+  };
+
+  long long u = wid;
+  if (u >= n_units) return;
+  uint4 cur[kRegVecs], nxt[kRegVecs];
+  Unit cu = describe(u);
+  load(cu, cur);
+  while (u < n_units) {
+    const long long un = u + nw;
+    Unit nu = cu;
+    if (un < n_units) {
+      nu = describe(un);
+      load(nu, nxt);
+    }
+    if (!cu.ok) {
+      if (lane == 0 && cu.kv == 0 && cu.h == 0 && p.status) atomicAdd(p.status, 1u);
+    } else {
+      const int nvalid_vec = cu.valid * VPR;
+      uint8_t* dcodes;
+      if (CODEC == ARGUS_FP16 || CODEC == ARGUS_BF16) dcodes = p.dst_codes + cu.dst * (size_t)P * D * 2;
+      else if (CODEC == ARGUS_INT4_G32) dcodes = p.dst_codes + cu.dst * (size_t)P * (D / 2);
+      else dcodes = p.dst_codes + cu.dst * (size_t)P * D;
+      float scale = 0.f;
+      if (CODEC == ARGUS_FP8_E4M3 || CODEC == ARGUS_INT8) {
+        float amax = 0.f;
+#pragma unroll
+        for (int k = 0; k < kRegVecs; ++k) {
+          const int v = lane + 32 * k;
+          if (v < nvalid_vec) {
+            float f[8];
+            unpack8<SBF16>(cur[k], f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        scale = amax > 0.f ? amax / (CODEC == ARGUS_FP8_E4M3 ? 448.f : 127.f) : 0.f;
+        if (lane == 0) reinterpret_cast<float*>(p.dst_meta)[cu.dst] = scale;
+      }
+      float ck[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < kRegVecs; ++k) {
+        const int v = lane + 32 * k;
+        if (v < nvec) {
+          float f[8], deq[8];
+          unpack8<SBF16>(cur[k], f);
+          uint8_t* meta_row = nullptr;
+          if (CODEC == ARGUS_INT4_G32) {
+            const int row = v / VPR, grp = (v % VPR) / 4;
+            meta_row = p.dst_meta + ((cu.dst * P + row) * (D / 32) + grp) * 4;
+          }
+          const bool valid_v = v < nvalid_vec;
+          encode_store<CODEC, SBF16>(f, cur[k], scale, dcodes, (size_t)v, valid_v, deq, meta_row, lane);
+          if (want_ck && valid_v) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ck[e] += deq[e];
+          }
+        }
+      }
+      if (want_ck && cu.kv == 0) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float x = ck[e];
+#pragma unroll
+          for (int o = VPR; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+          ck[e] = x;
+        }
+        if (lane < VPR) {
+          const float n_f = (float)max(cu.valid, 1);
+          uint32_t outw[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const float a0 = cu.valid ? ck[e] / n_f : 0.f;
+            const float a1 = cu.valid ? ck[e + 1] / n_f : 0.f;
+            outw[e / 2] = pack_bf16x2(a0, a1);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.ckey + ((size_t)cu.page * Hkv + cu.h) * D);
+          dst[lane] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+        }
+      }
+    }
+    u = un;
+    cu = nu;
+#pragma unroll
+    for (int k = 0; k < kRegVecs; ++k) cur[k] = nxt[k];
+  }
+}
+
 template <int D, bool SBF16, int CODEC>
 static argus_status launch3(const QParams& p, cudaStream_t s) {
   const long long units = (long long)p.n_pages * 2 * p.Hkv;
@@ -296,8 +453,8 @@ static argus_status launch3(const QParams& p, cudaStream_t s) {
   const bool small = (long long)p.P * D <= 32 * kRegVecs * 8;
   if (small) {
     const long long blocks_needed = (units + (kCtaThreads / 32) - 1) / (kCtaThreads / 32);
-    const int blocks = (int)std::max<long long>(1, std::min<long long>(blocks_needed, (long long)sms * 8));
-    quantize_kernel<D, SBF16, CODEC, 32><<<blocks, kCtaThreads, 0, s>>>(p);
+    const int blocks = (int)std::max<long long>(1, std::min<long long>(blocks_needed, (long long)sms * 4));
+    quantize_small_kernel<D, SBF16, CODEC><<<blocks, kCtaThreads, 0, s>>>(p);
   } else {
     const int blocks = (int)std::max<long long>(1, std::min<long long>(units, (long long)sms * 8));
     quantize_kernel<D, SBF16, CODEC, kCtaThreads><<<blocks, kCtaThreads, 0, s>>>(p);

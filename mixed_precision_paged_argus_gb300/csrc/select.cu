@@ -14,10 +14,13 @@
 // GB300 design: two launches.  (1) score: the slab is the dominant HBM stream
 // (D bf16 per page and head); CTAs tile (batch row, page range), lanes read 16
 // bytes of a compressed key each and reduce within the head's lanes; the
-// G-query sum is formed once per CTA in shared memory.  (2) top-k: one CTA per
-// (batch row, KV head) radix-selects the k-th largest score over the L2-resident
-// score row (four 8-bit passes with shared-memory histograms), then compacts
-// the chosen pages in ascending order with block-wide prefix sums.
+// G-query sum is formed once per CTA in shared memory; each lane keeps eight
+// rows' loads in flight; scores are stored as order-preserving uint32 keys.
+// (2) top-k: one CTA per (batch row, KV head) stages the row's keys in shared
+// memory, radix-selects the k-th largest (8-bit passes, shared-memory
+// histograms, bins chosen by a parallel scan, early exit when a bin is taken
+// whole), then compacts the chosen pages in ascending order with block-wide
+// prefix sums.
 #include <algorithm>
 
 #include "common.cuh"
@@ -28,11 +31,22 @@ namespace select {
 constexpr int kScoreThreads = 256;
 constexpr int kPagesPerCta = 64;
 constexpr int kTopkThreads = 512;
+constexpr int kRowBatch = 8;               // compressed-key loads in flight per lane
+constexpr int kTopkSmemKeys = 40 * 1024;   // rows up to this many pages are staged in shared memory
 
+// Order-preserving map of an fp32 score to uint32: a > b  <=>  key(a) > key(b).
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Writes the order key of each page's score, [B][Hkv][max_pages] uint32.
 template <int D, bool QBF16>
-__global__ void __launch_bounds__(kScoreThreads) score_kernel(int Hkv, int G, int max_pages, const void* q,
-                                                              const uint16_t* ckeys, const int32_t* n_pages,
-                                                              float* scores) {
+__global__ void __launch_bounds__(kScoreThreads) score_kernel(int Hkv, int G, int max_pages,
+                                                              const void* __restrict__ q,
+                                                              const uint16_t* __restrict__ ckeys,
+                                                              const int32_t* __restrict__ n_pages,
+                                                              uint32_t* __restrict__ keys) {
   extern __shared__ float qsum[];  // [Hkv][D]
   const int b = blockIdx.y;
   const int p0 = blockIdx.x * kPagesPerCta;
@@ -51,37 +65,44 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(int Hkv, int G, in
     qsum[idx] = s;
   }
   __syncthreads();
-  constexpr int LPH = D / 8;  // lanes per (page, head) row
+  constexpr int LPH = D / 8;               // lanes per (page, head) row, 16 bytes each
+  constexpr int RPW = 32 / LPH;            // rows per warp and pass
+  constexpr int RPP = (kScoreThreads / 32) * RPW;  // rows per CTA and pass
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int rows_per_warp = 32 / LPH;
   const int sub = lane / LPH, li = lane % LPH;
   const int p_end = min(n, p0 + kPagesPerCta);
   const int n_rows = (p_end - p0) * Hkv;
-  for (int row = warp * rows_per_warp + sub; row - sub < n_rows; row += (blockDim.x / 32) * rows_per_warp) {
-    float s = 0.f;
-    const bool live = row < n_rows;
-    int p = 0, h = 0;
-    if (live) {
-      p = p0 + row / Hkv;
-      h = row % Hkv;
-      const uint4 x = *reinterpret_cast<const uint4*>(ckeys + (((size_t)b * max_pages + p) * Hkv + h) * D + 8 * li);
-      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-      const float* qs = qsum + h * D + 8 * li;
+  // rows of this CTA are contiguous in the slab: (p0 * Hkv + row) * D
+  const uint16_t* base = ckeys + (((size_t)b * max_pages + p0) * Hkv) * D + 8 * li;
+  for (int r0 = warp * RPW + sub; r0 - sub < n_rows; r0 += kRowBatch * RPP) {
+    uint4 x[kRowBatch];
+#pragma unroll
+    for (int j = 0; j < kRowBatch; ++j) {
+      const int row = r0 + j * RPP;
+      if (row < n_rows) x[j] = __ldcs(reinterpret_cast<const uint4*>(base + (size_t)row * D));
+      else x[j] = make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < kRowBatch; ++j) {
+      const int row = r0 + j * RPP;
+      if (row - sub >= n_rows) break;       // warp-uniform: no row of this warp is left
+      const int h = row % Hkv;
+      const float* qs = qsum + (row < n_rows ? h : 0) * D + 8 * li;
+      const uint32_t w[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+      float s = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float k = __uint_as_float(((w[e / 2] >> (16 * (e & 1))) & 0xFFFFu) << 16);
         s = fmaf(k, qs[e], s);
       }
-    }
 #pragma unroll
-    for (int o = 1; o < LPH; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (live && li == 0) scores[((size_t)b * Hkv + h) * max_pages + p] = s;
+      for (int o = 1; o < LPH; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (row < n_rows && li == 0) {
+        const int p = p0 + row / Hkv;
+        keys[((size_t)b * Hkv + h) * max_pages + p] = order_key(s);
+      }
+    }
   }
-}
-
-__device__ __forceinline__ uint32_t order_key(float f) {
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 // Exclusive block-wide prefix sum of one int per thread; returns the total.
@@ -111,20 +132,24 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* sh, int& total) 
   return before + x - v;
 }
 
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pages, const float* scores,
+// One CTA per (KV head, batch row).  The row's keys are staged in shared
+// memory when stage != 0 (dynamic shared memory of max_pages words).
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pages, const uint32_t* keys_g,
                                                             const int32_t* n_pages, int top_k, int keep_newest,
                                                             int32_t* sel_pages, int32_t* sel_count, int width,
-                                                            uint32_t* drops) {
+                                                            uint32_t* drops, int stage) {
+  extern __shared__ uint32_t skeys[];
   __shared__ int hist[256];
   __shared__ int sh_scan[32];
-  __shared__ int sh_sel[2];
+  __shared__ int sh_sel[3];
   const int h = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, nthr = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5;
   int n = n_pages[b];
   const int n_raw = n;
   n = max(0, min(n, max_pages));
   int32_t* out = sel_pages + ((size_t)b * Hkv + h) * width;
-  const float* sc = scores + ((size_t)b * Hkv + h) * max_pages;
+  const uint32_t* keys = keys_g + ((size_t)b * Hkv + h) * max_pages;
   uint32_t dropped = 0;
   if (n_raw > max_pages && tid == 0 && h == 0) dropped += (uint32_t)(n_raw - max_pages);
   const int n_cand = (n > 0) ? (keep_newest ? n - 1 : n) : 0;
@@ -132,41 +157,60 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pag
   const int k_want = min(top_k, n_cand);
   const int k = max(0, min(k_want, room));
   if (tid == 0) dropped += (uint32_t)(k_want - k);
+  if (stage) {
+    for (int p = tid; p < n_cand; p += nthr) skeys[p] = keys[p];
+    keys = skeys;
+    __syncthreads();
+  }
 
-  // threshold T = k-th largest key; take all > T and the first k_rem equal to T
-  uint32_t T = 0u;
+  // Threshold on the masked key: all candidates with (key & mask) > T are
+  // taken, and the first k_rem (in page order) with (key & mask) == T.  Radix
+  // select from the top byte down; a pass that lands on a bin taken whole
+  // ends the search early.
+  uint32_t T = 0u, mask = 0u;
   int k_rem = 0;
   if (k > 0 && k < n_cand) {
-    uint32_t prefix = 0u, mask = 0u;
     int need = k;
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
-      for (int i = tid; i < 256; i += nthr) hist[i] = 0;
+      if (tid < 256) hist[tid] = 0;
       __syncthreads();
       for (int p = tid; p < n_cand; p += nthr) {
-        const uint32_t key = order_key(sc[p]);
-        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
+        const uint32_t key = keys[p];
+        if ((key & mask) == T) atomicAdd(&hist[(key >> shift) & 255], 1);
       }
       __syncthreads();
-      if (tid == 0) {
-        int acc = 0, dsel = 0;
-        for (int d = 255; d >= 0; --d) {
-          if (acc + hist[d] >= need) {
-            dsel = d;
-            break;
-          }
-          acc += hist[d];
+      // bins from the top: thread t holds bin 255 - t; inclusive prefix over threads
+      int c = 0, x = 0;
+      if (tid < 256) {
+        c = hist[255 - tid];
+        x = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
         }
-        sh_sel[0] = dsel;
-        sh_sel[1] = need - acc;
+        if (lane == 31) sh_scan[warp] = x;
       }
       __syncthreads();
-      prefix |= (uint32_t)sh_sel[0] << shift;
+      if (tid < 256) {
+        int before = 0;
+        for (int w = 0; w < warp; ++w) before += sh_scan[w];
+        const int incl = before + x;
+        if (incl >= need && incl - c < need) {
+          sh_sel[0] = 255 - tid;
+          sh_sel[1] = need - (incl - c);
+          sh_sel[2] = c;
+        }
+      }
+      __syncthreads();
+      T |= (uint32_t)sh_sel[0] << shift;
       mask |= 255u << shift;
       need = sh_sel[1];
+      const bool whole_bin = (need == sh_sel[2]);
       __syncthreads();
+      if (whole_bin) break;
     }
-    T = prefix;
     k_rem = need;
   }
   const bool take_all = (k >= n_cand);
@@ -175,41 +219,27 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pag
   const int lo = min(n, tid * per), hi = min(n, lo + per);
   int ties = 0;
   if (!take_all && k > 0) {
-    for (int p = lo; p < min(hi, n_cand); ++p) ties += (order_key(sc[p]) == T);
+    for (int p = lo; p < min(hi, n_cand); ++p) ties += ((keys[p] & mask) == T);
   }
   int tie_total;
-  int tie_before = block_exclusive_scan(ties, sh_scan, tie_total);
-  int mine = 0;
-  for (int p = lo; p < hi; ++p) {
-    bool take;
-    if (p >= n_cand) take = keep_newest && p == n - 1;
-    else if (take_all) take = true;
-    else if (k == 0) take = false;
-    else {
-      const uint32_t key = order_key(sc[p]);
-      if (key > T) take = true;
-      else if (key == T) take = (tie_before++ < k_rem);
-      else take = false;
-    }
-    mine += take;
-  }
+  const int tie_start = block_exclusive_scan(ties, sh_scan, tie_total);
+  auto take_of = [&](int p, int& tie_before) -> bool {
+    if (p >= n_cand) return keep_newest && p == n - 1;
+    if (take_all) return true;
+    if (k == 0) return false;
+    const uint32_t key = keys[p] & mask;
+    if (key > T) return true;
+    if (key == T) return tie_before++ < k_rem;
+    return false;
+  };
+  int mine = 0, tb = tie_start;
+  for (int p = lo; p < hi; ++p) mine += take_of(p, tb);
   int total;
   int pos = block_exclusive_scan(mine, sh_scan, total);
-  tie_before = block_exclusive_scan(ties, sh_scan, tie_total);
+  tb = tie_start;
   for (int p = lo; p < hi; ++p) {
-    bool take;
-    if (p >= n_cand) take = keep_newest && p == n - 1;
-    else if (take_all) take = true;
-    else if (k == 0) take = false;
-    else {
-      const uint32_t key = order_key(sc[p]);
-      if (key > T) take = true;
-      else if (key == T) take = (tie_before++ < k_rem);
-      else take = false;
-    }
-    if (take && pos < width) out[pos++] = p;
+    if (take_of(p, tb) && pos < width) out[pos++] = p;
   }
-  __syncthreads();
   for (int i = total + tid; i < width; i += nthr) out[i] = -1;
   if (tid == 0) {
     sel_count[(size_t)b * Hkv + h] = min(total, width);
@@ -226,7 +256,7 @@ extern "C" argus_status argus_select_workspace_bytes(const argus_geom* g, int32_
                                                      size_t* bytes) {
   if (!g || !bytes) return fail(ARGUS_E_INVALID, "select: NULL argument");
   if (batch < 0 || max_pages < 0 || g->n_kv_heads <= 0) return fail(ARGUS_E_INVALID, "select: bad sizes");
-  *bytes = (size_t)batch * g->n_kv_heads * max_pages * sizeof(float);
+  *bytes = (size_t)batch * g->n_kv_heads * max_pages * sizeof(uint32_t);
   return ARGUS_OK;
 }
 
@@ -248,28 +278,41 @@ extern "C" argus_status argus_select_pages(const argus_geom* g, int32_t batch, c
   if (!q || !ckeys || !n_pages || !sel_pages || !sel_count)
     return fail(ARGUS_E_INVALID, "select: NULL pointer");
   if (reinterpret_cast<uintptr_t>(ckeys) & 15) return fail(ARGUS_E_INVALID, "select: ckeys not 16-byte aligned");
-  size_t need = (size_t)batch * g->n_kv_heads * max_pages * sizeof(float);
+  size_t need = (size_t)batch * g->n_kv_heads * max_pages * sizeof(uint32_t);
   if (!ws || ws_bytes < need) return fail(ARGUS_E_WORKSPACE, "select: workspace %zu < %zu", ws_bytes, need);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int G = g->n_q_heads / g->n_kv_heads;
-  float* scores = static_cast<float*>(ws);
+  uint32_t* keys = static_cast<uint32_t*>(ws);
   dim3 grid1((max_pages + select::kPagesPerCta - 1) / select::kPagesPerCta, batch);
   const size_t sh = (size_t)g->n_kv_heads * g->head_dim * sizeof(float);
   if (sh > 48 * 1024) return fail(ARGUS_E_UNSUPPORTED, "select: n_kv_heads * head_dim too large");
   const uint16_t* ck = static_cast<const uint16_t*>(ckeys);
   const bool bf = (q_dtype == ARGUS_BF16);
   if (g->head_dim == 64) {
-    if (bf) select::score_kernel<64, true><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, q, ck, n_pages, scores);
-    else select::score_kernel<64, false><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, q, ck, n_pages, scores);
+    if (bf) select::score_kernel<64, true><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, q, ck, n_pages, keys);
+    else select::score_kernel<64, false><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, q, ck, n_pages, keys);
   } else {
-    if (bf) select::score_kernel<128, true><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, q, ck, n_pages, scores);
-    else select::score_kernel<128, false><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, q, ck, n_pages, scores);
+    if (bf) select::score_kernel<128, true><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, q, ck, n_pages, keys);
+    else select::score_kernel<128, false><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, q, ck, n_pages, keys);
   }
   argus_status st = launch_status("argus_select_pages (score)");
   if (st != ARGUS_OK) return st;
+  const int stage = max_pages <= select::kTopkSmemKeys ? 1 : 0;
+  const size_t tsh = stage ? (size_t)max_pages * sizeof(uint32_t) : 0;
+  if (tsh > 48 * 1024) {
+    static bool configured[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(ARGUS_E_LAUNCH, "select: no device");
+    if (!configured[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(select::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           select::kTopkSmemKeys * (int)sizeof(uint32_t));
+      if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "select: smem attribute: %s", cudaGetErrorString(e));
+      configured[dev] = true;
+    }
+  }
   dim3 grid2(g->n_kv_heads, batch);
-  select::topk_kernel<<<grid2, select::kTopkThreads, 0, s>>>(g->n_kv_heads, max_pages, scores, n_pages, top_k,
-                                                             keep_newest, sel_pages, sel_count, sel_width,
-                                                             drop_counter);
+  select::topk_kernel<<<grid2, select::kTopkThreads, tsh, s>>>(g->n_kv_heads, max_pages, keys, n_pages, top_k,
+                                                               keep_newest, sel_pages, sel_count, sel_width,
+                                                               drop_counter, stage);
   return launch_status("argus_select_pages (top-k)");
 }

@@ -144,3 +144,40 @@ def test_invalid_arguments_fail_closed():
     with pytest.raises(argus.ArgusError) as e:
         argus.quantize_pages(g, W.FP16, pool.codes, 1, pool.codes, pool, pool.codes, 1)
     assert e.value.status == 2
+
+
+def _near_boundary_units(boundaries, scale, P, D):
+    """fp16 pages whose values x give x / scale within a few ulps of each boundary."""
+    vals = []
+    for m in boundaries:
+        for k in range(-6, 7):
+            x = np.float32(m * scale) * np.float32(1 + k * 2.0 ** -10)
+            vals.append(x)
+    vals = np.array(vals, np.float32).astype(np.float16)
+    return vals
+
+
+@pytest.mark.parametrize("codec", [W.FP8_E4M3, W.INT8])
+def test_codes_near_rounding_boundaries_with_a_non_power_of_two_scale(codec):
+    P, D = 16, 128
+    tab = C.e4m3_table()[:127]
+    if codec == W.FP8_E4M3:
+        bounds = list((tab[1:] + tab[:-1]) / 2)               # e4m3 midpoints, subnormal ones included
+        amax = 448.0 * 1.37
+    else:
+        bounds = [k + 0.5 for k in range(-127, 127)]
+        amax = 127.0 * 1.37
+    vals = _near_boundary_units(bounds, amax / (448.0 if codec == W.FP8_E4M3 else 127.0), P, D)
+    per = P * D - 1
+    n = -(-len(vals) // per)
+    buf = np.zeros(n * per, np.float16)
+    buf[:len(vals)] = vals
+    units = np.concatenate([buf.reshape(n, per), np.full((n, 1), np.float16(amax))], axis=1).reshape(n, P, D)
+    src = np.zeros((n, 2, 1, P, D), np.uint16)
+    src[:, 0, 0] = units.view(np.uint16)
+    src[:, 1, 0] = units.view(np.uint16)
+    t = torch.from_numpy(src.view(np.int16)).view(torch.float16)
+    pool, _, _ = _gpu_quantize(t, W.FP16, codec, 1, P, D, list(range(n)), list(range(n)), n)
+    codes, meta = C.alloc_pool(codec, n, 1, P, D)
+    C.quantize_pages(src, C.CODEC_FP16, list(range(n)), codec, codes, meta, list(range(n)))
+    _compare(pool, codes, meta)
