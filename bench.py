@@ -85,7 +85,83 @@ def profiled_traffic(kernel_key, src_files):
 
 # ---------------------------------------------------------------- clocks
 
-class ClockSampler:
+class NvmlClockSampler:
+    """Samples the SM clock, its maximum, power and the clock-event reasons
+    through NVML (read-only queries) from a background thread about every
+    0.5 ms, so that even a timed region of a few milliseconds is covered."""
+    REASONS = ((0x4, "sw_power_cap"), (0x8, "hw_slowdown"), (0x20, "sw_thermal_slowdown"),
+               (0x40, "hw_thermal_slowdown"), (0x80, "hw_power_brake_slowdown"))
+
+    def __init__(self, dev_index):
+        import ctypes
+        import threading
+        self.ct = ctypes
+        self.lib = None
+        for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+            try:
+                self.lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                pass
+        if self.lib is None or self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("NVML unavailable")
+        self.handle = ctypes.c_void_p()
+        ok = False
+        try:
+            import torch
+            pr = torch.cuda.get_device_properties(dev_index)
+            bus = "%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+            ok = self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.handle)) == 0
+        except Exception:
+            ok = False
+        if not ok:
+            idx = dev_index
+            cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            parts = [x for x in cvd.split(",") if x.strip()]
+            if parts and all(x.strip().isdigit() for x in parts) and dev_index < len(parts):
+                idx = int(parts[dev_index])
+            if self.lib.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(self.handle)) != 0:
+                raise RuntimeError("NVML: no handle for device %d" % idx)
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = fn if fn is not None else self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.samples = []
+        self.stop_evt = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+
+    def _sample(self):
+        ct = self.ct
+        sm, mx, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.handle, 1, ct.byref(sm)) != 0:
+            return
+        self.lib.nvmlDeviceGetMaxClockInfo(self.handle, 1, ct.byref(mx))
+        self.lib.nvmlDeviceGetPowerUsage(self.handle, ct.byref(mw))
+        self.reasons_fn(self.handle, ct.byref(rs))
+        self.samples.append((sm.value, mx.value, mw.value / 1000.0, rs.value))
+
+    def _run(self):
+        while not self.stop_evt.is_set():
+            self._sample()
+            time.sleep(0.0005)
+
+    def start(self):
+        self._sample()
+        self.thread.start()
+
+    def stop(self):
+        self.stop_evt.set()
+        self.thread.join(timeout=5)
+        self._sample()
+        rows = self.samples
+        if not rows:
+            return None
+        reasons = sorted({name for r in rows for bit, name in self.REASONS if r[3] & bit})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "power_w_median": statistics.median(r[2] for r in rows),
+                "source": "nvml, ~0.5 ms sampling during the timed steps"}
+
+
+class SmiClockSampler:
+    """Fallback: nvidia-smi in a loop (200 ms); covers long timed regions only."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -127,7 +203,14 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "source": "nvidia-smi -lms 200"}
+
+
+def ClockSampler(dev_index):
+    try:
+        return NvmlClockSampler(dev_index)
+    except Exception:
+        return SmiClockSampler(dev_index)
 
 
 # ---------------------------------------------------------------- workload
@@ -175,8 +258,10 @@ def run_gpu(args, rank, world):
     g, pools, tables, qs, codec_row, lens = build_mixed_tier(dev)
     scale = W.softmax_scale(D)
     outs = [torch.empty((1, HQ, D), dtype=torch.float16, device=dev) for _ in range(LAYERS)]
-    arg_list = [argus.decode_args(g, 1, qs[l], pools, codec_row, tables[l], lens, NPAGES, scale, out=outs[l])
-                for l in range(LAYERS)]
+    # layer after layer: no call writes another's inputs, so each decode grid
+    # may start during its predecessor's tail (programmatic dependent launch)
+    arg_list = [argus.decode_args(g, 1, qs[l], pools, codec_row, tables[l], lens, NPAGES, scale, out=outs[l],
+                                  pdl=True) for l in range(LAYERS)]
     ws_bytes = max(argus.decode_workspace_bytes(a) for a in arg_list)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
@@ -235,7 +320,7 @@ def run_gpu(args, rank, world):
     q_dev = torch.empty((LAYERS, 1, HQ, D), dtype=torch.float16, device=dev)
     out_dev = torch.empty((LAYERS, 1, HQ, D), dtype=torch.float16, device=dev)
     e2e_args = [argus.decode_args(g, 1, q_dev[l], pools, codec_row, tables[l], lens, NPAGES, scale,
-                                  out=out_dev[l]) for l in range(LAYERS)]
+                                  out=out_dev[l], pdl=True) for l in range(LAYERS)]
 
     def e2e_step():
         q_dev.copy_(q_host, non_blocking=True)

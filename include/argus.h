@@ -160,7 +160,17 @@ typedef struct {
   float* lse2_out;            /* device [B][Hq] log2-sum-exp, or NULL */
   uint32_t* status;           /* device uint32 anomaly counter, or NULL */
   int32_t num_splits;         /* context splits per (b, KV head); 0 = automatic */
+  int32_t pdl;                /* programmatic dependent launch, see below */
 } argus_decode_args;
+
+/* args.pdl = 0: the kernels start after their stream predecessor completes
+ * (ordinary stream order; always safe).
+ * args.pdl = 1: the decode grid may start while its stream predecessor is
+ * still running, and it reads page_codec, block_table, seq_lens, sel_pages,
+ * sel_count, the pools' codes and meta BEFORE it waits for that predecessor
+ * (q is read, and every output written, after the wait).  Set it only when
+ * the predecessor does not write those inputs -- for example a previous
+ * argus_paged_decode_attn call, layer after layer.  When in doubt, 0. */
 
 /* Workspace needed by argus_paged_decode_attn for these arguments: fp32
  * partial outputs and log2-sum-exp values of the context splits.  Its contents

@@ -38,10 +38,18 @@ namespace argus {
 namespace decode {
 
 constexpr int kChunk = 16;
-constexpr int kConsumerWarps = 4;
-constexpr int kNC = 2;  // chunks a consumer warp processes together per stage
-constexpr int kChunksPerStage = kConsumerWarps * kNC;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kChunksPerStage = 8;
+
+// Consumer warps per CTA: head_dim 64 runs 4 warps of two chunks per stage
+// (two CTAs per SM; a second chunk in flight per warp hides MMA latency);
+// head_dim 128 runs 8 warps of one chunk (one CTA per SM, the ring fills
+// shared memory, so latency is hidden by warps instead).
+template <int D>
+struct Warps {
+  static constexpr int kConsumer = (D == 64) ? 4 : 8;
+  static constexpr int kNC = kChunksPerStage / kConsumer;  // chunks per warp and stage
+  static constexpr int kThreads = 32 * (kConsumer + 1);
+};
 constexpr int kMaxG = 8;
 constexpr int kMaxSplits = 512;  // bounds the split combine's per-thread loads
 constexpr int kFoldThreads = 256;
@@ -68,6 +76,7 @@ struct Params {
   uint32_t* status;
   int cps;         // chunks per split, a multiple of kChunksPerStage
   int num_splits;  // grid.x
+  int pdl;         // launch the decode grid with programmatic stream serialisation
   float* part_o;   // [B][Hkv][num_splits][G][D]
   float* part_lse; // [B][Hkv][num_splits][G]
 };
@@ -99,8 +108,9 @@ struct Layout {
   static constexpr int kMinBlocks = (D == 128) ? 1 : 2;  // by shared memory
 };
 
+template <int CW>
 __device__ __forceinline__ void consumer_bar() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory");
 }
 
 __device__ __forceinline__ int codec_family(int codec) { return codec == ARGUS_BF16 ? 1 : 0; }
@@ -133,28 +143,27 @@ __device__ __forceinline__ void load_k_frags(int codec, const uint8_t* chunk, in
         a[2 * i + 1][rr] = prmt(x.y, x.w, 0x5410);
         a[2 * i + 1][2 + rr] = prmt(x.y, x.w, 0x7632);
       }
-    } else if (codec == ARGUS_FP8_E4M3) {
+    } else if (codec == ARGUS_FP8_E4M3 || codec == ARGUS_INT8) {
+      // byte codes: lane t holds dims [64j + 16t, 64j + 16t + 16); word cc of
+      // that run feeds k-chunk 4j + cc (bytes 0,1 -> k 2t, 2t+1; bytes 2,3 ->
+      // k 2t+8, 2t+9), matching the query fragments qf8.  16-byte loads halve
+      // the shared-memory wavefronts of the 8-byte layout.
 #pragma unroll
-      for (int i = 0; i < L::kNI; ++i) {
-        const uint2 x = *reinterpret_cast<const uint2*>(chunk + L::kOffK + row * D + 32 * i + 8 * t);
-        const uint32_t u = prmt(x.x, x.y, 0x5140);  // e0 e4 e1 e5
-        const uint32_t v = prmt(x.x, x.y, 0x7362);  // e2 e6 e3 e7
-        a[2 * i][rr] = e4m3x2_to_f16x2(u);
-        a[2 * i][2 + rr] = e4m3x2_to_f16x2(u >> 16);
-        a[2 * i + 1][rr] = e4m3x2_to_f16x2(v);
-        a[2 * i + 1][2 + rr] = e4m3x2_to_f16x2(v >> 16);
-      }
-    } else if (codec == ARGUS_INT8) {
+      for (int j = 0; j < D / 64; ++j) {
+        const uint4 x = *reinterpret_cast<const uint4*>(chunk + L::kOffK + row * D + 64 * j + 16 * t);
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-      for (int i = 0; i < L::kNI; ++i) {
-        const uint2 x = *reinterpret_cast<const uint2*>(chunk + L::kOffK + row * D + 32 * i + 8 * t);
-        const uint32_t u = prmt(x.x, x.y, 0x5140) ^ 0x80808080u;
-        const uint32_t v = prmt(x.x, x.y, 0x7362) ^ 0x80808080u;
-        const uint32_t bias = 0x64806480u;  // 1152 = 1024 + 128
-        a[2 * i][rr] = hsub2_u32(f16_magic_pair(u, 0x4140), bias);
-        a[2 * i][2 + rr] = hsub2_u32(f16_magic_pair(u, 0x4342), bias);
-        a[2 * i + 1][rr] = hsub2_u32(f16_magic_pair(v, 0x4140), bias);
-        a[2 * i + 1][2 + rr] = hsub2_u32(f16_magic_pair(v, 0x4342), bias);
+        for (int cc = 0; cc < 4; ++cc) {
+          if (codec == ARGUS_FP8_E4M3) {
+            a[4 * j + cc][rr] = e4m3x2_to_f16x2(w[cc]);
+            a[4 * j + cc][2 + rr] = e4m3x2_to_f16x2(w[cc] >> 16);
+          } else {
+            const uint32_t u = w[cc] ^ 0x80808080u;
+            const uint32_t bias = 0x64806480u;  // 1152 = 1024 + 128
+            a[4 * j + cc][rr] = hsub2_u32(f16_magic_pair(u, 0x4140), bias);
+            a[4 * j + cc][2 + rr] = hsub2_u32(f16_magic_pair(u, 0x4342), bias);
+          }
+        }
       }
     } else {  // INT4 group 32
 #pragma unroll
@@ -288,8 +297,9 @@ __device__ __forceinline__ void load_v_frags(int codec, const uint8_t* chunk, in
 template <int D, int CODEC, int NCG, bool BF>
 __device__ __forceinline__ void group_scores(const uint8_t* const* cptr, const ChunkDesc* dsc, int r, int t,
                                              const uint32_t (&qf)[D / 16][2], const uint32_t (&qb)[D / 16][2],
+                                             const uint32_t (&qf8)[D / 16][2],
                                              const float (&qgs)[D / 32][2], float f0h, float f1h,
-                                             float scale_log2, float (&sv)[kNC][4], int c0) {
+                                             float scale_log2, float (*sv)[4], int c0) {
   constexpr int KC = D / 16;
   uint32_t a[NCG][KC][4];
   float kz[NCG][2][D / 32][2];
@@ -333,6 +343,8 @@ __device__ __forceinline__ void group_scores(const uint8_t* const* cptr, const C
 #pragma unroll
       for (int c = 0; c < NCG; ++c) {
         if constexpr (BF) mma_bf16(sc[c][k & 1], a[c][k][0], a[c][k][1], a[c][k][2], a[c][k][3], qb[k][0], qb[k][1]);
+        else if constexpr (CODEC == ARGUS_FP8_E4M3 || CODEC == ARGUS_INT8)
+          mma_f16(sc[c][k & 1], a[c][k][0], a[c][k][1], a[c][k][2], a[c][k][3], qf8[k][0], qf8[k][1]);
         else mma_f16(sc[c][k & 1], a[c][k][0], a[c][k][1], a[c][k][2], a[c][k][3], qf[k][0], qf[k][1]);
       }
 #pragma unroll
@@ -390,8 +402,10 @@ __device__ __forceinline__ void group_pv(const uint8_t* const* cptr, int r, int 
 }
 
 template <int D, bool QBF16, int FAM>
-__global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
+__global__ void __launch_bounds__(Warps<D>::kThreads, Layout<D>::kMinBlocks)
     decode_kernel(const Params p) {
+  constexpr int kConsumerWarps = Warps<D>::kConsumer;
+  constexpr int kNC = Warps<D>::kNC;
   using L = Layout<D>;
   constexpr int KC = D / 16;
   constexpr int MB = D / 16;
@@ -412,6 +426,31 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
   const int Hkv = p.Hkv, G = p.G, P = p.P;
   const int cpp = P / kChunk;
   const bool sparse = p.sel_pages != nullptr;
+
+  // Codec and slot of logical page `page` (both -1 outside the table).
+  auto lookup = [&](int page, int& codec, long long& slot) {
+    codec = -1;
+    slot = -1;
+    if (page >= 0 && page < p.max_pages) {
+      codec = p.page_codec[(size_t)b * p.max_pages + page];
+      slot = p.block_table[(size_t)b * p.max_pages + page];
+    }
+  };
+  // The producer lane's first chunk: its selection entry, or its codec and
+  // slot, requested before the sequence length arrives (indices stay inside
+  // their arrays whatever the length turns out to be).
+  const size_t sel_row = ((size_t)b * Hkv + h) * (size_t)p.sel_width;
+  int pf_page = -1, pf_codec = -1;
+  long long pf_slot = -1;
+  if (warp == kConsumerWarps) {
+    const int v = (split * p.cps + lane) / cpp;
+    if (sparse) {
+      pf_page = (v < p.sel_width) ? p.sel_pages[sel_row + v] : -1;
+    } else {
+      pf_page = v;
+      lookup(pf_page, pf_codec, pf_slot);
+    }
+  }
 
   int seq_len = p.seq_lens[b];
   seq_len = max(0, min(seq_len, p.max_pages * P));
@@ -460,11 +499,28 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    // Chunks are translated 32 at a time, one per lane, so that the block-table
-    // and scale lookups of eight stages cost two dependent round trips; the
-    // lanes then issue their chunk's bulk copies stage by stage.
+    // Chunks are translated 32 at a time, one per lane.  Lookups run one batch
+    // ahead of the copies: while a batch's stages are issued, the next batch's
+    // codec and slot loads and the selection entries of the batch after that
+    // are in flight.  The first batch's lookups were issued before the
+    // sequence length was known.
+    int cur_page = pf_page, cur_codec = pf_codec;
+    long long cur_slot = pf_slot;
+    if (sparse) lookup(cur_page, cur_codec, cur_slot);
+    auto page_at = [&](int base) -> int {
+      if (base >= n_local) return -1;
+      const int v = (c_begin + base + lane) / cpp;
+      if (!sparse) return v;
+      return (v < p.sel_width) ? p.sel_pages[sel_row + v] : -1;
+    };
+    int nxt_page = page_at(32);
     bool stop = false;
     for (int base = 0; base < n_local && !stop; base += 32) {
+      int nxt_codec = -1;
+      long long nxt_slot = -1;
+      if (base + 32 < n_local) lookup(nxt_page, nxt_codec, nxt_slot);
+      const int nn_page = page_at(base + 64);
+
       ChunkDesc d;
       d.codec = -1;
       d.n_valid = 0;
@@ -472,24 +528,21 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
       d.vscale = 1.f;
       uint32_t kv_bytes = 0, m_bytes = 0;
       const uint8_t *srcK = nullptr, *srcV = nullptr, *srcMK = nullptr, *srcMV = nullptr;
-      const int ci = c_begin + base + lane;
       if (base + lane < n_local) {
-        const int v = ci / cpp, cip = ci - v * cpp;
-        int page = v;
+        const int ci = c_begin + base + lane;
+        const int cip = ci - (ci / cpp) * cpp;
+        const int page = cur_page;
         bool good = true;
-        if (sparse) {
-          page = p.sel_pages[((size_t)b * Hkv + h) * p.sel_width + v];
-          if (page < 0 || page >= n_pages_b) {
-            good = false;
-            if (cip == 0 && p.status) atomicAdd(p.status, 1u);
-          }
+        if (sparse && (page < 0 || page >= n_pages_b)) {
+          good = false;
+          if (cip == 0 && p.status) atomicAdd(p.status, 1u);
         }
         if (good) {
           const int tok0 = page * P + cip * kChunk;
           const int nv = min(kChunk, seq_len - tok0);
           if (nv > 0) {
-            const int codec = p.page_codec[(size_t)b * p.max_pages + page];
-            const long long slot_id = p.block_table[(size_t)b * p.max_pages + page];
+            const int codec = cur_codec;
+            const long long slot_id = cur_slot;
             bool ok = codec >= 0 && codec <= 4 && p.codes[codec] != nullptr;
             if (ok) {
               const int fam = codec_family(codec);
@@ -505,6 +558,7 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
               srcK = p.codes[codec] + rk * rowb;
               srcV = p.codes[codec] + rv * rowb;
               kv_bytes = kChunk * rowb;
+              d.codec = codec;
               if (codec == ARGUS_INT4_G32) {
                 srcMK = p.meta[codec] + rk * (L::kNI * 4);
                 srcMV = p.meta[codec] + rv * (L::kNI * 4);
@@ -514,7 +568,6 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
                 d.kscale = ms[((size_t)slot_id * 2 + 0) * Hkv + h];
                 d.vscale = ms[((size_t)slot_id * 2 + 1) * Hkv + h];
               }
-              d.codec = codec;
               d.n_valid = nv;
             }
           }
@@ -558,6 +611,10 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
         __syncwarp();
         if (lane == 0) mbar_arrive(&full[slot]);
       }
+      cur_page = nxt_page;
+      cur_codec = nxt_codec;
+      cur_slot = nxt_slot;
+      nxt_page = nn_page;
     }
     return;
   }
@@ -572,6 +629,7 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
   const int r = lane >> 2, t = lane & 3;
   // query fragments (B operand of Q.K: k = head_dim, n = query head r)
   uint32_t qf[KC][2], qb[KC][2];
+  uint32_t qf8[KC][2];  // qf in the byte-codec dim order (see load_k_frags)
   float qgs[D / 32][2];  // per-group query sums of heads 2t, 2t+1 (fp16 domain)
   float qscale_h0 = 1.f, qscale_h1 = 1.f;  // 2^-e of heads 2t, 2t+1 (bf16 q in fp16 MMAs)
   {
@@ -630,6 +688,29 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
         qgs[i][0] = __shfl_sync(0xffffffffu, part, 4 * (2 * t));
         qgs[i][1] = __shfl_sync(0xffffffffu, part, 4 * (2 * t + 1));
       }
+      // the same query values (same fp16 rounding) in the byte-codec order
+#pragma unroll
+      for (int j = 0; j < D / 64; ++j) {
+        uint4 x[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        if (r < G) {
+          const uint4* qp = reinterpret_cast<const uint4*>(
+              reinterpret_cast<const uint16_t*>(p.q) + (row0 + r) * D + 64 * j + 16 * t);
+          x[0] = qp[0];
+          x[1] = qp[1];
+        }
+        const uint32_t wv[8] = {x[0].x, x[0].y, x[0].z, x[0].w, x[1].x, x[1].y, x[1].z, x[1].w};
+        float e16[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const uint16_t bits = (wv[e / 2] >> (16 * (e & 1))) & 0xFFFFu;
+          e16[e] = (QBF16 ? __uint_as_float((uint32_t)bits << 16) : __half2float(__ushort_as_half(bits))) * e_scale;
+        }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          qf8[4 * j + cc][0] = pack_f16x2(e16[4 * cc], e16[4 * cc + 1]);
+          qf8[4 * j + cc][1] = pack_f16x2(e16[4 * cc + 2], e16[4 * cc + 3]);
+        }
+      }
     }
   }
 
@@ -661,27 +742,29 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
       // ---- scores S^T[token][head] = K . q; a group whose chunks share one
       // codec runs as straight-line code so that all MMAs overlap
       float sv[kNC][4];
-      const bool same = (dsc[0].codec >= 0) && (dsc[1].codec == dsc[0].codec);
+      const bool same = (kNC == 2) && (dsc[0].codec >= 0) && (dsc[kNC - 1].codec == dsc[0].codec);
       const float fq0 = qscale_h0, fq1 = qscale_h1;
       auto scores = [&](int codec, int c0, int ncg) {
         const uint8_t* const* cp = cptr + c0;
         const ChunkDesc* dd = dsc + c0;
-        if (ncg == 2) {
-          switch (codec) {
-            case ARGUS_FP16: group_scores<D, ARGUS_FP16, 2, false>(cp, dd, r, t, qf, qb, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-            case ARGUS_BF16: group_scores<D, ARGUS_BF16, 2, true>(cp, dd, r, t, qf, qb, qgs, 1.f, 1.f, p.scale_log2, sv, c0); break;
-            case ARGUS_FP8_E4M3: group_scores<D, ARGUS_FP8_E4M3, 2, false>(cp, dd, r, t, qf, qb, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-            case ARGUS_INT8: group_scores<D, ARGUS_INT8, 2, false>(cp, dd, r, t, qf, qb, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-            default: group_scores<D, ARGUS_INT4_G32, 2, false>(cp, dd, r, t, qf, qb, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+        if constexpr (kNC == 2) {
+          if (ncg == 2) {
+            switch (codec) {
+              case ARGUS_FP16: group_scores<D, ARGUS_FP16, 2, false>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+              case ARGUS_BF16: group_scores<D, ARGUS_BF16, 2, true>(cp, dd, r, t, qf, qb, qf8, qgs, 1.f, 1.f, p.scale_log2, sv, c0); break;
+              case ARGUS_FP8_E4M3: group_scores<D, ARGUS_FP8_E4M3, 2, false>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+              case ARGUS_INT8: group_scores<D, ARGUS_INT8, 2, false>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+              default: group_scores<D, ARGUS_INT4_G32, 2, false>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+            }
+            return;
           }
-        } else {
-          switch (codec) {
-            case ARGUS_FP16: group_scores<D, ARGUS_FP16, 1, false>(cp, dd, r, t, qf, qb, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-            case ARGUS_BF16: group_scores<D, ARGUS_BF16, 1, true>(cp, dd, r, t, qf, qb, qgs, 1.f, 1.f, p.scale_log2, sv, c0); break;
-            case ARGUS_FP8_E4M3: group_scores<D, ARGUS_FP8_E4M3, 1, false>(cp, dd, r, t, qf, qb, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-            case ARGUS_INT8: group_scores<D, ARGUS_INT8, 1, false>(cp, dd, r, t, qf, qb, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-            default: group_scores<D, ARGUS_INT4_G32, 1, false>(cp, dd, r, t, qf, qb, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-          }
+        }
+        switch (codec) {
+          case ARGUS_FP16: group_scores<D, ARGUS_FP16, 1, false>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+          case ARGUS_BF16: group_scores<D, ARGUS_BF16, 1, true>(cp, dd, r, t, qf, qb, qf8, qgs, 1.f, 1.f, p.scale_log2, sv, c0); break;
+          case ARGUS_FP8_E4M3: group_scores<D, ARGUS_FP8_E4M3, 1, false>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+          case ARGUS_INT8: group_scores<D, ARGUS_INT8, 1, false>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+          default: group_scores<D, ARGUS_INT4_G32, 1, false>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
         }
       };
       if (same) {
@@ -722,12 +805,14 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
         sigma = vmax;
       }
       const float g0 = al0 * gs, g1 = al1 * gs;
+      if (__any_sync(0xffffffffu, g0 != 1.f || g1 != 1.f)) {  // most chunks move neither max nor sigma
 #pragma unroll
-      for (int j = 0; j < MB; ++j) {
-        acc[j][0] *= g0;
-        acc[j][1] *= g1;
-        acc[j][2] *= g0;
-        acc[j][3] *= g1;
+        for (int j = 0; j < MB; ++j) {
+          acc[j][0] *= g0;
+          acc[j][1] *= g1;
+          acc[j][2] *= g0;
+          acc[j][3] *= g1;
+        }
       }
       float pw[kNC][4];
       bool skip[kNC];
@@ -750,22 +835,24 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
       // ---- O^T[dim][head] += V^T . (w P)^T
       auto pv = [&](int codec, int c0, int ncg) {
         const uint8_t* const* cp = cptr + c0;
-        if (ncg == 2) {
-          switch (codec) {
-            case ARGUS_FP16: group_pv<D, ARGUS_FP16, 2, false>(cp, r, t, pw + c0, skip + c0, acc); break;
-            case ARGUS_BF16: group_pv<D, ARGUS_BF16, 2, true>(cp, r, t, pw + c0, skip + c0, acc); break;
-            case ARGUS_FP8_E4M3: group_pv<D, ARGUS_FP8_E4M3, 2, false>(cp, r, t, pw + c0, skip + c0, acc); break;
-            case ARGUS_INT8: group_pv<D, ARGUS_INT8, 2, false>(cp, r, t, pw + c0, skip + c0, acc); break;
-            default: group_pv<D, ARGUS_INT4_G32, 2, false>(cp, r, t, pw + c0, skip + c0, acc); break;
+        if constexpr (kNC == 2) {
+          if (ncg == 2) {
+            switch (codec) {
+              case ARGUS_FP16: group_pv<D, ARGUS_FP16, 2, false>(cp, r, t, pw + c0, skip + c0, acc); break;
+              case ARGUS_BF16: group_pv<D, ARGUS_BF16, 2, true>(cp, r, t, pw + c0, skip + c0, acc); break;
+              case ARGUS_FP8_E4M3: group_pv<D, ARGUS_FP8_E4M3, 2, false>(cp, r, t, pw + c0, skip + c0, acc); break;
+              case ARGUS_INT8: group_pv<D, ARGUS_INT8, 2, false>(cp, r, t, pw + c0, skip + c0, acc); break;
+              default: group_pv<D, ARGUS_INT4_G32, 2, false>(cp, r, t, pw + c0, skip + c0, acc); break;
+            }
+            return;
           }
-        } else {
-          switch (codec) {
-            case ARGUS_FP16: group_pv<D, ARGUS_FP16, 1, false>(cp, r, t, pw + c0, skip + c0, acc); break;
-            case ARGUS_BF16: group_pv<D, ARGUS_BF16, 1, true>(cp, r, t, pw + c0, skip + c0, acc); break;
-            case ARGUS_FP8_E4M3: group_pv<D, ARGUS_FP8_E4M3, 1, false>(cp, r, t, pw + c0, skip + c0, acc); break;
-            case ARGUS_INT8: group_pv<D, ARGUS_INT8, 1, false>(cp, r, t, pw + c0, skip + c0, acc); break;
-            default: group_pv<D, ARGUS_INT4_G32, 1, false>(cp, r, t, pw + c0, skip + c0, acc); break;
-          }
+        }
+        switch (codec) {
+          case ARGUS_FP16: group_pv<D, ARGUS_FP16, 1, false>(cp, r, t, pw + c0, skip + c0, acc); break;
+          case ARGUS_BF16: group_pv<D, ARGUS_BF16, 1, true>(cp, r, t, pw + c0, skip + c0, acc); break;
+          case ARGUS_FP8_E4M3: group_pv<D, ARGUS_FP8_E4M3, 1, false>(cp, r, t, pw + c0, skip + c0, acc); break;
+          case ARGUS_INT8: group_pv<D, ARGUS_INT8, 1, false>(cp, r, t, pw + c0, skip + c0, acc); break;
+          default: group_pv<D, ARGUS_INT4_G32, 1, false>(cp, r, t, pw + c0, skip + c0, acc); break;
         }
       };
       if (same) {
@@ -787,7 +874,7 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
     l1 += __shfl_xor_sync(0xffffffffu, l1, o);
   }
   if (sigma == 0.f) sigma = 1.f;  // nothing accumulated
-  consumer_bar();  // every warp is done with the stage ring; reuse it
+  consumer_bar<kConsumerWarps>();  // every warp is done with the stage ring; reuse it
   float* red_o = reinterpret_cast<float*>(smem);               // [warps][8][D]
   float* red_ml = red_o + kConsumerWarps * kMaxG * D;          // [warps][8][2]
   float* red_w = red_ml + kConsumerWarps * kMaxG * 2;          // [warps][8] merge weights
@@ -806,7 +893,7 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
     red_ml[(warp * kMaxG + 2 * t + 1) * 2 + 0] = m1;
     red_ml[(warp * kMaxG + 2 * t + 1) * 2 + 1] = l1;
   }
-  consumer_bar();
+  consumer_bar<kConsumerWarps>();
   const int tid = threadIdx.x;
   const int nthr = kConsumerWarps * 32;
   if (tid < G) {  // per head: weight of each warp's partial, and the CTA's lse
@@ -826,7 +913,7 @@ __global__ void __launch_bounds__(kThreads, Layout<D>::kMinBlocks)
     for (int w = 0; w < kConsumerWarps; ++w) red_w[w * kMaxG + g] = f[w] * inv;
     red_lse[g] = (Lsum > 0.f) ? M + log2f(Lsum) : -INFINITY;
   }
-  consumer_bar();
+  consumer_bar<kConsumerWarps>();
   const bool direct = (n_active == 1);
   const size_t bh = (size_t)b * Hkv + h;
   float* po_bh = p.part_o + bh * p.num_splits * G * D;
@@ -1054,14 +1141,14 @@ static argus_status launch_t(const Params& p, dim3 grid, cudaStream_t s) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(Warps<D>::kThreads);
   cfg.dynamicSmemBytes = L::kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = p.pdl ? 1 : 0;
   cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<D, QBF16, FAM>, p);
   if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "argus_paged_decode_attn: %s", cudaGetErrorString(e));
   if (p.num_splits > 1) {
@@ -1069,6 +1156,8 @@ static argus_status launch_t(const Params& p, dim3 grid, cudaStream_t s) {
     fc.gridDim = dim3(p.Hkv * p.G, p.B);
     fc.blockDim = dim3(kFoldThreads);
     fc.dynamicSmemBytes = 0;
+    fc.attrs = attr;  // the combine always overlaps its decode grid's tail
+    fc.numAttrs = 1;
     e = cudaLaunchKernelEx(&fc, decode_fold_kernel<D>, p);
     if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "argus_paged_decode_attn (combine): %s", cudaGetErrorString(e));
   }
@@ -1140,6 +1229,7 @@ static argus_status run(const argus_decode_args* a, const Plan& pl, void* ws, vo
   p.status = a->status;
   p.cps = pl.cps;
   p.num_splits = pl.num_splits;
+  p.pdl = a->pdl ? 1 : 0;
   p.part_o = static_cast<float*>(ws);
   p.part_lse = ws ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.part_o_bytes) : nullptr;
   dim3 grid(pl.num_splits, a->g.n_kv_heads, a->batch);

@@ -177,3 +177,52 @@ def test_unsupported_and_invalid_arguments():
     with pytest.raises(argus.ArgusError) as e:
         argus.paged_decode_attn(args, small)
     assert e.value.status == 3
+
+
+def test_layer_chain_with_programmatic_dependent_launch():
+    """Back-to-back calls with pdl=1 (each grid may start in its predecessor's
+    tail) give the same bits as ordinary stream order, eagerly and replayed
+    from a CUDA graph, and match the oracle."""
+    Hq, Hkv, D, P = 14, 2, 64, 64
+    n = 16
+    pc = W.mixed_tier_codecs(n).reshape(1, n)
+    cases = [build_case(Hq, Hkv, D, P, [n * P - 7 * l], pc, W.FP16, seed=300 + l, outliers=True) for l in range(4)]
+    want = []
+    for c in cases:
+        out, out32, lse, _ = run_decode(c, num_splits=0)
+        _check(c, out, out32, lse)
+        want.append(out32.clone())
+    outs = [torch.empty_like(w) for w in want]
+    args = [argus.decode_args(c.g, c.B, c.q, c.pools, c.d_codec, c.d_table, c.d_lens, c.max_pages, c.scale,
+                              out_f32=o, pdl=True) for c, o in zip(cases, outs)]
+    ws = torch.empty(max(argus.decode_workspace_bytes(a) for a in args), dtype=torch.uint8, device=DEV)
+    stream = torch.cuda.Stream(device=DEV)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            for a in args:
+                argus.paged_decode_attn(a, ws, stream=stream)
+        stream.synchronize()
+        for o, w in zip(outs, want):
+            assert torch.equal(o, w)
+            o.zero_()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for a in args:
+                argus.paged_decode_attn(a, ws, stream=stream)
+        graph.replay()
+        graph.replay()
+    torch.cuda.synchronize()
+    for o, w in zip(outs, want):
+        assert torch.equal(o, w)
+
+
+@pytest.mark.parametrize("codec", [W.FP8_E4M3, W.INT8])
+@pytest.mark.parametrize("Hkv,D", [(1, 64), (3, 128), (40, 64)])
+def test_scale_rows_loaded_by_the_producer(codec, Hkv, D):
+    """Odd KV-head counts, or scale rows wider than the chunk's meta area,
+    take the producer-side scale loads instead of the bulk-copied row."""
+    P = 16
+    pc = np.full((2, 8), codec)
+    c = build_case(2 * Hkv, Hkv, D, P, [100, 128], pc, W.FP16, seed=400 + Hkv + codec, outliers=True)
+    out, out32, lse, _ = run_decode(c, num_splits=2)
+    _check(c, out, out32, lse)
