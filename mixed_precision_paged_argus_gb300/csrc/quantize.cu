@@ -19,6 +19,7 @@
 // then encode), the second read served from L2.  Loads and stores are 16-byte
 // per lane and contiguous across the group.
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -104,42 +105,60 @@ __device__ __forceinline__ float quot_rint(float x, float s, float r) {
   return (fabsf(f - 0.5f) < 0x1p-12f) ? x / s : y;
 }
 
-// Encode 8 values of one 16-byte source vector and store them.
-template <int CODEC, bool SBF16>
-__device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& raw, float scale,
+//  INT4 scale: fp16_sat(RN(a / 15)).  a * RN(1/15) is within 3 ulp of RN(a/15);
+//  the fp16 rounding can only differ within a few ulps of an fp16 midpoint
+//  (fp32 mantissa bits below the fp16 ones equal to 0x1000) or in fp16's
+//  subnormal range, where the division itself is taken.
+__device__ __forceinline__ float scale_div15(float a) {
+  const float y = a * (1.f / 15.f);
+  const uint32_t low = __float_as_uint(y) & 0x1FFFu;
+  const bool near = (low - 0x1000u + 8u) <= 16u;
+  const bool small = fabsf(y) < 0x1p-14f;
+  return fp16_sat((near || small) ? a / 15.f : y);
+}
+
+// Encode 8 values of one 16-byte source vector and store them; with DEQ the
+// stored values are also decoded into deq (for the compressed key).  rscale is
+// RN(1 / scale) (FP8, INT8).
+template <int CODEC, bool SBF16, bool DEQ>
+__device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& raw, float scale, float rscale,
                                              uint8_t* dcodes, size_t vec, bool valid, float (&deq)[8],
                                              uint8_t* dmeta_row, int lane_in_group) {
   if (CODEC == ARGUS_FP16 || CODEC == ARGUS_BF16) {
     const uint4 z = make_uint4(0, 0, 0, 0);
     reinterpret_cast<uint4*>(dcodes)[vec] = valid ? raw : z;
+    if (DEQ) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) deq[e] = valid ? f[e] : 0.f;
+      for (int e = 0; e < 8; ++e) deq[e] = valid ? f[e] : 0.f;
+    }
   } else if (CODEC == ARGUS_FP8_E4M3) {
     uint32_t w[2] = {0u, 0u};
     if (valid && scale > 0.f) {
-      const float r = 1.f / scale;
 #pragma unroll
       for (int e = 0; e < 8; e += 2) {
-        const uint32_t two = f32x2_to_e4m3x2(quot_e4m3(f[e], scale, r), quot_e4m3(f[e + 1], scale, r));
+        const uint32_t two = f32x2_to_e4m3x2(quot_e4m3(f[e], scale, rscale), quot_e4m3(f[e + 1], scale, rscale));
         w[e / 4] |= two << (16 * ((e / 2) & 1));
       }
     }
+    if (DEQ) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) deq[e] = e4m3_value(w[e / 4] >> (8 * (e & 3))) * scale;
+      for (int e = 0; e < 8; ++e) deq[e] = e4m3_value(w[e / 4] >> (8 * (e & 3))) * scale;
+    }
     reinterpret_cast<uint2*>(dcodes)[vec] = make_uint2(w[0], w[1]);
   } else if (CODEC == ARGUS_INT8) {
     uint32_t w[2] = {0u, 0u};
     if (valid && scale > 0.f) {
-      const float r = 1.f / scale;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        int q = __float2int_rn(quot_rint(f[e], scale, r));
+        int q = __float2int_rn(quot_rint(f[e], scale, rscale));
         q = max(-127, min(127, q));
         w[e / 4] |= (uint32_t)(q & 0xFF) << (8 * (e & 3));
       }
     }
+    if (DEQ) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) deq[e] = (float)(int8_t)((w[e / 4] >> (8 * (e & 3))) & 0xFF) * scale;
+      for (int e = 0; e < 8; ++e) deq[e] = (float)(int8_t)((w[e / 4] >> (8 * (e & 3))) & 0xFF) * scale;
+    }
     reinterpret_cast<uint2*>(dcodes)[vec] = make_uint2(w[0], w[1]);
   } else {  // INT4: the 4 threads of a 32-element group cooperate
     float lo = f[0], hi = f[0];
@@ -153,10 +172,10 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
     lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 2));
     hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, 2));
     const float z = fp16_sat(lo);
-    const float s = fp16_sat((hi - z) / 15.f);
+    const float s = scale_div15(hi - z);
     uint32_t w = 0u;
     if (valid && s > 0.f) {
-      const float r = 1.f / s;
+      const float r = __frcp_rn(s);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         int q = __float2int_rn(quot_rint(f[e] - z, s, r));
@@ -165,8 +184,10 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
       }
     }
     const float zz = valid ? z : 0.f, ss = valid ? s : 0.f;
+    if (DEQ) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) deq[e] = fmaf((float)((w >> (4 * e)) & 0xF), ss, zz);
+      for (int e = 0; e < 8; ++e) deq[e] = fmaf((float)((w >> (4 * e)) & 0xF), ss, zz);
+    }
     reinterpret_cast<uint32_t*>(dcodes)[vec] = w;
     if ((lane_in_group & 3) == 0) {
       const __half2 sz = __halves2half2(__float2half_rn(ss), __float2half_rn(zz));
@@ -239,6 +260,7 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_kernel(const QParams p) 
       scale = amax > 0.f ? amax / (CODEC == ARGUS_FP8_E4M3 ? 448.f : 127.f) : 0.f;
       if (g == 0) reinterpret_cast<float*>(p.dst_meta)[unit_dst] = scale;
     }
+    const float rscale = scale > 0.f ? 1.f / scale : 0.f;
 
     float ck[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     auto do_vec = [&](int v, const uint4& raw) {
@@ -251,7 +273,7 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_kernel(const QParams p) 
         const int row = v / VPR, grp = (v % VPR) / 4;
         meta_row = p.dst_meta + ((unit_dst * P + row) * (D / 32) + grp) * 4;
       }
-      encode_store<CODEC, SBF16>(f, raw, scale, dcodes, (size_t)v, valid_v, deq, meta_row, g);
+      encode_store<CODEC, SBF16, true>(f, raw, scale, rscale, dcodes, (size_t)v, valid_v, deq, meta_row, g);
       if (valid_v) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) ck[e] += deq[e];
@@ -397,27 +419,36 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_small_kernel(const QPara
         scale = amax > 0.f ? amax / (CODEC == ARGUS_FP8_E4M3 ? 448.f : 127.f) : 0.f;
         if (lane == 0) reinterpret_cast<float*>(p.dst_meta)[cu.dst] = scale;
       }
+      const float rscale = scale > 0.f ? 1.f / scale : 0.f;
       float ck[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // decoding the stored values is needed only for a compressed key
+      auto encode_unit = [&](auto deq_tag) {
+        constexpr bool DEQ = decltype(deq_tag)::value;
 #pragma unroll
-      for (int k = 0; k < kRegVecs; ++k) {
-        const int v = lane + 32 * k;
-        if (v < nvec) {
-          float f[8], deq[8];
-          unpack8<SBF16>(cur[k], f);
-          uint8_t* meta_row = nullptr;
-          if (CODEC == ARGUS_INT4_G32) {
-            const int row = v / VPR, grp = (v % VPR) / 4;
-            meta_row = p.dst_meta + ((cu.dst * P + row) * (D / 32) + grp) * 4;
-          }
-          const bool valid_v = v < nvalid_vec;
-          encode_store<CODEC, SBF16>(f, cur[k], scale, dcodes, (size_t)v, valid_v, deq, meta_row, lane);
-          if (want_ck && valid_v) {
+        for (int k = 0; k < kRegVecs; ++k) {
+          const int v = lane + 32 * k;
+          if (v < nvec) {
+            float f[8], deq[8];
+            unpack8<SBF16>(cur[k], f);
+            uint8_t* meta_row = nullptr;
+            if (CODEC == ARGUS_INT4_G32) {
+              const int row = v / VPR, grp = (v % VPR) / 4;
+              meta_row = p.dst_meta + ((cu.dst * P + row) * (D / 32) + grp) * 4;
+            }
+            const bool valid_v = v < nvalid_vec;
+            encode_store<CODEC, SBF16, DEQ>(f, cur[k], scale, rscale, dcodes, (size_t)v, valid_v, deq, meta_row,
+                                            lane);
+            if (DEQ && valid_v) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ck[e] += deq[e];
+              for (int e = 0; e < 8; ++e) ck[e] += deq[e];
+            }
           }
         }
-      }
-      if (want_ck && cu.kv == 0) {
+      };
+      const bool ck_unit = want_ck && cu.kv == 0;
+      if (ck_unit) encode_unit(std::true_type{});
+      else encode_unit(std::false_type{});
+      if (ck_unit) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           float x = ck[e];
