@@ -84,25 +84,26 @@ __device__ __forceinline__ float group_reduce(float v, float* sh) {
 // Quotients for the encoders.  The codes are defined on RN(x / s) (IEEE fp32
 // division).  x * RN(1/s) is within 1.5 ulp of RN(x / s), so it selects the
 // same code unless it lies within a few ulps of a rounding boundary of the
-// target format; those rare elements (and e4m3's subnormal range) take the
-// IEEE division itself.  The codes are therefore identical to dividing every
-// element.
+// target format.  The encoders form all eight products of a vector, and only
+// when one of them is that close (or, for e4m3, in the subnormal range) redo
+// the vector with IEEE divisions, on an explicit branch so that the common
+// path never evaluates a division.  The codes are therefore identical to
+// dividing every element.
 //  e4m3 (normal range): boundaries are the midpoints between neighbouring
 //  codes, i.e. fp32 mantissas whose 20 bits below the 3 kept bits equal 0x80000.
-__device__ __forceinline__ float quot_e4m3(float x, float s, float r) {
-  const float y = x * r;
+__device__ __forceinline__ bool e4m3_unsure(float y) {
   const uint32_t low = __float_as_uint(y) & 0xFFFFFu;
-  const bool near = (low - 0x80000u + 8u) <= 16u;
-  const bool small = fabsf(y) < 0.0157f;   // e4m3 subnormals start below 2^-6
-  return (near || small) ? x / s : y;
+  return ((low - 0x80000u + 8u) <= 16u) || (fabsf(y) < 0.0157f);  // e4m3 subnormals start below 2^-6
 }
 
 //  integer codes: boundaries are the half-integers; |y| <= 128 keeps the
-//  quotient's ulp <= 2^-17, far inside the 2^-12 guard band.
-__device__ __forceinline__ float quot_rint(float x, float s, float r) {
-  const float y = x * r;
-  const float f = y - floorf(y);
-  return (fabsf(f - 0.5f) < 0x1p-12f) ? x / s : y;
+//  quotient's ulp <= 2^-17, far inside the 2^-12 guard band.  Rounding to an
+//  integer uses the fp32 adder: for |y| < 2^22, y + 1.5 * 2^23 rounds y to the
+//  nearest integer (ties to even) and leaves it in the low mantissa bits, so
+//  neither a round nor a float-to-int conversion instruction is needed.
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+__device__ __forceinline__ bool rint_unsure(float y, float t) {  // t = y + kRoundMagic
+  return fabsf(y - (t - kRoundMagic)) > 0.5f - 0x1p-12f;
 }
 
 //  INT4 scale: fp16_sat(RN(a / 15)).  a * RN(1/15) is within 3 ulp of RN(a/15);
@@ -110,11 +111,10 @@ __device__ __forceinline__ float quot_rint(float x, float s, float r) {
 //  (fp32 mantissa bits below the fp16 ones equal to 0x1000) or in fp16's
 //  subnormal range, where the division itself is taken.
 __device__ __forceinline__ float scale_div15(float a) {
-  const float y = a * (1.f / 15.f);
+  float y = a * (1.f / 15.f);
   const uint32_t low = __float_as_uint(y) & 0x1FFFu;
-  const bool near = (low - 0x1000u + 8u) <= 16u;
-  const bool small = fabsf(y) < 0x1p-14f;
-  return fp16_sat((near || small) ? a / 15.f : y);
+  if (((low - 0x1000u + 8u) <= 16u) || fabsf(y) < 0x1p-14f) y = a / 15.f;
+  return fp16_sat(y);
 }
 
 // Encode 8 values of one 16-byte source vector and store them; with DEQ the
@@ -134,9 +134,20 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
   } else if (CODEC == ARGUS_FP8_E4M3) {
     uint32_t w[2] = {0u, 0u};
     if (valid && scale > 0.f) {
+      float y[8];
+      bool unsure = false;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        y[e] = f[e] * rscale;
+        unsure |= e4m3_unsure(y[e]);
+      }
+      if (unsure) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = f[e] / scale;
+      }
 #pragma unroll
       for (int e = 0; e < 8; e += 2) {
-        const uint32_t two = f32x2_to_e4m3x2(quot_e4m3(f[e], scale, rscale), quot_e4m3(f[e + 1], scale, rscale));
+        const uint32_t two = f32x2_to_e4m3x2(y[e], y[e + 1]);
         w[e / 4] |= two << (16 * ((e / 2) & 1));
       }
     }
@@ -148,12 +159,23 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
   } else if (CODEC == ARGUS_INT8) {
     uint32_t w[2] = {0u, 0u};
     if (valid && scale > 0.f) {
+      // clamping before rounding equals clamping the rounded value (integer bounds)
+      uint32_t t[8];
+      bool unsure = false;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        int q = __float2int_rn(quot_rint(f[e], scale, rscale));
-        q = max(-127, min(127, q));
-        w[e / 4] |= (uint32_t)(q & 0xFF) << (8 * (e & 3));
+        const float y = fminf(fmaxf(f[e] * rscale, -127.f), 127.f);
+        const float tf = y + kRoundMagic;
+        unsure |= rint_unsure(y, tf);
+        t[e] = __float_as_uint(tf);
       }
+      if (unsure) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) t[e] = __float_as_uint(fminf(fmaxf(f[e] / scale, -127.f), 127.f) + kRoundMagic);
+      }
+      // the low byte of the mantissa is the code in two's complement
+      w[0] = prmt(prmt(t[0], t[1], 0x0040), prmt(t[2], t[3], 0x0040), 0x5410);
+      w[1] = prmt(prmt(t[4], t[5], 0x0040), prmt(t[6], t[7], 0x0040), 0x5410);
     }
     if (DEQ) {
 #pragma unroll
@@ -176,12 +198,23 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
     uint32_t w = 0u;
     if (valid && s > 0.f) {
       const float r = __frcp_rn(s);
+      float d[8];
+      uint32_t t[8];
+      bool unsure = false;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        int q = __float2int_rn(quot_rint(f[e] - z, s, r));
-        q = max(0, min(15, q));
-        w |= (uint32_t)q << (4 * e);
+        d[e] = f[e] - z;
+        const float y = fminf(fmaxf(d[e] * r, 0.f), 15.f);
+        const float tf = y + kRoundMagic;
+        unsure |= rint_unsure(y, tf);
+        t[e] = __float_as_uint(tf);
       }
+      if (unsure) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) t[e] = __float_as_uint(fminf(fmaxf(d[e] / s, 0.f), 15.f) + kRoundMagic);
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w |= (t[e] & 0xFu) << (4 * e);
     }
     const float zz = valid ? z : 0.f, ss = valid ? s : 0.f;
     if (DEQ) {
