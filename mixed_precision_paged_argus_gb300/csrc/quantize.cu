@@ -372,6 +372,76 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_kernel(const QParams p) 
   }
 }
 
+// INT4 with one lane per 32-element group (the group's four 16-byte source
+// vectors in x0..x3): the min / max reduction and the scale arithmetic are
+// lane-local and done once per group, and the 32 codes leave as one 16-byte
+// store.  Same arithmetic, hence the same codes, as encode_store's INT4 path.
+template <bool SBF16>
+__device__ __forceinline__ void encode_int4_group(const uint4 (&x)[4], bool valid, uint4& codes, uint32_t& meta) {
+  uint32_t mn, mx;
+  {
+    const uint32_t* wv = reinterpret_cast<const uint32_t*>(&x[0]);
+    if (SBF16) {
+      __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&wv[0]), b = a;
+#pragma unroll
+      for (int i = 1; i < 16; ++i) {
+        const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&wv[i]);
+        a = __hmin2(a, c);
+        b = __hmax2(b, c);
+      }
+      mn = *reinterpret_cast<uint32_t*>(&a);
+      mx = *reinterpret_cast<uint32_t*>(&b);
+    } else {
+      __half2 a = *reinterpret_cast<const __half2*>(&wv[0]), b = a;
+#pragma unroll
+      for (int i = 1; i < 16; ++i) {
+        const __half2 c = *reinterpret_cast<const __half2*>(&wv[i]);
+        a = __hmin2(a, c);
+        b = __hmax2(b, c);
+      }
+      mn = *reinterpret_cast<uint32_t*>(&a);
+      mx = *reinterpret_cast<uint32_t*>(&b);
+    }
+  }
+  auto to_f = [](uint32_t bits16) -> float {
+    return SBF16 ? __uint_as_float(bits16 << 16) : __half2float(__ushort_as_half((unsigned short)bits16));
+  };
+  const float lo = fminf(to_f(mn & 0xFFFFu), to_f(mn >> 16));
+  const float hi = fmaxf(to_f(mx & 0xFFFFu), to_f(mx >> 16));
+  const float z = fp16_sat(lo);
+  const float s = scale_div15(hi - z);
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+  if (valid && s > 0.f) {
+    const float r = __frcp_rn(s);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      float f[8], d[8];
+      uint32_t t[8];
+      unpack8<SBF16>(x[m], f);
+      float dev = 0.f;  // largest distance of a product from its rounded value
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        d[e] = f[e] - z;
+        const float y = fminf(fmaxf(d[e] * r, 0.f), 15.f);
+        const float tf = y + kRoundMagic;
+        dev = fmaxf(dev, fabsf(y - (tf - kRoundMagic)));
+        t[e] = __float_as_uint(tf);
+      }
+      if (dev > 0.5f - 0x1p-12f) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) t[e] = __float_as_uint(fminf(fmaxf(d[e] / s, 0.f), 15.f) + kRoundMagic);
+      }
+      // low bytes of t are the codes 0..15: even elements in the low nibbles
+      const uint32_t ev = prmt(prmt(t[0], t[2], 0x0040), prmt(t[4], t[6], 0x0040), 0x5410);
+      const uint32_t od = prmt(prmt(t[1], t[3], 0x0040), prmt(t[5], t[7], 0x0040), 0x5410);
+      w[m] = ev + (od << 4);
+    }
+  }
+  codes = make_uint4(w[0], w[1], w[2], w[3]);
+  const __half2 sz = __halves2half2(__float2half_rn(valid ? s : 0.f), __float2half_rn(valid ? z : 0.f));
+  meta = *reinterpret_cast<const uint32_t*>(&sz);
+}
+
 // Units of at most 2048 elements: one warp per unit, held in registers,
 // software-pipelined so that the next unit's loads are in flight while the
 // current one is reduced, encoded and stored.
@@ -406,10 +476,17 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_small_kernel(const QPara
     d.dst = ((size_t)ds * 2 + d.kv) * Hkv + d.h;
     return d;
   };
+  const bool want_ck_any = p.ckey != nullptr;
+  // INT4 units without a compressed key use one lane per 32-element group:
+  // slot 4j + m holds vector m of group lane + 32j
+  auto group_layout = [&](const Unit& d) {
+    return CODEC == ARGUS_INT4_G32 && !(want_ck_any && d.kv == 0);
+  };
   auto load = [&](const Unit& d, uint4 (&buf)[kRegVecs]) {
+    const bool gl = group_layout(d);
 #pragma unroll
     for (int k = 0; k < kRegVecs; ++k) {
-      const int v = lane + 32 * k;
+      const int v = gl ? 4 * (lane + 32 * (k >> 2)) + (k & 3) : lane + 32 * k;
       if (d.ok && v < nvec) buf[k] = __ldcs(d.src + v);   // streamed once: evict first
     }
   };
@@ -428,6 +505,22 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_small_kernel(const QPara
     }
     if (!cu.ok) {
       if (lane == 0 && cu.kv == 0 && cu.h == 0 && p.status) atomicAdd(p.status, 1u);
+    } else if (group_layout(cu)) {
+      constexpr int GPR = D / 32;  // groups per token row
+      uint4* gcodes = reinterpret_cast<uint4*>(p.dst_codes + cu.dst * (size_t)P * (D / 2));
+      uint32_t* gmeta = reinterpret_cast<uint32_t*>(p.dst_meta) + cu.dst * (size_t)P * GPR;
+#pragma unroll
+      for (int j = 0; j < kRegVecs / 4; ++j) {
+        const int idx = lane + 32 * j;
+        if (4 * idx < nvec) {
+          const uint4 xg[4] = {cur[4 * j], cur[4 * j + 1], cur[4 * j + 2], cur[4 * j + 3]};
+          uint4 c;
+          uint32_t m;
+          encode_int4_group<SBF16>(xg, idx / GPR < cu.valid, c, m);
+          gcodes[idx] = c;
+          gmeta[idx] = m;
+        }
+      }
     } else {
       const int nvalid_vec = cu.valid * VPR;
       uint8_t* dcodes;

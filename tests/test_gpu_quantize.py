@@ -181,3 +181,34 @@ def test_codes_near_rounding_boundaries_with_a_non_power_of_two_scale(codec):
     codes, meta = C.alloc_pool(codec, n, 1, P, D)
     C.quantize_pages(src, C.CODEC_FP16, list(range(n)), codec, codes, meta, list(range(n)))
     _compare(pool, codes, meta)
+
+
+@pytest.mark.parametrize("ckey", [False, True])
+@pytest.mark.parametrize("src_dtype", [W.FP16, W.BF16])
+def test_int4_groups_with_pinned_range_and_interior_values(ckey, src_dtype):
+    """Groups whose min and max pin z and s, interior values uniform in between
+    (many land within 2^-12 of a half-integer quotient, some on exact ties when
+    s is a power of two); V units use the one-lane-per-group path, K units the
+    compressed-key path when ckey is set."""
+    Hkv, P, D, n = 2, 16, 128, 48
+    rng = np.random.default_rng(7 + ckey + 2 * src_dtype)
+    groups = n * 2 * Hkv * P * (D // 32)
+    z = rng.standard_normal(groups) * 4
+    s = np.abs(rng.standard_normal(groups)) * 0.3 + 1e-3
+    s[::5] = 2.0 ** rng.integers(-6, 0, size=len(s[::5]))          # exact ties possible
+    k = rng.uniform(0, 15, size=(groups, 32))
+    k[:, 0], k[:, 1] = 0.0, 15.0
+    k[::3, 2:] = np.floor(k[::3, 2:]) + 0.5                          # on / near the half-integers
+    x = z[:, None] + k * s[:, None]
+    if src_dtype == W.FP16:
+        bits = x.astype(np.float16).view(np.uint16)
+    else:
+        bits = C.f64_to_bf16_bits(x)
+    src = bits.reshape(n, 2, Hkv, P, D)
+    t = torch.from_numpy(src.view(np.int16)).view(torch.float16 if src_dtype == W.FP16 else torch.bfloat16)
+    pool, ck, st = _gpu_quantize(t, src_dtype, W.INT4_G32, Hkv, P, D, list(range(n)), list(range(n)), n,
+                                 ckey=ckey)
+    assert st == 0
+    codes, meta = C.alloc_pool(C.CODEC_INT4_G32, n, Hkv, P, D)
+    C.quantize_pages(src, src_dtype, list(range(n)), C.CODEC_INT4_G32, codes, meta, list(range(n)))
+    _compare(pool, codes, meta)
