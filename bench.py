@@ -536,11 +536,14 @@ def leg_prefill(dev, timer, steps, warm, tflops_peak):
     acc_o = torch.empty((Hq, NQ, D_), dtype=torch.float32, device=dev)
     acc_l = torch.empty((Hq, NQ), dtype=torch.float32, device=dev)
     wins = [(w, w + WIN) for w in range(0, CTX, WIN)] + [(CTX, CTX + NQ)]
+    ws = torch.empty(max(16, max(argus.window_prefill_workspace_bytes(g, NQ, w1 - w0) for w0, w1 in wins)),
+                     dtype=torch.uint8, device=dev)
 
     def run():
         for i, (w0, w1) in enumerate(wins):
             argus.window_prefill_attn(g, NQ, q, k[:, w0:], v[:, w0:], kv_len * D_, w1 - w0, w0, CTX,
-                                      W.softmax_scale(D_), acc_o, acc_l, 1 if i else 0, stream=timer.stream)
+                                      W.softmax_scale(D_), acc_o, acc_l, 1 if i else 0, ws=ws,
+                                      stream=timer.stream)
 
     ms = timer.time(timer.graph(run).replay, max(3, steps // 10), warm)
     flops = A.prefill_flops(Hq, D_, NQ, NQ * CTX + NQ * (NQ + 1) // 2)
@@ -548,7 +551,9 @@ def leg_prefill(dev, timer, steps, warm, tflops_peak):
                        "causal chunk, 131072-token windows folded by log2-sum-exp",
            "ms": ms, "flops": flops, "tflops": flops / (ms * 1e-3) / 1e12,
            "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / tflops_peak,
-           "note": "useful FLOPs 4*D*Hq*visible pairs; the P.V product runs twice (bf16 hi + lo of P)"}
+           "splits": argus.window_prefill_workspace_bytes(g, NQ, WIN) // (Hq * NQ * (D_ + 1) * 4),
+           "note": "useful FLOPs 4*D*Hq*visible pairs; the P.V product runs twice (bf16 hi + lo of P); each "
+                   "128-row query tile's window split into key ranges over all SMs, partials folded"}
     del q, k, v
     torch.cuda.synchronize()
     torch.cuda.empty_cache()

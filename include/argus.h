@@ -266,13 +266,26 @@ argus_status argus_fold_lse(int64_t n_rows, int32_t head_dim, float* acc_o,
  * (h, j, d) at h * kv_head_stride + j * D + d (kv_head_stride = 0 means
  * win_len * D); acc_o device float [Hq][n_q][D]; acc_lse2 [Hq][n_q].
  * Supported: head_dim 128, n_q a multiple of 128, win_len a multiple of 128.
+ * num_splits: key ranges per 128-row query tile, each its own CTA, so that
+ * every SM works; their partial results are kept in ws and folded by a second
+ * kernel.  1 = one CTA per tile folding directly (ws unused); k > 1 = k ranges;
+ * 0 = chosen from the sizes and the SM count when ws != NULL, else 1.
+ * ws (device) holds argus_window_prefill_workspace_bytes(..., num_splits)
+ * bytes (ARGUS_E_WORKSPACE if smaller); it needs no initialisation, and calls
+ * sharing one must not overlap on the GPU.
  * ------------------------------------------------------------------------- */
+argus_status argus_window_prefill_workspace_bytes(const argus_geom* g, int32_t n_q,
+                                                  int64_t win_len, int32_t num_splits,
+                                                  size_t* bytes);
+
 argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n_q,
                                        const void* q, const void* k, const void* v,
                                        int64_t kv_head_stride, int64_t win_len,
                                        int64_t win_pos0, int64_t q_pos0,
                                        float softmax_scale, float* acc_o,
-                                       float* acc_lse2, int32_t fold, void* stream);
+                                       float* acc_lse2, int32_t fold,
+                                       int32_t num_splits, void* ws, size_t ws_bytes,
+                                       void* stream);
 
 const char* argus_status_string(argus_status s);
 

@@ -53,7 +53,8 @@ class DecodeArgs(ctypes.Structure):
 EXPORTS = ["argus_quantize_pages", "argus_decode_workspace_bytes", "argus_paged_decode_attn",
            "argus_paged_decode_attn_noalloc",
            "argus_select_workspace_bytes", "argus_select_pages", "argus_fold_lse",
-           "argus_window_prefill_attn", "argus_status_string", "argus_last_error"]
+           "argus_window_prefill_workspace_bytes", "argus_window_prefill_attn", "argus_status_string",
+           "argus_last_error"]
 
 
 def lib_path():
@@ -92,7 +93,9 @@ def lib():
     L.argus_fold_lse.argtypes = [i64, i32, vp, vp, vp, vp, vp]
     L.argus_window_prefill_attn.restype = ctypes.c_int
     L.argus_window_prefill_attn.argtypes = [ctypes.POINTER(Geom), i32, vp, vp, vp, i64, i64, i64, i64,
-                                            ctypes.c_float, vp, vp, i32, vp]
+                                            ctypes.c_float, vp, vp, i32, i32, vp, sz, vp]
+    L.argus_window_prefill_workspace_bytes.restype = ctypes.c_int
+    L.argus_window_prefill_workspace_bytes.argtypes = [ctypes.POINTER(Geom), i32, i64, i32, ctypes.POINTER(sz)]
     _lib = L
     return L
 
@@ -235,9 +238,20 @@ def fold_lse(acc_o, acc_lse2, part_o, part_lse2, stream=None):
                                 _ptr(part_lse2), _stream(stream)))
 
 
+def window_prefill_workspace_bytes(g, n_q, win_len, num_splits=0):
+    n = ctypes.c_size_t(0)
+    _check(lib().argus_window_prefill_workspace_bytes(ctypes.byref(g), int(n_q), int(win_len), int(num_splits),
+                                                      ctypes.byref(n)))
+    return n.value
+
+
 def window_prefill_attn(g, n_q, q, k, v, kv_head_stride, win_len, win_pos0, q_pos0, softmax_scale,
-                        acc_o, acc_lse2, fold, stream=None):
+                        acc_o, acc_lse2, fold, num_splits=0, ws=None, stream=None):
+    """num_splits / ws: key ranges per query tile and their partial-result
+    workspace (window_prefill_workspace_bytes bytes); 0 with ws chooses the
+    split count, 0 without ws is one CTA per tile."""
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(lib().argus_window_prefill_attn(ctypes.byref(g), int(n_q), _ptr(q), _ptr(k), _ptr(v),
                                            int(kv_head_stride), int(win_len), int(win_pos0), int(q_pos0),
                                            float(softmax_scale), _ptr(acc_o), _ptr(acc_lse2), int(fold),
-                                           _stream(stream)))
+                                           int(num_splits), _ptr(ws), nbytes, _stream(stream)))

@@ -66,6 +66,9 @@ struct PParams {
   float* acc_o;
   float* acc_lse2;
   int fold;
+  int nsplit;                       // key ranges per tile (grid.z)
+  float* ws_o;                      // nsplit > 1: partial o [tile][split][128][D], normalised
+  float* ws_lse;                    //             and its lse2 [tile][split][128]
 };
 
 // ---------------------------------------------------------------- PTX
@@ -189,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float2* ml1 = reinterpret_cast<float2*>(smem + kOffML);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x, h = blockIdx.y;
+  const int tile = blockIdx.x, h = blockIdx.y, split = blockIdx.z;
   const long long row0 = (long long)h * p.G * p.n_q + (long long)tile * kBM;   // first row of [Hq*n_q]
   const int hq = (int)(row0 / p.n_q);
   const long long i0 = row0 - (long long)hq * p.n_q;                              // first query index
@@ -198,7 +201,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   long long n_keys = last_visible + 1;
   if (n_keys < 0) n_keys = 0;
   if (n_keys > p.win_len) n_keys = p.win_len;
-  const int nb = (int)((n_keys + kBN - 1) / kBN);
+  const int nb_tile = (int)((n_keys + kBN - 1) / kBN);
+  // this CTA's key blocks: [jb, jb + nb) of the tile's nb_tile, balanced over the splits
+  const int jb = (int)((long long)split * nb_tile / p.nsplit);
+  const int nb = (int)((long long)(split + 1) * nb_tile / p.nsplit) - jb;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -234,19 +240,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(q_full, kTile);
       tma_load_2d(smem + kOffQ, &tmQ, 0, (int)row0, q_full);
       tma_load_2d(smem + kOffQ + kHalf, &tmQ, 64, (int)row0, q_full);
-      for (int j = 0; j < nb; ++j) {
-        const int st = j % kStages;
-        if (j >= kStages && !mbar_wait(&kv_empty[st], ((j / kStages) - 1) & 1, &misc[1])) {
+      for (int i = 0; i < nb; ++i) {
+        const int st = i % kStages;
+        const int y = (jb + i) * kBN;
+        if (i >= kStages && !mbar_wait(&kv_empty[st], ((i / kStages) - 1) & 1, &misc[1])) {
           misc[1] = 1;
           break;
         }
         mbar_arrive_expect_tx(&kv_full[st], 2 * kTile);
         uint8_t* kd = smem + kOffK + st * kTile;
         uint8_t* vd = smem + kOffV + st * kTile;
-        tma_load_3d(kd, &tmK, 0, j * kBN, h, &kv_full[st]);
-        tma_load_3d(kd + kHalf, &tmK, 64, j * kBN, h, &kv_full[st]);
-        tma_load_3d(vd, &tmV, 0, j * kBN, h, &kv_full[st]);
-        tma_load_3d(vd + kHalf, &tmV, 64, j * kBN, h, &kv_full[st]);
+        tma_load_3d(kd, &tmK, 0, y, h, &kv_full[st]);
+        tma_load_3d(kd + kHalf, &tmK, 64, y, h, &kv_full[st]);
+        tma_load_3d(vd, &tmV, 0, y, h, &kv_full[st]);
+        tma_load_3d(vd + kHalf, &tmV, 64, y, h, &kv_full[st]);
       }
     }
   } else if (warp == kSoftmaxWarps + 1) {
@@ -311,7 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m = -INFINITY, l = 0.f;
     bool alive = true;
     int k = 0;
-    for (int j = grp; j < nb && alive; j += 2, ++k) {
+    for (int i = grp; i < nb && alive; i += 2, ++k) {
+      const int j = jb + i;
       // keep the warp together: tcgen05.ld below is warp-collective
       if (!__all_sync(0xffffffffu, mbar_wait(&s_full[grp], k & 1, &misc[1]))) { alive = false; misc[1] = 1; break; }
       tc_fence_after();
@@ -426,50 +434,79 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lt = l0v * w0 + o1ml.y * w1;
       const bool have = alive && lt > 0.f;
       const long long orow = (long long)hq * p.n_q + qi;
-      float* ao = p.acc_o + orow * kD;
-      const float lse = have ? M + log2f(lt) : -INFINITY;
-      const float La = p.fold ? p.acc_lse2[orow] : -INFINITY;
-      float wa = 0.f, wb = 0.f, L = -INFINITY;
-      if (have) {
-        if (La == -INFINITY) {
-          wb = 1.f / lt;
-          L = lse;
-        } else {
-          const float Mx = fmaxf(La, lse);
-          L = Mx + log2f(exp2f(La - Mx) + exp2f(lse - Mx));
-          wa = exp2f(La - L);
-          wb = exp2f(lse - L) / lt;
-        }
-      } else {
-        wa = 1.f;
-        L = La;
-      }
       const uint32_t o0a = tO[0] + lane_off, o1a = tO[1] + lane_off;
+      if (p.nsplit > 1) {
+        // partial of this key range: normalised o and its lse2, folded later
+        const size_t part = ((size_t)h * p.n_tiles + tile) * p.nsplit + split;
+        float* po = p.ws_o + (part * kBM + row) * kD;
+        const float inv = have ? 1.f / lt : 0.f;
 #pragma unroll 1
-      for (int c = 0; c < kD / 16; ++c) {
-        uint32_t v0[16], v1[16];
-        if (nk > 0) tmem_ld16(o0a + c * 16, v0);     // nk, nk1 are uniform across the CTA
-        if (nk1 > 0) tmem_ld16(o1a + c * 16, v1);
-        tmem_wait_ld();
+        for (int c = 0; c < kD / 16; ++c) {
+          uint32_t v0[16], v1[16];
+          if (nk > 0) tmem_ld16(o0a + c * 16, v0);     // nk, nk1 are uniform across the CTA
+          if (nk1 > 0) tmem_ld16(o1a + c * 16, v1);
+          tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          float ov[4];
+          for (int e = 0; e < 16; e += 4) {
+            float ov[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            float x = 0.f;
-            if (have) {
-              if (nk > 0) x += w0 * __uint_as_float(v0[e + u]);
-              if (nk1 > 0) x += w1 * __uint_as_float(v1[e + u]);
+            for (int u = 0; u < 4; ++u) {
+              float x = 0.f;
+              if (have) {
+                if (nk > 0) x += w0 * __uint_as_float(v0[e + u]);
+                if (nk1 > 0) x += w1 * __uint_as_float(v1[e + u]);
+              }
+              ov[u] = x * inv;
             }
-            ov[u] = x * wb;
+            *reinterpret_cast<float4*>(po + c * 16 + e) = make_float4(ov[0], ov[1], ov[2], ov[3]);
           }
-          float4 a = (p.fold && wa != 0.f) ? *reinterpret_cast<const float4*>(ao + c * 16 + e)
-                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-          float4 o = make_float4(wa * a.x + ov[0], wa * a.y + ov[1], wa * a.z + ov[2], wa * a.w + ov[3]);
-          if (have || !p.fold) *reinterpret_cast<float4*>(ao + c * 16 + e) = o;
         }
+        p.ws_lse[part * kBM + row] = have ? M + log2f(lt) : -INFINITY;
+      } else {
+        float* ao = p.acc_o + orow * kD;
+        const float lse = have ? M + log2f(lt) : -INFINITY;
+        const float La = p.fold ? p.acc_lse2[orow] : -INFINITY;
+        float wa = 0.f, wb = 0.f, L = -INFINITY;
+        if (have) {
+          if (La == -INFINITY) {
+            wb = 1.f / lt;
+            L = lse;
+          } else {
+            const float Mx = fmaxf(La, lse);
+            L = Mx + log2f(exp2f(La - Mx) + exp2f(lse - Mx));
+            wa = exp2f(La - L);
+            wb = exp2f(lse - L) / lt;
+          }
+        } else {
+          wa = 1.f;
+          L = La;
+        }
+  #pragma unroll 1
+        for (int c = 0; c < kD / 16; ++c) {
+          uint32_t v0[16], v1[16];
+          if (nk > 0) tmem_ld16(o0a + c * 16, v0);     // nk, nk1 are uniform across the CTA
+          if (nk1 > 0) tmem_ld16(o1a + c * 16, v1);
+          tmem_wait_ld();
+  #pragma unroll
+          for (int e = 0; e < 16; e += 4) {
+            float ov[4];
+  #pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              float x = 0.f;
+              if (have) {
+                if (nk > 0) x += w0 * __uint_as_float(v0[e + u]);
+                if (nk1 > 0) x += w1 * __uint_as_float(v1[e + u]);
+              }
+              ov[u] = x * wb;
+            }
+            float4 a = (p.fold && wa != 0.f) ? *reinterpret_cast<const float4*>(ao + c * 16 + e)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 o = make_float4(wa * a.x + ov[0], wa * a.y + ov[1], wa * a.z + ov[2], wa * a.w + ov[3]);
+            if (have || !p.fold) *reinterpret_cast<float4*>(ao + c * 16 + e) = o;
+          }
+        }
+        if (have || !p.fold) p.acc_lse2[orow] = L;
       }
-      if (have || !p.fold) p.acc_lse2[orow] = L;
     }
   }
 
@@ -481,6 +518,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
+}
+
+// Fold the key-range partials of every row into the accumulator: one warp per
+// row, each lane a float4 of the 128 dims.  Same arithmetic as the direct
+// epilogue: L = max + log2(sum of 2^(lse - max)), o = sum of 2^(lse - L) o_s.
+constexpr int kFoldWarps = 8;
+__global__ void __launch_bounds__(32 * kFoldWarps) prefill_fold_kernel(const PParams p, long long n_rows) {
+  const long long r = (long long)blockIdx.x * kFoldWarps + (threadIdx.x >> 5);
+  if (r >= n_rows) return;
+  const int lane = threadIdx.x & 31;
+  const long long tile_lin = r / kBM;        // = h * n_tiles + tile
+  const int row = (int)(r - tile_lin * kBM);
+  const float* pl = p.ws_lse + (size_t)tile_lin * p.nsplit * kBM + row;
+  const float La = p.fold ? p.acc_lse2[r] : -INFINITY;
+  float M = La;
+  for (int s2 = 0; s2 < p.nsplit; ++s2) M = fmaxf(M, pl[(size_t)s2 * kBM]);
+  float4* ao = reinterpret_cast<float4*>(p.acc_o + r * kD) + lane;
+  if (M == -INFINITY) {  // nothing visible anywhere: o = 0, lse2 = -inf (kept when folding)
+    if (!p.fold) {
+      *ao = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (lane == 0) p.acc_lse2[r] = -INFINITY;
+    }
+    return;
+  }
+  float sum = (La == -INFINITY) ? 0.f : exp2f(La - M);
+  for (int s2 = 0; s2 < p.nsplit; ++s2) {
+    const float ls = pl[(size_t)s2 * kBM];
+    if (ls != -INFINITY) sum += exp2f(ls - M);
+  }
+  const float L = M + log2f(sum);
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (La != -INFINITY) {
+    const float wa = exp2f(La - L);
+    const float4 a = *ao;
+    o = make_float4(wa * a.x, wa * a.y, wa * a.z, wa * a.w);
+  }
+  const float4* po = reinterpret_cast<const float4*>(p.ws_o + ((size_t)tile_lin * p.nsplit * kBM + row) * kD) + lane;
+  for (int s2 = 0; s2 < p.nsplit; ++s2) {
+    const float ls = pl[(size_t)s2 * kBM];
+    if (ls == -INFINITY) continue;
+    const float w = exp2f(ls - L);
+    const float4 x = po[(size_t)s2 * kBM * (kD / 4)];
+    o.x += w * x.x;
+    o.y += w * x.y;
+    o.z += w * x.z;
+    o.w += w * x.w;
+  }
+  *ao = o;
+  if (lane == 0) p.acc_lse2[r] = L;
 }
 
 // ---------------------------------------------------------------- host
@@ -509,17 +595,27 @@ static bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_
   return r == CUDA_SUCCESS;
 }
 
-}  // namespace prefill
-}  // namespace argus
+// Key ranges per tile: enough CTAs that whole waves cover every SM, weighed
+// against the fixed cost of a CTA (Q load, pipeline fill, epilogue), counted
+// here as four key blocks.
+static int plan_splits(long long n_tiles_total, long long nb_tile) {
+  const long long sms = device_sm_count();
+  int best = 1;
+  double best_cost = 1e300;
+  for (int k = 1; k <= 32; ++k) {
+    if (k > 1 && nb_tile / k < 8) break;
+    const long long ctas = n_tiles_total * k;
+    const long long waves = (ctas + sms - 1) / sms;
+    const double cost = (double)waves * ((double)((nb_tile + k - 1) / k) + 4.0);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = k;
+    }
+  }
+  return best;
+}
 
-using namespace argus;
-using namespace argus::prefill;
-
-extern "C" argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n_q, const void* q,
-                                                  const void* k, const void* v, int64_t kv_head_stride,
-                                                  int64_t win_len, int64_t win_pos0, int64_t q_pos0,
-                                                  float softmax_scale, float* acc_o, float* acc_lse2,
-                                                  int32_t fold, void* stream) {
+static argus_status check_geom(const argus_geom* g, int32_t n_q, int64_t win_len) {
   if (!g) return fail(ARGUS_E_INVALID, "prefill: geometry is NULL");
   if (g->n_q_heads <= 0 || g->n_kv_heads <= 0 || g->n_q_heads % g->n_kv_heads)
     return fail(ARGUS_E_INVALID, "prefill: bad head counts");
@@ -528,19 +624,56 @@ extern "C" argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n
   if (n_q % kBM != 0 || win_len % kBN != 0)
     return fail(ARGUS_E_UNSUPPORTED, "prefill: n_q (%d) and win_len (%lld) must be multiples of 128", n_q,
                 (long long)win_len);
+  if ((long long)g->n_q_heads * n_q > (1LL << 31) || win_len > (1LL << 31))
+    return fail(ARGUS_E_UNSUPPORTED, "prefill: sizes beyond 2^31 rows");
+  return ARGUS_OK;
+}
+
+static size_t split_bytes(long long n_tiles_total, int nsplit) {
+  return nsplit > 1 ? (size_t)n_tiles_total * nsplit * kBM * (kD + 1) * sizeof(float) : 0;
+}
+
+static int resolve_splits(long long tiles, long long win_len, int32_t num_splits, bool have_ws) {
+  if (num_splits > 0) return num_splits;
+  return have_ws ? plan_splits(tiles, win_len / kBN) : 1;
+}
+
+}  // namespace prefill
+}  // namespace argus
+
+extern "C" argus_status argus_window_prefill_workspace_bytes(const argus_geom* g, int32_t n_q, int64_t win_len,
+                                                             int32_t num_splits, size_t* bytes) {
+  using namespace argus::prefill;
+  if (!bytes) return argus::fail(ARGUS_E_INVALID, "prefill: bytes is NULL");
+  argus_status st = check_geom(g, n_q, win_len);
+  if (st != ARGUS_OK) return st;
+  if (num_splits < 0 || num_splits > 1024) return argus::fail(ARGUS_E_INVALID, "prefill: num_splits out of range");
+  const long long tiles = (long long)g->n_q_heads * n_q / kBM;
+  *bytes = split_bytes(tiles, resolve_splits(tiles, win_len, num_splits, true));
+  return ARGUS_OK;
+}
+
+extern "C" argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n_q, const void* q,
+                                                  const void* k, const void* v, int64_t kv_head_stride,
+                                                  int64_t win_len, int64_t win_pos0, int64_t q_pos0,
+                                                  float softmax_scale, float* acc_o, float* acc_lse2,
+                                                  int32_t fold, int32_t num_splits, void* ws, size_t ws_bytes,
+                                                  void* stream) {
+  using namespace argus;
+  using namespace argus::prefill;
+  argus_status st0 = check_geom(g, n_q, win_len);
+  if (st0 != ARGUS_OK) return st0;
   if (fold != 0 && fold != 1) return fail(ARGUS_E_INVALID, "prefill: fold must be 0 or 1");
   if (!std::isfinite(softmax_scale)) return fail(ARGUS_E_INVALID, "prefill: softmax_scale not finite");
   if (n_q == 0) return ARGUS_OK;
   if (!q || !acc_o || !acc_lse2 || (win_len > 0 && (!k || !v)))
     return fail(ARGUS_E_INVALID, "prefill: NULL pointer");
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
-       reinterpret_cast<uintptr_t>(acc_o)) & 15)
+       reinterpret_cast<uintptr_t>(acc_o) | reinterpret_cast<uintptr_t>(ws)) & 15)
     return fail(ARGUS_E_INVALID, "prefill: pointers must be 16-byte aligned");
   const long long stride = kv_head_stride ? kv_head_stride : win_len * kD;
   if (stride % 8 != 0 || stride < win_len * kD)
     return fail(ARGUS_E_INVALID, "prefill: kv_head_stride must be >= win_len*head_dim and a multiple of 8");
-  if ((long long)g->n_q_heads * n_q > (1LL << 31) || win_len > (1LL << 31))
-    return fail(ARGUS_E_UNSUPPORTED, "prefill: sizes beyond 2^31 rows");
   const int G = g->n_q_heads / g->n_kv_heads;
   PParams p{};
   p.G = G;
@@ -553,6 +686,16 @@ extern "C" argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n
   p.acc_o = acc_o;
   p.acc_lse2 = acc_lse2;
   p.fold = fold;
+  const long long tiles_total = (long long)p.n_tiles * g->n_kv_heads;
+  if (num_splits < 0 || num_splits > 1024) return fail(ARGUS_E_INVALID, "prefill: num_splits out of range");
+  p.nsplit = resolve_splits(tiles_total, win_len, num_splits, ws != nullptr);
+  if (p.nsplit > 1) {
+    const size_t need = split_bytes(tiles_total, p.nsplit);
+    if (!ws || ws_bytes < need) return fail(ARGUS_E_WORKSPACE, "prefill: workspace %zu < %zu", ws_bytes, need);
+    p.ws_o = static_cast<float*>(ws);
+    p.ws_lse = p.ws_o + (size_t)tiles_total * p.nsplit * kBM * kD;
+  }
+  if (p.nsplit > 65535) return fail(ARGUS_E_UNSUPPORTED, "prefill: too many splits");
   CUtensorMap mq, mk, mv;
   const cuuint64_t qd[2] = {(cuuint64_t)kD, (cuuint64_t)g->n_q_heads * n_q};
   const cuuint64_t qs[1] = {(cuuint64_t)kD * 2};
@@ -570,7 +713,12 @@ extern "C" argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n
     if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "prefill: smem attribute: %s", cudaGetErrorString(e));
     configured[dev] = true;
   }
-  dim3 grid(p.n_tiles, g->n_kv_heads);
-  prefill_kernel<<<grid, kThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(mq, mk, mv, p);
-  return launch_status("argus_window_prefill_attn");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  dim3 grid(p.n_tiles, g->n_kv_heads, p.nsplit);
+  prefill_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
+  argus_status st = launch_status("argus_window_prefill_attn");
+  if (st != ARGUS_OK || p.nsplit == 1) return st;
+  const long long n_rows = (long long)g->n_q_heads * n_q;
+  prefill_fold_kernel<<<(unsigned)((n_rows + kFoldWarps - 1) / kFoldWarps), 32 * kFoldWarps, 0, s>>>(p, n_rows);
+  return launch_status("argus_window_prefill_attn (fold)");
 }

@@ -101,8 +101,9 @@ def _prefill(dev):
     g = argus.geom(Hq, Hkv, D, 16)
     acc_o = torch.zeros((Hq, NQ, D), dtype=torch.float32, device=dev)
     acc_l = torch.full((Hq, NQ), float("-inf"), device=dev)
+    ws = torch.empty(max(16, argus.window_prefill_workspace_bytes(g, NQ, WIN)), dtype=torch.uint8, device=dev)
     return lambda: argus.window_prefill_attn(g, NQ, q, k, v, 0, WIN, 0, 1 << 20, W.softmax_scale(D), acc_o,
-                                             acc_l, 1)
+                                             acc_l, 1, ws=ws)
 
 
 def _fold(dev):

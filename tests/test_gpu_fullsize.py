@@ -183,9 +183,12 @@ def test_windowed_prefill_full_size_sampled_rows():
     acc_o = torch.empty((Hq, NQ, D), dtype=torch.float32, device=dev)
     acc_l = torch.empty((Hq, NQ), dtype=torch.float32, device=dev)
     wins = [(w, w + WIN) for w in range(0, CTX, WIN)] + [(CTX, CTX + NQ)]
+    # the launch configuration the benchmark times: automatic key-range splits
+    ws = torch.empty(max(16, max(argus.window_prefill_workspace_bytes(g, NQ, w1 - w0) for w0, w1 in wins)),
+                     dtype=torch.uint8, device=dev)
     for i, (w0, w1) in enumerate(wins):
         argus.window_prefill_attn(g, NQ, q, k[:, w0:], v[:, w0:], kv_len * D, w1 - w0, w0, CTX,
-                                  W.softmax_scale(D), acc_o, acc_l, 1 if i else 0)
+                                  W.softmax_scale(D), acc_o, acc_l, 1 if i else 0, ws=ws)
     torch.cuda.synchronize()
     rows = [0, 1, 511, NQ - 1]
     q64 = C.bf16_bits_to_f64(W.to_bits(q[:, rows]))

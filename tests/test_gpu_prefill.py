@@ -30,7 +30,15 @@ def _data(Hq, Hkv, n_q, ctx, seed):
     return q, k, v, f(q), f(k), f(v)
 
 
-def _run_windows(Hq, Hkv, n_q, ctx, windows, seed, scale=None):
+def _ws(g, n_q, win_len, splits):
+    """A NaN-filled workspace for `splits` key ranges (None for one range)."""
+    if splits == 1:
+        return None
+    n = argus.window_prefill_workspace_bytes(g, n_q, win_len, splits)
+    return torch.full((max(n, 16) // 4,), float("nan"), dtype=torch.float32, device=DEV)
+
+
+def _run_windows(Hq, Hkv, n_q, ctx, windows, seed, scale=None, splits=1):
     q, k, v, q64, k64, v64 = _data(Hq, Hkv, n_q, ctx, seed)
     scale = W.softmax_scale(128) if scale is None else scale
     g = argus.geom(Hq, Hkv, 128, 16)
@@ -39,8 +47,9 @@ def _run_windows(Hq, Hkv, n_q, ctx, windows, seed, scale=None):
     acc_o = torch.zeros((Hq, n_q, 128), dtype=torch.float32, device=DEV)
     acc_l = torch.full((Hq, n_q), float("-inf"), dtype=torch.float32, device=DEV)
     for wi, (w0, w1) in enumerate(windows):
+        ws = _ws(g, n_q, w1 - w0, splits)
         argus.window_prefill_attn(g, n_q, qd, kd[:, w0:], vd[:, w0:], kv_len * 128, w1 - w0, w0, ctx, scale,
-                                  acc_o, acc_l, 1 if wi > 0 else 0)
+                                  acc_o, acc_l, 1 if wi > 0 else 0, num_splits=splits, ws=ws)
     torch.cuda.synchronize()
     ref_o, ref_l = oracle.window_attention(q64, k64, v64, 0, ctx, scale)
     return acc_o.cpu().numpy(), acc_l.cpu().numpy(), ref_o, ref_l
@@ -53,36 +62,41 @@ def _check(go, gl, ro, rl):
     assert np.abs(gl - rl).max() <= 1e-4 * np.abs(rl).max() + 1e-5
 
 
-def test_single_window_full_view_small():
-    go, gl, ro, rl = _run_windows(1, 1, 128, 128, [(0, 128)], seed=501)
+@pytest.mark.parametrize("splits", [1, 2])
+def test_single_window_full_view_small(splits):
+    go, gl, ro, rl = _run_windows(1, 1, 128, 128, [(0, 128)], seed=501, splits=splits)
     # the chunk itself is not part of this window: compare against the cache-only oracle
     q, k, v, q64, k64, v64 = _data(1, 1, 128, 128, 501)
     ro, rl = oracle.window_attention(q64, k64[:, :128], v64[:, :128], 0, 128, W.softmax_scale(128))
     _check(go, gl, ro, rl)
 
 
-def test_causal_chunk_window_only():
-    # a 256-row chunk attending only to itself: causal inside the chunk
+@pytest.mark.parametrize("splits", [1, 2, 5])
+def test_causal_chunk_window_only(splits):
+    # a 256-row chunk attending only to itself: causal inside the chunk; with 5
+    # key ranges over at most 2 visible blocks some ranges are empty
     q, k, v, q64, k64, v64 = _data(2, 1, 256, 0, 503)
     g = argus.geom(2, 1, 128, 16)
     acc_o = torch.empty((2, 256, 128), dtype=torch.float32, device=DEV)
     acc_l = torch.empty((2, 256), dtype=torch.float32, device=DEV)
     argus.window_prefill_attn(g, 256, q.to(DEV), k.to(DEV), v.to(DEV), 0, 256, 1000, 1000,
-                              W.softmax_scale(128), acc_o, acc_l, 0)
+                              W.softmax_scale(128), acc_o, acc_l, 0, num_splits=splits, ws=_ws(g, 256, 256, splits))
     torch.cuda.synchronize()
     ro, rl = oracle.window_attention(q64, k64, v64, 1000, 1000, W.softmax_scale(128))
     _check(acc_o.cpu().numpy(), acc_l.cpu().numpy(), ro, rl)
 
 
+@pytest.mark.parametrize("splits", [1, 3])
 @pytest.mark.parametrize("Hq,Hkv", [(2, 1), (16, 2)])
-def test_windows_folded_equal_single_pass(Hq, Hkv):
+def test_windows_folded_equal_single_pass(Hq, Hkv, splits):
     n_q, ctx = 256, 768
     windows = [(0, 256), (256, 768), (768, 1024)]      # two cache windows, then the chunk
-    go, gl, ro, rl = _run_windows(Hq, Hkv, n_q, ctx, windows, seed=505 + Hq)
+    go, gl, ro, rl = _run_windows(Hq, Hkv, n_q, ctx, windows, seed=505 + Hq, splits=splits)
     _check(go, gl, ro, rl)
 
 
-def test_window_beyond_every_query_is_identity():
+@pytest.mark.parametrize("splits", [1, 4])
+def test_window_beyond_every_query_is_identity(splits):
     q, k, v, q64, k64, v64 = _data(2, 1, 128, 256, 509)
     g = argus.geom(2, 1, 128, 16)
     acc_o = torch.randn((2, 128, 128), device=DEV)
@@ -90,7 +104,7 @@ def test_window_beyond_every_query_is_identity():
     o0, l0 = acc_o.clone(), acc_l.clone()
     # keys at positions 10_000.. are after every query (positions 256..383)
     argus.window_prefill_attn(g, 128, q.to(DEV), k.to(DEV), v.to(DEV), 0, 128, 10_000, 256,
-                              W.softmax_scale(128), acc_o, acc_l, 1)
+                              W.softmax_scale(128), acc_o, acc_l, 1, num_splits=splits, ws=_ws(g, 128, 128, splits))
     torch.cuda.synchronize()
     assert torch.equal(acc_o, o0) and torch.equal(acc_l, l0)
 
@@ -103,3 +117,25 @@ def test_rejects_unsupported_shapes():
     with pytest.raises(argus.ArgusError) as e:
         argus.window_prefill_attn(g, 128, t, t, t, 0, 128, 0, 0, 0.1, o, l, 0)
     assert e.value.status == 2
+
+
+def test_automatic_splits_with_a_long_window():
+    """4096 cached keys in one window: the automatic split count (> 1 here)
+    must give the same result as one CTA per tile, within the tolerance."""
+    Hq, Hkv, n_q, ctx = 16, 2, 128, 4096
+    g = argus.geom(Hq, Hkv, 128, 16)
+    assert argus.window_prefill_workspace_bytes(g, n_q, ctx, 0) > 0
+    go, gl, ro, rl = _run_windows(Hq, Hkv, n_q, ctx, [(0, ctx), (ctx, ctx + n_q)], seed=511, splits=0)
+    _check(go, gl, ro, rl)
+
+
+def test_split_workspace_too_small_is_rejected():
+    g = argus.geom(2, 1, 128, 16)
+    t = torch.zeros((2, 256, 128), dtype=torch.bfloat16, device=DEV)
+    o = torch.zeros((2, 256, 128), device=DEV)
+    l = torch.zeros((2, 256), device=DEV)
+    need = argus.window_prefill_workspace_bytes(g, 256, 256, 2)
+    small = torch.zeros((need - 16) // 4, dtype=torch.float32, device=DEV)
+    with pytest.raises(argus.ArgusError) as e:
+        argus.window_prefill_attn(g, 256, t, t, t, 0, 256, 0, 0, 0.1, o, l, 0, num_splits=2, ws=small)
+    assert e.value.status == 3
