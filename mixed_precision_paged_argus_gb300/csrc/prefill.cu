@@ -69,7 +69,19 @@ struct PParams {
   int nsplit;                       // key ranges per tile (grid.z)
   float* ws_o;                      // nsplit > 1: partial o [tile][split][128][D], normalised
   float* ws_lse;                    //             and its lse2 [tile][split][128]
+  const uint32_t* vmax_bits;        // fp16 P.V: bits of max |v| over the window
 };
+
+// fp16 P.V: V is converted once per window to fp16 scaled by 2^-e, e >= 0 the
+// smallest with max|v| * 2^-e < 2^15, so that nothing overflows; the output is
+// multiplied back by 2^e.  Every thread derives e from the same max word.
+__device__ __forceinline__ int v16_exponent(uint32_t vmax_bits) {
+  const float vm = __uint_as_float(vmax_bits);
+  if (!(vm < 3.0e38f) || vm < 32768.f) return 0;   // finite inputs below 2^15 need no scaling
+  int k = 0;
+  frexpf(vm, &k);                                    // vm < 2^k
+  return k - 15;
+}
 
 // ---------------------------------------------------------------- PTX
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
@@ -95,10 +107,11 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// instruction descriptor, kind::f16: bf16 x bf16 -> f32, M = 128, N = 128
-__host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(kBN >> 3) << 17) |
-         ((uint32_t)(kBM >> 4) << 24);
+// instruction descriptor, kind::f16 -> f32, M = 128, N = 128; operand type
+// 1 = bf16 (both operands), 0 = fp16 (both operands)
+__host__ __device__ constexpr uint32_t idesc_f16kind(bool bf16, bool b_mn_major) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -175,9 +188,13 @@ __device__ __forceinline__ void group_bar(int id) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kSoftmaxWarps * 32) : "memory");
 }
 
+// F16P: P.V in fp16 (P scaled by 2^7, V the scaled fp16 copy) with one MMA per
+// key step; otherwise bf16 with P split into hi + lo parts (two MMAs).
+template <bool F16P>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PParams p) {
+  constexpr float kPBias = F16P ? 7.f : 0.f;   // fp16 P is stored as P * 2^kPBias
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -261,8 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // order: S0, S1, then per block i: P.V of i, S of i+2 (into the buffer
     // P.V of i reads; the MMA pipe keeps the two in order)
     if (lane == 0 && nb > 0) {
-      constexpr uint32_t idQK = idesc_bf16(false);
-      constexpr uint32_t idPV = idesc_bf16(true);
+      constexpr uint32_t idQK = idesc_f16kind(true, false);
+      constexpr uint32_t idPV = idesc_f16kind(!F16P, true);
       const uint32_t q_s = smem_u32(smem + kOffQ);
       bool ok = mbar_wait(q_full, 0, &misc[1]);
       auto issue_s = [&](int j) {
@@ -291,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // 16kk + 8; V: 16 key rows = two 8-row swizzle atoms
           const uint64_t vd = sdesc(v_s + kk * 2048, kHalf, 1024);
           mma_ts(tO[b], tS[b] + kk * 16, vd, idPV, (i >= 2 || kk > 0) ? 1u : 0u);
-          mma_ts(tO[b], tS[b] + kk * 16 + 8, vd, idPV, 1u);
+          if (!F16P) mma_ts(tO[b], tS[b] + kk * 16 + 8, vd, idPV, 1u);
         }
         mma_commit(&o_done[b]);
         mma_commit(&kv_empty[st]);
@@ -369,11 +386,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= r;
       }
       if (move) m = mj;
-      // pass 2: P over the consumed scores as a bf16 pair hi + lo (P.V then
-      // carries about 16 significant bits of P).  A fully masked block has
-      // m = -inf and yields P = 0 through the mask below.
+      // pass 2: P over the consumed scores -- fp16 P * 2^7 (at most 2^15 under
+      // the 2^8 rescale threshold; l is summed in the same units), or a bf16
+      // pair hi + lo (P.V then carries about 16 significant bits of P).  A
+      // fully masked block has m = -inf and yields P = 0 through the mask below.
       const float sc = p.scale_log2;
-      const float mm = (m == -INFINITY) ? 0.f : m;
+      const float mm = (m == -INFINITY) ? 0.f : m - kPBias;
       const long long lim = edge ? vis_last - k0 : (long long)kBN;   // keys e <= lim are visible
 #pragma unroll 2
       for (int c = 0; c < kBN / 16; ++c) {
@@ -386,9 +404,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 8; ++e) {
             const float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e]), sc, -mm));
             const float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), sc, -mm));
-            const uint32_t hi = pack_bf16x2(p0, p1);
-            vh[e] = hi;
-            vl[e] = pack_bf16x2(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xFFFF0000u));
+            if (F16P) {
+              vh[e] = pack_f16x2(p0, p1);
+            } else {
+              const uint32_t hi = pack_bf16x2(p0, p1);
+              vh[e] = hi;
+              vl[e] = pack_bf16x2(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xFFFF0000u));
+            }
             l += p0 + p1;
           }
         } else {
@@ -398,16 +420,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool ok1 = (m != -INFINITY) && (c * 16 + 2 * e + 1 <= lim);
             const float p0 = ok0 ? fast_exp2(fmaf(__uint_as_float(v[2 * e]), sc, -mm)) : 0.f;
             const float p1 = ok1 ? fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), sc, -mm)) : 0.f;
-            const uint32_t hi = pack_bf16x2(p0, p1);
-            vh[e] = hi;
-            vl[e] = pack_bf16x2(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xFFFF0000u));
+            if (F16P) {
+              vh[e] = pack_f16x2(p0, p1);
+            } else {
+              const uint32_t hi = pack_bf16x2(p0, p1);
+              vh[e] = hi;
+              vl[e] = pack_bf16x2(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xFFFF0000u));
+            }
             l += p0 + p1;
           }
         }
-        // keys 16c .. 16c+15: high part in columns 16c .. 16c+7, low part in
+        // keys 16c .. 16c+15: (high part) in columns 16c .. 16c+7, low part in
         // 16c+8 .. 16c+15 -- exactly the columns just read, never unread ones
         tmem_st8(sS + c * 16, vh);
-        tmem_st8(sS + c * 16 + 8, vl);
+        if (!F16P) tmem_st8(sS + c * 16 + 8, vl);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -419,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&o_done[grp], (nk - 1) & 1, &misc[1])) misc[1] = 1;
       tc_fence_after();
     }
-    if (grp == 1) ml1[row] = make_float2(nk > 0 ? m : -INFINITY, nk > 0 ? l : 0.f);
+    if (grp == 1) ml1[row] = make_float2(nk > 0 ? m - kPBias : -INFINITY, nk > 0 ? l : 0.f);
     tc_fence_before();
     group_bar(1);
     if (grp == 0) {
@@ -427,8 +453,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float2 o1ml = ml1[row];
       const int nk1 = (nb > 1) ? nb / 2 : 0;
-      const float m0v = nk > 0 ? m : -INFINITY, l0v = nk > 0 ? l : 0.f;
+      // references in the units l was summed in (P scaled by 2^kPBias)
+      const float m0v = nk > 0 ? m - kPBias : -INFINITY, l0v = nk > 0 ? l : 0.f;
       const float M = fmaxf(m0v, o1ml.x);
+      const float vsc = F16P ? ldexpf(1.f, v16_exponent(*p.vmax_bits)) : 1.f;   // undo V's 2^-e
       const float w0 = (m0v == -INFINITY) ? 0.f : fast_exp2(m0v - M);
       const float w1 = (o1ml.x == -INFINITY) ? 0.f : fast_exp2(o1ml.x - M);
       const float lt = l0v * w0 + o1ml.y * w1;
@@ -439,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // partial of this key range: normalised o and its lse2, folded later
         const size_t part = ((size_t)h * p.n_tiles + tile) * p.nsplit + split;
         float* po = p.ws_o + (part * kBM + row) * kD;
-        const float inv = have ? 1.f / lt : 0.f;
+        const float inv = have ? vsc / lt : 0.f;
 #pragma unroll 1
         for (int c = 0; c < kD / 16; ++c) {
           uint32_t v0[16], v1[16];
@@ -469,13 +497,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         float wa = 0.f, wb = 0.f, L = -INFINITY;
         if (have) {
           if (La == -INFINITY) {
-            wb = 1.f / lt;
+            wb = vsc / lt;
             L = lse;
           } else {
             const float Mx = fmaxf(La, lse);
             L = Mx + log2f(exp2f(La - Mx) + exp2f(lse - Mx));
             wa = exp2f(La - L);
-            wb = exp2f(lse - L) / lt;
+            wb = exp2f(lse - L) * vsc / lt;
           }
         } else {
           wa = 1.f;
@@ -569,6 +597,53 @@ __global__ void __launch_bounds__(32 * kFoldWarps) prefill_fold_kernel(const PPa
   if (lane == 0) p.acc_lse2[r] = L;
 }
 
+// ---------------------------------------------------------------- fp16 V
+// max |v| over the window (bf16 element (h, j, d) at h * stride + j * D + d):
+// per-block reduction, one atomicMax on the bit pattern (non-negative floats
+// order like their bits).
+__global__ void __launch_bounds__(256) v16_max_kernel(const uint16_t* v, long long stride, long long win_len,
+                                                      long long n_vec, uint32_t* vmax) {
+  __shared__ float sh[8];
+  float mx = 0.f;
+  const long long per_head = win_len * (kD / 8);
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec; i += (long long)gridDim.x * blockDim.x) {
+    const long long h = i / per_head, r = i - h * per_head;
+    const uint4 x = __ldg(reinterpret_cast<const uint4*>(v + h * stride) + r);
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      mx = fmaxf(mx, fabsf(__uint_as_float(w[e] << 16)));
+      mx = fmaxf(mx, fabsf(__uint_as_float(w[e] & 0xFFFF0000u)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < 8; ++w) mx = fmaxf(mx, sh[w]);
+    atomicMax(vmax, __float_as_uint(mx));
+  }
+}
+
+// V16[h][j][d] = fp16_rn(v * 2^-e); scaling by a power of two is exact
+// outside fp16's subnormal range.
+__global__ void __launch_bounds__(256) v16_convert_kernel(const uint16_t* v, long long stride, long long win_len,
+                                                          long long n_vec, const uint32_t* vmax, uint16_t* v16) {
+  const float sc = ldexpf(1.f, -v16_exponent(*vmax));
+  const long long per_head = win_len * (kD / 8);
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec; i += (long long)gridDim.x * blockDim.x) {
+    const long long h = i / per_head, r = i - h * per_head;
+    const uint4 x = __ldg(reinterpret_cast<const uint4*>(v + h * stride) + r);
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      o[e] = pack_f16x2(__uint_as_float(w[e] << 16) * sc, __uint_as_float(w[e] & 0xFFFF0000u) * sc);
+    reinterpret_cast<uint4*>(v16)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 // ---------------------------------------------------------------- host
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -584,12 +659,13 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-static bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides) {
+static bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                     CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint32_t box[3] = {64, (cuuint32_t)kBM, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = fn(m, dtype, rank, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -633,6 +709,16 @@ static size_t split_bytes(long long n_tiles_total, int nsplit) {
   return nsplit > 1 ? (size_t)n_tiles_total * nsplit * kBM * (kD + 1) * sizeof(float) : 0;
 }
 
+// With a workspace, P.V runs in fp16: after the partials come the window's V
+// as scaled fp16 [Hkv][win_len][D] and the max-|v| word.
+static size_t v16_bytes(long long n_kv_heads, long long win_len) {
+  return (size_t)n_kv_heads * std::max<long long>(win_len, kBN) * kD * 2;
+}
+
+static size_t ws_total(long long n_tiles_total, int nsplit, long long n_kv_heads, long long win_len) {
+  return split_bytes(n_tiles_total, nsplit) + v16_bytes(n_kv_heads, win_len) + 16;
+}
+
 static int resolve_splits(long long tiles, long long win_len, int32_t num_splits, bool have_ws) {
   if (num_splits > 0) return num_splits;
   return have_ws ? plan_splits(tiles, win_len / kBN) : 1;
@@ -649,7 +735,7 @@ extern "C" argus_status argus_window_prefill_workspace_bytes(const argus_geom* g
   if (st != ARGUS_OK) return st;
   if (num_splits < 0 || num_splits > 1024) return argus::fail(ARGUS_E_INVALID, "prefill: num_splits out of range");
   const long long tiles = (long long)g->n_q_heads * n_q / kBM;
-  *bytes = split_bytes(tiles, resolve_splits(tiles, win_len, num_splits, true));
+  *bytes = ws_total(tiles, resolve_splits(tiles, win_len, num_splits, true), g->n_kv_heads, win_len);
   return ARGUS_OK;
 }
 
@@ -689,13 +775,22 @@ extern "C" argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n
   const long long tiles_total = (long long)p.n_tiles * g->n_kv_heads;
   if (num_splits < 0 || num_splits > 1024) return fail(ARGUS_E_INVALID, "prefill: num_splits out of range");
   p.nsplit = resolve_splits(tiles_total, win_len, num_splits, ws != nullptr);
-  if (p.nsplit > 1) {
-    const size_t need = split_bytes(tiles_total, p.nsplit);
-    if (!ws || ws_bytes < need) return fail(ARGUS_E_WORKSPACE, "prefill: workspace %zu < %zu", ws_bytes, need);
-    p.ws_o = static_cast<float*>(ws);
-    p.ws_lse = p.ws_o + (size_t)tiles_total * p.nsplit * kBM * kD;
-  }
   if (p.nsplit > 65535) return fail(ARGUS_E_UNSUPPORTED, "prefill: too many splits");
+  const bool f16p = ws != nullptr;
+  uint16_t* v16 = nullptr;
+  uint32_t* vmax = nullptr;
+  if (p.nsplit > 1 || f16p) {
+    const size_t need = ws_total(tiles_total, p.nsplit, g->n_kv_heads, win_len);
+    if (!ws || ws_bytes < need) return fail(ARGUS_E_WORKSPACE, "prefill: workspace %zu < %zu", ws_bytes, need);
+    uint8_t* w8 = static_cast<uint8_t*>(ws);
+    if (p.nsplit > 1) {
+      p.ws_o = reinterpret_cast<float*>(w8);
+      p.ws_lse = p.ws_o + (size_t)tiles_total * p.nsplit * kBM * kD;
+    }
+    v16 = reinterpret_cast<uint16_t*>(w8 + split_bytes(tiles_total, p.nsplit));
+    vmax = reinterpret_cast<uint32_t*>(w8 + split_bytes(tiles_total, p.nsplit) + v16_bytes(g->n_kv_heads, win_len));
+    p.vmax_bits = vmax;
+  }
   CUtensorMap mq, mk, mv;
   const cuuint64_t qd[2] = {(cuuint64_t)kD, (cuuint64_t)g->n_q_heads * n_q};
   const cuuint64_t qs[1] = {(cuuint64_t)kD * 2};
@@ -704,18 +799,41 @@ extern "C" argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n
   const cuuint64_t ks[2] = {(cuuint64_t)kD * 2, (cuuint64_t)stride * 2};
   if (!make_map(&mq, q, 2, qd, qs)) return fail(ARGUS_E_LAUNCH, "prefill: tensor map for q failed");
   if (!make_map(&mk, win_len > 0 ? k : q, 3, kd, ks)) return fail(ARGUS_E_LAUNCH, "prefill: tensor map for k failed");
-  if (!make_map(&mv, win_len > 0 ? v : q, 3, kd, ks)) return fail(ARGUS_E_LAUNCH, "prefill: tensor map for v failed");
+  if (f16p) {
+    const cuuint64_t vd[3] = {(cuuint64_t)kD, (cuuint64_t)wl, (cuuint64_t)g->n_kv_heads};
+    const cuuint64_t vs[2] = {(cuuint64_t)kD * 2, (cuuint64_t)wl * kD * 2};
+    if (!make_map(&mv, v16, 3, vd, vs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
+      return fail(ARGUS_E_LAUNCH, "prefill: tensor map for the fp16 v failed");
+  } else if (!make_map(&mv, win_len > 0 ? v : q, 3, kd, ks)) {
+    return fail(ARGUS_E_LAUNCH, "prefill: tensor map for v failed");
+  }
   static bool configured[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(ARGUS_E_LAUNCH, "prefill: no device");
   if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "prefill: smem attribute: %s", cudaGetErrorString(e));
     configured[dev] = true;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (f16p) {
+    // the window's V in fp16, scaled by 2^-e from its max |v|
+    if (cudaMemsetAsync(vmax, 0, sizeof(uint32_t), s) != cudaSuccess)
+      return fail(ARGUS_E_LAUNCH, "prefill: clearing the max word failed");
+    const long long n_vec = (long long)g->n_kv_heads * win_len * (kD / 8);
+    const int blocks = (int)std::max<long long>(1, std::min<long long>((n_vec + 255) / 256, 8LL * device_sm_count()));
+    if (win_len > 0) {
+      v16_max_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint16_t*>(v), stride, win_len, n_vec, vmax);
+      v16_convert_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint16_t*>(v), stride, win_len, n_vec, vmax, v16);
+      argus_status stc = launch_status("argus_window_prefill_attn (fp16 v)");
+      if (stc != ARGUS_OK) return stc;
+    }
+  }
   dim3 grid(p.n_tiles, g->n_kv_heads, p.nsplit);
-  prefill_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
+  if (f16p) prefill_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
+  else prefill_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
   argus_status st = launch_status("argus_window_prefill_attn");
   if (st != ARGUS_OK || p.nsplit == 1) return st;
   const long long n_rows = (long long)g->n_q_heads * n_q;

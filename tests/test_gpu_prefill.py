@@ -30,16 +30,25 @@ def _data(Hq, Hkv, n_q, ctx, seed):
     return q, k, v, f(q), f(k), f(v)
 
 
-def _ws(g, n_q, win_len, splits):
-    """A NaN-filled workspace for `splits` key ranges (None for one range)."""
-    if splits == 1:
+# (num_splits, workspace): no workspace = bf16 P.V with a hi + lo P, one CTA
+# per tile; with a workspace = fp16 P.V over the scaled fp16 copy of V, with
+# one or more key ranges per tile
+MODES = [(1, False), (1, True), (3, True)]
+
+
+def _ws(g, n_q, win_len, splits, use_ws=True):
+    """A NaN-filled workspace for `splits` key ranges, or None."""
+    if not use_ws:
         return None
     n = argus.window_prefill_workspace_bytes(g, n_q, win_len, splits)
     return torch.full((max(n, 16) // 4,), float("nan"), dtype=torch.float32, device=DEV)
 
 
-def _run_windows(Hq, Hkv, n_q, ctx, windows, seed, scale=None, splits=1):
+def _run_windows(Hq, Hkv, n_q, ctx, windows, seed, scale=None, splits=1, use_ws=False, vmul=1.0):
     q, k, v, q64, k64, v64 = _data(Hq, Hkv, n_q, ctx, seed)
+    if vmul != 1.0:
+        v = (v.float() * vmul).to(torch.bfloat16)
+        v64 = C.bf16_bits_to_f64(W.to_bits(v))
     scale = W.softmax_scale(128) if scale is None else scale
     g = argus.geom(Hq, Hkv, 128, 16)
     qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
@@ -47,7 +56,7 @@ def _run_windows(Hq, Hkv, n_q, ctx, windows, seed, scale=None, splits=1):
     acc_o = torch.zeros((Hq, n_q, 128), dtype=torch.float32, device=DEV)
     acc_l = torch.full((Hq, n_q), float("-inf"), dtype=torch.float32, device=DEV)
     for wi, (w0, w1) in enumerate(windows):
-        ws = _ws(g, n_q, w1 - w0, splits)
+        ws = _ws(g, n_q, w1 - w0, splits, use_ws)
         argus.window_prefill_attn(g, n_q, qd, kd[:, w0:], vd[:, w0:], kv_len * 128, w1 - w0, w0, ctx, scale,
                                   acc_o, acc_l, 1 if wi > 0 else 0, num_splits=splits, ws=ws)
     torch.cuda.synchronize()
@@ -62,17 +71,17 @@ def _check(go, gl, ro, rl):
     assert np.abs(gl - rl).max() <= 1e-4 * np.abs(rl).max() + 1e-5
 
 
-@pytest.mark.parametrize("splits", [1, 2])
-def test_single_window_full_view_small(splits):
-    go, gl, ro, rl = _run_windows(1, 1, 128, 128, [(0, 128)], seed=501, splits=splits)
+@pytest.mark.parametrize("splits,use_ws", MODES + [(2, True)])
+def test_single_window_full_view_small(splits, use_ws):
+    go, gl, ro, rl = _run_windows(1, 1, 128, 128, [(0, 128)], seed=501, splits=splits, use_ws=use_ws)
     # the chunk itself is not part of this window: compare against the cache-only oracle
     q, k, v, q64, k64, v64 = _data(1, 1, 128, 128, 501)
     ro, rl = oracle.window_attention(q64, k64[:, :128], v64[:, :128], 0, 128, W.softmax_scale(128))
     _check(go, gl, ro, rl)
 
 
-@pytest.mark.parametrize("splits", [1, 2, 5])
-def test_causal_chunk_window_only(splits):
+@pytest.mark.parametrize("splits,use_ws", MODES + [(2, True), (5, True)])
+def test_causal_chunk_window_only(splits, use_ws):
     # a 256-row chunk attending only to itself: causal inside the chunk; with 5
     # key ranges over at most 2 visible blocks some ranges are empty
     q, k, v, q64, k64, v64 = _data(2, 1, 256, 0, 503)
@@ -80,23 +89,24 @@ def test_causal_chunk_window_only(splits):
     acc_o = torch.empty((2, 256, 128), dtype=torch.float32, device=DEV)
     acc_l = torch.empty((2, 256), dtype=torch.float32, device=DEV)
     argus.window_prefill_attn(g, 256, q.to(DEV), k.to(DEV), v.to(DEV), 0, 256, 1000, 1000,
-                              W.softmax_scale(128), acc_o, acc_l, 0, num_splits=splits, ws=_ws(g, 256, 256, splits))
+                              W.softmax_scale(128), acc_o, acc_l, 0, num_splits=splits,
+                              ws=_ws(g, 256, 256, splits, use_ws))
     torch.cuda.synchronize()
     ro, rl = oracle.window_attention(q64, k64, v64, 1000, 1000, W.softmax_scale(128))
     _check(acc_o.cpu().numpy(), acc_l.cpu().numpy(), ro, rl)
 
 
-@pytest.mark.parametrize("splits", [1, 3])
+@pytest.mark.parametrize("splits,use_ws", MODES)
 @pytest.mark.parametrize("Hq,Hkv", [(2, 1), (16, 2)])
-def test_windows_folded_equal_single_pass(Hq, Hkv, splits):
+def test_windows_folded_equal_single_pass(Hq, Hkv, splits, use_ws):
     n_q, ctx = 256, 768
     windows = [(0, 256), (256, 768), (768, 1024)]      # two cache windows, then the chunk
-    go, gl, ro, rl = _run_windows(Hq, Hkv, n_q, ctx, windows, seed=505 + Hq, splits=splits)
+    go, gl, ro, rl = _run_windows(Hq, Hkv, n_q, ctx, windows, seed=505 + Hq, splits=splits, use_ws=use_ws)
     _check(go, gl, ro, rl)
 
 
-@pytest.mark.parametrize("splits", [1, 4])
-def test_window_beyond_every_query_is_identity(splits):
+@pytest.mark.parametrize("splits,use_ws", MODES + [(4, True)])
+def test_window_beyond_every_query_is_identity(splits, use_ws):
     q, k, v, q64, k64, v64 = _data(2, 1, 128, 256, 509)
     g = argus.geom(2, 1, 128, 16)
     acc_o = torch.randn((2, 128, 128), device=DEV)
@@ -104,7 +114,8 @@ def test_window_beyond_every_query_is_identity(splits):
     o0, l0 = acc_o.clone(), acc_l.clone()
     # keys at positions 10_000.. are after every query (positions 256..383)
     argus.window_prefill_attn(g, 128, q.to(DEV), k.to(DEV), v.to(DEV), 0, 128, 10_000, 256,
-                              W.softmax_scale(128), acc_o, acc_l, 1, num_splits=splits, ws=_ws(g, 128, 128, splits))
+                              W.softmax_scale(128), acc_o, acc_l, 1, num_splits=splits,
+                              ws=_ws(g, 128, 128, splits, use_ws))
     torch.cuda.synchronize()
     assert torch.equal(acc_o, o0) and torch.equal(acc_l, l0)
 
@@ -125,7 +136,17 @@ def test_automatic_splits_with_a_long_window():
     Hq, Hkv, n_q, ctx = 16, 2, 128, 4096
     g = argus.geom(Hq, Hkv, 128, 16)
     assert argus.window_prefill_workspace_bytes(g, n_q, ctx, 0) > 0
-    go, gl, ro, rl = _run_windows(Hq, Hkv, n_q, ctx, [(0, ctx), (ctx, ctx + n_q)], seed=511, splits=0)
+    go, gl, ro, rl = _run_windows(Hq, Hkv, n_q, ctx, [(0, ctx), (ctx, ctx + n_q)], seed=511, splits=0,
+                                  use_ws=True)
+    _check(go, gl, ro, rl)
+
+
+@pytest.mark.parametrize("vmul", [3.0e5, 2.0 ** -20])
+def test_fp16_value_path_scales_v_outside_the_fp16_range(vmul):
+    """V far above fp16's range is scaled by a power of two before the fp16
+    copy (and the output scaled back); V far below keeps its accuracy."""
+    go, gl, ro, rl = _run_windows(2, 1, 128, 256, [(0, 256), (256, 384)], seed=513, splits=2, use_ws=True,
+                                  vmul=vmul)
     _check(go, gl, ro, rl)
 
 
