@@ -154,9 +154,9 @@ typedef struct {
   const int32_t* sel_count;   /* device [B][Hkv] entries used, or NULL */
   int32_t sel_width;
   float softmax_scale;
-  void* out;                  /* device [B][Hq][D] in out_dtype, or NULL */
+  void* out;                  /* device [B][Hq][D] in out_dtype (8-byte aligned), or NULL */
   int32_t out_dtype;          /* ARGUS_FP16 or ARGUS_BF16 */
-  float* out_f32;             /* device [B][Hq][D] fp32 output, or NULL */
+  float* out_f32;             /* device [B][Hq][D] fp32 output (16-byte aligned), or NULL */
   float* lse2_out;            /* device [B][Hq] log2-sum-exp, or NULL */
   uint32_t* status;           /* device uint32 anomaly counter, or NULL */
   int32_t num_splits;         /* context splits per (b, KV head); 0 = automatic */

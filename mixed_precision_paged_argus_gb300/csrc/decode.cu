@@ -635,13 +635,24 @@ __global__ void __launch_bounds__(Warps<D>::kThreads, Layout<D>::kMinBlocks)
   {
     float qv[D / 4];
     const bool live = r < G;
+    // every query load of this lane is issued here, in one round trip: the
+    // run layout (x32) and the byte-codec layout (x64)
+    uint4 x32[D / 32], x64[D / 64][2];
+    {
+      const uint16_t* qrow = reinterpret_cast<const uint16_t*>(p.q) + (row0 + r) * D;
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i)
+        x32[i] = live ? *reinterpret_cast<const uint4*>(qrow + 32 * i + 8 * t) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int j = 0; j < D / 64; ++j) {
+        const bool need = live && FAM != kFamBF16;
+        x64[j][0] = need ? *reinterpret_cast<const uint4*>(qrow + 64 * j + 16 * t) : make_uint4(0, 0, 0, 0);
+        x64[j][1] = need ? *reinterpret_cast<const uint4*>(qrow + 64 * j + 16 * t + 8) : make_uint4(0, 0, 0, 0);
+      }
+    }
 #pragma unroll
     for (int i = 0; i < D / 32; ++i) {
-      uint4 x = make_uint4(0, 0, 0, 0);
-      if (live) {
-        const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) + (row0 + r) * D + 32 * i + 8 * t;
-        x = *reinterpret_cast<const uint4*>(qp);
-      }
+      const uint4 x = x32[i];
       const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -691,13 +702,7 @@ __global__ void __launch_bounds__(Warps<D>::kThreads, Layout<D>::kMinBlocks)
       // the same query values (same fp16 rounding) in the byte-codec order
 #pragma unroll
       for (int j = 0; j < D / 64; ++j) {
-        uint4 x[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-        if (r < G) {
-          const uint4* qp = reinterpret_cast<const uint4*>(
-              reinterpret_cast<const uint16_t*>(p.q) + (row0 + r) * D + 64 * j + 16 * t);
-          x[0] = qp[0];
-          x[1] = qp[1];
-        }
+        const uint4* x = x64[j];
         const uint32_t wv[8] = {x[0].x, x[0].y, x[0].z, x[0].w, x[1].x, x[1].y, x[1].z, x[1].w};
         float e16[16];
 #pragma unroll
@@ -877,8 +882,6 @@ __global__ void __launch_bounds__(Warps<D>::kThreads, Layout<D>::kMinBlocks)
   consumer_bar<kConsumerWarps>();  // every warp is done with the stage ring; reuse it
   float* red_o = reinterpret_cast<float*>(smem);               // [warps][8][D]
   float* red_ml = red_o + kConsumerWarps * kMaxG * D;          // [warps][8][2]
-  float* red_w = red_ml + kConsumerWarps * kMaxG * 2;          // [warps][8] merge weights
-  float* red_lse = red_w + kConsumerWarps * kMaxG;             // [8]
 #pragma unroll
   for (int j = 0; j < MB; ++j) {
     const int d0 = DL * r + 2 * j, d1 = d0 + 1;
@@ -894,10 +897,12 @@ __global__ void __launch_bounds__(Warps<D>::kThreads, Layout<D>::kMinBlocks)
     red_ml[(warp * kMaxG + 2 * t + 1) * 2 + 1] = l1;
   }
   consumer_bar<kConsumerWarps>();
+  // one float4 of one head per thread (G * D / 4 <= consumer threads): each
+  // thread forms its head's merge weights itself, so no further barrier
+  static_assert(kMaxG * D / 4 <= kConsumerWarps * 32, "one float4 per consumer thread");
   const int tid = threadIdx.x;
-  const int nthr = kConsumerWarps * 32;
-  if (tid < G) {  // per head: weight of each warp's partial, and the CTA's lse
-    const int g = tid;
+  const int g = tid / (D / 4), c4 = tid - g * (D / 4);
+  if (g < G) {
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_ml[(w * kMaxG + g) * 2]);
@@ -909,32 +914,37 @@ __global__ void __launch_bounds__(Warps<D>::kThreads, Layout<D>::kMinBlocks)
       Lsum += red_ml[(w * kMaxG + g) * 2 + 1] * f[w];
     }
     const float inv = (Lsum > 0.f) ? 1.f / Lsum : 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) red_w[w * kMaxG + g] = f[w] * inv;
-    red_lse[g] = (Lsum > 0.f) ? M + log2f(Lsum) : -INFINITY;
-  }
-  consumer_bar<kConsumerWarps>();
-  const bool direct = (n_active == 1);
-  const size_t bh = (size_t)b * Hkv + h;
-  float* po_bh = p.part_o + bh * p.num_splits * G * D;
-  float* pl_bh = p.part_lse + bh * p.num_splits * G;
-  for (int idx = tid; idx < G * D; idx += nthr) {
-    const int g = idx / D, dd = idx - g * D;
-    float o = 0.f;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) o += red_w[w * kMaxG + g] * red_o[(w * kMaxG + g) * D + dd];
-    const float lse2 = red_lse[g];
-    if (direct) {
-      const size_t oi = (row0 + g) * D + dd;
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float4 x = *reinterpret_cast<const float4*>(red_o + (w * kMaxG + g) * D + 4 * c4);
+      const float fw = f[w] * inv;
+      o.x += fw * x.x;
+      o.y += fw * x.y;
+      o.z += fw * x.z;
+      o.w += fw * x.w;
+    }
+    const float lse2 = (Lsum > 0.f) ? M + log2f(Lsum) : -INFINITY;
+    if (n_active == 1) {
+      const size_t oi = (row0 + g) * D + 4 * c4;
       if (p.out) {
-        if (p.out_bf16) reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
-        else reinterpret_cast<__half*>(p.out)[oi] = __float2half_rn(o);
+        uint2 v2;
+        if (p.out_bf16) {
+          v2.x = pack_bf16x2(o.x, o.y);
+          v2.y = pack_bf16x2(o.z, o.w);
+        } else {
+          v2.x = pack_f16x2(o.x, o.y);
+          v2.y = pack_f16x2(o.z, o.w);
+        }
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.out) + oi) = v2;
       }
-      if (p.out_f32) p.out_f32[oi] = o;
-      if (p.lse2_out && dd == 0) p.lse2_out[row0 + g] = lse2;
+      if (p.out_f32) *reinterpret_cast<float4*>(p.out_f32 + oi) = o;
+      if (p.lse2_out && c4 == 0) p.lse2_out[row0 + g] = lse2;
     } else {
-      po_bh[((size_t)split * G + g) * D + dd] = o;
-      if (dd == 0) pl_bh[(size_t)split * G + g] = lse2;
+      const size_t bh = (size_t)b * Hkv + h;
+      float* po = p.part_o + (bh * p.num_splits + split) * G * D + (size_t)g * D + 4 * c4;
+      *reinterpret_cast<float4*>(po) = o;
+      if (c4 == 0) p.part_lse[(bh * p.num_splits + split) * G + g] = lse2;
     }
   }
 }
@@ -1192,6 +1202,8 @@ static argus_status check_io(const argus_decode_args* a) {
     return fail(ARGUS_E_INVALID, "decode: q, page_codec, block_table and seq_lens are required");
   if (reinterpret_cast<uintptr_t>(a->q) & 15) return fail(ARGUS_E_INVALID, "decode: q not 16-byte aligned");
   if (!a->out && !a->out_f32 && !a->lse2_out) return fail(ARGUS_E_INVALID, "decode: no output given");
+  if ((reinterpret_cast<uintptr_t>(a->out) & 7) || (reinterpret_cast<uintptr_t>(a->out_f32) & 15))
+    return fail(ARGUS_E_INVALID, "decode: out must be 8-byte and out_f32 16-byte aligned");
   return ARGUS_OK;
 }
 
@@ -1247,6 +1259,7 @@ extern "C" argus_status argus_paged_decode_attn(const argus_decode_args* a, void
   if ((st = check_io(a)) != ARGUS_OK) return st;
   if (ws_bytes < pl.ws_bytes || (pl.num_splits > 1 && !ws))
     return fail(ARGUS_E_WORKSPACE, "decode: workspace %zu bytes < %zu needed", ws_bytes, pl.ws_bytes);
+  if (reinterpret_cast<uintptr_t>(ws) & 15) return fail(ARGUS_E_INVALID, "decode: workspace not 16-byte aligned");
   return run(a, pl, ws, stream);
 }
 
