@@ -223,9 +223,9 @@ argus_status argus_paged_decode_attn_noalloc(const argus_decode_args* args, void
  *   -1.  Entries that do not fit in sel_width are dropped, lowest score first,
  *   and counted in *drop_counter.
  * Arguments: q device [B][Hq][D] (q_dtype FP16 / BF16); ckeys device bf16
- * [B][max_pages][Hkv][D] in logical page order; n_pages device int32 [B]
+ * [B][max_pages][Hkv][D] in logical page order (q and ckeys 16-byte aligned); n_pages device int32 [B]
  * (values above max_pages are clamped and counted as drops); ws of
- * argus_select_workspace_bytes bytes.
+ * argus_select_workspace_bytes bytes.  max_pages is at most 65535.
  * ------------------------------------------------------------------------- */
 argus_status argus_select_workspace_bytes(const argus_geom* g, int32_t batch,
                                           int32_t max_pages, size_t* bytes);

@@ -1122,8 +1122,13 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
   if (a->num_splits > 0) {
     cps = (max_chunks + a->num_splits - 1) / a->num_splits;
   } else {
+    // Dense pages: about eight CTAs per SM, so that rows of unequal length
+    // balance.  Selected pages: the list width bounds the work but typically
+    // about half of it is used, and each split is a CTA that pays the whole
+    // lookup-and-load latency; one CTA per resident slot does best there.
     const long long total = (long long)std::max(a->batch, 1) * g.n_kv_heads * max_chunks;
-    const long long target = 8LL * device_sm_count();
+    const long long slots = (long long)device_sm_count() * (g.head_dim == 64 ? 2 : 1);
+    const long long target = a->sel_pages ? slots : 8LL * device_sm_count();
     cps = std::max<long long>(kChunksPerStage, (total + target - 1) / target);
   }
   cps = std::max<long long>(cps, (max_chunks + kMaxSplits - 1) / kMaxSplits);

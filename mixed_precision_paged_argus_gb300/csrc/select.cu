@@ -17,10 +17,9 @@
 // G-query sum is formed once per CTA in shared memory; each lane keeps eight
 // rows' loads in flight; scores are stored as order-preserving uint32 keys.
 // (2) top-k: one CTA per (batch row, KV head) stages the row's keys in shared
-// memory, radix-selects the k-th largest (8-bit passes, shared-memory
-// histograms, bins chosen by a parallel scan, early exit when a bin is taken
-// whole), then compacts the chosen pages in ascending order with block-wide
-// prefix sums.
+// memory, finds the k-th largest key bit by bit with block-wide counts (one
+// barrier per bit), then compacts the chosen pages in ascending order with
+// block-wide prefix sums.
 #include <algorithm>
 
 #include "common.cuh"
@@ -29,8 +28,9 @@ namespace argus {
 namespace select {
 
 constexpr int kScoreThreads = 256;
-constexpr int kPagesPerCta = 64;
+constexpr int kScoreCtasPerSm = 3;          // resident score CTAs per SM (register-limited)
 constexpr int kTopkThreads = 512;
+constexpr int kKeysPerThread = 8;             // top-k keys held in registers per thread
 constexpr int kRowBatch = 8;               // compressed-key loads in flight per lane
 constexpr int kTopkSmemKeys = 40 * 1024;   // rows up to this many pages are staged in shared memory
 
@@ -42,27 +42,42 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 
 // Writes the order key of each page's score, [B][Hkv][max_pages] uint32.
 template <int D, bool QBF16>
-__global__ void __launch_bounds__(kScoreThreads) score_kernel(int Hkv, int G, int max_pages,
+__global__ void __launch_bounds__(kScoreThreads) score_kernel(int Hkv, int G, int max_pages, int ppc,
                                                               const void* __restrict__ q,
                                                               const uint16_t* __restrict__ ckeys,
                                                               const int32_t* __restrict__ n_pages,
                                                               uint32_t* __restrict__ keys) {
   extern __shared__ float qsum[];  // [Hkv][D]
   const int b = blockIdx.y;
-  const int p0 = blockIdx.x * kPagesPerCta;
+  const int p0 = blockIdx.x * ppc;
   const int Hq = Hkv * G;
   int n = n_pages[b];
   n = max(0, min(n, max_pages));
   if (p0 >= n) return;
   const uint16_t* qb = static_cast<const uint16_t*>(q) + (size_t)b * Hq * D;
-  for (int idx = threadIdx.x; idx < Hkv * D; idx += blockDim.x) {
-    const int h = idx / D, d = idx - h * D;
-    float s = 0.f;
-    for (int g = 0; g < G; ++g) {
-      const uint16_t bits = qb[(size_t)(h * G + g) * D + d];
-      s += QBF16 ? __uint_as_float((uint32_t)bits << 16) : __half2float(__ushort_as_half(bits));
+  // G-query sums: a thread per (KV head, 8 dims); the rows' 16-byte loads are
+  // issued together, eight at a time
+  for (int idx = threadIdx.x; idx < Hkv * (D / 8); idx += blockDim.x) {
+    const int h = idx / (D / 8), c = idx - h * (D / 8);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int g0 = 0; g0 < G; g0 += 8) {
+      uint4 xs[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        xs[u] = (g0 + u < G) ? *reinterpret_cast<const uint4*>(qb + (size_t)(h * G + g0 + u) * D + 8 * c)
+                             : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t w[4] = {xs[u].x, xs[u].y, xs[u].z, xs[u].w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t bits = (w[e / 2] >> (16 * (e & 1))) & 0xFFFFu;
+          acc[e] += QBF16 ? __uint_as_float(bits << 16) : __half2float(__ushort_as_half((unsigned short)bits));
+        }
+      }
     }
-    qsum[idx] = s;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) qsum[h * D + 8 * c + e] = acc[e];
   }
   __syncthreads();
   constexpr int LPH = D / 8;               // lanes per (page, head) row, 16 bytes each
@@ -70,7 +85,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(int Hkv, int G, in
   constexpr int RPP = (kScoreThreads / 32) * RPW;  // rows per CTA and pass
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = lane / LPH, li = lane % LPH;
-  const int p_end = min(n, p0 + kPagesPerCta);
+  const int p_end = min(n, p0 + ppc);
   const int n_rows = (p_end - p0) * Hkv;
   // rows of this CTA are contiguous in the slab: (p0 * Hkv + row) * D
   const uint16_t* base = ckeys + (((size_t)b * max_pages + p0) * Hkv) * D + 8 * li;
@@ -139,9 +154,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pag
                                                             int32_t* sel_pages, int32_t* sel_count, int width,
                                                             uint32_t* drops, int stage) {
   extern __shared__ uint32_t skeys[];
-  __shared__ int hist[256];
   __shared__ int sh_scan[32];
-  __shared__ int sh_sel[3];
+  __shared__ uint32_t sh_cnt[4][32];
   const int h = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5;
@@ -157,61 +171,81 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pag
   const int k_want = min(top_k, n_cand);
   const int k = max(0, min(k_want, room));
   if (tid == 0) dropped += (uint32_t)(k_want - k);
-  if (stage) {
-    for (int p = tid; p < n_cand; p += nthr) skeys[p] = keys[p];
+  if (stage) {  // eight loads in flight per thread
+    for (int p0 = 0; p0 < n_cand; p0 += 8 * nthr) {
+      uint32_t v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int pk = p0 + k * nthr + tid;
+        v[k] = pk < n_cand ? keys[pk] : 0u;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int pk = p0 + k * nthr + tid;
+        if (pk < n_cand) skeys[pk] = v[k];
+      }
+    }
     keys = skeys;
     __syncthreads();
   }
 
-  // Threshold on the masked key: all candidates with (key & mask) > T are
-  // taken, and the first k_rem (in page order) with (key & mask) == T.  Radix
-  // select from the top byte down; a pass that lands on a bin taken whole
-  // ends the search early.
-  uint32_t T = 0u, mask = 0u;
+  // Threshold: T = the k-th largest key, found bit by bit from the top as the
+  // largest value with at least k keys >= T (block-wide counts: per-warp
+  // reductions, double-buffered partial sums, one barrier per bit).  All keys
+  // > T are taken, and the first k_rem (in page order) equal to T.
+  const uint32_t mask = 0xFFFFFFFFu;
+  uint32_t T = 0u;
   int k_rem = 0;
   if (k > 0 && k < n_cand) {
-    int need = k;
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      if (tid < 256) hist[tid] = 0;
-      __syncthreads();
-      for (int p = tid; p < n_cand; p += nthr) {
-        const uint32_t key = keys[p];
-        if ((key & mask) == T) atomicAdd(&hist[(key >> shift) & 255], 1);
-      }
-      __syncthreads();
-      // bins from the top: thread t holds bin 255 - t; inclusive prefix over threads
-      int c = 0, x = 0;
-      if (tid < 256) {
-        c = hist[255 - tid];
-        x = c;
+    // up to kKeysPerThread keys per thread live in registers; longer rows are
+    // re-read from memory every bit
+    constexpr int KPT = kKeysPerThread;
+    const bool in_regs = n_cand <= KPT * nthr;
+    uint32_t kr[KPT];
+    bool kv[KPT];
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, x, o);
-          if (lane >= o) x += y;
-        }
-        if (lane == 31) sh_scan[warp] = x;
-      }
-      __syncthreads();
-      if (tid < 256) {
-        int before = 0;
-        for (int w = 0; w < warp; ++w) before += sh_scan[w];
-        const int incl = before + x;
-        if (incl >= need && incl - c < need) {
-          sh_sel[0] = 255 - tid;
-          sh_sel[1] = need - (incl - c);
-          sh_sel[2] = c;
-        }
-      }
-      __syncthreads();
-      T |= (uint32_t)sh_sel[0] << shift;
-      mask |= 255u << shift;
-      need = sh_sel[1];
-      const bool whole_bin = (need == sh_sel[2]);
-      __syncthreads();
-      if (whole_bin) break;
+    for (int j = 0; j < KPT; ++j) {
+      const int pk = tid + j * nthr;
+      kv[j] = in_regs && pk < n_cand;
+      kr[j] = kv[j] ? keys[pk] : 0u;
     }
-    k_rem = need;
+    // counts of keys >= a, >= b (strict: > a) packed as two 16-bit fields
+    // (a row has at most kTopkSmemKeys < 2^16 candidates), one reduction
+    auto count2 = [&](uint32_t a, uint32_t b, bool strict) -> uint32_t {
+      uint32_t c = 0;
+      if (in_regs) {
+#pragma unroll
+        for (int j = 0; j < KPT; ++j)
+          c += kv[j] ? ((strict ? kr[j] > a : kr[j] >= a) ? 1u : 0u) + (kr[j] >= b ? 0x10000u : 0u) : 0u;
+      } else {
+        for (int pk = tid; pk < n_cand; pk += nthr) {
+          const uint32_t x = keys[pk];
+          c += ((strict ? x > a : x >= a) ? 1u : 0u) + (x >= b ? 0x10000u : 0u);
+        }
+      }
+      return __reduce_add_sync(0xffffffffu, c);
+    };
+    // block total: each warp posts its count, then every warp sums the posts
+    // (one per lane) -- one barrier per round, buffers alternate
+    auto block_total = [&](uint32_t c, int buf) -> uint32_t {
+      if (lane == 0) sh_cnt[buf][warp] = c;
+      __syncthreads();
+      const uint32_t x = lane < (nthr >> 5) ? sh_cnt[buf][lane] : 0u;
+      return __reduce_add_sync(0xffffffffu, x);
+    };
+    // two bits per round: candidates T|01, T|10, T|11 in bits (b+1, b)
+    for (int b = 30, round = 0; b >= 0; b -= 2, ++round) {
+      const uint32_t c1 = T | (1u << b), c2 = T | (2u << b), c3 = T | (3u << b);
+      const uint32_t n12 = block_total(count2(c1, c2, false), round & 1);
+      const uint32_t n3 = block_total(count2(c3, 0xFFFFFFFFu, false), 2 + (round & 1)) & 0xFFFFu;
+      const uint32_t n1 = n12 & 0xFFFFu, n2 = n12 >> 16;
+      if (n3 >= (uint32_t)k) T = c3;
+      else if (n2 >= (uint32_t)k) T = c2;
+      else if (n1 >= (uint32_t)k) T = c1;
+    }
+    // rounds used buffers (0, 2) and (1, 3) alternately; the last round (15)
+    // used 1 and 3, so 0 is free
+    k_rem = k - (int)(block_total(count2(T, 0xFFFFFFFFu, true), 0) & 0xFFFFu);
   }
   const bool take_all = (k >= n_cand);
   // per thread: a contiguous range of pages so that scans keep page order
@@ -274,26 +308,32 @@ extern "C" argus_status argus_select_pages(const argus_geom* g, int32_t batch, c
   if (batch < 0 || max_pages <= 0 || top_k < 0 || sel_width <= 0)
     return fail(ARGUS_E_INVALID, "select: bad batch / max_pages / top_k / sel_width");
   if (batch > 65535 || g->n_kv_heads > 65535) return fail(ARGUS_E_UNSUPPORTED, "select: grid too large");
+  if (max_pages > 65535) return fail(ARGUS_E_UNSUPPORTED, "select: max_pages %d (at most 65535)", max_pages);
   if (batch == 0) return ARGUS_OK;
   if (!q || !ckeys || !n_pages || !sel_pages || !sel_count)
     return fail(ARGUS_E_INVALID, "select: NULL pointer");
-  if (reinterpret_cast<uintptr_t>(ckeys) & 15) return fail(ARGUS_E_INVALID, "select: ckeys not 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(ckeys) | reinterpret_cast<uintptr_t>(q)) & 15)
+    return fail(ARGUS_E_INVALID, "select: q and ckeys must be 16-byte aligned");
   size_t need = (size_t)batch * g->n_kv_heads * max_pages * sizeof(uint32_t);
   if (!ws || ws_bytes < need) return fail(ARGUS_E_WORKSPACE, "select: workspace %zu < %zu", ws_bytes, need);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int G = g->n_q_heads / g->n_kv_heads;
   uint32_t* keys = static_cast<uint32_t*>(ws);
-  dim3 grid1((max_pages + select::kPagesPerCta - 1) / select::kPagesPerCta, batch);
+  // pages per CTA: the whole slab in one wave of resident CTAs
+  const long long resident = (long long)device_sm_count() * select::kScoreCtasPerSm;
+  long long ppc = ((long long)batch * max_pages + resident - 1) / resident;
+  ppc = std::max<long long>(8, (ppc + 7) / 8 * 8);
+  dim3 grid1((unsigned)((max_pages + ppc - 1) / ppc), batch);
   const size_t sh = (size_t)g->n_kv_heads * g->head_dim * sizeof(float);
   if (sh > 48 * 1024) return fail(ARGUS_E_UNSUPPORTED, "select: n_kv_heads * head_dim too large");
   const uint16_t* ck = static_cast<const uint16_t*>(ckeys);
   const bool bf = (q_dtype == ARGUS_BF16);
   if (g->head_dim == 64) {
-    if (bf) select::score_kernel<64, true><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, q, ck, n_pages, keys);
-    else select::score_kernel<64, false><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, q, ck, n_pages, keys);
+    if (bf) select::score_kernel<64, true><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, (int)ppc, q, ck, n_pages, keys);
+    else select::score_kernel<64, false><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, (int)ppc, q, ck, n_pages, keys);
   } else {
-    if (bf) select::score_kernel<128, true><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, q, ck, n_pages, keys);
-    else select::score_kernel<128, false><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, q, ck, n_pages, keys);
+    if (bf) select::score_kernel<128, true><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, (int)ppc, q, ck, n_pages, keys);
+    else select::score_kernel<128, false><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, (int)ppc, q, ck, n_pages, keys);
   }
   argus_status st = launch_status("argus_select_pages (score)");
   if (st != ARGUS_OK) return st;
