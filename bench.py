@@ -551,9 +551,11 @@ def leg_prefill(dev, timer, steps, warm, tflops_peak):
                        "causal chunk, 131072-token windows folded by log2-sum-exp",
            "ms": ms, "flops": flops, "tflops": flops / (ms * 1e-3) / 1e12,
            "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / tflops_peak,
-           "splits": argus.window_prefill_workspace_bytes(g, NQ, WIN) // (Hq * NQ * (D_ + 1) * 4),
-           "note": "useful FLOPs 4*D*Hq*visible pairs; the P.V product runs twice (bf16 hi + lo of P); each "
-                   "128-row query tile's window split into key ranges over all SMs, partials folded"}
+           "splits": (argus.window_prefill_workspace_bytes(g, NQ, WIN) - Hkv * WIN * D_ * 2 - 16)
+                     // (Hq * NQ * (D_ + 1) * 4),
+           "note": "useful FLOPs 4*D*Hq*visible pairs; Q.K^T in bf16, P.V in fp16 (P * 2^7, V converted per "
+                   "window to fp16 scaled by a power of two); each 128-row query tile's window split into key "
+                   "ranges over all SMs, partials folded"}
     del q, k, v
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
@@ -579,9 +581,10 @@ def run_legs(steps, warm):
 
 # ---------------------------------------------------------------- oracle leg
 
-def _oracle_layer(layer):
+def _oracle_layer(job):
     """One layer of the mixed-tier workload in the oracle: generate, demote
-    (oracle), then time the decode alone.  Returns seconds of decode."""
+    (oracle), then decode it `reps` times.  Returns (seconds of decode, reps)."""
+    layer, reps = job
     import oracle
     from oracle import codecs as C
     from mixed_precision_paged_argus_gb300 import workloads as W
@@ -597,32 +600,34 @@ def _oracle_layer(layer):
         pools[codec] = (codes, meta)
         table[0, pages] = [0, 1, 2, 3]
     t0 = time.perf_counter()
-    oracle.paged_decode(q64, HKV, P, pools, tiers.reshape(1, -1).astype(np.uint8), table,
-                        np.array([CTX]), float(np.float32(1 / math.sqrt(D))))
-    return time.perf_counter() - t0
+    for _ in range(reps):
+        oracle.paged_decode(q64, HKV, P, pools, tiers.reshape(1, -1).astype(np.uint8), table,
+                            np.array([CTX]), float(np.float32(1 / math.sqrt(D))))
+    return time.perf_counter() - t0, reps
 
 
-def oracle_leg(budget_s=15.0, max_layers=None):
-    """Oracle throughput on the host cores: layers decoded in parallel, one
-    process per core (spawn), until about budget_s of work."""
+def oracle_leg(budget_s=15.0):
+    """Oracle throughput on the host cores: one process per core (spawn), each
+    demoting one layer and then decoding it repeatedly for about budget_s / 2
+    seconds; the rate is the decodes of all processes over the summed time."""
     import multiprocessing as mp
     os.environ.setdefault("OMP_NUM_THREADS", "1")
     os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
     cores = os.cpu_count() or 1
-    t_one = _oracle_layer(0)                       # calibrate (also warms imports)
-    per_core = max(1, int(budget_s / max(t_one, 1e-3) / 2))
-    n_layers = min(LAYERS * 4, cores * per_core) if max_layers is None else max_layers
+    t_one, _ = _oracle_layer((0, 1))               # calibrate (also warms imports)
+    reps = max(1, int(budget_s / 2 / max(t_one, 1e-3)))
     ctx = mp.get_context("spawn")
     t0 = time.perf_counter()
     with ctx.Pool(cores) as pool:
-        decode_s = pool.map(_oracle_layer, [l % LAYERS for l in range(n_layers)])
+        res = pool.map(_oracle_layer, [(l % LAYERS, reps) for l in range(cores)])
     wall = time.perf_counter() - t0
-    # decode-only time per layer per core; throughput across cores
-    per_layer = sum(decode_s) / len(decode_s)
+    n = sum(r for _, r in res)
+    per_layer = sum(t for t, _ in res) / n          # decode seconds per layer-decode on one core
     us_per_token_layer = per_layer / cores * 1e6
     return {"value": us_per_token_layer, "unit": "us/token/layer", "cores": cores, "kind": "oracle",
-            "sample": "%d layer-decodes of the mixed-tier workload (one token, 16384-token context each) on "
-                      "%d processes; decode time only, %.1f s wall incl. oracle demotion" % (n_layers, cores, wall),
+            "sample": "%d layer-decodes of the mixed-tier workload (one token, 16384-token context each; %d "
+                      "layers x %d repeats) on %d processes; decode time only, %.1f s wall incl. oracle "
+                      "demotion" % (n, cores, reps, cores, wall),
             "single_core_us_per_token_layer": per_layer * 1e6}
 
 

@@ -9,7 +9,8 @@ and use inputs larger than L2 where the kernel streams HBM.
   decode_mixed    one layer of the mixed-tier decode (14/2 heads, D 64, 16 pages x 1024)
   decode_bf16     batched BF16 decode, batch 8 of the batched workload's shape
   decode_fp8      the same pages demoted to FP8
-  quantize_fp8    demote 64 Ki 16x128 BF16 units to FP8 (256 MB read)
+  decode_sparse   one layer of the sparse workload: decode over the indexer's selection
+  quantize_fp8    demote 128 Ki 16x128 BF16 units to FP8 (512 MB read)
   quantize_int4   the same to INT4
   select          indexer scores + top-k for one layer of the sparse workload
   prefill         one 131072-token window of the windowed prefill
@@ -80,6 +81,32 @@ def _quantize(dev, codec):
     return lambda: argus.quantize_pages(g, W.BF16, src, n, ids, dst, ids, n)
 
 
+def _decode_sparse(dev):
+    B, Hq, Hkv, D, P, NP, K = 8, 32, 4, 128, 64, 4096, 32
+    width = 2 * K + 8
+    g = argus.geom(Hq, Hkv, D, P)
+    ids = torch.arange(NP, dtype=torch.int32, device=dev)
+    pool = argus.Pool.empty(W.FP8_E4M3, B * NP, Hkv, P, D, device=dev)
+    ck = torch.empty((B, NP, Hkv, D), dtype=torch.bfloat16, device=dev)
+    for b in range(B):
+        src = W.normal((NP, 2, Hkv, P, D), W.BF16, W.seed_of("sparse", 0, 1) * 16 + b, device=dev)
+        argus.quantize_pages(g, W.BF16, src, NP, ids, pool, ids + b * NP, NP, ckey_out=ck[b])
+        del src
+    q = W.normal((B, Hq, D), W.BF16, W.seed_of("sparse", 0, 0), device=dev)
+    npg = torch.full((B,), NP, dtype=torch.int32, device=dev)
+    sel = torch.empty((B, Hkv, width), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B, Hkv), dtype=torch.int32, device=dev)
+    sws = torch.empty(argus.select_workspace_bytes(g, B, NP), dtype=torch.uint8, device=dev)
+    argus.select_pages(g, B, q, ck, npg, NP, K, True, sel, cnt, width, None, sws)
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    a = argus.decode_args(g, B, q, [pool], torch.full((B, NP), W.FP8_E4M3, dtype=torch.uint8, device=dev),
+                          torch.arange(B * NP, dtype=torch.int32, device=dev).reshape(B, NP),
+                          torch.full((B,), NP * P, dtype=torch.int32, device=dev), NP, W.softmax_scale(D), out=out,
+                          sel_pages=sel, sel_count=cnt, sel_width=width)
+    ws = torch.empty(max(1, argus.decode_workspace_bytes(a)), dtype=torch.uint8, device=dev)
+    return lambda: argus.paged_decode_attn(a, ws)
+
+
 def _select(dev):
     B, Hq, Hkv, D, NP, K = 8, 32, 4, 128, 4096, 32
     g = argus.geom(Hq, Hkv, D, 64)
@@ -119,6 +146,7 @@ CASES = {
     "decode_mixed": _decode_mixed,
     "decode_bf16": lambda d: _decode_batched(d, False),
     "decode_fp8": lambda d: _decode_batched(d, True),
+    "decode_sparse": _decode_sparse,
     "quantize_fp8": lambda d: _quantize(d, W.FP8_E4M3),
     "quantize_int4": lambda d: _quantize(d, W.INT4_G32),
     "select": _select,
