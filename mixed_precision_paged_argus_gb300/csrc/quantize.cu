@@ -96,14 +96,29 @@ __device__ __forceinline__ bool e4m3_unsure(float y) {
   return ((low - 0x80000u + 8u) <= 16u) || (fabsf(y) < 0.0157f);  // e4m3 subnormals start below 2^-6
 }
 
-//  integer codes: boundaries are the half-integers; |y| <= 128 keeps the
-//  quotient's ulp <= 2^-17, far inside the 2^-12 guard band.  Rounding to an
+//  integer codes: boundaries are the half-integers.  For |y| <= 128 the
+//  product differs from x / s by at most 128 * 2^-23 = 2^-16 and RN(x / s)
+//  from x / s by at most 2^-18, so a product farther than kIntGuard = 2^-14
+//  from a half-integer rounds like the quotient.  Rounding to an
 //  integer uses the fp32 adder: for |y| < 2^22, y + 1.5 * 2^23 rounds y to the
 //  nearest integer (ties to even) and leaves it in the low mantissa bits, so
 //  neither a round nor a float-to-int conversion instruction is needed.
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr float kIntGuard = 0x1p-14f;
 __device__ __forceinline__ bool rint_unsure(float y, float t) {  // t = y + kRoundMagic
-  return fabsf(y - (t - kRoundMagic)) > 0.5f - 0x1p-12f;
+  return fabsf(y - (t - kRoundMagic)) > 0.5f - kIntGuard;
+}
+
+// The rare exact path: eight IEEE quotients, kept out of line so that the
+// unrolled encoders stay small in the instruction cache.
+struct F8 {
+  float v[8];
+};
+__device__ __noinline__ F8 div8(F8 x, float s) {
+  F8 q;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) q.v[e] = x.v[e] / s;
+  return q;
 }
 
 //  INT4 scale: fp16_sat(RN(a / 15)).  a * RN(1/15) is within 3 ulp of RN(a/15);
@@ -134,22 +149,27 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
   } else if (CODEC == ARGUS_FP8_E4M3) {
     uint32_t w[2] = {0u, 0u};
     if (valid && scale > 0.f) {
+      // the boundary test of e4m3_unsure as running minima: of the distance
+      // (low mantissa bits - midpoint + 8, unsigned) and of |y|
       float y[8];
-      bool unsure = false;
+      uint32_t dmin = 0xFFFFFFFFu;
+      float amin = INFINITY;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         y[e] = f[e] * rscale;
-        unsure |= e4m3_unsure(y[e]);
+        dmin = min(dmin, (__float_as_uint(y[e]) & 0xFFFFFu) - 0x80000u + 8u);
+        amin = fminf(amin, fabsf(y[e]));
       }
-      if (unsure) {
+      if (dmin <= 16u || amin < 0.0157f) {   // near a midpoint, or e4m3 subnormal range
+        F8 x;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = f[e] / scale;
-      }
+        for (int e = 0; e < 8; ++e) x.v[e] = f[e];
+        const F8 q = div8(x, scale);
 #pragma unroll
-      for (int e = 0; e < 8; e += 2) {
-        const uint32_t two = f32x2_to_e4m3x2(y[e], y[e + 1]);
-        w[e / 4] |= two << (16 * ((e / 2) & 1));
+        for (int e = 0; e < 8; ++e) y[e] = q.v[e];
       }
+      w[0] = f32x2_to_e4m3x2(y[0], y[1]) | (f32x2_to_e4m3x2(y[2], y[3]) << 16);
+      w[1] = f32x2_to_e4m3x2(y[4], y[5]) | (f32x2_to_e4m3x2(y[6], y[7]) << 16);
     }
     if (DEQ) {
 #pragma unroll
@@ -159,19 +179,27 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
   } else if (CODEC == ARGUS_INT8) {
     uint32_t w[2] = {0u, 0u};
     if (valid && scale > 0.f) {
-      // clamping before rounding equals clamping the rounded value (integer bounds)
+      // |x * RN(1/s)| <= 127 (1 + 2^-22) while s is a normal number, so the
+      // clamp is needed only for the tiny scales of subnormal units; clamping
+      // before rounding equals clamping the rounded value (integer bounds)
+      const bool clamp = scale < 0x1p-100f;
       uint32_t t[8];
-      bool unsure = false;
+      float dev = 0.f;   // largest distance of a product from its rounded value
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float y = fminf(fmaxf(f[e] * rscale, -127.f), 127.f);
+        float y = f[e] * rscale;
+        if (clamp) y = fminf(fmaxf(y, -127.f), 127.f);
         const float tf = y + kRoundMagic;
-        unsure |= rint_unsure(y, tf);
+        dev = fmaxf(dev, fabsf(y - (tf - kRoundMagic)));
         t[e] = __float_as_uint(tf);
       }
-      if (unsure) {
+      if (dev > 0.5f - kIntGuard) {
+        F8 x;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) t[e] = __float_as_uint(fminf(fmaxf(f[e] / scale, -127.f), 127.f) + kRoundMagic);
+        for (int e = 0; e < 8; ++e) x.v[e] = f[e];
+        const F8 q = div8(x, scale);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) t[e] = __float_as_uint(fminf(fmaxf(q.v[e], -127.f), 127.f) + kRoundMagic);
       }
       // the low byte of the mantissa is the code in two's complement
       w[0] = prmt(prmt(t[0], t[1], 0x0040), prmt(t[2], t[3], 0x0040), 0x5410);
@@ -210,8 +238,12 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
         t[e] = __float_as_uint(tf);
       }
       if (unsure) {
+        F8 x;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) t[e] = __float_as_uint(fminf(fmaxf(d[e] / s, 0.f), 15.f) + kRoundMagic);
+        for (int e = 0; e < 8; ++e) x.v[e] = d[e];
+        const F8 q = div8(x, s);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) t[e] = __float_as_uint(fminf(fmaxf(q.v[e], 0.f), 15.f) + kRoundMagic);
       }
 #pragma unroll
       for (int e = 0; e < 8; ++e) w |= (t[e] & 0xFu) << (4 * e);
@@ -413,6 +445,9 @@ __device__ __forceinline__ void encode_int4_group(const uint4 (&x)[4], bool vali
   uint32_t w[4] = {0u, 0u, 0u, 0u};
   if (valid && s > 0.f) {
     const float r = __frcp_rn(s);
+    // the products are monotone in x: when those of the group's min and max
+    // round into 0..15, no product needs the clamp
+    const bool clamp = !((lo - z) * r > -0.49f && (hi - z) * r < 15.49f);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       float f[8], d[8];
@@ -422,14 +457,19 @@ __device__ __forceinline__ void encode_int4_group(const uint4 (&x)[4], bool vali
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         d[e] = f[e] - z;
-        const float y = fminf(fmaxf(d[e] * r, 0.f), 15.f);
+        float y = d[e] * r;
+        if (clamp) y = fminf(fmaxf(y, 0.f), 15.f);
         const float tf = y + kRoundMagic;
         dev = fmaxf(dev, fabsf(y - (tf - kRoundMagic)));
         t[e] = __float_as_uint(tf);
       }
-      if (dev > 0.5f - 0x1p-12f) {
+      if (dev > 0.5f - kIntGuard) {
+        F8 x;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) t[e] = __float_as_uint(fminf(fmaxf(d[e] / s, 0.f), 15.f) + kRoundMagic);
+        for (int e = 0; e < 8; ++e) x.v[e] = d[e];
+        const F8 q = div8(x, s);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) t[e] = __float_as_uint(fminf(fmaxf(q.v[e], 0.f), 15.f) + kRoundMagic);
       }
       // low bytes of t are the codes 0..15: even elements in the low nibbles
       const uint32_t ev = prmt(prmt(t[0], t[2], 0x0040), prmt(t[4], t[6], 0x0040), 0x5410);
@@ -445,7 +485,9 @@ __device__ __forceinline__ void encode_int4_group(const uint4 (&x)[4], bool vali
 // Units of at most 2048 elements: one warp per unit, held in registers,
 // software-pipelined so that the next unit's loads are in flight while the
 // current one is reduced, encoded and stored.
-template <int D, bool SBF16, int CODEC>
+// CK: compressed keys requested (the kernel is instantiated for both, so that
+// the common case carries no decode-and-sum code)
+template <int D, bool SBF16, int CODEC, bool CK>
 __global__ void __launch_bounds__(kCtaThreads) quantize_small_kernel(const QParams p) {
   constexpr int VPR = D / 8;
   const int lane = threadIdx.x & 31;
@@ -454,7 +496,7 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_small_kernel(const QPara
   const int Hkv = p.Hkv, P = p.P;
   const long long n_units = (long long)p.n_pages * 2 * Hkv;
   const int nvec = P * VPR;
-  const bool want_ck = p.ckey != nullptr;
+  constexpr bool want_ck = CK;
 
   struct Unit {
     const uint4* src;
@@ -476,7 +518,7 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_small_kernel(const QPara
     d.dst = ((size_t)ds * 2 + d.kv) * Hkv + d.h;
     return d;
   };
-  const bool want_ck_any = p.ckey != nullptr;
+  constexpr bool want_ck_any = CK;
   // INT4 units without a compressed key use one lane per 32-element group:
   // slot 4j + m holds vector m of group lane + 32j
   auto group_layout = [&](const Unit& d) {
@@ -611,7 +653,8 @@ static argus_status launch3(const QParams& p, cudaStream_t s) {
   if (small) {
     const long long blocks_needed = (units + (kCtaThreads / 32) - 1) / (kCtaThreads / 32);
     const int blocks = (int)std::max<long long>(1, std::min<long long>(blocks_needed, (long long)sms * 4));
-    quantize_small_kernel<D, SBF16, CODEC><<<blocks, kCtaThreads, 0, s>>>(p);
+    if (p.ckey) quantize_small_kernel<D, SBF16, CODEC, true><<<blocks, kCtaThreads, 0, s>>>(p);
+    else quantize_small_kernel<D, SBF16, CODEC, false><<<blocks, kCtaThreads, 0, s>>>(p);
   } else {
     const int blocks = (int)std::max<long long>(1, std::min<long long>(units, (long long)sms * 8));
     quantize_kernel<D, SBF16, CODEC, kCtaThreads><<<blocks, kCtaThreads, 0, s>>>(p);

@@ -11,6 +11,7 @@ and use inputs larger than L2 where the kernel streams HBM.
   decode_fp8      the same pages demoted to FP8
   decode_sparse   one layer of the sparse workload: decode over the indexer's selection
   quantize_fp8    demote 128 Ki 16x128 BF16 units to FP8 (512 MB read)
+  quantize_int8   the same to INT8
   quantize_int4   the same to INT4
   select          indexer scores + top-k for one layer of the sparse workload
   prefill         one 131072-token window of the windowed prefill
@@ -148,6 +149,7 @@ CASES = {
     "decode_fp8": lambda d: _decode_batched(d, True),
     "decode_sparse": _decode_sparse,
     "quantize_fp8": lambda d: _quantize(d, W.FP8_E4M3),
+    "quantize_int8": lambda d: _quantize(d, W.INT8),
     "quantize_int4": lambda d: _quantize(d, W.INT4_G32),
     "select": _select,
     "prefill": _prefill,
