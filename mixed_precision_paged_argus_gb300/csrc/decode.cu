@@ -40,14 +40,20 @@ namespace decode {
 constexpr int kChunk = 16;
 constexpr int kChunksPerStage = 8;
 
+// Chunks per ring stage: 8, or 16 in the narrow layout -- launches whose pools
+// all hold byte or nibble codes (FP8, INT8, INT4) at head_dim 128, where a
+// chunk slot needs half the bytes.
+template <bool NARROW>
+constexpr int chunks_per_stage() { return NARROW ? 16 : kChunksPerStage; }
+
 // Consumer warps per CTA: head_dim 64 runs 4 warps of two chunks per stage
 // (two CTAs per SM; a second chunk in flight per warp hides MMA latency);
-// head_dim 128 runs 8 warps of one chunk (one CTA per SM, the ring fills
-// shared memory, so latency is hidden by warps instead).
-template <int D>
+// head_dim 128 runs 8 warps, of one chunk (16-bit layout: the ring fills
+// shared memory) or two chunks (narrow layout) per stage.
+template <int D, bool NARROW = false>
 struct Warps {
   static constexpr int kConsumer = (D == 64) ? 4 : 8;
-  static constexpr int kNC = kChunksPerStage / kConsumer;  // chunks per warp and stage
+  static constexpr int kNC = chunks_per_stage<NARROW>() / kConsumer;  // chunks per warp and stage
   static constexpr int kThreads = 32 * (kConsumer + 1);
 };
 constexpr int kMaxG = 8;
@@ -88,22 +94,23 @@ struct ChunkDesc {
   float vscale;
 };
 
-template <int D>
+template <int D, bool NARROW = false>
 struct Layout {
+  static constexpr int kCPS = chunks_per_stage<NARROW>();
   static constexpr int kNI = D / 32;                   // 32-dim groups per row
-  static constexpr int kKV = kChunk * 2 * D;           // K (or V) bytes of a chunk, 16-bit
+  static constexpr int kKV = kChunk * (NARROW ? 1 : 2) * D;   // K (or V) bytes of a chunk slot
   static constexpr int kMeta = kChunk * kNI * 4;       // INT4 {scale, zero} of a chunk
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kKV;
   static constexpr int kOffMK = 2 * kKV;
   static constexpr int kOffMV = 2 * kKV + kMeta;
   static constexpr int kChunkBytes = 2 * kKV + 2 * kMeta;
-  static constexpr int kStageBytes = kChunksPerStage * kChunkBytes;
+  static constexpr int kStageBytes = kCPS * kChunkBytes;
   static constexpr int kStages = 3;
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kBarOff = kRingBytes;
   static constexpr int kDescOff = kBarOff + 2 * kStages * 8;
-  static constexpr int kMiscOff = kDescOff + kStages * kChunksPerStage * (int)sizeof(ChunkDesc);
+  static constexpr int kMiscOff = kDescOff + kStages * kCPS * (int)sizeof(ChunkDesc);
   static constexpr int kSmemBytes = kMiscOff + 64;
   static constexpr int kMinBlocks = (D == 128) ? 1 : 2;  // by shared memory
 };
@@ -127,10 +134,10 @@ __device__ __forceinline__ uint32_t f16_magic_pair(uint32_t u, uint32_t sel) {
 // INT4 pages give the raw codes (exact in fp16) and each row's per-group
 // {scale, zero} in kz, so that the scores can be formed exactly as
 // sum_g scale_g * (q_g . c_g) + zero_g * sum(q_g).
-template <int D>
+template <int D, bool NARROW>
 __device__ __forceinline__ void load_k_frags(int codec, const uint8_t* chunk, int r, int t,
                                              uint32_t (&a)[D / 16][4], float (&kz)[2][D / 32][2]) {
-  using L = Layout<D>;
+  using L = Layout<D, NARROW>;
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
     const int row = r + 8 * rr;
@@ -186,10 +193,10 @@ __device__ __forceinline__ void load_k_frags(int codec, const uint8_t* chunk, in
 // the P.V MMA (M = head_dim, K = tokens).  Lane (r, t) holds dims
 // [DL*r, DL*r + DL) with m-block j covering dims DL*r + 2j (rows r) and
 // DL*r + 2j + 1 (rows r + 8), and token rows 2t, 2t+1 (k 0..7) and 2t+8, 2t+9.
-template <int D>
+template <int D, bool NARROW>
 __device__ __forceinline__ void load_v_frags(int codec, const uint8_t* chunk, int r, int t,
                                              uint32_t (&v)[D / 16][4]) {
-  using L = Layout<D>;
+  using L = Layout<D, NARROW>;
   constexpr int DL = D / 8;
   const int rows[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
   if (codec == ARGUS_FP16 || codec == ARGUS_BF16) {
@@ -294,7 +301,7 @@ __device__ __forceinline__ void load_v_frags(int codec, const uint8_t* chunk, in
 // group is issued before any result is consumed (the m16n8k16 MMA latency is
 // long), with two accumulator chains per chunk.  sv is masked and scaled to
 // the log2 domain; kscale and the query exponent are applied here.
-template <int D, int CODEC, int NCG, bool BF>
+template <int D, int CODEC, int NCG, bool BF, bool NARROW>
 __device__ __forceinline__ void group_scores(const uint8_t* const* cptr, const ChunkDesc* dsc, int r, int t,
                                              const uint32_t (&qf)[D / 16][2], const uint32_t (&qb)[D / 16][2],
                                              const uint32_t (&qf8)[D / 16][2],
@@ -304,7 +311,7 @@ __device__ __forceinline__ void group_scores(const uint8_t* const* cptr, const C
   uint32_t a[NCG][KC][4];
   float kz[NCG][2][D / 32][2];
 #pragma unroll
-  for (int c = 0; c < NCG; ++c) load_k_frags<D>(CODEC, cptr[c], r, t, a[c], kz[c]);
+  for (int c = 0; c < NCG; ++c) load_k_frags<D, NARROW>(CODEC, cptr[c], r, t, a[c], kz[c]);
   if constexpr (CODEC == ARGUS_INT4_G32) {
     float sg[NCG][D / 32][4];
 #pragma unroll
@@ -363,7 +370,7 @@ __device__ __forceinline__ void group_scores(const uint8_t* const* cptr, const C
 // O^T += V^T . (w P)^T for NCG chunks of one codec; all V fragments and P
 // transposes are formed before the MMAs.  pw[c] = {p0, p1, p2, p3} already
 // multiplied by the chunk's V-scale weight; chunks with skip[c] contribute nothing.
-template <int D, int CODEC, int NCG, bool BF>
+template <int D, int CODEC, int NCG, bool BF, bool NARROW>
 __device__ __forceinline__ void group_pv(const uint8_t* const* cptr, int r, int t, const float (*pw)[4],
                                          const bool* skip, float (&acc)[D / 16][4]) {
   constexpr int MB = D / 16;
@@ -371,7 +378,7 @@ __device__ __forceinline__ void group_pv(const uint8_t* const* cptr, int r, int 
   uint32_t bh[NCG][2], bl[NCG][2];
 #pragma unroll
   for (int c = 0; c < NCG; ++c) {
-    load_v_frags<D>(CODEC, cptr[c], r, t, vf[c]);
+    load_v_frags<D, NARROW>(CODEC, cptr[c], r, t, vf[c]);
     if constexpr (BF) {
       const float* q = pw[c];
       const uint32_t h01 = pack_bf16x2(q[0], q[1]), h23 = pack_bf16x2(q[2], q[3]);
@@ -401,12 +408,13 @@ __device__ __forceinline__ void group_pv(const uint8_t* const* cptr, int r, int 
   }
 }
 
-template <int D, bool QBF16, int FAM>
-__global__ void __launch_bounds__(Warps<D>::kThreads, Layout<D>::kMinBlocks)
+template <int D, bool QBF16, int FAM, bool NARROW>
+__global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>::kMinBlocks)
     decode_kernel(const Params p) {
-  constexpr int kConsumerWarps = Warps<D>::kConsumer;
-  constexpr int kNC = Warps<D>::kNC;
-  using L = Layout<D>;
+  constexpr int kConsumerWarps = Warps<D, NARROW>::kConsumer;
+  constexpr int kNC = Warps<D, NARROW>::kNC;
+  constexpr int kChunksPerStage = Layout<D, NARROW>::kCPS;   // this layout's stage size
+  using L = Layout<D, NARROW>;
   constexpr int KC = D / 16;
   constexpr int MB = D / 16;
   constexpr int DL = D / 8;
@@ -549,6 +557,7 @@ __global__ void __launch_bounds__(Warps<D>::kThreads, Layout<D>::kMinBlocks)
               ok = (FAM == kFamMixed) || (FAM == fam);
             }
             if (ok) ok = slot_id >= 0 && slot_id < p.n_slots[codec];
+            if (NARROW && codec <= ARGUS_BF16) ok = false;   // 16-bit rows do not fit a narrow slot
             if (!ok) {
               if (cip == 0 && p.status) atomicAdd(p.status, 1u);
             } else {
@@ -755,21 +764,21 @@ __global__ void __launch_bounds__(Warps<D>::kThreads, Layout<D>::kMinBlocks)
         if constexpr (kNC == 2) {
           if (ncg == 2) {
             switch (codec) {
-              case ARGUS_FP16: group_scores<D, ARGUS_FP16, 2, false>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-              case ARGUS_BF16: group_scores<D, ARGUS_BF16, 2, true>(cp, dd, r, t, qf, qb, qf8, qgs, 1.f, 1.f, p.scale_log2, sv, c0); break;
-              case ARGUS_FP8_E4M3: group_scores<D, ARGUS_FP8_E4M3, 2, false>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-              case ARGUS_INT8: group_scores<D, ARGUS_INT8, 2, false>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-              default: group_scores<D, ARGUS_INT4_G32, 2, false>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+              case ARGUS_FP16: group_scores<D, ARGUS_FP16, 2, false, NARROW>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+              case ARGUS_BF16: group_scores<D, ARGUS_BF16, 2, true, NARROW>(cp, dd, r, t, qf, qb, qf8, qgs, 1.f, 1.f, p.scale_log2, sv, c0); break;
+              case ARGUS_FP8_E4M3: group_scores<D, ARGUS_FP8_E4M3, 2, false, NARROW>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+              case ARGUS_INT8: group_scores<D, ARGUS_INT8, 2, false, NARROW>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+              default: group_scores<D, ARGUS_INT4_G32, 2, false, NARROW>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
             }
             return;
           }
         }
         switch (codec) {
-          case ARGUS_FP16: group_scores<D, ARGUS_FP16, 1, false>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-          case ARGUS_BF16: group_scores<D, ARGUS_BF16, 1, true>(cp, dd, r, t, qf, qb, qf8, qgs, 1.f, 1.f, p.scale_log2, sv, c0); break;
-          case ARGUS_FP8_E4M3: group_scores<D, ARGUS_FP8_E4M3, 1, false>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-          case ARGUS_INT8: group_scores<D, ARGUS_INT8, 1, false>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-          default: group_scores<D, ARGUS_INT4_G32, 1, false>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+          case ARGUS_FP16: group_scores<D, ARGUS_FP16, 1, false, NARROW>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+          case ARGUS_BF16: group_scores<D, ARGUS_BF16, 1, true, NARROW>(cp, dd, r, t, qf, qb, qf8, qgs, 1.f, 1.f, p.scale_log2, sv, c0); break;
+          case ARGUS_FP8_E4M3: group_scores<D, ARGUS_FP8_E4M3, 1, false, NARROW>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+          case ARGUS_INT8: group_scores<D, ARGUS_INT8, 1, false, NARROW>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+          default: group_scores<D, ARGUS_INT4_G32, 1, false, NARROW>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
         }
       };
       if (same) {
@@ -843,21 +852,21 @@ __global__ void __launch_bounds__(Warps<D>::kThreads, Layout<D>::kMinBlocks)
         if constexpr (kNC == 2) {
           if (ncg == 2) {
             switch (codec) {
-              case ARGUS_FP16: group_pv<D, ARGUS_FP16, 2, false>(cp, r, t, pw + c0, skip + c0, acc); break;
-              case ARGUS_BF16: group_pv<D, ARGUS_BF16, 2, true>(cp, r, t, pw + c0, skip + c0, acc); break;
-              case ARGUS_FP8_E4M3: group_pv<D, ARGUS_FP8_E4M3, 2, false>(cp, r, t, pw + c0, skip + c0, acc); break;
-              case ARGUS_INT8: group_pv<D, ARGUS_INT8, 2, false>(cp, r, t, pw + c0, skip + c0, acc); break;
-              default: group_pv<D, ARGUS_INT4_G32, 2, false>(cp, r, t, pw + c0, skip + c0, acc); break;
+              case ARGUS_FP16: group_pv<D, ARGUS_FP16, 2, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc); break;
+              case ARGUS_BF16: group_pv<D, ARGUS_BF16, 2, true, NARROW>(cp, r, t, pw + c0, skip + c0, acc); break;
+              case ARGUS_FP8_E4M3: group_pv<D, ARGUS_FP8_E4M3, 2, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc); break;
+              case ARGUS_INT8: group_pv<D, ARGUS_INT8, 2, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc); break;
+              default: group_pv<D, ARGUS_INT4_G32, 2, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc); break;
             }
             return;
           }
         }
         switch (codec) {
-          case ARGUS_FP16: group_pv<D, ARGUS_FP16, 1, false>(cp, r, t, pw + c0, skip + c0, acc); break;
-          case ARGUS_BF16: group_pv<D, ARGUS_BF16, 1, true>(cp, r, t, pw + c0, skip + c0, acc); break;
-          case ARGUS_FP8_E4M3: group_pv<D, ARGUS_FP8_E4M3, 1, false>(cp, r, t, pw + c0, skip + c0, acc); break;
-          case ARGUS_INT8: group_pv<D, ARGUS_INT8, 1, false>(cp, r, t, pw + c0, skip + c0, acc); break;
-          default: group_pv<D, ARGUS_INT4_G32, 1, false>(cp, r, t, pw + c0, skip + c0, acc); break;
+          case ARGUS_FP16: group_pv<D, ARGUS_FP16, 1, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc); break;
+          case ARGUS_BF16: group_pv<D, ARGUS_BF16, 1, true, NARROW>(cp, r, t, pw + c0, skip + c0, acc); break;
+          case ARGUS_FP8_E4M3: group_pv<D, ARGUS_FP8_E4M3, 1, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc); break;
+          case ARGUS_INT8: group_pv<D, ARGUS_INT8, 1, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc); break;
+          default: group_pv<D, ARGUS_INT4_G32, 1, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc); break;
         }
       };
       if (same) {
@@ -1060,7 +1069,7 @@ __global__ void __launch_bounds__(kFoldThreads) decode_fold_kernel(const Params 
 // ---------------------------------------------------------------------------
 struct Plan {
   int D, G, cps, num_splits, fam;
-  bool q_bf16;
+  bool q_bf16, narrow;
   size_t part_o_bytes, ws_bytes;
 };
 
@@ -1116,23 +1125,26 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
   pl->fam = (has_bf16 && has_f16) ? kFamMixed : (has_bf16 ? kFamBF16 : kFamF16);
   pl->D = g.head_dim;
   pl->G = G;
+  // narrow ring: every pool holds byte or nibble codes, head_dim 128
+  pl->narrow = g.head_dim == 128 && !has_bf16 && !seen[ARGUS_FP16] && a->n_pools > 0;
+  const long long cps_unit = pl->narrow ? chunks_per_stage<true>() : kChunksPerStage;
   const int cpp = g.page_tokens / kChunk;
   const long long max_chunks = a->sel_pages ? (long long)a->sel_width * cpp : (long long)a->max_pages * cpp;
   long long cps;
   if (a->num_splits > 0) {
     cps = (max_chunks + a->num_splits - 1) / a->num_splits;
   } else {
-    // Dense pages: about eight CTAs per SM, so that rows of unequal length
+    // Dense pages: about ten CTAs per SM, so that rows of unequal length
     // balance.  Selected pages: the list width bounds the work but typically
     // about half of it is used, and each split is a CTA that pays the whole
     // lookup-and-load latency; one CTA per resident slot does best there.
     const long long total = (long long)std::max(a->batch, 1) * g.n_kv_heads * max_chunks;
     const long long slots = (long long)device_sm_count() * (g.head_dim == 64 ? 2 : 1);
-    const long long target = a->sel_pages ? slots : 8LL * device_sm_count();
-    cps = std::max<long long>(kChunksPerStage, (total + target - 1) / target);
+    const long long target = a->sel_pages ? slots : 10LL * device_sm_count();
+    cps = std::max<long long>(cps_unit, (total + target - 1) / target);
   }
   cps = std::max<long long>(cps, (max_chunks + kMaxSplits - 1) / kMaxSplits);
-  cps = std::max<long long>(kChunksPerStage, (cps + kChunksPerStage - 1) / kChunksPerStage * kChunksPerStage);
+  cps = std::max<long long>(cps_unit, (cps + cps_unit - 1) / cps_unit * cps_unit);
   pl->cps = (int)cps;
   pl->num_splits = (int)std::max<long long>(1, (max_chunks + cps - 1) / cps);
   if (pl->num_splits > 65535) return fail(ARGUS_E_UNSUPPORTED, "decode: too many splits");
@@ -1142,21 +1154,21 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
   return ARGUS_OK;
 }
 
-template <int D, bool QBF16, int FAM>
+template <int D, bool QBF16, int FAM, bool NARROW>
 static argus_status launch_t(const Params& p, dim3 grid, cudaStream_t s) {
-  using L = Layout<D>;
+  using L = Layout<D, NARROW>;
   static bool configured[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(ARGUS_E_LAUNCH, "decode: no device");
   if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, QBF16, FAM>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, QBF16, FAM, NARROW>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "decode: smem attribute: %s", cudaGetErrorString(e));
     configured[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(Warps<D>::kThreads);
+  cfg.blockDim = dim3(Warps<D, NARROW>::kThreads);
   cfg.dynamicSmemBytes = L::kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -1164,7 +1176,7 @@ static argus_status launch_t(const Params& p, dim3 grid, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<D, QBF16, FAM>, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<D, QBF16, FAM, NARROW>, p);
   if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "argus_paged_decode_attn: %s", cudaGetErrorString(e));
   if (p.num_splits > 1) {
     cudaLaunchConfig_t fc = cfg;
@@ -1181,10 +1193,16 @@ static argus_status launch_t(const Params& p, dim3 grid, cudaStream_t s) {
 
 template <int D>
 static argus_status launch_d(const Params& p, const Plan& pl, dim3 grid, cudaStream_t s) {
-  if (!pl.q_bf16) return launch_t<D, false, kFamF16>(p, grid, s);
-  if (pl.fam == kFamF16) return launch_t<D, true, kFamF16>(p, grid, s);
-  if (pl.fam == kFamBF16) return launch_t<D, true, kFamBF16>(p, grid, s);
-  return launch_t<D, true, kFamMixed>(p, grid, s);
+  if constexpr (D == 128) {
+    if (pl.narrow) {
+      if (!pl.q_bf16) return launch_t<D, false, kFamF16, true>(p, grid, s);
+      return launch_t<D, true, kFamF16, true>(p, grid, s);
+    }
+  }
+  if (!pl.q_bf16) return launch_t<D, false, kFamF16, false>(p, grid, s);
+  if (pl.fam == kFamF16) return launch_t<D, true, kFamF16, false>(p, grid, s);
+  if (pl.fam == kFamBF16) return launch_t<D, true, kFamBF16, false>(p, grid, s);
+  return launch_t<D, true, kFamMixed, false>(p, grid, s);
 }
 
 }  // namespace decode
