@@ -12,14 +12,16 @@
 //   the lower page index; the newest page is always added; ascending order.
 //
 // GB300 design: two launches.  (1) score: the slab is the dominant HBM stream
-// (D bf16 per page and head); CTAs tile (batch row, page range), lanes read 16
-// bytes of a compressed key each and reduce within the head's lanes; the
-// G-query sum is formed once per CTA in shared memory; each lane keeps eight
-// rows' loads in flight; scores are stored as order-preserving uint32 keys.
+// (D bf16 per page and head); one wave of CTAs tiles (batch row, page range),
+// lanes read 16 bytes of a compressed key each, eight rows' loads in flight,
+// and fold eight rows' partial dot products across the head's lanes in one
+// transposed reduction; the G-query sum is formed once per CTA and kept in
+// registers; scores are stored as order-preserving uint32 keys.
 // (2) top-k: one CTA per (batch row, KV head) stages the row's keys in shared
-// memory, finds the k-th largest key bit by bit with block-wide counts (one
-// barrier per bit), then compacts the chosen pages in ascending order with
-// block-wide prefix sums.
+// memory and registers; each warp narrows its keys to those at or above its
+// own k-th largest, the k-th largest of the survivors is the row's threshold
+// (both searches two bits per round by warp reductions), then the chosen
+// pages are compacted in ascending order with block-wide prefix sums.
 #include <algorithm>
 
 #include "common.cuh"
@@ -89,6 +91,16 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(int Hkv, int G, in
   const int n_rows = (p_end - p0) * Hkv;
   // rows of this CTA are contiguous in the slab: (p0 * Hkv + row) * D
   const uint16_t* base = ckeys + (((size_t)b * max_pages + p0) * Hkv) * D + 8 * li;
+  // when Hkv divides the rows per pass, a lane's rows all belong to one KV
+  // head: its 8 q-sum values stay in registers
+  const bool fixed_h = (RPP % Hkv) == 0;
+  float qv[8];
+  {
+    const int h0 = (warp * RPW + sub) % Hkv;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) qv[e] = qsum[h0 * D + 8 * li + e];
+  }
+  static_assert(kRowBatch == 8, "the transposed reduction below folds 8 rows");
   for (int r0 = warp * RPW + sub; r0 - sub < n_rows; r0 += kRowBatch * RPP) {
     uint4 x[kRowBatch];
 #pragma unroll
@@ -97,25 +109,64 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(int Hkv, int G, in
       if (row < n_rows) x[j] = __ldcs(reinterpret_cast<const uint4*>(base + (size_t)row * D));
       else x[j] = make_uint4(0u, 0u, 0u, 0u);
     }
+    float sv[kRowBatch];
 #pragma unroll
     for (int j = 0; j < kRowBatch; ++j) {
       const int row = r0 + j * RPP;
-      if (row - sub >= n_rows) break;       // warp-uniform: no row of this warp is left
-      const int h = row % Hkv;
-      const float* qs = qsum + (row < n_rows ? h : 0) * D + 8 * li;
+      float qe[8];
+      if (fixed_h) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) qe[e] = qv[e];
+      } else {
+        const float* qs = qsum + (row % Hkv) * D + 8 * li;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) qe[e] = qs[e];
+      }
       const uint32_t w[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
-      float s = 0.f;
+      float acc = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float k = __uint_as_float(((w[e / 2] >> (16 * (e & 1))) & 0xFFFFu) << 16);
-        s = fmaf(k, qs[e], s);
+        acc = fmaf(k, qe[e], acc);
       }
+      sv[j] = acc;
+    }
+    // transposed reduction over the row's LPH lanes: each step halves the
+    // values a lane holds (8 -> 4 -> 2 -> 1), then plain sums finish
+    float v4[4], v2[2], v1;
+    {
+      constexpr int o = LPH / 2;
+      const bool up = (li & o) != 0;
 #pragma unroll
-      for (int o = 1; o < LPH; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (row < n_rows && li == 0) {
-        const int p = p0 + row / Hkv;
-        keys[((size_t)b * Hkv + h) * max_pages + p] = order_key(s);
+      for (int v = 0; v < 4; ++v) {
+        const float mine = up ? sv[v + 4] : sv[v], other = up ? sv[v] : sv[v + 4];
+        v4[v] = mine + __shfl_xor_sync(0xffffffffu, other, o);
       }
+    }
+    {
+      constexpr int o = LPH / 4;
+      const bool up = (li & o) != 0;
+#pragma unroll
+      for (int v = 0; v < 2; ++v) {
+        const float mine = up ? v4[v + 2] : v4[v], other = up ? v4[v] : v4[v + 2];
+        v2[v] = mine + __shfl_xor_sync(0xffffffffu, other, o);
+      }
+    }
+    {
+      constexpr int o = LPH / 8;
+      const bool up = (li & o) != 0;
+      const float mine = up ? v2[1] : v2[0], other = up ? v2[0] : v2[1];
+      v1 = mine + __shfl_xor_sync(0xffffffffu, other, o);
+    }
+#pragma unroll
+    for (int o = LPH / 16; o >= 1; o >>= 1) v1 += __shfl_xor_sync(0xffffffffu, v1, o);
+    // this lane now holds the sum of row j, the bits of j chosen by the steps above
+    const int j = ((li & (LPH / 2)) ? 4 : 0) + ((li & (LPH / 4)) ? 2 : 0) + ((li & (LPH / 8)) ? 1 : 0);
+    const int row = r0 + j * RPP;
+    // (with LPH = 16, lanes li and li ^ 1 hold the same row: the even one writes)
+    if ((LPH == 8 || (li & 1) == 0) && row < n_rows) {
+      const int p = p0 + row / Hkv;
+      keys[((size_t)b * Hkv + row % Hkv) * max_pages + p] = order_key(v1);
     }
   }
 }
@@ -155,7 +206,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pag
                                                             uint32_t* drops, int stage) {
   extern __shared__ uint32_t skeys[];
   __shared__ int sh_scan[32];
-  __shared__ uint32_t sh_cnt[4][32];
+  __shared__ uint2 sh_cnt2[2][32];
+  __shared__ int sh_wc[32];
+  __shared__ uint32_t sh_thr[2];
+  __shared__ uint32_t sh_cand[kKeysPerThread * kTopkThreads];   // survivors of the per-warp search
   const int h = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5;
@@ -225,27 +279,113 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pag
       }
       return __reduce_add_sync(0xffffffffu, c);
     };
-    // block total: each warp posts its count, then every warp sums the posts
-    // (one per lane) -- one barrier per round, buffers alternate
-    auto block_total = [&](uint32_t c, int buf) -> uint32_t {
-      if (lane == 0) sh_cnt[buf][warp] = c;
+    // block totals of two packed words: each warp posts its pair, then every
+    // warp sums the posts (one per lane) -- one barrier per round, the two
+    // buffers alternate
+    auto block_total2 = [&](uint32_t c0, uint32_t c1, int buf) -> uint2 {
+      if (lane == 0) sh_cnt2[buf][warp] = make_uint2(c0, c1);
       __syncthreads();
-      const uint32_t x = lane < (nthr >> 5) ? sh_cnt[buf][lane] : 0u;
-      return __reduce_add_sync(0xffffffffu, x);
+      const uint2 x = lane < (nthr >> 5) ? sh_cnt2[buf][lane] : make_uint2(0u, 0u);
+      return make_uint2(__reduce_add_sync(0xffffffffu, x.x), __reduce_add_sync(0xffffffffu, x.y));
     };
-    // two bits per round: candidates T|01, T|10, T|11 in bits (b+1, b)
-    for (int b = 30, round = 0; b >= 0; b -= 2, ++round) {
-      const uint32_t c1 = T | (1u << b), c2 = T | (2u << b), c3 = T | (3u << b);
-      const uint32_t n12 = block_total(count2(c1, c2, false), round & 1);
-      const uint32_t n3 = block_total(count2(c3, 0xFFFFFFFFu, false), 2 + (round & 1)) & 0xFFFFu;
-      const uint32_t n1 = n12 & 0xFFFFu, n2 = n12 >> 16;
-      if (n3 >= (uint32_t)k) T = c3;
-      else if (n2 >= (uint32_t)k) T = c2;
-      else if (n1 >= (uint32_t)k) T = c1;
+    // Warp-level search for the kk-th largest of the values a warp holds
+    // (nv per lane in registers, valid flags vf): two bits per round, the
+    // three candidate counts in two warp reductions.  No barrier.
+    // Empty slots hold 0, which no candidate (always >= 1) counts.  (A key of 0
+    // is the order key of a negative NaN score: NaN scores are unordered.)
+    auto warp_kth = [&](const uint32_t* vals, int nv, int kk) -> uint32_t {
+      uint32_t t = 0u;
+      for (int bb = 30; bb >= 0; bb -= 2) {
+        const uint32_t c1 = t | (1u << bb), c2 = t | (2u << bb), c3 = t | (3u << bb);
+        uint32_t a = 0u, c = 0u;
+        for (int j = 0; j < nv; ++j) {
+          a += (vals[j] >= c1 ? 1u : 0u) + (vals[j] >= c2 ? 0x10000u : 0u);
+          c += vals[j] >= c3 ? 1u : 0u;
+        }
+        a = __reduce_add_sync(0xffffffffu, a);
+        c = __reduce_add_sync(0xffffffffu, c);
+        if (c >= (uint32_t)kk) t = c3;
+        else if ((a >> 16) >= (uint32_t)kk) t = c2;
+        else if ((a & 0xFFFFu) >= (uint32_t)kk) t = c1;
+      }
+      return t;
+    };
+    if (in_regs) {
+      // (1) each warp keeps its keys >= its own min(k, n_w)-th largest: every
+      // key >= the row's k-th largest survives, so (2) the row's threshold is
+      // the k-th largest of the survivors, found by every warp alike
+      int nw_valid = 0;
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) nw_valid += kv[j] ? 1 : 0;
+      nw_valid = (int)__reduce_add_sync(0xffffffffu, (uint32_t)nw_valid);
+      const int kw = min(k, nw_valid);
+      const uint32_t Tw = kw > 0 ? warp_kth(kr, KPT, kw) : 0xFFFFFFFFu;
+      int my = 0;
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) my += (kv[j] && kw > 0 && kr[j] >= Tw) ? 1 : 0;
+      int incl = my;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) sh_wc[warp] = incl;
+      __syncthreads();
+      const int nwarps = nthr >> 5;
+      const int wcl = lane < nwarps ? sh_wc[lane] : 0;
+      const int M = (int)__reduce_add_sync(0xffffffffu, (uint32_t)wcl);
+      const int wbase = (int)__reduce_add_sync(0xffffffffu, (uint32_t)(lane < warp ? wcl : 0));
+      int pos = wbase + incl - my;
+#pragma unroll
+      for (int j = 0; j < KPT; ++j)
+        if (kv[j] && kw > 0 && kr[j] >= Tw) sh_cand[pos++] = kr[j];
+      __syncthreads();
+      constexpr int CPL = 16;   // survivors per lane held in registers
+      if (M <= 32 * CPL) {
+        // one warp searches the survivors; the others wait for its answer
+        if (warp == 0) {
+          uint32_t cv[CPL];
+#pragma unroll
+          for (int m = 0; m < CPL; ++m) {
+            const int i = lane + 32 * m;
+            cv[m] = i < M ? sh_cand[i] : 0u;
+          }
+          const uint32_t t = warp_kth(cv, CPL, k);
+          uint32_t gt = 0u;
+#pragma unroll
+          for (int m = 0; m < CPL; ++m) gt += cv[m] > t ? 1u : 0u;
+          gt = __reduce_add_sync(0xffffffffu, gt);
+          if (lane == 0) {
+            sh_thr[0] = t;
+            sh_thr[1] = (uint32_t)(k - (int)gt);
+          }
+        }
+        __syncthreads();
+        T = sh_thr[0];
+        k_rem = (int)sh_thr[1];
+      } else {
+        // many survivors (ties): block-wide search over every key
+        for (int b = 30, round = 0; b >= 0; b -= 2, ++round) {
+          const uint32_t c1 = T | (1u << b), c2 = T | (2u << b), c3 = T | (3u << b);
+          const uint2 n = block_total2(count2(c1, c2, false), count2(c3, 0xFFFFFFFFu, false), round & 1);
+          if ((n.y & 0xFFFFu) >= (uint32_t)k) T = c3;
+          else if ((n.x >> 16) >= (uint32_t)k) T = c2;
+          else if ((n.x & 0xFFFFu) >= (uint32_t)k) T = c1;
+        }
+        k_rem = k - (int)(block_total2(count2(T, 0xFFFFFFFFu, true), 0u, 0).x & 0xFFFFu);
+      }
+    } else {
+      // rows longer than the registers hold: block-wide search, two bits per round
+      for (int b = 30, round = 0; b >= 0; b -= 2, ++round) {
+        const uint32_t c1 = T | (1u << b), c2 = T | (2u << b), c3 = T | (3u << b);
+        const uint2 n = block_total2(count2(c1, c2, false), count2(c3, 0xFFFFFFFFu, false), round & 1);
+        if ((n.y & 0xFFFFu) >= (uint32_t)k) T = c3;
+        else if ((n.x >> 16) >= (uint32_t)k) T = c2;
+        else if ((n.x & 0xFFFFu) >= (uint32_t)k) T = c1;
+      }
+      // the last round (15) used buffer 1, so 0 is free
+      k_rem = k - (int)(block_total2(count2(T, 0xFFFFFFFFu, true), 0u, 0).x & 0xFFFFu);
     }
-    // rounds used buffers (0, 2) and (1, 3) alternately; the last round (15)
-    // used 1 and 3, so 0 is free
-    k_rem = k - (int)(block_total(count2(T, 0xFFFFFFFFu, true), 0) & 0xFFFFu);
   }
   const bool take_all = (k >= n_cand);
   // per thread: a contiguous range of pages so that scans keep page order
