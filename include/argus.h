@@ -112,7 +112,8 @@ typedef struct {
  *                keys, summed in fp32 and rounded to bf16 ([PR499] "Why this
  *                works": the indexer scores a compressed slab)
  * Slots outside their pools are skipped on the device (counted in *status if
- * status != NULL, device uint32).
+ * status != NULL, device uint32).  Source values must be finite: codes for
+ * units holding inf or NaN are unspecified.
  * ------------------------------------------------------------------------- */
 argus_status argus_quantize_pages(const argus_geom* g, int32_t src_dtype,
                                   const void* src_codes, int64_t n_src_slots,

@@ -53,6 +53,14 @@ __device__ __forceinline__ void unpack8(const uint4& x, float (&f)[8]) {
   }
 }
 
+// |x| maxima and minima on the packed 16-bit sources: non-negative fp16 and
+// bf16 values order like their bit patterns, so a packed unsigned max / min of
+// the sign-cleared halves finds the largest / smallest magnitude exactly.
+template <bool SBF16>
+__device__ __forceinline__ float mag_to_float(uint32_t bits16) {
+  return SBF16 ? __uint_as_float(bits16 << 16) : __half2float(__ushort_as_half((unsigned short)bits16));
+}
+
 __device__ __forceinline__ float fp16_sat(float x) {
   return __half2float(__float2half_rn(fminf(fmaxf(x, -65504.f), 65504.f)));
 }
@@ -153,13 +161,16 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
       // (low mantissa bits - midpoint + 8, unsigned) and of |y|
       float y[8];
       uint32_t dmin = 0xFFFFFFFFu;
-      float amin = INFINITY;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         y[e] = f[e] * rscale;
         dmin = min(dmin, (__float_as_uint(y[e]) & 0xFFFFFu) - 0x80000u + 8u);
-        amin = fminf(amin, fabsf(y[e]));
       }
+      // the smallest |y| is the product of the smallest |x| (the product is
+      // monotone in |x|), found on the packed source
+      const uint32_t mn2 = __vminu2(__vminu2(raw.x & 0x7FFF7FFFu, raw.y & 0x7FFF7FFFu),
+                                    __vminu2(raw.z & 0x7FFF7FFFu, raw.w & 0x7FFF7FFFu));
+      const float amin = mag_to_float<SBF16>(min(mn2 & 0xFFFFu, mn2 >> 16)) * rscale;
       if (dmin <= 16u || amin < 0.0157f) {   // near a midpoint, or e4m3 subnormal range
         F8 x;
 #pragma unroll
@@ -571,17 +582,17 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_small_kernel(const QPara
       else dcodes = p.dst_codes + cu.dst * (size_t)P * D;
       float scale = 0.f;
       if (CODEC == ARGUS_FP8_E4M3 || CODEC == ARGUS_INT8) {
-        float amax = 0.f;
+        uint32_t mx2 = 0u;   // per 16-bit half: the largest sign-cleared code
 #pragma unroll
         for (int k = 0; k < kRegVecs; ++k) {
           const int v = lane + 32 * k;
           if (v < nvalid_vec) {
-            float f[8];
-            unpack8<SBF16>(cur[k], f);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+            const uint4 x = cur[k];
+            mx2 = __vmaxu2(mx2, __vmaxu2(__vmaxu2(x.x & 0x7FFF7FFFu, x.y & 0x7FFF7FFFu),
+                                         __vmaxu2(x.z & 0x7FFF7FFFu, x.w & 0x7FFF7FFFu)));
           }
         }
+        float amax = mag_to_float<SBF16>(max(mx2 & 0xFFFFu, mx2 >> 16));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         scale = amax > 0.f ? amax / (CODEC == ARGUS_FP8_E4M3 ? 448.f : 127.f) : 0.f;

@@ -226,3 +226,18 @@ def test_scale_rows_loaded_by_the_producer(codec, Hkv, D):
     c = build_case(2 * Hkv, Hkv, D, P, [100, 128], pc, W.FP16, seed=400 + Hkv + codec, outliers=True)
     out, out32, lse, _ = run_decode(c, num_splits=2)
     _check(c, out, out32, lse)
+
+
+@pytest.mark.parametrize("q_dtype", [W.FP16, W.BF16])
+def test_narrow_ring_with_mixed_byte_and_nibble_codecs(q_dtype):
+    """head_dim 128 with FP8, INT8 and INT4 pools only runs the narrow ring
+    (16 chunks per stage, two per warp); chunks of different codecs share a
+    warp and a stage."""
+    Hq, Hkv, D, P = 16, 2, 128, 16
+    rng = np.random.default_rng(77)
+    pc = rng.choice([W.FP8_E4M3, W.INT8, W.INT4_G32], size=(3, 40))
+    c = build_case(Hq, Hkv, D, P, [640, 333, 17], pc, q_dtype, seed=501, outliers=True)
+    for splits in (0, 1, 3):
+        out, out32, lse, _ = run_decode(c, out_dtype=torch.float16 if q_dtype == W.FP16 else torch.bfloat16,
+                                        num_splits=splits)
+        _check(c, out, out32, lse)
