@@ -215,6 +215,25 @@ def ClockSampler(dev_index):
 
 # ---------------------------------------------------------------- workload
 
+def max_over_ranks(value, world, dev):
+    """The largest of every rank's value (the slowest replica sets the time),
+    followed by a barrier; the value itself when there is one rank."""
+    if world <= 1:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.barrier()
+    return float(t.item())
+
+
+def aggregate_us_per_token_layer(ms_step, world):
+    """Whole-job rate for N independent replicas: every rank decodes one token
+    through all layers per step, so the job finishes world * LAYERS
+    token-layers per (max-over-ranks) step."""
+    return ms_step * 1000.0 / (LAYERS * max(1, world))
+
+
 def build_mixed_tier(dev):
     """Device pools for all 24 layers (one pool per codec, 4 slots per layer),
     per-layer block tables and queries.  Setup only: quantisation by the
@@ -305,12 +324,7 @@ def run_gpu(args, rank, world):
     t_wall = time.perf_counter() - t_wall0
     clocks = sampler.stop()
     torch.cuda.synchronize()
-    ms_step = sum(times) / len(times)
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
-        torch.distributed.barrier()
+    ms_step = max_over_ranks(sum(times) / len(times), world, dev)
 
     # ---- end to end through the public API with host buffers
     q_host = torch.empty((LAYERS, 1, HQ, D), dtype=torch.float16).pin_memory()
@@ -330,11 +344,7 @@ def run_gpu(args, rank, world):
 
     timed(args.warmup, e2e_step)
     e2e_times = timed(args.steps, e2e_step)
-    ms_e2e = sum(e2e_times) / len(e2e_times)
-    if world > 1:
-        t = torch.tensor([ms_e2e], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(sum(e2e_times) / len(e2e_times), world, dev)
     return ms_step, ms_e2e, clocks, t_wall, q_host.numel() * 2, out_host.numel() * 2
 
 
@@ -678,7 +688,7 @@ def main():
     bytes_layer = kv_bytes_per_layer()
     launch_ms = ms_step / LAYERS
     achieved = bytes_layer / (launch_ms * 1e-3) / 1e9
-    us_tl = ms_step * 1000.0 / (LAYERS * world)
+    us_tl = aggregate_us_per_token_layer(ms_step, world)
     traffic = profiled_traffic("decode_mixed_tier", ["decode.cu", "common.cuh"])
     line = {
         "metric": METRIC, "value": us_tl, "unit": "us/token/layer", "n_gpus": n_gpus, "steps": args.steps,
