@@ -56,6 +56,27 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(int Hkv, int G, in
   int n = n_pages[b];
   n = max(0, min(n, max_pages));
   if (p0 >= n) return;
+  constexpr int LPH = D / 8;               // lanes per (page, head) row, 16 bytes each
+  constexpr int RPW = 32 / LPH;            // rows per warp and pass
+  constexpr int RPP = (kScoreThreads / 32) * RPW;  // rows per CTA and pass
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane / LPH, li = lane % LPH;
+  const int p_end = min(n, p0 + ppc);
+  const int n_rows = (p_end - p0) * Hkv;
+  // rows of this CTA are contiguous in the slab: (p0 * Hkv + row) * D
+  const uint16_t* base = ckeys + (((size_t)b * max_pages + p0) * Hkv) * D + 8 * li;
+  // the first batch of rows does not depend on the q sums: its loads go out
+  // before them, so the two latencies overlap
+  uint4 x[kRowBatch];
+  auto load_batch = [&](int r0) {
+#pragma unroll
+    for (int j = 0; j < kRowBatch; ++j) {
+      const int row = r0 + j * RPP;
+      if (row < n_rows) x[j] = __ldcs(reinterpret_cast<const uint4*>(base + (size_t)row * D));
+      else x[j] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  load_batch(warp * RPW + sub);
   const uint16_t* qb = static_cast<const uint16_t*>(q) + (size_t)b * Hq * D;
   // G-query sums: a thread per (KV head, 8 dims); the rows' 16-byte loads are
   // issued together, eight at a time
@@ -82,15 +103,6 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(int Hkv, int G, in
     for (int e = 0; e < 8; ++e) qsum[h * D + 8 * c + e] = acc[e];
   }
   __syncthreads();
-  constexpr int LPH = D / 8;               // lanes per (page, head) row, 16 bytes each
-  constexpr int RPW = 32 / LPH;            // rows per warp and pass
-  constexpr int RPP = (kScoreThreads / 32) * RPW;  // rows per CTA and pass
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int sub = lane / LPH, li = lane % LPH;
-  const int p_end = min(n, p0 + ppc);
-  const int n_rows = (p_end - p0) * Hkv;
-  // rows of this CTA are contiguous in the slab: (p0 * Hkv + row) * D
-  const uint16_t* base = ckeys + (((size_t)b * max_pages + p0) * Hkv) * D + 8 * li;
   // when Hkv divides the rows per pass, a lane's rows all belong to one KV
   // head: its 8 q-sum values stay in registers
   const bool fixed_h = (RPP % Hkv) == 0;
@@ -102,13 +114,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(int Hkv, int G, in
   }
   static_assert(kRowBatch == 8, "the transposed reduction below folds 8 rows");
   for (int r0 = warp * RPW + sub; r0 - sub < n_rows; r0 += kRowBatch * RPP) {
-    uint4 x[kRowBatch];
-#pragma unroll
-    for (int j = 0; j < kRowBatch; ++j) {
-      const int row = r0 + j * RPP;
-      if (row < n_rows) x[j] = __ldcs(reinterpret_cast<const uint4*>(base + (size_t)row * D));
-      else x[j] = make_uint4(0u, 0u, 0u, 0u);
-    }
+    if (r0 != warp * RPW + sub) load_batch(r0);   // the first batch is already loaded
     float sv[kRowBatch];
 #pragma unroll
     for (int j = 0; j < kRowBatch; ++j) {
