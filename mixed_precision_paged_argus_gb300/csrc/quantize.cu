@@ -98,11 +98,9 @@ __device__ __forceinline__ float group_reduce(float v, float* sh) {
 // path never evaluates a division.  The codes are therefore identical to
 // dividing every element.
 //  e4m3 (normal range): boundaries are the midpoints between neighbouring
-//  codes, i.e. fp32 mantissas whose 20 bits below the 3 kept bits equal 0x80000.
-__device__ __forceinline__ bool e4m3_unsure(float y) {
-  const uint32_t low = __float_as_uint(y) & 0xFFFFFu;
-  return ((low - 0x80000u + 8u) <= 16u) || (fabsf(y) < 0.0157f);  // e4m3 subnormals start below 2^-6
-}
+//  codes, i.e. fp32 mantissas whose 20 bits below the 3 kept bits equal
+//  0x80000; a product within 8 of them in those bits, or below 0.0157 in
+//  magnitude (e4m3 subnormals start below 2^-6), takes the division.
 
 //  integer codes: boundaries are the half-integers.  For |y| <= 128 the
 //  product differs from x / s by at most 128 * 2^-23 = 2^-16 and RN(x / s)
@@ -157,7 +155,7 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
   } else if (CODEC == ARGUS_FP8_E4M3) {
     uint32_t w[2] = {0u, 0u};
     if (valid && scale > 0.f) {
-      // the boundary test of e4m3_unsure as running minima: of the distance
+      // the e4m3 boundary test as running minima: of the distance
       // (low mantissa bits - midpoint + 8, unsigned) and of |y|
       float y[8];
       uint32_t dmin = 0xFFFFFFFFu;
