@@ -191,17 +191,20 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
       // |x * RN(1/s)| <= 127 (1 + 2^-22) while s is a normal number, so the
       // clamp is needed only for the tiny scales of subnormal units; clamping
       // before rounding equals clamping the rounded value (integer bounds)
-      const bool clamp = scale < 0x1p-100f;
       uint32_t t[8];
       float dev = 0.f;   // largest distance of a product from its rounded value
+      auto round8 = [&](auto clamp_tag) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        float y = f[e] * rscale;
-        if (clamp) y = fminf(fmaxf(y, -127.f), 127.f);
-        const float tf = y + kRoundMagic;
-        dev = fmaxf(dev, fabsf(y - (tf - kRoundMagic)));
-        t[e] = __float_as_uint(tf);
-      }
+        for (int e = 0; e < 8; ++e) {
+          float y = f[e] * rscale;
+          if (decltype(clamp_tag)::value) y = fminf(fmaxf(y, -127.f), 127.f);
+          const float tf = y + kRoundMagic;
+          dev = fmaxf(dev, fabsf(y - (tf - kRoundMagic)));
+          t[e] = __float_as_uint(tf);
+        }
+      };
+      if (scale < 0x1p-100f) round8(std::true_type{});   // the branch stays outside the loop
+      else round8(std::false_type{});
       if (dev > 0.5f - kIntGuard) {
         F8 x;
 #pragma unroll
@@ -463,15 +466,19 @@ __device__ __forceinline__ void encode_int4_group(const uint4 (&x)[4], bool vali
       uint32_t t[8];
       unpack8<SBF16>(x[m], f);
       float dev = 0.f;  // largest distance of a product from its rounded value
+      auto round8 = [&](auto clamp_tag) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        d[e] = f[e] - z;
-        float y = d[e] * r;
-        if (clamp) y = fminf(fmaxf(y, 0.f), 15.f);
-        const float tf = y + kRoundMagic;
-        dev = fmaxf(dev, fabsf(y - (tf - kRoundMagic)));
-        t[e] = __float_as_uint(tf);
-      }
+        for (int e = 0; e < 8; ++e) {
+          d[e] = f[e] - z;
+          float y = d[e] * r;
+          if (decltype(clamp_tag)::value) y = fminf(fmaxf(y, 0.f), 15.f);
+          const float tf = y + kRoundMagic;
+          dev = fmaxf(dev, fabsf(y - (tf - kRoundMagic)));
+          t[e] = __float_as_uint(tf);
+        }
+      };
+      if (clamp) round8(std::true_type{});
+      else round8(std::false_type{});
       if (dev > 0.5f - kIntGuard) {
         F8 x;
 #pragma unroll
