@@ -241,3 +241,18 @@ def test_narrow_ring_with_mixed_byte_and_nibble_codecs(q_dtype):
         out, out32, lse, _ = run_decode(c, out_dtype=torch.float16 if q_dtype == W.FP16 else torch.bfloat16,
                                         num_splits=splits)
         _check(c, out, out32, lse)
+
+
+def test_split_count_is_capped_and_many_splits_fold():
+    """An explicit split count above the cap is clamped (at most 512 splits per
+    row); with hundreds of splits the combine folds several batches per thread."""
+    Hq, Hkv, D, P = 8, 1, 64, 16
+    n = 2000
+    pc = np.full((1, n), W.FP16)
+    c = build_case(Hq, Hkv, D, P, [n * P - 3], pc, W.FP16, seed=601, permute=False)
+    out, out32, lse, ws = run_decode(c, num_splits=100000)
+    _check(c, out, out32, lse)
+    args = argus.decode_args(c.g, c.B, c.q, c.pools, c.d_codec, c.d_table, c.d_lens, c.max_pages, c.scale,
+                             out_f32=torch.empty_like(out32), num_splits=100000)
+    # workspace = splits * G * (D + 1) floats per row: at most 512 splits
+    assert argus.decode_workspace_bytes(args) <= 512 * Hq * (D + 1) * 4

@@ -141,3 +141,21 @@ def test_select_width_overflow_drops():
     osel, ocnt, odrops = oracle.select_pages(q64, ck, [100], Hkv, 20, True, 10)
     assert drops == odrops == 2 * 11
     assert np.array_equal(cnt, ocnt)
+
+
+@pytest.mark.parametrize("max_pages,n_pages", [(4000, [4000, 3999]), (50000, [50000, 777])])
+def test_select_many_ties_and_long_rows(max_pages, n_pages):
+    """Scores drawn from 7 values: most pages tie, so each warp keeps far more
+    than k survivors (the block-wide search takes over); rows longer than the
+    shared-memory stage read their keys from memory."""
+    B, Hq, Hkv, D = 2, 4, 1, 64
+    q, q64, ck = _select_case(B, Hq, Hkv, D, max_pages, n_pages, 31, ties=True)
+    qn = np.zeros((B, Hq, D), np.float32)
+    qn[:, :, 0] = 0.25
+    q = torch.from_numpy(qn).to(torch.bfloat16)
+    q64 = C.bf16_bits_to_f64(W.to_bits(q))
+    for top_k in (32, 200):
+        sel, cnt, drops = _run_select(q, ck, n_pages, Hq, Hkv, D, max_pages, top_k, 2 * top_k + 8)
+        osel, ocnt, odrops = oracle.select_pages(q64, ck, n_pages, Hkv, top_k, True, 2 * top_k + 8)
+        assert np.array_equal(cnt, ocnt) and drops == odrops
+        assert np.array_equal(sel[:, :, :cnt.max()], osel[:, :, :cnt.max()])
