@@ -57,3 +57,16 @@ def quantize_bytes(dst_codec, src_elem_bytes, units, page_tokens, head_dim):
 def prefill_flops(q_heads, head_dim, n_q, visible_pairs):
     """4 * D * Hq * (number of visible (query, key) pairs): QK^T and PV."""
     return 4 * head_dim * q_heads * visible_pairs
+
+
+def window_visible(seq_len, page_tokens, window, sinks):
+    """(tokens, pages) a decode query reads under a sliding window of `window`
+    newest tokens plus `sinks` leading ones (window <= 0: every token); pages
+    counts the logical pages holding at least one visible token."""
+    L, P = int(seq_len), int(page_tokens)
+    if window <= 0:
+        return L, (L + P - 1) // P
+    lo = max(0, L - window)
+    s = min(sinks, lo)                       # sinks that lie before the window
+    pages = set(range((lo // P), (L + P - 1) // P)) | set(range((s + P - 1) // P))
+    return (L - lo) + s, len(pages)

@@ -67,8 +67,25 @@ def _visible_pages(b, h, seq_len, P, max_pages, sel_pages, sel_count, sel_width)
     return pages, bad
 
 
+def visible_positions(L, window=0, sinks=0):
+    """Positions 0..L-1 that the newest query of a sequence of L tokens sees.
+
+    "ARGUS: Heterogeneous KV-cache memory management", section "v0.5:
+    model-independent KV placement", lists sliding-window masks among what
+    direct attention supports, and its "HuggingFace example" passes
+    sink_tokens=4; neither spells the mask out.  Read plainly: a window of W
+    keeps the newest W positions (L-W .. L-1) and the first `sinks` positions
+    stay visible as well.  window <= 0 means no window (every position).
+    Returns a boolean array of length L.
+    """
+    pos = np.arange(L)
+    if window <= 0:
+        return np.ones(L, dtype=bool)
+    return (pos >= L - window) | (pos < sinks)
+
+
 def paged_decode(q_f64, Hkv, P, pools, page_codec, block_table, seq_lens, scale,
-                 sel_pages=None, sel_count=None, sel_width=0):
+                 sel_pages=None, sel_count=None, sel_width=0, window=0, sinks=0):
     """Single-token decode attention over a paged mixed-codec KV cache.
 
     q_f64       float64 [B][Hq][D] (the query values)
@@ -81,6 +98,9 @@ def paged_decode(q_f64, Hkv, P, pools, page_codec, block_table, seq_lens, scale,
                 position p*P + t, visible iff < seq_len
     sel_pages / sel_count / sel_width: optional selected-page lists
                 [B][Hkv][width] (sparse decode over the indexer's selection)
+    window / sinks: sliding window of the newest `window` positions plus the
+                first `sinks` (see visible_positions); a page without a
+                visible position is neither read nor checked
 
     Returns (o [B][Hq][D], lse2 [B][Hq], bad) where bad counts pages skipped
     because their slot is out of range plus rejected selection entries.
@@ -93,21 +113,25 @@ def paged_decode(q_f64, Hkv, P, pools, page_codec, block_table, seq_lens, scale,
     bad = 0
     for b in range(B):
         L = int(seq_lens[b])
+        vis = visible_positions(L, window, sinks)
         for h in range(Hkv):
             pages, nbad = _visible_pages(b, h, L, P, max_pages, sel_pages,
                                          sel_count, sel_width)
             bad += nbad
             Ks, Vs = [], []
             for p in pages:
+                n_tok = min(P, L - p * P)
+                keep = vis[p * P:p * P + n_tok]
+                if not keep.any():
+                    continue
                 codec = int(page_codec[b, p])
                 slot = int(block_table[b, p])
                 codes, meta = pools[codec]
                 if slot < 0 or slot >= codes.shape[0]:
                     bad += 1
                     continue
-                n_tok = min(P, L - p * P)
-                Ks.append(dequant_page(codec, codes, meta, slot, 0, h)[:n_tok])
-                Vs.append(dequant_page(codec, codes, meta, slot, 1, h)[:n_tok])
+                Ks.append(dequant_page(codec, codes, meta, slot, 0, h)[:n_tok][keep])
+                Vs.append(dequant_page(codec, codes, meta, slot, 1, h)[:n_tok][keep])
             K = np.concatenate(Ks) if Ks else np.zeros((0, D))
             V = np.concatenate(Vs) if Vs else np.zeros((0, D))
             for g in range(G):

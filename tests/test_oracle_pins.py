@@ -358,6 +358,77 @@ def test_bad_slot_is_skipped_and_counted():
     assert np.allclose(o, o2, atol=1e-13)
 
 
+# ---------------------------------------------------------------- sliding window + sinks
+
+def _window_set(L, W, S):
+    """Visible positions built from plain ranges (independent of the oracle)."""
+    if W <= 0:
+        return set(range(L))
+    return set(range(max(0, L - W), L)) | set(range(min(S, L)))
+
+
+@pytest.mark.parametrize("L,W,S", [(0, 5, 2), (1, 1, 0), (37, 5, 0), (37, 5, 4), (37, 40, 4), (37, 33, 4),
+                                   (37, 34, 4), (37, 1, 36), (37, 1, 37), (64, 16, 16), (64, 17, 15), (20, 3, 100)])
+def test_window_positions_brute_force_and_count(L, W, S):
+    vis = A.visible_positions(L, W, S)
+    assert set(np.nonzero(vis)[0].tolist()) == _window_set(L, W, S)
+    # closed form: the window, plus the sinks that lie before it
+    assert int(vis.sum()) == min(L, W) + min(S, max(0, L - W))
+
+
+def test_window_decode_equals_torch_on_gathered_positions():
+    lens = (37, 64, 129)
+    q, pool, table, codecs, lens, Hkv, P = _fp16_paged_case(B=3, lens=lens, seed=31)
+    B, Hq, D = q.shape
+    G = Hq // Hkv
+    for W_, S_ in [(5, 0), (5, 4), (20, 3), (16, 16), (1, 33), (200, 4)]:
+        o, lse2, bad = A.paged_decode(q, Hkv, P, {0: (pool, None)}, codecs, table, lens, 0.125,
+                                      window=W_, sinks=S_)
+        assert bad == 0
+        for b in range(B):
+            pos = sorted(_window_set(int(lens[b]), W_, S_))
+            for h in range(Hkv):
+                rows = [C.f16_bits_to_f64(pool[table[b, t // P], :, h, t % P]) for t in pos]
+                K = np.stack([r[0] for r in rows])
+                V = np.stack([r[1] for r in rows])
+                for g in range(G):
+                    ro, rl = _torch_attention(q[b, h * G + g], K, V, 0.125)
+                    assert np.allclose(o[b, h * G + g], ro, atol=1e-12, rtol=0)
+                    assert abs(lse2[b, h * G + g] - rl) < 1e-12
+
+
+def test_window_zero_query_gives_log2_of_the_visible_count():
+    q, pool, table, codecs, lens, Hkv, P = _fp16_paged_case(B=2, lens=(37, 64), seed=41)
+    q = np.zeros_like(q)
+    for W_, S_ in [(5, 4), (33, 4), (34, 4), (1, 0), (64, 3)]:
+        _, lse2, _ = A.paged_decode(q, Hkv, P, {0: (pool, None)}, codecs, table, lens, 0.125,
+                                    window=W_, sinks=S_)
+        for b, L in enumerate(lens):
+            n = min(int(L), W_) + min(S_, max(0, int(L) - W_))
+            assert np.all(np.abs(lse2[b] - math.log2(n)) < 1e-12)
+
+
+def test_window_wider_than_the_sequence_is_full_attention():
+    q, pool, table, codecs, lens, Hkv, P = _fp16_paged_case(seed=51)
+    o0, l0, _ = A.paged_decode(q, Hkv, P, {0: (pool, None)}, codecs, table, lens, 0.125)
+    o1, l1, _ = A.paged_decode(q, Hkv, P, {0: (pool, None)}, codecs, table, lens, 0.125,
+                               window=int(max(lens)), sinks=3)
+    o2, l2, _ = A.paged_decode(q, Hkv, P, {0: (pool, None)}, codecs, table, lens, 0.125,
+                               window=0, sinks=7)
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+    assert np.array_equal(o0, o2) and np.array_equal(l0, l2)
+
+
+def test_window_bad_slot_counted_only_on_pages_it_reads():
+    q, pool, table, codecs, lens, Hkv, P = _fp16_paged_case(lens=(64, 64), seed=61)
+    t2 = table.copy()
+    t2[0, 1] = pool.shape[0] + 5          # page 1 = positions 16..31
+    _, _, bad = A.paged_decode(q, Hkv, P, {0: (pool, None)}, codecs, t2, lens, 0.125, window=20, sinks=4)
+    assert bad == 0                       # visible: 0..3 and 44..63
+    _, _, bad = A.paged_decode(q, Hkv, P, {0: (pool, None)}, codecs, t2, lens, 0.125, window=40, sinks=4)
+    assert bad == Hkv                     # 24..63 reaches into page 1: one count per KV head
+
+
 # ---------------------------------------------------------------- fold
 
 def test_fold_of_any_partition_equals_single_pass():
@@ -484,3 +555,15 @@ def test_golden_byte_accounting_of_the_32k_engine_example():
     # both printed figures carry the same fixed overhead above the K/V bytes
     assert abs((g["fp16_mib"] - fp16) - (g["q4_0_mib"] - q40)) < 0.01
     assert round(g["fp16_mib"] / g["q4_0_mib"], 1) == g["ratio_printed"]
+
+
+def test_window_byte_accounting_matches_the_visible_positions():
+    rng = np.random.default_rng(77)
+    for _ in range(300):
+        L = int(rng.integers(0, 3000))
+        P = int(rng.choice([16, 64, 1024]))
+        Wn = int(rng.integers(0, 4000))
+        Sn = int(rng.integers(0, 70))
+        vis = A.visible_positions(L, Wn, Sn)
+        pages = {int(p) // P for p in np.nonzero(vis)[0]}
+        assert accounting.window_visible(L, P, Wn, Sn) == (int(vis.sum()), len(pages))
