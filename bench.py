@@ -451,14 +451,26 @@ def leg_batched(dev, timer, steps, warm, hbm):
         torch.cuda.synchronize()
     for name, pool, codec in (("bf16", bf, W.BF16), ("fp8", fp8, W.FP8_E4M3)):
         out = torch.empty((B, Hq, D_), dtype=torch.bfloat16, device=dev)
-        a = argus.decode_args(g, B, q, [pool], torch.full((B, MAXP), codec, dtype=torch.uint8, device=dev),
-                              d_table, d_lens, MAXP, W.softmax_scale(D_), out=out)
+        d_codec = torch.full((B, MAXP), codec, dtype=torch.uint8, device=dev)
+        a = argus.decode_args(g, B, q, [pool], d_codec, d_table, d_lens, MAXP, W.softmax_scale(D_), out=out)
         ws = torch.empty(max(1, argus.decode_workspace_bytes(a)), dtype=torch.uint8, device=dev)
         gr = timer.graph(lambda: argus.paged_decode_attn(a, ws, stream=timer.stream))
         ms = timer.time(gr.replay, steps, warm)
         nb = A.kv_bytes(codec, tokens, Hkv, D_, pages) + 2 * B * Hq * D_ * 2
         res["decode_" + name] = {"us_per_step": ms * 1e3, "us_per_token_layer": ms * 1e3 / B, "bytes": nb,
                                  "gbs": nb / (ms * 1e-3) / 1e9, "frac_of_hbm": nb / (ms * 1e-3) / 1e9 / hbm}
+        # the same rows under a sliding window of the newest 4096 tokens plus 4 sink tokens
+        WIN, SINK = 4096, 4
+        aw = argus.decode_args(g, B, q, [pool], d_codec, d_table, d_lens, MAXP, W.softmax_scale(D_), out=out,
+                               window_tokens=WIN, sink_tokens=SINK)
+        wsw = torch.empty(max(1, argus.decode_workspace_bytes(aw)), dtype=torch.uint8, device=dev)
+        gr = timer.graph(lambda: argus.paged_decode_attn(aw, wsw, stream=timer.stream))
+        ms = timer.time(gr.replay, steps, warm)
+        vis = [A.window_visible(L, P_, WIN, SINK) for L in lens]
+        nb = A.kv_bytes(codec, sum(t for t, _ in vis), Hkv, D_, sum(n for _, n in vis)) + 2 * B * Hq * D_ * 2
+        res["decode_%s_window" % name] = {"window": WIN, "sinks": SINK, "us_per_step": ms * 1e3,
+                                          "bytes": nb, "gbs": nb / (ms * 1e-3) / 1e9,
+                                          "frac_of_hbm": nb / (ms * 1e-3) / 1e9 / hbm}
     del bf, fp8
     torch.cuda.synchronize()
     torch.cuda.empty_cache()

@@ -162,7 +162,20 @@ typedef struct {
   uint32_t* status;           /* device uint32 anomaly counter, or NULL */
   int32_t num_splits;         /* context splits per (b, KV head); 0 = automatic */
   int32_t pdl;                /* programmatic dependent launch, see below */
+  int32_t window_tokens;      /* > 0: sliding window, see below; 0 = every token */
+  int32_t sink_tokens;        /* with a window: leading tokens that stay visible */
 } argus_decode_args;
+
+/* Sliding window with sink tokens ([ARGUS] v0.5, "Standalone PageStore /
+ * DiskBlockPool": direct attention supports sliding-window masks; the
+ * HuggingFace example's sink_tokens = 4).  With window_tokens = W > 0 the
+ * decode query of a sequence of L tokens sees the positions p with
+ *   L - W <= p < L   or   p < sink_tokens,
+ * and nothing else; pages with no visible position are not read.  Dense pages
+ * only: W > 0 together with sel_pages is ARGUS_E_UNSUPPORTED; negative values
+ * are ARGUS_E_INVALID.  W = 0 ignores sink_tokens.  The workspace and split
+ * count are sized for at most ceil(sink/16) + ceil(W/16) + 1 chunks of 16
+ * tokens per sequence. */
 
 /* args.pdl = 0: the kernels start after their stream predecessor completes
  * (ordinary stream order; always safe).

@@ -47,7 +47,8 @@ class DecodeArgs(ctypes.Structure):
                 ("softmax_scale", ctypes.c_float), ("out", ctypes.c_void_p),
                 ("out_dtype", ctypes.c_int32), ("out_f32", ctypes.c_void_p),
                 ("lse2_out", ctypes.c_void_p), ("status", ctypes.c_void_p),
-                ("num_splits", ctypes.c_int32), ("pdl", ctypes.c_int32)]
+                ("num_splits", ctypes.c_int32), ("pdl", ctypes.c_int32),
+                ("window_tokens", ctypes.c_int32), ("sink_tokens", ctypes.c_int32)]
 
 
 EXPORTS = ["argus_quantize_pages", "argus_decode_workspace_bytes", "argus_paged_decode_attn",
@@ -165,7 +166,7 @@ def quantize_pages(g, src_dtype, src_codes, n_src_slots, src_slots, dst, dst_slo
 
 def decode_args(g, batch, q, pools, page_codec, block_table, seq_lens, max_pages, softmax_scale,
                 out=None, out_f32=None, lse2_out=None, sel_pages=None, sel_count=None, sel_width=0,
-                status=None, num_splits=0, pdl=False):
+                status=None, num_splits=0, pdl=False, window_tokens=0, sink_tokens=0):
     """Build an argus_decode_args struct (keeps the pool array alive on the struct)."""
     arr = (PoolDesc * max(1, len(pools)))(*[p.desc() for p in pools])
     a = DecodeArgs()
@@ -190,6 +191,8 @@ def decode_args(g, batch, q, pools, page_codec, block_table, seq_lens, max_pages
     a.status = _ptr(status)
     a.num_splits = int(num_splits)
     a.pdl = 1 if pdl else 0
+    a.window_tokens = int(window_tokens)
+    a.sink_tokens = int(sink_tokens)
     # the struct holds raw pointers: keep every tensor it points to alive with it
     a._keep = (arr, list(pools), q, page_codec, block_table, seq_lens, sel_pages, sel_count, out,
                out_f32, lse2_out, status)

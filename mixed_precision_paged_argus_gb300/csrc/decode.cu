@@ -83,16 +83,56 @@ struct Params {
   int cps;         // chunks per split, a multiple of kChunksPerStage
   int num_splits;  // grid.x
   int pdl;         // launch the decode grid with programmatic stream serialisation
+  int window;      // > 0: only the newest `window` tokens and the first `sinks` are visible
+  int sinks;
   float* part_o;   // [B][Hkv][num_splits][G][D]
   float* part_lse; // [B][Hkv][num_splits][G]
 };
 
 struct ChunkDesc {
   int32_t codec;  // -1: empty slot in the stage
-  int32_t n_valid;
+  uint32_t vmask; // sliding window: bit r set for each visible row r; otherwise
+                  // the number of leading visible rows
   float kscale;
   float vscale;
 };
+
+// Dense chunk list of one sequence of seq_len tokens.  Without a window every
+// 16-token chunk is listed.  With window > 0 the visible tokens are the first
+// `sinks` and the newest `window` ones: the list is the sink chunks [0, cs)
+// followed by the window chunks [cw, ceil(seq_len / 16)), cw >= cs, so that
+// list entry v is chunk v (v < cs) or chunk v - cs + cw.
+struct ChunkList {
+  int n, cs, cw;
+  __host__ __device__ int chunk(int v) const { return v < cs ? v : v - cs + cw; }
+};
+
+__host__ __device__ inline ChunkList dense_chunks(int seq_len, int window, int sinks) {
+  const int nc = (seq_len + kChunk - 1) / kChunk;
+  ChunkList cl{nc, nc, nc};
+  if (window > 0) {
+    const int lo = seq_len > window ? seq_len - window : 0;   // first window token
+    cl.cs = sinks > 0 ? min((sinks + kChunk - 1) / kChunk, nc) : 0;
+    cl.cw = max(cl.cs, lo / kChunk);
+    cl.n = cl.cs + (nc - cl.cw);
+  }
+  return cl;
+}
+
+// Visible rows of the chunk starting at token tok0: bit r for token tok0 + r.
+__device__ __forceinline__ uint32_t chunk_rows(int tok0, int seq_len, int window, int sinks) {
+  const int nv = seq_len - tok0;
+  if (nv <= 0) return 0u;
+  uint32_t m = nv >= kChunk ? 0xFFFFu : (1u << nv) - 1u;
+  if (window > 0) {
+    const long long a = (long long)seq_len - window - tok0;   // rows >= a are inside the window
+    const uint32_t win = a <= 0 ? 0xFFFFu : (a >= kChunk ? 0u : (0xFFFFu << (int)a) & 0xFFFFu);
+    const int sb = sinks - tok0;              // rows < sb are sink tokens
+    const uint32_t snk = sb <= 0 ? 0u : (sb >= kChunk ? 0xFFFFu : (1u << sb) - 1u);
+    m &= win | snk;
+  }
+  return m;
+}
 
 template <int D, bool NARROW = false>
 struct Layout {
@@ -301,13 +341,14 @@ __device__ __forceinline__ void load_v_frags(int codec, const uint8_t* chunk, in
 // group is issued before any result is consumed (the m16n8k16 MMA latency is
 // long), with two accumulator chains per chunk.  sv is masked and scaled to
 // the log2 domain; kscale and the query exponent are applied here.
-template <int D, int CODEC, int NCG, bool BF, bool NARROW>
+template <int D, int CODEC, int NCG, bool BF, bool NARROW, bool WIN>
 __device__ __forceinline__ void group_scores(const uint8_t* const* cptr, const ChunkDesc* dsc, int r, int t,
                                              const uint32_t (&qf)[D / 16][2], const uint32_t (&qb)[D / 16][2],
                                              const uint32_t (&qf8)[D / 16][2],
                                              const float (&qgs)[D / 32][2], float f0h, float f1h,
                                              float scale_log2, float (*sv)[4], int c0) {
   constexpr int KC = D / 16;
+  const uint32_t rbit = 1u << r;   // WIN: this thread's rows r and r + 8 in the chunk's row mask
   uint32_t a[NCG][KC][4];
   float kz[NCG][2][D / 32][2];
 #pragma unroll
@@ -333,11 +374,13 @@ __device__ __forceinline__ void group_scores(const uint8_t* const* cptr, const C
         sc[3] += kz[c][1][i][0] * sg[c][i][3] + kz[c][1][i][1] * qgs[i][1];
       }
       const float f0 = scale_log2 * f0h, f1 = scale_log2 * f1h;
-      const int nv = dsc[c].n_valid;
-      sv[c0 + c][0] = (r < nv) ? sc[0] * f0 : -INFINITY;
-      sv[c0 + c][1] = (r < nv) ? sc[1] * f1 : -INFINITY;
-      sv[c0 + c][2] = (r + 8 < nv) ? sc[2] * f0 : -INFINITY;
-      sv[c0 + c][3] = (r + 8 < nv) ? sc[3] * f1 : -INFINITY;
+      const uint32_t vk = dsc[c].vmask;
+      const bool v0 = WIN ? (vk & rbit) != 0u : r < (int)vk;
+      const bool v1 = WIN ? (vk & (rbit << 8)) != 0u : r + 8 < (int)vk;
+      sv[c0 + c][0] = v0 ? sc[0] * f0 : -INFINITY;
+      sv[c0 + c][1] = v0 ? sc[1] * f1 : -INFINITY;
+      sv[c0 + c][2] = v1 ? sc[2] * f0 : -INFINITY;
+      sv[c0 + c][3] = v1 ? sc[3] * f1 : -INFINITY;
     }
   } else {
     float sc[NCG][2][4];
@@ -358,11 +401,13 @@ __device__ __forceinline__ void group_scores(const uint8_t* const* cptr, const C
     for (int c = 0; c < NCG; ++c) {
       const float fk = scale_log2 * dsc[c].kscale;
       const float f0 = fk * f0h, f1 = fk * f1h;
-      const int nv = dsc[c].n_valid;
-      sv[c0 + c][0] = (r < nv) ? (sc[c][0][0] + sc[c][1][0]) * f0 : -INFINITY;
-      sv[c0 + c][1] = (r < nv) ? (sc[c][0][1] + sc[c][1][1]) * f1 : -INFINITY;
-      sv[c0 + c][2] = (r + 8 < nv) ? (sc[c][0][2] + sc[c][1][2]) * f0 : -INFINITY;
-      sv[c0 + c][3] = (r + 8 < nv) ? (sc[c][0][3] + sc[c][1][3]) * f1 : -INFINITY;
+      const uint32_t vk = dsc[c].vmask;
+      const bool v0 = WIN ? (vk & rbit) != 0u : r < (int)vk;
+      const bool v1 = WIN ? (vk & (rbit << 8)) != 0u : r + 8 < (int)vk;
+      sv[c0 + c][0] = v0 ? (sc[c][0][0] + sc[c][1][0]) * f0 : -INFINITY;
+      sv[c0 + c][1] = v0 ? (sc[c][0][1] + sc[c][1][1]) * f1 : -INFINITY;
+      sv[c0 + c][2] = v1 ? (sc[c][0][2] + sc[c][1][2]) * f0 : -INFINITY;
+      sv[c0 + c][3] = v1 ? (sc[c][0][3] + sc[c][1][3]) * f1 : -INFINITY;
     }
   }
 }
@@ -408,7 +453,7 @@ __device__ __forceinline__ void group_pv(const uint8_t* const* cptr, int r, int 
   }
 }
 
-template <int D, bool QBF16, int FAM, bool NARROW>
+template <int D, bool QBF16, int FAM, bool NARROW, bool WIN>
 __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>::kMinBlocks)
     decode_kernel(const Params p) {
   constexpr int kConsumerWarps = Warps<D, NARROW>::kConsumer;
@@ -464,8 +509,10 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
   seq_len = max(0, min(seq_len, p.max_pages * P));
   const int n_pages_b = (seq_len + P - 1) / P;
   int n_chunks;
+  ChunkList cl{0, 0, 0};
   if (!sparse) {
-    n_chunks = (seq_len + kChunk - 1) / kChunk;
+    cl = dense_chunks(seq_len, WIN ? p.window : 0, WIN ? p.sinks : 0);
+    n_chunks = cl.n;
   } else {
     const int cnt = p.sel_count[b * Hkv + h];
     const int n_sel = max(0, min(cnt, p.sel_width));
@@ -514,11 +561,16 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
     // sequence length was known.
     int cur_page = pf_page, cur_codec = pf_codec;
     long long cur_slot = pf_slot;
-    if (sparse) lookup(cur_page, cur_codec, cur_slot);
+    if (sparse) {
+      lookup(cur_page, cur_codec, cur_slot);
+    } else if (WIN) {   // the speculative lookup assumed the unwindowed list
+      cur_page = cl.chunk(c_begin + lane) / cpp;
+      lookup(cur_page, cur_codec, cur_slot);
+    }
     auto page_at = [&](int base) -> int {
       if (base >= n_local) return -1;
+      if (!sparse) return (WIN ? cl.chunk(c_begin + base + lane) : c_begin + base + lane) / cpp;
       const int v = (c_begin + base + lane) / cpp;
-      if (!sparse) return v;
       return (v < p.sel_width) ? p.sel_pages[sel_row + v] : -1;
     };
     int nxt_page = page_at(32);
@@ -531,14 +583,16 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
 
       ChunkDesc d;
       d.codec = -1;
-      d.n_valid = 0;
+      d.vmask = 0;
       d.kscale = 1.f;
       d.vscale = 1.f;
       uint32_t kv_bytes = 0, m_bytes = 0;
       const uint8_t *srcK = nullptr, *srcV = nullptr, *srcMK = nullptr, *srcMV = nullptr;
       if (base + lane < n_local) {
-        const int ci = c_begin + base + lane;
+        const int ci = (WIN && !sparse) ? cl.chunk(c_begin + base + lane) : c_begin + base + lane;
         const int cip = ci - (ci / cpp) * cpp;
+        // anomalies are counted once per page: at its first listed chunk
+        const bool first = cip == 0 || (WIN && !sparse && ci == cl.cw && (cl.cs == 0 || (cl.cs - 1) / cpp != ci / cpp));
         const int page = cur_page;
         bool good = true;
         if (sparse && (page < 0 || page >= n_pages_b)) {
@@ -547,8 +601,9 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
         }
         if (good) {
           const int tok0 = page * P + cip * kChunk;
-          const int nv = min(kChunk, seq_len - tok0);
-          if (nv > 0) {
+          const uint32_t vm = WIN ? chunk_rows(tok0, seq_len, p.window, p.sinks)
+                                  : (uint32_t)max(0, min(kChunk, seq_len - tok0));
+          if (vm != 0u) {
             const int codec = cur_codec;
             const long long slot_id = cur_slot;
             bool ok = codec >= 0 && codec <= 4 && p.codes[codec] != nullptr;
@@ -559,7 +614,7 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
             if (ok) ok = slot_id >= 0 && slot_id < p.n_slots[codec];
             if (NARROW && codec <= ARGUS_BF16) ok = false;   // 16-bit rows do not fit a narrow slot
             if (!ok) {
-              if (cip == 0 && p.status) atomicAdd(p.status, 1u);
+              if (first && p.status) atomicAdd(p.status, 1u);
             } else {
               const int rowb = (codec <= ARGUS_BF16) ? 2 * D : (codec == ARGUS_INT4_G32 ? D / 2 : D);
               const size_t rk = (((size_t)slot_id * 2 + 0) * Hkv + h) * P + (size_t)cip * kChunk;
@@ -577,7 +632,7 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
                 d.kscale = ms[((size_t)slot_id * 2 + 0) * Hkv + h];
                 d.vscale = ms[((size_t)slot_id * 2 + 1) * Hkv + h];
               }
-              d.n_valid = nv;
+              d.vmask = vm;
             }
           }
         }
@@ -764,21 +819,21 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
         if constexpr (kNC == 2) {
           if (ncg == 2) {
             switch (codec) {
-              case ARGUS_FP16: group_scores<D, ARGUS_FP16, 2, false, NARROW>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-              case ARGUS_BF16: group_scores<D, ARGUS_BF16, 2, true, NARROW>(cp, dd, r, t, qf, qb, qf8, qgs, 1.f, 1.f, p.scale_log2, sv, c0); break;
-              case ARGUS_FP8_E4M3: group_scores<D, ARGUS_FP8_E4M3, 2, false, NARROW>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-              case ARGUS_INT8: group_scores<D, ARGUS_INT8, 2, false, NARROW>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-              default: group_scores<D, ARGUS_INT4_G32, 2, false, NARROW>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+              case ARGUS_FP16: group_scores<D, ARGUS_FP16, 2, false, NARROW, WIN>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+              case ARGUS_BF16: group_scores<D, ARGUS_BF16, 2, true, NARROW, WIN>(cp, dd, r, t, qf, qb, qf8, qgs, 1.f, 1.f, p.scale_log2, sv, c0); break;
+              case ARGUS_FP8_E4M3: group_scores<D, ARGUS_FP8_E4M3, 2, false, NARROW, WIN>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+              case ARGUS_INT8: group_scores<D, ARGUS_INT8, 2, false, NARROW, WIN>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+              default: group_scores<D, ARGUS_INT4_G32, 2, false, NARROW, WIN>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
             }
             return;
           }
         }
         switch (codec) {
-          case ARGUS_FP16: group_scores<D, ARGUS_FP16, 1, false, NARROW>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-          case ARGUS_BF16: group_scores<D, ARGUS_BF16, 1, true, NARROW>(cp, dd, r, t, qf, qb, qf8, qgs, 1.f, 1.f, p.scale_log2, sv, c0); break;
-          case ARGUS_FP8_E4M3: group_scores<D, ARGUS_FP8_E4M3, 1, false, NARROW>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-          case ARGUS_INT8: group_scores<D, ARGUS_INT8, 1, false, NARROW>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-          default: group_scores<D, ARGUS_INT4_G32, 1, false, NARROW>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+          case ARGUS_FP16: group_scores<D, ARGUS_FP16, 1, false, NARROW, WIN>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+          case ARGUS_BF16: group_scores<D, ARGUS_BF16, 1, true, NARROW, WIN>(cp, dd, r, t, qf, qb, qf8, qgs, 1.f, 1.f, p.scale_log2, sv, c0); break;
+          case ARGUS_FP8_E4M3: group_scores<D, ARGUS_FP8_E4M3, 1, false, NARROW, WIN>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+          case ARGUS_INT8: group_scores<D, ARGUS_INT8, 1, false, NARROW, WIN>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+          default: group_scores<D, ARGUS_INT4_G32, 1, false, NARROW, WIN>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
         }
       };
       if (same) {
@@ -976,7 +1031,7 @@ __global__ void __launch_bounds__(kFoldThreads) decode_fold_kernel(const Params 
   int seq_len = p.seq_lens[b];
   seq_len = max(0, min(seq_len, p.max_pages * p.P));
   int n_chunks;
-  if (!p.sel_pages) n_chunks = (seq_len + kChunk - 1) / kChunk;
+  if (!p.sel_pages) n_chunks = dense_chunks(seq_len, p.window, p.sinks).n;
   else n_chunks = max(0, min(p.sel_count[b * Hkv + h], p.sel_width)) * cpp;
   const int n_active = (n_chunks + p.cps - 1) / p.cps;
   if (n_active <= 1) return;
@@ -1126,10 +1181,17 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
   pl->D = g.head_dim;
   pl->G = G;
   // narrow ring: every pool holds byte or nibble codes, head_dim 128
-  pl->narrow = g.head_dim == 128 && !has_bf16 && !seen[ARGUS_FP16] && a->n_pools > 0;
+  pl->narrow = g.head_dim == 128 && !has_bf16 && !seen[ARGUS_FP16] && a->n_pools > 0 && a->window_tokens <= 0;
   const long long cps_unit = pl->narrow ? chunks_per_stage<true>() : kChunksPerStage;
   const int cpp = g.page_tokens / kChunk;
-  const long long max_chunks = a->sel_pages ? (long long)a->sel_width * cpp : (long long)a->max_pages * cpp;
+  if (a->window_tokens < 0 || a->sink_tokens < 0)
+    return fail(ARGUS_E_INVALID, "decode: window_tokens and sink_tokens must be >= 0");
+  if (a->window_tokens > 0 && a->sel_pages)
+    return fail(ARGUS_E_UNSUPPORTED, "decode: a sliding window applies to dense pages, not to a selection");
+  long long max_chunks = a->sel_pages ? (long long)a->sel_width * cpp : (long long)a->max_pages * cpp;
+  if (a->window_tokens > 0)   // sink chunks + window chunks (+1 when the window starts mid-chunk)
+    max_chunks = std::min<long long>(max_chunks, ((long long)a->sink_tokens + kChunk - 1) / kChunk +
+                                                     ((long long)a->window_tokens + kChunk - 1) / kChunk + 1);
   long long cps;
   if (a->num_splits > 0) {
     cps = (max_chunks + a->num_splits - 1) / a->num_splits;
@@ -1140,7 +1202,9 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
     // lookup-and-load latency; one CTA per resident slot does best there.
     const long long total = (long long)std::max(a->batch, 1) * g.n_kv_heads * max_chunks;
     const long long slots = (long long)device_sm_count() * (g.head_dim == 64 ? 2 : 1);
-    const long long target = a->sel_pages ? slots : 10LL * device_sm_count();
+    // A sliding window gives every row the same bounded work: one wave of
+    // CTAs (about one per SM) beats ten short ones per SM there.
+    const long long target = a->sel_pages ? slots : (a->window_tokens > 0 ? 1LL : 10LL) * device_sm_count();
     cps = std::max<long long>(cps_unit, (total + target - 1) / target);
   }
   cps = std::max<long long>(cps, (max_chunks + kMaxSplits - 1) / kMaxSplits);
@@ -1154,14 +1218,14 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
   return ARGUS_OK;
 }
 
-template <int D, bool QBF16, int FAM, bool NARROW>
+template <int D, bool QBF16, int FAM, bool NARROW, bool WIN>
 static argus_status launch_t(const Params& p, dim3 grid, cudaStream_t s) {
   using L = Layout<D, NARROW>;
   static bool configured[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(ARGUS_E_LAUNCH, "decode: no device");
   if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, QBF16, FAM, NARROW>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, QBF16, FAM, NARROW, WIN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "decode: smem attribute: %s", cudaGetErrorString(e));
     configured[dev] = true;
@@ -1176,7 +1240,7 @@ static argus_status launch_t(const Params& p, dim3 grid, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<D, QBF16, FAM, NARROW>, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<D, QBF16, FAM, NARROW, WIN>, p);
   if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "argus_paged_decode_attn: %s", cudaGetErrorString(e));
   if (p.num_splits > 1) {
     cudaLaunchConfig_t fc = cfg;
@@ -1193,16 +1257,20 @@ static argus_status launch_t(const Params& p, dim3 grid, cudaStream_t s) {
 
 template <int D>
 static argus_status launch_d(const Params& p, const Plan& pl, dim3 grid, cudaStream_t s) {
+  if (p.window > 0) {   // sliding window: the wide ring, one kernel per query type
+    if (!pl.q_bf16) return launch_t<D, false, kFamF16, false, true>(p, grid, s);
+    return launch_t<D, true, kFamMixed, false, true>(p, grid, s);
+  }
   if constexpr (D == 128) {
     if (pl.narrow) {
-      if (!pl.q_bf16) return launch_t<D, false, kFamF16, true>(p, grid, s);
-      return launch_t<D, true, kFamF16, true>(p, grid, s);
+      if (!pl.q_bf16) return launch_t<D, false, kFamF16, true, false>(p, grid, s);
+      return launch_t<D, true, kFamF16, true, false>(p, grid, s);
     }
   }
-  if (!pl.q_bf16) return launch_t<D, false, kFamF16, false>(p, grid, s);
-  if (pl.fam == kFamF16) return launch_t<D, true, kFamF16, false>(p, grid, s);
-  if (pl.fam == kFamBF16) return launch_t<D, true, kFamBF16, false>(p, grid, s);
-  return launch_t<D, true, kFamMixed, false>(p, grid, s);
+  if (!pl.q_bf16) return launch_t<D, false, kFamF16, false, false>(p, grid, s);
+  if (pl.fam == kFamF16) return launch_t<D, true, kFamF16, false, false>(p, grid, s);
+  if (pl.fam == kFamBF16) return launch_t<D, true, kFamBF16, false, false>(p, grid, s);
+  return launch_t<D, true, kFamMixed, false, false>(p, grid, s);
 }
 
 }  // namespace decode
@@ -1265,6 +1333,10 @@ static argus_status run(const argus_decode_args* a, const Plan& pl, void* ws, vo
   p.cps = pl.cps;
   p.num_splits = pl.num_splits;
   p.pdl = a->pdl ? 1 : 0;
+  // at most 2^30 tokens are ever visible (max_pages * page_tokens <= 2^30):
+  // larger values mean the same and keep the device arithmetic in range
+  p.window = std::min(a->window_tokens, 1 << 30);
+  p.sinks = a->window_tokens > 0 ? std::min(a->sink_tokens, 1 << 30) : 0;
   p.part_o = static_cast<float*>(ws);
   p.part_lse = ws ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.part_o_bytes) : nullptr;
   dim3 grid(pl.num_splits, a->g.n_kv_heads, a->batch);

@@ -77,14 +77,15 @@ def build_case(Hq, Hkv, D, P, lens, page_codecs, src_dtype=W.FP16, q_dtype=None,
 
 
 def run_decode(c, out_dtype=torch.float16, num_splits=0, sel=None, sel_count=None, sel_width=0,
-               status=None, table=None):
+               status=None, table=None, window=0, sinks=0):
     out = torch.full((c.B, c.Hq, c.D), float("nan"), dtype=out_dtype, device=DEV)
     out32 = torch.full((c.B, c.Hq, c.D), float("nan"), dtype=torch.float32, device=DEV)
     lse = torch.full((c.B, c.Hq), float("nan"), dtype=torch.float32, device=DEV)
     args = argus.decode_args(c.g, c.B, c.q, c.pools, c.d_codec,
                              c.d_table if table is None else table, c.d_lens, c.max_pages, c.scale,
                              out=out, out_f32=out32, lse2_out=lse, sel_pages=sel, sel_count=sel_count,
-                             sel_width=sel_width, status=status, num_splits=num_splits)
+                             sel_width=sel_width, status=status, num_splits=num_splits,
+                             window_tokens=window, sink_tokens=sinks)
     ws = torch.zeros(max(1, argus.decode_workspace_bytes(args)), dtype=torch.uint8, device=DEV)
     argus.paged_decode_attn(args, ws)
     torch.cuda.synchronize()

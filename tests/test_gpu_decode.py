@@ -20,9 +20,10 @@ from paged_cases import DEV, build_case, run_decode, tol
 pytestmark = pytest.mark.gpu
 
 
-def _check(c, out, out32, lse, sel=None, cnt=None, width=0, expect_bad=0):
+def _check(c, out, out32, lse, sel=None, cnt=None, width=0, expect_bad=0, window=0, sinks=0):
     ref, ref_lse, bad = oracle.paged_decode(c.q64, c.Hkv, c.P, c.opools, c.page_codec, c.table, c.lens,
-                                            c.scale, sel_pages=sel, sel_count=cnt, sel_width=width)
+                                            c.scale, sel_pages=sel, sel_count=cnt, sel_width=width,
+                                            window=window, sinks=sinks)
     assert bad == expect_bad
     got = out32.cpu().numpy().astype(np.float64)
     t = tol(ref)
@@ -256,3 +257,96 @@ def test_split_count_is_capped_and_many_splits_fold():
                              out_f32=torch.empty_like(out32), num_splits=100000)
     # workspace = splits * G * (D + 1) floats per row: at most 512 splits
     assert argus.decode_workspace_bytes(args) <= 512 * Hq * (D + 1) * 4
+
+
+# ---------------------------------------------------------------- sliding window + sink tokens
+
+WINDOWS = [(5, 0), (5, 4), (40, 4), (33, 16), (1, 33), (17, 15), (100000, 4), (64, 64)]
+
+
+@pytest.mark.parametrize("W_,S_", WINDOWS)
+@pytest.mark.parametrize("P", [16, 64])
+def test_sliding_window_with_sinks_mixed_codecs(W_, S_, P):
+    """Windows that start mid-chunk and mid-page, sinks that end mid-chunk or
+    overlap the window, windows wider than the sequence; ragged rows."""
+    Hq, Hkv, D = 14, 2, 64
+    lens = [0, 1, 37, 300, 1023]
+    maxp = -(-max(lens) // P)
+    rng = np.random.default_rng(P + W_ + S_)
+    pc = rng.choice([W.FP16, W.FP8_E4M3, W.INT8, W.INT4_G32], size=(len(lens), maxp))
+    c = build_case(Hq, Hkv, D, P, lens, pc, W.FP16, seed=500 + P, outliers=True)
+    for splits in (0, 1, 3):
+        out, out32, lse, _ = run_decode(c, num_splits=splits, window=W_, sinks=S_)
+        _check(c, out, out32, lse, window=W_, sinks=S_)
+
+
+@pytest.mark.parametrize("q_dtype", [W.FP16, W.BF16])
+def test_sliding_window_head_dim_128_narrow_and_wide_rings(q_dtype):
+    Hq, Hkv, D, P = 32, 8, 128, 16
+    lens = [2000, 513, 16]
+    maxp = 125
+    codecs = [W.FP8_E4M3, W.INT4_G32] if q_dtype == W.FP16 else [W.BF16, W.INT8]
+    pc = np.random.default_rng(5).choice(codecs, size=(3, maxp))
+    c = build_case(Hq, Hkv, D, P, lens, pc, q_dtype, seed=520)
+    out_dtype = torch.float16 if q_dtype == W.FP16 else torch.bfloat16
+    for W_, S_ in [(256, 4), (1000, 0), (77, 20)]:
+        out, out32, lse, _ = run_decode(c, out_dtype=out_dtype, window=W_, sinks=S_)
+        _check(c, out, out32, lse, window=W_, sinks=S_)
+
+
+def test_sliding_window_mixed_tier_layer_full_size():
+    """One layer of the mixed-tier workload (16 x 1024-token pages, 14 / 2 heads,
+    head_dim 64) with a 4096-token window and 4 sink tokens."""
+    Hq, Hkv, D, P = 14, 2, 64, 1024
+    pc = W.mixed_tier_codecs(16).reshape(1, 16)
+    c = build_case(Hq, Hkv, D, P, [16 * 1024], pc, W.FP16, seed=530, outliers=True)
+    out, out32, lse, _ = run_decode(c, window=4096, sinks=4)
+    _check(c, out, out32, lse, window=4096, sinks=4)
+    full = run_decode(c)[1]
+    assert not torch.allclose(full, out32)      # the window changes the result
+
+
+def test_sliding_window_bad_slots_counted_once_per_read_page():
+    Hq, Hkv, D, P = 8, 2, 64, 16
+    pc = np.full((1, 8), W.INT8)
+    c = build_case(Hq, Hkv, D, P, [128], pc, W.FP16, seed=540)
+    table = c.table.copy()
+    table[0, 1] = 1000    # positions 16..31: outside sinks 0..3 and window 58..127
+    table[0, 3] = 1001    # positions 48..63: the window starts mid-page (58)
+    table[0, 0] = 1002    # positions 0..15: sink tokens 0..3
+    c.table = table
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, out32, lse, _ = run_decode(c, status=status, table=torch.from_numpy(table).to(DEV),
+                                    window=70, sinks=4, num_splits=2)
+    _check(c, out, out32, lse, expect_bad=2 * Hkv, window=70, sinks=4)
+    assert int(status.item()) == 2 * Hkv
+    # one page holding both sink tokens and the window's start: counted once
+    c2 = build_case(Hq, Hkv, D, 64, [100], np.full((1, 2), W.INT8), W.FP16, seed=541)
+    t2 = c2.table.copy()
+    t2[0, 0] = 1000       # positions 0..63 hold the sinks 0..3 and the window from 40
+    c2.table = t2
+    status.zero_()
+    out, out32, lse, _ = run_decode(c2, status=status, table=torch.from_numpy(t2).to(DEV), window=60, sinks=4)
+    _check(c2, out, out32, lse, expect_bad=Hkv, window=60, sinks=4)
+    assert int(status.item()) == Hkv
+
+
+def test_sliding_window_argument_checks_and_smaller_workspace():
+    Hq, Hkv, D, P = 8, 1, 64, 16
+    c = build_case(Hq, Hkv, D, P, [200], np.full((1, 13), W.FP16), W.FP16, seed=550)
+    with pytest.raises(argus.ArgusError) as e:
+        run_decode(c, window=-1)
+    assert e.value.status == 1
+    with pytest.raises(argus.ArgusError) as e:
+        run_decode(c, window=8, sinks=-2)
+    assert e.value.status == 1
+    sel = torch.zeros((1, Hkv, 2), dtype=torch.int32, device=DEV)
+    cnt = torch.ones((1, Hkv), dtype=torch.int32, device=DEV)
+    with pytest.raises(argus.ArgusError) as e:
+        run_decode(c, sel=sel, sel_count=cnt, sel_width=2, window=8)
+    assert e.value.status == 2
+    def ws_bytes(**kw):
+        a = argus.decode_args(c.g, 1, c.q, c.pools, c.d_codec, c.d_table, c.d_lens, 4096, c.scale,
+                              out_f32=torch.empty((1, Hq, D), device=DEV), num_splits=0, **kw)
+        return argus.decode_workspace_bytes(a)
+    assert ws_bytes(window_tokens=64, sink_tokens=4) < ws_bytes()
