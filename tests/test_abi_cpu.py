@@ -66,3 +66,34 @@ def test_host_validation_without_gpu():
     g = argus.geom(8, 2, 128, 16)
     assert L.argus_select_workspace_bytes(ctypes.byref(g), 2, 10, ctypes.byref(n)) == 0
     assert n.value == 2 * 2 * 10 * 4
+
+
+def _c_layout(struct, fields, tmp_path):
+    """sizeof and offsetof of a header struct, from a C program compiled by gcc."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "layout.c"
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "argus.h"', 'int main(void) {',
+             '  printf("%%zu\\n", sizeof(%s));' % struct]
+    lines += ['  printf("%%zu\\n", offsetof(%s, %s));' % (struct, f) for f in fields]
+    lines += ['  return 0;', '}']
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    return int(out[0]), [int(x) for x in out[1:]]
+
+
+@pytest.mark.parametrize("cls,struct", [(argus.Geom, "argus_geom"), (argus.PoolDesc, "argus_pool"),
+                                        (argus.DecodeArgs, "argus_decode_args")])
+def test_binding_structs_match_the_header_layout(cls, struct, tmp_path):
+    """Every field of the ctypes mirror sits at the C offset, and the sizes agree
+    (the header's structs are what the library reads)."""
+    names = [f[0] for f in cls._fields_]
+    size, offs = _c_layout(struct, names, tmp_path)
+    assert ctypes.sizeof(cls) == size
+    for name, off in zip(names, offs):
+        assert getattr(cls, name).offset == off, name
