@@ -20,6 +20,11 @@ out; the readings taken here (all listed in the design notes) are:
   min/max; z = fp16_sat(lo); s = fp16_sat(fp32(fp32(hi - z) / 15));
   q = s > 0 ? clamp(rint_even(fp32(fp32(x - z) / s)), 0, 15) : 0; two codes per
   byte, the even element in the low nibble.  Dequantised value = q * s + z.
+* INT2 with 32-element groups: the same "unsigned_affine" encoder with
+  bits = 2 (the pluggable-tier example registers
+  NativeCodecSpec(kind="unsigned_affine", bits=2)), i.e. 3 in place of 15:
+  s = fp16_sat(fp32(fp32(hi - z) / 3)), q = clamp(rint_even(...), 0, 3); four
+  codes per byte, element 4k + j in bits 2j, 2j + 1 of byte k.
 
 Each "fp32(...)" is one IEEE single-precision operation with
 round-to-nearest-even, emulated as the float64 operation followed by a cast
@@ -28,9 +33,9 @@ to float32 (exact for one +, -, * or / of float32 operands, since
 
 Layouts (shared by definition with the C ABI, not by code):
   codes  [n_slots][2 (K, V)][Hkv][P][row]  row = D halves (FP16/BF16),
-         D bytes (FP8/INT8), D/2 bytes (INT4)
+         D bytes (FP8/INT8), D/2 bytes (INT4), D/4 bytes (INT2)
   meta   FP8/INT8: float32 [n_slots][2][Hkv];
-         INT4: float16 [n_slots][2][Hkv][P][D/32][2] = (scale, zero)
+         INT4 / INT2: float16 [n_slots][2][Hkv][P][D/32][2] = (scale, zero)
 """
 
 import math
@@ -42,6 +47,7 @@ CODEC_BF16 = 1
 CODEC_FP8_E4M3 = 2
 CODEC_INT8 = 3
 CODEC_INT4_G32 = 4
+CODEC_INT2_G32 = 5
 
 F16_MAX = 65504.0
 
@@ -179,17 +185,28 @@ def quantize_group_int4(x32):
     x32 shape [..., 32]; returns codes [..., 32] (uint8, one per element),
     s [...] float16, z [...] float16.
     """
+    return _quantize_group_affine(x32, 15)
+
+
+def quantize_group_int2(x32):
+    """Groups of 32 along the last axis -> (codes 0..3, fp16 scale, fp16 zero);
+    the INT4 steps with 3 levels above the zero point in place of 15."""
+    return _quantize_group_affine(x32, 3)
+
+
+def _quantize_group_affine(x32, top):
+    """unsigned_affine over groups of 32: codes 0..top (top = 2^bits - 1)."""
     x32 = _f32(x32)
     lo = np.min(x32, axis=-1)
     hi = np.max(x32, axis=-1)
     z = fp16_rne_sat(lo)
     span = _f32(hi.astype(np.float64) - z.astype(np.float64))
-    s = fp16_rne_sat(_f32(span.astype(np.float64) / 15.0))
+    s = fp16_rne_sat(_f32(span.astype(np.float64) / float(top)))
     num = _f32(x32.astype(np.float64) - z.astype(np.float64)[..., None])
     s64 = s.astype(np.float64)[..., None]
     with np.errstate(divide="ignore", invalid="ignore"):
         y = _f32(num.astype(np.float64) / np.where(s64 > 0, s64, 1.0))
-    q = np.clip(np.rint(y), 0, 15)
+    q = np.clip(np.rint(y), 0, top)
     q = np.where(s64 > 0, q, 0)
     return q.astype(np.uint8), s, z
 
@@ -198,6 +215,20 @@ def pack_int4(codes):
     """[..., D] codes 0..15 -> [..., D/2] bytes, even element in the low nibble."""
     c = codes.astype(np.uint8)
     return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+
+
+def pack_int2(codes):
+    """[..., D] codes 0..3 -> [..., D/4] bytes, element 4k + j in bits 2j of byte k."""
+    c = codes.astype(np.uint8)
+    return (c[..., 0::4] | (c[..., 1::4] << 2) | (c[..., 2::4] << 4) | (c[..., 3::4] << 6)).astype(np.uint8)
+
+
+def unpack_int2(packed):
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (p.shape[-1] * 4,), np.uint8)
+    for j in range(4):
+        out[..., j::4] = (p >> (2 * j)) & 3
+    return out
 
 
 def unpack_int4(packed):
@@ -221,8 +252,8 @@ def dequant_page(codec, codes, meta, slot, kv, h):
         return e4m3_table()[c.astype(np.int64)] * np.float64(meta[slot, kv, h])
     if codec == CODEC_INT8:
         return c.view(np.int8).astype(np.float64) * np.float64(meta[slot, kv, h])
-    if codec == CODEC_INT4_G32:
-        q = unpack_int4(c).astype(np.float64)              # [P][D]
+    if codec in (CODEC_INT4_G32, CODEC_INT2_G32):
+        q = (unpack_int4(c) if codec == CODEC_INT4_G32 else unpack_int2(c)).astype(np.float64)   # [P][D]
         P, D = q.shape
         sz = meta[slot, kv, h].astype(np.float64)          # [P][D/32][2]
         qg = q.reshape(P, D // 32, 32)
@@ -241,8 +272,9 @@ def alloc_pool(codec, n_slots, hkv, P, D):
     if codec in (CODEC_FP8_E4M3, CODEC_INT8):
         return (np.zeros((n_slots, 2, hkv, P, D), np.uint8),
                 np.zeros((n_slots, 2, hkv), np.float32))
-    if codec == CODEC_INT4_G32:
-        return (np.zeros((n_slots, 2, hkv, P, D // 2), np.uint8),
+    if codec in (CODEC_INT4_G32, CODEC_INT2_G32):
+        row = D // 2 if codec == CODEC_INT4_G32 else D // 4
+        return (np.zeros((n_slots, 2, hkv, P, row), np.uint8),
                 np.zeros((n_slots, 2, hkv, P, D // 32, 2), np.float16))
     raise ValueError("unknown codec %r" % codec)
 
@@ -289,15 +321,16 @@ def quantize_pages(src_bits, src_dtype, src_slots, dst_codec, dst_codes, dst_met
                     out[:valid] = codes
                     dst_codes[di, kv, h] = out.view(np.uint8)
                     dst_meta[di, kv, h] = scale
-                elif dst_codec == CODEC_INT4_G32:
+                elif dst_codec in (CODEC_INT4_G32, CODEC_INT2_G32):
                     q = np.zeros((P, D), np.uint8)
                     sz = np.zeros((P, D // 32, 2), np.float16)
                     if valid:
-                        qc, s, z = quantize_group_int4(xv.reshape(valid, D // 32, 32))
+                        enc = quantize_group_int4 if dst_codec == CODEC_INT4_G32 else quantize_group_int2
+                        qc, s, z = enc(xv.reshape(valid, D // 32, 32))
                         q[:valid] = qc.reshape(valid, D)
                         sz[:valid, :, 0] = s
                         sz[:valid, :, 1] = z
-                    dst_codes[di, kv, h] = pack_int4(q)
+                    dst_codes[di, kv, h] = pack_int4(q) if dst_codec == CODEC_INT4_G32 else pack_int2(q)
                     dst_meta[di, kv, h] = sz
                 else:
                     raise ValueError("unknown codec %r" % dst_codec)

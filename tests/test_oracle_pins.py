@@ -163,6 +163,61 @@ def test_int4_error_bound_and_degenerate_group():
     assert s0[0] == 0 and z0[0] == np.float16(1.25) and not c.any()
 
 
+# ---------------------------------------------------------------- INT2 codec
+
+def test_int2_pack_order_element_4k_plus_j_in_bits_2j():
+    # byte 0: 1 | 2<<2 | 3<<4 | 0<<6 = 0x39; byte 1: 3 | 3<<2 | 0<<4 | 1<<6 = 0x4F
+    assert C.pack_int2(np.array([1, 2, 3, 0, 3, 3, 0, 1], np.uint8)).tolist() == [0x39, 0x4F]
+    assert C.unpack_int2(np.array([0x39, 0x4F], np.uint8)).tolist() == [1, 2, 3, 0, 3, 3, 0, 1]
+
+
+def test_int2_round_trip_exact_on_representable_groups():
+    rng = np.random.default_rng(13)
+    for s_exp in (-6, -2, 0, 3):
+        s = 2.0 ** s_exp
+        q = rng.integers(0, 4, size=(20, 32))
+        q[:, 0], q[:, 1] = 0, 3
+        z = rng.integers(-40, 40, size=(20, 1)) * s
+        x = (q * s + z).astype(np.float32)
+        codes, ss, zz = C.quantize_group_int2(x)
+        assert np.all(ss.astype(np.float64) == s)
+        assert np.array_equal(zz.astype(np.float64), z[:, 0])
+        assert np.array_equal(codes.astype(np.int64), q)
+
+
+def test_int2_error_bound_and_degenerate_group():
+    rng = np.random.default_rng(14)
+    x = (rng.standard_normal((500, 32)) * rng.uniform(0.1, 10, (500, 1))).astype(np.float32)
+    codes, s, z = C.quantize_group_int2(x)
+    assert codes.max() <= 3
+    rec = codes * s.astype(np.float64)[:, None] + z.astype(np.float64)[:, None]
+    lo = x.min(axis=1).astype(np.float64)
+    hi = x.max(axis=1).astype(np.float64)
+    s64, z64 = s.astype(np.float64), z.astype(np.float64)
+    bound = 0.5 * s64 + np.abs(lo - z64) + 4 * np.abs((hi - z64) / 3 - s64) + 1e-6
+    assert np.all(np.abs(rec - x) <= bound[:, None])
+    assert np.all(codes.max(axis=1) >= 2)
+    c, s0, z0 = C.quantize_group_int2(np.full((1, 32), -3.5, np.float32))
+    assert s0[0] == 0 and z0[0] == np.float16(-3.5) and not c.any()
+
+
+def test_int2_codes_against_a_torch_float32_pipeline():
+    """torch's IEEE float32 ops (no float64 emulation) give the same codes,
+    scales and zero points inside fp16's range."""
+    rng = np.random.default_rng(15)
+    x = (rng.standard_normal((2000, 32)) * rng.uniform(0.01, 100, (2000, 1))).astype(np.float32)
+    x[::7, 5:9] = np.floor(x[::7, 5:9]) + 0.5
+    codes, s, z = C.quantize_group_int2(x)
+    t = torch.from_numpy(x)
+    tz = t.min(dim=1).values.to(torch.float16)
+    ts = ((t.max(dim=1).values - tz.float()) / 3.0).to(torch.float16)
+    y = (t - tz.float()[:, None]) / torch.where(ts > 0, ts, torch.ones_like(ts)).float()[:, None]
+    tq = torch.clamp(torch.round(y), 0, 3)
+    tq = torch.where((ts > 0)[:, None], tq, torch.zeros_like(tq))
+    assert np.array_equal(z, tz.numpy()) and np.array_equal(s, ts.numpy())
+    assert np.array_equal(codes.astype(np.int64), tq.numpy().astype(np.int64))
+
+
 # ---------------------------------------------------------------- bf16 rounding
 
 def test_round_to_bf16_matches_torch_for_float32_inputs():
@@ -180,7 +235,7 @@ def _src_pool(n, hkv, P, D, dtype, seed):
     return W.to_bits(t)
 
 
-@pytest.mark.parametrize("codec", [C.CODEC_FP8_E4M3, C.CODEC_INT8, C.CODEC_INT4_G32])
+@pytest.mark.parametrize("codec", [C.CODEC_FP8_E4M3, C.CODEC_INT8, C.CODEC_INT4_G32, C.CODEC_INT2_G32])
 def test_quantize_pages_units_independent_and_ckey(codec):
     hkv, P, D = 2, 16, 64
     src = _src_pool(3, hkv, P, D, C.CODEC_BF16, 11)
