@@ -34,12 +34,16 @@
  * Pool layout (one pool per codec; a pool is an array of physical page slots):
  *   codes  [n_slots][2 (K, V)][Hkv][P][row]   row = head_dim 16-bit values
  *          (FP16 / BF16), head_dim bytes (FP8 e4m3 / INT8), head_dim/2 bytes
- *          (INT4: two codes per byte, the even element in the low nibble)
+ *          (INT4: two codes per byte, the even element in the low nibble),
+ *          head_dim/4 bytes (INT2: element 4k + j in bits 2j, 2j+1 of byte k)
  *   meta   FP16 / BF16: unused (NULL)
  *          FP8 / INT8:  float [n_slots][2][Hkv]  one scale per (page, head, K|V)
- *          INT4:        half2 {scale, zero} [n_slots][2][Hkv][P][head_dim/32]
+ *          INT4 / INT2: half2 {scale, zero} [n_slots][2][Hkv][P][head_dim/32]
  *   Dequantised value: FP8 e4m3_value(code) * scale; INT8 code * scale;
- *   INT4 code * scale + zero.  Codes and pools must be 16-byte aligned.
+ *   INT4 / INT2 code * scale + zero.  INT4 per token and group of 32:
+ *   z = fp16_sat(min), s = fp16_sat(RN(RN(max - z) / 15)), code =
+ *   clamp(rint(RN(x - z) / s), 0, 15) (s = 0: code 0); INT2 the same with 3
+ *   in place of 15.  Codes and pools must be 16-byte aligned.
  */
 #ifndef ARGUS_H
 #define ARGUS_H
@@ -60,13 +64,16 @@ typedef enum {
 } argus_status;
 
 /* Codec tiers of [ARGUS] (summary; "Direct paged attention": FP16, Q8, Q4 pages)
- * and [PR499] update 20f3b23 ("e4m3 codes + fp32 scales"). */
+ * and [PR499] update 20f3b23 ("e4m3 codes + fp32 scales").  INT2 is the
+ * summary's INT2 tier in the "unsigned_affine, bits = 2" form of the ARGUS
+ * page's "Pluggable tiers" example, with the INT4 tier's 32-element groups. */
 typedef enum {
   ARGUS_FP16 = 0,
   ARGUS_BF16 = 1,
   ARGUS_FP8_E4M3 = 2,
   ARGUS_INT8 = 3,
-  ARGUS_INT4_G32 = 4
+  ARGUS_INT4_G32 = 4,
+  ARGUS_INT2_G32 = 5
 } argus_codec;
 
 typedef struct {
@@ -87,7 +94,8 @@ typedef struct {
 /* ---------------------------------------------------------------------------
  * argus_quantize_pages -- page demotion through the codec tiers.
  *
- * [ARGUS] summary: older pages are demoted from FP16 through FP8, INT8, INT4;
+ * [ARGUS] summary: older pages are demoted from FP16 through FP8, INT8, INT4
+ * (and INT2);
  * [PR499] update 20f3b23: the pool holds e4m3 codes + fp32 scales and is the
  * source of truth.  For each listed page i and each (K|V, KV head h) unit:
  *   FP8:  a = max|x| over the unit's valid tokens; scale = a / 448 (fp32);

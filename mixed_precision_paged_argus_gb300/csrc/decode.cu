@@ -65,9 +65,9 @@ enum Family { kFamF16 = 0, kFamBF16 = 1, kFamMixed = 2 };
 struct Params {
   int B, Hkv, G, P, max_pages;
   const void* q;
-  const uint8_t* codes[5];
-  const uint8_t* meta[5];
-  long long n_slots[5];
+  const uint8_t* codes[6];   // indexed by argus_codec
+  const uint8_t* meta[6];
+  long long n_slots[6];
   const uint8_t* page_codec;
   const int32_t* block_table;
   const int32_t* seq_lens;
@@ -212,6 +212,23 @@ __device__ __forceinline__ void load_k_frags(int codec, const uint8_t* chunk, in
           }
         }
       }
+    } else if (codec == ARGUS_INT2_G32) {
+      // the lane's 8-element run of group i is 2 bytes: byte b holds elements
+      // 4b .. 4b+3 in bit pairs; spread to the two halves, shifts of 0, 2, 4, 6
+      // give the element pairs (0,4), (1,5), (2,6), (3,7) of the INT4 map
+#pragma unroll
+      for (int i = 0; i < L::kNI; ++i) {
+        const uint32_t w16 = *reinterpret_cast<const uint16_t*>(chunk + L::kOffK + row * (D / 4) + 8 * i + 2 * t);
+        const uint32_t w = prmt(w16, 0u, 0x4140);
+        const __half2 mz = *reinterpret_cast<const __half2*>(chunk + L::kOffMK + (row * L::kNI + i) * 4);
+        kz[rr][i][0] = __low2float(mz);
+        kz[rr][i][1] = __high2float(mz);
+        const uint32_t magic = 0x64006400u;
+        a[2 * i][rr] = hsub2_u32(lop3_and_or(w, 0x00030003u, magic), magic);
+        a[2 * i][2 + rr] = hsub2_u32(lop3_and_or(w >> 2, 0x00030003u, magic), magic);
+        a[2 * i + 1][rr] = hsub2_u32(lop3_and_or(w >> 4, 0x00030003u, magic), magic);
+        a[2 * i + 1][2 + rr] = hsub2_u32(lop3_and_or(w >> 6, 0x00030003u, magic), magic);
+      }
     } else {  // INT4 group 32
 #pragma unroll
       for (int i = 0; i < L::kNI; ++i) {
@@ -299,6 +316,36 @@ __device__ __forceinline__ void load_v_frags(int codec, const uint8_t* chunk, in
         }
       }
     }
+  } else if (codec == ARGUS_INT2_G32) {
+    // the lane's DL elements of a row are DL/4 bytes (DL = 16: one word)
+    uint32_t cw[4];
+    uint32_t m[4];
+    const int grp = (DL * r) / 32;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint8_t* src = chunk + L::kOffV + rows[q] * (D / 4) + (DL / 4) * r;
+      if constexpr (DL == 16) cw[q] = *reinterpret_cast<const uint32_t*>(src);
+      else cw[q] = *reinterpret_cast<const uint16_t*>(src);
+      m[q] = *reinterpret_cast<const uint32_t*>(chunk + L::kOffMV + (rows[q] * L::kNI + grp) * 4);
+    }
+    const uint32_t magic = 0x64006400u;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int q0 = 2 * half;
+      const uint32_t s2 = prmt(m[q0], m[q0 + 1], 0x5410);
+      const uint32_t z2 = prmt(m[q0], m[q0 + 1], 0x7632);
+#pragma unroll
+      for (int b = 0; b < DL / 4; ++b) {
+        // byte b of row a to byte 0, of row b to byte 2 (bytes 1, 3 are masked off)
+        const uint32_t x = prmt(cw[q0], cw[q0 + 1], (uint32_t)(b | (b << 4) | ((4 + b) << 8) | ((4 + b) << 12)));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t c = hsub2_u32(lop3_and_or(x >> (2 * j), 0x00030003u, magic), magic);
+          const int d = 4 * b + j;
+          v[d / 2][2 * half + (d & 1)] = hfma2_u32(c, s2, z2);
+        }
+      }
+    }
   } else {  // INT4
     uint32_t w[4][DL / 8];
     uint32_t m[4];
@@ -341,19 +388,19 @@ __device__ __forceinline__ void load_v_frags(int codec, const uint8_t* chunk, in
 // group is issued before any result is consumed (the m16n8k16 MMA latency is
 // long), with two accumulator chains per chunk.  sv is masked and scaled to
 // the log2 domain; kscale and the query exponent are applied here.
-template <int D, int CODEC, int NCG, bool BF, bool NARROW, bool WIN>
+template <int D, int CODEC, int NCG, bool BF, bool NARROW, bool EXT>
 __device__ __forceinline__ void group_scores(const uint8_t* const* cptr, const ChunkDesc* dsc, int r, int t,
                                              const uint32_t (&qf)[D / 16][2], const uint32_t (&qb)[D / 16][2],
                                              const uint32_t (&qf8)[D / 16][2],
                                              const float (&qgs)[D / 32][2], float f0h, float f1h,
                                              float scale_log2, float (*sv)[4], int c0) {
   constexpr int KC = D / 16;
-  const uint32_t rbit = 1u << r;   // WIN: this thread's rows r and r + 8 in the chunk's row mask
+  const uint32_t rbit = 1u << r;   // EXT: this thread's rows r and r + 8 in the chunk's row mask
   uint32_t a[NCG][KC][4];
   float kz[NCG][2][D / 32][2];
 #pragma unroll
   for (int c = 0; c < NCG; ++c) load_k_frags<D, NARROW>(CODEC, cptr[c], r, t, a[c], kz[c]);
-  if constexpr (CODEC == ARGUS_INT4_G32) {
+  if constexpr (CODEC == ARGUS_INT4_G32 || CODEC == ARGUS_INT2_G32) {
     float sg[NCG][D / 32][4];
 #pragma unroll
     for (int c = 0; c < NCG; ++c)
@@ -375,8 +422,8 @@ __device__ __forceinline__ void group_scores(const uint8_t* const* cptr, const C
       }
       const float f0 = scale_log2 * f0h, f1 = scale_log2 * f1h;
       const uint32_t vk = dsc[c].vmask;
-      const bool v0 = WIN ? (vk & rbit) != 0u : r < (int)vk;
-      const bool v1 = WIN ? (vk & (rbit << 8)) != 0u : r + 8 < (int)vk;
+      const bool v0 = EXT ? (vk & rbit) != 0u : r < (int)vk;
+      const bool v1 = EXT ? (vk & (rbit << 8)) != 0u : r + 8 < (int)vk;
       sv[c0 + c][0] = v0 ? sc[0] * f0 : -INFINITY;
       sv[c0 + c][1] = v0 ? sc[1] * f1 : -INFINITY;
       sv[c0 + c][2] = v1 ? sc[2] * f0 : -INFINITY;
@@ -402,8 +449,8 @@ __device__ __forceinline__ void group_scores(const uint8_t* const* cptr, const C
       const float fk = scale_log2 * dsc[c].kscale;
       const float f0 = fk * f0h, f1 = fk * f1h;
       const uint32_t vk = dsc[c].vmask;
-      const bool v0 = WIN ? (vk & rbit) != 0u : r < (int)vk;
-      const bool v1 = WIN ? (vk & (rbit << 8)) != 0u : r + 8 < (int)vk;
+      const bool v0 = EXT ? (vk & rbit) != 0u : r < (int)vk;
+      const bool v1 = EXT ? (vk & (rbit << 8)) != 0u : r + 8 < (int)vk;
       sv[c0 + c][0] = v0 ? (sc[c][0][0] + sc[c][1][0]) * f0 : -INFINITY;
       sv[c0 + c][1] = v0 ? (sc[c][0][1] + sc[c][1][1]) * f1 : -INFINITY;
       sv[c0 + c][2] = v1 ? (sc[c][0][2] + sc[c][1][2]) * f0 : -INFINITY;
@@ -453,7 +500,7 @@ __device__ __forceinline__ void group_pv(const uint8_t* const* cptr, int r, int 
   }
 }
 
-template <int D, bool QBF16, int FAM, bool NARROW, bool WIN>
+template <int D, bool QBF16, int FAM, bool NARROW, bool EXT>
 __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>::kMinBlocks)
     decode_kernel(const Params p) {
   constexpr int kConsumerWarps = Warps<D, NARROW>::kConsumer;
@@ -511,7 +558,7 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
   int n_chunks;
   ChunkList cl{0, 0, 0};
   if (!sparse) {
-    cl = dense_chunks(seq_len, WIN ? p.window : 0, WIN ? p.sinks : 0);
+    cl = dense_chunks(seq_len, EXT ? p.window : 0, EXT ? p.sinks : 0);
     n_chunks = cl.n;
   } else {
     const int cnt = p.sel_count[b * Hkv + h];
@@ -563,13 +610,13 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
     long long cur_slot = pf_slot;
     if (sparse) {
       lookup(cur_page, cur_codec, cur_slot);
-    } else if (WIN) {   // the speculative lookup assumed the unwindowed list
+    } else if (EXT) {   // the speculative lookup assumed the unwindowed list
       cur_page = cl.chunk(c_begin + lane) / cpp;
       lookup(cur_page, cur_codec, cur_slot);
     }
     auto page_at = [&](int base) -> int {
       if (base >= n_local) return -1;
-      if (!sparse) return (WIN ? cl.chunk(c_begin + base + lane) : c_begin + base + lane) / cpp;
+      if (!sparse) return (EXT ? cl.chunk(c_begin + base + lane) : c_begin + base + lane) / cpp;
       const int v = (c_begin + base + lane) / cpp;
       return (v < p.sel_width) ? p.sel_pages[sel_row + v] : -1;
     };
@@ -589,10 +636,10 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
       uint32_t kv_bytes = 0, m_bytes = 0;
       const uint8_t *srcK = nullptr, *srcV = nullptr, *srcMK = nullptr, *srcMV = nullptr;
       if (base + lane < n_local) {
-        const int ci = (WIN && !sparse) ? cl.chunk(c_begin + base + lane) : c_begin + base + lane;
+        const int ci = (EXT && !sparse) ? cl.chunk(c_begin + base + lane) : c_begin + base + lane;
         const int cip = ci - (ci / cpp) * cpp;
         // anomalies are counted once per page: at its first listed chunk
-        const bool first = cip == 0 || (WIN && !sparse && ci == cl.cw && (cl.cs == 0 || (cl.cs - 1) / cpp != ci / cpp));
+        const bool first = cip == 0 || (EXT && !sparse && ci == cl.cw && (cl.cs == 0 || (cl.cs - 1) / cpp != ci / cpp));
         const int page = cur_page;
         bool good = true;
         if (sparse && (page < 0 || page >= n_pages_b)) {
@@ -601,12 +648,13 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
         }
         if (good) {
           const int tok0 = page * P + cip * kChunk;
-          const uint32_t vm = WIN ? chunk_rows(tok0, seq_len, p.window, p.sinks)
+          const uint32_t vm = EXT ? chunk_rows(tok0, seq_len, p.window, p.sinks)
                                   : (uint32_t)max(0, min(kChunk, seq_len - tok0));
           if (vm != 0u) {
             const int codec = cur_codec;
             const long long slot_id = cur_slot;
-            bool ok = codec >= 0 && codec <= 4 && p.codes[codec] != nullptr;
+            // INT2 pages are read by the extended kernels only
+            bool ok = codec >= 0 && codec <= (EXT ? ARGUS_INT2_G32 : ARGUS_INT4_G32) && p.codes[codec] != nullptr;
             if (ok) {
               const int fam = codec_family(codec);
               ok = (FAM == kFamMixed) || (FAM == fam);
@@ -616,14 +664,15 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
             if (!ok) {
               if (first && p.status) atomicAdd(p.status, 1u);
             } else {
-              const int rowb = (codec <= ARGUS_BF16) ? 2 * D : (codec == ARGUS_INT4_G32 ? D / 2 : D);
+              const int rowb = (codec <= ARGUS_BF16) ? 2 * D
+                             : (codec == ARGUS_INT4_G32 ? D / 2 : (codec == ARGUS_INT2_G32 ? D / 4 : D));
               const size_t rk = (((size_t)slot_id * 2 + 0) * Hkv + h) * P + (size_t)cip * kChunk;
               const size_t rv = (((size_t)slot_id * 2 + 1) * Hkv + h) * P + (size_t)cip * kChunk;
               srcK = p.codes[codec] + rk * rowb;
               srcV = p.codes[codec] + rv * rowb;
               kv_bytes = kChunk * rowb;
               d.codec = codec;
-              if (codec == ARGUS_INT4_G32) {
+              if (codec == ARGUS_INT4_G32 || codec == ARGUS_INT2_G32) {
                 srcMK = p.meta[codec] + rk * (L::kNI * 4);
                 srcMV = p.meta[codec] + rv * (L::kNI * 4);
                 m_bytes = kChunk * L::kNI * 4;
@@ -819,21 +868,37 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
         if constexpr (kNC == 2) {
           if (ncg == 2) {
             switch (codec) {
-              case ARGUS_FP16: group_scores<D, ARGUS_FP16, 2, false, NARROW, WIN>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-              case ARGUS_BF16: group_scores<D, ARGUS_BF16, 2, true, NARROW, WIN>(cp, dd, r, t, qf, qb, qf8, qgs, 1.f, 1.f, p.scale_log2, sv, c0); break;
-              case ARGUS_FP8_E4M3: group_scores<D, ARGUS_FP8_E4M3, 2, false, NARROW, WIN>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-              case ARGUS_INT8: group_scores<D, ARGUS_INT8, 2, false, NARROW, WIN>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-              default: group_scores<D, ARGUS_INT4_G32, 2, false, NARROW, WIN>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+              case ARGUS_FP16: group_scores<D, ARGUS_FP16, 2, false, NARROW, EXT>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+              case ARGUS_BF16: group_scores<D, ARGUS_BF16, 2, true, NARROW, EXT>(cp, dd, r, t, qf, qb, qf8, qgs, 1.f, 1.f, p.scale_log2, sv, c0); break;
+              case ARGUS_FP8_E4M3: group_scores<D, ARGUS_FP8_E4M3, 2, false, NARROW, EXT>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+              case ARGUS_INT8: group_scores<D, ARGUS_INT8, 2, false, NARROW, EXT>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+              default:
+                if constexpr (EXT) {   // the INT2 tier exists in the extended kernels only
+                  if (codec == ARGUS_INT2_G32) {
+                    group_scores<D, ARGUS_INT2_G32, 2, false, NARROW, EXT>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0);
+                    break;
+                  }
+                }
+                group_scores<D, ARGUS_INT4_G32, 2, false, NARROW, EXT>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0);
+                break;
             }
             return;
           }
         }
         switch (codec) {
-          case ARGUS_FP16: group_scores<D, ARGUS_FP16, 1, false, NARROW, WIN>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-          case ARGUS_BF16: group_scores<D, ARGUS_BF16, 1, true, NARROW, WIN>(cp, dd, r, t, qf, qb, qf8, qgs, 1.f, 1.f, p.scale_log2, sv, c0); break;
-          case ARGUS_FP8_E4M3: group_scores<D, ARGUS_FP8_E4M3, 1, false, NARROW, WIN>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-          case ARGUS_INT8: group_scores<D, ARGUS_INT8, 1, false, NARROW, WIN>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
-          default: group_scores<D, ARGUS_INT4_G32, 1, false, NARROW, WIN>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+          case ARGUS_FP16: group_scores<D, ARGUS_FP16, 1, false, NARROW, EXT>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+          case ARGUS_BF16: group_scores<D, ARGUS_BF16, 1, true, NARROW, EXT>(cp, dd, r, t, qf, qb, qf8, qgs, 1.f, 1.f, p.scale_log2, sv, c0); break;
+          case ARGUS_FP8_E4M3: group_scores<D, ARGUS_FP8_E4M3, 1, false, NARROW, EXT>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+          case ARGUS_INT8: group_scores<D, ARGUS_INT8, 1, false, NARROW, EXT>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0); break;
+          default:
+            if constexpr (EXT) {   // the INT2 tier exists in the extended kernels only
+              if (codec == ARGUS_INT2_G32) {
+                group_scores<D, ARGUS_INT2_G32, 1, false, NARROW, EXT>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0);
+                break;
+              }
+            }
+            group_scores<D, ARGUS_INT4_G32, 1, false, NARROW, EXT>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0);
+            break;
         }
       };
       if (same) {
@@ -911,7 +976,15 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
               case ARGUS_BF16: group_pv<D, ARGUS_BF16, 2, true, NARROW>(cp, r, t, pw + c0, skip + c0, acc); break;
               case ARGUS_FP8_E4M3: group_pv<D, ARGUS_FP8_E4M3, 2, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc); break;
               case ARGUS_INT8: group_pv<D, ARGUS_INT8, 2, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc); break;
-              default: group_pv<D, ARGUS_INT4_G32, 2, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc); break;
+              default:
+                if constexpr (EXT) {
+                  if (codec == ARGUS_INT2_G32) {
+                    group_pv<D, ARGUS_INT2_G32, 2, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc);
+                    break;
+                  }
+                }
+                group_pv<D, ARGUS_INT4_G32, 2, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc);
+                break;
             }
             return;
           }
@@ -921,7 +994,15 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
           case ARGUS_BF16: group_pv<D, ARGUS_BF16, 1, true, NARROW>(cp, r, t, pw + c0, skip + c0, acc); break;
           case ARGUS_FP8_E4M3: group_pv<D, ARGUS_FP8_E4M3, 1, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc); break;
           case ARGUS_INT8: group_pv<D, ARGUS_INT8, 1, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc); break;
-          default: group_pv<D, ARGUS_INT4_G32, 1, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc); break;
+          default:
+            if constexpr (EXT) {
+              if (codec == ARGUS_INT2_G32) {
+                group_pv<D, ARGUS_INT2_G32, 1, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc);
+                break;
+              }
+            }
+            group_pv<D, ARGUS_INT4_G32, 1, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc);
+            break;
         }
       };
       if (same) {
@@ -1125,6 +1206,7 @@ __global__ void __launch_bounds__(kFoldThreads) decode_fold_kernel(const Params 
 struct Plan {
   int D, G, cps, num_splits, fam;
   bool q_bf16, narrow;
+  bool ext;   // extended kernels: a sliding window or an INT2 pool
   size_t part_o_bytes, ws_bytes;
 };
 
@@ -1156,11 +1238,11 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
   if (!std::isfinite(a->softmax_scale)) return fail(ARGUS_E_INVALID, "decode: softmax_scale not finite");
   if (a->out && a->out_dtype != ARGUS_FP16 && a->out_dtype != ARGUS_BF16)
     return fail(ARGUS_E_INVALID, "decode: out_dtype must be FP16 or BF16");
-  bool seen[5] = {false, false, false, false, false};
+  bool seen[6] = {false, false, false, false, false, false};
   bool has_bf16 = false, has_f16 = false;
   for (int i = 0; i < a->n_pools; ++i) {
     const argus_pool& pool = a->pools[i];
-    if (pool.codec < 0 || pool.codec > 4) return fail(ARGUS_E_INVALID, "decode: pool %d has codec %d", i, pool.codec);
+    if (pool.codec < 0 || pool.codec > ARGUS_INT2_G32) return fail(ARGUS_E_INVALID, "decode: pool %d has codec %d", i, pool.codec);
     if (seen[pool.codec]) return fail(ARGUS_E_INVALID, "decode: two pools with codec %d", pool.codec);
     seen[pool.codec] = true;
     if (pool.n_slots < 0) return fail(ARGUS_E_INVALID, "decode: pool %d n_slots < 0", i);
@@ -1181,7 +1263,8 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
   pl->D = g.head_dim;
   pl->G = G;
   // narrow ring: every pool holds byte or nibble codes, head_dim 128
-  pl->narrow = g.head_dim == 128 && !has_bf16 && !seen[ARGUS_FP16] && a->n_pools > 0 && a->window_tokens <= 0;
+  pl->ext = a->window_tokens > 0 || seen[ARGUS_INT2_G32];
+  pl->narrow = g.head_dim == 128 && !has_bf16 && !seen[ARGUS_FP16] && a->n_pools > 0 && !pl->ext;
   const long long cps_unit = pl->narrow ? chunks_per_stage<true>() : kChunksPerStage;
   const int cpp = g.page_tokens / kChunk;
   if (a->window_tokens < 0 || a->sink_tokens < 0)
@@ -1218,14 +1301,14 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
   return ARGUS_OK;
 }
 
-template <int D, bool QBF16, int FAM, bool NARROW, bool WIN>
+template <int D, bool QBF16, int FAM, bool NARROW, bool EXT>
 static argus_status launch_t(const Params& p, dim3 grid, cudaStream_t s) {
   using L = Layout<D, NARROW>;
   static bool configured[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(ARGUS_E_LAUNCH, "decode: no device");
   if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, QBF16, FAM, NARROW, WIN>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, QBF16, FAM, NARROW, EXT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "decode: smem attribute: %s", cudaGetErrorString(e));
     configured[dev] = true;
@@ -1240,7 +1323,7 @@ static argus_status launch_t(const Params& p, dim3 grid, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<D, QBF16, FAM, NARROW, WIN>, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<D, QBF16, FAM, NARROW, EXT>, p);
   if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "argus_paged_decode_attn: %s", cudaGetErrorString(e));
   if (p.num_splits > 1) {
     cudaLaunchConfig_t fc = cfg;
@@ -1257,7 +1340,7 @@ static argus_status launch_t(const Params& p, dim3 grid, cudaStream_t s) {
 
 template <int D>
 static argus_status launch_d(const Params& p, const Plan& pl, dim3 grid, cudaStream_t s) {
-  if (p.window > 0) {   // sliding window: the wide ring, one kernel per query type
+  if (pl.ext) {   // sliding window or INT2 pages: the wide ring, one kernel per query type
     if (!pl.q_bf16) return launch_t<D, false, kFamF16, false, true>(p, grid, s);
     return launch_t<D, true, kFamMixed, false, true>(p, grid, s);
   }
@@ -1307,7 +1390,7 @@ static argus_status run(const argus_decode_args* a, const Plan& pl, void* ws, vo
   p.P = a->g.page_tokens;
   p.max_pages = a->max_pages;
   p.q = a->q;
-  for (int c = 0; c < 5; ++c) {
+  for (int c = 0; c < 6; ++c) {
     p.codes[c] = nullptr;
     p.meta[c] = nullptr;
     p.n_slots[c] = 0;

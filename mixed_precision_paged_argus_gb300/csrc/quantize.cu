@@ -127,16 +127,18 @@ __device__ __noinline__ F8 div8(F8 x, float s) {
   return q;
 }
 
-//  INT4 scale: fp16_sat(RN(a / 15)).  a * RN(1/15) is within 3 ulp of RN(a/15);
-//  the fp16 rounding can only differ within a few ulps of an fp16 midpoint
-//  (fp32 mantissa bits below the fp16 ones equal to 0x1000) or in fp16's
-//  subnormal range, where the division itself is taken.
-__device__ __forceinline__ float scale_div15(float a) {
-  float y = a * (1.f / 15.f);
+//  INT4 / INT2 scale: fp16_sat(RN(a / TOP)), TOP = 15 or 3.  a * RN(1/TOP) is
+//  within 3 ulp of RN(a/TOP); the fp16 rounding can only differ within a few
+//  ulps of an fp16 midpoint (fp32 mantissa bits below the fp16 ones equal to
+//  0x1000) or in fp16's subnormal range, where the division itself is taken.
+template <int TOP>
+__device__ __forceinline__ float scale_div(float a) {
+  float y = a * (1.f / (float)TOP);
   const uint32_t low = __float_as_uint(y) & 0x1FFFu;
-  if (((low - 0x1000u + 8u) <= 16u) || fabsf(y) < 0x1p-14f) y = a / 15.f;
+  if (((low - 0x1000u + 8u) <= 16u) || fabsf(y) < 0x1p-14f) y = a / (float)TOP;
   return fp16_sat(y);
 }
+__device__ __forceinline__ float scale_div15(float a) { return scale_div<15>(a); }
 
 // Encode 8 values of one 16-byte source vector and store them; with DEQ the
 // stored values are also decoded into deq (for the compressed key).  rscale is
@@ -222,7 +224,10 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
       for (int e = 0; e < 8; ++e) deq[e] = (float)(int8_t)((w[e / 4] >> (8 * (e & 3))) & 0xFF) * scale;
     }
     reinterpret_cast<uint2*>(dcodes)[vec] = make_uint2(w[0], w[1]);
-  } else {  // INT4: the 4 threads of a 32-element group cooperate
+  } else {  // INT4 / INT2: the 4 threads of a 32-element group cooperate
+    constexpr int BITS = (CODEC == ARGUS_INT4_G32) ? 4 : 2;
+    constexpr int TOP = (1 << BITS) - 1;
+    constexpr uint32_t MASK = (uint32_t)TOP;
     float lo = f[0], hi = f[0];
 #pragma unroll
     for (int e = 1; e < 8; ++e) {
@@ -234,7 +239,7 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
     lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, 2));
     hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, 2));
     const float z = fp16_sat(lo);
-    const float s = scale_div15(hi - z);
+    const float s = scale_div<TOP>(hi - z);
     uint32_t w = 0u;
     if (valid && s > 0.f) {
       const float r = __frcp_rn(s);
@@ -244,7 +249,7 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         d[e] = f[e] - z;
-        const float y = fminf(fmaxf(d[e] * r, 0.f), 15.f);
+        const float y = fminf(fmaxf(d[e] * r, 0.f), (float)TOP);
         const float tf = y + kRoundMagic;
         unsure |= rint_unsure(y, tf);
         t[e] = __float_as_uint(tf);
@@ -255,17 +260,20 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
         for (int e = 0; e < 8; ++e) x.v[e] = d[e];
         const F8 q = div8(x, s);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) t[e] = __float_as_uint(fminf(fmaxf(q.v[e], 0.f), 15.f) + kRoundMagic);
+        for (int e = 0; e < 8; ++e) t[e] = __float_as_uint(fminf(fmaxf(q.v[e], 0.f), (float)TOP) + kRoundMagic);
       }
+      // code e of the 8 at bits BITS * e: INT4 even elements in the low
+      // nibbles, INT2 element 4k + j at bits 2j of byte k
 #pragma unroll
-      for (int e = 0; e < 8; ++e) w |= (t[e] & 0xFu) << (4 * e);
+      for (int e = 0; e < 8; ++e) w |= (t[e] & MASK) << (BITS * e);
     }
     const float zz = valid ? z : 0.f, ss = valid ? s : 0.f;
     if (DEQ) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) deq[e] = fmaf((float)((w >> (4 * e)) & 0xF), ss, zz);
+      for (int e = 0; e < 8; ++e) deq[e] = fmaf((float)((w >> (BITS * e)) & MASK), ss, zz);
     }
-    reinterpret_cast<uint32_t*>(dcodes)[vec] = w;
+    if (BITS == 4) reinterpret_cast<uint32_t*>(dcodes)[vec] = w;
+    else reinterpret_cast<uint16_t*>(dcodes)[vec] = (uint16_t)w;
     if ((lane_in_group & 3) == 0) {
       const __half2 sz = __halves2half2(__float2half_rn(ss), __float2half_rn(zz));
       *reinterpret_cast<__half2*>(dmeta_row) = sz;
@@ -304,6 +312,7 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_kernel(const QParams p) 
     uint8_t* dcodes;
     if (CODEC == ARGUS_FP16 || CODEC == ARGUS_BF16) dcodes = p.dst_codes + unit_dst * (size_t)P * D * 2;
     else if (CODEC == ARGUS_INT4_G32) dcodes = p.dst_codes + unit_dst * (size_t)P * (D / 2);
+    else if (CODEC == ARGUS_INT2_G32) dcodes = p.dst_codes + unit_dst * (size_t)P * (D / 4);
     else dcodes = p.dst_codes + unit_dst * (size_t)P * D;
 
     const bool regs = (GROUP == 32) && (nvec <= 32 * kRegVecs);
@@ -346,7 +355,7 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_kernel(const QParams p) 
       const bool valid_v = v < nvalid_vec;
       float deq[8];
       uint8_t* meta_row = nullptr;
-      if (CODEC == ARGUS_INT4_G32) {
+      if (CODEC == ARGUS_INT4_G32 || CODEC == ARGUS_INT2_G32) {
         const int row = v / VPR, grp = (v % VPR) / 4;
         meta_row = p.dst_meta + ((unit_dst * P + row) * (D / 32) + grp) * 4;
       }
@@ -584,6 +593,7 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_small_kernel(const QPara
       uint8_t* dcodes;
       if (CODEC == ARGUS_FP16 || CODEC == ARGUS_BF16) dcodes = p.dst_codes + cu.dst * (size_t)P * D * 2;
       else if (CODEC == ARGUS_INT4_G32) dcodes = p.dst_codes + cu.dst * (size_t)P * (D / 2);
+      else if (CODEC == ARGUS_INT2_G32) dcodes = p.dst_codes + cu.dst * (size_t)P * (D / 4);
       else dcodes = p.dst_codes + cu.dst * (size_t)P * D;
       float scale = 0.f;
       if (CODEC == ARGUS_FP8_E4M3 || CODEC == ARGUS_INT8) {
@@ -615,7 +625,7 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_small_kernel(const QPara
             float f[8], deq[8];
             unpack8<SBF16>(cur[k], f);
             uint8_t* meta_row = nullptr;
-            if (CODEC == ARGUS_INT4_G32) {
+            if (CODEC == ARGUS_INT4_G32 || CODEC == ARGUS_INT2_G32) {
               const int row = v / VPR, grp = (v % VPR) / 4;
               meta_row = p.dst_meta + ((cu.dst * P + row) * (D / 32) + grp) * 4;
             }
@@ -685,6 +695,7 @@ static argus_status launch2(int codec, const QParams& p, cudaStream_t s) {
     case ARGUS_BF16: return launch3<D, SBF16, ARGUS_BF16>(p, s);
     case ARGUS_FP8_E4M3: return launch3<D, SBF16, ARGUS_FP8_E4M3>(p, s);
     case ARGUS_INT8: return launch3<D, SBF16, ARGUS_INT8>(p, s);
+    case ARGUS_INT2_G32: return launch3<D, SBF16, ARGUS_INT2_G32>(p, s);
     default: return launch3<D, SBF16, ARGUS_INT4_G32>(p, s);
   }
 }
@@ -708,7 +719,7 @@ extern "C" argus_status argus_quantize_pages(const argus_geom* g, int32_t src_dt
     return fail(ARGUS_E_UNSUPPORTED, "quantize: head_dim %d (supported: 64, 128)", g->head_dim);
   if (src_dtype != ARGUS_FP16 && src_dtype != ARGUS_BF16)
     return fail(ARGUS_E_INVALID, "quantize: src_dtype must be FP16 or BF16");
-  if (dst->codec < 0 || dst->codec > 4) return fail(ARGUS_E_INVALID, "quantize: bad destination codec");
+  if (dst->codec < 0 || dst->codec > ARGUS_INT2_G32) return fail(ARGUS_E_INVALID, "quantize: bad destination codec");
   if ((dst->codec == ARGUS_FP16 || dst->codec == ARGUS_BF16) && dst->codec != src_dtype)
     return fail(ARGUS_E_UNSUPPORTED, "quantize: a 16-bit destination must match the source dtype");
   if (n_pages < 0) return fail(ARGUS_E_INVALID, "quantize: negative n_pages");

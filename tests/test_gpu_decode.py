@@ -41,7 +41,7 @@ def _check(c, out, out32, lse, sel=None, cnt=None, width=0, expect_bad=0, window
     return err
 
 
-@pytest.mark.parametrize("codec", [W.FP16, W.FP8_E4M3, W.INT8, W.INT4_G32])
+@pytest.mark.parametrize("codec", [W.FP16, W.FP8_E4M3, W.INT8, W.INT4_G32, W.INT2_G32])
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("G", [1, 7, 8])
 def test_single_codec_fp16_query(codec, D, G):
@@ -54,7 +54,7 @@ def test_single_codec_fp16_query(codec, D, G):
     _check(c, out, out32, lse)
 
 
-@pytest.mark.parametrize("codec", [W.BF16, W.FP8_E4M3, W.INT8, W.INT4_G32])
+@pytest.mark.parametrize("codec", [W.BF16, W.FP8_E4M3, W.INT8, W.INT4_G32, W.INT2_G32])
 @pytest.mark.parametrize("G", [4, 8])
 def test_single_codec_bf16_query(codec, G):
     Hkv, D, P = 2, 128, 16
@@ -350,3 +350,45 @@ def test_sliding_window_argument_checks_and_smaller_workspace():
                               out_f32=torch.empty((1, Hq, D), device=DEV), num_splits=0, **kw)
         return argus.decode_workspace_bytes(a)
     assert ws_bytes(window_tokens=64, sink_tokens=4) < ws_bytes()
+
+
+# ---------------------------------------------------------------- INT2 tier
+
+@pytest.mark.parametrize("q_dtype", [W.FP16, W.BF16])
+@pytest.mark.parametrize("D", [64, 128])
+def test_five_tiers_with_int2_oldest(q_dtype, D):
+    """Newest pages FP16 (BF16 for a bf16 query), then FP8, INT8, INT4 and the
+    oldest INT2; ragged rows, several split counts, with and without a window."""
+    Hq, Hkv, P = 16, 2, 64
+    n = 20
+    top = W.FP16 if q_dtype == W.FP16 else W.BF16
+    row = np.array([W.INT2_G32] * 4 + [W.INT4_G32] * 4 + [W.INT8] * 4 + [W.FP8_E4M3] * 4 + [top] * 4)
+    pc = np.stack([row, np.roll(row, 7)])
+    c = build_case(Hq, Hkv, D, P, [n * P - 9, 700], pc, q_dtype, seed=600 + D, outliers=True)
+    out_dtype = torch.float16 if q_dtype == W.FP16 else torch.bfloat16
+    for splits in (0, 1, 5):
+        out, out32, lse, _ = run_decode(c, out_dtype=out_dtype, num_splits=splits)
+        _check(c, out, out32, lse)
+    out, out32, lse, _ = run_decode(c, out_dtype=out_dtype, window=300, sinks=4)
+    _check(c, out, out32, lse, window=300, sinks=4)
+
+
+def test_int2_selected_pages():
+    Hq, Hkv, D, P = 32, 4, 128, 64
+    maxp = 24
+    lens = [24 * 64 - 3, 10 * 64 + 5]
+    pc = np.full((2, maxp), W.INT2_G32)
+    c = build_case(Hq, Hkv, D, P, lens, pc, W.BF16, seed=610)
+    width = 8
+    sel = np.full((2, Hkv, width), -1, np.int32)
+    cnt = np.zeros((2, Hkv), np.int32)
+    rng = np.random.default_rng(611)
+    for b in range(2):
+        n = -(-lens[b] // P)
+        for h in range(Hkv):
+            pages = sorted(rng.choice(n - 1, size=4, replace=False).tolist() + [n - 1])
+            sel[b, h, :len(pages)] = pages
+            cnt[b, h] = len(pages)
+    out, out32, lse, _ = run_decode(c, out_dtype=torch.bfloat16, sel=torch.from_numpy(sel).to(DEV),
+                                    sel_count=torch.from_numpy(cnt).to(DEV), sel_width=width)
+    _check(c, out, out32, lse, sel=sel, cnt=cnt, width=width)

@@ -90,7 +90,7 @@ def test_int8_rounding_exhaustive_over_fp16():
     _compare(pool, codes, meta)
 
 
-@pytest.mark.parametrize("codec", [W.FP8_E4M3, W.INT8, W.INT4_G32, "copy"])
+@pytest.mark.parametrize("codec", [W.FP8_E4M3, W.INT8, W.INT4_G32, W.INT2_G32, "copy"])
 @pytest.mark.parametrize("src_dtype", [W.FP16, W.BF16])
 @pytest.mark.parametrize("D,P", [(64, 16), (128, 16), (128, 64), (64, 1024)])
 def test_random_pages_bit_exact_with_ckeys(codec, src_dtype, D, P):
@@ -133,7 +133,7 @@ def test_bad_slots_are_counted_and_skipped():
 def test_zero_unit_gives_zero_scale():
     Hkv, P, D = 1, 16, 128
     src = torch.zeros((1, 2, Hkv, P, D), dtype=torch.bfloat16)
-    for codec in (W.FP8_E4M3, W.INT8, W.INT4_G32):
+    for codec in (W.FP8_E4M3, W.INT8, W.INT4_G32, W.INT2_G32):
         pool, _, _ = _gpu_quantize(src, W.BF16, codec, Hkv, P, D, [0], [0], 1)
         assert not _codes_np(pool).any() and not _meta_np(pool).any()
 
@@ -183,21 +183,23 @@ def test_codes_near_rounding_boundaries_with_a_non_power_of_two_scale(codec):
     _compare(pool, codes, meta)
 
 
+@pytest.mark.parametrize("codec", [W.INT4_G32, W.INT2_G32])
 @pytest.mark.parametrize("ckey", [False, True])
 @pytest.mark.parametrize("src_dtype", [W.FP16, W.BF16])
-def test_int4_groups_with_pinned_range_and_interior_values(ckey, src_dtype):
+def test_int4_groups_with_pinned_range_and_interior_values(ckey, src_dtype, codec):
     """Groups whose min and max pin z and s, interior values uniform in between
     (many land within 2^-12 of a half-integer quotient, some on exact ties when
-    s is a power of two); V units use the one-lane-per-group path, K units the
-    compressed-key path when ckey is set."""
+    s is a power of two); INT4 V units use the one-lane-per-group path, K units
+    the compressed-key path when ckey is set; INT2 units the cooperative path."""
     Hkv, P, D, n = 2, 16, 128, 48
-    rng = np.random.default_rng(7 + ckey + 2 * src_dtype)
+    top = 15 if codec == W.INT4_G32 else 3
+    rng = np.random.default_rng(7 + ckey + 2 * src_dtype + codec)
     groups = n * 2 * Hkv * P * (D // 32)
     z = rng.standard_normal(groups) * 4
     s = np.abs(rng.standard_normal(groups)) * 0.3 + 1e-3
     s[::5] = 2.0 ** rng.integers(-6, 0, size=len(s[::5]))          # exact ties possible
-    k = rng.uniform(0, 15, size=(groups, 32))
-    k[:, 0], k[:, 1] = 0.0, 15.0
+    k = rng.uniform(0, top, size=(groups, 32))
+    k[:, 0], k[:, 1] = 0.0, float(top)
     k[::3, 2:] = np.floor(k[::3, 2:]) + 0.5                          # on / near the half-integers
     x = z[:, None] + k * s[:, None]
     if src_dtype == W.FP16:
@@ -206,9 +208,9 @@ def test_int4_groups_with_pinned_range_and_interior_values(ckey, src_dtype):
         bits = C.f64_to_bf16_bits(x)
     src = bits.reshape(n, 2, Hkv, P, D)
     t = torch.from_numpy(src.view(np.int16)).view(torch.float16 if src_dtype == W.FP16 else torch.bfloat16)
-    pool, ck, st = _gpu_quantize(t, src_dtype, W.INT4_G32, Hkv, P, D, list(range(n)), list(range(n)), n,
+    pool, ck, st = _gpu_quantize(t, src_dtype, codec, Hkv, P, D, list(range(n)), list(range(n)), n,
                                  ckey=ckey)
     assert st == 0
-    codes, meta = C.alloc_pool(C.CODEC_INT4_G32, n, Hkv, P, D)
-    C.quantize_pages(src, src_dtype, list(range(n)), C.CODEC_INT4_G32, codes, meta, list(range(n)))
+    codes, meta = C.alloc_pool(codec, n, Hkv, P, D)
+    C.quantize_pages(src, src_dtype, list(range(n)), codec, codes, meta, list(range(n)))
     _compare(pool, codes, meta)
