@@ -13,6 +13,7 @@ and use inputs larger than L2 where the kernel streams HBM.
   quantize_fp8    demote 128 Ki 16x128 BF16 units to FP8 (512 MB read)
   quantize_int8   the same to INT8
   quantize_int4   the same to INT4
+  quantize_int2   the same to INT2
   select          indexer scores + top-k for one layer of the sparse workload
   prefill         one 131072-token window of the windowed prefill
   fold            fold a 16 x 1024 x 128 fp32 partial into an accumulator
@@ -151,6 +152,7 @@ CASES = {
     "quantize_fp8": lambda d: _quantize(d, W.FP8_E4M3),
     "quantize_int8": lambda d: _quantize(d, W.INT8),
     "quantize_int4": lambda d: _quantize(d, W.INT4_G32),
+    "quantize_int2": lambda d: _quantize(d, W.INT2_G32),
     "select": _select,
     "prefill": _prefill,
     "fold": _fold,
