@@ -138,7 +138,6 @@ __device__ __forceinline__ float scale_div(float a) {
   if (((low - 0x1000u + 8u) <= 16u) || fabsf(y) < 0x1p-14f) y = a / (float)TOP;
   return fp16_sat(y);
 }
-__device__ __forceinline__ float scale_div15(float a) { return scale_div<15>(a); }
 
 // Encode 8 values of one 16-byte source vector and store them; with DEQ the
 // stored values are also decoded into deq (for the compressed key).  rscale is
@@ -425,12 +424,15 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_kernel(const QParams p) 
   }
 }
 
-// INT4 with one lane per 32-element group (the group's four 16-byte source
-// vectors in x0..x3): the min / max reduction and the scale arithmetic are
-// lane-local and done once per group, and the 32 codes leave as one 16-byte
-// store.  Same arithmetic, hence the same codes, as encode_store's INT4 path.
-template <bool SBF16>
-__device__ __forceinline__ void encode_int4_group(const uint4 (&x)[4], bool valid, uint4& codes, uint32_t& meta) {
+// INT4 / INT2 with one lane per 32-element group (the group's four 16-byte
+// source vectors in x0..x3): the min / max reduction and the scale arithmetic
+// are lane-local and done once per group, and the 32 codes leave as one store
+// (16 bytes of INT4 in w[0..3], 8 bytes of INT2 in w[0..1]).  Same arithmetic,
+// hence the same codes, as encode_store's INT4 / INT2 path.
+template <bool SBF16, int BITS>
+__device__ __forceinline__ void encode_affine_group(const uint4 (&x)[4], bool valid, uint32_t (&wout)[4],
+                                                    uint32_t& meta) {
+  constexpr int TOP = (1 << BITS) - 1;
   uint32_t mn, mx;
   {
     const uint32_t* wv = reinterpret_cast<const uint32_t*>(&x[0]);
@@ -462,13 +464,13 @@ __device__ __forceinline__ void encode_int4_group(const uint4 (&x)[4], bool vali
   const float lo = fminf(to_f(mn & 0xFFFFu), to_f(mn >> 16));
   const float hi = fmaxf(to_f(mx & 0xFFFFu), to_f(mx >> 16));
   const float z = fp16_sat(lo);
-  const float s = scale_div15(hi - z);
+  const float s = scale_div<TOP>(hi - z);
   uint32_t w[4] = {0u, 0u, 0u, 0u};
   if (valid && s > 0.f) {
     const float r = __frcp_rn(s);
     // the products are monotone in x: when those of the group's min and max
-    // round into 0..15, no product needs the clamp
-    const bool clamp = !((lo - z) * r > -0.49f && (hi - z) * r < 15.49f);
+    // round into 0..TOP, no product needs the clamp
+    const bool clamp = !((lo - z) * r > -0.49f && (hi - z) * r < (float)TOP + 0.49f);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       float f[8], d[8];
@@ -480,7 +482,7 @@ __device__ __forceinline__ void encode_int4_group(const uint4 (&x)[4], bool vali
         for (int e = 0; e < 8; ++e) {
           d[e] = f[e] - z;
           float y = d[e] * r;
-          if (decltype(clamp_tag)::value) y = fminf(fmaxf(y, 0.f), 15.f);
+          if (decltype(clamp_tag)::value) y = fminf(fmaxf(y, 0.f), (float)TOP);
           const float tf = y + kRoundMagic;
           dev = fmaxf(dev, fabsf(y - (tf - kRoundMagic)));
           t[e] = __float_as_uint(tf);
@@ -494,15 +496,25 @@ __device__ __forceinline__ void encode_int4_group(const uint4 (&x)[4], bool vali
         for (int e = 0; e < 8; ++e) x.v[e] = d[e];
         const F8 q = div8(x, s);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) t[e] = __float_as_uint(fminf(fmaxf(q.v[e], 0.f), 15.f) + kRoundMagic);
+        for (int e = 0; e < 8; ++e) t[e] = __float_as_uint(fminf(fmaxf(q.v[e], 0.f), (float)TOP) + kRoundMagic);
       }
-      // low bytes of t are the codes 0..15: even elements in the low nibbles
-      const uint32_t ev = prmt(prmt(t[0], t[2], 0x0040), prmt(t[4], t[6], 0x0040), 0x5410);
-      const uint32_t od = prmt(prmt(t[1], t[3], 0x0040), prmt(t[5], t[7], 0x0040), 0x5410);
-      w[m] = ev + (od << 4);
+      if (BITS == 4) {
+        // low bytes of t are the codes 0..15: even elements in the low nibbles
+        const uint32_t ev = prmt(prmt(t[0], t[2], 0x0040), prmt(t[4], t[6], 0x0040), 0x5410);
+        const uint32_t od = prmt(prmt(t[1], t[3], 0x0040), prmt(t[5], t[7], 0x0040), 0x5410);
+        w[m] = ev + (od << 4);
+      } else {
+        // codes 0..3: byte 0 takes elements 0..3, byte 1 elements 4..7, element
+        // j of a byte at bits 2j; xj holds elements j and 4 + j in bytes 0, 1
+        const uint32_t x0 = prmt(t[0], t[4], 0x0040), x1 = prmt(t[1], t[5], 0x0040);
+        const uint32_t x2 = prmt(t[2], t[6], 0x0040), x3 = prmt(t[3], t[7], 0x0040);
+        const uint32_t w16 = (x0 | (x1 << 2) | (x2 << 4) | (x3 << 6)) & 0xFFFFu;
+        w[m >> 1] |= w16 << (16 * (m & 1));
+      }
     }
   }
-  codes = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) wout[k] = w[k];
   const __half2 sz = __halves2half2(__float2half_rn(valid ? s : 0.f), __float2half_rn(valid ? z : 0.f));
   meta = *reinterpret_cast<const uint32_t*>(&sz);
 }
@@ -547,7 +559,7 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_small_kernel(const QPara
   // INT4 units without a compressed key use one lane per 32-element group:
   // slot 4j + m holds vector m of group lane + 32j
   auto group_layout = [&](const Unit& d) {
-    return CODEC == ARGUS_INT4_G32 && !(want_ck_any && d.kv == 0);
+    return (CODEC == ARGUS_INT4_G32 || CODEC == ARGUS_INT2_G32) && !(want_ck_any && d.kv == 0);
   };
   auto load = [&](const Unit& d, uint4 (&buf)[kRegVecs]) {
     const bool gl = group_layout(d);
@@ -574,17 +586,19 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_small_kernel(const QPara
       if (lane == 0 && cu.kv == 0 && cu.h == 0 && p.status) atomicAdd(p.status, 1u);
     } else if (group_layout(cu)) {
       constexpr int GPR = D / 32;  // groups per token row
-      uint4* gcodes = reinterpret_cast<uint4*>(p.dst_codes + cu.dst * (size_t)P * (D / 2));
+      constexpr int BITS = (CODEC == ARGUS_INT4_G32) ? 4 : 2;
+      uint8_t* gcodes = p.dst_codes + cu.dst * (size_t)P * (D * BITS / 8);
       uint32_t* gmeta = reinterpret_cast<uint32_t*>(p.dst_meta) + cu.dst * (size_t)P * GPR;
 #pragma unroll
       for (int j = 0; j < kRegVecs / 4; ++j) {
         const int idx = lane + 32 * j;
         if (4 * idx < nvec) {
           const uint4 xg[4] = {cur[4 * j], cur[4 * j + 1], cur[4 * j + 2], cur[4 * j + 3]};
-          uint4 c;
+          uint32_t c[4];
           uint32_t m;
-          encode_int4_group<SBF16>(xg, idx / GPR < cu.valid, c, m);
-          gcodes[idx] = c;
+          encode_affine_group<SBF16, BITS>(xg, idx / GPR < cu.valid, c, m);
+          if (BITS == 4) reinterpret_cast<uint4*>(gcodes)[idx] = make_uint4(c[0], c[1], c[2], c[3]);
+          else reinterpret_cast<uint2*>(gcodes)[idx] = make_uint2(c[0], c[1]);
           gmeta[idx] = m;
         }
       }
