@@ -68,6 +68,47 @@ def test_host_validation_without_gpu():
     assert n.value == 2 * 2 * 10 * 4
 
 
+def test_codec_range_window_and_int2_checks_without_gpu():
+    """Codec numbers outside 0..5 fail closed; an INT2 pool is accepted; a window
+    rejects negative values and selection lists; a window shrinks the workspace."""
+    L = _lib()
+    n = ctypes.c_size_t(0)
+    a = argus.DecodeArgs()
+    a.g = argus.geom(8, 2, 128, 16)
+    a.batch, a.q_dtype, a.max_pages, a.num_splits = 2, 0, 256, 4
+
+    def pools(*codecs):
+        arr = (argus.PoolDesc * len(codecs))(*[argus.PoolDesc(c, 0, 16, 16, 8) for c in codecs])
+        a.pools = ctypes.cast(arr, ctypes.POINTER(argus.PoolDesc))
+        a.n_pools = len(codecs)
+        return arr
+
+    keep = pools(argus.INT2_G32, argus.FP8_E4M3)
+    assert L.argus_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 0
+    full = n.value
+    keep = pools(6)
+    assert L.argus_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 1
+    keep = pools(argus.INT2_G32)
+    a.window_tokens, a.sink_tokens = 64, 4
+    assert L.argus_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 0
+    assert n.value < full
+    a.window_tokens = -1
+    assert L.argus_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 1
+    a.window_tokens, a.sink_tokens = 64, -4
+    assert L.argus_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 1
+    a.sink_tokens = 4
+    sel = ctypes.c_int32(0)
+    a.sel_pages = a.sel_count = ctypes.cast(ctypes.byref(sel), ctypes.c_void_p)
+    a.sel_width = 4
+    assert L.argus_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 2
+    del keep
+    # quantize: destination codec 6 is rejected before any device work
+    g = argus.geom(8, 2, 128, 16)
+    dst = argus.PoolDesc(6, 0, 16, 16, 4)
+    assert L.argus_quantize_pages(ctypes.byref(g), argus.FP16, 16, 4, 16, ctypes.byref(dst), 16, 1,
+                                  None, None, None, None) == 1
+
+
 def _c_layout(struct, fields, tmp_path):
     """sizeof and offsetof of a header struct, from a C program compiled by gcc."""
     import shutil
