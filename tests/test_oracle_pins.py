@@ -259,10 +259,10 @@ def test_quantize_pages_units_independent_and_ckey(codec):
 
 
 def test_dequant_independent_of_oracle_helpers():
-    """Dequantise FP8 / INT8 / INT4 with torch (library view of the codes)."""
+    """Dequantise FP8 / INT8 / INT4 / INT2 with torch (library view of the codes)."""
     hkv, P, D = 1, 16, 64
     src = _src_pool(1, hkv, P, D, C.CODEC_FP16, 12)
-    for codec in (C.CODEC_FP8_E4M3, C.CODEC_INT8, C.CODEC_INT4_G32):
+    for codec in (C.CODEC_FP8_E4M3, C.CODEC_INT8, C.CODEC_INT4_G32, C.CODEC_INT2_G32):
         codes, meta = C.alloc_pool(codec, 1, hkv, P, D)
         C.quantize_pages(src, C.CODEC_FP16, [0], codec, codes, meta, [0])
         got = C.dequant_page(codec, codes, meta, 0, 1, 0)
@@ -272,13 +272,17 @@ def test_dequant_independent_of_oracle_helpers():
         elif codec == C.CODEC_INT8:
             ref = tc.view(torch.int8).double() * float(meta[0, 1, 0])
         else:
-            lo, hi = (tc & 0xF).double(), (tc >> 4).double()
-            q = torch.stack([lo, hi], dim=-1).reshape(P, D)
+            if codec == C.CODEC_INT4_G32:
+                q = torch.stack([(tc & 0xF).double(), (tc >> 4).double()], dim=-1).reshape(P, D)
+            else:   # four 2-bit codes per byte, lowest bits first
+                q = torch.stack([((tc >> (2 * j)) & 3).double() for j in range(4)], dim=-1).reshape(P, D)
             sz = torch.from_numpy(meta[0, 1, 0].astype(np.float64))   # [P][D/32][2]
             ref = (q.reshape(P, D // 32, 32) * sz[..., :1] + sz[..., 1:]).reshape(P, D)
         assert np.array_equal(got, ref.numpy())
         x = C.f16_bits_to_f64(src[0, 1, 0])
-        assert np.max(np.abs(got - x)) <= 0.1 * np.max(np.abs(x))
+        # INT2 keeps 4 levels per group: a coarser (but bounded) reconstruction
+        frac = 0.4 if codec == C.CODEC_INT2_G32 else 0.1
+        assert np.max(np.abs(got - x)) <= frac * np.max(np.abs(x))
 
 
 # ---------------------------------------------------------------- attention
@@ -364,12 +368,13 @@ def test_mixed_codec_decode_equals_torch_dense_on_dequantised_pages():
     Hkv, G, D, P = 2, 4, 64, 16
     lens = [80]
     q = C.f16_bits_to_f64(W.to_bits(W.normal((1, Hkv * G, D), C.CODEC_FP16, 31)))
-    src = W.to_bits(W.normal((5, 2, Hkv, P, D), C.CODEC_FP16, 32))
-    pools, page_codec = {}, np.array([[4, 3, 2, 0, 2]])
-    table = np.array([[0, 0, 1, 0, 0]], np.int32)
-    for codec in (0, 2, 3, 4):
+    src = W.to_bits(W.normal((6, 2, Hkv, P, D), C.CODEC_FP16, 32))
+    pools, page_codec = {}, np.array([[5, 4, 3, 2, 0, 2]])
+    table = np.array([[0, 0, 0, 1, 0, 0]], np.int32)
+    lens = [96]
+    for codec in (0, 2, 3, 4, 5):
         pools[codec] = C.alloc_pool(codec, 2, Hkv, P, D)
-    for p in range(5):
+    for p in range(6):
         c = int(page_codec[0, p])
         C.quantize_pages(src, C.CODEC_FP16, [p], c, pools[c][0], pools[c][1], [int(table[0, p])])
     o, _, bad = A.paged_decode(q, Hkv, P, pools, page_codec, table, np.array(lens), 0.125)
@@ -377,7 +382,7 @@ def test_mixed_codec_decode_equals_torch_dense_on_dequantised_pages():
     # independent dequantisation with torch views of the stored codes
     for h in range(Hkv):
         Ks, Vs = [], []
-        for p in range(5):
+        for p in range(6):
             c, slot = int(page_codec[0, p]), int(table[0, p])
             codes, meta = pools[c]
             for kv, acc in ((0, Ks), (1, Vs)):
@@ -389,7 +394,10 @@ def test_mixed_codec_decode_equals_torch_dense_on_dequantised_pages():
                 elif c == 3:
                     acc.append(t.view(torch.int8).double() * float(meta[slot, kv, h]))
                 else:
-                    qn = torch.stack([(t & 0xF).double(), (t >> 4).double()], -1).reshape(P, D)
+                    if c == 4:
+                        qn = torch.stack([(t & 0xF).double(), (t >> 4).double()], -1).reshape(P, D)
+                    else:
+                        qn = torch.stack([((t >> (2 * j)) & 3).double() for j in range(4)], -1).reshape(P, D)
                     sz = torch.from_numpy(meta[slot, kv, h].astype(np.float64))
                     acc.append((qn.reshape(P, D // 32, 32) * sz[..., :1] + sz[..., 1:]).reshape(P, D))
         K, V = torch.cat(Ks).numpy(), torch.cat(Vs).numpy()
