@@ -10,7 +10,10 @@ It follows three web pages:
 * "ARGUS: Heterogeneous KV-cache memory management" (argus-cache 0.5.1 on PyPI),
   sections "Why decode is slow" and "Direct paged attention": codec tiers,
   an exact online softmax over one page at a time with grouped-query
-  attention, a structure-of-arrays page table.
+  attention, a structure-of-arrays page table; "Pluggable tiers" (the INT2
+  tier as unsigned_affine with bits = 2) and "v0.5: model-independent KV
+  placement" with the "HuggingFace example" (sliding-window masks, sink
+  tokens).
 * "feat(kvcache): host-RAM KV tier for sparse-attention models" (FreeToken
   PR #499 and its discussion), sections "Why this works for sparse attention",
   "Design", the update that stores "e4m3 codes + fp32 scales", and the
@@ -33,12 +36,12 @@ invariance), closed-form special cases, or numbers printed on the pages.
 """
 
 from .codecs import (  # noqa: F401
-    CODEC_FP16, CODEC_BF16, CODEC_FP8_E4M3, CODEC_INT8, CODEC_INT4_G32,
+    CODEC_FP16, CODEC_BF16, CODEC_FP8_E4M3, CODEC_INT8, CODEC_INT4_G32, CODEC_INT2_G32,
     e4m3_value, e4m3_table, e4m3_encode, f16_bits_to_f64, bf16_bits_to_f64,
     round_to_bf16, f64_to_bf16_bits, quantize_unit_fp8, quantize_unit_int8,
-    quantize_group_int4, quantize_pages, dequant_page,
+    quantize_group_int4, quantize_group_int2, quantize_pages, dequant_page,
 )
 from .attention import (  # noqa: F401
-    softmax_attention, paged_decode, fold_lse, window_attention,
+    softmax_attention, paged_decode, fold_lse, window_attention, visible_positions,
 )
 from .selection import compressed_key_scores, select_pages  # noqa: F401
