@@ -193,6 +193,54 @@ def window_attention(q_f64, k_f64, v_f64, win_pos0, q_pos0, scale, rows=None):
     return o, lse2
 
 
+def gather_window(Hkv, P, pools, page_codec, block_table, b, win_pos0, win_len):
+    """K and V of one window of a paged, mixed-codec cache.
+
+    The comment on "--kv-placement host" in "feat(kvcache): host-RAM KV tier
+    for sparse-attention models" stages a prefill's cached pages into a
+    device window before attending to it.  Here the window holds logical
+    positions win_pos0 .. win_pos0 + win_len - 1 of sequence b: position p
+    lies in logical page p // P at row p % P, whose codec and physical slot
+    come from page_codec / block_table, and is dequantised exactly (float64).
+    Returns (K, V) float64 [Hkv][win_len][D]; win_len >= 1.
+    """
+    assert win_len >= 1
+    Ks, Vs = [], []
+    cache = {}
+    for p in range(win_pos0, win_pos0 + win_len):
+        page = p // P
+        if page not in cache:
+            codec = int(page_codec[b, page])
+            slot = int(block_table[b, page])
+            codes, meta = pools[codec]
+            cache[page] = [(dequant_page(codec, codes, meta, slot, 0, h),
+                            dequant_page(codec, codes, meta, slot, 1, h)) for h in range(Hkv)]
+        kv = cache[page]
+        Ks.append(np.stack([kv[h][0][p % P] for h in range(Hkv)]))
+        Vs.append(np.stack([kv[h][1][p % P] for h in range(Hkv)]))
+    return np.stack(Ks, axis=1), np.stack(Vs, axis=1)
+
+
+def paged_window_attention(q_f64, Hkv, P, pools, page_codec, block_table, b, win_pos0, win_len,
+                           q_pos0, scale, rows=None):
+    """window_attention over a window gathered from the paged cache
+    (gather_window): the staged-prefill step, with pages in any codec tier."""
+    if win_len == 0:
+        K = V = np.zeros((Hkv, 0, q_f64.shape[-1]))
+    else:
+        K, V = gather_window(Hkv, P, pools, page_codec, block_table, b, win_pos0, win_len)
+    return window_attention(q_f64, K, V, win_pos0, q_pos0, scale, rows)
+
+
+def staging_moves_less(row_read_bytes, cache_bytes):
+    """The host-placement comment's staging_moves_less: a prefill stages the
+    cache into device windows when its rows, each reading its own pages in
+    place, would together read more than the whole cache.  row_read_bytes:
+    bytes each query row would read in place (an iterable); True means stage.
+    """
+    return sum(int(x) for x in row_read_bytes) > int(cache_bytes)
+
+
 def to_f64(bits, dtype):
     """16-bit bit patterns (numpy uint16) -> float64 values."""
     return bits_to_f64(bits, dtype)

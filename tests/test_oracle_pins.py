@@ -545,6 +545,106 @@ def test_window_causality_brute_force_and_fold_of_windows():
     assert np.allclose(acc_o, full_o, atol=1e-12) and np.allclose(acc_l, full_l, atol=1e-12)
 
 
+# ---------------------------------------------------------------- paged windows (staged prefill)
+
+def _torch_dequant(codec, codes, meta, slot, kv, h, P, D):
+    """Dequantise one unit with torch views of the stored codes (independent of the oracle)."""
+    t = torch.from_numpy(codes[slot, kv, h].copy())
+    if codec == C.CODEC_FP16:
+        return t.view(torch.float16).double()
+    if codec == C.CODEC_FP8_E4M3:
+        return t.view(torch.float8_e4m3fn).double() * float(meta[slot, kv, h])
+    if codec == C.CODEC_INT8:
+        return t.view(torch.int8).double() * float(meta[slot, kv, h])
+    if codec == C.CODEC_INT4_G32:
+        q = torch.stack([(t & 0xF).double(), (t >> 4).double()], -1).reshape(P, D)
+    else:
+        q = torch.stack([((t >> (2 * j)) & 3).double() for j in range(4)], -1).reshape(P, D)
+    sz = torch.from_numpy(meta[slot, kv, h].astype(np.float64))
+    return (q.reshape(P, D // 32, 32) * sz[..., :1] + sz[..., 1:]).reshape(P, D)
+
+
+def _mixed_paged_cache(Hkv, D, P, n_pages, seed, codecs=(5, 4, 3, 2, 0)):
+    src = W.to_bits(W.normal((n_pages, 2, Hkv, P, D), C.CODEC_FP16, seed))
+    page_codec = np.array([[codecs[p % len(codecs)] for p in range(n_pages)]])
+    perm = W.permutation(n_pages, seed + 1)
+    table = np.zeros((1, n_pages), np.int32)
+    pools = {c: C.alloc_pool(c, n_pages, Hkv, P, D) for c in set(codecs)}
+    for p in range(n_pages):
+        c = int(page_codec[0, p])
+        table[0, p] = perm[p]
+        C.quantize_pages(src, C.CODEC_FP16, [p], c, pools[c][0], pools[c][1], [int(perm[p])])
+    return pools, page_codec, table
+
+
+def test_gather_window_is_a_plain_gather_and_table_invariant():
+    Hkv, D, P, n = 2, 32, 16, 6
+    pools, pc, table = _mixed_paged_cache(Hkv, D, P, n, 70, codecs=(0,))
+    codes = pools[0][0]
+    K, V = A.gather_window(Hkv, P, pools, pc, table, 0, 13, 50)
+    for j, p in enumerate(range(13, 63)):
+        for h in range(Hkv):
+            row = torch.from_numpy(codes[table[0, p // P], :, h, p % P].copy()).view(torch.float16).double()
+            assert np.array_equal(K[h, j], row[0].numpy()) and np.array_equal(V[h, j], row[1].numpy())
+    # the same pages under another slot permutation give the same window
+    perm = W.permutation(codes.shape[0], 71)
+    codes2 = np.empty_like(codes)
+    codes2[perm] = codes
+    K2, V2 = A.gather_window(Hkv, P, {0: (codes2, None)}, pc, perm[table].astype(np.int32), 0, 13, 50)
+    assert np.array_equal(K, K2) and np.array_equal(V, V2)
+
+
+def test_paged_window_attention_over_five_tiers_equals_torch_causal():
+    Hkv, G, D, P, n = 2, 3, 64, 16, 10
+    pools, pc, table = _mixed_paged_cache(Hkv, D, P, n, 72)
+    nq, q_pos0, w0, wl = 5, 150, 21, 134            # window 21..154, crossing pages mid-page
+    q = C.f16_bits_to_f64(W.to_bits(W.normal((Hkv * G, nq, D), C.CODEC_FP16, 73)))
+    o, lse2 = A.paged_window_attention(q, Hkv, P, pools, pc, table, 0, w0, wl, q_pos0, 0.125)
+    for h in range(Hkv):
+        rows = []
+        for p in range(w0, w0 + wl):
+            c, slot = int(pc[0, p // P]), int(table[0, p // P])
+            rows.append((_torch_dequant(c, *pools[c], slot, 0, h, P, D)[p % P],
+                         _torch_dequant(c, *pools[c], slot, 1, h, P, D)[p % P]))
+        K = torch.stack([r[0] for r in rows]).numpy()
+        V = torch.stack([r[1] for r in rows]).numpy()
+        for g in range(G):
+            for i in range(nq):
+                n_vis = q_pos0 + i - w0 + 1            # keys at positions <= q_pos0 + i
+                ro, rl = _torch_attention(q[h * G + g, i], K[:n_vis], V[:n_vis], 0.125)
+                assert np.allclose(o[h * G + g, i], ro, atol=1e-12, rtol=0)
+                assert abs(lse2[h * G + g, i] - rl) < 1e-12
+
+
+def test_fold_of_paged_windows_equals_one_window():
+    Hkv, G, D, P, n = 2, 2, 32, 16, 8
+    pools, pc, table = _mixed_paged_cache(Hkv, D, P, n, 74)
+    nq, q_pos0 = 4, 124
+    q = C.f16_bits_to_f64(W.to_bits(W.normal((Hkv * G, nq, D), C.CODEC_FP16, 75)))
+    full_o, full_l = A.paged_window_attention(q, Hkv, P, pools, pc, table, 0, 0, 128, q_pos0, 0.2)
+    acc_o = np.zeros_like(full_o)
+    acc_l = np.full_like(full_l, -math.inf)
+    for w0, w1 in ((0, 37), (37, 37), (37, 100), (100, 128)):
+        po, pl = A.paged_window_attention(q, Hkv, P, pools, pc, table, 0, w0, w1 - w0, q_pos0, 0.2)
+        acc_o, acc_l = A.fold_lse(acc_o, acc_l, po, pl)
+    assert np.allclose(acc_o, full_o, atol=1e-12) and np.allclose(acc_l, full_l, atol=1e-12)
+
+
+def test_staging_moves_less_with_the_pages_numbers():
+    """Rows reading their selected pages in place (2,051 tokens each, the
+    host-placement comment) against staging a ~985k-token cache once: the
+    decision turns where the rows' reads pass the cache size."""
+    g = json.load(open(GOLDEN))["selection_budget"]
+    per_row = g["tokens_per_query_printed"]
+    cache = 985_000
+    assert A.staging_moves_less([per_row] * 1024, cache)           # 2.1 M tokens read in place
+    assert not A.staging_moves_less([per_row] * 256, cache)        # 0.5 M
+    n_turn = cache // per_row + 1                                   # first row count that reads more
+    assert A.staging_moves_less([per_row] * n_turn, cache)
+    assert not A.staging_moves_less([per_row] * (n_turn - 1), cache)
+    assert not A.staging_moves_less([cache // 2, cache - cache // 2], cache)   # equal: in place
+
+
 # ---------------------------------------------------------------- selection
 
 def test_scores_equal_torch_einsum():
