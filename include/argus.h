@@ -309,6 +309,23 @@ argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n_q,
                                        int32_t num_splits, void* ws, size_t ws_bytes,
                                        void* stream);
 
+/* ---------------------------------------------------------------------------
+ * argus_staging_moves_less -- whether a prefill should stage the cache into
+ * device windows (argus_window_prefill_attn) rather than read pages in place.
+ *
+ * [PR499] comment on "--kv-placement host": a prefill whose rows would
+ * together read more than the whole cache stages the cached pages into a
+ * device window, attends per window and folds the windows.  *stage = 1 when
+ * the sum of row_read_bytes[0 .. n_rows) is strictly greater than
+ * cache_bytes, else 0.
+ * Arguments (all HOST memory, no device work): row_read_bytes int64 [n_rows],
+ * the bytes each query row would read in place (>= 0); n_rows >= 0;
+ * cache_bytes >= 0; stage int32 out.  A NULL pointer (row_read_bytes may be
+ * NULL when n_rows = 0) or a negative value is ARGUS_E_INVALID.
+ * ------------------------------------------------------------------------- */
+argus_status argus_staging_moves_less(const int64_t* row_read_bytes, int64_t n_rows,
+                                      int64_t cache_bytes, int32_t* stage);
+
 const char* argus_status_string(argus_status s);
 
 /* One-line reason for the calling thread's most recent non-OK status. */

@@ -55,8 +55,8 @@ class DecodeArgs(ctypes.Structure):
 EXPORTS = ["argus_quantize_pages", "argus_decode_workspace_bytes", "argus_paged_decode_attn",
            "argus_paged_decode_attn_noalloc",
            "argus_select_workspace_bytes", "argus_select_pages", "argus_fold_lse",
-           "argus_window_prefill_workspace_bytes", "argus_window_prefill_attn", "argus_status_string",
-           "argus_last_error"]
+           "argus_window_prefill_workspace_bytes", "argus_window_prefill_attn", "argus_staging_moves_less",
+           "argus_status_string", "argus_last_error"]
 
 
 def lib_path():
@@ -98,6 +98,8 @@ def lib():
                                             ctypes.c_float, vp, vp, i32, i32, vp, sz, vp]
     L.argus_window_prefill_workspace_bytes.restype = ctypes.c_int
     L.argus_window_prefill_workspace_bytes.argtypes = [ctypes.POINTER(Geom), i32, i64, i32, ctypes.POINTER(sz)]
+    L.argus_staging_moves_less.restype = ctypes.c_int
+    L.argus_staging_moves_less.argtypes = [ctypes.POINTER(ctypes.c_int64), i64, i64, ctypes.POINTER(i32)]
     _lib = L
     return L
 
@@ -247,6 +249,15 @@ def window_prefill_workspace_bytes(g, n_q, win_len, num_splits=0):
     _check(lib().argus_window_prefill_workspace_bytes(ctypes.byref(g), int(n_q), int(win_len), int(num_splits),
                                                       ctypes.byref(n)))
     return n.value
+
+
+def staging_moves_less(row_read_bytes, cache_bytes):
+    """Whether a prefill should stage the cache into device windows: the rows'
+    in-place reads (host list of byte counts) together exceed cache_bytes."""
+    rows = (ctypes.c_int64 * max(1, len(row_read_bytes)))(*[int(x) for x in row_read_bytes])
+    out = ctypes.c_int32(0)
+    _check(lib().argus_staging_moves_less(rows, len(row_read_bytes), int(cache_bytes), ctypes.byref(out)))
+    return bool(out.value)
 
 
 def window_prefill_attn(g, n_q, q, k, v, kv_head_stride, win_len, win_pos0, q_pos0, softmax_scale,

@@ -46,3 +46,27 @@ extern "C" const char* argus_status_string(argus_status s) {
 }
 
 extern "C" const char* argus_last_error(void) { return argus::g_last_error; }
+
+// Host-only decision of the staged prefill: stage when the rows' in-place
+// reads together exceed the cache ("--kv-placement host" comment of the
+// host-RAM KV tier pull request).  Each row is compared with the headroom
+// left under cache_bytes, so no sum can overflow.
+extern "C" argus_status argus_staging_moves_less(const int64_t* row_read_bytes, int64_t n_rows,
+                                                 int64_t cache_bytes, int32_t* stage) {
+  using argus::fail;
+  if (!stage) return fail(ARGUS_E_INVALID, "staging: stage is NULL");
+  if (n_rows < 0 || cache_bytes < 0) return fail(ARGUS_E_INVALID, "staging: negative n_rows or cache_bytes");
+  if (n_rows > 0 && !row_read_bytes) return fail(ARGUS_E_INVALID, "staging: row_read_bytes is NULL");
+  int64_t sum = 0;
+  int32_t more = 0;
+  for (int64_t i = 0; i < n_rows; ++i) {
+    const int64_t b = row_read_bytes[i];
+    if (b < 0) return fail(ARGUS_E_INVALID, "staging: row %lld reads a negative byte count", (long long)i);
+    if (!more) {
+      if (b > cache_bytes - sum) more = 1;   // sum <= cache_bytes: the difference is >= 0
+      else sum += b;
+    }
+  }
+  *stage = more;
+  return ARGUS_OK;
+}

@@ -138,3 +138,26 @@ def test_binding_structs_match_the_header_layout(cls, struct, tmp_path):
     assert ctypes.sizeof(cls) == size
     for name, off in zip(names, offs):
         assert getattr(cls, name).offset == off, name
+
+
+def test_staging_decision_matches_the_oracle_without_gpu():
+    """argus_staging_moves_less is host logic: it runs here, against the oracle's
+    reading of the staging rule, including sums far beyond int64 headroom."""
+    from oracle import attention as A
+    import numpy as np
+    _lib()
+    rng = np.random.default_rng(5)
+    for _ in range(300):
+        n = int(rng.integers(0, 40))
+        rows = rng.integers(0, 5000, size=n).tolist()
+        cache = int(rng.integers(0, 100000))
+        assert argus.staging_moves_less(rows, cache) == A.staging_moves_less(rows, cache)
+    big = 2 ** 62
+    assert argus.staging_moves_less([big, big, big], 2 ** 63 - 1)      # no overflow in the sum
+    assert not argus.staging_moves_less([big - 1, big], 2 ** 63 - 1)
+    assert not argus.staging_moves_less([], 0)
+    with pytest.raises(argus.ArgusError) as e:
+        argus.staging_moves_less([3, -1], 10)
+    assert e.value.status == 1
+    with pytest.raises(argus.ArgusError):
+        argus.staging_moves_less([1], -5)
