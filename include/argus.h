@@ -220,6 +220,9 @@ argus_status argus_paged_decode_attn(const argus_decode_args* args, void* ws,
  * cudaMalloc, no cudaFree, no allocating library routine.
  *   - The first call on a device resolves the array's device address (with
  *     that device current); make that first call before any stream capture.
+ *     The address is resolved again by the first call after the device's
+ *     context was destroyed and created anew (cudaDeviceReset), so a stale
+ *     address is never used.
  *   - The array keeps the previous call's contents; nothing in it needs to
  *     start at zero (every partial result is written before it is read).
  *   - All calls share the one array: calls that overlap on the GPU (different
@@ -313,9 +316,10 @@ argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n_q,
  * argus_staging_moves_less -- whether a prefill should stage the cache into
  * device windows (argus_window_prefill_attn) rather than read pages in place.
  *
- * [PR499] comment on "--kv-placement host": a prefill whose rows would
- * together read more than the whole cache stages the cached pages into a
- * device window, attends per window and folds the windows.  *stage = 1 when
+ * [PR499] comment on "--kv-placement host": when the in-place reads of a
+ * prefill's rows add up to more bytes than the cache holds, the cached pages
+ * are staged into a device window, attended per window, and the windows
+ * folded.  *stage = 1 when
  * the sum of row_read_bytes[0 .. n_rows) is strictly greater than
  * cache_bytes, else 0.
  * Arguments (all HOST memory, no device work): row_read_bytes int64 [n_rows],

@@ -254,9 +254,15 @@ def window_prefill_workspace_bytes(g, n_q, win_len, num_splits=0):
 def staging_moves_less(row_read_bytes, cache_bytes):
     """Whether a prefill should stage the cache into device windows: the rows'
     in-place reads (host list of byte counts) together exceed cache_bytes."""
-    rows = (ctypes.c_int64 * max(1, len(row_read_bytes)))(*[int(x) for x in row_read_bytes])
+    vals = [int(x) for x in row_read_bytes] + [int(cache_bytes)]
+    for x in vals:
+        # ctypes wraps integers silently; a byte count outside int64 must not
+        # turn into a small valid one
+        if not (-2 ** 63 <= x < 2 ** 63):
+            raise ValueError("staging_moves_less: byte count %d does not fit in int64" % x)
+    rows = (ctypes.c_int64 * max(1, len(row_read_bytes)))(*vals[:-1])
     out = ctypes.c_int32(0)
-    _check(lib().argus_staging_moves_less(rows, len(row_read_bytes), int(cache_bytes), ctypes.byref(out)))
+    _check(lib().argus_staging_moves_less(rows, len(row_read_bytes), vals[-1], ctypes.byref(out)))
     return bool(out.value)
 
 

@@ -3,6 +3,8 @@
 #include <cstdio>
 #include <cstring>
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace argus {
@@ -30,6 +32,34 @@ int device_sm_count() {
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
   return n > 0 ? n : 1;
+}
+
+// The driver's cuCtxGetCurrent / cuCtxGetId, reached through the runtime's
+// entry-point query so that the library links against the runtime only.
+unsigned long long context_id() {
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 4000, cudaEnableDefault, &qa) == cudaSuccess &&
+        qa == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) == cudaSuccess &&
+        qb == cudaDriverEntryPointSuccess) {
+      get_current = reinterpret_cast<GetCurrentFn>(a);
+      get_id = reinterpret_cast<GetIdFn>(b);
+    }
+  });
+  if (!get_current || !get_id) return 0ull;
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0ull;
+  if (get_id(c, &id) != CUDA_SUCCESS) return 0ull;
+  return id;
 }
 
 }  // namespace argus

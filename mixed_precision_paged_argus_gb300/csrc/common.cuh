@@ -9,6 +9,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/argus.h"
 
 namespace argus {
@@ -19,6 +21,35 @@ namespace argus {
 argus_status fail(argus_status s, const char* fmt, ...);
 argus_status launch_status(const char* what);
 int device_sm_count();
+
+// Identifier of the calling thread's current CUDA context, unique for the life
+// of the process; 0 when no context is current or the driver cannot say.
+unsigned long long context_id();
+
+// One-time setup per device that must be redone in a new context: kernel
+// attributes, resolved symbol addresses.  A device's context changes when it is
+// destroyed and created again (cudaDeviceReset), and whatever was set up in the
+// old one no longer holds, so the record is keyed on the context identifier.
+struct PerContext {
+  unsigned long long ctx[64] = {};
+  std::mutex mu;
+
+  // Runs setup(dev) unless it already succeeded in the current context of the
+  // current device; returns its status.  Without a context identifier the
+  // setup runs on every call.
+  template <class F>
+  argus_status ensure(F&& setup) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+      return fail(ARGUS_E_LAUNCH, "no current CUDA device");
+    std::lock_guard<std::mutex> lock(mu);
+    const unsigned long long id = context_id();
+    if (id != 0 && ctx[dev] == id) return ARGUS_OK;
+    const argus_status st = setup(dev);
+    ctx[dev] = (st == ARGUS_OK) ? context_id() : 0ull;   // setup may have created the context
+    return st;
+  }
+};
 
 // Upper bound on any wait (nanoseconds of %globaltimer); a wait that runs out
 // sets the top bit of the caller-visible status word and the kernel winds down.

@@ -30,7 +30,6 @@
 //    fully parallel kernel chained with programmatic dependent launch.
 #include <algorithm>
 #include <cmath>
-#include <mutex>
 
 #include "common.cuh"
 
@@ -1304,15 +1303,14 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
 template <int D, bool QBF16, int FAM, bool NARROW, bool EXT>
 static argus_status launch_t(const Params& p, dim3 grid, cudaStream_t s) {
   using L = Layout<D, NARROW>;
-  static bool configured[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(ARGUS_E_LAUNCH, "decode: no device");
-  if (!configured[dev]) {
+  static PerContext configured;
+  argus_status st = configured.ensure([](int) {
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, QBF16, FAM, NARROW, EXT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "decode: smem attribute: %s", cudaGetErrorString(e));
-    configured[dev] = true;
-  }
+    return ARGUS_OK;
+  });
+  if (st != ARGUS_OK) return st;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(Warps<D, NARROW>::kThreads);
@@ -1457,22 +1455,26 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[ARGUS_NOALLOC_SCRATCH
 namespace argus {
 namespace decode {
 
-// Device address of g_noalloc_scratch, resolved once per device with that
-// device current (the host-side name is only a stand-in for the symbol).
+// Device address of g_noalloc_scratch, resolved with the device current once
+// per device and context (the host-side name is only a stand-in for the
+// symbol; a context created again after cudaDeviceReset gets a new address).
 static argus_status noalloc_scratch(void** out) {
   static void* addr[64] = {};
-  static std::mutex mu;
+  static PerContext resolved;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
     return fail(ARGUS_E_LAUNCH, "decode (no-alloc): no current device");
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  argus_status st = resolved.ensure([](int d) {
     void* ptr = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (e != cudaSuccess || !ptr)
+    if (e != cudaSuccess || !ptr) {
+      addr[d] = nullptr;
       return fail(ARGUS_E_LAUNCH, "decode (no-alloc): cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
-    addr[dev] = ptr;
-  }
+    }
+    addr[d] = ptr;
+    return ARGUS_OK;
+  });
+  if (st != ARGUS_OK) return st;
   *out = addr[dev];
   return ARGUS_OK;
 }

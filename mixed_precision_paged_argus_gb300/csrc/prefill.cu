@@ -2,8 +2,8 @@
 // cached keys, folded into an fp32 accumulator by log2-sum-exp.
 //
 // "feat(kvcache): host-RAM KV tier for sparse-attention models", comment on
-// "--kv-placement host": when a prefill's rows would together read more than
-// the cache, the cached pages are staged into a 131,072-token device window,
+// "--kv-placement host": when the in-place reads of a prefill's rows add up to
+// more bytes than the cache holds, the cached pages are staged into a 131,072-token device window,
 // attended per window, and the windows folded by their log2-sum-exp into a
 // float32 accumulator allocated up front (fold_attention_pass).
 //
@@ -807,16 +807,15 @@ extern "C" argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n
   } else if (!make_map(&mv, win_len > 0 ? v : q, 3, kd, ks)) {
     return fail(ARGUS_E_LAUNCH, "prefill: tensor map for v failed");
   }
-  static bool configured[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(ARGUS_E_LAUNCH, "prefill: no device");
-  if (!configured[dev]) {
+  static PerContext configured;
+  argus_status sta = configured.ensure([](int) {
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "prefill: smem attribute: %s", cudaGetErrorString(e));
-    configured[dev] = true;
-  }
+    return ARGUS_OK;
+  });
+  if (sta != ARGUS_OK) return sta;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (f16p) {
     // the window's V in fp16, scaled by 2^-e from its max |v|

@@ -486,15 +486,14 @@ extern "C" argus_status argus_select_pages(const argus_geom* g, int32_t batch, c
   const int stage = max_pages <= select::kTopkSmemKeys ? 1 : 0;
   const size_t tsh = stage ? (size_t)max_pages * sizeof(uint32_t) : 0;
   if (tsh > 48 * 1024) {
-    static bool configured[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(ARGUS_E_LAUNCH, "select: no device");
-    if (!configured[dev]) {
+    static PerContext configured;
+    argus_status sta = configured.ensure([](int) {
       cudaError_t e = cudaFuncSetAttribute(select::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            select::kTopkSmemKeys * (int)sizeof(uint32_t));
       if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "select: smem attribute: %s", cudaGetErrorString(e));
-      configured[dev] = true;
-    }
+      return ARGUS_OK;
+    });
+    if (sta != ARGUS_OK) return sta;
   }
   dim3 grid2(g->n_kv_heads, batch);
   select::topk_kernel<<<grid2, select::kTopkThreads, tsh, s>>>(g->n_kv_heads, max_pages, keys, n_pages, top_k,

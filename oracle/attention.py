@@ -193,7 +193,7 @@ def window_attention(q_f64, k_f64, v_f64, win_pos0, q_pos0, scale, rows=None):
     return o, lse2
 
 
-def gather_window(Hkv, P, pools, page_codec, block_table, b, win_pos0, win_len):
+def gather_window(Hkv, P, pools, page_codec, block_table, b, win_pos0, win_len, seq_len=None):
     """K and V of one window of a paged, mixed-codec cache.
 
     The comment on "--kv-placement host" in "feat(kvcache): host-RAM KV tier
@@ -202,9 +202,12 @@ def gather_window(Hkv, P, pools, page_codec, block_table, b, win_pos0, win_len):
     positions win_pos0 .. win_pos0 + win_len - 1 of sequence b: position p
     lies in logical page p // P at row p % P, whose codec and physical slot
     come from page_codec / block_table, and is dequantised exactly (float64).
-    Returns (K, V) float64 [Hkv][win_len][D]; win_len >= 1.
+    The window must lie inside the table's pages and, when seq_len is given,
+    end at or before it.  Returns (K, V) float64 [Hkv][win_len][D]; win_len >= 1.
     """
     assert win_len >= 1
+    assert 0 <= win_pos0 and win_pos0 + win_len <= block_table.shape[1] * P, "window outside the block table"
+    assert seq_len is None or win_pos0 + win_len <= seq_len, "window runs past the sequence"
     Ks, Vs = [], []
     cache = {}
     for p in range(win_pos0, win_pos0 + win_len):
@@ -222,20 +225,20 @@ def gather_window(Hkv, P, pools, page_codec, block_table, b, win_pos0, win_len):
 
 
 def paged_window_attention(q_f64, Hkv, P, pools, page_codec, block_table, b, win_pos0, win_len,
-                           q_pos0, scale, rows=None):
+                           q_pos0, scale, rows=None, seq_len=None):
     """window_attention over a window gathered from the paged cache
     (gather_window): the staged-prefill step, with pages in any codec tier."""
     if win_len == 0:
         K = V = np.zeros((Hkv, 0, q_f64.shape[-1]))
     else:
-        K, V = gather_window(Hkv, P, pools, page_codec, block_table, b, win_pos0, win_len)
+        K, V = gather_window(Hkv, P, pools, page_codec, block_table, b, win_pos0, win_len, seq_len)
     return window_attention(q_f64, K, V, win_pos0, q_pos0, scale, rows)
 
 
 def staging_moves_less(row_read_bytes, cache_bytes):
     """The host-placement comment's staging_moves_less: a prefill stages the
-    cache into device windows when its rows, each reading its own pages in
-    place, would together read more than the whole cache.  row_read_bytes:
+    cache into device windows when the in-place reads of its rows (each row
+    reading its own pages) add up to more bytes than the cache holds.  row_read_bytes:
     bytes each query row would read in place (an iterable); True means stage.
     """
     return sum(int(x) for x in row_read_bytes) > int(cache_bytes)

@@ -1,6 +1,6 @@
 """Small, self-contained cases of each kernel, sized for Nsight Compute.
 
-  python -m mixed_precision_paged_argus_gb300.profile_cases <case> [--reps N]
+  python profile_cases.py <case> [--reps N]
 
 Every case builds its inputs with the seeded generators, runs the library
 call `reps` times and synchronises.  Cases keep a few GB at most on the device
@@ -20,13 +20,18 @@ and use inputs larger than L2 where the kernel streams HBM.
 """
 
 import argparse
+import os
 import sys
 
 import numpy as np
 import torch
 
-from . import argus
-from . import workloads as W
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import mixed_precision_paged_argus_gb300.argus as argus  # noqa: E402
+from mixed_precision_paged_argus_gb300 import workloads as W  # noqa: E402
 
 
 def _decode_mixed(dev):

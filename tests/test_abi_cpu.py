@@ -161,3 +161,8 @@ def test_staging_decision_matches_the_oracle_without_gpu():
     assert e.value.status == 1
     with pytest.raises(argus.ArgusError):
         argus.staging_moves_less([1], -5)
+    # counts outside int64 are refused by the binding before ctypes could wrap them
+    with pytest.raises(ValueError):
+        argus.staging_moves_less([2 ** 64 + 3], 10)
+    with pytest.raises(ValueError):
+        argus.staging_moves_less([1], 2 ** 63)
