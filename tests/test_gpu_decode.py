@@ -1,8 +1,8 @@
 """argus_paged_decode_attn on the GPU against the double-precision oracle.
 
 Tolerance (stated for attention outputs): max|err| <= 1e-3 * max|ref| + 1e-4 on
-the fp32 output; the fp16 output is compared the same way; the bf16 output
-must equal the round-to-nearest-even of the kernel's own fp32 output.
+the fp32 output; the fp16 or bf16 output must equal the round-to-nearest-even
+of the kernel's own fp32 output.
 """
 
 import math
@@ -29,11 +29,8 @@ def _check(c, out, out32, lse, sel=None, cnt=None, width=0, expect_bad=0, window
     t = tol(ref)
     err = np.abs(got - ref).max()
     assert err <= t, "fp32 output max err %.3g > tol %.3g" % (err, t)
-    if out.dtype == torch.float16:
-        e16 = np.abs(out.float().cpu().numpy() - ref).max()
-        assert e16 <= t + np.abs(ref).max() * 2.0 ** -11, "fp16 output max err %.3g" % e16
-    else:
-        assert torch.equal(out.cpu(), out32.cpu().to(torch.bfloat16))
+    # the 16-bit output is the round-to-nearest-even of the kernel's own fp32 output
+    assert torch.equal(out.cpu(), out32.cpu().to(out.dtype))
     gl = lse.cpu().numpy().astype(np.float64)
     fin = np.isfinite(ref_lse)
     assert np.array_equal(np.isfinite(gl), fin)

@@ -160,3 +160,46 @@ def test_split_workspace_too_small_is_rejected():
     with pytest.raises(argus.ArgusError) as e:
         argus.window_prefill_attn(g, 256, t, t, t, 0, 256, 0, 0, 0.1, o, l, 0, num_splits=2, ws=small)
     assert e.value.status == 3
+
+
+@pytest.mark.parametrize("splits,use_ws", MODES)
+@pytest.mark.parametrize("ramp", ["rising", "late_key"])
+def test_scores_growing_past_the_lazy_rescale_threshold(splits, use_ws, ramp):
+    """Key blocks whose scores rise by more than 2^8 (8 in log2 units) over the
+    running maximum, block after block: the softmax must rescale the TMEM
+    accumulator of O (the lazy max moves).  "rising" scales the keys of block j
+    by 1 + 1.5 j, so each softmax group (even / odd blocks) sees a jump of about
+    10 at every block; "late_key" plants one key per KV head in the last cache
+    block aligned with the first query rows, far above everything before it.
+    The host checks on the oracle's own scores that such jumps occur."""
+    Hq, Hkv, n_q, ctx = 2, 1, 128, 1024
+    q, k, v, q64, k64, v64 = _data(Hq, Hkv, n_q, ctx, 521)
+    kf = k.float()
+    if ramp == "rising":
+        for j in range(ctx // 128):
+            kf[:, j * 128:(j + 1) * 128] *= 1.0 + 1.5 * j
+    else:
+        kf[:, 7 * 128 + 5] = q.float()[0, 0] * 12.0
+        kf[:, 6 * 128 + 9] = q.float()[1, 3] * 9.0
+    k = kf.to(torch.bfloat16)
+    k64 = C.bf16_bits_to_f64(W.to_bits(k))
+    scale = W.softmax_scale(128)
+    # the branch is reached: some row's block maximum (log2 units) jumps by > 8
+    # over the maximum of the earlier blocks its softmax group saw
+    s2 = np.einsum("hqd,hkd->hqk", q64.reshape(Hq, n_q, 128), np.repeat(k64[:, :ctx], Hq // Hkv, 0)) * scale / math.log(2)
+    bm = s2.reshape(Hq, n_q, ctx // 128, 128).max(axis=3)           # [Hq][n_q][block]
+    jumps = [np.max(bm[:, :, j] - np.maximum.accumulate(bm[:, :, g::2], axis=2)[:, :, (j - g) // 2 - 1])
+             for g in (0, 1) for j in range(g + 2, ctx // 128, 2)]
+    assert max(jumps) > 8.0
+    g = argus.geom(Hq, Hkv, 128, 16)
+    kd, vd = k.to(DEV), v.to(DEV)
+    kv_len = ctx + n_q
+    acc_o = torch.zeros((Hq, n_q, 128), dtype=torch.float32, device=DEV)
+    acc_l = torch.full((Hq, n_q), float("-inf"), dtype=torch.float32, device=DEV)
+    for wi, (w0, w1) in enumerate([(0, ctx), (ctx, kv_len)]):
+        argus.window_prefill_attn(g, n_q, q.to(DEV), kd[:, w0:], vd[:, w0:], kv_len * 128, w1 - w0, w0, ctx,
+                                  scale, acc_o, acc_l, 1 if wi else 0, num_splits=splits,
+                                  ws=_ws(g, n_q, w1 - w0, splits, use_ws))
+    torch.cuda.synchronize()
+    ro, rl = oracle.window_attention(q64, k64, v64, 0, ctx, scale)
+    _check(acc_o.cpu().numpy(), acc_l.cpu().numpy(), ro, rl)

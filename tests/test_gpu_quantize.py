@@ -214,3 +214,91 @@ def test_int4_groups_with_pinned_range_and_interior_values(ckey, src_dtype, code
     codes, meta = C.alloc_pool(codec, n, Hkv, P, D)
     C.quantize_pages(src, src_dtype, list(range(n)), codec, codes, meta, list(range(n)))
     _compare(pool, codes, meta)
+
+
+@pytest.mark.parametrize("codec", [W.INT4_G32, W.INT2_G32])
+@pytest.mark.parametrize("ckey", [False, True])
+def test_affine_zero_point_and_scale_saturate_at_65504(codec, ckey):
+    """bf16 groups whose min is below -65504 or whose (max - z) / top is above
+    65504: the fp16 zero point and scale saturate (never inf), the all-below
+    group gets a negative scale and zero codes -- bit-exact with the oracle on
+    both encode paths (one lane per group, and the compressed-key path)."""
+    Hkv, P, D, n = 2, 16, 128, 6
+    rng = np.random.default_rng(31 + codec + 2 * ckey)
+    sat = np.zeros((4, 32), np.float32)
+    sat[0] = np.linspace(-2.0 ** 17, 2.0 ** 20, 32)
+    sat[0, 7] = 65504.0 * 2.5
+    sat[1] = np.linspace(0.0, 2.0 ** 20, 32)
+    sat[2] = -2.0 ** 17 + np.arange(32, dtype=np.float32) * 64.0
+    sat[3] = np.linspace(-2.0 ** 16, 2.0 ** 16, 32)
+    groups = n * 2 * Hkv * P * (D // 32)
+    x = rng.standard_normal((groups, 32)) * 1e3
+    pick = rng.integers(0, 4, groups)
+    use = rng.random(groups) < 0.6
+    x[use] = sat[pick[use]] * rng.choice([1.0, 0.5, 2.0], size=(int(use.sum()), 1))
+    rng.shuffle(x, axis=1)
+    bits = C.f64_to_bf16_bits(x).reshape(n, 2, Hkv, P, D)
+    t = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    pool, ck, st = _gpu_quantize(t, W.BF16, codec, Hkv, P, D, list(range(n)), list(range(n)), n, ckey=ckey)
+    assert st == 0
+    codes, meta = C.alloc_pool(codec, n, Hkv, P, D)
+    C.quantize_pages(bits, C.CODEC_BF16, list(range(n)), codec, codes, meta, list(range(n)))
+    m = meta.astype(np.float64)
+    assert np.all(np.isfinite(m)) and np.any(np.abs(m) == 65504.0) and np.any(m[..., 0] < 0)
+    _compare(pool, codes, meta)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("codec", [W.FP8_E4M3, W.INT8, W.INT4_G32, W.INT2_G32])
+@pytest.mark.parametrize("ckey", [False, True])
+def test_full_size_demotion_bit_exact_on_sampled_pages(codec, ckey):
+    """The batched workload's unit shape (16 x 128 bf16) at 20,480 pages x 8 KV
+    heads x K|V = 327,680 units: far more than one unit per warp of the grid, so
+    the software-pipelined hand-off from unit to unit runs many times per warp.
+    Pages with a partial valid-token count are mixed in.  Codes and metadata of
+    sampled pages -- the first, the last, and pages whose units land on a
+    warp's 2nd and later turn -- are compared bit for bit with the oracle run on
+    those pages only; compressed keys within one bf16 ulp + the fp32 sum bound."""
+    n_pages, Hkv, P, D = 20480, 8, 16, 128
+    dev = torch.device(DEV)
+    g = argus.geom(Hkv, Hkv, D, P)
+    src = W.normal((n_pages, 2, Hkv, P, D), W.BF16, 4321 + codec, device=dev, outlier_seed=4322)
+    rng = np.random.default_rng(77 + codec)
+    valid = np.full(n_pages, P, np.int32)
+    part = rng.random(n_pages) < 0.1
+    valid[part] = rng.integers(0, P, int(part.sum()))
+    dst_slots = rng.permutation(n_pages).astype(np.int32)
+    pool = argus.Pool.empty(codec, n_pages, Hkv, P, D, device=dev)
+    ck = torch.empty((n_pages, Hkv, D), dtype=torch.bfloat16, device=dev) if ckey else None
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    argus.quantize_pages(g, W.BF16, src, n_pages, torch.arange(n_pages, dtype=torch.int32, device=dev), pool,
+                         torch.from_numpy(dst_slots).to(dev), n_pages, torch.from_numpy(valid).to(dev), ck, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    # warps of the grid: at most 4 CTAs of 8 warps per SM, one unit per warp per turn
+    n_warps = torch.cuda.get_device_properties(dev).multi_processor_count * 4 * 8
+    units_per_page = 2 * Hkv
+    assert n_pages * units_per_page > 20 * n_warps
+    sample = sorted(set([0, 1, n_pages - 1] + [int(x) for x in rng.integers(0, n_pages, 150)] +
+                        [(n_warps * t) // units_per_page + 3 for t in (1, 2, 7, 19)]))
+    idx = torch.tensor(sample, dtype=torch.int64, device=dev)
+    src_s = W.to_bits(src[idx])
+    dsel = torch.from_numpy(dst_slots[sample].astype(np.int64)).to(dev)
+    got_codes = pool.codes[dsel].contiguous().view(torch.uint8).cpu().numpy()
+    got_meta = pool.meta[dsel].contiguous().view(torch.uint8).cpu().numpy()
+    codes, meta = C.alloc_pool(codec, len(sample), Hkv, P, D)
+    ock = C.quantize_pages(src_s, C.CODEC_BF16, list(range(len(sample))), codec, codes, meta,
+                           list(range(len(sample))), valid_tokens=valid[sample], want_ckey=ckey)
+    assert np.array_equal(got_codes, codes.view(np.uint8).reshape(got_codes.shape))
+    assert np.array_equal(got_meta, meta.view(np.uint8).reshape(got_meta.shape))
+    if ckey:
+        got = C.bf16_bits_to_f64(W.to_bits(ck[idx].cpu()))
+        want = C.bf16_bits_to_f64(ock)
+        mean_abs = np.zeros_like(want)
+        for i in range(len(sample)):
+            if valid[sample[i]]:
+                for h in range(Hkv):
+                    kk = C.dequant_page(codec, codes, meta, i, 0, h)[:valid[sample[i]]]
+                    mean_abs[i, h] = np.abs(kk).mean(axis=0)
+        bound = np.abs(want) * 2.0 ** -7 + (P + 2) * 2.0 ** -24 * mean_abs + 2.0 ** -133
+        assert np.all(np.abs(got - want) <= bound)

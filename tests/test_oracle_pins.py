@@ -218,6 +218,61 @@ def test_int2_codes_against_a_torch_float32_pipeline():
     assert np.array_equal(codes.astype(np.int64), tq.numpy().astype(np.int64))
 
 
+def test_int4_codes_against_a_torch_float32_pipeline():
+    """The INT4 encoder pinned on its own: torch's IEEE float32 ops (no float64
+    emulation) give the same codes, scales and zero points inside fp16's
+    range, including values on exact half-integer quotients."""
+    rng = np.random.default_rng(16)
+    x = (rng.standard_normal((3000, 32)) * rng.uniform(0.01, 300, (3000, 1))).astype(np.float32)
+    x[::5, 3:11] = np.floor(x[::5, 3:11]) + 0.5
+    x[::11] = np.float32(2.0 ** -3) * rng.integers(-60, 60, (len(x[::11]), 32)).astype(np.float32)
+    codes, s, z = C.quantize_group_int4(x)
+    t = torch.from_numpy(x)
+    tz = t.min(dim=1).values.to(torch.float16)
+    ts = ((t.max(dim=1).values - tz.float()) / 15.0).to(torch.float16)
+    y = (t - tz.float()[:, None]) / torch.where(ts > 0, ts, torch.ones_like(ts)).float()[:, None]
+    tq = torch.clamp(torch.round(y), 0, 15)
+    tq = torch.where((ts > 0)[:, None], tq, torch.zeros_like(tq))
+    assert np.array_equal(z, tz.numpy()) and np.array_equal(s, ts.numpy())
+    assert np.array_equal(codes.astype(np.int64), tq.numpy().astype(np.int64))
+
+
+def _sat_groups():
+    """bf16-representable groups whose zero point or scale leaves fp16's range."""
+    g = np.zeros((4, 32), np.float32)
+    g[0] = np.linspace(-2.0 ** 17, 2.0 ** 20, 32)            # min and span beyond 65504
+    g[0, 7] = 65504.0 * 3.5 - 65504.0                          # (x - z) / s = 3.5 when s saturates
+    g[1] = np.linspace(0.0, 2.0 ** 20, 32)                     # span only: z = 0, s saturates
+    g[2] = -2.0 ** 17 + np.arange(32, dtype=np.float32) * 64.0  # every value below -65504
+    g[3] = np.linspace(-2.0 ** 16, 2.0 ** 16, 32)              # -65536 .. 65536
+    return C.round_to_bf16(g).astype(np.float32)
+
+
+@pytest.mark.parametrize("top", [15, 3])
+def test_affine_encoder_saturates_zero_point_and_scale_at_65504(top):
+    """fp16_sat clips to +-65504 (torch's half cast would give inf there).
+    Closed form per group: z = max(lo, -65504) rounded to fp16, s =
+    min((hi - z) / top, 65504); codes from Python float division."""
+    x = _sat_groups()
+    codes, s, z = C._quantize_group_affine(x, top)
+    assert np.all(np.isfinite(z.astype(np.float64))) and np.all(np.isfinite(s.astype(np.float64)))
+    assert z[0] == -65504 and z[2] == -65504 and z[1] == 0 and z[3] == -65504
+    assert s[0] == 65504 and s[1] == 65504
+    # all values below the saturated zero point: hi - z < 0, so s < 0 and every code is 0
+    assert s[2] < 0 and not codes[2].any()
+    for gi in (0, 1, 3):
+        zz, ss = float(z[gi]), float(s[gi])
+        for e in range(32):
+            xv = float(x[gi, e])
+            num = float(np.float32(xv - zz))
+            want = min(max(round(float(np.float32(num / ss))), 0), top)   # round(): half to even
+            assert codes[gi, e] == want, (gi, e, xv)
+    if top == 15:
+        assert codes[0, 7] == 4                                 # 3.5 rounds to even
+    # group 3: z saturates (lo = -65536), s does not: (65536 + 65504) / top is an fp16 value
+    assert float(s[3]) == (65536.0 + 65504.0) / top
+
+
 # ---------------------------------------------------------------- bf16 rounding
 
 def test_round_to_bf16_matches_torch_for_float32_inputs():
