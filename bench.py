@@ -587,6 +587,70 @@ def leg_prefill(dev, timer, steps, warm, tflops_peak):
     return res
 
 
+def leg_prefill_paged(dev, timer, steps, warm, tflops_peak):
+    """The windowed prefill over a paged, mixed-codec cache: the same 16 q / 2 KV
+    heads, head_dim 128, 1048576 cached tokens, now in 64-token FP8 e4m3 pages
+    at random physical slots, with the 1024-token chunk in BF16 pages; each of
+    the eight 131072-token windows and the chunk window is staged through the
+    block table (dequantised to scaled fp16) and attended with fp16 MMAs, folded
+    by log2-sum-exp.  Timed: staging and attention of all nine windows."""
+    import torch
+    import mixed_precision_paged_argus_gb300.argus as argus
+    from mixed_precision_paged_argus_gb300 import workloads as W, accounting as A
+    Hq, Hkv, D_, NQ, CTX, WIN, P_ = 16, 2, 128, 1024, 1 << 20, 131072, 64
+    n_cache, n_chunk = CTX // P_, NQ // P_
+    n_pages = n_cache + n_chunk
+    g = argus.geom(Hq, Hkv, D_, P_)
+    perm = W.permutation(n_cache, W.seed_of("prefill", 0, 4))
+    fp8 = argus.Pool.empty(W.FP8_E4M3, n_cache, Hkv, P_, D_, device=dev)
+    bf = argus.Pool.empty(W.BF16, n_chunk, Hkv, P_, D_, device=dev)
+    step_pages = 4096                                  # demote the cache in pieces (bounded source buffer)
+    for p0 in range(0, n_cache, step_pages):
+        n = min(step_pages, n_cache - p0)
+        src = W.normal((n, 2, Hkv, P_, D_), W.BF16, W.seed_of("prefill", 0, 1) * 64 + p0 // step_pages, device=dev)
+        argus.quantize_pages(g, W.BF16, src, n, torch.arange(n, dtype=torch.int32, device=dev), fp8,
+                             torch.from_numpy(perm[p0:p0 + n].astype(np.int32)).to(dev), n)
+        del src
+    src = W.normal((n_chunk, 2, Hkv, P_, D_), W.BF16, W.seed_of("prefill", 0, 3), device=dev)
+    ids = torch.arange(n_chunk, dtype=torch.int32, device=dev)
+    argus.quantize_pages(g, W.BF16, src, n_chunk, ids, bf, ids, n_chunk)
+    del src
+    table = torch.from_numpy(np.concatenate([perm, np.arange(n_chunk)]).astype(np.int32)).to(dev)
+    codecs = torch.from_numpy(np.array([W.FP8_E4M3] * n_cache + [W.BF16] * n_chunk, np.uint8)).to(dev)
+    q = W.normal((Hq, NQ, D_), W.BF16, W.seed_of("prefill", 0, 0), device=dev)
+    acc_o = torch.empty((Hq, NQ, D_), dtype=torch.float32, device=dev)
+    acc_l = torch.empty((Hq, NQ), dtype=torch.float32, device=dev)
+    wins = [(w, WIN) for w in range(0, CTX, WIN)] + [(CTX, NQ)]
+    ws = torch.empty(max(argus.paged_window_prefill_workspace_bytes(g, NQ, wl) for _, wl in wins), dtype=torch.uint8,
+                     device=dev)
+    # the staging decision: each query row would read every visible page in place
+    tok_fp8 = 2 * Hkv * D_                              # bytes per cached token (K + V codes), FP8 pages
+    cache_bytes = int(n_cache * (2 * Hkv * P_ * D_ + 2 * Hkv * 4) + n_chunk * 2 * Hkv * P_ * D_ * 2)
+    rows = [int(CTX * tok_fp8 + (i + 1) * 2 * Hkv * D_ * 2) for i in range(NQ)]
+    stage = argus.staging_moves_less(rows, cache_bytes)
+
+    def run():
+        for i, (w0, wl) in enumerate(wins):
+            argus.paged_window_prefill_attn(g, NQ, q, [fp8, bf], codecs, table, n_pages, w0, wl, CTX,
+                                            W.softmax_scale(D_), acc_o, acc_l, 1 if i else 0, ws, stream=timer.stream)
+
+    ms = timer.time(timer.graph(run).replay, max(3, steps // 10), warm)
+    flops = A.prefill_flops(Hq, D_, NQ, NQ * CTX + NQ * (NQ + 1) // 2)
+    res = {"workload": "paged_windowed_prefill: 16 q / 2 kv, head_dim 128, 1048576 cached tokens in 64-token FP8 e4m3 "
+                       "pages (random slots) + 1024-token chunk in BF16 pages, 131072-token windows staged through "
+                       "the block table and folded by log2-sum-exp",
+           "ms": ms, "flops": flops, "tflops": flops / (ms * 1e-3) / 1e12,
+           "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / tflops_peak,
+           "staging_moves_less": stage, "rows_read_in_place_bytes": sum(rows), "cache_bytes": cache_bytes,
+           "note": "timed: per window, dequantise + scale to fp16 (two passes over the window's codes), query to "
+                   "fp16, then Q.K^T and P.V in fp16 on tcgen05 (same FLOP count as the BF16 leg); fp16 dense peak "
+                   "= bf16 dense peak"}
+    del fp8, bf, q, ws
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_legs(steps, warm):
     import torch
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
@@ -594,7 +658,8 @@ def run_legs(steps, warm):
     hbm, tf, _ = peaks()
     out = {}
     for name, fn, arg in (("tiny_fp16", leg_tiny, hbm), ("batched", leg_batched, hbm),
-                          ("sparse", leg_sparse, hbm), ("prefill", leg_prefill, tf)):
+                          ("sparse", leg_sparse, hbm), ("prefill", leg_prefill, tf),
+                          ("prefill_paged_fp8", leg_prefill_paged, tf)):
         t0 = time.perf_counter()
         try:
             out[name] = fn(dev, timer, steps, warm, arg)

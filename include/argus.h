@@ -290,7 +290,8 @@ argus_status argus_fold_lse(int64_t n_rows, int32_t head_dim, float* acc_o,
  * Arguments: q device bf16 [Hq][n_q][D]; k, v device bf16 with element
  * (h, j, d) at h * kv_head_stride + j * D + d (kv_head_stride = 0 means
  * win_len * D); acc_o device float [Hq][n_q][D]; acc_lse2 [Hq][n_q].
- * Supported: head_dim 128, n_q a multiple of 128, win_len a multiple of 128.
+ * softmax_scale finite and >= 0.  Supported: head_dim 128, any n_q and
+ * win_len (keys past win_len and query rows past n_q are masked).
  * num_splits: key ranges per 128-row query tile, each its own CTA, so that
  * every SM works; their partial results are kept in ws and folded by a second
  * kernel.  1 = one CTA per tile folding directly (ws unused); k > 1 = k ranges;
@@ -311,6 +312,47 @@ argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n_q,
                                        float* acc_lse2, int32_t fold,
                                        int32_t num_splits, void* ws, size_t ws_bytes,
                                        void* stream);
+
+/* ---------------------------------------------------------------------------
+ * argus_paged_window_prefill_attn -- the staged prefill over a paged, mixed-
+ * codec cache: one window of the cache is staged into device memory through
+ * the block table and attended as argus_window_prefill_attn does ([PR499]
+ * comment on "--kv-placement host": cached pages are staged into a device
+ * window, attended per window, and the windows folded by log2-sum-exp).
+ *   The window holds positions win_pos0 .. win_pos0 + win_len - 1 of one
+ *   sequence: position p is row p % P of logical page p / P, whose codec and
+ *   physical slot are page_codec[p / P] and block_table[p / P] (pages of any
+ *   codec, FP8 included).  Key j of the window is at absolute position
+ *   win_pos0 + j; query row i at q_pos0 + i; visible iff win_pos0 + j <=
+ *   q_pos0 + i.  fold as in argus_window_prefill_attn.
+ *   Staging (in the workspace): every key and value of the window is
+ *   dequantised from its page's codes and written as fp16, scaled by a power
+ *   of two chosen from the window's largest |k| (resp. |v|) so that it lies in
+ *   [2^14, 2^15); each query row is written as fp16 scaled the same way by its
+ *   own power of two.  Q.K^T and P.V then run in fp16 on the tensor cores with
+ *   fp32 accumulation; the powers of two are undone exactly on the scores and
+ *   the output.
+ * Arguments: q device bf16 [Hq][n_q][D]; pools host array (layout as for
+ * argus_paged_decode_attn, at most one pool per codec); page_codec,
+ * block_table device [max_pages] rows of the sequence; the window must lie in
+ * [0, max_pages * P) (else ARGUS_E_INVALID).  A page whose codec has no pool or
+ * whose slot is outside its pool reads as zeros and is counted once per
+ * window in *status (device uint32, may be NULL).  ws (device, 16-byte
+ * aligned) of argus_paged_window_prefill_workspace_bytes(g, n_q, win_len,
+ * num_splits) bytes, required; no initialisation needed.  head_dim 128.
+ * ------------------------------------------------------------------------- */
+argus_status argus_paged_window_prefill_workspace_bytes(const argus_geom* g, int32_t n_q,
+                                                        int64_t win_len, int32_t num_splits,
+                                                        size_t* bytes);
+
+argus_status argus_paged_window_prefill_attn(const argus_geom* g, int32_t n_q, const void* q,
+                                             const argus_pool* pools, int32_t n_pools,
+                                             const uint8_t* page_codec,
+                                             const int32_t* block_table, int32_t max_pages,
+                                             int64_t win_pos0, int64_t win_len, int64_t q_pos0,
+                                             float softmax_scale, float* acc_o, float* acc_lse2,
+                                             int32_t fold, int32_t num_splits, void* ws,
+                                             size_t ws_bytes, uint32_t* status, void* stream);
 
 /* ---------------------------------------------------------------------------
  * argus_staging_moves_less -- whether a prefill should stage the cache into

@@ -55,7 +55,9 @@ class DecodeArgs(ctypes.Structure):
 EXPORTS = ["argus_quantize_pages", "argus_decode_workspace_bytes", "argus_paged_decode_attn",
            "argus_paged_decode_attn_noalloc",
            "argus_select_workspace_bytes", "argus_select_pages", "argus_fold_lse",
-           "argus_window_prefill_workspace_bytes", "argus_window_prefill_attn", "argus_staging_moves_less",
+           "argus_window_prefill_workspace_bytes", "argus_window_prefill_attn",
+           "argus_paged_window_prefill_workspace_bytes", "argus_paged_window_prefill_attn",
+           "argus_staging_moves_less",
            "argus_status_string", "argus_last_error"]
 
 
@@ -98,6 +100,11 @@ def lib():
                                             ctypes.c_float, vp, vp, i32, i32, vp, sz, vp]
     L.argus_window_prefill_workspace_bytes.restype = ctypes.c_int
     L.argus_window_prefill_workspace_bytes.argtypes = [ctypes.POINTER(Geom), i32, i64, i32, ctypes.POINTER(sz)]
+    L.argus_paged_window_prefill_workspace_bytes.restype = ctypes.c_int
+    L.argus_paged_window_prefill_workspace_bytes.argtypes = [ctypes.POINTER(Geom), i32, i64, i32, ctypes.POINTER(sz)]
+    L.argus_paged_window_prefill_attn.restype = ctypes.c_int
+    L.argus_paged_window_prefill_attn.argtypes = [ctypes.POINTER(Geom), i32, vp, ctypes.POINTER(PoolDesc), i32, vp, vp,
+                                                  i32, i64, i64, i64, ctypes.c_float, vp, vp, i32, i32, vp, sz, vp, vp]
     L.argus_staging_moves_less.restype = ctypes.c_int
     L.argus_staging_moves_less.argtypes = [ctypes.POINTER(ctypes.c_int64), i64, i64, ctypes.POINTER(i32)]
     _lib = L
@@ -276,3 +283,24 @@ def window_prefill_attn(g, n_q, q, k, v, kv_head_stride, win_len, win_pos0, q_po
                                            int(kv_head_stride), int(win_len), int(win_pos0), int(q_pos0),
                                            float(softmax_scale), _ptr(acc_o), _ptr(acc_lse2), int(fold),
                                            int(num_splits), _ptr(ws), nbytes, _stream(stream)))
+
+
+def paged_window_prefill_workspace_bytes(g, n_q, win_len, num_splits=0):
+    n = ctypes.c_size_t(0)
+    _check(lib().argus_paged_window_prefill_workspace_bytes(ctypes.byref(g), int(n_q), int(win_len), int(num_splits),
+                                                            ctypes.byref(n)))
+    return n.value
+
+
+def paged_window_prefill_attn(g, n_q, q, pools, page_codec, block_table, max_pages, win_pos0, win_len, q_pos0,
+                              softmax_scale, acc_o, acc_lse2, fold, ws, num_splits=0, status=None, stream=None):
+    """Stage one window of the paged cache (block_table / page_codec rows of one
+    sequence, pools of any codec) and attend the query chunk to it, folding
+    into acc_o / acc_lse2; ws of paged_window_prefill_workspace_bytes bytes."""
+    arr = (PoolDesc * max(1, len(pools)))(*[p.desc() for p in pools])
+    _check(lib().argus_paged_window_prefill_attn(ctypes.byref(g), int(n_q), _ptr(q),
+                                                 ctypes.cast(arr, ctypes.POINTER(PoolDesc)), len(pools),
+                                                 _ptr(page_codec), _ptr(block_table), int(max_pages), int(win_pos0),
+                                                 int(win_len), int(q_pos0), float(softmax_scale), _ptr(acc_o),
+                                                 _ptr(acc_lse2), int(fold), int(num_splits), _ptr(ws),
+                                                 ws.numel() * ws.element_size(), _ptr(status), _stream(stream)))

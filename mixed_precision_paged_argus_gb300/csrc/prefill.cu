@@ -60,7 +60,8 @@ constexpr int kOffML = kOffMisc + 64;                 // group 1's (m, l) per ro
 constexpr int kSmemBytes = kOffML + kBM * 8 + 1024;   // + alignment slack
 
 struct PParams {
-  int G, n_q, n_tiles;              // tiles per KV head = G * n_q / 128
+  int G, n_q, n_tiles;              // tiles per KV head = ceil(G * n_q / 128)
+  long long rows_h;                 // query rows per KV head = G * n_q (its G heads stacked)
   long long win_len, win_pos0, q_pos0;
   float scale_log2;
   float* acc_o;
@@ -70,16 +71,22 @@ struct PParams {
   float* ws_o;                      // nsplit > 1: partial o [tile][split][128][D], normalised
   float* ws_lse;                    //             and its lse2 [tile][split][128]
   const uint32_t* vmax_bits;        // fp16 P.V: bits of max |v| over the window
+  // fp16 Q.K^T (staged paged windows): K scaled by 2^-ek from max |k| (bits at
+  // kmax_bits), query row r scaled by 1 / qfac[r]; score = S' * qfac[r] * 2^ek
+  const uint32_t* kmax_bits;
+  const float* qfac;
 };
 
-// fp16 P.V: V is converted once per window to fp16 scaled by 2^-e, e >= 0 the
-// smallest with max|v| * 2^-e < 2^15, so that nothing overflows; the output is
-// multiplied back by 2^e.  Every thread derives e from the same max word.
-__device__ __forceinline__ int v16_exponent(uint32_t vmax_bits) {
-  const float vm = __uint_as_float(vmax_bits);
-  if (!(vm < 3.0e38f) || vm < 32768.f) return 0;   // finite inputs below 2^15 need no scaling
+// fp16 copies (V for fp16 P.V; K and V of a staged paged window) are scaled by
+// 2^-e with e chosen from the largest magnitude m of the copied values so that
+// m * 2^-e lies in [2^14, 2^15): nothing overflows fp16 and small values keep
+// their precision.  The result is multiplied back by 2^e.  Every thread derives
+// e from the same max word.  m = 0 (or not finite) gives e = 0.
+__device__ __forceinline__ int f16_exponent(uint32_t max_bits) {
+  const float m = __uint_as_float(max_bits);
+  if (!(m > 0.f) || !(m < 3.0e38f)) return 0;
   int k = 0;
-  frexpf(vm, &k);                                    // vm < 2^k
+  frexpf(m, &k);                                     // 2^(k-1) <= m < 2^k
   return k - 15;
 }
 
@@ -188,12 +195,17 @@ __device__ __forceinline__ void group_bar(int id) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kSoftmaxWarps * 32) : "memory");
 }
 
-// F16P: P.V in fp16 (P scaled by 2^7, V the scaled fp16 copy) with one MMA per
-// key step; otherwise bf16 with P split into hi + lo parts (two MMAs).
-template <bool F16P>
+// MODE 0: Q.K^T in bf16, P.V in bf16 with P split into hi + lo parts (two MMAs).
+// MODE 1: Q.K^T in bf16, P.V in fp16 (P scaled by 2^7, V the scaled fp16 copy),
+//         one MMA per key step.
+// MODE 2: both in fp16 over a staged window: fp16 K and V copies scaled by
+//         powers of two and an fp16 query scaled per row (score scale per row).
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PParams p) {
+  constexpr bool F16P = MODE >= 1;
+  constexpr bool F16QK = MODE == 2;
   constexpr float kPBias = F16P ? 7.f : 0.f;   // fp16 P is stored as P * 2^kPBias
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -210,11 +222,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x, h = blockIdx.y, split = blockIdx.z;
-  const long long row0 = (long long)h * p.G * p.n_q + (long long)tile * kBM;   // first row of [Hq*n_q]
-  const int hq = (int)(row0 / p.n_q);
-  const long long i0 = row0 - (long long)hq * p.n_q;                              // first query index
+  // The G query heads of KV head h are stacked: row lin of the head's rows_h
+  // rows is query index lin % n_q of query head h * G + lin / n_q, and Q / the
+  // accumulator row h * rows_h + lin.  A tile may straddle two query heads; its
+  // rows past rows_h (last tile) are computed on whatever the load gave and
+  // never written.
+  const long long lin0 = (long long)tile * kBM;
+  const long long row0 = (long long)h * p.rows_h + lin0;                      // first row of [Hq*n_q]
+  const long long lin_last = min(lin0 + kBM - 1, p.rows_h - 1);
+  const long long qi_max = (lin0 / p.n_q != lin_last / p.n_q) ? p.n_q - 1 : lin_last % p.n_q;
   // keys j < n_keys can be visible to some row of the tile
-  const long long last_visible = p.q_pos0 + i0 + kBM - 1 - p.win_pos0;
+  const long long last_visible = p.q_pos0 + qi_max - p.win_pos0;
   long long n_keys = last_visible + 1;
   if (n_keys < 0) n_keys = 0;
   if (n_keys > p.win_len) n_keys = p.win_len;
@@ -278,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // order: S0, S1, then per block i: P.V of i, S of i+2 (into the buffer
     // P.V of i reads; the MMA pipe keeps the two in order)
     if (lane == 0 && nb > 0) {
-      constexpr uint32_t idQK = idesc_f16kind(true, false);
+      constexpr uint32_t idQK = idesc_f16kind(!F16QK, false);
       constexpr uint32_t idPV = idesc_f16kind(!F16P, true);
       const uint32_t q_s = smem_u32(smem + kOffQ);
       bool ok = mbar_wait(q_full, 0, &misc[1]);
@@ -328,8 +346,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int grp = warp / kGroupWarps;                // this group takes blocks grp, grp+2, ...
     const int wq = warp % kGroupWarps;                 // TMEM lane quarter
     const int row = wq * 32 + lane;                    // TMEM lane = tile row
-    const long long qi = i0 + row;                     // query index within the chunk
-    const long long vis_last = p.q_pos0 + qi - p.win_pos0;   // last visible key index
+    const long long lin = lin0 + row;
+    const bool valid_row = lin < p.rows_h;
+    const long long qi = lin % p.n_q;                  // query index within the chunk
+    // last visible key index (-1: none), never past the window's last key
+    const long long vis_last = valid_row ? min(p.q_pos0 + qi - p.win_pos0, p.win_len - 1) : -1;
+    float sc_row = p.scale_log2;                       // log2-domain score scale of this row
+    if constexpr (F16QK) {
+      if (valid_row) sc_row *= ldexpf(p.qfac[row0 + row], f16_exponent(*p.kmax_bits));
+    }
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t sS = tS[grp] + lane_off, sO = tO[grp] + lane_off;
     float m = -INFINITY, l = 0.f;
@@ -366,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (k0 + c * 32 + e <= vis_last) mj = fmaxf(mj, __uint_as_float(v[e]));
         }
       }
-      mj *= p.scale_log2;
+      mj *= sc_row;
       const bool move = mj > m + kRescaleThreshold || (m == -INFINITY && mj != -INFINITY);
       const bool scale_o = move && m != -INFINITY;
       if (__any_sync(0xffffffffu, scale_o)) {
@@ -390,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the 2^8 rescale threshold; l is summed in the same units), or a bf16
       // pair hi + lo (P.V then carries about 16 significant bits of P).  A
       // fully masked block has m = -inf and yields P = 0 through the mask below.
-      const float sc = p.scale_log2;
+      const float sc = sc_row;
       const float mm = (m == -INFINITY) ? 0.f : m - kPBias;
       const long long lim = edge ? vis_last - k0 : (long long)kBN;   // keys e <= lim are visible
 #pragma unroll 2
@@ -456,12 +481,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // references in the units l was summed in (P scaled by 2^kPBias)
       const float m0v = nk > 0 ? m - kPBias : -INFINITY, l0v = nk > 0 ? l : 0.f;
       const float M = fmaxf(m0v, o1ml.x);
-      const float vsc = F16P ? ldexpf(1.f, v16_exponent(*p.vmax_bits)) : 1.f;   // undo V's 2^-e
+      const float vsc = F16P ? ldexpf(1.f, f16_exponent(*p.vmax_bits)) : 1.f;   // undo V's 2^-e
       const float w0 = (m0v == -INFINITY) ? 0.f : fast_exp2(m0v - M);
       const float w1 = (o1ml.x == -INFINITY) ? 0.f : fast_exp2(o1ml.x - M);
       const float lt = l0v * w0 + o1ml.y * w1;
       const bool have = alive && lt > 0.f;
-      const long long orow = (long long)hq * p.n_q + qi;
+      const long long orow = row0 + row;               // = (query head) * n_q + qi
       const uint32_t o0a = tO[0] + lane_off, o1a = tO[1] + lane_off;
       if (p.nsplit > 1) {
         // partial of this key range: normalised o and its lse2, folded later
@@ -491,9 +516,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         p.ws_lse[part * kBM + row] = have ? M + log2f(lt) : -INFINITY;
       } else {
+        // every lane runs the (warp-collective) TMEM loads; rows past the
+        // head's last row neither read nor write the accumulator
         float* ao = p.acc_o + orow * kD;
         const float lse = have ? M + log2f(lt) : -INFINITY;
-        const float La = p.fold ? p.acc_lse2[orow] : -INFINITY;
+        const float La = (p.fold && valid_row) ? p.acc_lse2[orow] : -INFINITY;
         float wa = 0.f, wb = 0.f, L = -INFINITY;
         if (have) {
           if (La == -INFINITY) {
@@ -509,6 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           wa = 1.f;
           L = La;
         }
+        const bool write = valid_row && (have || !p.fold);
   #pragma unroll 1
         for (int c = 0; c < kD / 16; ++c) {
           uint32_t v0[16], v1[16];
@@ -527,13 +555,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               ov[u] = x * wb;
             }
-            float4 a = (p.fold && wa != 0.f) ? *reinterpret_cast<const float4*>(ao + c * 16 + e)
-                                             : make_float4(0.f, 0.f, 0.f, 0.f);
-            float4 o = make_float4(wa * a.x + ov[0], wa * a.y + ov[1], wa * a.z + ov[2], wa * a.w + ov[3]);
-            if (have || !p.fold) *reinterpret_cast<float4*>(ao + c * 16 + e) = o;
+            if (write) {
+              float4 a = (p.fold && wa != 0.f) ? *reinterpret_cast<const float4*>(ao + c * 16 + e)
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+              float4 o = make_float4(wa * a.x + ov[0], wa * a.y + ov[1], wa * a.z + ov[2], wa * a.w + ov[3]);
+              *reinterpret_cast<float4*>(ao + c * 16 + e) = o;
+            }
           }
         }
-        if (have || !p.fold) p.acc_lse2[orow] = L;
+        if (write) p.acc_lse2[orow] = L;
       }
     }
   }
@@ -553,11 +583,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // epilogue: L = max + log2(sum of 2^(lse - max)), o = sum of 2^(lse - L) o_s.
 constexpr int kFoldWarps = 8;
 __global__ void __launch_bounds__(32 * kFoldWarps) prefill_fold_kernel(const PParams p, long long n_rows) {
-  const long long r = (long long)blockIdx.x * kFoldWarps + (threadIdx.x >> 5);
+  const long long r = (long long)blockIdx.x * kFoldWarps + (threadIdx.x >> 5);   // = h * rows_h + lin
   if (r >= n_rows) return;
   const int lane = threadIdx.x & 31;
-  const long long tile_lin = r / kBM;        // = h * n_tiles + tile
-  const int row = (int)(r - tile_lin * kBM);
+  const long long hh = r / p.rows_h, lin = r - hh * p.rows_h;
+  const long long tile_lin = hh * p.n_tiles + lin / kBM;
+  const int row = (int)(lin % kBM);
   const float* pl = p.ws_lse + (size_t)tile_lin * p.nsplit * kBM + row;
   const float La = p.fold ? p.acc_lse2[r] : -INFINITY;
   float M = La;
@@ -630,7 +661,7 @@ __global__ void __launch_bounds__(256) v16_max_kernel(const uint16_t* v, long lo
 // outside fp16's subnormal range.
 __global__ void __launch_bounds__(256) v16_convert_kernel(const uint16_t* v, long long stride, long long win_len,
                                                           long long n_vec, const uint32_t* vmax, uint16_t* v16) {
-  const float sc = ldexpf(1.f, -v16_exponent(*vmax));
+  const float sc = ldexpf(1.f, -f16_exponent(*vmax));
   const long long per_head = win_len * (kD / 8);
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec; i += (long long)gridDim.x * blockDim.x) {
     const long long h = i / per_head, r = i - h * per_head;
@@ -697,31 +728,307 @@ static argus_status check_geom(const argus_geom* g, int32_t n_q, int64_t win_len
     return fail(ARGUS_E_INVALID, "prefill: bad head counts");
   if (g->head_dim != kD) return fail(ARGUS_E_UNSUPPORTED, "prefill: head_dim %d (supported: 128)", g->head_dim);
   if (n_q < 0 || win_len < 0) return fail(ARGUS_E_INVALID, "prefill: negative n_q or win_len");
-  if (n_q % kBM != 0 || win_len % kBN != 0)
-    return fail(ARGUS_E_UNSUPPORTED, "prefill: n_q (%d) and win_len (%lld) must be multiples of 128", n_q,
-                (long long)win_len);
-  if ((long long)g->n_q_heads * n_q > (1LL << 31) || win_len > (1LL << 31))
+  if ((long long)g->n_q_heads * n_q > (1LL << 31) - kBM || win_len > (1LL << 31) - kBN)
     return fail(ARGUS_E_UNSUPPORTED, "prefill: sizes beyond 2^31 rows");
   return ARGUS_OK;
 }
+
+// query tiles of one KV head (its G heads' rows stacked)
+static long long tiles_per_head(const argus_geom* g, int32_t n_q) {
+  return ((long long)(g->n_q_heads / g->n_kv_heads) * n_q + kBM - 1) / kBM;
+}
+
+static size_t up16(size_t x) { return (x + 15) / 16 * 16; }
 
 static size_t split_bytes(long long n_tiles_total, int nsplit) {
   return nsplit > 1 ? (size_t)n_tiles_total * nsplit * kBM * (kD + 1) * sizeof(float) : 0;
 }
 
-// With a workspace, P.V runs in fp16: after the partials come the window's V
-// as scaled fp16 [Hkv][win_len][D] and the max-|v| word.
-static size_t v16_bytes(long long n_kv_heads, long long win_len) {
-  return (size_t)n_kv_heads * std::max<long long>(win_len, kBN) * kD * 2;
+// fp16 copy of one operand over the window: [Hkv][win_len][D]
+static size_t win16_bytes(long long n_kv_heads, long long win_len) {
+  return (size_t)n_kv_heads * std::max<long long>(win_len, 1) * kD * 2;
 }
 
+// With a workspace, P.V runs in fp16: after the partials come the window's V
+// as scaled fp16 [Hkv][win_len][D] and the max-|v| word.
 static size_t ws_total(long long n_tiles_total, int nsplit, long long n_kv_heads, long long win_len) {
-  return split_bytes(n_tiles_total, nsplit) + v16_bytes(n_kv_heads, win_len) + 16;
+  return split_bytes(n_tiles_total, nsplit) + win16_bytes(n_kv_heads, win_len) + 16;
+}
+
+// Staged paged window: partials, fp16 K, fp16 V, fp16 Q [Hq * n_q][D], the
+// per-row query factors, then the max-|k| and max-|v| words.
+struct PagedWs {
+  size_t part, k16, v16, q16, qfac, words, total;
+};
+static PagedWs paged_ws(const argus_geom* g, int32_t n_q, long long win_len, long long n_tiles_total, int nsplit) {
+  PagedWs w;
+  const long long rows = (long long)g->n_q_heads * n_q;
+  w.part = 0;
+  w.k16 = split_bytes(n_tiles_total, nsplit);
+  w.v16 = w.k16 + win16_bytes(g->n_kv_heads, win_len);
+  w.q16 = w.v16 + win16_bytes(g->n_kv_heads, win_len);
+  w.qfac = w.q16 + up16((size_t)std::max<long long>(rows, 1) * kD * 2);
+  w.words = w.qfac + up16((size_t)std::max<long long>(rows, 1) * 4);
+  w.total = w.words + 16;
+  return w;
 }
 
 static int resolve_splits(long long tiles, long long win_len, int32_t num_splits, bool have_ws) {
   if (num_splits > 0) return num_splits;
-  return have_ws ? plan_splits(tiles, win_len / kBN) : 1;
+  return have_ws ? plan_splits(tiles, (win_len + kBN - 1) / kBN) : 1;
+}
+
+// Tensor maps over Q [rows][D] and K, V [Hkv][rows of a window][D] (element
+// strides in elements), all in `dtype`; a window of 0 keys maps one row.
+static argus_status make_maps(CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv, const void* q, long long q_rows,
+                              const void* k, const void* v, long long n_kv_heads, long long win_len,
+                              long long kv_stride, CUtensorMapDataType qdt, CUtensorMapDataType kdt,
+                              CUtensorMapDataType vdt, long long v_stride) {
+  const long long wl = std::max<long long>(win_len, 1);
+  const cuuint64_t qd[2] = {(cuuint64_t)kD, (cuuint64_t)std::max<long long>(q_rows, 1)};
+  const cuuint64_t qs[1] = {(cuuint64_t)kD * 2};
+  const cuuint64_t kd[3] = {(cuuint64_t)kD, (cuuint64_t)wl, (cuuint64_t)n_kv_heads};
+  const cuuint64_t ks[2] = {(cuuint64_t)kD * 2, (cuuint64_t)kv_stride * 2};
+  const cuuint64_t vs[2] = {(cuuint64_t)kD * 2, (cuuint64_t)v_stride * 2};
+  if (!make_map(mq, q, 2, qd, qs, qdt)) return fail(ARGUS_E_LAUNCH, "prefill: tensor map for q failed");
+  if (!make_map(mk, k, 3, kd, ks, kdt)) return fail(ARGUS_E_LAUNCH, "prefill: tensor map for k failed");
+  if (!make_map(mv, v, 3, kd, vs, vdt)) return fail(ARGUS_E_LAUNCH, "prefill: tensor map for v failed");
+  return ARGUS_OK;
+}
+
+// Launch the attention kernel of `mode` over (tiles, Hkv, splits) and, with
+// more than one split, the fold of the partials.
+static argus_status launch_attention(int mode, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                                     const PParams& p, long long n_kv_heads, long long n_rows, cudaStream_t s) {
+  static PerContext configured;
+  argus_status sta = configured.ensure([](int) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(prefill_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(prefill_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "prefill: smem attribute: %s", cudaGetErrorString(e));
+    return ARGUS_OK;
+  });
+  if (sta != ARGUS_OK) return sta;
+  dim3 grid(p.n_tiles, (unsigned)n_kv_heads, p.nsplit);
+  if (mode == 0) prefill_kernel<0><<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
+  else if (mode == 1) prefill_kernel<1><<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
+  else prefill_kernel<2><<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
+  argus_status st = launch_status("window prefill attention");
+  if (st != ARGUS_OK || p.nsplit == 1) return st;
+  prefill_fold_kernel<<<(unsigned)((n_rows + kFoldWarps - 1) / kFoldWarps), 32 * kFoldWarps, 0, s>>>(p, n_rows);
+  return launch_status("window prefill attention (fold)");
+}
+
+static argus_status common_args(const argus_geom* g, int32_t n_q, int64_t win_len, float softmax_scale, int32_t fold,
+                                int32_t num_splits) {
+  argus_status st0 = check_geom(g, n_q, win_len);
+  if (st0 != ARGUS_OK) return st0;
+  if (fold != 0 && fold != 1) return fail(ARGUS_E_INVALID, "prefill: fold must be 0 or 1");
+  // the lazy running maximum takes the largest raw score as the largest scaled one
+  if (!std::isfinite(softmax_scale) || softmax_scale < 0.f)
+    return fail(ARGUS_E_INVALID, "prefill: softmax_scale must be finite and >= 0");
+  if (num_splits < 0 || num_splits > 1024) return fail(ARGUS_E_INVALID, "prefill: num_splits out of range");
+  return ARGUS_OK;
+}
+
+static PParams base_params(const argus_geom* g, int32_t n_q, int64_t win_len, int64_t win_pos0, int64_t q_pos0,
+                           float softmax_scale, float* acc_o, float* acc_lse2, int32_t fold) {
+  PParams p{};
+  p.G = g->n_q_heads / g->n_kv_heads;
+  p.n_q = n_q;
+  p.rows_h = (long long)p.G * n_q;
+  p.n_tiles = (int)tiles_per_head(g, n_q);
+  p.win_len = win_len;
+  p.win_pos0 = win_pos0;
+  p.q_pos0 = q_pos0;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.acc_o = acc_o;
+  p.acc_lse2 = acc_lse2;
+  p.fold = fold;
+  return p;
+}
+
+// ---------------------------------------------------------------- staging
+// A window of a paged, mixed-codec cache staged into fp16 copies: element
+// (h, j, d) of K (or V) is position win_pos0 + j of the sequence, found in
+// logical page pos / P, row pos % P, whose codec and slot come from
+// page_codec / block_table.  Values are dequantised exactly as the pool defines
+// them (codes x scale; INT4 / INT2 code x s + z in fp32), then scaled by the
+// window's power of two and rounded to fp16.
+struct SParams {
+  int Hkv, P, max_pages;
+  const uint8_t* codes[6];
+  const uint8_t* meta[6];
+  long long n_slots[6];
+  const uint8_t* page_codec;
+  const int32_t* block_table;
+  long long win_pos0, win_len, n_vec;   // n_vec = Hkv * win_len * D / 8
+  uint16_t* k16;
+  uint16_t* v16;
+  uint32_t* kmax;
+  uint32_t* vmax;
+  uint32_t* status;
+  // query staging
+  const uint16_t* q;
+  uint16_t* q16;
+  float* qfac;
+  long long q_rows;
+};
+
+__device__ __forceinline__ float f16_to_f32(uint32_t bits16) {
+  return __half2float(__ushort_as_half((unsigned short)(bits16 & 0xFFFFu)));
+}
+
+// Dequantise elements d0 .. d0 + 7 of the key (kv = 0) or value (kv = 1) row at
+// sequence position pos for KV head h.  A page whose codec has no pool or whose
+// slot lies outside it gives zeros and false.
+__device__ __forceinline__ bool stage_load8(const SParams& p, int kv, int h, long long pos, int d0, float (&x)[8]) {
+  const long long page = pos / p.P;
+  const int row = (int)(pos - page * p.P);
+  const int codec = p.page_codec[page];
+  const long long slot = p.block_table[page];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) x[e] = 0.f;
+  if (codec < 0 || codec > ARGUS_INT2_G32 || p.codes[codec] == nullptr || slot < 0 || slot >= p.n_slots[codec])
+    return false;
+  const size_t unit = ((size_t)slot * 2 + kv) * p.Hkv + h;   // (slot, K|V, head)
+  const size_t r = unit * p.P + row;                          // token row of the pool
+  const uint8_t* c = p.codes[codec];
+  if (codec == ARGUS_FP16 || codec == ARGUS_BF16) {
+    const uint4 w = *reinterpret_cast<const uint4*>(c + (r * kD + d0) * 2);
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (codec == ARGUS_BF16) {
+        x[2 * e] = __uint_as_float(ww[e] << 16);
+        x[2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
+      } else {
+        x[2 * e] = f16_to_f32(ww[e]);
+        x[2 * e + 1] = f16_to_f32(ww[e] >> 16);
+      }
+    }
+  } else if (codec == ARGUS_FP8_E4M3 || codec == ARGUS_INT8) {
+    const uint2 w = *reinterpret_cast<const uint2*>(c + r * kD + d0);
+    const float sc = reinterpret_cast<const float*>(p.meta[codec])[unit];
+    const uint32_t ww[2] = {w.x, w.y};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      if (codec == ARGUS_FP8_E4M3) {
+        const uint32_t lo = e4m3x2_to_f16x2(ww[e]), hi = e4m3x2_to_f16x2(ww[e] >> 16);
+        x[4 * e] = f16_to_f32(lo) * sc;
+        x[4 * e + 1] = f16_to_f32(lo >> 16) * sc;
+        x[4 * e + 2] = f16_to_f32(hi) * sc;
+        x[4 * e + 3] = f16_to_f32(hi >> 16) * sc;
+      } else {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) x[4 * e + b] = (float)(int8_t)((ww[e] >> (8 * b)) & 0xFFu) * sc;
+      }
+    }
+  } else {
+    const __half2 sz = reinterpret_cast<const __half2*>(p.meta[codec])[r * (kD / 32) + d0 / 32];
+    const float s = __low2float(sz), z = __high2float(sz);
+    if (codec == ARGUS_INT4_G32) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(c + r * (kD / 2) + d0 / 2);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = fmaf((float)((w >> (4 * e)) & 0xFu), s, z);
+    } else {
+      const uint32_t w = *reinterpret_cast<const uint16_t*>(c + r * (kD / 4) + d0 / 4);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = fmaf((float)((w >> (2 * e)) & 0x3u), s, z);
+    }
+  }
+  return true;
+}
+
+// Vector i of the window: KV head h, window row j, dims d0 .. d0 + 7.
+__device__ __forceinline__ void stage_vec(const SParams& p, long long i, int& h, long long& j, int& d0) {
+  const long long per_head = p.win_len * (kD / 8);
+  h = (int)(i / per_head);
+  const long long rr = i - h * per_head;
+  j = rr / (kD / 8);
+  d0 = (int)(rr - j * (kD / 8)) * 8;
+}
+
+// Pass 1: max |k| and max |v| over the window (block reduction, one atomicMax
+// per block on the bit pattern: non-negative floats order like their bits);
+// unusable pages are counted once, at their first key vector in the window.
+__global__ void __launch_bounds__(256) stage_max_kernel(const SParams p) {
+  __shared__ float sh[2][8];
+  float mk = 0.f, mv = 0.f;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < p.n_vec; i += (long long)gridDim.x * blockDim.x) {
+    int h, d0;
+    long long j;
+    stage_vec(p, i, h, j, d0);
+    const long long pos = p.win_pos0 + j;
+    float x[8];
+    const bool ok = stage_load8(p, 0, h, pos, d0, x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) mk = fmaxf(mk, fabsf(x[e]));
+    stage_load8(p, 1, h, pos, d0, x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) mv = fmaxf(mv, fabsf(x[e]));
+    if (!ok && p.status && h == 0 && d0 == 0 && (j == 0 || pos % p.P == 0)) atomicAdd(p.status, 1u);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, o));
+    mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    sh[0][threadIdx.x >> 5] = mk;
+    sh[1][threadIdx.x >> 5] = mv;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < 8; ++w) {
+      mk = fmaxf(mk, sh[0][w]);
+      mv = fmaxf(mv, sh[1][w]);
+    }
+    atomicMax(p.kmax, __float_as_uint(mk));
+    atomicMax(p.vmax, __float_as_uint(mv));
+  }
+}
+
+// Pass 2: the scaled fp16 copies of K and V.
+__global__ void __launch_bounds__(256) stage_write_kernel(const SParams p) {
+  const float sk = ldexpf(1.f, -f16_exponent(*p.kmax));
+  const float sv = ldexpf(1.f, -f16_exponent(*p.vmax));
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < p.n_vec; i += (long long)gridDim.x * blockDim.x) {
+    int h, d0;
+    long long j;
+    stage_vec(p, i, h, j, d0);
+    const long long pos = p.win_pos0 + j;
+    float x[8];
+    uint32_t o[4];
+    stage_load8(p, 0, h, pos, d0, x);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] = pack_f16x2(x[2 * e] * sk, x[2 * e + 1] * sk);
+    reinterpret_cast<uint4*>(p.k16)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    stage_load8(p, 1, h, pos, d0, x);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] = pack_f16x2(x[2 * e] * sv, x[2 * e + 1] * sv);
+    reinterpret_cast<uint4*>(p.v16)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// The query in fp16: one warp per row of [Hq * n_q][D] bf16, scaled by 2^-e
+// from the row's max |q| (into [2^14, 2^15)); qfac[row] = 2^e.
+__global__ void __launch_bounds__(256) stage_q_kernel(const SParams p) {
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= p.q_rows) return;
+  const int lane = threadIdx.x & 31;
+  const uint2 w = reinterpret_cast<const uint2*>(p.q + row * kD)[lane];   // dims 4 lane .. 4 lane + 3
+  const float x[4] = {__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u), __uint_as_float(w.y << 16),
+                      __uint_as_float(w.y & 0xFFFF0000u)};
+  float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const int e = f16_exponent(__float_as_uint(m));
+  const float sc = ldexpf(1.f, -e);
+  reinterpret_cast<uint2*>(p.q16 + row * kD)[lane] = make_uint2(pack_f16x2(x[0] * sc, x[1] * sc), pack_f16x2(x[2] * sc, x[3] * sc));
+  if (lane == 0) p.qfac[row] = ldexpf(1.f, e);
 }
 
 }  // namespace prefill
@@ -734,7 +1041,7 @@ extern "C" argus_status argus_window_prefill_workspace_bytes(const argus_geom* g
   argus_status st = check_geom(g, n_q, win_len);
   if (st != ARGUS_OK) return st;
   if (num_splits < 0 || num_splits > 1024) return argus::fail(ARGUS_E_INVALID, "prefill: num_splits out of range");
-  const long long tiles = (long long)g->n_q_heads * n_q / kBM;
+  const long long tiles = tiles_per_head(g, n_q) * g->n_kv_heads;
   *bytes = ws_total(tiles, resolve_splits(tiles, win_len, num_splits, true), g->n_kv_heads, win_len);
   return ARGUS_OK;
 }
@@ -747,10 +1054,8 @@ extern "C" argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n
                                                   void* stream) {
   using namespace argus;
   using namespace argus::prefill;
-  argus_status st0 = check_geom(g, n_q, win_len);
+  argus_status st0 = common_args(g, n_q, win_len, softmax_scale, fold, num_splits);
   if (st0 != ARGUS_OK) return st0;
-  if (fold != 0 && fold != 1) return fail(ARGUS_E_INVALID, "prefill: fold must be 0 or 1");
-  if (!std::isfinite(softmax_scale)) return fail(ARGUS_E_INVALID, "prefill: softmax_scale not finite");
   if (n_q == 0) return ARGUS_OK;
   if (!q || !acc_o || !acc_lse2 || (win_len > 0 && (!k || !v)))
     return fail(ARGUS_E_INVALID, "prefill: NULL pointer");
@@ -760,20 +1065,8 @@ extern "C" argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n
   const long long stride = kv_head_stride ? kv_head_stride : win_len * kD;
   if (stride % 8 != 0 || stride < win_len * kD)
     return fail(ARGUS_E_INVALID, "prefill: kv_head_stride must be >= win_len*head_dim and a multiple of 8");
-  const int G = g->n_q_heads / g->n_kv_heads;
-  PParams p{};
-  p.G = G;
-  p.n_q = n_q;
-  p.n_tiles = G * n_q / kBM;
-  p.win_len = win_len;
-  p.win_pos0 = win_pos0;
-  p.q_pos0 = q_pos0;
-  p.scale_log2 = softmax_scale * 1.4426950408889634f;
-  p.acc_o = acc_o;
-  p.acc_lse2 = acc_lse2;
-  p.fold = fold;
+  PParams p = base_params(g, n_q, win_len, win_pos0, q_pos0, softmax_scale, acc_o, acc_lse2, fold);
   const long long tiles_total = (long long)p.n_tiles * g->n_kv_heads;
-  if (num_splits < 0 || num_splits > 1024) return fail(ARGUS_E_INVALID, "prefill: num_splits out of range");
   p.nsplit = resolve_splits(tiles_total, win_len, num_splits, ws != nullptr);
   if (p.nsplit > 65535) return fail(ARGUS_E_UNSUPPORTED, "prefill: too many splits");
   const bool f16p = ws != nullptr;
@@ -788,34 +1081,18 @@ extern "C" argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n
       p.ws_lse = p.ws_o + (size_t)tiles_total * p.nsplit * kBM * kD;
     }
     v16 = reinterpret_cast<uint16_t*>(w8 + split_bytes(tiles_total, p.nsplit));
-    vmax = reinterpret_cast<uint32_t*>(w8 + split_bytes(tiles_total, p.nsplit) + v16_bytes(g->n_kv_heads, win_len));
+    vmax = reinterpret_cast<uint32_t*>(w8 + split_bytes(tiles_total, p.nsplit) + win16_bytes(g->n_kv_heads, win_len));
     p.vmax_bits = vmax;
   }
   CUtensorMap mq, mk, mv;
-  const cuuint64_t qd[2] = {(cuuint64_t)kD, (cuuint64_t)g->n_q_heads * n_q};
-  const cuuint64_t qs[1] = {(cuuint64_t)kD * 2};
-  const long long wl = std::max<long long>(win_len, kBN);
-  const cuuint64_t kd[3] = {(cuuint64_t)kD, (cuuint64_t)wl, (cuuint64_t)g->n_kv_heads};
-  const cuuint64_t ks[2] = {(cuuint64_t)kD * 2, (cuuint64_t)stride * 2};
-  if (!make_map(&mq, q, 2, qd, qs)) return fail(ARGUS_E_LAUNCH, "prefill: tensor map for q failed");
-  if (!make_map(&mk, win_len > 0 ? k : q, 3, kd, ks)) return fail(ARGUS_E_LAUNCH, "prefill: tensor map for k failed");
-  if (f16p) {
-    const cuuint64_t vd[3] = {(cuuint64_t)kD, (cuuint64_t)wl, (cuuint64_t)g->n_kv_heads};
-    const cuuint64_t vs[2] = {(cuuint64_t)kD * 2, (cuuint64_t)wl * kD * 2};
-    if (!make_map(&mv, v16, 3, vd, vs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
-      return fail(ARGUS_E_LAUNCH, "prefill: tensor map for the fp16 v failed");
-  } else if (!make_map(&mv, win_len > 0 ? v : q, 3, kd, ks)) {
-    return fail(ARGUS_E_LAUNCH, "prefill: tensor map for v failed");
-  }
-  static PerContext configured;
-  argus_status sta = configured.ensure([](int) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "prefill: smem attribute: %s", cudaGetErrorString(e));
-    return ARGUS_OK;
-  });
-  if (sta != ARGUS_OK) return sta;
+  const void* kk = win_len > 0 ? k : q;
+  argus_status stm = f16p ? make_maps(&mq, &mk, &mv, q, (long long)g->n_q_heads * n_q, kk, v16, g->n_kv_heads, win_len,
+                                      stride, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                      CU_TENSOR_MAP_DATA_TYPE_FLOAT16, std::max<long long>(win_len, 1) * kD)
+                          : make_maps(&mq, &mk, &mv, q, (long long)g->n_q_heads * n_q, kk, win_len > 0 ? v : q,
+                                      g->n_kv_heads, win_len, stride, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                      CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, stride);
+  if (stm != ARGUS_OK) return stm;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (f16p) {
     // the window's V in fp16, scaled by 2^-e from its max |v|
@@ -830,12 +1107,107 @@ extern "C" argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n
       if (stc != ARGUS_OK) return stc;
     }
   }
-  dim3 grid(p.n_tiles, g->n_kv_heads, p.nsplit);
-  if (f16p) prefill_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
-  else prefill_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
-  argus_status st = launch_status("argus_window_prefill_attn");
-  if (st != ARGUS_OK || p.nsplit == 1) return st;
-  const long long n_rows = (long long)g->n_q_heads * n_q;
-  prefill_fold_kernel<<<(unsigned)((n_rows + kFoldWarps - 1) / kFoldWarps), 32 * kFoldWarps, 0, s>>>(p, n_rows);
-  return launch_status("argus_window_prefill_attn (fold)");
+  return launch_attention(f16p ? 1 : 0, mq, mk, mv, p, g->n_kv_heads, (long long)g->n_q_heads * n_q, s);
+}
+
+extern "C" argus_status argus_paged_window_prefill_workspace_bytes(const argus_geom* g, int32_t n_q, int64_t win_len,
+                                                                   int32_t num_splits, size_t* bytes) {
+  using namespace argus::prefill;
+  if (!bytes) return argus::fail(ARGUS_E_INVALID, "paged prefill: bytes is NULL");
+  argus_status st = check_geom(g, n_q, win_len);
+  if (st != ARGUS_OK) return st;
+  if (num_splits < 0 || num_splits > 1024) return argus::fail(ARGUS_E_INVALID, "prefill: num_splits out of range");
+  const long long tiles = tiles_per_head(g, n_q) * g->n_kv_heads;
+  *bytes = paged_ws(g, n_q, win_len, tiles, resolve_splits(tiles, win_len, num_splits, true)).total;
+  return ARGUS_OK;
+}
+
+extern "C" argus_status argus_paged_window_prefill_attn(const argus_geom* g, int32_t n_q, const void* q,
+                                                        const argus_pool* pools, int32_t n_pools,
+                                                        const uint8_t* page_codec, const int32_t* block_table,
+                                                        int32_t max_pages, int64_t win_pos0, int64_t win_len,
+                                                        int64_t q_pos0, float softmax_scale, float* acc_o,
+                                                        float* acc_lse2, int32_t fold, int32_t num_splits, void* ws,
+                                                        size_t ws_bytes, uint32_t* status, void* stream) {
+  using namespace argus;
+  using namespace argus::prefill;
+  argus_status st0 = common_args(g, n_q, win_len, softmax_scale, fold, num_splits);
+  if (st0 != ARGUS_OK) return st0;
+  if (g->page_tokens <= 0) return fail(ARGUS_E_INVALID, "paged prefill: page_tokens must be positive");
+  if (max_pages <= 0 || win_pos0 < 0 || win_pos0 + win_len > (long long)max_pages * g->page_tokens)
+    return fail(ARGUS_E_INVALID, "paged prefill: window [%lld, %lld) outside the %d pages of the table",
+                (long long)win_pos0, (long long)(win_pos0 + win_len), max_pages);
+  if (n_pools < 0 || n_pools > 6 || (n_pools > 0 && !pools)) return fail(ARGUS_E_INVALID, "paged prefill: bad pool list");
+  if (n_q == 0) return ARGUS_OK;
+  if (!q || !acc_o || !acc_lse2 || !ws || (win_len > 0 && (!page_codec || !block_table)))
+    return fail(ARGUS_E_INVALID, "paged prefill: NULL pointer");
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(acc_o) | reinterpret_cast<uintptr_t>(ws)) & 15)
+    return fail(ARGUS_E_INVALID, "paged prefill: q, acc_o and ws must be 16-byte aligned");
+  SParams sp{};
+  bool seen[6] = {false, false, false, false, false, false};
+  for (int i = 0; i < n_pools; ++i) {
+    const argus_pool& pool = pools[i];
+    if (pool.codec < 0 || pool.codec > ARGUS_INT2_G32 || seen[pool.codec] || pool.n_slots < 0)
+      return fail(ARGUS_E_INVALID, "paged prefill: pool %d (codec %d) invalid or repeated", i, pool.codec);
+    seen[pool.codec] = true;
+    if (pool.n_slots > 0) {
+      if (!pool.codes || (reinterpret_cast<uintptr_t>(pool.codes) & 15))
+        return fail(ARGUS_E_INVALID, "paged prefill: pool %d codes NULL or not 16-byte aligned", i);
+      if (pool.codec >= ARGUS_FP8_E4M3 && (!pool.meta || (reinterpret_cast<uintptr_t>(pool.meta) & 15)))
+        return fail(ARGUS_E_INVALID, "paged prefill: pool %d meta NULL or not 16-byte aligned", i);
+    }
+    sp.codes[pool.codec] = static_cast<const uint8_t*>(pool.codes);
+    sp.meta[pool.codec] = static_cast<const uint8_t*>(pool.meta);
+    sp.n_slots[pool.codec] = pool.n_slots;
+  }
+  PParams p = base_params(g, n_q, win_len, win_pos0, q_pos0, softmax_scale, acc_o, acc_lse2, fold);
+  const long long tiles_total = (long long)p.n_tiles * g->n_kv_heads;
+  p.nsplit = resolve_splits(tiles_total, win_len, num_splits, true);
+  if (p.nsplit > 65535) return fail(ARGUS_E_UNSUPPORTED, "prefill: too many splits");
+  const PagedWs L = paged_ws(g, n_q, win_len, tiles_total, p.nsplit);
+  if (ws_bytes < L.total) return fail(ARGUS_E_WORKSPACE, "paged prefill: workspace %zu < %zu", ws_bytes, L.total);
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  if (p.nsplit > 1) {
+    p.ws_o = reinterpret_cast<float*>(w8 + L.part);
+    p.ws_lse = p.ws_o + (size_t)tiles_total * p.nsplit * kBM * kD;
+  }
+  uint32_t* words = reinterpret_cast<uint32_t*>(w8 + L.words);
+  sp.Hkv = g->n_kv_heads;
+  sp.P = g->page_tokens;
+  sp.max_pages = max_pages;
+  sp.page_codec = page_codec;
+  sp.block_table = block_table;
+  sp.win_pos0 = win_pos0;
+  sp.win_len = win_len;
+  sp.n_vec = (long long)g->n_kv_heads * win_len * (kD / 8);
+  sp.k16 = reinterpret_cast<uint16_t*>(w8 + L.k16);
+  sp.v16 = reinterpret_cast<uint16_t*>(w8 + L.v16);
+  sp.kmax = words;
+  sp.vmax = words + 1;
+  sp.status = status;
+  sp.q = static_cast<const uint16_t*>(q);
+  sp.q16 = reinterpret_cast<uint16_t*>(w8 + L.q16);
+  sp.qfac = reinterpret_cast<float*>(w8 + L.qfac);
+  sp.q_rows = (long long)g->n_q_heads * n_q;
+  p.kmax_bits = sp.kmax;
+  p.vmax_bits = sp.vmax;
+  p.qfac = sp.qfac;
+  CUtensorMap mq, mk, mv;
+  const long long wl = std::max<long long>(win_len, 1);
+  argus_status stm = make_maps(&mq, &mk, &mv, sp.q16, sp.q_rows, sp.k16, sp.v16, g->n_kv_heads, win_len, wl * kD,
+                               CU_TENSOR_MAP_DATA_TYPE_FLOAT16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                               CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wl * kD);
+  if (stm != ARGUS_OK) return stm;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(words, 0, 16, s) != cudaSuccess) return fail(ARGUS_E_LAUNCH, "paged prefill: clearing the max words failed");
+  const int sms = device_sm_count();
+  if (win_len > 0) {
+    const int blocks = (int)std::max<long long>(1, std::min<long long>((sp.n_vec + 255) / 256, 8LL * sms));
+    stage_max_kernel<<<blocks, 256, 0, s>>>(sp);
+    stage_write_kernel<<<blocks, 256, 0, s>>>(sp);
+  }
+  stage_q_kernel<<<(unsigned)((sp.q_rows + 7) / 8), 256, 0, s>>>(sp);
+  argus_status stc = launch_status("argus_paged_window_prefill_attn (staging)");
+  if (stc != ARGUS_OK) return stc;
+  return launch_attention(2, mq, mk, mv, p, g->n_kv_heads, sp.q_rows, s);
 }

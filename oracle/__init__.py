@@ -43,5 +43,6 @@ from .codecs import (  # noqa: F401
 )
 from .attention import (  # noqa: F401
     softmax_attention, paged_decode, fold_lse, window_attention, visible_positions,
+    gather_window, paged_window_attention, staging_moves_less,
 )
 from .selection import compressed_key_scores, select_pages  # noqa: F401

@@ -208,3 +208,59 @@ def test_windowed_prefill_full_size_sampled_rows():
                 ro, rl = oracle.window_attention(qi, k64, v64, 0, CTX, W.softmax_scale(D), rows=[i])
                 assert np.abs(got_o[hq, r] - ro[0, 0]).max() <= _tol(ro), (hq, i)
                 assert abs(got_l[hq, r] - rl[0, 0]) <= 1e-4 * abs(rl[0, 0]) + 1e-5
+
+
+def test_paged_fp8_window_prefill_full_window_sampled_rows():
+    """The staged prefill at the full window size: 131,072 cached tokens in
+    64-token FP8 pages (random physical slots) plus the 1,024-token chunk in
+    BF16 pages, attended as two windows (the cache window, then the chunk) and
+    folded; sampled query rows against the oracle's gather of the same pages."""
+    Hq, Hkv, D, P, NQ, WIN = 16, 2, 128, 64, 1024, 131072
+    dev = torch.device(DEV)
+    n_cache, n_chunk = WIN // P, NQ // P
+    n_pages = n_cache + n_chunk
+    g = argus.geom(Hq, Hkv, D, P)
+    src = W.normal((n_pages, 2, Hkv, P, D), W.BF16, W.seed_of("prefill", 0, 1), device=dev)
+    perm = W.permutation(n_cache, W.seed_of("prefill", 0, 4))
+    fp8 = argus.Pool.empty(W.FP8_E4M3, n_cache, Hkv, P, D, device=dev)
+    bf = argus.Pool.empty(W.BF16, n_chunk, Hkv, P, D, device=dev)
+    ids = torch.arange(n_pages, dtype=torch.int32, device=dev)
+    argus.quantize_pages(g, W.BF16, src, n_pages, ids[:n_cache], fp8, torch.from_numpy(perm.astype(np.int32)).to(dev),
+                         n_cache)
+    argus.quantize_pages(g, W.BF16, src, n_pages, ids[n_cache:], bf, ids[:n_chunk], n_chunk)
+    table = np.concatenate([perm, np.arange(n_chunk)]).astype(np.int32)
+    codecs = np.array([W.FP8_E4M3] * n_cache + [W.BF16] * n_chunk, np.uint8)
+    q = W.normal((Hq, NQ, D), W.BF16, W.seed_of("prefill", 0, 0), device=dev)
+    acc_o = torch.empty((Hq, NQ, D), dtype=torch.float32, device=dev)
+    acc_l = torch.empty((Hq, NQ), dtype=torch.float32, device=dev)
+    d_codec, d_table = torch.from_numpy(codecs).to(dev), torch.from_numpy(table).to(dev)
+    for i, (w0, wl) in enumerate([(0, WIN), (WIN, NQ)]):
+        ws = torch.empty(argus.paged_window_prefill_workspace_bytes(g, NQ, wl), dtype=torch.uint8, device=dev)
+        argus.paged_window_prefill_attn(g, NQ, q, [fp8, bf], d_codec, d_table, n_pages, w0, wl, WIN,
+                                        W.softmax_scale(D), acc_o, acc_l, 1 if i else 0, ws)
+        del ws
+    torch.cuda.synchronize()
+    # the oracle demotes the same source pages itself and gathers the window
+    src_bits = W.to_bits(src)
+    codes, meta = C.alloc_pool(W.FP8_E4M3, n_cache, Hkv, P, D)
+    C.quantize_pages(src_bits, C.CODEC_BF16, list(range(n_cache)), W.FP8_E4M3, codes, meta, [int(x) for x in perm])
+    bcodes, _ = C.alloc_pool(W.BF16, n_chunk, Hkv, P, D)
+    C.quantize_pages(src_bits, C.CODEC_BF16, list(range(n_cache, n_pages)), W.BF16, bcodes, None, list(range(n_chunk)))
+    pools = {W.FP8_E4M3: (codes, meta), W.BF16: (bcodes, None)}
+    rows = [0, 1, 511, NQ - 1]
+    q64 = C.bf16_bits_to_f64(W.to_bits(q))
+    qs = np.zeros((Hq, NQ, D))
+    qs[:, rows] = q64[:, rows]
+    ro, rl = oracle.paged_window_attention(qs, Hkv, P, pools, codecs[None], table[None], 0, 0, WIN + NQ, WIN,
+                                           W.softmax_scale(D), rows=rows, seq_len=WIN + NQ)
+    got_o = acc_o[:, rows].cpu().numpy()
+    got_l = acc_l[:, rows].cpu().numpy()
+    assert np.abs(got_o - ro).max() <= _tol(ro)
+    # lse2 within the staged window's bound: each key rounded to fp16 moves a
+    # log2 score by <= scale * log2(e) * 2^-11 * sum_d |q_d k_d|; bound it with
+    # Cauchy-Schwarz by |q| * max_j |k_j|
+    K, _ = oracle.gather_window(Hkv, P, pools, codecs[None], table[None], 0, 0, WIN + NQ)
+    kmax = np.sqrt((K ** 2).sum(axis=2)).max(axis=1)                         # [Hkv]
+    qn = np.sqrt((q64[:, rows] ** 2).sum(axis=2))                           # [Hq][rows]
+    bound = W.softmax_scale(D) / math.log(2) * 2.0 ** -11 * qn * np.repeat(kmax, Hq // Hkv)[:, None]
+    assert np.all(np.abs(got_l - rl) <= bound + 1e-5 * np.abs(rl) + 1e-5)
