@@ -83,11 +83,26 @@ typedef struct {
   int32_t page_tokens;  /* P */
 } argus_geom;
 
+/* Where a pool's pages live ([PR499] "Design" and the comment on
+ * "--kv-placement host": a host-RAM tier whose pages attention reads in place).
+ * ARGUS_PLACE_HOST: codes and meta are HOST pointers into page-locked memory
+ * (cudaHostAlloc / cudaMallocHost / cudaHostRegister) that the device can map;
+ * decode reads the selected pages in place over the host link, with plain
+ * 16-byte loads, without staging them into device memory.  Accepted by
+ * argus_paged_decode_attn (not together with a sliding window or an INT2 pool:
+ * ARGUS_E_UNSUPPORTED), argus_paged_window_prefill_attn (staged from host
+ * memory) and as the destination of argus_quantize_pages (demotion into the
+ * host tier).  Host memory the device cannot map is ARGUS_E_INVALID. */
+typedef enum {
+  ARGUS_PLACE_DEVICE = 0,
+  ARGUS_PLACE_HOST = 1
+} argus_placement;
+
 typedef struct {
   int32_t codec;        /* argus_codec of every page in this pool */
-  int32_t reserved;     /* must be 0 */
-  void* codes;          /* device, layout above */
-  void* meta;           /* device, layout above; NULL for FP16 / BF16 */
+  int32_t placement;    /* argus_placement: ARGUS_PLACE_DEVICE (0) or ARGUS_PLACE_HOST */
+  void* codes;          /* layout above; device memory, or host memory for ARGUS_PLACE_HOST */
+  void* meta;           /* layout above; NULL for FP16 / BF16 */
   int64_t n_slots;      /* physical page slots in the pool */
 } argus_pool;
 

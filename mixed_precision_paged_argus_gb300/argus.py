@@ -32,8 +32,11 @@ class Geom(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("page_tokens", ctypes.c_int32)]
 
 
+PLACE_DEVICE, PLACE_HOST = 0, 1
+
+
 class PoolDesc(ctypes.Structure):
-    _fields_ = [("codec", ctypes.c_int32), ("reserved", ctypes.c_int32),
+    _fields_ = [("codec", ctypes.c_int32), ("placement", ctypes.c_int32),
                 ("codes", ctypes.c_void_p), ("meta", ctypes.c_void_p),
                 ("n_slots", ctypes.c_int64)]
 
@@ -138,17 +141,33 @@ def geom(n_q_heads, n_kv_heads, head_dim, page_tokens):
 
 
 class Pool:
-    """A physical page pool of one codec: codes (and meta) device tensors."""
+    """A physical page pool of one codec: codes (and meta) tensors, on the
+    device, or in page-locked host memory (placement PLACE_HOST: read in place
+    by decode over the host link)."""
 
-    def __init__(self, codec, codes, meta, n_slots):
+    def __init__(self, codec, codes, meta, n_slots, placement=None):
         self.codec, self.codes, self.meta, self.n_slots = codec, codes, meta, int(n_slots)
+        if placement is None:
+            placement = PLACE_HOST if (codes is not None and not codes.is_cuda) else PLACE_DEVICE
+        self.placement = placement
 
     def desc(self):
-        return PoolDesc(self.codec, 0, _ptr(self.codes), _ptr(self.meta), self.n_slots)
+        return PoolDesc(self.codec, self.placement, _ptr(self.codes), _ptr(self.meta), self.n_slots)
+
+    def to_host(self):
+        """A copy of this pool in page-locked host memory (PLACE_HOST)."""
+        codes = self.codes.cpu().pin_memory()
+        meta = None if self.meta is None else self.meta.cpu().pin_memory()
+        return Pool(self.codec, codes, meta, self.n_slots, PLACE_HOST)
 
     @staticmethod
     def empty(codec, n_slots, n_kv_heads, page_tokens, head_dim, device="cuda", zero=False):
-        """Allocate a pool in the layout of include/argus.h."""
+        """Allocate a pool in the layout of include/argus.h (device="host":
+        page-locked host memory)."""
+        if str(device) == "host":
+            p = Pool.empty(codec, n_slots, n_kv_heads, page_tokens, head_dim, device="cpu", zero=zero)
+            return Pool(codec, p.codes.pin_memory(), None if p.meta is None else p.meta.pin_memory(), n_slots,
+                        PLACE_HOST)
         alloc = torch.zeros if zero else torch.empty
         shape = (n_slots, 2, n_kv_heads, page_tokens)
         if codec in (FP16, BF16):

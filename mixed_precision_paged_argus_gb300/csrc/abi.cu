@@ -34,6 +34,35 @@ int device_sm_count() {
   return n > 0 ? n : 1;
 }
 
+argus_status pool_device_ptrs(const argus_pool& pool, const void** codes, const void** meta) {
+  *codes = pool.codes;
+  *meta = pool.meta;
+  if (pool.placement == ARGUS_PLACE_DEVICE) return ARGUS_OK;
+  if (pool.placement != ARGUS_PLACE_HOST) return fail(ARGUS_E_INVALID, "pool placement %d unknown", pool.placement);
+  if (pool.n_slots == 0) return ARGUS_OK;
+  // page-locked (allocated or registered with CUDA) host memory only: pageable
+  // memory is refused even where the platform could reach it
+  auto pinned = [](const void* ptr) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    return at.type == cudaMemoryTypeHost;
+  };
+  void* dc = nullptr;
+  void* dm = nullptr;
+  if (!pool.codes || !pinned(pool.codes) || (pool.meta && !pinned(pool.meta)) ||
+      cudaHostGetDevicePointer(&dc, pool.codes, 0) != cudaSuccess ||
+      (pool.meta && cudaHostGetDevicePointer(&dm, pool.meta, 0) != cudaSuccess)) {
+    cudaGetLastError();   // clear the (non-sticky) error of a failed query
+    return fail(ARGUS_E_INVALID, "host pool (codec %d) is not page-locked memory the device can map", pool.codec);
+  }
+  *codes = dc;
+  *meta = dm;
+  return ARGUS_OK;
+}
+
 // The driver's cuCtxGetCurrent / cuCtxGetId, reached through the runtime's
 // entry-point query so that the library links against the runtime only.
 unsigned long long context_id() {

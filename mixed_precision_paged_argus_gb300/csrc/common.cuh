@@ -22,6 +22,11 @@ argus_status fail(argus_status s, const char* fmt, ...);
 argus_status launch_status(const char* what);
 int device_sm_count();
 
+// Device address of a pool's codes and meta: device pools as given; host pools
+// (ARGUS_PLACE_HOST, page-locked) through cudaHostGetDevicePointer.  Returns
+// ARGUS_E_INVALID for an unknown placement or host memory the device cannot map.
+argus_status pool_device_ptrs(const argus_pool& pool, const void** codes, const void** meta);
+
 // Identifier of the calling thread's current CUDA context, unique for the life
 // of the process; 0 when no context is current or the driver cannot say.
 unsigned long long context_id();

@@ -67,6 +67,7 @@ struct Params {
   const uint8_t* codes[6];   // indexed by argus_codec
   const uint8_t* meta[6];
   long long n_slots[6];
+  uint32_t host_mask;        // bit c: the pool of codec c lives in host memory
   const uint8_t* page_codec;
   const int32_t* block_table;
   const int32_t* seq_lens;
@@ -94,6 +95,13 @@ struct ChunkDesc {
                   // the number of leading visible rows
   float kscale;
   float vscale;
+  // a page of a pool in host memory: the chunk's K and V rows (and INT4 / INT2
+  // metadata), read in place by the consuming warp; null for device pages,
+  // which the producer copies into the stage
+  const uint8_t* hk;
+  const uint8_t* hv;
+  const uint8_t* hmk;
+  const uint8_t* hmv;
 };
 
 // Dense chunk list of one sequence of seq_len tokens.  Without a window every
@@ -499,7 +507,47 @@ __device__ __forceinline__ void group_pv(const uint8_t* const* cptr, int r, int 
   }
 }
 
-template <int D, bool QBF16, int FAM, bool NARROW, bool EXT>
+// A chunk of a page in host memory, copied into its stage slot by the warp that
+// consumes it: K and V rows (16 x row bytes each) as one run of 16-byte vectors
+// over the lanes, eight loads per lane in flight before their stores, then the
+// INT4 / INT2 group metadata.  Plain loads: the pages are read in place over
+// the host link.
+template <int D, bool NARROW>
+__device__ __forceinline__ void copy_host_chunk(const ChunkDesc& d, uint8_t* slot, int lane) {
+  using L = Layout<D, NARROW>;
+  const int rowb = (d.codec <= ARGUS_BF16) ? 2 * D
+                 : (d.codec == ARGUS_INT4_G32 ? D / 2 : (d.codec == ARGUS_INT2_G32 ? D / 4 : D));
+  const int n16 = kChunk * rowb / 16;          // 16-byte vectors of K (and of V)
+  const uint4* srcK = reinterpret_cast<const uint4*>(d.hk);
+  const uint4* srcV = reinterpret_cast<const uint4*>(d.hv);
+  uint4* dstK = reinterpret_cast<uint4*>(slot + L::kOffK);
+  uint4* dstV = reinterpret_cast<uint4*>(slot + L::kOffV);
+  for (int base = 0; base < 2 * n16; base += 32 * 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int idx = base + lane + 32 * i;
+      if (idx < 2 * n16) v[i] = idx < n16 ? srcK[idx] : srcV[idx - n16];
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int idx = base + lane + 32 * i;
+      if (idx < n16) dstK[idx] = v[i];
+      else if (idx < 2 * n16) dstV[idx - n16] = v[i];
+    }
+  }
+  if (d.hmk) {
+    constexpr int m16 = kChunk * L::kNI * 4 / 16;   // 16-byte vectors of one side's metadata
+    if (lane < 2 * m16) {
+      const int side = lane / m16, idx = lane - side * m16;
+      const uint4 x = reinterpret_cast<const uint4*>(side ? d.hmv : d.hmk)[idx];
+      reinterpret_cast<uint4*>(slot + (side ? L::kOffMV : L::kOffMK))[idx] = x;
+    }
+  }
+}
+
+// HOSTOK: some pools live in host memory (see copy_host_chunk).
+template <int D, bool QBF16, int FAM, bool NARROW, bool EXT, bool HOSTOK = false>
 __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>::kMinBlocks)
     decode_kernel(const Params p) {
   constexpr int kConsumerWarps = Warps<D, NARROW>::kConsumer;
@@ -632,6 +680,7 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
       d.vmask = 0;
       d.kscale = 1.f;
       d.vscale = 1.f;
+      d.hk = d.hv = d.hmk = d.hmv = nullptr;
       uint32_t kv_bytes = 0, m_bytes = 0;
       const uint8_t *srcK = nullptr, *srcV = nullptr, *srcMK = nullptr, *srcMV = nullptr;
       if (base + lane < n_local) {
@@ -675,7 +724,15 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
                 srcMK = p.meta[codec] + rk * (L::kNI * 4);
                 srcMV = p.meta[codec] + rv * (L::kNI * 4);
                 m_bytes = kChunk * L::kNI * 4;
-              } else if (codec == ARGUS_FP8_E4M3 || codec == ARGUS_INT8) {
+              }
+              if (HOSTOK && ((p.host_mask >> codec) & 1u)) {   // read in place by the consumer
+                d.hk = srcK;
+                d.hv = srcV;
+                d.hmk = srcMK;
+                d.hmv = srcMV;
+                kv_bytes = m_bytes = 0;
+              }
+              if (codec == ARGUS_FP8_E4M3 || codec == ARGUS_INT8) {
                 const float* ms = reinterpret_cast<const float*>(p.meta[codec]);
                 d.kscale = ms[((size_t)slot_id * 2 + 0) * Hkv + h];
                 d.vscale = ms[((size_t)slot_id * 2 + 1) * Hkv + h];
@@ -854,6 +911,14 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
       dsc[c] = descs[slot * kChunksPerStage + warp * kNC + c];
       cptr[c] = smem + slot * L::kStageBytes + (warp * kNC + c) * L::kChunkBytes;
       any |= dsc[c].codec >= 0;
+    }
+    if constexpr (HOSTOK) {
+      if (alive) {
+#pragma unroll
+        for (int c = 0; c < kNC; ++c)
+          if (dsc[c].codec >= 0 && dsc[c].hk) copy_host_chunk<D, NARROW>(dsc[c], const_cast<uint8_t*>(cptr[c]), lane);
+        __syncwarp();
+      }
     }
     if (alive && any) {
       // ---- scores S^T[token][head] = K . q; a group whose chunks share one
@@ -1206,6 +1271,7 @@ struct Plan {
   int D, G, cps, num_splits, fam;
   bool q_bf16, narrow;
   bool ext;   // extended kernels: a sliding window or an INT2 pool
+  bool host;  // some pool lives in host memory
   size_t part_o_bytes, ws_bytes;
 };
 
@@ -1242,6 +1308,8 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
   for (int i = 0; i < a->n_pools; ++i) {
     const argus_pool& pool = a->pools[i];
     if (pool.codec < 0 || pool.codec > ARGUS_INT2_G32) return fail(ARGUS_E_INVALID, "decode: pool %d has codec %d", i, pool.codec);
+    if (pool.placement != ARGUS_PLACE_DEVICE && pool.placement != ARGUS_PLACE_HOST)
+      return fail(ARGUS_E_INVALID, "decode: pool %d has placement %d", i, pool.placement);
     if (seen[pool.codec]) return fail(ARGUS_E_INVALID, "decode: two pools with codec %d", pool.codec);
     seen[pool.codec] = true;
     if (pool.n_slots < 0) return fail(ARGUS_E_INVALID, "decode: pool %d n_slots < 0", i);
@@ -1263,6 +1331,10 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
   pl->G = G;
   // narrow ring: every pool holds byte or nibble codes, head_dim 128
   pl->ext = a->window_tokens > 0 || seen[ARGUS_INT2_G32];
+  pl->host = false;
+  for (int i = 0; i < a->n_pools; ++i) pl->host |= a->pools[i].placement == ARGUS_PLACE_HOST;
+  if (pl->host && pl->ext)
+    return fail(ARGUS_E_UNSUPPORTED, "decode: host-memory pools with a sliding window or an INT2 pool");
   pl->narrow = g.head_dim == 128 && !has_bf16 && !seen[ARGUS_FP16] && a->n_pools > 0 && !pl->ext;
   const long long cps_unit = pl->narrow ? chunks_per_stage<true>() : kChunksPerStage;
   const int cpp = g.page_tokens / kChunk;
@@ -1300,12 +1372,12 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
   return ARGUS_OK;
 }
 
-template <int D, bool QBF16, int FAM, bool NARROW, bool EXT>
+template <int D, bool QBF16, int FAM, bool NARROW, bool EXT, bool HOSTOK = false>
 static argus_status launch_t(const Params& p, dim3 grid, cudaStream_t s) {
   using L = Layout<D, NARROW>;
   static PerContext configured;
   argus_status st = configured.ensure([](int) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, QBF16, FAM, NARROW, EXT>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, QBF16, FAM, NARROW, EXT, HOSTOK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "decode: smem attribute: %s", cudaGetErrorString(e));
     return ARGUS_OK;
@@ -1321,7 +1393,7 @@ static argus_status launch_t(const Params& p, dim3 grid, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<D, QBF16, FAM, NARROW, EXT>, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<D, QBF16, FAM, NARROW, EXT, HOSTOK>, p);
   if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "argus_paged_decode_attn: %s", cudaGetErrorString(e));
   if (p.num_splits > 1) {
     cudaLaunchConfig_t fc = cfg;
@@ -1338,6 +1410,10 @@ static argus_status launch_t(const Params& p, dim3 grid, cudaStream_t s) {
 
 template <int D>
 static argus_status launch_d(const Params& p, const Plan& pl, dim3 grid, cudaStream_t s) {
+  if (pl.host) {   // pools in host memory: the wide ring, one kernel per query type
+    if (!pl.q_bf16) return launch_t<D, false, kFamMixed, false, false, true>(p, grid, s);
+    return launch_t<D, true, kFamMixed, false, false, true>(p, grid, s);
+  }
   if (pl.ext) {   // sliding window or INT2 pages: the wide ring, one kernel per query type
     if (!pl.q_bf16) return launch_t<D, false, kFamF16, false, true>(p, grid, s);
     return launch_t<D, true, kFamMixed, false, true>(p, grid, s);
@@ -1393,11 +1469,21 @@ static argus_status run(const argus_decode_args* a, const Plan& pl, void* ws, vo
     p.meta[c] = nullptr;
     p.n_slots[c] = 0;
   }
+  p.host_mask = 0;
   for (int i = 0; i < a->n_pools; ++i) {
     const argus_pool& pool = a->pools[i];
     p.codes[pool.codec] = static_cast<const uint8_t*>(pool.codes);
     p.meta[pool.codec] = static_cast<const uint8_t*>(pool.meta);
     p.n_slots[pool.codec] = pool.n_slots;
+    if (pool.placement == ARGUS_PLACE_HOST) {   // page-locked host memory: the device's address of it
+      const void* dc = nullptr;
+      const void* dm = nullptr;
+      const argus_status st = pool_device_ptrs(pool, &dc, &dm);
+      if (st != ARGUS_OK) return st;
+      p.codes[pool.codec] = static_cast<const uint8_t*>(dc);
+      p.meta[pool.codec] = static_cast<const uint8_t*>(dm);
+      p.host_mask |= 1u << pool.codec;
+    }
   }
   p.page_codec = a->page_codec;
   p.block_table = a->block_table;

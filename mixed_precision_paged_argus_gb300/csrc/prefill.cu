@@ -1156,8 +1156,13 @@ extern "C" argus_status argus_paged_window_prefill_attn(const argus_geom* g, int
       if (pool.codec >= ARGUS_FP8_E4M3 && (!pool.meta || (reinterpret_cast<uintptr_t>(pool.meta) & 15)))
         return fail(ARGUS_E_INVALID, "paged prefill: pool %d meta NULL or not 16-byte aligned", i);
     }
-    sp.codes[pool.codec] = static_cast<const uint8_t*>(pool.codes);
-    sp.meta[pool.codec] = static_cast<const uint8_t*>(pool.meta);
+    // host pools are staged from host memory with the same plain loads
+    const void* dc = nullptr;
+    const void* dm = nullptr;
+    const argus_status stp = pool_device_ptrs(pool, &dc, &dm);
+    if (stp != ARGUS_OK) return stp;
+    sp.codes[pool.codec] = static_cast<const uint8_t*>(dc);
+    sp.meta[pool.codec] = static_cast<const uint8_t*>(dm);
     sp.n_slots[pool.codec] = pool.n_slots;
   }
   PParams p = base_params(g, n_q, win_len, win_pos0, q_pos0, softmax_scale, acc_o, acc_lse2, fold);

@@ -757,8 +757,13 @@ extern "C" argus_status argus_quantize_pages(const argus_geom* g, int32_t src_dt
   p.src_slots = src_slots;
   p.dst_slots = dst_slots;
   p.valid_tokens = valid_tokens;
-  p.dst_codes = static_cast<uint8_t*>(dst->codes);
-  p.dst_meta = static_cast<uint8_t*>(dst->meta);
+  // a destination pool in host memory (the host tier) is written in place
+  const void* dcodes = nullptr;
+  const void* dmeta = nullptr;
+  argus_status stp = pool_device_ptrs(*dst, &dcodes, &dmeta);
+  if (stp != ARGUS_OK) return stp;
+  p.dst_codes = static_cast<uint8_t*>(const_cast<void*>(dcodes));
+  p.dst_meta = static_cast<uint8_t*>(const_cast<void*>(dmeta));
   p.n_dst = dst->n_slots;
   p.ckey = static_cast<uint16_t*>(ckey_out);
   p.status = status;
