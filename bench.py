@@ -782,6 +782,150 @@ def oracle_leg(budget_s=15.0):
             "single_core_us_per_token_layer": per_layer * 1e6}
 
 
+# ---------------------------------------------------------------- oracle per leg
+# The oracle (float64, plain numpy) timed on the host cores for each of the
+# other workloads, as a reported baseline beside the GPU legs.  Every job builds
+# its own seeded inputs of the workload's shape on the CPU; only the steps the
+# GPU leg times are timed (demotion of the pools is set-up, not part of a
+# decode step).  Jobs are top-level functions for a spawned process pool.
+
+def _cpu_tiny(reps):
+    """Single-threaded: the tiny FP16 decode, `reps` times."""
+    import oracle
+    from oracle import codecs as C
+    from mixed_precision_paged_argus_gb300 import workloads as W
+    Hq, Hkv, D_, P_ = 14, 2, 64, 1024
+    src = W.to_bits(W.normal((4, 2, Hkv, P_, D_), W.FP16, W.seed_of("tiny_fp16", 0, 1)))
+    q64 = C.f16_bits_to_f64(W.to_bits(W.normal((1, Hq, D_), W.FP16, W.seed_of("tiny_fp16", 0, 0))))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.paged_decode(q64, Hkv, P_, {0: (src, None)}, np.zeros((1, 4), np.uint8),
+                            np.arange(4, dtype=np.int32)[None], np.array([4096]), W.softmax_scale(D_))
+    return (time.perf_counter() - t0) / reps
+
+
+def _cpu_batched_row(job):
+    """One sequence of the batched workload (BF16 pages, or demoted to FP8
+    first, untimed): seconds of the oracle's decode of that row."""
+    b, codec = job
+    import oracle
+    from oracle import codecs as C
+    from mixed_precision_paged_argus_gb300 import workloads as W
+    Hq, Hkv, D_, P_ = 32, 8, 128, 16
+    L = int(W.uniform_ints(32, 8192, 32768, W.seed_of("batched", 0, 3))[b])
+    n = (L + P_ - 1) // P_
+    src = W.to_bits(W.normal((n, 2, Hkv, P_, D_), W.BF16, W.seed_of("batched", b, 1) * 64 + 7))
+    q64 = C.bf16_bits_to_f64(W.to_bits(W.normal((1, Hq, D_), W.BF16, W.seed_of("batched", b, 0) * 64 + 7)))
+    if codec == C.CODEC_BF16:
+        pools = {codec: (src, None)}
+    else:
+        codes, meta = C.alloc_pool(codec, n, Hkv, P_, D_)
+        C.quantize_pages(src, C.CODEC_BF16, list(range(n)), codec, codes, meta, list(range(n)))
+        pools = {codec: (codes, meta)}
+    t0 = time.perf_counter()
+    oracle.paged_decode(q64, Hkv, P_, pools, np.full((1, n), codec, np.uint8), np.arange(n, dtype=np.int32)[None],
+                        np.array([L]), W.softmax_scale(D_))
+    return time.perf_counter() - t0
+
+
+def _cpu_sparse_task(job):
+    """One (layer, sequence) of the sparse workload: indexer scores over the
+    4096 compressed keys, top-32 + newest selection, decode over the selected
+    FP8 pages.  Timed: scores, selection and decode (the selected pages'
+    codes are demoted beforehand, untimed)."""
+    layer, b = job
+    import oracle
+    from oracle import codecs as C
+    from mixed_precision_paged_argus_gb300 import workloads as W
+    Hq, Hkv, D_, P_, NP, K_ = 32, 4, 128, 64, 4096, 32
+    width = 2 * K_ + 8
+    ck = W.to_bits(W.normal((1, NP, Hkv, D_), W.BF16, W.seed_of("sparse", layer, 6) * 16 + b))
+    q64 = C.bf16_bits_to_f64(W.to_bits(W.normal((1, Hq, D_), W.BF16, W.seed_of("sparse", layer, 0) * 16 + b)))
+    # the pool: only the pages a selection can name are materialised (demoted)
+    t0 = time.perf_counter()
+    sel, cnt, _ = oracle.select_pages(q64, ck, [NP], Hkv, K_, True, width)
+    t_sel = time.perf_counter() - t0
+    pages = sorted(set(int(x) for x in sel[0].ravel() if x >= 0))
+    slot_of = {p: i for i, p in enumerate(pages)}
+    src = W.to_bits(W.normal((len(pages), 2, Hkv, P_, D_), W.BF16, W.seed_of("sparse", layer, 1) * 16 + b))
+    codes, meta = C.alloc_pool(C.CODEC_FP8_E4M3, len(pages), Hkv, P_, D_)
+    C.quantize_pages(src, C.CODEC_BF16, list(range(len(pages))), C.CODEC_FP8_E4M3, codes, meta,
+                     list(range(len(pages))))
+    table = np.zeros((1, NP), np.int32)
+    for p_, i in slot_of.items():
+        table[0, p_] = i
+    t1 = time.perf_counter()
+    oracle.paged_decode(q64, Hkv, P_, {C.CODEC_FP8_E4M3: (codes, meta)}, np.full((1, NP), C.CODEC_FP8_E4M3, np.uint8),
+                        table, np.array([NP * P_]), W.softmax_scale(D_), sel_pages=sel, sel_count=cnt,
+                        sel_width=width)
+    return t_sel + (time.perf_counter() - t1)
+
+
+def _cpu_prefill_row(job):
+    """One query row of the windowed prefill: its attention against each of the
+    eight 131072-token windows of the cache and the chunk window, folded by
+    log2-sum-exp (the oracle's window_attention and fold_lse).  Seconds."""
+    hq, i = job
+    import oracle
+    from oracle import codecs as C
+    from mixed_precision_paged_argus_gb300 import workloads as W
+    NQ, CTX, WIN, D_ = 1024, 1 << 20, 131072, 128
+    q = np.zeros((1, NQ, D_))
+    q[0, i] = C.bf16_bits_to_f64(W.to_bits(W.normal((D_,), W.BF16, W.seed_of("prefill", hq, 0) * 1024 + i)))
+    acc_o, acc_l = None, None
+    spent = 0.0
+    for w0, wl in [(w, WIN) for w in range(0, CTX, WIN)] + [(CTX, NQ)]:
+        k = C.bf16_bits_to_f64(W.to_bits(W.normal((1, wl, D_), W.BF16, W.seed_of("prefill", hq, 1) * 64 + w0 // WIN)))
+        v = C.bf16_bits_to_f64(W.to_bits(W.normal((1, wl, D_), W.BF16, W.seed_of("prefill", hq, 2) * 64 + w0 // WIN)))
+        t0 = time.perf_counter()
+        o, l = oracle.window_attention(q, k, v, w0, CTX, W.softmax_scale(D_), rows=[i])
+        acc_o, acc_l = (o, l) if acc_o is None else oracle.fold_lse(acc_o, acc_l, o, l)
+        spent += time.perf_counter() - t0
+    return spent
+
+
+def cpu_legs():
+    """The oracle's time for the tiny (one core), batched, sparse and prefill
+    workloads; returns {leg: cpu_baseline dict}."""
+    import multiprocessing as mp
+    from oracle import codecs as C
+    cores = os.cpu_count() or 1
+    out = {}
+    per = _cpu_tiny(1)
+    reps = max(1, int(2.0 / max(per, 1e-4)))
+    per = _cpu_tiny(reps)
+    out["tiny_fp16"] = {"value": per * 1e6, "unit": "us/step", "cores": 1, "kind": "oracle",
+                        "sample": "%d full steps (the whole workload), single-threaded" % reps}
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores) as pool:
+        for name, codec in (("decode_bf16", C.CODEC_BF16), ("decode_fp8", C.CODEC_FP8_E4M3)):
+            t0 = time.perf_counter()
+            secs = pool.map(_cpu_batched_row, [(b, codec) for b in range(32)])
+            wall = time.perf_counter() - t0
+            out["batched_" + name] = {
+                "value": sum(secs) / cores * 1e6, "unit": "us/step", "cores": cores, "kind": "oracle",
+                "sample": "one full step (all 32 sequences) in %d processes; value = summed decode seconds / cores "
+                          "(%.1f s wall incl. input generation%s)" % (cores, wall,
+                                                                      ", FP8 demotion untimed" if codec else "")}
+        t0 = time.perf_counter()
+        secs = pool.map(_cpu_sparse_task, [(l, b) for l in range(12) for b in range(8)])
+        wall = time.perf_counter() - t0
+        out["sparse"] = {"value": sum(secs) / cores * 1e6, "unit": "us/step", "cores": cores, "kind": "oracle",
+                         "sample": "one full step (12 layers x 8 sequences: scores, top-k, decode over the selected "
+                                   "FP8 pages; their demotion untimed) in %d processes (%.1f s wall)" % (cores, wall)}
+        rows = [(hq, i) for hq in (0, 9) for i in (0, 1, 511, 1023)]
+        t0 = time.perf_counter()
+        secs = pool.map(_cpu_prefill_row, rows)
+        wall = time.perf_counter() - t0
+        per_row = sum(secs) / len(rows)
+        out["prefill"] = {"value": per_row * 16 * 1024 / cores * 1e3, "unit": "ms/step (extrapolated)", "cores": cores,
+                          "kind": "oracle",
+                          "sample": "EXTRAPOLATED: %d sampled query rows (heads 0 and 9; rows 0, 1, 511, 1023), each "
+                                    "against all nine windows and folded; mean %.3f s per row x 16384 rows / %d "
+                                    "cores (%.1f s wall)" % (len(rows), per_row, cores, wall)}
+    return out
+
+
 # ---------------------------------------------------------------- main
 
 def main():
@@ -817,8 +961,11 @@ def main():
         import torch
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     cpu = None
+    cpu_leg = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_leg()                         # before the first GPU call (spawned pool)
+        if not args.no_legs:
+            cpu_leg = cpu_legs()
     ms_step, ms_e2e, clocks, t_wall, h2d, d2h = run_gpu(args, rank, world)
     legs = None
     if rank == 0 and not args.no_legs:
@@ -859,6 +1006,15 @@ def main():
     if cpu is not None:
         line["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
     if legs is not None:
+        if cpu_leg:
+            # each leg's oracle time beside it
+            for key, cb in cpu_leg.items():
+                if key.startswith("batched_"):
+                    target = legs.get("batched", {}).get(key[len("batched_"):])
+                else:
+                    target = legs.get(key)
+                if isinstance(target, dict):
+                    target["cpu_baseline"] = cb
         line["legs"] = legs
     print(json.dumps(line))
 
