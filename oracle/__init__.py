@@ -11,7 +11,7 @@ It follows three web pages:
   sections "Why decode is slow" and "Direct paged attention": codec tiers,
   an exact online softmax over one page at a time with grouped-query
   attention, a structure-of-arrays page table; "Pluggable tiers" (the INT2
-  tier as unsigned_affine with bits = 2) and "v0.5: model-independent KV
+  and 1-bit tiers as unsigned_affine with bits = 2 and bits = 1) and "v0.5: model-independent KV
   placement" with the "HuggingFace example" (sliding-window masks, sink
   tokens).
 * "feat(kvcache): host-RAM KV tier for sparse-attention models" (FreeToken
@@ -36,10 +36,10 @@ invariance), closed-form special cases, or numbers printed on the pages.
 """
 
 from .codecs import (  # noqa: F401
-    CODEC_FP16, CODEC_BF16, CODEC_FP8_E4M3, CODEC_INT8, CODEC_INT4_G32, CODEC_INT2_G32,
+    CODEC_FP16, CODEC_BF16, CODEC_FP8_E4M3, CODEC_INT8, CODEC_INT4_G32, CODEC_INT2_G32, CODEC_INT1_G32,
     e4m3_value, e4m3_table, e4m3_encode, f16_bits_to_f64, bf16_bits_to_f64,
     round_to_bf16, f64_to_bf16_bits, quantize_unit_fp8, quantize_unit_int8,
-    quantize_group_int4, quantize_group_int2, quantize_pages, dequant_page,
+    quantize_group_int4, quantize_group_int2, quantize_group_int1, quantize_pages, dequant_page,
 )
 from .attention import (  # noqa: F401
     softmax_attention, paged_decode, fold_lse, window_attention, visible_positions,

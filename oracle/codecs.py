@@ -25,6 +25,10 @@ out; the readings taken here (all listed in the design notes) are:
   NativeCodecSpec(kind="unsigned_affine", bits=2)), i.e. 3 in place of 15:
   s = fp16_sat(fp32(fp32(hi - z) / 3)), q = clamp(rint_even(...), 0, 3); four
   codes per byte, element 4k + j in bits 2j, 2j + 1 of byte k.
+* 1-bit with 32-element groups (the summary's 1-bit tier): the same encoder
+  with bits = 1, i.e. 1 in place of 15: s = fp16_sat(fp32(fp32(hi - z) / 1)) =
+  fp16_sat(hi - z), q = clamp(rint_even(fp32(fp32(x - z) / s)), 0, 1); eight
+  codes per byte, element 8k + j in bit j of byte k.
 
 Each "fp32(...)" is one IEEE single-precision operation with
 round-to-nearest-even, emulated as the float64 operation followed by a cast
@@ -33,9 +37,9 @@ to float32 (exact for one +, -, * or / of float32 operands, since
 
 Layouts (shared by definition with the C ABI, not by code):
   codes  [n_slots][2 (K, V)][Hkv][P][row]  row = D halves (FP16/BF16),
-         D bytes (FP8/INT8), D/2 bytes (INT4), D/4 bytes (INT2)
+         D bytes (FP8/INT8), D/2 bytes (INT4), D/4 bytes (INT2), D/8 bytes (INT1)
   meta   FP8/INT8: float32 [n_slots][2][Hkv];
-         INT4 / INT2: float16 [n_slots][2][Hkv][P][D/32][2] = (scale, zero)
+         INT4 / INT2 / INT1: float16 [n_slots][2][Hkv][P][D/32][2] = (scale, zero)
 """
 
 import math
@@ -48,6 +52,7 @@ CODEC_FP8_E4M3 = 2
 CODEC_INT8 = 3
 CODEC_INT4_G32 = 4
 CODEC_INT2_G32 = 5
+CODEC_INT1_G32 = 6
 
 F16_MAX = 65504.0
 
@@ -194,6 +199,12 @@ def quantize_group_int2(x32):
     return _quantize_group_affine(x32, 3)
 
 
+def quantize_group_int1(x32):
+    """Groups of 32 along the last axis -> (codes 0..1, fp16 scale, fp16 zero);
+    the INT4 steps with 1 level above the zero point in place of 15."""
+    return _quantize_group_affine(x32, 1)
+
+
 def _quantize_group_affine(x32, top):
     """unsigned_affine over groups of 32: codes 0..top (top = 2^bits - 1)."""
     x32 = _f32(x32)
@@ -221,6 +232,23 @@ def pack_int2(codes):
     """[..., D] codes 0..3 -> [..., D/4] bytes, element 4k + j in bits 2j of byte k."""
     c = codes.astype(np.uint8)
     return (c[..., 0::4] | (c[..., 1::4] << 2) | (c[..., 2::4] << 4) | (c[..., 3::4] << 6)).astype(np.uint8)
+
+
+def pack_int1(codes):
+    """[..., D] codes 0..1 -> [..., D/8] bytes, element 8k + j in bit j of byte k."""
+    c = codes.astype(np.uint8)
+    out = np.zeros(c.shape[:-1] + (c.shape[-1] // 8,), np.uint8)
+    for j in range(8):
+        out |= (c[..., j::8] << j).astype(np.uint8)
+    return out
+
+
+def unpack_int1(packed):
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (p.shape[-1] * 8,), np.uint8)
+    for j in range(8):
+        out[..., j::8] = (p >> j) & 1
+    return out
 
 
 def unpack_int2(packed):
@@ -252,8 +280,9 @@ def dequant_page(codec, codes, meta, slot, kv, h):
         return e4m3_table()[c.astype(np.int64)] * np.float64(meta[slot, kv, h])
     if codec == CODEC_INT8:
         return c.view(np.int8).astype(np.float64) * np.float64(meta[slot, kv, h])
-    if codec in (CODEC_INT4_G32, CODEC_INT2_G32):
-        q = (unpack_int4(c) if codec == CODEC_INT4_G32 else unpack_int2(c)).astype(np.float64)   # [P][D]
+    if codec in (CODEC_INT4_G32, CODEC_INT2_G32, CODEC_INT1_G32):
+        unpack = {CODEC_INT4_G32: unpack_int4, CODEC_INT2_G32: unpack_int2, CODEC_INT1_G32: unpack_int1}[codec]
+        q = unpack(c).astype(np.float64)                                                     # [P][D]
         P, D = q.shape
         sz = meta[slot, kv, h].astype(np.float64)          # [P][D/32][2]
         qg = q.reshape(P, D // 32, 32)
@@ -272,8 +301,8 @@ def alloc_pool(codec, n_slots, hkv, P, D):
     if codec in (CODEC_FP8_E4M3, CODEC_INT8):
         return (np.zeros((n_slots, 2, hkv, P, D), np.uint8),
                 np.zeros((n_slots, 2, hkv), np.float32))
-    if codec in (CODEC_INT4_G32, CODEC_INT2_G32):
-        row = D // 2 if codec == CODEC_INT4_G32 else D // 4
+    if codec in (CODEC_INT4_G32, CODEC_INT2_G32, CODEC_INT1_G32):
+        row = {CODEC_INT4_G32: D // 2, CODEC_INT2_G32: D // 4, CODEC_INT1_G32: D // 8}[codec]
         return (np.zeros((n_slots, 2, hkv, P, row), np.uint8),
                 np.zeros((n_slots, 2, hkv, P, D // 32, 2), np.float16))
     raise ValueError("unknown codec %r" % codec)
@@ -321,16 +350,18 @@ def quantize_pages(src_bits, src_dtype, src_slots, dst_codec, dst_codes, dst_met
                     out[:valid] = codes
                     dst_codes[di, kv, h] = out.view(np.uint8)
                     dst_meta[di, kv, h] = scale
-                elif dst_codec in (CODEC_INT4_G32, CODEC_INT2_G32):
+                elif dst_codec in (CODEC_INT4_G32, CODEC_INT2_G32, CODEC_INT1_G32):
                     q = np.zeros((P, D), np.uint8)
                     sz = np.zeros((P, D // 32, 2), np.float16)
                     if valid:
-                        enc = quantize_group_int4 if dst_codec == CODEC_INT4_G32 else quantize_group_int2
+                        enc = {CODEC_INT4_G32: quantize_group_int4, CODEC_INT2_G32: quantize_group_int2,
+                               CODEC_INT1_G32: quantize_group_int1}[dst_codec]
                         qc, s, z = enc(xv.reshape(valid, D // 32, 32))
                         q[:valid] = qc.reshape(valid, D)
                         sz[:valid, :, 0] = s
                         sz[:valid, :, 1] = z
-                    dst_codes[di, kv, h] = pack_int4(q) if dst_codec == CODEC_INT4_G32 else pack_int2(q)
+                    pack = {CODEC_INT4_G32: pack_int4, CODEC_INT2_G32: pack_int2, CODEC_INT1_G32: pack_int1}[dst_codec]
+                    dst_codes[di, kv, h] = pack(q)
                     dst_meta[di, kv, h] = sz
                 else:
                     raise ValueError("unknown codec %r" % dst_codec)

@@ -248,7 +248,7 @@ def _sat_groups():
     return C.round_to_bf16(g).astype(np.float32)
 
 
-@pytest.mark.parametrize("top", [15, 3])
+@pytest.mark.parametrize("top", [15, 3, 1])
 def test_affine_encoder_saturates_zero_point_and_scale_at_65504(top):
     """fp16_sat clips to +-65504 (torch's half cast would give inf there).
     Closed form per group: z = max(lo, -65504) rounded to fp16, s =
@@ -269,8 +269,71 @@ def test_affine_encoder_saturates_zero_point_and_scale_at_65504(top):
             assert codes[gi, e] == want, (gi, e, xv)
     if top == 15:
         assert codes[0, 7] == 4                                 # 3.5 rounds to even
-    # group 3: z saturates (lo = -65536), s does not: (65536 + 65504) / top is an fp16 value
-    assert float(s[3]) == (65536.0 + 65504.0) / top
+    # group 3: z saturates (lo = -65536); (65536 + 65504) / top is an fp16 value
+    # for top 15 and 3, and saturates for top 1
+    assert float(s[3]) == min((65536.0 + 65504.0) / top, 65504.0)
+
+
+# ---------------------------------------------------------------- 1-bit codec
+
+def test_int1_pack_order_element_8k_plus_j_in_bit_j():
+    # byte 0: elements 0..7 = 1,0,1,1,0,0,0,1 -> 0b10001101 = 0x8D; byte 1: 0,1,0,0,0,0,1,0 -> 0x42
+    codes = np.array([1, 0, 1, 1, 0, 0, 0, 1, 0, 1, 0, 0, 0, 0, 1, 0], np.uint8)
+    assert C.pack_int1(codes).tolist() == [0x8D, 0x42]
+    assert C.unpack_int1(np.array([0x8D, 0x42], np.uint8)).tolist() == codes.tolist()
+
+
+def test_int1_round_trip_exact_on_representable_groups():
+    """Groups of exactly two values z and z + s (s a power of two, z a
+    multiple of s): codes are the membership bits, scale and zero exact."""
+    rng = np.random.default_rng(23)
+    for s_exp in (-7, -1, 0, 4):
+        s = 2.0 ** s_exp
+        q = rng.integers(0, 2, size=(30, 32))
+        q[:, 0], q[:, 1] = 0, 1
+        z = rng.integers(-50, 50, size=(30, 1)) * s
+        x = (q * s + z).astype(np.float32)
+        codes, ss, zz = C.quantize_group_int1(x)
+        assert np.all(ss.astype(np.float64) == s)
+        assert np.array_equal(zz.astype(np.float64), z[:, 0])
+        assert np.array_equal(codes.astype(np.int64), q)
+
+
+def test_int1_error_bound_and_degenerate_group():
+    """Each value lands on the nearer of z and z + s (s = max - min up to fp16
+    rounding): |x - rec| <= s / 2 plus the fp16 rounding of z and s; a group of
+    equal values has s = 0, codes 0, and reconstructs to z."""
+    rng = np.random.default_rng(24)
+    x = (rng.standard_normal((500, 32)) * rng.uniform(0.1, 10, (500, 1))).astype(np.float32)
+    codes, s, z = C.quantize_group_int1(x)
+    assert codes.max() <= 1
+    rec = codes * s.astype(np.float64)[:, None] + z.astype(np.float64)[:, None]
+    lo = x.min(axis=1).astype(np.float64)
+    hi = x.max(axis=1).astype(np.float64)
+    s64, z64 = s.astype(np.float64), z.astype(np.float64)
+    bound = 0.5 * s64 + np.abs(lo - z64) + 2 * np.abs((hi - z64) - s64) + 1e-6
+    assert np.all(np.abs(rec - x) <= bound[:, None])
+    assert np.all(codes[np.arange(500), x.argmax(axis=1)] == 1)   # the maximum takes the top code
+    assert np.all(codes[np.arange(500), x.argmin(axis=1)] == 0)
+    c, s0, z0 = C.quantize_group_int1(np.full((1, 32), 7.25, np.float32))
+    assert s0[0] == 0 and z0[0] == np.float16(7.25) and not c.any()
+
+
+def test_int1_codes_against_a_torch_float32_pipeline():
+    """torch's IEEE float32 ops give the same codes, scales and zero points
+    inside fp16's range, including values exactly half way between z and z+s."""
+    rng = np.random.default_rng(25)
+    x = (rng.standard_normal((2000, 32)) * rng.uniform(0.01, 100, (2000, 1))).astype(np.float32)
+    x[::9] = np.float32(0.25) * rng.integers(-8, 8, (len(x[::9]), 32)).astype(np.float32)
+    codes, s, z = C.quantize_group_int1(x)
+    t = torch.from_numpy(x)
+    tz = t.min(dim=1).values.to(torch.float16)
+    ts = (t.max(dim=1).values - tz.float()).to(torch.float16)
+    y = (t - tz.float()[:, None]) / torch.where(ts > 0, ts, torch.ones_like(ts)).float()[:, None]
+    tq = torch.clamp(torch.round(y), 0, 1)
+    tq = torch.where((ts > 0)[:, None], tq, torch.zeros_like(tq))
+    assert np.array_equal(z, tz.numpy()) and np.array_equal(s, ts.numpy())
+    assert np.array_equal(codes.astype(np.int64), tq.numpy().astype(np.int64))
 
 
 # ---------------------------------------------------------------- bf16 rounding
@@ -290,7 +353,8 @@ def _src_pool(n, hkv, P, D, dtype, seed):
     return W.to_bits(t)
 
 
-@pytest.mark.parametrize("codec", [C.CODEC_FP8_E4M3, C.CODEC_INT8, C.CODEC_INT4_G32, C.CODEC_INT2_G32])
+@pytest.mark.parametrize("codec", [C.CODEC_FP8_E4M3, C.CODEC_INT8, C.CODEC_INT4_G32, C.CODEC_INT2_G32,
+                                   C.CODEC_INT1_G32])
 def test_quantize_pages_units_independent_and_ckey(codec):
     hkv, P, D = 2, 16, 64
     src = _src_pool(3, hkv, P, D, C.CODEC_BF16, 11)
@@ -314,10 +378,10 @@ def test_quantize_pages_units_independent_and_ckey(codec):
 
 
 def test_dequant_independent_of_oracle_helpers():
-    """Dequantise FP8 / INT8 / INT4 / INT2 with torch (library view of the codes)."""
+    """Dequantise FP8 / INT8 / INT4 / INT2 / INT1 with torch (library view of the codes)."""
     hkv, P, D = 1, 16, 64
     src = _src_pool(1, hkv, P, D, C.CODEC_FP16, 12)
-    for codec in (C.CODEC_FP8_E4M3, C.CODEC_INT8, C.CODEC_INT4_G32, C.CODEC_INT2_G32):
+    for codec in (C.CODEC_FP8_E4M3, C.CODEC_INT8, C.CODEC_INT4_G32, C.CODEC_INT2_G32, C.CODEC_INT1_G32):
         codes, meta = C.alloc_pool(codec, 1, hkv, P, D)
         C.quantize_pages(src, C.CODEC_FP16, [0], codec, codes, meta, [0])
         got = C.dequant_page(codec, codes, meta, 0, 1, 0)
@@ -329,14 +393,16 @@ def test_dequant_independent_of_oracle_helpers():
         else:
             if codec == C.CODEC_INT4_G32:
                 q = torch.stack([(tc & 0xF).double(), (tc >> 4).double()], dim=-1).reshape(P, D)
-            else:   # four 2-bit codes per byte, lowest bits first
+            elif codec == C.CODEC_INT2_G32:   # four 2-bit codes per byte, lowest bits first
                 q = torch.stack([((tc >> (2 * j)) & 3).double() for j in range(4)], dim=-1).reshape(P, D)
+            else:   # eight 1-bit codes per byte, lowest bit first
+                q = torch.stack([((tc >> j) & 1).double() for j in range(8)], dim=-1).reshape(P, D)
             sz = torch.from_numpy(meta[0, 1, 0].astype(np.float64))   # [P][D/32][2]
             ref = (q.reshape(P, D // 32, 32) * sz[..., :1] + sz[..., 1:]).reshape(P, D)
         assert np.array_equal(got, ref.numpy())
         x = C.f16_bits_to_f64(src[0, 1, 0])
-        # INT2 keeps 4 levels per group: a coarser (but bounded) reconstruction
-        frac = 0.4 if codec == C.CODEC_INT2_G32 else 0.1
+        # INT2 keeps 4 levels per group, INT1 two: coarser (but bounded) reconstructions
+        frac = {C.CODEC_INT2_G32: 0.4, C.CODEC_INT1_G32: 1.0}.get(codec, 0.1)
         assert np.max(np.abs(got - x)) <= frac * np.max(np.abs(x))
 
 
@@ -423,13 +489,13 @@ def test_mixed_codec_decode_equals_torch_dense_on_dequantised_pages():
     Hkv, G, D, P = 2, 4, 64, 16
     lens = [80]
     q = C.f16_bits_to_f64(W.to_bits(W.normal((1, Hkv * G, D), C.CODEC_FP16, 31)))
-    src = W.to_bits(W.normal((6, 2, Hkv, P, D), C.CODEC_FP16, 32))
-    pools, page_codec = {}, np.array([[5, 4, 3, 2, 0, 2]])
-    table = np.array([[0, 0, 0, 1, 0, 0]], np.int32)
-    lens = [96]
-    for codec in (0, 2, 3, 4, 5):
+    pools, page_codec = {}, np.array([[6, 5, 4, 3, 2, 0, 2]])
+    table = np.array([[0, 0, 0, 0, 1, 0, 0]], np.int32)
+    lens = [112]
+    src = W.to_bits(W.normal((7, 2, Hkv, P, D), C.CODEC_FP16, 32))
+    for codec in (0, 2, 3, 4, 5, 6):
         pools[codec] = C.alloc_pool(codec, 2, Hkv, P, D)
-    for p in range(6):
+    for p in range(7):
         c = int(page_codec[0, p])
         C.quantize_pages(src, C.CODEC_FP16, [p], c, pools[c][0], pools[c][1], [int(table[0, p])])
     o, _, bad = A.paged_decode(q, Hkv, P, pools, page_codec, table, np.array(lens), 0.125)
@@ -437,7 +503,7 @@ def test_mixed_codec_decode_equals_torch_dense_on_dequantised_pages():
     # independent dequantisation with torch views of the stored codes
     for h in range(Hkv):
         Ks, Vs = [], []
-        for p in range(6):
+        for p in range(7):
             c, slot = int(page_codec[0, p]), int(table[0, p])
             codes, meta = pools[c]
             for kv, acc in ((0, Ks), (1, Vs)):
@@ -451,8 +517,10 @@ def test_mixed_codec_decode_equals_torch_dense_on_dequantised_pages():
                 else:
                     if c == 4:
                         qn = torch.stack([(t & 0xF).double(), (t >> 4).double()], -1).reshape(P, D)
-                    else:
+                    elif c == 5:
                         qn = torch.stack([((t >> (2 * j)) & 3).double() for j in range(4)], -1).reshape(P, D)
+                    else:
+                        qn = torch.stack([((t >> j) & 1).double() for j in range(8)], -1).reshape(P, D)
                     sz = torch.from_numpy(meta[slot, kv, h].astype(np.float64))
                     acc.append((qn.reshape(P, D // 32, 32) * sz[..., :1] + sz[..., 1:]).reshape(P, D))
         K, V = torch.cat(Ks).numpy(), torch.cat(Vs).numpy()
