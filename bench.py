@@ -417,8 +417,8 @@ def leg_tiny(dev, timer, steps, warm, hbm):
 def leg_batched(dev, timer, steps, warm, hbm):
     """Batch 32, 32 q / 8 KV heads, head_dim 128, 16-token pages, lengths
     U[8192, 32768], random physical slots; demotion of the BF16 pages to FP8 /
-    INT8 / INT4 / INT2, and BF16, FP8 and INT2 decode (each also under a
-    4096-token window with 4 sink tokens)."""
+    INT8 / INT4 / INT2 / INT1, and BF16, FP8, INT2 and INT1 decode (each also
+    under a 4096-token window with 4 sink tokens)."""
     import torch
     import mixed_precision_paged_argus_gb300.argus as argus
     from mixed_precision_paged_argus_gb300 import workloads as W, accounting as A
@@ -437,7 +437,8 @@ def leg_batched(dev, timer, steps, warm, hbm):
     tokens = int(lens.sum())
     pages = int(sum((L + P_ - 1) // P_ for L in lens))
     # demotion of every BF16 page
-    for name, codec in (("fp8", W.FP8_E4M3), ("int8", W.INT8), ("int4", W.INT4_G32), ("int2", W.INT2_G32)):
+    for name, codec in (("fp8", W.FP8_E4M3), ("int8", W.INT8), ("int4", W.INT4_G32), ("int2", W.INT2_G32),
+                        ("int1", W.INT1_G32)):
         dst = argus.Pool.empty(codec, n_slots, Hkv, P_, D_, device=dev)
         gr = timer.graph(lambda: argus.quantize_pages(g, W.BF16, bf.codes, n_slots, ids, dst, ids, n_slots,
                                                       stream=timer.stream))
@@ -449,10 +450,13 @@ def leg_batched(dev, timer, steps, warm, hbm):
             fp8 = dst
         elif codec == W.INT2_G32:
             int2 = dst
+        elif codec == W.INT1_G32:
+            int1 = dst
         else:
             del dst
         torch.cuda.synchronize()
-    for name, pool, codec in (("bf16", bf, W.BF16), ("fp8", fp8, W.FP8_E4M3), ("int2", int2, W.INT2_G32)):
+    for name, pool, codec in (("bf16", bf, W.BF16), ("fp8", fp8, W.FP8_E4M3), ("int2", int2, W.INT2_G32),
+                              ("int1", int1, W.INT1_G32)):
         out = torch.empty((B, Hq, D_), dtype=torch.bfloat16, device=dev)
         d_codec = torch.full((B, MAXP), codec, dtype=torch.uint8, device=dev)
         a = argus.decode_args(g, B, q, [pool], d_codec, d_table, d_lens, MAXP, W.softmax_scale(D_), out=out)
@@ -474,7 +478,7 @@ def leg_batched(dev, timer, steps, warm, hbm):
         res["decode_%s_window" % name] = {"window": WIN, "sinks": SINK, "us_per_step": ms * 1e3,
                                           "bytes": nb, "gbs": nb / (ms * 1e-3) / 1e9,
                                           "frac_of_hbm": nb / (ms * 1e-3) / 1e9 / hbm}
-    del bf, fp8, int2
+    del bf, fp8, int2, int1
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return res

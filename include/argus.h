@@ -35,15 +35,16 @@
  *   codes  [n_slots][2 (K, V)][Hkv][P][row]   row = head_dim 16-bit values
  *          (FP16 / BF16), head_dim bytes (FP8 e4m3 / INT8), head_dim/2 bytes
  *          (INT4: two codes per byte, the even element in the low nibble),
- *          head_dim/4 bytes (INT2: element 4k + j in bits 2j, 2j+1 of byte k)
+ *          head_dim/4 bytes (INT2: element 4k + j in bits 2j, 2j+1 of byte k),
+ *          head_dim/8 bytes (INT1: element 8k + j in bit j of byte k)
  *   meta   FP16 / BF16: unused (NULL)
  *          FP8 / INT8:  float [n_slots][2][Hkv]  one scale per (page, head, K|V)
- *          INT4 / INT2: half2 {scale, zero} [n_slots][2][Hkv][P][head_dim/32]
+ *          INT4 / INT2 / INT1: half2 {scale, zero} [n_slots][2][Hkv][P][head_dim/32]
  *   Dequantised value: FP8 e4m3_value(code) * scale; INT8 code * scale;
- *   INT4 / INT2 code * scale + zero.  INT4 per token and group of 32:
+ *   INT4 / INT2 / INT1 code * scale + zero.  INT4 per token and group of 32:
  *   z = fp16_sat(min), s = fp16_sat(RN(RN(max - z) / 15)), code =
  *   clamp(rint(RN(x - z) / s), 0, 15) (s = 0: code 0); INT2 the same with 3
- *   in place of 15.  Codes and pools must be 16-byte aligned.
+ *   and INT1 with 1 in place of 15.  Codes and pools must be 16-byte aligned.
  */
 #ifndef ARGUS_H
 #define ARGUS_H
@@ -66,14 +67,16 @@ typedef enum {
 /* Codec tiers of [ARGUS] (summary; "Direct paged attention": FP16, Q8, Q4 pages)
  * and [PR499] update 20f3b23 ("e4m3 codes + fp32 scales").  INT2 is the
  * summary's INT2 tier in the "unsigned_affine, bits = 2" form of the ARGUS
- * page's "Pluggable tiers" example, with the INT4 tier's 32-element groups. */
+ * page's "Pluggable tiers" example, with the INT4 tier's 32-element groups;
+ * INT1 is the summary's 1-bit tier in the same form with bits = 1. */
 typedef enum {
   ARGUS_FP16 = 0,
   ARGUS_BF16 = 1,
   ARGUS_FP8_E4M3 = 2,
   ARGUS_INT8 = 3,
   ARGUS_INT4_G32 = 4,
-  ARGUS_INT2_G32 = 5
+  ARGUS_INT2_G32 = 5,
+  ARGUS_INT1_G32 = 6
 } argus_codec;
 
 typedef struct {

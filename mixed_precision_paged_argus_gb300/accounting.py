@@ -7,7 +7,7 @@ T >= S_wire / B of "Storage contracts for hybrid KV cache offloading"
 (section "Stored-byte savings are not a latency result").
 """
 
-FP16, BF16, FP8_E4M3, INT8, INT4_G32, INT2_G32 = 0, 1, 2, 3, 4, 5
+FP16, BF16, FP8_E4M3, INT8, INT4_G32, INT2_G32, INT1_G32 = 0, 1, 2, 3, 4, 5, 6
 
 
 def code_bytes_per_row(codec, head_dim):
@@ -20,12 +20,14 @@ def code_bytes_per_row(codec, head_dim):
         return head_dim // 2
     if codec == INT2_G32:
         return head_dim // 4
+    if codec == INT1_G32:
+        return head_dim // 8
     raise ValueError(codec)
 
 
 def meta_bytes_per_row(codec, head_dim):
-    """Per-token metadata bytes of one head (INT4 / INT2: one fp16 scale + zero per group)."""
-    if codec in (INT4_G32, INT2_G32):
+    """Per-token metadata bytes of one head (INT4 / INT2 / INT1: one fp16 scale + zero per group)."""
+    if codec in (INT4_G32, INT2_G32, INT1_G32):
         return 4 * (head_dim // 32)
     return 0
 

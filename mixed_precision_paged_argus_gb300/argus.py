@@ -12,9 +12,9 @@ import os
 
 import torch
 
-FP16, BF16, FP8_E4M3, INT8, INT4_G32, INT2_G32 = 0, 1, 2, 3, 4, 5
+FP16, BF16, FP8_E4M3, INT8, INT4_G32, INT2_G32, INT1_G32 = 0, 1, 2, 3, 4, 5, 6
 CODEC_NAMES = {FP16: "fp16", BF16: "bf16", FP8_E4M3: "fp8_e4m3", INT8: "int8", INT4_G32: "int4_g32",
-               INT2_G32: "int2_g32"}
+               INT2_G32: "int2_g32", INT1_G32: "int1_g32"}
 DTYPE_CODEC = {torch.float16: FP16, torch.bfloat16: BF16}
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libargus.so")
@@ -177,8 +177,9 @@ class Pool:
         elif codec in (FP8_E4M3, INT8):
             codes = alloc(shape + (head_dim,), dtype=torch.uint8, device=device)
             meta = alloc((n_slots, 2, n_kv_heads), dtype=torch.float32, device=device)
-        elif codec in (INT4_G32, INT2_G32):
-            codes = alloc(shape + (head_dim // (2 if codec == INT4_G32 else 4),), dtype=torch.uint8, device=device)
+        elif codec in (INT4_G32, INT2_G32, INT1_G32):
+            per_byte = {INT4_G32: 2, INT2_G32: 4, INT1_G32: 8}[codec]
+            codes = alloc(shape + (head_dim // per_byte,), dtype=torch.uint8, device=device)
             meta = alloc(shape + (head_dim // 32, 2), dtype=torch.float16, device=device)
         else:
             raise ValueError(codec)

@@ -56,6 +56,7 @@ struct Warps {
   static constexpr int kThreads = 32 * (kConsumer + 1);
 };
 constexpr int kMaxG = 8;
+constexpr int kNumCodecs = ARGUS_INT1_G32 + 1;
 constexpr int kMaxSplits = 512;  // bounds the split combine's per-thread loads
 constexpr int kFoldThreads = 256;
 
@@ -64,9 +65,9 @@ enum Family { kFamF16 = 0, kFamBF16 = 1, kFamMixed = 2 };
 struct Params {
   int B, Hkv, G, P, max_pages;
   const void* q;
-  const uint8_t* codes[6];   // indexed by argus_codec
-  const uint8_t* meta[6];
-  long long n_slots[6];
+  const uint8_t* codes[kNumCodecs];   // indexed by argus_codec
+  const uint8_t* meta[kNumCodecs];
+  long long n_slots[kNumCodecs];
   uint32_t host_mask;        // bit c: the pool of codec c lives in host memory
   const uint8_t* page_codec;
   const int32_t* block_table;
@@ -162,6 +163,19 @@ struct Layout {
   static constexpr int kMinBlocks = (D == 128) ? 1 : 2;  // by shared memory
 };
 
+// Bytes of one token row of one head in a pool of `codec`.
+__host__ __device__ constexpr int row_bytes(int codec, int D) {
+  return codec <= ARGUS_BF16 ? 2 * D
+       : codec == ARGUS_INT4_G32 ? D / 2
+       : codec == ARGUS_INT2_G32 ? D / 4
+       : codec == ARGUS_INT1_G32 ? D / 8 : D;
+}
+
+// codecs stored as per-group {scale, zero} affine codes
+__host__ __device__ constexpr bool affine_codec(int codec) {
+  return codec == ARGUS_INT4_G32 || codec == ARGUS_INT2_G32 || codec == ARGUS_INT1_G32;
+}
+
 template <int CW>
 __device__ __forceinline__ void consumer_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory");
@@ -218,6 +232,23 @@ __device__ __forceinline__ void load_k_frags(int codec, const uint8_t* chunk, in
             a[4 * j + cc][2 + rr] = hsub2_u32(f16_magic_pair(u, 0x4342), bias);
           }
         }
+      }
+    } else if (codec == ARGUS_INT1_G32) {
+      // the lane's 8-element run of group i is one byte, element e at bit e;
+      // B | B << 12 puts bit e in the low half and bit e + 4 at bit 16 + e, so
+      // shifts of 0..3 give the element pairs (0,4) .. (3,7) of the INT4 map
+#pragma unroll
+      for (int i = 0; i < L::kNI; ++i) {
+        const uint32_t b8 = *(chunk + L::kOffK + row * (D / 8) + 4 * i + t);
+        const uint32_t w = b8 | (b8 << 12);
+        const __half2 mz = *reinterpret_cast<const __half2*>(chunk + L::kOffMK + (row * L::kNI + i) * 4);
+        kz[rr][i][0] = __low2float(mz);
+        kz[rr][i][1] = __high2float(mz);
+        const uint32_t magic = 0x64006400u;
+        a[2 * i][rr] = hsub2_u32(lop3_and_or(w, 0x00010001u, magic), magic);
+        a[2 * i][2 + rr] = hsub2_u32(lop3_and_or(w >> 1, 0x00010001u, magic), magic);
+        a[2 * i + 1][rr] = hsub2_u32(lop3_and_or(w >> 2, 0x00010001u, magic), magic);
+        a[2 * i + 1][2 + rr] = hsub2_u32(lop3_and_or(w >> 3, 0x00010001u, magic), magic);
       }
     } else if (codec == ARGUS_INT2_G32) {
       // the lane's 8-element run of group i is 2 bytes: byte b holds elements
@@ -323,6 +354,36 @@ __device__ __forceinline__ void load_v_frags(int codec, const uint8_t* chunk, in
         }
       }
     }
+  } else if (codec == ARGUS_INT1_G32) {
+    // the lane's DL elements of a row are DL/8 bytes (DL = 16: two bytes)
+    uint32_t cw[4];
+    uint32_t m[4];
+    const int grp = (DL * r) / 32;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint8_t* src = chunk + L::kOffV + rows[q] * (D / 8) + (DL / 8) * r;
+      if constexpr (DL == 16) cw[q] = *reinterpret_cast<const uint16_t*>(src);
+      else cw[q] = *src;
+      m[q] = *reinterpret_cast<const uint32_t*>(chunk + L::kOffMV + (rows[q] * L::kNI + grp) * 4);
+    }
+    const uint32_t magic = 0x64006400u;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int q0 = 2 * half;
+      const uint32_t s2 = prmt(m[q0], m[q0 + 1], 0x5410);
+      const uint32_t z2 = prmt(m[q0], m[q0 + 1], 0x7632);
+#pragma unroll
+      for (int b = 0; b < DL / 8; ++b) {
+        // byte b of row a to byte 0, of row b to byte 2
+        const uint32_t x = prmt(cw[q0], cw[q0 + 1], (uint32_t)(b | (b << 4) | ((4 + b) << 8) | ((4 + b) << 12)));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t c = hsub2_u32(lop3_and_or(x >> j, 0x00010001u, magic), magic);
+          const int d = 8 * b + j;
+          v[d / 2][2 * half + (d & 1)] = hfma2_u32(c, s2, z2);
+        }
+      }
+    }
   } else if (codec == ARGUS_INT2_G32) {
     // the lane's DL elements of a row are DL/4 bytes (DL = 16: one word)
     uint32_t cw[4];
@@ -407,7 +468,7 @@ __device__ __forceinline__ void group_scores(const uint8_t* const* cptr, const C
   float kz[NCG][2][D / 32][2];
 #pragma unroll
   for (int c = 0; c < NCG; ++c) load_k_frags<D, NARROW>(CODEC, cptr[c], r, t, a[c], kz[c]);
-  if constexpr (CODEC == ARGUS_INT4_G32 || CODEC == ARGUS_INT2_G32) {
+  if constexpr (affine_codec(CODEC)) {
     float sg[NCG][D / 32][4];
 #pragma unroll
     for (int c = 0; c < NCG; ++c)
@@ -515,8 +576,7 @@ __device__ __forceinline__ void group_pv(const uint8_t* const* cptr, int r, int 
 template <int D, bool NARROW>
 __device__ __forceinline__ void copy_host_chunk(const ChunkDesc& d, uint8_t* slot, int lane) {
   using L = Layout<D, NARROW>;
-  const int rowb = (d.codec <= ARGUS_BF16) ? 2 * D
-                 : (d.codec == ARGUS_INT4_G32 ? D / 2 : (d.codec == ARGUS_INT2_G32 ? D / 4 : D));
+  const int rowb = row_bytes(d.codec, D);
   const int n16 = kChunk * rowb / 16;          // 16-byte vectors of K (and of V)
   const uint4* srcK = reinterpret_cast<const uint4*>(d.hk);
   const uint4* srcV = reinterpret_cast<const uint4*>(d.hv);
@@ -702,7 +762,7 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
             const int codec = cur_codec;
             const long long slot_id = cur_slot;
             // INT2 pages are read by the extended kernels only
-            bool ok = codec >= 0 && codec <= (EXT ? ARGUS_INT2_G32 : ARGUS_INT4_G32) && p.codes[codec] != nullptr;
+            bool ok = codec >= 0 && codec <= (EXT ? ARGUS_INT1_G32 : ARGUS_INT4_G32) && p.codes[codec] != nullptr;
             if (ok) {
               const int fam = codec_family(codec);
               ok = (FAM == kFamMixed) || (FAM == fam);
@@ -712,15 +772,14 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
             if (!ok) {
               if (first && p.status) atomicAdd(p.status, 1u);
             } else {
-              const int rowb = (codec <= ARGUS_BF16) ? 2 * D
-                             : (codec == ARGUS_INT4_G32 ? D / 2 : (codec == ARGUS_INT2_G32 ? D / 4 : D));
+              const int rowb = row_bytes(codec, D);
               const size_t rk = (((size_t)slot_id * 2 + 0) * Hkv + h) * P + (size_t)cip * kChunk;
               const size_t rv = (((size_t)slot_id * 2 + 1) * Hkv + h) * P + (size_t)cip * kChunk;
               srcK = p.codes[codec] + rk * rowb;
               srcV = p.codes[codec] + rv * rowb;
               kv_bytes = kChunk * rowb;
               d.codec = codec;
-              if (codec == ARGUS_INT4_G32 || codec == ARGUS_INT2_G32) {
+              if (affine_codec(codec)) {
                 srcMK = p.meta[codec] + rk * (L::kNI * 4);
                 srcMV = p.meta[codec] + rv * (L::kNI * 4);
                 m_bytes = kChunk * L::kNI * 4;
@@ -942,6 +1001,10 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
                     group_scores<D, ARGUS_INT2_G32, 2, false, NARROW, EXT>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0);
                     break;
                   }
+                  if (codec == ARGUS_INT1_G32) {
+                    group_scores<D, ARGUS_INT1_G32, 2, false, NARROW, EXT>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0);
+                    break;
+                  }
                 }
                 group_scores<D, ARGUS_INT4_G32, 2, false, NARROW, EXT>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0);
                 break;
@@ -958,6 +1021,10 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
             if constexpr (EXT) {   // the INT2 tier exists in the extended kernels only
               if (codec == ARGUS_INT2_G32) {
                 group_scores<D, ARGUS_INT2_G32, 1, false, NARROW, EXT>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0);
+                break;
+              }
+              if (codec == ARGUS_INT1_G32) {
+                group_scores<D, ARGUS_INT1_G32, 1, false, NARROW, EXT>(cp, dd, r, t, qf, qb, qf8, qgs, fq0, fq1, p.scale_log2, sv, c0);
                 break;
               }
             }
@@ -1046,6 +1113,10 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
                     group_pv<D, ARGUS_INT2_G32, 2, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc);
                     break;
                   }
+                  if (codec == ARGUS_INT1_G32) {
+                    group_pv<D, ARGUS_INT1_G32, 2, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc);
+                    break;
+                  }
                 }
                 group_pv<D, ARGUS_INT4_G32, 2, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc);
                 break;
@@ -1062,6 +1133,10 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
             if constexpr (EXT) {
               if (codec == ARGUS_INT2_G32) {
                 group_pv<D, ARGUS_INT2_G32, 1, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc);
+                break;
+              }
+              if (codec == ARGUS_INT1_G32) {
+                group_pv<D, ARGUS_INT1_G32, 1, false, NARROW>(cp, r, t, pw + c0, skip + c0, acc);
                 break;
               }
             }
@@ -1298,16 +1373,16 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
   if ((a->sel_pages == nullptr) != (a->sel_count == nullptr))
     return fail(ARGUS_E_INVALID, "decode: sel_pages and sel_count must both be set or both NULL");
   if (a->sel_pages && a->sel_width <= 0) return fail(ARGUS_E_INVALID, "decode: sel_width must be positive");
-  if (a->n_pools < 0 || a->n_pools > 5 || (a->n_pools > 0 && !a->pools))
+  if (a->n_pools < 0 || a->n_pools > kNumCodecs || (a->n_pools > 0 && !a->pools))
     return fail(ARGUS_E_INVALID, "decode: bad pool list");
   if (!std::isfinite(a->softmax_scale)) return fail(ARGUS_E_INVALID, "decode: softmax_scale not finite");
   if (a->out && a->out_dtype != ARGUS_FP16 && a->out_dtype != ARGUS_BF16)
     return fail(ARGUS_E_INVALID, "decode: out_dtype must be FP16 or BF16");
-  bool seen[6] = {false, false, false, false, false, false};
+  bool seen[kNumCodecs] = {};
   bool has_bf16 = false, has_f16 = false;
   for (int i = 0; i < a->n_pools; ++i) {
     const argus_pool& pool = a->pools[i];
-    if (pool.codec < 0 || pool.codec > ARGUS_INT2_G32) return fail(ARGUS_E_INVALID, "decode: pool %d has codec %d", i, pool.codec);
+    if (pool.codec < 0 || pool.codec > ARGUS_INT1_G32) return fail(ARGUS_E_INVALID, "decode: pool %d has codec %d", i, pool.codec);
     if (pool.placement != ARGUS_PLACE_DEVICE && pool.placement != ARGUS_PLACE_HOST)
       return fail(ARGUS_E_INVALID, "decode: pool %d has placement %d", i, pool.placement);
     if (seen[pool.codec]) return fail(ARGUS_E_INVALID, "decode: two pools with codec %d", pool.codec);
@@ -1330,11 +1405,11 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
   pl->D = g.head_dim;
   pl->G = G;
   // narrow ring: every pool holds byte or nibble codes, head_dim 128
-  pl->ext = a->window_tokens > 0 || seen[ARGUS_INT2_G32];
+  pl->ext = a->window_tokens > 0 || seen[ARGUS_INT2_G32] || seen[ARGUS_INT1_G32];
   pl->host = false;
   for (int i = 0; i < a->n_pools; ++i) pl->host |= a->pools[i].placement == ARGUS_PLACE_HOST;
   if (pl->host && pl->ext)
-    return fail(ARGUS_E_UNSUPPORTED, "decode: host-memory pools with a sliding window or an INT2 pool");
+    return fail(ARGUS_E_UNSUPPORTED, "decode: host-memory pools with a sliding window or an INT2 / INT1 pool");
   pl->narrow = g.head_dim == 128 && !has_bf16 && !seen[ARGUS_FP16] && a->n_pools > 0 && !pl->ext;
   const long long cps_unit = pl->narrow ? chunks_per_stage<true>() : kChunksPerStage;
   const int cpp = g.page_tokens / kChunk;
@@ -1464,7 +1539,7 @@ static argus_status run(const argus_decode_args* a, const Plan& pl, void* ws, vo
   p.P = a->g.page_tokens;
   p.max_pages = a->max_pages;
   p.q = a->q;
-  for (int c = 0; c < 6; ++c) {
+  for (int c = 0; c < kNumCodecs; ++c) {
     p.codes[c] = nullptr;
     p.meta[c] = nullptr;
     p.n_slots[c] = 0;

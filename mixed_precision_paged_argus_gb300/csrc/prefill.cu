@@ -859,9 +859,9 @@ static PParams base_params(const argus_geom* g, int32_t n_q, int64_t win_len, in
 // window's power of two and rounded to fp16.
 struct SParams {
   int Hkv, P, max_pages;
-  const uint8_t* codes[6];
-  const uint8_t* meta[6];
-  long long n_slots[6];
+  const uint8_t* codes[ARGUS_INT1_G32 + 1];
+  const uint8_t* meta[ARGUS_INT1_G32 + 1];
+  long long n_slots[ARGUS_INT1_G32 + 1];
   const uint8_t* page_codec;
   const int32_t* block_table;
   long long win_pos0, win_len, n_vec;   // n_vec = Hkv * win_len * D / 8
@@ -891,7 +891,7 @@ __device__ __forceinline__ bool stage_load8(const SParams& p, int kv, int h, lon
   const long long slot = p.block_table[page];
 #pragma unroll
   for (int e = 0; e < 8; ++e) x[e] = 0.f;
-  if (codec < 0 || codec > ARGUS_INT2_G32 || p.codes[codec] == nullptr || slot < 0 || slot >= p.n_slots[codec])
+  if (codec < 0 || codec > ARGUS_INT1_G32 || p.codes[codec] == nullptr || slot < 0 || slot >= p.n_slots[codec])
     return false;
   const size_t unit = ((size_t)slot * 2 + kv) * p.Hkv + h;   // (slot, K|V, head)
   const size_t r = unit * p.P + row;                          // token row of the pool
@@ -933,6 +933,10 @@ __device__ __forceinline__ bool stage_load8(const SParams& p, int kv, int h, lon
       const uint32_t w = *reinterpret_cast<const uint32_t*>(c + r * (kD / 2) + d0 / 2);
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] = fmaf((float)((w >> (4 * e)) & 0xFu), s, z);
+    } else if (codec == ARGUS_INT1_G32) {
+      const uint32_t w = c[r * (kD / 8) + d0 / 8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = fmaf((float)((w >> e) & 0x1u), s, z);
     } else {
       const uint32_t w = *reinterpret_cast<const uint16_t*>(c + r * (kD / 4) + d0 / 4);
 #pragma unroll
@@ -1137,17 +1141,18 @@ extern "C" argus_status argus_paged_window_prefill_attn(const argus_geom* g, int
   if (max_pages <= 0 || win_pos0 < 0 || win_pos0 + win_len > (long long)max_pages * g->page_tokens)
     return fail(ARGUS_E_INVALID, "paged prefill: window [%lld, %lld) outside the %d pages of the table",
                 (long long)win_pos0, (long long)(win_pos0 + win_len), max_pages);
-  if (n_pools < 0 || n_pools > 6 || (n_pools > 0 && !pools)) return fail(ARGUS_E_INVALID, "paged prefill: bad pool list");
+  if (n_pools < 0 || n_pools > ARGUS_INT1_G32 + 1 || (n_pools > 0 && !pools))
+    return fail(ARGUS_E_INVALID, "paged prefill: bad pool list");
   if (n_q == 0) return ARGUS_OK;
   if (!q || !acc_o || !acc_lse2 || !ws || (win_len > 0 && (!page_codec || !block_table)))
     return fail(ARGUS_E_INVALID, "paged prefill: NULL pointer");
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(acc_o) | reinterpret_cast<uintptr_t>(ws)) & 15)
     return fail(ARGUS_E_INVALID, "paged prefill: q, acc_o and ws must be 16-byte aligned");
   SParams sp{};
-  bool seen[6] = {false, false, false, false, false, false};
+  bool seen[ARGUS_INT1_G32 + 1] = {};
   for (int i = 0; i < n_pools; ++i) {
     const argus_pool& pool = pools[i];
-    if (pool.codec < 0 || pool.codec > ARGUS_INT2_G32 || seen[pool.codec] || pool.n_slots < 0)
+    if (pool.codec < 0 || pool.codec > ARGUS_INT1_G32 || seen[pool.codec] || pool.n_slots < 0)
       return fail(ARGUS_E_INVALID, "paged prefill: pool %d (codec %d) invalid or repeated", i, pool.codec);
     seen[pool.codec] = true;
     if (pool.n_slots > 0) {

@@ -223,8 +223,8 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
       for (int e = 0; e < 8; ++e) deq[e] = (float)(int8_t)((w[e / 4] >> (8 * (e & 3))) & 0xFF) * scale;
     }
     reinterpret_cast<uint2*>(dcodes)[vec] = make_uint2(w[0], w[1]);
-  } else {  // INT4 / INT2: the 4 threads of a 32-element group cooperate
-    constexpr int BITS = (CODEC == ARGUS_INT4_G32) ? 4 : 2;
+  } else {  // INT4 / INT2 / INT1: the 4 threads of a 32-element group cooperate
+    constexpr int BITS = (CODEC == ARGUS_INT4_G32) ? 4 : (CODEC == ARGUS_INT2_G32 ? 2 : 1);
     constexpr int TOP = (1 << BITS) - 1;
     constexpr uint32_t MASK = (uint32_t)TOP;
     float lo = f[0], hi = f[0];
@@ -262,7 +262,7 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
         for (int e = 0; e < 8; ++e) t[e] = __float_as_uint(fminf(fmaxf(q.v[e], 0.f), (float)TOP) + kRoundMagic);
       }
       // code e of the 8 at bits BITS * e: INT4 even elements in the low
-      // nibbles, INT2 element 4k + j at bits 2j of byte k
+      // nibbles, INT2 element 4k + j at bits 2j of byte k, INT1 element e at bit e
 #pragma unroll
       for (int e = 0; e < 8; ++e) w |= (t[e] & MASK) << (BITS * e);
     }
@@ -272,7 +272,8 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
       for (int e = 0; e < 8; ++e) deq[e] = fmaf((float)((w >> (BITS * e)) & MASK), ss, zz);
     }
     if (BITS == 4) reinterpret_cast<uint32_t*>(dcodes)[vec] = w;
-    else reinterpret_cast<uint16_t*>(dcodes)[vec] = (uint16_t)w;
+    else if (BITS == 2) reinterpret_cast<uint16_t*>(dcodes)[vec] = (uint16_t)w;
+    else dcodes[vec] = (uint8_t)w;
     if ((lane_in_group & 3) == 0) {
       const __half2 sz = __halves2half2(__float2half_rn(ss), __float2half_rn(zz));
       *reinterpret_cast<__half2*>(dmeta_row) = sz;
@@ -312,6 +313,7 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_kernel(const QParams p) 
     if (CODEC == ARGUS_FP16 || CODEC == ARGUS_BF16) dcodes = p.dst_codes + unit_dst * (size_t)P * D * 2;
     else if (CODEC == ARGUS_INT4_G32) dcodes = p.dst_codes + unit_dst * (size_t)P * (D / 2);
     else if (CODEC == ARGUS_INT2_G32) dcodes = p.dst_codes + unit_dst * (size_t)P * (D / 4);
+    else if (CODEC == ARGUS_INT1_G32) dcodes = p.dst_codes + unit_dst * (size_t)P * (D / 8);
     else dcodes = p.dst_codes + unit_dst * (size_t)P * D;
 
     const bool regs = (GROUP == 32) && (nvec <= 32 * kRegVecs);
@@ -354,7 +356,7 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_kernel(const QParams p) 
       const bool valid_v = v < nvalid_vec;
       float deq[8];
       uint8_t* meta_row = nullptr;
-      if (CODEC == ARGUS_INT4_G32 || CODEC == ARGUS_INT2_G32) {
+      if (CODEC == ARGUS_INT4_G32 || CODEC == ARGUS_INT2_G32 || CODEC == ARGUS_INT1_G32) {
         const int row = v / VPR, grp = (v % VPR) / 4;
         meta_row = p.dst_meta + ((unit_dst * P + row) * (D / 32) + grp) * 4;
       }
@@ -424,11 +426,12 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_kernel(const QParams p) 
   }
 }
 
-// INT4 / INT2 with one lane per 32-element group (the group's four 16-byte
-// source vectors in x0..x3): the min / max reduction and the scale arithmetic
-// are lane-local and done once per group, and the 32 codes leave as one store
-// (16 bytes of INT4 in w[0..3], 8 bytes of INT2 in w[0..1]).  Same arithmetic,
-// hence the same codes, as encode_store's INT4 / INT2 path.
+// INT4 / INT2 / INT1 with one lane per 32-element group (the group's four
+// 16-byte source vectors in x0..x3): the min / max reduction and the scale
+// arithmetic are lane-local and done once per group, and the 32 codes leave as
+// one store (16 bytes of INT4 in w[0..3], 8 bytes of INT2 in w[0..1], 4 bytes
+// of INT1 in w[0]).  Same arithmetic, hence the same codes, as encode_store's
+// affine path.
 template <bool SBF16, int BITS>
 __device__ __forceinline__ void encode_affine_group(const uint4 (&x)[4], bool valid, uint32_t (&wout)[4],
                                                     uint32_t& meta) {
@@ -503,13 +506,19 @@ __device__ __forceinline__ void encode_affine_group(const uint4 (&x)[4], bool va
         const uint32_t ev = prmt(prmt(t[0], t[2], 0x0040), prmt(t[4], t[6], 0x0040), 0x5410);
         const uint32_t od = prmt(prmt(t[1], t[3], 0x0040), prmt(t[5], t[7], 0x0040), 0x5410);
         w[m] = ev + (od << 4);
-      } else {
+      } else if (BITS == 2) {
         // codes 0..3: byte 0 takes elements 0..3, byte 1 elements 4..7, element
         // j of a byte at bits 2j; xj holds elements j and 4 + j in bytes 0, 1
         const uint32_t x0 = prmt(t[0], t[4], 0x0040), x1 = prmt(t[1], t[5], 0x0040);
         const uint32_t x2 = prmt(t[2], t[6], 0x0040), x3 = prmt(t[3], t[7], 0x0040);
         const uint32_t w16 = (x0 | (x1 << 2) | (x2 << 4) | (x3 << 6)) & 0xFFFFu;
         w[m >> 1] |= w16 << (16 * (m & 1));
+      } else {
+        // codes 0..1: vector m's eight elements fill byte m, element e at bit e
+        uint32_t b = 0u;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) b |= (t[e] & 1u) << e;
+        w[0] |= b << (8 * m);
       }
     }
   }
@@ -559,7 +568,8 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_small_kernel(const QPara
   // INT4 units without a compressed key use one lane per 32-element group:
   // slot 4j + m holds vector m of group lane + 32j
   auto group_layout = [&](const Unit& d) {
-    return (CODEC == ARGUS_INT4_G32 || CODEC == ARGUS_INT2_G32) && !(want_ck_any && d.kv == 0);
+    return (CODEC == ARGUS_INT4_G32 || CODEC == ARGUS_INT2_G32 || CODEC == ARGUS_INT1_G32) &&
+           !(want_ck_any && d.kv == 0);
   };
   auto load = [&](const Unit& d, uint4 (&buf)[kRegVecs]) {
     const bool gl = group_layout(d);
@@ -586,7 +596,7 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_small_kernel(const QPara
       if (lane == 0 && cu.kv == 0 && cu.h == 0 && p.status) atomicAdd(p.status, 1u);
     } else if (group_layout(cu)) {
       constexpr int GPR = D / 32;  // groups per token row
-      constexpr int BITS = (CODEC == ARGUS_INT4_G32) ? 4 : 2;
+      constexpr int BITS = (CODEC == ARGUS_INT4_G32) ? 4 : (CODEC == ARGUS_INT2_G32 ? 2 : 1);
       uint8_t* gcodes = p.dst_codes + cu.dst * (size_t)P * (D * BITS / 8);
       uint32_t* gmeta = reinterpret_cast<uint32_t*>(p.dst_meta) + cu.dst * (size_t)P * GPR;
 #pragma unroll
@@ -598,7 +608,8 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_small_kernel(const QPara
           uint32_t m;
           encode_affine_group<SBF16, BITS>(xg, idx / GPR < cu.valid, c, m);
           if (BITS == 4) reinterpret_cast<uint4*>(gcodes)[idx] = make_uint4(c[0], c[1], c[2], c[3]);
-          else reinterpret_cast<uint2*>(gcodes)[idx] = make_uint2(c[0], c[1]);
+          else if (BITS == 2) reinterpret_cast<uint2*>(gcodes)[idx] = make_uint2(c[0], c[1]);
+          else reinterpret_cast<uint32_t*>(gcodes)[idx] = c[0];
           gmeta[idx] = m;
         }
       }
@@ -608,6 +619,7 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_small_kernel(const QPara
       if (CODEC == ARGUS_FP16 || CODEC == ARGUS_BF16) dcodes = p.dst_codes + cu.dst * (size_t)P * D * 2;
       else if (CODEC == ARGUS_INT4_G32) dcodes = p.dst_codes + cu.dst * (size_t)P * (D / 2);
       else if (CODEC == ARGUS_INT2_G32) dcodes = p.dst_codes + cu.dst * (size_t)P * (D / 4);
+      else if (CODEC == ARGUS_INT1_G32) dcodes = p.dst_codes + cu.dst * (size_t)P * (D / 8);
       else dcodes = p.dst_codes + cu.dst * (size_t)P * D;
       float scale = 0.f;
       if (CODEC == ARGUS_FP8_E4M3 || CODEC == ARGUS_INT8) {
@@ -639,7 +651,7 @@ __global__ void __launch_bounds__(kCtaThreads) quantize_small_kernel(const QPara
             float f[8], deq[8];
             unpack8<SBF16>(cur[k], f);
             uint8_t* meta_row = nullptr;
-            if (CODEC == ARGUS_INT4_G32 || CODEC == ARGUS_INT2_G32) {
+            if (CODEC == ARGUS_INT4_G32 || CODEC == ARGUS_INT2_G32 || CODEC == ARGUS_INT1_G32) {
               const int row = v / VPR, grp = (v % VPR) / 4;
               meta_row = p.dst_meta + ((cu.dst * P + row) * (D / 32) + grp) * 4;
             }
@@ -710,6 +722,7 @@ static argus_status launch2(int codec, const QParams& p, cudaStream_t s) {
     case ARGUS_FP8_E4M3: return launch3<D, SBF16, ARGUS_FP8_E4M3>(p, s);
     case ARGUS_INT8: return launch3<D, SBF16, ARGUS_INT8>(p, s);
     case ARGUS_INT2_G32: return launch3<D, SBF16, ARGUS_INT2_G32>(p, s);
+    case ARGUS_INT1_G32: return launch3<D, SBF16, ARGUS_INT1_G32>(p, s);
     default: return launch3<D, SBF16, ARGUS_INT4_G32>(p, s);
   }
 }
@@ -733,7 +746,7 @@ extern "C" argus_status argus_quantize_pages(const argus_geom* g, int32_t src_dt
     return fail(ARGUS_E_UNSUPPORTED, "quantize: head_dim %d (supported: 64, 128)", g->head_dim);
   if (src_dtype != ARGUS_FP16 && src_dtype != ARGUS_BF16)
     return fail(ARGUS_E_INVALID, "quantize: src_dtype must be FP16 or BF16");
-  if (dst->codec < 0 || dst->codec > ARGUS_INT2_G32) return fail(ARGUS_E_INVALID, "quantize: bad destination codec");
+  if (dst->codec < 0 || dst->codec > ARGUS_INT1_G32) return fail(ARGUS_E_INVALID, "quantize: bad destination codec");
   if ((dst->codec == ARGUS_FP16 || dst->codec == ARGUS_BF16) && dst->codec != src_dtype)
     return fail(ARGUS_E_UNSUPPORTED, "quantize: a 16-bit destination must match the source dtype");
   if (n_pages < 0) return fail(ARGUS_E_INVALID, "quantize: negative n_pages");

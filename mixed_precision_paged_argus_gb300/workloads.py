@@ -32,7 +32,7 @@ import math
 import numpy as np
 import torch
 
-FP16, BF16, FP8_E4M3, INT8, INT4_G32, INT2_G32 = 0, 1, 2, 3, 4, 5
+FP16, BF16, FP8_E4M3, INT8, INT4_G32, INT2_G32, INT1_G32 = 0, 1, 2, 3, 4, 5, 6
 
 WORKLOAD_IDS = {"tiny_fp16": 1, "mixed_tier": 2, "batched": 3, "sparse": 4,
                 "prefill": 5}

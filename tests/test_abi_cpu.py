@@ -69,7 +69,7 @@ def test_host_validation_without_gpu():
 
 
 def test_codec_range_window_and_int2_checks_without_gpu():
-    """Codec numbers outside 0..5 fail closed; an INT2 pool is accepted; a window
+    """Codec numbers outside 0..6 fail closed; INT2 and INT1 pools are accepted; a window
     rejects negative values and selection lists; a window shrinks the workspace."""
     L = _lib()
     n = ctypes.c_size_t(0)
@@ -86,7 +86,9 @@ def test_codec_range_window_and_int2_checks_without_gpu():
     keep = pools(argus.INT2_G32, argus.FP8_E4M3)
     assert L.argus_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 0
     full = n.value
-    keep = pools(6)
+    keep = pools(argus.INT1_G32, argus.INT8)
+    assert L.argus_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 0
+    keep = pools(7)
     assert L.argus_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 1
     keep = pools(argus.INT2_G32)
     a.window_tokens, a.sink_tokens = 64, 4
@@ -102,9 +104,9 @@ def test_codec_range_window_and_int2_checks_without_gpu():
     a.sel_width = 4
     assert L.argus_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 2
     del keep
-    # quantize: destination codec 6 is rejected before any device work
+    # quantize: destination codec 7 is rejected before any device work
     g = argus.geom(8, 2, 128, 16)
-    dst = argus.PoolDesc(6, 0, 16, 16, 4)
+    dst = argus.PoolDesc(7, 0, 16, 16, 4)
     assert L.argus_quantize_pages(ctypes.byref(g), argus.FP16, 16, 4, 16, ctypes.byref(dst), 16, 1,
                                   None, None, None, None) == 1
 

@@ -38,7 +38,7 @@ def _check(c, out, out32, lse, sel=None, cnt=None, width=0, expect_bad=0, window
     return err
 
 
-@pytest.mark.parametrize("codec", [W.FP16, W.FP8_E4M3, W.INT8, W.INT4_G32, W.INT2_G32])
+@pytest.mark.parametrize("codec", [W.FP16, W.FP8_E4M3, W.INT8, W.INT4_G32, W.INT2_G32, W.INT1_G32])
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("G", [1, 7, 8])
 def test_single_codec_fp16_query(codec, D, G):
@@ -51,7 +51,7 @@ def test_single_codec_fp16_query(codec, D, G):
     _check(c, out, out32, lse)
 
 
-@pytest.mark.parametrize("codec", [W.BF16, W.FP8_E4M3, W.INT8, W.INT4_G32, W.INT2_G32])
+@pytest.mark.parametrize("codec", [W.BF16, W.FP8_E4M3, W.INT8, W.INT4_G32, W.INT2_G32, W.INT1_G32])
 @pytest.mark.parametrize("G", [4, 8])
 def test_single_codec_bf16_query(codec, G):
     Hkv, D, P = 2, 128, 16
@@ -389,3 +389,21 @@ def test_int2_selected_pages():
     out, out32, lse, _ = run_decode(c, out_dtype=torch.bfloat16, sel=torch.from_numpy(sel).to(DEV),
                                     sel_count=torch.from_numpy(cnt).to(DEV), sel_width=width)
     _check(c, out, out32, lse, sel=sel, cnt=cnt, width=width)
+
+
+@pytest.mark.parametrize("q_dtype", [W.FP16, W.BF16])
+@pytest.mark.parametrize("D", [64, 128])
+def test_six_tiers_with_int1_oldest(q_dtype, D):
+    """Every tier in one row, oldest first: 1-bit, INT2, INT4, INT8, FP8 and the
+    16-bit tier; ragged rows, several split counts, with and without a window."""
+    Hq, Hkv, P = 16, 2, 64
+    top = W.FP16 if q_dtype == W.FP16 else W.BF16
+    row = np.array([W.INT1_G32] * 3 + [W.INT2_G32] * 3 + [W.INT4_G32] * 3 + [W.INT8] * 3 + [W.FP8_E4M3] * 3 + [top] * 3)
+    pc = np.stack([row, np.roll(row, 5)])
+    c = build_case(Hq, Hkv, D, P, [18 * P - 11, 600], pc, q_dtype, seed=660 + D, outliers=True)
+    out_dtype = torch.float16 if q_dtype == W.FP16 else torch.bfloat16
+    for splits in (0, 1, 4):
+        out, out32, lse, _ = run_decode(c, out_dtype=out_dtype, num_splits=splits)
+        _check(c, out, out32, lse)
+    out, out32, lse, _ = run_decode(c, out_dtype=out_dtype, window=250, sinks=4)
+    _check(c, out, out32, lse, window=250, sinks=4)

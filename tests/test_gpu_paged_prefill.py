@@ -112,7 +112,7 @@ def _run_paged(c, n_q, ctx, cuts, splits=0, status=None):
     return acc_o.cpu().numpy(), acc_l.cpu().numpy()
 
 
-FIVE = [W.INT2_G32, W.INT4_G32, W.INT8, W.FP8_E4M3, W.BF16]
+FIVE = [W.INT1_G32, W.INT2_G32, W.INT4_G32, W.INT8, W.FP8_E4M3, W.BF16]   # every tier (16-bit as BF16)
 
 
 @pytest.mark.parametrize("splits", [1, 0, 3])
@@ -128,7 +128,7 @@ def test_paged_windows_five_tiers_fold_to_single_pass(P, n_q, ctx, cuts, splits)
     _check(go, gl, ro, rl, _staged_lse_bound(c, ctx + n_q))
 
 
-@pytest.mark.parametrize("codec", [W.FP16, W.BF16, W.FP8_E4M3, W.INT8, W.INT4_G32, W.INT2_G32])
+@pytest.mark.parametrize("codec", [W.FP16, W.BF16, W.FP8_E4M3, W.INT8, W.INT4_G32, W.INT2_G32, W.INT1_G32])
 def test_paged_window_single_codec(codec):
     c = _paged(8, 1, 16, 96, 500, [codec], seed=740 + codec)
     go, gl = _run_paged(c, 96, 500, [250])

@@ -90,7 +90,7 @@ def test_int8_rounding_exhaustive_over_fp16():
     _compare(pool, codes, meta)
 
 
-@pytest.mark.parametrize("codec", [W.FP8_E4M3, W.INT8, W.INT4_G32, W.INT2_G32, "copy"])
+@pytest.mark.parametrize("codec", [W.FP8_E4M3, W.INT8, W.INT4_G32, W.INT2_G32, W.INT1_G32, "copy"])
 @pytest.mark.parametrize("src_dtype", [W.FP16, W.BF16])
 @pytest.mark.parametrize("D,P", [(64, 16), (128, 16), (128, 64), (64, 1024)])
 def test_random_pages_bit_exact_with_ckeys(codec, src_dtype, D, P):
@@ -133,7 +133,7 @@ def test_bad_slots_are_counted_and_skipped():
 def test_zero_unit_gives_zero_scale():
     Hkv, P, D = 1, 16, 128
     src = torch.zeros((1, 2, Hkv, P, D), dtype=torch.bfloat16)
-    for codec in (W.FP8_E4M3, W.INT8, W.INT4_G32, W.INT2_G32):
+    for codec in (W.FP8_E4M3, W.INT8, W.INT4_G32, W.INT2_G32, W.INT1_G32):
         pool, _, _ = _gpu_quantize(src, W.BF16, codec, Hkv, P, D, [0], [0], 1)
         assert not _codes_np(pool).any() and not _meta_np(pool).any()
 
@@ -183,7 +183,7 @@ def test_codes_near_rounding_boundaries_with_a_non_power_of_two_scale(codec):
     _compare(pool, codes, meta)
 
 
-@pytest.mark.parametrize("codec", [W.INT4_G32, W.INT2_G32])
+@pytest.mark.parametrize("codec", [W.INT4_G32, W.INT2_G32, W.INT1_G32])
 @pytest.mark.parametrize("ckey", [False, True])
 @pytest.mark.parametrize("src_dtype", [W.FP16, W.BF16])
 def test_int4_groups_with_pinned_range_and_interior_values(ckey, src_dtype, codec):
@@ -192,7 +192,7 @@ def test_int4_groups_with_pinned_range_and_interior_values(ckey, src_dtype, code
     s is a power of two); INT4 V units use the one-lane-per-group path, K units
     the compressed-key path when ckey is set; INT2 units the cooperative path."""
     Hkv, P, D, n = 2, 16, 128, 48
-    top = 15 if codec == W.INT4_G32 else 3
+    top = {W.INT4_G32: 15, W.INT2_G32: 3, W.INT1_G32: 1}[codec]
     rng = np.random.default_rng(7 + ckey + 2 * src_dtype + codec)
     groups = n * 2 * Hkv * P * (D // 32)
     z = rng.standard_normal(groups) * 4
@@ -216,7 +216,7 @@ def test_int4_groups_with_pinned_range_and_interior_values(ckey, src_dtype, code
     _compare(pool, codes, meta)
 
 
-@pytest.mark.parametrize("codec", [W.INT4_G32, W.INT2_G32])
+@pytest.mark.parametrize("codec", [W.INT4_G32, W.INT2_G32, W.INT1_G32])
 @pytest.mark.parametrize("ckey", [False, True])
 def test_affine_zero_point_and_scale_saturate_at_65504(codec, ckey):
     """bf16 groups whose min is below -65504 or whose (max - z) / top is above
@@ -249,7 +249,7 @@ def test_affine_zero_point_and_scale_saturate_at_65504(codec, ckey):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("codec", [W.FP8_E4M3, W.INT8, W.INT4_G32, W.INT2_G32])
+@pytest.mark.parametrize("codec", [W.FP8_E4M3, W.INT8, W.INT4_G32, W.INT2_G32, W.INT1_G32])
 @pytest.mark.parametrize("ckey", [False, True])
 def test_full_size_demotion_bit_exact_on_sampled_pages(codec, ckey):
     """The batched workload's unit shape (16 x 128 bf16) at 20,480 pages x 8 KV
