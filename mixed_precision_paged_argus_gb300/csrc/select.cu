@@ -16,12 +16,18 @@
 // lanes read 16 bytes of a compressed key each, eight rows' loads in flight,
 // and fold eight rows' partial dot products across the head's lanes in one
 // transposed reduction; the G-query sum is formed once per CTA and kept in
-// registers; scores are stored as order-preserving uint32 keys.
-// (2) top-k: one CTA per (batch row, KV head) stages the row's keys in shared
-// memory and registers; each warp narrows its keys to those at or above its
-// own k-th largest, the k-th largest of the survivors is the row's threshold
-// (both searches two bits per round by warp reductions), then the chosen
-// pages are compacted in ascending order with block-wide prefix sums.
+// registers; scores are stored as order-preserving uint32 keys.  Each CTA also
+// reports, per KV head, the 4 largest keys of its own page range.
+// (2) top-k: one CTA per (batch row, KV head).  The row's k-th largest key T is
+// at least T0, the k-th largest of the reported keys (they are keys of
+// distinct pages of the row), and since the row's top k rarely crowd more than
+// 4 into one range, T0 is T or close to it: only the keys >= T0 -- about k of
+// them -- are searched.  The top-k grid starts behind the score grid with
+// programmatic dependent launch.  They are compacted in page order, one warp finds T
+// among them (two bits per round by warp reductions) and writes the chosen
+// pages, ascending, with ties to the lower page index.  Many keys >= T0 (heavy
+// ties) or rows longer than the registers hold take block-wide searches over
+// every key.
 #include <algorithm>
 
 #include "common.cuh"
@@ -35,6 +41,24 @@ constexpr int kTopkThreads = 512;
 constexpr int kKeysPerThread = 8;             // top-k keys held in registers per thread
 constexpr int kRowBatch = 8;               // compressed-key loads in flight per lane
 constexpr int kTopkSmemKeys = 40 * 1024;   // rows up to this many pages are staged in shared memory
+constexpr int kMaxPpc = 256;               // pages per score CTA (its keys per head in registers)
+constexpr int kEmit = 4;                   // largest keys each score CTA reports per KV head
+constexpr long long kScoreSmemBytes = 75 * 1024;   // a score CTA's shared memory (3 CTAs per SM)
+
+// Whether each score lane's rows all belong to one KV head (the rows per pass
+// are a multiple of Hkv): its G-query sums then live in registers.
+__host__ __device__ constexpr bool score_fixed_head(int D, int Hkv) {
+  return ((kScoreThreads / 32) * (32 / (D / 8))) % Hkv == 0;
+}
+
+// Dynamic shared memory of a score CTA: its range's compressed keys, the
+// G-query sums (only when lanes mix heads), the range's order keys, an mbarrier.
+inline size_t score_smem_bytes(long long Hkv, long long D, long long ppc) {
+  const size_t slab = ((size_t)ppc * Hkv * D * 2 + 127) / 128 * 128;
+  const size_t qs = score_fixed_head((int)D, (int)Hkv) ? 0 : (size_t)Hkv * D * 4;
+  return slab + qs + (size_t)((ppc * Hkv + 1) & ~1LL) * 4 + 16;
+}
+constexpr int kSurvivorsPerLane = 16;      // keys >= T0 that one warp searches in registers
 
 // Order-preserving map of an fp32 score to uint32: a > b  <=>  key(a) > key(b).
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -42,14 +66,89 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Writes the order key of each page's score, [B][Hkv][max_pages] uint32.
+// The kk-th largest of the values a warp holds (nv per lane; empty slots hold
+// 0, which no candidate -- always >= 1 -- counts): two bits per round, the
+// three candidate counts in two warp reductions.  No barrier.  (A key of 0 is
+// the order key of a negative NaN score: NaN scores are unordered.)
+template <int NV>
+__device__ __forceinline__ uint32_t warp_kth(const uint32_t (&vals)[NV], int kk) {
+  uint32_t t = 0u;
+  for (int bb = 30; bb >= 0; bb -= 2) {
+    const uint32_t c1 = t | (1u << bb), c2 = t | (2u << bb), c3 = t | (3u << bb);
+    uint32_t a = 0u, c = 0u;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      a += (vals[j] >= c1 ? 1u : 0u) + (vals[j] >= c2 ? 0x10000u : 0u);
+      c += vals[j] >= c3 ? 1u : 0u;
+    }
+    a = __reduce_add_sync(0xffffffffu, a);
+    c = __reduce_add_sync(0xffffffffu, c);
+    if (c >= (uint32_t)kk) t = c3;
+    else if ((a >> 16) >= (uint32_t)kk) t = c2;
+    else if ((a & 0xFFFFu) >= (uint32_t)kk) t = c1;
+  }
+  return t;
+}
+
+// The kEmit largest keys of each KV head over one score CTA's candidate pages
+// (out of line: it runs once per CTA and keeps its registers apart from the
+// scoring loop's).  Warp w takes KV heads w, w + 8, ...; lane l holds the keys
+// of pages l + 32 m of the range (skeys [page][Hkv]); each round takes the
+// warp's maximum and removes one instance of it.  out[h * stride + j], j <
+// kEmit, gets the j-th largest key, or 0 past the range's n_loc candidates.
+__device__ __noinline__ void local_top(const uint32_t* skeys, int Hkv, int n_loc, uint32_t* out, int stride) {
+  const int lane = threadIdx.x & 31;
+  for (int h = threadIdx.x >> 5; h < Hkv; h += kScoreThreads / 32) {
+    uint32_t v[kMaxPpc / 32];
+#pragma unroll
+    for (int m = 0; m < kMaxPpc / 32; ++m) {
+      const int lp = lane + 32 * m;
+      v[m] = lp < n_loc ? skeys[lp * Hkv + h] : 0u;
+    }
+    for (int j = 0; j < kEmit; ++j) {
+      uint32_t mx = 0u;
+#pragma unroll
+      for (int m = 0; m < kMaxPpc / 32; ++m) mx = max(mx, v[m]);
+      const uint32_t top = __reduce_max_sync(0xffffffffu, mx);
+      // the lowest lane holding it drops one instance
+      const uint32_t holders = __ballot_sync(0xffffffffu, mx == top);
+      if (top != 0u && lane == __ffs(holders) - 1) {
+        bool done = false;
+#pragma unroll
+        for (int m = 0; m < kMaxPpc / 32; ++m) {
+          if (!done && v[m] == top) {
+            v[m] = 0u;
+            done = true;
+          }
+        }
+      }
+      if (lane == 0) out[(size_t)h * stride + j] = top;
+    }
+  }
+}
+
+// Writes the order key of each page's score, [B][Hkv][max_pages] uint32, and
+// (emit != NULL) each KV head's kEmit largest keys over the CTA's candidate
+// pages (below n_cand(b) = n - 1 with keep_newest, else n),
+// emit[B][Hkv][gridDim.x][kEmit], 0 where the range has fewer.
 template <int D, bool QBF16>
-__global__ void __launch_bounds__(kScoreThreads) score_kernel(int Hkv, int G, int max_pages, int ppc,
+__global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) score_kernel(int Hkv, int G, int max_pages, int ppc,
                                                               const void* __restrict__ q,
                                                               const uint16_t* __restrict__ ckeys,
                                                               const int32_t* __restrict__ n_pages,
-                                                              uint32_t* __restrict__ keys) {
-  extern __shared__ float qsum[];  // [Hkv][D]
+                                                              uint32_t* __restrict__ keys, int keep_newest,
+                                                              uint32_t* __restrict__ emit) {
+  // the top-k grid may start its prologue now; it waits for this grid's keys
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // shared memory: the range's compressed keys [ppc * Hkv][D] bf16, the
+  // G-query sums [Hkv][D] fp32, the range's order keys [ppc][Hkv], an mbarrier
+  extern __shared__ __align__(128) uint8_t sm_raw[];
+  const size_t slab_bytes = ((size_t)ppc * Hkv * D * 2 + 127) / 128 * 128;
+  const uint16_t* slab = reinterpret_cast<const uint16_t*>(sm_raw);
+  const bool fixed_h = score_fixed_head(D, Hkv);
+  float* qsum = reinterpret_cast<float*>(sm_raw + slab_bytes);   // [Hkv][D] when !fixed_h
+  uint32_t* skeys = reinterpret_cast<uint32_t*>(qsum + (fixed_h ? 0 : Hkv * D));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(skeys + ((ppc * Hkv + 1) & ~1));
   const int b = blockIdx.y;
   const int p0 = blockIdx.x * ppc;
   const int Hq = Hkv * G;
@@ -63,26 +162,33 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(int Hkv, int G, in
   const int sub = lane / LPH, li = lane % LPH;
   const int p_end = min(n, p0 + ppc);
   const int n_rows = (p_end - p0) * Hkv;
-  // rows of this CTA are contiguous in the slab: (p0 * Hkv + row) * D
-  const uint16_t* base = ckeys + (((size_t)b * max_pages + p0) * Hkv) * D + 8 * li;
-  // the first batch of rows does not depend on the q sums: its loads go out
-  // before them, so the two latencies overlap
+  // rows of this CTA are contiguous in the slab: (p0 * Hkv + row) * D.  One
+  // thread streams them into shared memory with bulk copies (16 KB pieces on
+  // one mbarrier) before the query sums, so the whole range is in flight at once
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    const uint32_t total = (uint32_t)n_rows * D * 2;
+    mbar_arrive_expect_tx(bar, total);
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(ckeys + (((size_t)b * max_pages + p0) * Hkv) * D);
+    for (uint32_t off = 0; off < total; off += 16384u)
+      bulk_g2s(sm_raw + off, src + off, min(16384u, total - off), bar);
+  }
   uint4 x[kRowBatch];
   auto load_batch = [&](int r0) {
 #pragma unroll
     for (int j = 0; j < kRowBatch; ++j) {
       const int row = r0 + j * RPP;
-      if (row < n_rows) x[j] = __ldcs(reinterpret_cast<const uint4*>(base + (size_t)row * D));
+      if (row < n_rows) x[j] = *reinterpret_cast<const uint4*>(slab + (size_t)row * D + 8 * li);
       else x[j] = make_uint4(0u, 0u, 0u, 0u);
     }
   };
-  load_batch(warp * RPW + sub);
   const uint16_t* qb = static_cast<const uint16_t*>(q) + (size_t)b * Hq * D;
-  // G-query sums: a thread per (KV head, 8 dims); the rows' 16-byte loads are
-  // issued together, eight at a time
-  for (int idx = threadIdx.x; idx < Hkv * (D / 8); idx += blockDim.x) {
-    const int h = idx / (D / 8), c = idx - h * (D / 8);
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  // sum over the G query heads of head h of dims 8 c .. 8 c + 7; the rows'
+  // 16-byte loads are issued together, eight at a time
+  auto q_sum8 = [&](int h, int c, float (&acc)[8]) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
     for (int g0 = 0; g0 < G; g0 += 8) {
       uint4 xs[8];
 #pragma unroll
@@ -99,22 +205,28 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(int Hkv, int G, in
         }
       }
     }
+  };
+  // a lane whose rows share one KV head keeps that head's sums in registers;
+  // otherwise the CTA forms every head's sums in shared memory
+  float qv[8];
+  if (fixed_h) {
+    q_sum8((warp * RPW + sub) % Hkv, li, qv);
+  } else {
+    for (int idx = threadIdx.x; idx < Hkv * (D / 8); idx += blockDim.x) {
+      const int h = idx / (D / 8), c = idx - h * (D / 8);
+      float acc[8];
+      q_sum8(h, c, acc);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) qsum[h * D + 8 * c + e] = acc[e];
+      for (int e = 0; e < 8; ++e) qsum[h * D + 8 * c + e] = acc[e];
+    }
   }
   __syncthreads();
-  // when Hkv divides the rows per pass, a lane's rows all belong to one KV
-  // head: its 8 q-sum values stay in registers
-  const bool fixed_h = (RPP % Hkv) == 0;
-  float qv[8];
-  {
-    const int h0 = (warp * RPW + sub) % Hkv;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) qv[e] = qsum[h0 * D + 8 * li + e];
-  }
+  // the rows have landed (a copy that never completes leaves this CTA's keys
+  // unwritten rather than waiting forever)
+  if (!mbar_wait(bar, 0)) return;
   static_assert(kRowBatch == 8, "the transposed reduction below folds 8 rows");
   for (int r0 = warp * RPW + sub; r0 - sub < n_rows; r0 += kRowBatch * RPP) {
-    if (r0 != warp * RPW + sub) load_batch(r0);   // the first batch is already loaded
+    load_batch(r0);
     float sv[kRowBatch];
 #pragma unroll
     for (int j = 0; j < kRowBatch; ++j) {
@@ -172,9 +284,16 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(int Hkv, int G, in
     // (with LPH = 16, lanes li and li ^ 1 hold the same row: the even one writes)
     if ((LPH == 8 || (li & 1) == 0) && row < n_rows) {
       const int p = p0 + row / Hkv;
-      keys[((size_t)b * Hkv + row % Hkv) * max_pages + p] = order_key(v1);
+      const uint32_t key = order_key(v1);
+      keys[((size_t)b * Hkv + row % Hkv) * max_pages + p] = key;
+      skeys[row] = key;
     }
   }
+  if (emit == nullptr) return;
+  __syncthreads();
+  const int n_cand = keep_newest ? n - 1 : n;
+  local_top(skeys, Hkv, max(0, min(p_end, n_cand) - p0),
+            emit + ((size_t)b * Hkv * gridDim.x + blockIdx.x) * kEmit, gridDim.x * kEmit);
 }
 
 // Exclusive block-wide prefix sum of one int per thread; returns the total.
@@ -205,17 +324,20 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* sh, int& total) 
 }
 
 // One CTA per (KV head, batch row).  The row's keys are staged in shared
-// memory when stage != 0 (dynamic shared memory of max_pages words).
+// memory when stage != 0 (dynamic shared memory of max_pages words).  emit:
+// the score kernel's largest keys per page range (n_chunks ranges of ppc
+// pages per row, kEmit keys each).
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pages, const uint32_t* keys_g,
                                                             const int32_t* n_pages, int top_k, int keep_newest,
                                                             int32_t* sel_pages, int32_t* sel_count, int width,
-                                                            uint32_t* drops, int stage) {
+                                                            uint32_t* drops, int stage, const uint32_t* emit_g,
+                                                            int n_chunks, int ppc) {
   extern __shared__ uint32_t skeys[];
   __shared__ int sh_scan[32];
   __shared__ uint2 sh_cnt2[2][32];
-  __shared__ int sh_wc[32];
-  __shared__ uint32_t sh_thr[2];
-  __shared__ uint32_t sh_cand[kKeysPerThread * kTopkThreads];   // survivors of the per-warp search
+  __shared__ uint32_t sh_t0;
+  __shared__ uint32_t sh_cand[kKeysPerThread * kTopkThreads];   // keys >= T0, in page order
+  __shared__ uint16_t sh_page[kKeysPerThread * kTopkThreads];   // their pages
   const int h = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5;
@@ -231,36 +353,143 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pag
   const int k_want = min(top_k, n_cand);
   const int k = max(0, min(k_want, room));
   if (tid == 0) dropped += (uint32_t)(k_want - k);
+  // launched behind the score grid with programmatic dependent launch: its
+  // keys are read after this wait
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int KPT = kKeysPerThread;
+  const bool in_regs = n_cand <= KPT * nthr;
+  const bool search = k > 0 && k < n_cand;
+
+  // ---- fast path: the keys >= T0, in page order, searched by one warp
+  if (search && in_regs) {
+    // thread t holds pages [KPT t, KPT t + KPT): page order is (thread, slot)
+    uint32_t kr[KPT];
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      const int pk = KPT * tid + j;
+      kr[j] = pk < n_cand ? keys[pk] : 0u;
+    }
+    // T0 = the k-th largest of the keys the ranges reported: real keys of
+    // distinct pages, so T0 <= T, the row's k-th largest (0 when the report is
+    // too long to hold, or holds fewer than k keys)
+    // (warp 0 alone, then one barrier)
+    const int n_ranges = min(n_chunks, (n_cand + ppc - 1) / ppc);
+    const int n_emit = n_ranges * kEmit;
+    if (warp == 0) {
+      uint32_t t0w = 0u;
+      const uint32_t* er = emit_g + ((size_t)b * Hkv + h) * n_chunks * kEmit;
+      if (n_emit >= k && n_emit <= 256) {   // eight per lane
+        uint32_t ev[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const int i = lane + 32 * m;
+          ev[m] = i < n_emit ? er[i] : 0u;
+        }
+        t0w = warp_kth(ev, k);
+      } else if (n_emit >= k && n_emit <= 32 * kSurvivorsPerLane) {
+        uint32_t ev[kSurvivorsPerLane];
+#pragma unroll
+        for (int m = 0; m < kSurvivorsPerLane; ++m) {
+          const int i = lane + 32 * m;
+          ev[m] = i < n_emit ? er[i] : 0u;
+        }
+        t0w = warp_kth(ev, k);
+      }
+      if (lane == 0) sh_t0 = t0w;
+    }
+    __syncthreads();
+    const uint32_t t0 = sh_t0;
+    int my = 0;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) my += (KPT * tid + j < n_cand && kr[j] >= t0) ? 1 : 0;
+    int M;
+    int pos = block_exclusive_scan(my, sh_scan, M);
+    if (M <= 32 * kSurvivorsPerLane) {
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) {
+        const int pk = KPT * tid + j;
+        if (pk < n_cand && kr[j] >= t0) {
+          sh_cand[pos] = kr[j];
+          sh_page[pos] = (uint16_t)pk;
+          ++pos;
+        }
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // survivor i = lane + 32 m: index order is page order
+        uint32_t cv[kSurvivorsPerLane];
+#pragma unroll
+        for (int m = 0; m < kSurvivorsPerLane; ++m) {
+          const int i = lane + 32 * m;
+          cv[m] = i < M ? sh_cand[i] : 0u;
+        }
+        uint32_t T;
+        if (M <= 64) {   // the usual case: about k survivors, two per lane
+          const uint32_t c2[2] = {cv[0], cv[1]};
+          T = warp_kth(c2, k);
+        } else {
+          T = warp_kth(cv, k);
+        }
+        uint32_t gt = 0u;
+#pragma unroll
+        for (int m = 0; m < kSurvivorsPerLane; ++m) gt += cv[m] > T ? 1u : 0u;
+        gt = __reduce_add_sync(0xffffffffu, gt);
+        const int k_rem = k - (int)gt;   // ties at T taken, lowest pages first
+        int written = 0, ties_seen = 0;
+        const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+        for (int m = 0; m < kSurvivorsPerLane; ++m) {
+          const int i = lane + 32 * m;
+          const bool tie = i < M && cv[m] == T;
+          const uint32_t tb = __ballot_sync(0xffffffffu, tie);
+          const bool take = (i < M && cv[m] > T) || (tie && ties_seen + __popc(tb & below) < k_rem);
+          const uint32_t kb = __ballot_sync(0xffffffffu, take);
+          if (take) out[written + __popc(kb & below)] = sh_page[i];
+          written += __popc(kb);
+          ties_seen += __popc(tb);
+        }
+        // written == k <= room; the newest page (larger than every candidate) last
+        int total = written;
+        if (keep_newest && n > 0) {
+          if (lane == 0) out[total] = n - 1;
+          ++total;
+        }
+        for (int i = total + lane; i < width; i += 32) out[i] = -1;
+        if (lane == 0) {
+          sel_count[(size_t)b * Hkv + h] = total;
+          if (dropped && drops) atomicAdd(drops, dropped);
+        }
+      }
+      return;
+    }
+    __syncthreads();   // many ties: fall through to the block-wide search
+  }
+
   if (stage) {  // eight loads in flight per thread
     for (int p0 = 0; p0 < n_cand; p0 += 8 * nthr) {
       uint32_t v[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int pk = p0 + k * nthr + tid;
-        v[k] = pk < n_cand ? keys[pk] : 0u;
+      for (int kk = 0; kk < 8; ++kk) {
+        const int pk = p0 + kk * nthr + tid;
+        v[kk] = pk < n_cand ? keys[pk] : 0u;
       }
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int pk = p0 + k * nthr + tid;
-        if (pk < n_cand) skeys[pk] = v[k];
+      for (int kk = 0; kk < 8; ++kk) {
+        const int pk = p0 + kk * nthr + tid;
+        if (pk < n_cand) skeys[pk] = v[kk];
       }
     }
     keys = skeys;
     __syncthreads();
   }
 
-  // Threshold: T = the k-th largest key, found bit by bit from the top as the
-  // largest value with at least k keys >= T (block-wide counts: per-warp
-  // reductions, double-buffered partial sums, one barrier per bit).  All keys
-  // > T are taken, and the first k_rem (in page order) equal to T.
-  const uint32_t mask = 0xFFFFFFFFu;
+  // Block-wide threshold: T = the k-th largest key, found bit by bit from the
+  // top as the largest value with at least k keys >= T (block-wide counts:
+  // per-warp reductions, double-buffered partial sums, one barrier per two
+  // bits).  All keys > T are taken, and the first k_rem (in page order) equal to T.
   uint32_t T = 0u;
   int k_rem = 0;
-  if (k > 0 && k < n_cand) {
-    // up to kKeysPerThread keys per thread live in registers; longer rows are
-    // re-read from memory every bit
-    constexpr int KPT = kKeysPerThread;
-    const bool in_regs = n_cand <= KPT * nthr;
+  if (search) {
     uint32_t kr[KPT];
     bool kv[KPT];
 #pragma unroll
@@ -270,17 +499,17 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pag
       kr[j] = kv[j] ? keys[pk] : 0u;
     }
     // counts of keys >= a, >= b (strict: > a) packed as two 16-bit fields
-    // (a row has at most kTopkSmemKeys < 2^16 candidates), one reduction
-    auto count2 = [&](uint32_t a, uint32_t b, bool strict) -> uint32_t {
+    // (a row has at most 65535 candidates), one reduction
+    auto count2 = [&](uint32_t a, uint32_t bnd, bool strict) -> uint32_t {
       uint32_t c = 0;
       if (in_regs) {
 #pragma unroll
         for (int j = 0; j < KPT; ++j)
-          c += kv[j] ? ((strict ? kr[j] > a : kr[j] >= a) ? 1u : 0u) + (kr[j] >= b ? 0x10000u : 0u) : 0u;
+          c += kv[j] ? ((strict ? kr[j] > a : kr[j] >= a) ? 1u : 0u) + (kr[j] >= bnd ? 0x10000u : 0u) : 0u;
       } else {
         for (int pk = tid; pk < n_cand; pk += nthr) {
           const uint32_t x = keys[pk];
-          c += ((strict ? x > a : x >= a) ? 1u : 0u) + (x >= b ? 0x10000u : 0u);
+          c += ((strict ? x > a : x >= a) ? 1u : 0u) + (x >= bnd ? 0x10000u : 0u);
         }
       }
       return __reduce_add_sync(0xffffffffu, c);
@@ -294,104 +523,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pag
       const uint2 x = lane < (nthr >> 5) ? sh_cnt2[buf][lane] : make_uint2(0u, 0u);
       return make_uint2(__reduce_add_sync(0xffffffffu, x.x), __reduce_add_sync(0xffffffffu, x.y));
     };
-    // Warp-level search for the kk-th largest of the values a warp holds
-    // (nv per lane in registers, valid flags vf): two bits per round, the
-    // three candidate counts in two warp reductions.  No barrier.
-    // Empty slots hold 0, which no candidate (always >= 1) counts.  (A key of 0
-    // is the order key of a negative NaN score: NaN scores are unordered.)
-    auto warp_kth = [&](const uint32_t* vals, int nv, int kk) -> uint32_t {
-      uint32_t t = 0u;
-      for (int bb = 30; bb >= 0; bb -= 2) {
-        const uint32_t c1 = t | (1u << bb), c2 = t | (2u << bb), c3 = t | (3u << bb);
-        uint32_t a = 0u, c = 0u;
-        for (int j = 0; j < nv; ++j) {
-          a += (vals[j] >= c1 ? 1u : 0u) + (vals[j] >= c2 ? 0x10000u : 0u);
-          c += vals[j] >= c3 ? 1u : 0u;
-        }
-        a = __reduce_add_sync(0xffffffffu, a);
-        c = __reduce_add_sync(0xffffffffu, c);
-        if (c >= (uint32_t)kk) t = c3;
-        else if ((a >> 16) >= (uint32_t)kk) t = c2;
-        else if ((a & 0xFFFFu) >= (uint32_t)kk) t = c1;
-      }
-      return t;
-    };
-    if (in_regs) {
-      // (1) each warp keeps its keys >= its own min(k, n_w)-th largest: every
-      // key >= the row's k-th largest survives, so (2) the row's threshold is
-      // the k-th largest of the survivors, found by every warp alike
-      int nw_valid = 0;
-#pragma unroll
-      for (int j = 0; j < KPT; ++j) nw_valid += kv[j] ? 1 : 0;
-      nw_valid = (int)__reduce_add_sync(0xffffffffu, (uint32_t)nw_valid);
-      const int kw = min(k, nw_valid);
-      const uint32_t Tw = kw > 0 ? warp_kth(kr, KPT, kw) : 0xFFFFFFFFu;
-      int my = 0;
-#pragma unroll
-      for (int j = 0; j < KPT; ++j) my += (kv[j] && kw > 0 && kr[j] >= Tw) ? 1 : 0;
-      int incl = my;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (lane == 31) sh_wc[warp] = incl;
-      __syncthreads();
-      const int nwarps = nthr >> 5;
-      const int wcl = lane < nwarps ? sh_wc[lane] : 0;
-      const int M = (int)__reduce_add_sync(0xffffffffu, (uint32_t)wcl);
-      const int wbase = (int)__reduce_add_sync(0xffffffffu, (uint32_t)(lane < warp ? wcl : 0));
-      int pos = wbase + incl - my;
-#pragma unroll
-      for (int j = 0; j < KPT; ++j)
-        if (kv[j] && kw > 0 && kr[j] >= Tw) sh_cand[pos++] = kr[j];
-      __syncthreads();
-      constexpr int CPL = 16;   // survivors per lane held in registers
-      if (M <= 32 * CPL) {
-        // one warp searches the survivors; the others wait for its answer
-        if (warp == 0) {
-          uint32_t cv[CPL];
-#pragma unroll
-          for (int m = 0; m < CPL; ++m) {
-            const int i = lane + 32 * m;
-            cv[m] = i < M ? sh_cand[i] : 0u;
-          }
-          const uint32_t t = warp_kth(cv, CPL, k);
-          uint32_t gt = 0u;
-#pragma unroll
-          for (int m = 0; m < CPL; ++m) gt += cv[m] > t ? 1u : 0u;
-          gt = __reduce_add_sync(0xffffffffu, gt);
-          if (lane == 0) {
-            sh_thr[0] = t;
-            sh_thr[1] = (uint32_t)(k - (int)gt);
-          }
-        }
-        __syncthreads();
-        T = sh_thr[0];
-        k_rem = (int)sh_thr[1];
-      } else {
-        // many survivors (ties): block-wide search over every key
-        for (int b = 30, round = 0; b >= 0; b -= 2, ++round) {
-          const uint32_t c1 = T | (1u << b), c2 = T | (2u << b), c3 = T | (3u << b);
-          const uint2 n = block_total2(count2(c1, c2, false), count2(c3, 0xFFFFFFFFu, false), round & 1);
-          if ((n.y & 0xFFFFu) >= (uint32_t)k) T = c3;
-          else if ((n.x >> 16) >= (uint32_t)k) T = c2;
-          else if ((n.x & 0xFFFFu) >= (uint32_t)k) T = c1;
-        }
-        k_rem = k - (int)(block_total2(count2(T, 0xFFFFFFFFu, true), 0u, 0).x & 0xFFFFu);
-      }
-    } else {
-      // rows longer than the registers hold: block-wide search, two bits per round
-      for (int b = 30, round = 0; b >= 0; b -= 2, ++round) {
-        const uint32_t c1 = T | (1u << b), c2 = T | (2u << b), c3 = T | (3u << b);
-        const uint2 n = block_total2(count2(c1, c2, false), count2(c3, 0xFFFFFFFFu, false), round & 1);
-        if ((n.y & 0xFFFFu) >= (uint32_t)k) T = c3;
-        else if ((n.x >> 16) >= (uint32_t)k) T = c2;
-        else if ((n.x & 0xFFFFu) >= (uint32_t)k) T = c1;
-      }
-      // the last round (15) used buffer 1, so 0 is free
-      k_rem = k - (int)(block_total2(count2(T, 0xFFFFFFFFu, true), 0u, 0).x & 0xFFFFu);
+    for (int bb = 30, round = 0; bb >= 0; bb -= 2, ++round) {
+      const uint32_t c1 = T | (1u << bb), c2 = T | (2u << bb), c3 = T | (3u << bb);
+      const uint2 cnt = block_total2(count2(c1, c2, false), count2(c3, 0xFFFFFFFFu, false), round & 1);
+      if ((cnt.y & 0xFFFFu) >= (uint32_t)k) T = c3;
+      else if ((cnt.x >> 16) >= (uint32_t)k) T = c2;
+      else if ((cnt.x & 0xFFFFu) >= (uint32_t)k) T = c1;
     }
+    // the last round (15) used buffer 1, so 0 is free
+    k_rem = k - (int)(block_total2(count2(T, 0xFFFFFFFFu, true), 0u, 0).x & 0xFFFFu);
   }
   const bool take_all = (k >= n_cand);
   // per thread: a contiguous range of pages so that scans keep page order
@@ -399,7 +539,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pag
   const int lo = min(n, tid * per), hi = min(n, lo + per);
   int ties = 0;
   if (!take_all && k > 0) {
-    for (int p = lo; p < min(hi, n_cand); ++p) ties += ((keys[p] & mask) == T);
+    for (int p = lo; p < min(hi, n_cand); ++p) ties += (keys[p] == T);
   }
   int tie_total;
   const int tie_start = block_exclusive_scan(ties, sh_scan, tie_total);
@@ -407,7 +547,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pag
     if (p >= n_cand) return keep_newest && p == n - 1;
     if (take_all) return true;
     if (k == 0) return false;
-    const uint32_t key = keys[p] & mask;
+    const uint32_t key = keys[p];
     if (key > T) return true;
     if (key == T) return tie_before++ < k_rem;
     return false;
@@ -432,11 +572,20 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pag
 
 using namespace argus;
 
+// Workspace: the order keys [B][Hkv][max_pages], then the reported largest
+// keys [B][Hkv][chunks][kEmit] for at most ceil(max_pages / 8) page ranges
+// (ranges hold at least 8 pages), so that the size does not depend on the
+// device.
+static size_t select_ws(long long batch, long long n_kv_heads, long long max_pages) {
+  const size_t keys = (size_t)batch * n_kv_heads * max_pages * sizeof(uint32_t);
+  return keys + (size_t)batch * n_kv_heads * ((max_pages + 7) / 8) * select::kEmit * sizeof(uint32_t);
+}
+
 extern "C" argus_status argus_select_workspace_bytes(const argus_geom* g, int32_t batch, int32_t max_pages,
                                                      size_t* bytes) {
   if (!g || !bytes) return fail(ARGUS_E_INVALID, "select: NULL argument");
   if (batch < 0 || max_pages < 0 || g->n_kv_heads <= 0) return fail(ARGUS_E_INVALID, "select: bad sizes");
-  *bytes = (size_t)batch * g->n_kv_heads * max_pages * sizeof(uint32_t);
+  *bytes = select_ws(batch, g->n_kv_heads, max_pages);
   return ARGUS_OK;
 }
 
@@ -460,26 +609,48 @@ extern "C" argus_status argus_select_pages(const argus_geom* g, int32_t batch, c
     return fail(ARGUS_E_INVALID, "select: NULL pointer");
   if ((reinterpret_cast<uintptr_t>(ckeys) | reinterpret_cast<uintptr_t>(q)) & 15)
     return fail(ARGUS_E_INVALID, "select: q and ckeys must be 16-byte aligned");
-  size_t need = (size_t)batch * g->n_kv_heads * max_pages * sizeof(uint32_t);
+  size_t need = select_ws(batch, g->n_kv_heads, max_pages);
   if (!ws || ws_bytes < need) return fail(ARGUS_E_WORKSPACE, "select: workspace %zu < %zu", ws_bytes, need);
+  if (reinterpret_cast<uintptr_t>(ws) & 3) return fail(ARGUS_E_INVALID, "select: workspace not 4-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int G = g->n_q_heads / g->n_kv_heads;
   uint32_t* keys = static_cast<uint32_t*>(ws);
-  // pages per CTA: the whole slab in one wave of resident CTAs
+  uint32_t* emit = keys + (size_t)batch * g->n_kv_heads * max_pages;
+  // pages per CTA: the whole slab in one wave of resident CTAs, 8 .. 256 pages,
+  // as long as a CTA's shared memory stays within kScoreSmemBytes (three per SM)
   const long long resident = (long long)device_sm_count() * select::kScoreCtasPerSm;
   long long ppc = ((long long)batch * max_pages + resident - 1) / resident;
-  ppc = std::max<long long>(8, (ppc + 7) / 8 * 8);
-  dim3 grid1((unsigned)((max_pages + ppc - 1) / ppc), batch);
-  const size_t sh = (size_t)g->n_kv_heads * g->head_dim * sizeof(float);
-  if (sh > 48 * 1024) return fail(ARGUS_E_UNSUPPORTED, "select: n_kv_heads * head_dim too large");
+  ppc = std::min<long long>(select::kMaxPpc, std::max<long long>(8, (ppc + 7) / 8 * 8));
+  while (ppc > 8 && (long long)select::score_smem_bytes(g->n_kv_heads, g->head_dim, ppc) > select::kScoreSmemBytes)
+    ppc -= 8;
+  const int n_chunks = (int)((max_pages + ppc - 1) / ppc);
+  dim3 grid1((unsigned)n_chunks, batch);
+  const size_t sh = select::score_smem_bytes(g->n_kv_heads, g->head_dim, ppc);
+  if (sh > 227 * 1024) return fail(ARGUS_E_UNSUPPORTED, "select: n_kv_heads * head_dim too large");
+  {
+    static PerContext configured;
+    argus_status sta = configured.ensure([](int) {
+      cudaError_t e = cudaSuccess;
+      const int mx = 227 * 1024;
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(select::score_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(select::score_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(select::score_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(select::score_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+      if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "select: score smem attribute: %s", cudaGetErrorString(e));
+      return ARGUS_OK;
+    });
+    if (sta != ARGUS_OK) return sta;
+  }
+  uint32_t* emit_arg = top_k > 0 ? emit : nullptr;
   const uint16_t* ck = static_cast<const uint16_t*>(ckeys);
   const bool bf = (q_dtype == ARGUS_BF16);
+  const int kn = keep_newest ? 1 : 0;
   if (g->head_dim == 64) {
-    if (bf) select::score_kernel<64, true><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, (int)ppc, q, ck, n_pages, keys);
-    else select::score_kernel<64, false><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, (int)ppc, q, ck, n_pages, keys);
+    if (bf) select::score_kernel<64, true><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, (int)ppc, q, ck, n_pages, keys, kn, emit_arg);
+    else select::score_kernel<64, false><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, (int)ppc, q, ck, n_pages, keys, kn, emit_arg);
   } else {
-    if (bf) select::score_kernel<128, true><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, (int)ppc, q, ck, n_pages, keys);
-    else select::score_kernel<128, false><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, (int)ppc, q, ck, n_pages, keys);
+    if (bf) select::score_kernel<128, true><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, (int)ppc, q, ck, n_pages, keys, kn, emit_arg);
+    else select::score_kernel<128, false><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, (int)ppc, q, ck, n_pages, keys, kn, emit_arg);
   }
   argus_status st = launch_status("argus_select_pages (score)");
   if (st != ARGUS_OK) return st;
@@ -495,9 +666,19 @@ extern "C" argus_status argus_select_pages(const argus_geom* g, int32_t batch, c
     });
     if (sta != ARGUS_OK) return sta;
   }
-  dim3 grid2(g->n_kv_heads, batch);
-  select::topk_kernel<<<grid2, select::kTopkThreads, tsh, s>>>(g->n_kv_heads, max_pages, keys, n_pages, top_k,
-                                                               keep_newest, sel_pages, sel_count, sel_width,
-                                                               drop_counter, stage);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(g->n_kv_heads, batch);
+  cfg.blockDim = dim3(select::kTopkThreads);
+  cfg.dynamicSmemBytes = tsh;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, select::topk_kernel, g->n_kv_heads, max_pages, (const uint32_t*)keys,
+                                     n_pages, top_k, (int)keep_newest, sel_pages, sel_count, sel_width, drop_counter,
+                                     stage, (const uint32_t*)emit, n_chunks, (int)ppc);
+  if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "argus_select_pages (top-k): %s", cudaGetErrorString(e));
   return launch_status("argus_select_pages (top-k)");
 }
