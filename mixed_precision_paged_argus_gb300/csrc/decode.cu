@@ -1404,13 +1404,14 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
   pl->fam = (has_bf16 && has_f16) ? kFamMixed : (has_bf16 ? kFamBF16 : kFamF16);
   pl->D = g.head_dim;
   pl->G = G;
-  // narrow ring: every pool holds byte or nibble codes, head_dim 128
+  // extended kernels: a sliding window, INT2 or INT1 pages
   pl->ext = a->window_tokens > 0 || seen[ARGUS_INT2_G32] || seen[ARGUS_INT1_G32];
   pl->host = false;
   for (int i = 0; i < a->n_pools; ++i) pl->host |= a->pools[i].placement == ARGUS_PLACE_HOST;
   if (pl->host && pl->ext)
     return fail(ARGUS_E_UNSUPPORTED, "decode: host-memory pools with a sliding window or an INT2 / INT1 pool");
-  pl->narrow = g.head_dim == 128 && !has_bf16 && !seen[ARGUS_FP16] && a->n_pools > 0 && !pl->ext;
+  // narrow ring: every pool holds byte or sub-byte codes, head_dim 128
+  pl->narrow = g.head_dim == 128 && !has_bf16 && !seen[ARGUS_FP16] && a->n_pools > 0 && !pl->host;
   const long long cps_unit = pl->narrow ? chunks_per_stage<true>() : kChunksPerStage;
   const int cpp = g.page_tokens / kChunk;
   if (a->window_tokens < 0 || a->sink_tokens < 0)
@@ -1489,7 +1490,13 @@ static argus_status launch_d(const Params& p, const Plan& pl, dim3 grid, cudaStr
     if (!pl.q_bf16) return launch_t<D, false, kFamMixed, false, false, true>(p, grid, s);
     return launch_t<D, true, kFamMixed, false, false, true>(p, grid, s);
   }
-  if (pl.ext) {   // sliding window or INT2 pages: the wide ring, one kernel per query type
+  if (pl.ext) {   // sliding window or INT2 / INT1 pages: one kernel per ring and query type
+    if constexpr (D == 128) {
+      if (pl.narrow) {
+        if (!pl.q_bf16) return launch_t<D, false, kFamF16, true, true>(p, grid, s);
+        return launch_t<D, true, kFamF16, true, true>(p, grid, s);
+      }
+    }
     if (!pl.q_bf16) return launch_t<D, false, kFamF16, false, true>(p, grid, s);
     return launch_t<D, true, kFamMixed, false, true>(p, grid, s);
   }
