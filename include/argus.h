@@ -203,6 +203,11 @@ typedef struct {
  * count are sized for at most ceil(sink/16) + ceil(W/16) + 1 chunks of 16
  * tokens per sequence. */
 
+/* args.status: the decode kernel ORs bit 31 (0x80000000) into *status when
+ * one of their waits for a copy or for a sibling warp runs out (2 s).  The
+ * results of that call are then undefined; the kernel still ends, and the
+ * context stays usable. */
+
 /* args.pdl = 0: the kernels start after their stream predecessor completes
  * (ordinary stream order; always safe).
  * args.pdl = 1: the decode grid may start while its stream predecessor is
@@ -308,7 +313,7 @@ argus_status argus_fold_lse(int64_t n_rows, int32_t head_dim, float* acc_o,
  * Arguments: q device bf16 [Hq][n_q][D]; k, v device bf16 with element
  * (h, j, d) at h * kv_head_stride + j * D + d (kv_head_stride = 0 means
  * win_len * D); acc_o device float [Hq][n_q][D]; acc_lse2 [Hq][n_q].
- * softmax_scale finite and >= 0.  Supported: head_dim 128, any n_q and
+ * softmax_scale finite and >= 0.  Supported: head_dim 64 or 128, any n_q and
  * win_len (keys past win_len and query rows past n_q are masked).
  * num_splits: key ranges per 128-row query tile, each its own CTA, so that
  * every SM works; their partial results are kept in ws and folded by a second
@@ -357,7 +362,7 @@ argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n_q,
  * whose slot is outside its pool reads as zeros and is counted once per
  * window in *status (device uint32, may be NULL).  ws (device, 16-byte
  * aligned) of argus_paged_window_prefill_workspace_bytes(g, n_q, win_len,
- * num_splits) bytes, required; no initialisation needed.  head_dim 128.
+ * num_splits) bytes, required; no initialisation needed.  head_dim 64 or 128.
  * ------------------------------------------------------------------------- */
 argus_status argus_paged_window_prefill_workspace_bytes(const argus_geom* g, int32_t n_q,
                                                         int64_t win_len, int32_t num_splits,
@@ -389,6 +394,21 @@ argus_status argus_paged_window_prefill_attn(const argus_geom* g, int32_t n_q, c
  * ------------------------------------------------------------------------- */
 argus_status argus_staging_moves_less(const int64_t* row_read_bytes, int64_t n_rows,
                                       int64_t cache_bytes, int32_t* stage);
+
+/* ---------------------------------------------------------------------------
+ * Testing only.  argus_test_decode_stall runs argus_paged_decode_attn with
+ * every device wait limited to wait_limit_us microseconds (1 .. 2,000,000),
+ * and the producer warp (the one issuing copies) of each CTA that reaches stage
+ * stall_stage (>= 0; a stage is one ring slot of 16-token chunks) withholds
+ * that stage's arrival until the consumer warps have given up on it.  Such a
+ * CTA sets bit 31 of *status (args.status is required), waits until every copy
+ * it issued has landed, and ends; CTAs with fewer stages run normally.
+ * Nothing faults, and each wait ends within wait_limit_us (the producer allows
+ * the consumers twice that to give up).  The outputs of the call are
+ * undefined.
+ * ------------------------------------------------------------------------- */
+argus_status argus_test_decode_stall(const argus_decode_args* args, void* ws, size_t ws_bytes,
+                                     uint32_t wait_limit_us, int32_t stall_stage, void* stream);
 
 const char* argus_status_string(argus_status s);
 

@@ -60,7 +60,7 @@ EXPORTS = ["argus_quantize_pages", "argus_decode_workspace_bytes", "argus_paged_
            "argus_select_workspace_bytes", "argus_select_pages", "argus_fold_lse",
            "argus_window_prefill_workspace_bytes", "argus_window_prefill_attn",
            "argus_paged_window_prefill_workspace_bytes", "argus_paged_window_prefill_attn",
-           "argus_staging_moves_less",
+           "argus_staging_moves_less", "argus_test_decode_stall",
            "argus_status_string", "argus_last_error"]
 
 
@@ -89,6 +89,8 @@ def lib():
     L.argus_decode_workspace_bytes.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.POINTER(sz)]
     L.argus_paged_decode_attn.restype = ctypes.c_int
     L.argus_paged_decode_attn.argtypes = [ctypes.POINTER(DecodeArgs), vp, sz, vp]
+    L.argus_test_decode_stall.restype = ctypes.c_int
+    L.argus_test_decode_stall.argtypes = [ctypes.POINTER(DecodeArgs), vp, sz, ctypes.c_uint32, i32, vp]
     L.argus_paged_decode_attn_noalloc.restype = ctypes.c_int
     L.argus_paged_decode_attn_noalloc.argtypes = [ctypes.POINTER(DecodeArgs), vp]
     L.argus_select_workspace_bytes.restype = ctypes.c_int
@@ -239,6 +241,17 @@ def paged_decode_attn(args, ws, ws_bytes=None, stream=None):
     if ws_bytes is None:
         ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(lib().argus_paged_decode_attn(ctypes.byref(args), _ptr(ws), int(ws_bytes), _stream(stream)))
+
+
+STATUS_TIMEOUT_BIT = 0x80000000
+
+
+def test_decode_stall(args, ws, wait_limit_us, stall_stage, stream=None):
+    """Testing only: the decode with every device wait limited to wait_limit_us
+    and stage stall_stage's arrival withheld, so that the waits run out."""
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().argus_test_decode_stall(ctypes.byref(args), _ptr(ws), nbytes, int(wait_limit_us),
+                                         int(stall_stage), _stream(stream)))
 
 
 NOALLOC_SCRATCH_BYTES = 4 << 20

@@ -109,14 +109,15 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // within kWaitLimitNs, or if *abort (a CTA-wide error flag in shared memory)
 // was raised meanwhile, so that one failed wait ends every other wait quickly.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          const volatile uint32_t* abort = nullptr) {
+                                          const volatile uint32_t* abort = nullptr,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 0) {
       if (abort && *abort) return false;
-      if (global_ns() - t0 > kWaitLimitNs) return false;
+      if (global_ns() - t0 > limit_ns) return false;
     }
   }
 }

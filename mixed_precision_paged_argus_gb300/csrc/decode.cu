@@ -88,6 +88,9 @@ struct Params {
   int sinks;
   float* part_o;   // [B][Hkv][num_splits][G][D]
   float* part_lse; // [B][Hkv][num_splits][G]
+  unsigned long long wait_ns;  // limit of every mbarrier wait
+  int stall_stage; // >= 0 only in the stall test: the producer withholds this
+                   // stage's descriptor arrival until the consumers give up
 };
 
 struct ChunkDesc {
@@ -160,6 +163,7 @@ struct Layout {
   static constexpr int kDescOff = kBarOff + 2 * kStages * 8;
   static constexpr int kMiscOff = kDescOff + kStages * kCPS * (int)sizeof(ChunkDesc);
   static constexpr int kSmemBytes = kMiscOff + 64;
+  static_assert(kMiscOff % 8 == 0, "misc holds an mbarrier at byte 8");
   static constexpr int kMinBlocks = (D == 128) ? 1 : 2;  // by shared memory
 };
 
@@ -622,6 +626,8 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
   uint64_t* empty = full + L::kStages;
   ChunkDesc* descs = reinterpret_cast<ChunkDesc*>(smem + L::kDescOff);
   int* misc = reinterpret_cast<int*>(smem + L::kMiscOff);
+  volatile int* abort_flag = misc;
+  uint64_t* drained = reinterpret_cast<uint64_t*>(misc + 2);
 
   // Programmatic dependent launch: the next kernel on the stream may start its
   // prologue (block-table walk and K/V prefetch) while this grid finishes; every
@@ -702,6 +708,7 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
       mbar_init(&empty[s], kConsumerWarps);
     }
     misc[0] = 0;  // timeout flag
+    mbar_init(drained, 1);  // the producer's copies have all landed (after a timeout)
     fence_mbar_init();
   }
   __syncthreads();
@@ -729,6 +736,7 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
     };
     int nxt_page = page_at(32);
     bool stop = false;
+    int withheld = -1, last_issued = -1;  // stages (warp-uniform)
     for (int base = 0; base < n_local && !stop; base += 32) {
       int nxt_codec = -1;
       long long nxt_slot = -1;
@@ -807,11 +815,16 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
         const int s = base / kChunksPerStage + st;
         const int slot = s % L::kStages;
         if (s >= L::kStages) {
-          if (!mbar_wait(&empty[slot], ((s / L::kStages) - 1) & 1, reinterpret_cast<volatile uint32_t*>(misc))) {
+          if (!mbar_wait(&empty[slot], ((s / L::kStages) - 1) & 1, reinterpret_cast<volatile uint32_t*>(misc),
+                         p.wait_ns)) {
             if (lane == 0) {
-              misc[0] = 1;
+              *abort_flag = 1;
               if (p.status) atomicOr(p.status, kStatusTimeoutBit);
             }
+            stop = true;
+            break;
+          }
+          if (*abort_flag) {  // the consumers gave up (they arrive on empty after setting the flag)
             stop = true;
             break;
           }
@@ -837,13 +850,32 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
           descs[slot * kChunksPerStage + j] = d;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&full[slot]);
+        if (s == p.stall_stage) withheld = s;
+        else if (lane == 0) mbar_arrive(&full[slot]);
+        last_issued = s;
       }
       cur_page = nxt_page;
       cur_codec = nxt_codec;
       cur_slot = nxt_slot;
       nxt_page = nn_page;
     }
+    if (!stop && withheld < 0) return;
+    // Wind-down after a timeout.  Bulk copies may still be landing in the
+    // ring, which the consumers reuse for their merge: complete the withheld
+    // arrival (once the consumers have given up on that stage), wait until
+    // the stages issued last have received all their bytes, then release the
+    // consumers through `drained`.  Every wait here is bounded as well.
+    if (withheld >= 0) {
+      const unsigned long long t0 = global_ns();
+      // the consumers start their wait on this stage within microseconds of
+      // its issue; twice their limit leaves ample margin
+      while (!*abort_flag && global_ns() - t0 <= 2 * p.wait_ns) __nanosleep(1000);
+      if (lane == 0) mbar_arrive(&full[withheld % L::kStages]);
+    }
+    for (int s = max(0, last_issued - L::kStages + 1); s <= last_issued; ++s)
+      mbar_wait(&full[s % L::kStages], (s / L::kStages) & 1, nullptr, p.wait_ns);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(drained);
     return;
   }
 
@@ -957,11 +989,15 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
 
   for (int s = 0; s < n_stages; ++s) {
     const int slot = s % L::kStages;
-    if (alive && !mbar_wait(&full[slot], (s / L::kStages) & 1, reinterpret_cast<volatile uint32_t*>(misc))) {
+    if (alive && !mbar_wait(&full[slot], (s / L::kStages) & 1, reinterpret_cast<volatile uint32_t*>(misc),
+                            p.wait_ns)) {
       alive = false;
-      if (lane == 0 && p.status) atomicOr(p.status, kStatusTimeoutBit);
+      if (lane == 0) {
+        *abort_flag = 1;
+        if (p.status) atomicOr(p.status, kStatusTimeoutBit);
+      }
     }
-    if (alive && misc[0]) alive = false;
+    if (alive && *abort_flag) alive = false;
     ChunkDesc dsc[kNC];
     const uint8_t* cptr[kNC];
     bool any = false;
@@ -1163,6 +1199,10 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
     l1 += __shfl_xor_sync(0xffffffffu, l1, o);
   }
   if (sigma == 0.f) sigma = 1.f;  // nothing accumulated
+  // After a timeout the ring may still be receiving copies: wait (bounded)
+  // until the producer reports them landed.  Every warp sees the flag here:
+  // no warp completes all its stages once another has given up.
+  if (*abort_flag) mbar_wait(drained, 0, nullptr, p.wait_ns);
   consumer_bar<kConsumerWarps>();  // every warp is done with the stage ring; reuse it
   float* red_o = reinterpret_cast<float*>(smem);               // [warps][8][D]
   float* red_ml = red_o + kConsumerWarps * kMaxG * D;          // [warps][8][2]
@@ -1538,7 +1578,8 @@ static argus_status check_io(const argus_decode_args* a) {
 }
 
 // Fill the kernel parameters and launch; ws holds pl.ws_bytes bytes.
-static argus_status run(const argus_decode_args* a, const Plan& pl, void* ws, void* stream) {
+static argus_status run(const argus_decode_args* a, const Plan& pl, void* ws, void* stream,
+                        unsigned long long wait_ns = kWaitLimitNs, int stall_stage = -1) {
   Params p{};
   p.B = a->batch;
   p.Hkv = a->g.n_kv_heads;
@@ -1588,10 +1629,19 @@ static argus_status run(const argus_decode_args* a, const Plan& pl, void* ws, vo
   p.sinks = a->window_tokens > 0 ? std::min(a->sink_tokens, 1 << 30) : 0;
   p.part_o = static_cast<float*>(ws);
   p.part_lse = ws ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.part_o_bytes) : nullptr;
+  p.wait_ns = wait_ns;
+  p.stall_stage = stall_stage;
   dim3 grid(pl.num_splits, a->g.n_kv_heads, a->batch);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (pl.D == 64) return launch_d<64>(p, pl, grid, s);
   return launch_d<128>(p, pl, grid, s);
+}
+
+static argus_status check_ws(const Plan& pl, void* ws, size_t ws_bytes) {
+  if (ws_bytes < pl.ws_bytes || (pl.num_splits > 1 && !ws))
+    return fail(ARGUS_E_WORKSPACE, "decode: workspace %zu bytes < %zu needed", ws_bytes, pl.ws_bytes);
+  if (reinterpret_cast<uintptr_t>(ws) & 15) return fail(ARGUS_E_INVALID, "decode: workspace not 16-byte aligned");
+  return ARGUS_OK;
 }
 
 extern "C" argus_status argus_paged_decode_attn(const argus_decode_args* a, void* ws,
@@ -1601,10 +1651,24 @@ extern "C" argus_status argus_paged_decode_attn(const argus_decode_args* a, void
   if (st != ARGUS_OK) return st;
   if (a->batch == 0) return ARGUS_OK;
   if ((st = check_io(a)) != ARGUS_OK) return st;
-  if (ws_bytes < pl.ws_bytes || (pl.num_splits > 1 && !ws))
-    return fail(ARGUS_E_WORKSPACE, "decode: workspace %zu bytes < %zu needed", ws_bytes, pl.ws_bytes);
-  if (reinterpret_cast<uintptr_t>(ws) & 15) return fail(ARGUS_E_INVALID, "decode: workspace not 16-byte aligned");
+  if ((st = check_ws(pl, ws, ws_bytes)) != ARGUS_OK) return st;
   return run(a, pl, ws, stream);
+}
+
+extern "C" argus_status argus_test_decode_stall(const argus_decode_args* a, void* ws, size_t ws_bytes,
+                                                uint32_t wait_limit_us, int32_t stall_stage,
+                                                void* stream) {
+  if (wait_limit_us < 1 || wait_limit_us > 2000000u)
+    return fail(ARGUS_E_INVALID, "decode stall test: wait_limit_us %u outside [1, 2000000]", wait_limit_us);
+  if (stall_stage < 0) return fail(ARGUS_E_INVALID, "decode stall test: stall_stage must be >= 0");
+  if (!a->status) return fail(ARGUS_E_INVALID, "decode stall test: status is required");
+  Plan pl;
+  argus_status st = plan(a, &pl);
+  if (st != ARGUS_OK) return st;
+  if (a->batch == 0) return ARGUS_OK;
+  if ((st = check_io(a)) != ARGUS_OK) return st;
+  if ((st = check_ws(pl, ws, ws_bytes)) != ARGUS_OK) return st;
+  return run(a, pl, ws, stream, 1000ull * wait_limit_us, stall_stage);
 }
 
 // ---------------------------------------------------------------------------

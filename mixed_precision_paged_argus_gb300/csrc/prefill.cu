@@ -38,26 +38,30 @@ namespace prefill {
 
 constexpr int kBM = 128;          // query rows per CTA (TMEM lanes)
 constexpr int kBN = 128;          // keys per block
-constexpr int kD = 128;           // head_dim
 constexpr int kStages = 3;        // K/V ring depth
 constexpr int kGroupWarps = 4;    // one softmax warpgroup: a thread per row
 constexpr int kSoftmaxWarps = 2 * kGroupWarps;   // two groups take alternate key blocks
 constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
-constexpr int kTile = kBM * kD * 2;   // 32 KB: a 128 x 128 bf16 tile as two 16 KB swizzled halves
-constexpr int kHalf = kTile / 2;
-constexpr int kTmemCols = 512;        // S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512)
+constexpr int kHalf = kBM * 64 * 2;   // 16 KB: 128 rows x 64 dims, one 128-byte swizzle column
+constexpr int kTmemCols = 512;        // S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [384,384+D)
 constexpr float kRescaleThreshold = 8.f;
 
-// shared memory map (offsets from a 1024-byte aligned base)
-constexpr int kOffQ = 0;
-constexpr int kOffK = kTile;
-constexpr int kOffV = kOffK + kStages * kTile;
-constexpr int kOffBar = kOffV + kStages * kTile;
-// barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], s_free[2], o_done[2]
-constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 2;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kOffML = kOffMisc + 64;                 // group 1's (m, l) per row
-constexpr int kSmemBytes = kOffML + kBM * 8 + 1024;   // + alignment slack
+// Shared memory map of head_dim D (offsets from a 1024-byte aligned base): a
+// 128-row bf16 / fp16 tile is D / 64 swizzled 16 KB halves of 64 dims each.
+template <int D>
+struct Smem {
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static constexpr int kTile = kBM * D * 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kTile;
+  static constexpr int kOffV = kOffK + kStages * kTile;
+  static constexpr int kOffBar = kOffV + kStages * kTile;
+  // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], s_free[2], o_done[2]
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 2 + 2;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kOffML = kOffMisc + 64;                 // group 1's (m, l) per row
+  static constexpr int kBytes = kOffML + kBM * 8 + 1024;       // + alignment slack
+};
 
 struct PParams {
   int G, n_q, n_tiles;              // tiles per KV head = ceil(G * n_q / 128)
@@ -114,11 +118,11 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// instruction descriptor, kind::f16 -> f32, M = 128, N = 128; operand type
+// instruction descriptor, kind::f16 -> f32, M = 128, N = n; operand type
 // 1 = bf16 (both operands), 0 = fp16 (both operands)
-__host__ __device__ constexpr uint32_t idesc_f16kind(bool bf16, bool b_mn_major) {
+__host__ __device__ constexpr uint32_t idesc_f16kind(bool bf16, bool b_mn_major, int n) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-         ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -200,16 +204,18 @@ __device__ __forceinline__ void group_bar(int id) {
 //         one MMA per key step.
 // MODE 2: both in fp16 over a staged window: fp16 K and V copies scaled by
 //         powers of two and an fp16 query scaled per row (score scale per row).
-template <int MODE>
+template <int MODE, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PParams p) {
+  using SM = Smem<D>;
+  constexpr int kTile = SM::kTile;
   constexpr bool F16P = MODE >= 1;
   constexpr bool F16QK = MODE == 2;
   constexpr float kPBias = F16P ? 7.f : 0.f;   // fp16 P is stored as P * 2^kPBias
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kOffBar);
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + kStages;
@@ -217,8 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_full + 2;
   uint64_t* s_free = p_full + 2;
   uint64_t* o_done = s_free + 2;
-  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc);  // [0] tmem base, [1] error
-  float2* ml1 = reinterpret_cast<float2*>(smem + kOffML);
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + SM::kOffMisc);  // [0] tmem base, [1] error
+  float2* ml1 = reinterpret_cast<float2*>(smem + SM::kOffML);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x, h = blockIdx.y, split = blockIdx.z;
@@ -273,8 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- TMA producer
     if (lane == 0 && nb > 0) {
       mbar_arrive_expect_tx(q_full, kTile);
-      tma_load_2d(smem + kOffQ, &tmQ, 0, (int)row0, q_full);
-      tma_load_2d(smem + kOffQ + kHalf, &tmQ, 64, (int)row0, q_full);
+#pragma unroll
+      for (int hf = 0; hf < D / 64; ++hf) tma_load_2d(smem + SM::kOffQ + hf * kHalf, &tmQ, 64 * hf, (int)row0, q_full);
       for (int i = 0; i < nb; ++i) {
         const int st = i % kStages;
         const int y = (jb + i) * kBN;
@@ -283,12 +289,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         mbar_arrive_expect_tx(&kv_full[st], 2 * kTile);
-        uint8_t* kd = smem + kOffK + st * kTile;
-        uint8_t* vd = smem + kOffV + st * kTile;
-        tma_load_3d(kd, &tmK, 0, y, h, &kv_full[st]);
-        tma_load_3d(kd + kHalf, &tmK, 64, y, h, &kv_full[st]);
-        tma_load_3d(vd, &tmV, 0, y, h, &kv_full[st]);
-        tma_load_3d(vd + kHalf, &tmV, 64, y, h, &kv_full[st]);
+        uint8_t* kd = smem + SM::kOffK + st * kTile;
+        uint8_t* vd = smem + SM::kOffV + st * kTile;
+#pragma unroll
+        for (int hf = 0; hf < D / 64; ++hf) {
+          tma_load_3d(kd + hf * kHalf, &tmK, 64 * hf, y, h, &kv_full[st]);
+          tma_load_3d(vd + hf * kHalf, &tmV, 64 * hf, y, h, &kv_full[st]);
+        }
       }
     }
   } else if (warp == kSoftmaxWarps + 1) {
@@ -296,9 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // order: S0, S1, then per block i: P.V of i, S of i+2 (into the buffer
     // P.V of i reads; the MMA pipe keeps the two in order)
     if (lane == 0 && nb > 0) {
-      constexpr uint32_t idQK = idesc_f16kind(!F16QK, false);
-      constexpr uint32_t idPV = idesc_f16kind(!F16P, true);
-      const uint32_t q_s = smem_u32(smem + kOffQ);
+      constexpr uint32_t idQK = idesc_f16kind(!F16QK, false, kBN);
+      constexpr uint32_t idPV = idesc_f16kind(!F16P, true, D);
+      const uint32_t q_s = smem_u32(smem + SM::kOffQ);
       bool ok = mbar_wait(q_full, 0, &misc[1]);
       auto issue_s = [&](int j) {
         const int st = j % kStages, b = j & 1;
@@ -306,9 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // no wait for the P.V that last read this buffer: tcgen05.mma from one
         // thread execute in issue order, so these writes follow its reads
         tc_fence_after();
-        const uint32_t k_s = smem_u32(smem + kOffK + st * kTile);
+        const uint32_t k_s = smem_u32(smem + SM::kOffK + st * kTile);
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
           mma_ss(tS[b], sdesc(q_s + off, kHalf, 1024), sdesc(k_s + off, kHalf, 1024), idQK, kk > 0 ? 1u : 0u);
         }
@@ -319,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = i & 1, st = i % kStages;
         if (!mbar_wait(&p_full[b], (i >> 1) & 1, &misc[1])) return false;
         tc_fence_after();
-        const uint32_t v_s = smem_u32(smem + kOffV + st * kTile);
+        const uint32_t v_s = smem_u32(smem + SM::kOffV + st * kTile);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           // P: 16 keys = 8 packed bf16x2 columns, high part at 16kk, low part at
@@ -399,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // previous P.V is complete too (all earlier MMAs were committed)
         const float r = scale_o ? fast_exp2(m - mj) : 1.f;
 #pragma unroll
-        for (int c = 0; c < kD / 32; ++c) {
+        for (int c = 0; c < D / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(sO + c * 32, v);
           tmem_wait_ld();
@@ -491,10 +498,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.nsplit > 1) {
         // partial of this key range: normalised o and its lse2, folded later
         const size_t part = ((size_t)h * p.n_tiles + tile) * p.nsplit + split;
-        float* po = p.ws_o + (part * kBM + row) * kD;
+        float* po = p.ws_o + (part * kBM + row) * D;
         const float inv = have ? vsc / lt : 0.f;
 #pragma unroll 1
-        for (int c = 0; c < kD / 16; ++c) {
+        for (int c = 0; c < D / 16; ++c) {
           uint32_t v0[16], v1[16];
           if (nk > 0) tmem_ld16(o0a + c * 16, v0);     // nk, nk1 are uniform across the CTA
           if (nk1 > 0) tmem_ld16(o1a + c * 16, v1);
@@ -518,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         // every lane runs the (warp-collective) TMEM loads; rows past the
         // head's last row neither read nor write the accumulator
-        float* ao = p.acc_o + orow * kD;
+        float* ao = p.acc_o + orow * D;
         const float lse = have ? M + log2f(lt) : -INFINITY;
         const float La = (p.fold && valid_row) ? p.acc_lse2[orow] : -INFINITY;
         float wa = 0.f, wb = 0.f, L = -INFINITY;
@@ -538,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const bool write = valid_row && (have || !p.fold);
   #pragma unroll 1
-        for (int c = 0; c < kD / 16; ++c) {
+        for (int c = 0; c < D / 16; ++c) {
           uint32_t v0[16], v1[16];
           if (nk > 0) tmem_ld16(o0a + c * 16, v0);     // nk, nk1 are uniform across the CTA
           if (nk1 > 0) tmem_ld16(o1a + c * 16, v1);
@@ -579,13 +586,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Fold the key-range partials of every row into the accumulator: one warp per
-// row, each lane a float4 of the 128 dims.  Same arithmetic as the direct
-// epilogue: L = max + log2(sum of 2^(lse - max)), o = sum of 2^(lse - L) o_s.
+// row, each of the first D / 4 lanes a float4 of the D dims.  Same arithmetic
+// as the direct epilogue: L = max + log2(sum of 2^(lse - max)),
+// o = sum of 2^(lse - L) o_s.
 constexpr int kFoldWarps = 8;
+template <int D>
 __global__ void __launch_bounds__(32 * kFoldWarps) prefill_fold_kernel(const PParams p, long long n_rows) {
   const long long r = (long long)blockIdx.x * kFoldWarps + (threadIdx.x >> 5);   // = h * rows_h + lin
-  if (r >= n_rows) return;
   const int lane = threadIdx.x & 31;
+  if (r >= n_rows || lane >= D / 4) return;
   const long long hh = r / p.rows_h, lin = r - hh * p.rows_h;
   const long long tile_lin = hh * p.n_tiles + lin / kBM;
   const int row = (int)(lin % kBM);
@@ -593,7 +602,7 @@ __global__ void __launch_bounds__(32 * kFoldWarps) prefill_fold_kernel(const PPa
   const float La = p.fold ? p.acc_lse2[r] : -INFINITY;
   float M = La;
   for (int s2 = 0; s2 < p.nsplit; ++s2) M = fmaxf(M, pl[(size_t)s2 * kBM]);
-  float4* ao = reinterpret_cast<float4*>(p.acc_o + r * kD) + lane;
+  float4* ao = reinterpret_cast<float4*>(p.acc_o + r * D) + lane;
   if (M == -INFINITY) {  // nothing visible anywhere: o = 0, lse2 = -inf (kept when folding)
     if (!p.fold) {
       *ao = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -613,12 +622,12 @@ __global__ void __launch_bounds__(32 * kFoldWarps) prefill_fold_kernel(const PPa
     const float4 a = *ao;
     o = make_float4(wa * a.x, wa * a.y, wa * a.z, wa * a.w);
   }
-  const float4* po = reinterpret_cast<const float4*>(p.ws_o + ((size_t)tile_lin * p.nsplit * kBM + row) * kD) + lane;
+  const float4* po = reinterpret_cast<const float4*>(p.ws_o + ((size_t)tile_lin * p.nsplit * kBM + row) * D) + lane;
   for (int s2 = 0; s2 < p.nsplit; ++s2) {
     const float ls = pl[(size_t)s2 * kBM];
     if (ls == -INFINITY) continue;
     const float w = exp2f(ls - L);
-    const float4 x = po[(size_t)s2 * kBM * (kD / 4)];
+    const float4 x = po[(size_t)s2 * kBM * (D / 4)];
     o.x += w * x.x;
     o.y += w * x.y;
     o.z += w * x.z;
@@ -633,10 +642,10 @@ __global__ void __launch_bounds__(32 * kFoldWarps) prefill_fold_kernel(const PPa
 // per-block reduction, one atomicMax on the bit pattern (non-negative floats
 // order like their bits).
 __global__ void __launch_bounds__(256) v16_max_kernel(const uint16_t* v, long long stride, long long win_len,
-                                                      long long n_vec, uint32_t* vmax) {
+                                                      int D, long long n_vec, uint32_t* vmax) {
   __shared__ float sh[8];
   float mx = 0.f;
-  const long long per_head = win_len * (kD / 8);
+  const long long per_head = win_len * (D / 8);
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec; i += (long long)gridDim.x * blockDim.x) {
     const long long h = i / per_head, r = i - h * per_head;
     const uint4 x = __ldg(reinterpret_cast<const uint4*>(v + h * stride) + r);
@@ -660,9 +669,9 @@ __global__ void __launch_bounds__(256) v16_max_kernel(const uint16_t* v, long lo
 // V16[h][j][d] = fp16_rn(v * 2^-e); scaling by a power of two is exact
 // outside fp16's subnormal range.
 __global__ void __launch_bounds__(256) v16_convert_kernel(const uint16_t* v, long long stride, long long win_len,
-                                                          long long n_vec, const uint32_t* vmax, uint16_t* v16) {
+                                                          int D, long long n_vec, const uint32_t* vmax, uint16_t* v16) {
   const float sc = ldexpf(1.f, -f16_exponent(*vmax));
-  const long long per_head = win_len * (kD / 8);
+  const long long per_head = win_len * (D / 8);
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec; i += (long long)gridDim.x * blockDim.x) {
     const long long h = i / per_head, r = i - h * per_head;
     const uint4 x = __ldg(reinterpret_cast<const uint4*>(v + h * stride) + r);
@@ -726,7 +735,8 @@ static argus_status check_geom(const argus_geom* g, int32_t n_q, int64_t win_len
   if (!g) return fail(ARGUS_E_INVALID, "prefill: geometry is NULL");
   if (g->n_q_heads <= 0 || g->n_kv_heads <= 0 || g->n_q_heads % g->n_kv_heads)
     return fail(ARGUS_E_INVALID, "prefill: bad head counts");
-  if (g->head_dim != kD) return fail(ARGUS_E_UNSUPPORTED, "prefill: head_dim %d (supported: 128)", g->head_dim);
+  if (g->head_dim != 64 && g->head_dim != 128)
+    return fail(ARGUS_E_UNSUPPORTED, "prefill: head_dim %d (supported: 64, 128)", g->head_dim);
   if (n_q < 0 || win_len < 0) return fail(ARGUS_E_INVALID, "prefill: negative n_q or win_len");
   if ((long long)g->n_q_heads * n_q > (1LL << 31) - kBM || win_len > (1LL << 31) - kBN)
     return fail(ARGUS_E_UNSUPPORTED, "prefill: sizes beyond 2^31 rows");
@@ -740,19 +750,19 @@ static long long tiles_per_head(const argus_geom* g, int32_t n_q) {
 
 static size_t up16(size_t x) { return (x + 15) / 16 * 16; }
 
-static size_t split_bytes(long long n_tiles_total, int nsplit) {
-  return nsplit > 1 ? (size_t)n_tiles_total * nsplit * kBM * (kD + 1) * sizeof(float) : 0;
+static size_t split_bytes(long long n_tiles_total, int nsplit, int D) {
+  return nsplit > 1 ? (size_t)n_tiles_total * nsplit * kBM * (D + 1) * sizeof(float) : 0;
 }
 
 // fp16 copy of one operand over the window: [Hkv][win_len][D]
-static size_t win16_bytes(long long n_kv_heads, long long win_len) {
-  return (size_t)n_kv_heads * std::max<long long>(win_len, 1) * kD * 2;
+static size_t win16_bytes(long long n_kv_heads, long long win_len, int D) {
+  return (size_t)n_kv_heads * std::max<long long>(win_len, 1) * D * 2;
 }
 
 // With a workspace, P.V runs in fp16: after the partials come the window's V
 // as scaled fp16 [Hkv][win_len][D] and the max-|v| word.
-static size_t ws_total(long long n_tiles_total, int nsplit, long long n_kv_heads, long long win_len) {
-  return split_bytes(n_tiles_total, nsplit) + win16_bytes(n_kv_heads, win_len) + 16;
+static size_t ws_total(long long n_tiles_total, int nsplit, long long n_kv_heads, long long win_len, int D) {
+  return split_bytes(n_tiles_total, nsplit, D) + win16_bytes(n_kv_heads, win_len, D) + 16;
 }
 
 // Staged paged window: partials, fp16 K, fp16 V, fp16 Q [Hq * n_q][D], the
@@ -763,11 +773,12 @@ struct PagedWs {
 static PagedWs paged_ws(const argus_geom* g, int32_t n_q, long long win_len, long long n_tiles_total, int nsplit) {
   PagedWs w;
   const long long rows = (long long)g->n_q_heads * n_q;
+  const int D = g->head_dim;
   w.part = 0;
-  w.k16 = split_bytes(n_tiles_total, nsplit);
-  w.v16 = w.k16 + win16_bytes(g->n_kv_heads, win_len);
-  w.q16 = w.v16 + win16_bytes(g->n_kv_heads, win_len);
-  w.qfac = w.q16 + up16((size_t)std::max<long long>(rows, 1) * kD * 2);
+  w.k16 = split_bytes(n_tiles_total, nsplit, D);
+  w.v16 = w.k16 + win16_bytes(g->n_kv_heads, win_len, D);
+  w.q16 = w.v16 + win16_bytes(g->n_kv_heads, win_len, D);
+  w.qfac = w.q16 + up16((size_t)std::max<long long>(rows, 1) * D * 2);
   w.words = w.qfac + up16((size_t)std::max<long long>(rows, 1) * 4);
   w.total = w.words + 16;
   return w;
@@ -779,45 +790,64 @@ static int resolve_splits(long long tiles, long long win_len, int32_t num_splits
 }
 
 // Tensor maps over Q [rows][D] and K, V [Hkv][rows of a window][D] (element
-// strides in elements), all in `dtype`; a window of 0 keys maps one row.
-static argus_status make_maps(CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv, const void* q, long long q_rows,
-                              const void* k, const void* v, long long n_kv_heads, long long win_len,
-                              long long kv_stride, CUtensorMapDataType qdt, CUtensorMapDataType kdt,
-                              CUtensorMapDataType vdt, long long v_stride) {
+// strides in elements), all in `dtype`; a window of 0 keys maps one row.  The
+// box is 64 dims x 128 rows: one swizzled half of a tile.
+static argus_status make_maps(CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv, int D, const void* q,
+                              long long q_rows, const void* k, const void* v, long long n_kv_heads,
+                              long long win_len, long long kv_stride, CUtensorMapDataType qdt,
+                              CUtensorMapDataType kdt, CUtensorMapDataType vdt, long long v_stride) {
   const long long wl = std::max<long long>(win_len, 1);
-  const cuuint64_t qd[2] = {(cuuint64_t)kD, (cuuint64_t)std::max<long long>(q_rows, 1)};
-  const cuuint64_t qs[1] = {(cuuint64_t)kD * 2};
-  const cuuint64_t kd[3] = {(cuuint64_t)kD, (cuuint64_t)wl, (cuuint64_t)n_kv_heads};
-  const cuuint64_t ks[2] = {(cuuint64_t)kD * 2, (cuuint64_t)kv_stride * 2};
-  const cuuint64_t vs[2] = {(cuuint64_t)kD * 2, (cuuint64_t)v_stride * 2};
+  const cuuint64_t qd[2] = {(cuuint64_t)D, (cuuint64_t)std::max<long long>(q_rows, 1)};
+  const cuuint64_t qs[1] = {(cuuint64_t)D * 2};
+  const cuuint64_t kd[3] = {(cuuint64_t)D, (cuuint64_t)wl, (cuuint64_t)n_kv_heads};
+  const cuuint64_t ks[2] = {(cuuint64_t)D * 2, (cuuint64_t)kv_stride * 2};
+  const cuuint64_t vs[2] = {(cuuint64_t)D * 2, (cuuint64_t)v_stride * 2};
   if (!make_map(mq, q, 2, qd, qs, qdt)) return fail(ARGUS_E_LAUNCH, "prefill: tensor map for q failed");
   if (!make_map(mk, k, 3, kd, ks, kdt)) return fail(ARGUS_E_LAUNCH, "prefill: tensor map for k failed");
   if (!make_map(mv, v, 3, kd, vs, vdt)) return fail(ARGUS_E_LAUNCH, "prefill: tensor map for v failed");
   return ARGUS_OK;
 }
 
+template <int D>
+static cudaError_t set_smem_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<0, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<D>::kBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(prefill_kernel<1, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<D>::kBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(prefill_kernel<2, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<D>::kBytes);
+  return e;
+}
+
+template <int D>
+static void launch_mode(int mode, dim3 grid, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                        const PParams& p, cudaStream_t s) {
+  constexpr int smem = Smem<D>::kBytes;
+  if (mode == 0) prefill_kernel<0, D><<<grid, kThreads, smem, s>>>(mq, mk, mv, p);
+  else if (mode == 1) prefill_kernel<1, D><<<grid, kThreads, smem, s>>>(mq, mk, mv, p);
+  else prefill_kernel<2, D><<<grid, kThreads, smem, s>>>(mq, mk, mv, p);
+}
+
 // Launch the attention kernel of `mode` over (tiles, Hkv, splits) and, with
 // more than one split, the fold of the partials.
-static argus_status launch_attention(int mode, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                                     const PParams& p, long long n_kv_heads, long long n_rows, cudaStream_t s) {
+static argus_status launch_attention(int mode, int D, const CUtensorMap& mq, const CUtensorMap& mk,
+                                     const CUtensorMap& mv, const PParams& p, long long n_kv_heads, long long n_rows,
+                                     cudaStream_t s) {
   static PerContext configured;
   argus_status sta = configured.ensure([](int) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(prefill_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(prefill_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = set_smem_attributes<128>();
+    if (e == cudaSuccess) e = set_smem_attributes<64>();
     if (e != cudaSuccess) return fail(ARGUS_E_LAUNCH, "prefill: smem attribute: %s", cudaGetErrorString(e));
     return ARGUS_OK;
   });
   if (sta != ARGUS_OK) return sta;
   dim3 grid(p.n_tiles, (unsigned)n_kv_heads, p.nsplit);
-  if (mode == 0) prefill_kernel<0><<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
-  else if (mode == 1) prefill_kernel<1><<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
-  else prefill_kernel<2><<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
+  if (D == 64) launch_mode<64>(mode, grid, mq, mk, mv, p, s);
+  else launch_mode<128>(mode, grid, mq, mk, mv, p, s);
   argus_status st = launch_status("window prefill attention");
   if (st != ARGUS_OK || p.nsplit == 1) return st;
-  prefill_fold_kernel<<<(unsigned)((n_rows + kFoldWarps - 1) / kFoldWarps), 32 * kFoldWarps, 0, s>>>(p, n_rows);
+  const unsigned blocks = (unsigned)((n_rows + kFoldWarps - 1) / kFoldWarps);
+  if (D == 64) prefill_fold_kernel<64><<<blocks, 32 * kFoldWarps, 0, s>>>(p, n_rows);
+  else prefill_fold_kernel<128><<<blocks, 32 * kFoldWarps, 0, s>>>(p, n_rows);
   return launch_status("window prefill attention (fold)");
 }
 
@@ -858,7 +888,7 @@ static PParams base_params(const argus_geom* g, int32_t n_q, int64_t win_len, in
 // them (codes x scale; INT4 / INT2 code x s + z in fp32), then scaled by the
 // window's power of two and rounded to fp16.
 struct SParams {
-  int Hkv, P, max_pages;
+  int Hkv, P, max_pages, D;
   const uint8_t* codes[ARGUS_INT1_G32 + 1];
   const uint8_t* meta[ARGUS_INT1_G32 + 1];
   long long n_slots[ARGUS_INT1_G32 + 1];
@@ -897,7 +927,7 @@ __device__ __forceinline__ bool stage_load8(const SParams& p, int kv, int h, lon
   const size_t r = unit * p.P + row;                          // token row of the pool
   const uint8_t* c = p.codes[codec];
   if (codec == ARGUS_FP16 || codec == ARGUS_BF16) {
-    const uint4 w = *reinterpret_cast<const uint4*>(c + (r * kD + d0) * 2);
+    const uint4 w = *reinterpret_cast<const uint4*>(c + (r * p.D + d0) * 2);
     const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -910,7 +940,7 @@ __device__ __forceinline__ bool stage_load8(const SParams& p, int kv, int h, lon
       }
     }
   } else if (codec == ARGUS_FP8_E4M3 || codec == ARGUS_INT8) {
-    const uint2 w = *reinterpret_cast<const uint2*>(c + r * kD + d0);
+    const uint2 w = *reinterpret_cast<const uint2*>(c + r * p.D + d0);
     const float sc = reinterpret_cast<const float*>(p.meta[codec])[unit];
     const uint32_t ww[2] = {w.x, w.y};
 #pragma unroll
@@ -927,18 +957,18 @@ __device__ __forceinline__ bool stage_load8(const SParams& p, int kv, int h, lon
       }
     }
   } else {
-    const __half2 sz = reinterpret_cast<const __half2*>(p.meta[codec])[r * (kD / 32) + d0 / 32];
+    const __half2 sz = reinterpret_cast<const __half2*>(p.meta[codec])[r * (p.D / 32) + d0 / 32];
     const float s = __low2float(sz), z = __high2float(sz);
     if (codec == ARGUS_INT4_G32) {
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(c + r * (kD / 2) + d0 / 2);
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(c + r * (p.D / 2) + d0 / 2);
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] = fmaf((float)((w >> (4 * e)) & 0xFu), s, z);
     } else if (codec == ARGUS_INT1_G32) {
-      const uint32_t w = c[r * (kD / 8) + d0 / 8];
+      const uint32_t w = c[r * (p.D / 8) + d0 / 8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] = fmaf((float)((w >> e) & 0x1u), s, z);
     } else {
-      const uint32_t w = *reinterpret_cast<const uint16_t*>(c + r * (kD / 4) + d0 / 4);
+      const uint32_t w = *reinterpret_cast<const uint16_t*>(c + r * (p.D / 4) + d0 / 4);
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] = fmaf((float)((w >> (2 * e)) & 0x3u), s, z);
     }
@@ -948,11 +978,12 @@ __device__ __forceinline__ bool stage_load8(const SParams& p, int kv, int h, lon
 
 // Vector i of the window: KV head h, window row j, dims d0 .. d0 + 7.
 __device__ __forceinline__ void stage_vec(const SParams& p, long long i, int& h, long long& j, int& d0) {
-  const long long per_head = p.win_len * (kD / 8);
+  const int dv = p.D / 8;
+  const long long per_head = p.win_len * dv;
   h = (int)(i / per_head);
   const long long rr = i - h * per_head;
-  j = rr / (kD / 8);
-  d0 = (int)(rr - j * (kD / 8)) * 8;
+  j = rr / dv;
+  d0 = (int)(rr - j * dv) * 8;
 }
 
 // Pass 1: max |k| and max |v| over the window (block reduction, one atomicMax
@@ -1023,7 +1054,8 @@ __global__ void __launch_bounds__(256) stage_q_kernel(const SParams p) {
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (row >= p.q_rows) return;
   const int lane = threadIdx.x & 31;
-  const uint2 w = reinterpret_cast<const uint2*>(p.q + row * kD)[lane];   // dims 4 lane .. 4 lane + 3
+  const bool mine = lane < p.D / 4;   // dims 4 lane .. 4 lane + 3
+  const uint2 w = mine ? reinterpret_cast<const uint2*>(p.q + row * p.D)[lane] : make_uint2(0u, 0u);
   const float x[4] = {__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u), __uint_as_float(w.y << 16),
                       __uint_as_float(w.y & 0xFFFF0000u)};
   float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
@@ -1031,7 +1063,9 @@ __global__ void __launch_bounds__(256) stage_q_kernel(const SParams p) {
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   const int e = f16_exponent(__float_as_uint(m));
   const float sc = ldexpf(1.f, -e);
-  reinterpret_cast<uint2*>(p.q16 + row * kD)[lane] = make_uint2(pack_f16x2(x[0] * sc, x[1] * sc), pack_f16x2(x[2] * sc, x[3] * sc));
+  if (mine)
+    reinterpret_cast<uint2*>(p.q16 + row * p.D)[lane] =
+        make_uint2(pack_f16x2(x[0] * sc, x[1] * sc), pack_f16x2(x[2] * sc, x[3] * sc));
   if (lane == 0) p.qfac[row] = ldexpf(1.f, e);
 }
 
@@ -1046,7 +1080,7 @@ extern "C" argus_status argus_window_prefill_workspace_bytes(const argus_geom* g
   if (st != ARGUS_OK) return st;
   if (num_splits < 0 || num_splits > 1024) return argus::fail(ARGUS_E_INVALID, "prefill: num_splits out of range");
   const long long tiles = tiles_per_head(g, n_q) * g->n_kv_heads;
-  *bytes = ws_total(tiles, resolve_splits(tiles, win_len, num_splits, true), g->n_kv_heads, win_len);
+  *bytes = ws_total(tiles, resolve_splits(tiles, win_len, num_splits, true), g->n_kv_heads, win_len, g->head_dim);
   return ARGUS_OK;
 }
 
@@ -1066,8 +1100,9 @@ extern "C" argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
        reinterpret_cast<uintptr_t>(acc_o) | reinterpret_cast<uintptr_t>(ws)) & 15)
     return fail(ARGUS_E_INVALID, "prefill: pointers must be 16-byte aligned");
-  const long long stride = kv_head_stride ? kv_head_stride : win_len * kD;
-  if (stride % 8 != 0 || stride < win_len * kD)
+  const int D = g->head_dim;
+  const long long stride = kv_head_stride ? kv_head_stride : win_len * D;
+  if (stride % 8 != 0 || stride < win_len * D)
     return fail(ARGUS_E_INVALID, "prefill: kv_head_stride must be >= win_len*head_dim and a multiple of 8");
   PParams p = base_params(g, n_q, win_len, win_pos0, q_pos0, softmax_scale, acc_o, acc_lse2, fold);
   const long long tiles_total = (long long)p.n_tiles * g->n_kv_heads;
@@ -1077,23 +1112,24 @@ extern "C" argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n
   uint16_t* v16 = nullptr;
   uint32_t* vmax = nullptr;
   if (p.nsplit > 1 || f16p) {
-    const size_t need = ws_total(tiles_total, p.nsplit, g->n_kv_heads, win_len);
+    const size_t need = ws_total(tiles_total, p.nsplit, g->n_kv_heads, win_len, D);
     if (!ws || ws_bytes < need) return fail(ARGUS_E_WORKSPACE, "prefill: workspace %zu < %zu", ws_bytes, need);
     uint8_t* w8 = static_cast<uint8_t*>(ws);
     if (p.nsplit > 1) {
       p.ws_o = reinterpret_cast<float*>(w8);
-      p.ws_lse = p.ws_o + (size_t)tiles_total * p.nsplit * kBM * kD;
+      p.ws_lse = p.ws_o + (size_t)tiles_total * p.nsplit * kBM * D;
     }
-    v16 = reinterpret_cast<uint16_t*>(w8 + split_bytes(tiles_total, p.nsplit));
-    vmax = reinterpret_cast<uint32_t*>(w8 + split_bytes(tiles_total, p.nsplit) + win16_bytes(g->n_kv_heads, win_len));
+    v16 = reinterpret_cast<uint16_t*>(w8 + split_bytes(tiles_total, p.nsplit, D));
+    vmax = reinterpret_cast<uint32_t*>(w8 + split_bytes(tiles_total, p.nsplit, D) + win16_bytes(g->n_kv_heads, win_len, D));
     p.vmax_bits = vmax;
   }
   CUtensorMap mq, mk, mv;
   const void* kk = win_len > 0 ? k : q;
-  argus_status stm = f16p ? make_maps(&mq, &mk, &mv, q, (long long)g->n_q_heads * n_q, kk, v16, g->n_kv_heads, win_len,
-                                      stride, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                                      CU_TENSOR_MAP_DATA_TYPE_FLOAT16, std::max<long long>(win_len, 1) * kD)
-                          : make_maps(&mq, &mk, &mv, q, (long long)g->n_q_heads * n_q, kk, win_len > 0 ? v : q,
+  argus_status stm = f16p ? make_maps(&mq, &mk, &mv, D, q, (long long)g->n_q_heads * n_q, kk, v16, g->n_kv_heads,
+                                      win_len, stride, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                      CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                                      std::max<long long>(win_len, 1) * D)
+                          : make_maps(&mq, &mk, &mv, D, q, (long long)g->n_q_heads * n_q, kk, win_len > 0 ? v : q,
                                       g->n_kv_heads, win_len, stride, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                                       CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, stride);
   if (stm != ARGUS_OK) return stm;
@@ -1102,16 +1138,16 @@ extern "C" argus_status argus_window_prefill_attn(const argus_geom* g, int32_t n
     // the window's V in fp16, scaled by 2^-e from its max |v|
     if (cudaMemsetAsync(vmax, 0, sizeof(uint32_t), s) != cudaSuccess)
       return fail(ARGUS_E_LAUNCH, "prefill: clearing the max word failed");
-    const long long n_vec = (long long)g->n_kv_heads * win_len * (kD / 8);
+    const long long n_vec = (long long)g->n_kv_heads * win_len * (D / 8);
     const int blocks = (int)std::max<long long>(1, std::min<long long>((n_vec + 255) / 256, 8LL * device_sm_count()));
     if (win_len > 0) {
-      v16_max_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint16_t*>(v), stride, win_len, n_vec, vmax);
-      v16_convert_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint16_t*>(v), stride, win_len, n_vec, vmax, v16);
+      v16_max_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint16_t*>(v), stride, win_len, D, n_vec, vmax);
+      v16_convert_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint16_t*>(v), stride, win_len, D, n_vec, vmax, v16);
       argus_status stc = launch_status("argus_window_prefill_attn (fp16 v)");
       if (stc != ARGUS_OK) return stc;
     }
   }
-  return launch_attention(f16p ? 1 : 0, mq, mk, mv, p, g->n_kv_heads, (long long)g->n_q_heads * n_q, s);
+  return launch_attention(f16p ? 1 : 0, D, mq, mk, mv, p, g->n_kv_heads, (long long)g->n_q_heads * n_q, s);
 }
 
 extern "C" argus_status argus_paged_window_prefill_workspace_bytes(const argus_geom* g, int32_t n_q, int64_t win_len,
@@ -1179,17 +1215,18 @@ extern "C" argus_status argus_paged_window_prefill_attn(const argus_geom* g, int
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   if (p.nsplit > 1) {
     p.ws_o = reinterpret_cast<float*>(w8 + L.part);
-    p.ws_lse = p.ws_o + (size_t)tiles_total * p.nsplit * kBM * kD;
+    p.ws_lse = p.ws_o + (size_t)tiles_total * p.nsplit * kBM * g->head_dim;
   }
   uint32_t* words = reinterpret_cast<uint32_t*>(w8 + L.words);
   sp.Hkv = g->n_kv_heads;
   sp.P = g->page_tokens;
   sp.max_pages = max_pages;
+  sp.D = g->head_dim;
   sp.page_codec = page_codec;
   sp.block_table = block_table;
   sp.win_pos0 = win_pos0;
   sp.win_len = win_len;
-  sp.n_vec = (long long)g->n_kv_heads * win_len * (kD / 8);
+  sp.n_vec = (long long)g->n_kv_heads * win_len * (sp.D / 8);
   sp.k16 = reinterpret_cast<uint16_t*>(w8 + L.k16);
   sp.v16 = reinterpret_cast<uint16_t*>(w8 + L.v16);
   sp.kmax = words;
@@ -1204,9 +1241,9 @@ extern "C" argus_status argus_paged_window_prefill_attn(const argus_geom* g, int
   p.qfac = sp.qfac;
   CUtensorMap mq, mk, mv;
   const long long wl = std::max<long long>(win_len, 1);
-  argus_status stm = make_maps(&mq, &mk, &mv, sp.q16, sp.q_rows, sp.k16, sp.v16, g->n_kv_heads, win_len, wl * kD,
-                               CU_TENSOR_MAP_DATA_TYPE_FLOAT16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                               CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wl * kD);
+  argus_status stm = make_maps(&mq, &mk, &mv, sp.D, sp.q16, sp.q_rows, sp.k16, sp.v16, g->n_kv_heads, win_len,
+                               wl * sp.D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                               CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wl * sp.D);
   if (stm != ARGUS_OK) return stm;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(words, 0, 16, s) != cudaSuccess) return fail(ARGUS_E_LAUNCH, "paged prefill: clearing the max words failed");
@@ -1219,5 +1256,5 @@ extern "C" argus_status argus_paged_window_prefill_attn(const argus_geom* g, int
   stage_q_kernel<<<(unsigned)((sp.q_rows + 7) / 8), 256, 0, s>>>(sp);
   argus_status stc = launch_status("argus_paged_window_prefill_attn (staging)");
   if (stc != ARGUS_OK) return stc;
-  return launch_attention(2, mq, mk, mv, p, g->n_kv_heads, sp.q_rows, s);
+  return launch_attention(2, sp.D, mq, mk, mv, p, g->n_kv_heads, sp.q_rows, s);
 }

@@ -46,7 +46,7 @@ def _staged_lse_bound(c, win_len):
     G = c.Hq // c.Hkv
     Kh = np.repeat(np.abs(K), G, axis=0)                                 # [Hq][W][D]
     m = np.einsum("hqd,hkd->hqk", np.abs(c.pq64), Kh).max(axis=2)         # [Hq][n_q]
-    return W.softmax_scale(128) / np.log(2.0) * 2.0 ** -11 * m
+    return W.softmax_scale(c.D) / np.log(2.0) * 2.0 ** -11 * m
 
 
 MODES = [(1, False), (1, True), (3, True)]
@@ -59,15 +59,16 @@ MODES = [(1, False), (1, True), (3, True)]
     (3, 3, 1, 5, [2, 5]),               # a single query row, windows of 2, 3 and 1 keys
     (4, 2, 129, 1000, [129, 640, 1000]),
 ])
-def test_window_prefill_at_unaligned_shapes(Hq, Hkv, n_q, ctx, cuts, splits, use_ws):
-    q = W.normal((Hq, n_q, 128), W.BF16, 701 + n_q)
+@pytest.mark.parametrize("D", [128, 64])
+def test_window_prefill_at_unaligned_shapes(Hq, Hkv, n_q, ctx, cuts, splits, use_ws, D):
+    q = W.normal((Hq, n_q, D), W.BF16, 701 + n_q)
     kv_len = ctx + n_q
-    k = W.normal((Hkv, kv_len, 128), W.BF16, 702 + n_q)
-    v = W.normal((Hkv, kv_len, 128), W.BF16, 703 + n_q)
+    k = W.normal((Hkv, kv_len, D), W.BF16, 702 + n_q)
+    v = W.normal((Hkv, kv_len, D), W.BF16, 703 + n_q)
     f = lambda t: C.bf16_bits_to_f64(W.to_bits(t))
-    g = argus.geom(Hq, Hkv, 128, 16)
+    g = argus.geom(Hq, Hkv, D, 16)
     qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
-    acc_o = torch.full((Hq, n_q, 128), float("nan"), dtype=torch.float32, device=DEV)
+    acc_o = torch.full((Hq, n_q, D), float("nan"), dtype=torch.float32, device=DEV)
     acc_l = torch.full((Hq, n_q), float("nan"), dtype=torch.float32, device=DEV)
     bounds = [0] + cuts + [kv_len]
     for wi, (w0, w1) in enumerate(zip(bounds[:-1], bounds[1:])):
@@ -75,22 +76,22 @@ def test_window_prefill_at_unaligned_shapes(Hq, Hkv, n_q, ctx, cuts, splits, use
         if use_ws:
             n = argus.window_prefill_workspace_bytes(g, n_q, w1 - w0, splits)
             ws = torch.full((max(n, 16) // 4 + 1,), float("nan"), dtype=torch.float32, device=DEV)
-        argus.window_prefill_attn(g, n_q, qd, kd[:, w0:], vd[:, w0:], kv_len * 128, w1 - w0, w0, ctx,
-                                  W.softmax_scale(128), acc_o, acc_l, 1 if wi else 0, num_splits=splits, ws=ws)
+        argus.window_prefill_attn(g, n_q, qd, kd[:, w0:], vd[:, w0:], kv_len * D, w1 - w0, w0, ctx,
+                                  W.softmax_scale(D), acc_o, acc_l, 1 if wi else 0, num_splits=splits, ws=ws)
     torch.cuda.synchronize()
-    ro, rl = oracle.window_attention(f(q), f(k), f(v), 0, ctx, W.softmax_scale(128))
+    ro, rl = oracle.window_attention(f(q), f(k), f(v), 0, ctx, W.softmax_scale(D))
     _check(acc_o.cpu().numpy(), acc_l.cpu().numpy(), ro, rl)
 
 
-def _paged(Hq, Hkv, P, n_q, ctx, tiers, seed):
+def _paged(Hq, Hkv, P, n_q, ctx, tiers, seed, D=128):
     """One sequence of ctx + n_q tokens in pages of the given codecs (cycled,
     oldest first), demoted by the library and by the oracle; bf16 query."""
     total = ctx + n_q
     n_pages = -(-total // P)
     pc = np.array([tiers[i % len(tiers)] for i in range(n_pages)]).reshape(1, n_pages)
     src = W.FP16 if W.FP16 in tiers else W.BF16          # a 16-bit tier stores its own source type
-    c = build_case(Hq, Hkv, 128, P, [total], pc, src, q_dtype=W.BF16, seed=seed, outliers=True, extra_slots=3)
-    q = W.normal((Hq, n_q, 128), W.BF16, seed + 50)
+    c = build_case(Hq, Hkv, D, P, [total], pc, src, q_dtype=W.BF16, seed=seed, outliers=True, extra_slots=3)
+    q = W.normal((Hq, n_q, D), W.BF16, seed + 50)
     c.pq = q.to(DEV)
     c.pq64 = C.bf16_bits_to_f64(W.to_bits(q))
     c.n_pages = n_pages
@@ -98,15 +99,15 @@ def _paged(Hq, Hkv, P, n_q, ctx, tiers, seed):
 
 
 def _run_paged(c, n_q, ctx, cuts, splits=0, status=None):
-    g = argus.geom(c.Hq, c.Hkv, 128, c.P)
-    acc_o = torch.full((c.Hq, n_q, 128), float("nan"), dtype=torch.float32, device=DEV)
+    g = argus.geom(c.Hq, c.Hkv, c.D, c.P)
+    acc_o = torch.full((c.Hq, n_q, c.D), float("nan"), dtype=torch.float32, device=DEV)
     acc_l = torch.full((c.Hq, n_q), float("nan"), dtype=torch.float32, device=DEV)
     bounds = [0] + cuts + [ctx + n_q]
     for wi, (w0, w1) in enumerate(zip(bounds[:-1], bounds[1:])):
         n = argus.paged_window_prefill_workspace_bytes(g, n_q, w1 - w0, splits)
         ws = torch.full((n,), 0xFF, dtype=torch.uint8, device=DEV)      # NaN-filled: needs no initialisation
         argus.paged_window_prefill_attn(g, n_q, c.pq, c.pools, c.d_codec[0], c.d_table[0], c.n_pages, w0, w1 - w0,
-                                        ctx, W.softmax_scale(128), acc_o, acc_l, 1 if wi else 0, ws,
+                                        ctx, W.softmax_scale(c.D), acc_o, acc_l, 1 if wi else 0, ws,
                                         num_splits=splits, status=status)
     torch.cuda.synchronize()
     return acc_o.cpu().numpy(), acc_l.cpu().numpy()
@@ -120,20 +121,22 @@ FIVE = [W.INT1_G32, W.INT2_G32, W.INT4_G32, W.INT8, W.FP8_E4M3, W.BF16]   # ever
     (16, 128, 37 * 16 + 5, [100, 333, 597]),      # windows start mid-page; the last one is the chunk plus a tail
     (64, 70, 900, [450]),
 ])
-def test_paged_windows_five_tiers_fold_to_single_pass(P, n_q, ctx, cuts, splits):
-    c = _paged(16, 2, P, n_q, ctx, FIVE, seed=720 + P)
+@pytest.mark.parametrize("D", [128, 64])
+def test_paged_windows_five_tiers_fold_to_single_pass(P, n_q, ctx, cuts, splits, D):
+    c = _paged(16, 2, P, n_q, ctx, FIVE, seed=720 + P, D=D)
     go, gl = _run_paged(c, n_q, ctx, cuts, splits=splits)
     ro, rl = oracle.paged_window_attention(c.pq64, c.Hkv, c.P, c.opools, c.page_codec, c.table, 0, 0, ctx + n_q, ctx,
-                                           W.softmax_scale(128), seq_len=ctx + n_q)
+                                           W.softmax_scale(D), seq_len=ctx + n_q)
     _check(go, gl, ro, rl, _staged_lse_bound(c, ctx + n_q))
 
 
 @pytest.mark.parametrize("codec", [W.FP16, W.BF16, W.FP8_E4M3, W.INT8, W.INT4_G32, W.INT2_G32, W.INT1_G32])
-def test_paged_window_single_codec(codec):
-    c = _paged(8, 1, 16, 96, 500, [codec], seed=740 + codec)
+@pytest.mark.parametrize("D", [128, 64])
+def test_paged_window_single_codec(codec, D):
+    c = _paged(8, 1, 16, 96, 500, [codec], seed=740 + codec, D=D)
     go, gl = _run_paged(c, 96, 500, [250])
     ro, rl = oracle.paged_window_attention(c.pq64, c.Hkv, c.P, c.opools, c.page_codec, c.table, 0, 0, 596, 500,
-                                           W.softmax_scale(128), seq_len=596)
+                                           W.softmax_scale(D), seq_len=596)
     _check(go, gl, ro, rl, _staged_lse_bound(c, 596))
 
 

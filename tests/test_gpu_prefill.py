@@ -21,11 +21,11 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _data(Hq, Hkv, n_q, ctx, seed):
-    q = W.normal((Hq, n_q, 128), W.BF16, seed)
+def _data(Hq, Hkv, n_q, ctx, seed, D=128):
+    q = W.normal((Hq, n_q, D), W.BF16, seed)
     kv_len = ctx + n_q
-    k = W.normal((Hkv, kv_len, 128), W.BF16, seed + 1)
-    v = W.normal((Hkv, kv_len, 128), W.BF16, seed + 2)
+    k = W.normal((Hkv, kv_len, D), W.BF16, seed + 1)
+    v = W.normal((Hkv, kv_len, D), W.BF16, seed + 2)
     f = lambda t: C.bf16_bits_to_f64(W.to_bits(t))
     return q, k, v, f(q), f(k), f(v)
 
@@ -44,20 +44,20 @@ def _ws(g, n_q, win_len, splits, use_ws=True):
     return torch.full((max(n, 16) // 4,), float("nan"), dtype=torch.float32, device=DEV)
 
 
-def _run_windows(Hq, Hkv, n_q, ctx, windows, seed, scale=None, splits=1, use_ws=False, vmul=1.0):
-    q, k, v, q64, k64, v64 = _data(Hq, Hkv, n_q, ctx, seed)
+def _run_windows(Hq, Hkv, n_q, ctx, windows, seed, scale=None, splits=1, use_ws=False, vmul=1.0, D=128):
+    q, k, v, q64, k64, v64 = _data(Hq, Hkv, n_q, ctx, seed, D)
     if vmul != 1.0:
         v = (v.float() * vmul).to(torch.bfloat16)
         v64 = C.bf16_bits_to_f64(W.to_bits(v))
-    scale = W.softmax_scale(128) if scale is None else scale
-    g = argus.geom(Hq, Hkv, 128, 16)
+    scale = W.softmax_scale(D) if scale is None else scale
+    g = argus.geom(Hq, Hkv, D, 16)
     qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
     kv_len = ctx + n_q
-    acc_o = torch.zeros((Hq, n_q, 128), dtype=torch.float32, device=DEV)
+    acc_o = torch.zeros((Hq, n_q, D), dtype=torch.float32, device=DEV)
     acc_l = torch.full((Hq, n_q), float("-inf"), dtype=torch.float32, device=DEV)
     for wi, (w0, w1) in enumerate(windows):
         ws = _ws(g, n_q, w1 - w0, splits, use_ws)
-        argus.window_prefill_attn(g, n_q, qd, kd[:, w0:], vd[:, w0:], kv_len * 128, w1 - w0, w0, ctx, scale,
+        argus.window_prefill_attn(g, n_q, qd, kd[:, w0:], vd[:, w0:], kv_len * D, w1 - w0, w0, ctx, scale,
                                   acc_o, acc_l, 1 if wi > 0 else 0, num_splits=splits, ws=ws)
     torch.cuda.synchronize()
     ref_o, ref_l = oracle.window_attention(q64, k64, v64, 0, ctx, scale)
@@ -81,27 +81,29 @@ def test_single_window_full_view_small(splits, use_ws):
 
 
 @pytest.mark.parametrize("splits,use_ws", MODES + [(2, True), (5, True)])
-def test_causal_chunk_window_only(splits, use_ws):
+@pytest.mark.parametrize("D", [128, 64])
+def test_causal_chunk_window_only(splits, use_ws, D):
     # a 256-row chunk attending only to itself: causal inside the chunk; with 5
     # key ranges over at most 2 visible blocks some ranges are empty
-    q, k, v, q64, k64, v64 = _data(2, 1, 256, 0, 503)
-    g = argus.geom(2, 1, 128, 16)
-    acc_o = torch.empty((2, 256, 128), dtype=torch.float32, device=DEV)
+    q, k, v, q64, k64, v64 = _data(2, 1, 256, 0, 503, D)
+    g = argus.geom(2, 1, D, 16)
+    acc_o = torch.empty((2, 256, D), dtype=torch.float32, device=DEV)
     acc_l = torch.empty((2, 256), dtype=torch.float32, device=DEV)
     argus.window_prefill_attn(g, 256, q.to(DEV), k.to(DEV), v.to(DEV), 0, 256, 1000, 1000,
-                              W.softmax_scale(128), acc_o, acc_l, 0, num_splits=splits,
+                              W.softmax_scale(D), acc_o, acc_l, 0, num_splits=splits,
                               ws=_ws(g, 256, 256, splits, use_ws))
     torch.cuda.synchronize()
-    ro, rl = oracle.window_attention(q64, k64, v64, 1000, 1000, W.softmax_scale(128))
+    ro, rl = oracle.window_attention(q64, k64, v64, 1000, 1000, W.softmax_scale(D))
     _check(acc_o.cpu().numpy(), acc_l.cpu().numpy(), ro, rl)
 
 
 @pytest.mark.parametrize("splits,use_ws", MODES)
 @pytest.mark.parametrize("Hq,Hkv", [(2, 1), (16, 2)])
-def test_windows_folded_equal_single_pass(Hq, Hkv, splits, use_ws):
+@pytest.mark.parametrize("D", [128, 64])
+def test_windows_folded_equal_single_pass(Hq, Hkv, splits, use_ws, D):
     n_q, ctx = 256, 768
     windows = [(0, 256), (256, 768), (768, 1024)]      # two cache windows, then the chunk
-    go, gl, ro, rl = _run_windows(Hq, Hkv, n_q, ctx, windows, seed=505 + Hq, splits=splits, use_ws=use_ws)
+    go, gl, ro, rl = _run_windows(Hq, Hkv, n_q, ctx, windows, seed=505 + Hq, splits=splits, use_ws=use_ws, D=D)
     _check(go, gl, ro, rl)
 
 
@@ -121,9 +123,9 @@ def test_window_beyond_every_query_is_identity(splits, use_ws):
 
 
 def test_rejects_unsupported_shapes():
-    g = argus.geom(2, 1, 64, 16)
-    t = torch.zeros((2, 128, 64), dtype=torch.bfloat16, device=DEV)
-    o = torch.zeros((2, 128, 64), device=DEV)
+    g = argus.geom(2, 1, 96, 16)
+    t = torch.zeros((2, 128, 96), dtype=torch.bfloat16, device=DEV)
+    o = torch.zeros((2, 128, 96), device=DEV)
     l = torch.zeros((2, 128), device=DEV)
     with pytest.raises(argus.ArgusError) as e:
         argus.window_prefill_attn(g, 128, t, t, t, 0, 128, 0, 0, 0.1, o, l, 0)
@@ -142,11 +144,12 @@ def test_automatic_splits_with_a_long_window():
 
 
 @pytest.mark.parametrize("vmul", [3.0e5, 2.0 ** -20])
-def test_fp16_value_path_scales_v_outside_the_fp16_range(vmul):
+@pytest.mark.parametrize("D", [128, 64])
+def test_fp16_value_path_scales_v_outside_the_fp16_range(vmul, D):
     """V far above fp16's range is scaled by a power of two before the fp16
     copy (and the output scaled back); V far below keeps its accuracy."""
     go, gl, ro, rl = _run_windows(2, 1, 128, 256, [(0, 256), (256, 384)], seed=513, splits=2, use_ws=True,
-                                  vmul=vmul)
+                                  vmul=vmul, D=D)
     _check(go, gl, ro, rl)
 
 
@@ -164,7 +167,8 @@ def test_split_workspace_too_small_is_rejected():
 
 @pytest.mark.parametrize("splits,use_ws", MODES)
 @pytest.mark.parametrize("ramp", ["rising", "late_key"])
-def test_scores_growing_past_the_lazy_rescale_threshold(splits, use_ws, ramp):
+@pytest.mark.parametrize("D", [128, 64])
+def test_scores_growing_past_the_lazy_rescale_threshold(splits, use_ws, ramp, D):
     """Key blocks whose scores rise by more than 2^8 (8 in log2 units) over the
     running maximum, block after block: the softmax must rescale the TMEM
     accumulator of O (the lazy max moves).  "rising" scales the keys of block j
@@ -173,7 +177,7 @@ def test_scores_growing_past_the_lazy_rescale_threshold(splits, use_ws, ramp):
     block aligned with the first query rows, far above everything before it.
     The host checks on the oracle's own scores that such jumps occur."""
     Hq, Hkv, n_q, ctx = 2, 1, 128, 1024
-    q, k, v, q64, k64, v64 = _data(Hq, Hkv, n_q, ctx, 521)
+    q, k, v, q64, k64, v64 = _data(Hq, Hkv, n_q, ctx, 521, D)
     kf = k.float()
     if ramp == "rising":
         for j in range(ctx // 128):
@@ -183,21 +187,21 @@ def test_scores_growing_past_the_lazy_rescale_threshold(splits, use_ws, ramp):
         kf[:, 6 * 128 + 9] = q.float()[1, 3] * 9.0
     k = kf.to(torch.bfloat16)
     k64 = C.bf16_bits_to_f64(W.to_bits(k))
-    scale = W.softmax_scale(128)
+    scale = W.softmax_scale(D)
     # the branch is reached: some row's block maximum (log2 units) jumps by > 8
     # over the maximum of the earlier blocks its softmax group saw
-    s2 = np.einsum("hqd,hkd->hqk", q64.reshape(Hq, n_q, 128), np.repeat(k64[:, :ctx], Hq // Hkv, 0)) * scale / math.log(2)
+    s2 = np.einsum("hqd,hkd->hqk", q64.reshape(Hq, n_q, D), np.repeat(k64[:, :ctx], Hq // Hkv, 0)) * scale / math.log(2)
     bm = s2.reshape(Hq, n_q, ctx // 128, 128).max(axis=3)           # [Hq][n_q][block]
     jumps = [np.max(bm[:, :, j] - np.maximum.accumulate(bm[:, :, g::2], axis=2)[:, :, (j - g) // 2 - 1])
              for g in (0, 1) for j in range(g + 2, ctx // 128, 2)]
     assert max(jumps) > 8.0
-    g = argus.geom(Hq, Hkv, 128, 16)
+    g = argus.geom(Hq, Hkv, D, 16)
     kd, vd = k.to(DEV), v.to(DEV)
     kv_len = ctx + n_q
-    acc_o = torch.zeros((Hq, n_q, 128), dtype=torch.float32, device=DEV)
+    acc_o = torch.zeros((Hq, n_q, D), dtype=torch.float32, device=DEV)
     acc_l = torch.full((Hq, n_q), float("-inf"), dtype=torch.float32, device=DEV)
     for wi, (w0, w1) in enumerate([(0, ctx), (ctx, kv_len)]):
-        argus.window_prefill_attn(g, n_q, q.to(DEV), kd[:, w0:], vd[:, w0:], kv_len * 128, w1 - w0, w0, ctx,
+        argus.window_prefill_attn(g, n_q, q.to(DEV), kd[:, w0:], vd[:, w0:], kv_len * D, w1 - w0, w0, ctx,
                                   scale, acc_o, acc_l, 1 if wi else 0, num_splits=splits,
                                   ws=_ws(g, n_q, w1 - w0, splits, use_ws))
     torch.cuda.synchronize()
