@@ -191,6 +191,29 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
       : "memory");
 }
 
+// Two IEEE fp32 operations in one instruction (packed f32x2, each lane rounded
+// to nearest even like its scalar form): d = a * b + c and d = a + b.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0, float c1) {
+  asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -255,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], kGroupWarps * 32);
+      mbar_init(&p_full[b], kGroupWarps);   // one arrival per softmax warp
       mbar_init(&s_free[b], 1);
       mbar_init(&o_done[b], 1);
     }
@@ -364,7 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t sS = tS[grp] + lane_off, sO = tO[grp] + lane_off;
-    float m = -INFINITY, l = 0.f;
+    // l is kept as two partial sums (even and odd keys) for the packed adds
+    float m = -INFINITY, la = 0.f, lb = 0.f;
     bool alive = true;
     int k = 0;
     for (int i = grp; i < nb && alive; i += 2, ++k) {
@@ -379,14 +403,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       // pass 1: block maximum (masking only on a block that crosses the edge)
       float mj = -INFINITY;
       if (!edge) {
+        // four independent running maxima: a single chain of 64 dependent
+        // max instructions would set the pace of this pass
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int c = 0; c < kBN / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(sS + c * 32, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) mj = fmaxf(mj, fmaxf(__uint_as_float(v[e]), __uint_as_float(v[e + 1])));
+          for (int e = 0; e < 32; e += 2)
+            mx[(e / 2) & 3] = max3(mx[(e / 2) & 3], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
         }
+        mj = max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
       } else {
 #pragma unroll
         for (int c = 0; c < kBN / 32; ++c) {
@@ -415,7 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(sO + c * 32, v);
         }
         tmem_wait_st();
-        l *= r;
+        la *= r;
+        lb *= r;
       }
       if (move) m = mj;
       // pass 2: P over the consumed scores -- fp16 P * 2^7 (at most 2^15 under
@@ -434,8 +464,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!edge && m != -INFINITY) {   // per-row branch: math only
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e]), sc, -mm));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), sc, -mm));
+            // a key pair's exponents and sums in packed f32x2 instructions
+            float x0, x1;
+            fma2(x0, x1, __uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]), sc, sc, -mm, -mm);
+            const float p0 = fast_exp2(x0);
+            const float p1 = fast_exp2(x1);
             if (F16P) {
               vh[e] = pack_f16x2(p0, p1);
             } else {
@@ -443,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               vh[e] = hi;
               vl[e] = pack_bf16x2(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xFFFF0000u));
             }
-            l += p0 + p1;
+            add2(la, lb, la, lb, p0, p1);
           }
         } else {
 #pragma unroll
@@ -459,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               vh[e] = hi;
               vl[e] = pack_bf16x2(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xFFFF0000u));
             }
-            l += p0 + p1;
+            add2(la, lb, la, lb, p0, p1);
           }
         }
         // keys 16c .. 16c+15: (high part) in columns 16c .. 16c+7, low part in
@@ -467,10 +500,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st8(sS + c * 16, vh);
         if (!F16P) tmem_st8(sS + c * 16 + 8, vl);
       }
+      // every lane's P stores have completed (wait::st) before the warp's one
+      // arrival releases them to the MMA thread
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[grp]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[grp]);
     }
+    const float l = la + lb;
     // ---- this group's last P.V
     const int nk = (nb > grp) ? (nb - grp + 1) / 2 : 0;   // blocks this group owned
     if (alive && nk > 0) {

@@ -9,11 +9,14 @@ and use inputs larger than L2 where the kernel streams HBM.
   decode_mixed    one layer of the mixed-tier decode (14/2 heads, D 64, 16 pages x 1024)
   decode_bf16     batched BF16 decode, batch 8 of the batched workload's shape
   decode_fp8      the same pages demoted to FP8
+  decode_int2     the same pages demoted to INT2
+  decode_int1     the same pages demoted to INT1
   decode_sparse   one layer of the sparse workload: decode over the indexer's selection
   quantize_fp8    demote 128 Ki 16x128 BF16 units to FP8 (512 MB read)
   quantize_int8   the same to INT8
   quantize_int4   the same to INT4
   quantize_int2   the same to INT2
+  quantize_int1   the same to INT1
   select          indexer scores + top-k for one layer of the sparse workload
   prefill         one 131072-token window of the windowed prefill
   fold            fold a 16 x 1024 x 128 fp32 partial into an accumulator
@@ -57,19 +60,18 @@ def _decode_mixed(dev):
     return lambda: argus.paged_decode_attn(a, ws)
 
 
-def _decode_batched(dev, fp8):
+def _decode_batched(dev, codec):
     B, Hq, Hkv, D, P, MAXP = 8, 32, 8, 128, 16, 2048
     lens = W.uniform_ints(B, 8192, 32768, W.seed_of("batched", 0, 3))
     table, n_slots = W.paged_block_table(lens, P, MAXP, W.seed_of("batched", 0, 4))
     g = argus.geom(Hq, Hkv, D, P)
     pool = argus.Pool(W.BF16, W.normal((n_slots, 2, Hkv, P, D), W.BF16, W.seed_of("batched", 0, 1), device=dev),
                       None, n_slots)
-    codec = W.BF16
-    if fp8:
+    if codec != W.BF16:
         ids = torch.arange(n_slots, dtype=torch.int32, device=dev)
-        dst = argus.Pool.empty(W.FP8_E4M3, n_slots, Hkv, P, D, device=dev)
+        dst = argus.Pool.empty(codec, n_slots, Hkv, P, D, device=dev)
         argus.quantize_pages(g, W.BF16, pool.codes, n_slots, ids, dst, ids, n_slots)
-        pool, codec = dst, W.FP8_E4M3
+        pool = dst
     q = W.normal((B, Hq, D), W.BF16, W.seed_of("batched", 0, 0), device=dev)
     out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
     a = argus.decode_args(g, B, q, [pool], torch.full((B, MAXP), codec, dtype=torch.uint8, device=dev),
@@ -151,13 +153,16 @@ def _fold(dev):
 
 CASES = {
     "decode_mixed": _decode_mixed,
-    "decode_bf16": lambda d: _decode_batched(d, False),
-    "decode_fp8": lambda d: _decode_batched(d, True),
+    "decode_bf16": lambda d: _decode_batched(d, W.BF16),
+    "decode_fp8": lambda d: _decode_batched(d, W.FP8_E4M3),
+    "decode_int2": lambda d: _decode_batched(d, W.INT2_G32),
+    "decode_int1": lambda d: _decode_batched(d, W.INT1_G32),
     "decode_sparse": _decode_sparse,
     "quantize_fp8": lambda d: _quantize(d, W.FP8_E4M3),
     "quantize_int8": lambda d: _quantize(d, W.INT8),
     "quantize_int4": lambda d: _quantize(d, W.INT4_G32),
     "quantize_int2": lambda d: _quantize(d, W.INT2_G32),
+    "quantize_int1": lambda d: _quantize(d, W.INT1_G32),
     "select": _select,
     "prefill": _prefill,
     "fold": _fold,
