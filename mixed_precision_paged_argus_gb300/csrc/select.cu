@@ -44,6 +44,9 @@ constexpr int kTopkSmemKeys = 40 * 1024;   // rows up to this many pages are sta
 constexpr int kMaxPpc = 256;               // pages per score CTA (its keys per head in registers)
 constexpr int kEmit = 4;                   // largest keys each score CTA reports per KV head
 constexpr long long kScoreSmemBytes = 75 * 1024;   // a score CTA's shared memory (3 CTAs per SM)
+constexpr int kPieceBytes = 16384;         // bulk-copy pieces of a score CTA's slab range, one mbarrier each
+constexpr int kMaxPieces = 8;
+static_assert(kScoreSmemBytes <= (long long)kPieceBytes * kMaxPieces, "one mbarrier per piece");
 
 // Whether each score lane's rows all belong to one KV head (the rows per pass
 // are a multiple of Hkv): its G-query sums then live in registers.
@@ -52,11 +55,12 @@ __host__ __device__ constexpr bool score_fixed_head(int D, int Hkv) {
 }
 
 // Dynamic shared memory of a score CTA: its range's compressed keys, the
-// G-query sums (only when lanes mix heads), the range's order keys, an mbarrier.
+// G-query sums (only when lanes mix heads), the range's order keys, the
+// pieces' mbarriers.
 inline size_t score_smem_bytes(long long Hkv, long long D, long long ppc) {
   const size_t slab = ((size_t)ppc * Hkv * D * 2 + 127) / 128 * 128;
   const size_t qs = score_fixed_head((int)D, (int)Hkv) ? 0 : (size_t)Hkv * D * 4;
-  return slab + qs + (size_t)((ppc * Hkv + 1) & ~1LL) * 4 + 16;
+  return slab + qs + (size_t)((ppc * Hkv + 1) & ~1LL) * 4 + 8 * kMaxPieces;
 }
 constexpr int kSurvivorsPerLane = 16;      // keys >= T0 that one warp searches in registers
 
@@ -141,38 +145,43 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) score_kernel(i
   // the top-k grid may start its prologue now; it waits for this grid's keys
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // shared memory: the range's compressed keys [ppc * Hkv][D] bf16, the
-  // G-query sums [Hkv][D] fp32, the range's order keys [ppc][Hkv], an mbarrier
+  // G-query sums [Hkv][D] fp32, the range's order keys [ppc][Hkv], mbarriers
   extern __shared__ __align__(128) uint8_t sm_raw[];
   const size_t slab_bytes = ((size_t)ppc * Hkv * D * 2 + 127) / 128 * 128;
   const uint16_t* slab = reinterpret_cast<const uint16_t*>(sm_raw);
   const bool fixed_h = score_fixed_head(D, Hkv);
   float* qsum = reinterpret_cast<float*>(sm_raw + slab_bytes);   // [Hkv][D] when !fixed_h
   uint32_t* skeys = reinterpret_cast<uint32_t*>(qsum + (fixed_h ? 0 : Hkv * D));
-  uint64_t* bar = reinterpret_cast<uint64_t*>(skeys + ((ppc * Hkv + 1) & ~1));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(skeys + ((ppc * Hkv + 1) & ~1));
   const int b = blockIdx.y;
   const int p0 = blockIdx.x * ppc;
   const int Hq = Hkv * G;
   int n = n_pages[b];
   n = max(0, min(n, max_pages));
-  if (p0 >= n) return;
+  const bool active = p0 < n;   // the range holds pages of the row
   constexpr int LPH = D / 8;               // lanes per (page, head) row, 16 bytes each
   constexpr int RPW = 32 / LPH;            // rows per warp and pass
   constexpr int RPP = (kScoreThreads / 32) * RPW;  // rows per CTA and pass
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = lane / LPH, li = lane % LPH;
-  const int p_end = min(n, p0 + ppc);
+  const int p_end = active ? min(n, p0 + ppc) : p0;
   const int n_rows = (p_end - p0) * Hkv;
+  const uint32_t total = (uint32_t)n_rows * D * 2;
+  const int n_pieces = (int)((total + kPieceBytes - 1) / kPieceBytes);
   // rows of this CTA are contiguous in the slab: (p0 * Hkv + row) * D.  One
-  // thread streams them into shared memory with bulk copies (16 KB pieces on
-  // one mbarrier) before the query sums, so the whole range is in flight at once
-  if (threadIdx.x == 0) {
-    mbar_init(bar, 1);
+  // thread streams them into shared memory with bulk copies, 16 KB pieces on
+  // an mbarrier each, while the other warps form the query sums: the whole
+  // range is in flight at once, and scoring starts as soon as its first rows
+  // have landed
+  if (threadIdx.x == 0 && active) {
+    for (int i = 0; i < n_pieces; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
-    const uint32_t total = (uint32_t)n_rows * D * 2;
-    mbar_arrive_expect_tx(bar, total);
     const uint8_t* src = reinterpret_cast<const uint8_t*>(ckeys + (((size_t)b * max_pages + p0) * Hkv) * D);
-    for (uint32_t off = 0; off < total; off += 16384u)
-      bulk_g2s(sm_raw + off, src + off, min(16384u, total - off), bar);
+    for (int i = 0; i < n_pieces; ++i) {
+      const uint32_t off = (uint32_t)i * kPieceBytes, bytes = min((uint32_t)kPieceBytes, total - off);
+      mbar_arrive_expect_tx(&bars[i], bytes);
+      bulk_g2s(sm_raw + off, src + off, bytes, &bars[i]);
+    }
   }
   uint4 x[kRowBatch];
   auto load_batch = [&](int r0) {
@@ -221,11 +230,16 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) score_kernel(i
     }
   }
   __syncthreads();
-  // the rows have landed (a copy that never completes leaves this CTA's keys
-  // unwritten rather than waiting forever)
-  if (!mbar_wait(bar, 0)) return;
+  if (!active) return;   // no copy was issued
   static_assert(kRowBatch == 8, "the transposed reduction below folds 8 rows");
+  int ready = 0;   // pieces known to have landed
   for (int r0 = warp * RPW + sub; r0 - sub < n_rows; r0 += kRowBatch * RPP) {
+    // the pieces holding this warp's rows of the batch (a copy that never
+    // completes leaves this CTA's keys unwritten rather than waiting forever)
+    const int last_row = min(r0 - sub + (kRowBatch - 1) * RPP + RPW - 1, n_rows - 1);
+    const int need = (int)(((uint32_t)(last_row + 1) * D * 2 - 1) / kPieceBytes);
+    for (; ready <= need; ++ready)
+      if (!mbar_wait(&bars[ready], 0)) return;
     load_batch(r0);
     float sv[kRowBatch];
 #pragma unroll
