@@ -188,6 +188,30 @@ __device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
+// Two IEEE fp32 operations in one instruction (packed f32x2, sm_100 and later):
+// each lane is rounded to nearest even exactly as its scalar form, and nothing
+// is contracted into a fused multiply-add that the scalar code would not form.
+#define ARGUS_F2_BINARY(name, op)                                                              \
+  __device__ __forceinline__ void name(float& d0, float& d1, float a0, float a1, float b0, float b1) { \
+    asm("{\n\t.reg .b64 a, b, d;\n\t"                                                         \
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t" op                                   \
+        " d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"                                               \
+        : "=f"(d0), "=f"(d1)                                                                    \
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));                                                 \
+  }
+ARGUS_F2_BINARY(f2_add, "add.rn.f32x2")
+ARGUS_F2_BINARY(f2_sub, "sub.rn.f32x2")
+ARGUS_F2_BINARY(f2_mul, "mul.rn.f32x2")
+#undef ARGUS_F2_BINARY
+__device__ __forceinline__ void f2_fma(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                       float c1) {
+  asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

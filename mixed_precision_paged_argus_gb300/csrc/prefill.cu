@@ -191,22 +191,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
       : "memory");
 }
 
-// Two IEEE fp32 operations in one instruction (packed f32x2, each lane rounded
-// to nearest even like its scalar form): d = a * b + c and d = a + b.
-__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0, float c1) {
-  asm("{\n\t.reg .b64 a, b, c, d;\n\t"
-      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
-      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
-}
-__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
-  asm("{\n\t.reg .b64 a, b, d;\n\t"
-      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-      "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
 // max(a, b, c) in one instruction
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
@@ -466,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 8; ++e) {
             // a key pair's exponents and sums in packed f32x2 instructions
             float x0, x1;
-            fma2(x0, x1, __uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]), sc, sc, -mm, -mm);
+            f2_fma(x0, x1, __uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]), sc, sc, -mm, -mm);
             const float p0 = fast_exp2(x0);
             const float p1 = fast_exp2(x1);
             if (F16P) {
@@ -476,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               vh[e] = hi;
               vl[e] = pack_bf16x2(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xFFFF0000u));
             }
-            add2(la, lb, la, lb, p0, p1);
+            f2_add(la, lb, la, lb, p0, p1);
           }
         } else {
 #pragma unroll
@@ -492,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               vh[e] = hi;
               vl[e] = pack_bf16x2(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xFFFF0000u));
             }
-            add2(la, lb, la, lb, p0, p1);
+            f2_add(la, lb, la, lb, p0, p1);
           }
         }
         // keys 16c .. 16c+15: (high part) in columns 16c .. 16c+7, low part in

@@ -161,10 +161,9 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
       float y[8];
       uint32_t dmin = 0xFFFFFFFFu;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        y[e] = f[e] * rscale;
-        dmin = min(dmin, (__float_as_uint(y[e]) & 0xFFFFFu) - 0x80000u + 8u);
-      }
+      for (int e = 0; e < 8; e += 2) f2_mul(y[e], y[e + 1], f[e], f[e + 1], rscale, rscale);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) dmin = min(dmin, (__float_as_uint(y[e]) & 0xFFFFFu) - 0x80000u + 8u);
       // the smallest |y| is the product of the smallest |x| (the product is
       // monotone in |x|), found on the packed source
       const uint32_t mn2 = __vminu2(__vminu2(raw.x & 0x7FFF7FFFu, raw.y & 0x7FFF7FFFu),
@@ -196,12 +195,19 @@ __device__ __forceinline__ void encode_store(const float (&f)[8], const uint4& r
       float dev = 0.f;   // largest distance of a product from its rounded value
       auto round8 = [&](auto clamp_tag) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float y = f[e] * rscale;
-          if (decltype(clamp_tag)::value) y = fminf(fmaxf(y, -127.f), 127.f);
-          const float tf = y + kRoundMagic;
-          dev = fmaxf(dev, fabsf(y - (tf - kRoundMagic)));
-          t[e] = __float_as_uint(tf);
+        for (int e = 0; e < 8; e += 2) {
+          float y0, y1, t0, t1, q0, q1, e0, e1;
+          f2_mul(y0, y1, f[e], f[e + 1], rscale, rscale);
+          if (decltype(clamp_tag)::value) {
+            y0 = fminf(fmaxf(y0, -127.f), 127.f);
+            y1 = fminf(fmaxf(y1, -127.f), 127.f);
+          }
+          f2_add(t0, t1, y0, y1, kRoundMagic, kRoundMagic);
+          f2_sub(q0, q1, t0, t1, kRoundMagic, kRoundMagic);
+          f2_sub(e0, e1, y0, y1, q0, q1);
+          dev = fmaxf(dev, fmaxf(fabsf(e0), fabsf(e1)));
+          t[e] = __float_as_uint(t0);
+          t[e + 1] = __float_as_uint(t1);
         }
       };
       if (scale < 0x1p-100f) round8(std::true_type{});   // the branch stays outside the loop
@@ -480,15 +486,23 @@ __device__ __forceinline__ void encode_affine_group(const uint4 (&x)[4], bool va
       uint32_t t[8];
       unpack8<SBF16>(x[m], f);
       float dev = 0.f;  // largest distance of a product from its rounded value
+      // element pairs in packed f32x2 instructions (the same IEEE operations)
       auto round8 = [&](auto clamp_tag) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          d[e] = f[e] - z;
-          float y = d[e] * r;
-          if (decltype(clamp_tag)::value) y = fminf(fmaxf(y, 0.f), (float)TOP);
-          const float tf = y + kRoundMagic;
-          dev = fmaxf(dev, fabsf(y - (tf - kRoundMagic)));
-          t[e] = __float_as_uint(tf);
+        for (int e = 0; e < 8; e += 2) {
+          f2_sub(d[e], d[e + 1], f[e], f[e + 1], z, z);
+          float y0, y1, t0, t1, q0, q1, e0, e1;
+          f2_mul(y0, y1, d[e], d[e + 1], r, r);
+          if (decltype(clamp_tag)::value) {
+            y0 = fminf(fmaxf(y0, 0.f), (float)TOP);
+            y1 = fminf(fmaxf(y1, 0.f), (float)TOP);
+          }
+          f2_add(t0, t1, y0, y1, kRoundMagic, kRoundMagic);
+          f2_sub(q0, q1, t0, t1, kRoundMagic, kRoundMagic);
+          f2_sub(e0, e1, y0, y1, q0, q1);
+          dev = fmaxf(dev, fmaxf(fabsf(e0), fabsf(e1)));
+          t[e] = __float_as_uint(t0);
+          t[e + 1] = __float_as_uint(t1);
         }
       };
       if (clamp) round8(std::true_type{});
