@@ -279,8 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  const uint32_t tS[2] = {tmem, tmem + 128};
-  const uint32_t tO[2] = {tmem + 256, tmem + 384};
+  // TMEM columns of score buffer b and O accumulator b (arithmetic, not a
+  // table: a runtime index into an array would put it in local memory)
+  auto tS = [tmem](int b) { return tmem + 128u * (uint32_t)b; };
+  auto tO = [tmem](int b) { return tmem + 256u + 128u * (uint32_t)b; };
 
   if (warp == kSoftmaxWarps) {
     // ---------------------------------------------------------- TMA producer
@@ -324,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          mma_ss(tS[b], sdesc(q_s + off, kHalf, 1024), sdesc(k_s + off, kHalf, 1024), idQK, kk > 0 ? 1u : 0u);
+          mma_ss(tS(b), sdesc(q_s + off, kHalf, 1024), sdesc(k_s + off, kHalf, 1024), idQK, kk > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[b]);
         return true;
@@ -339,8 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // P: 16 keys = 8 packed bf16x2 columns, high part at 16kk, low part at
           // 16kk + 8; V: 16 key rows = two 8-row swizzle atoms
           const uint64_t vd = sdesc(v_s + kk * 2048, kHalf, 1024);
-          mma_ts(tO[b], tS[b] + kk * 16, vd, idPV, (i >= 2 || kk > 0) ? 1u : 0u);
-          if (!F16P) mma_ts(tO[b], tS[b] + kk * 16 + 8, vd, idPV, 1u);
+          mma_ts(tO(b), tS(b) + kk * 16, vd, idPV, (i >= 2 || kk > 0) ? 1u : 0u);
+          if (!F16P) mma_ts(tO(b), tS(b) + kk * 16 + 8, vd, idPV, 1u);
         }
         mma_commit(&o_done[b]);
         mma_commit(&kv_empty[st]);
@@ -370,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (valid_row) sc_row *= ldexpf(p.qfac[row0 + row], f16_exponent(*p.kmax_bits));
     }
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t sS = tS[grp] + lane_off, sO = tO[grp] + lane_off;
+    const uint32_t sS = tS(grp) + lane_off, sO = tO(grp) + lane_off;
     // l is kept as two partial sums (even and odd keys) for the packed adds
     float m = -INFINITY, la = 0.f, lb = 0.f;
     bool alive = true;
@@ -389,17 +391,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!edge) {
         // four independent running maxima: a single chain of 64 dependent
         // max instructions would set the pace of this pass
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
         for (int c = 0; c < kBN / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(sS + c * 32, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            mx[(e / 2) & 3] = max3(mx[(e / 2) & 3], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+          for (int e = 0; e < 32; e += 8) {
+            mx0 = max3(mx0, __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+            mx1 = max3(mx1, __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+            mx2 = max3(mx2, __uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
+            mx3 = max3(mx3, __uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
+          }
         }
-        mj = max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+        mj = max3(mx0, mx1, fmaxf(mx2, mx3));
       } else {
 #pragma unroll
         for (int c = 0; c < kBN / 32; ++c) {
@@ -515,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lt = l0v * w0 + o1ml.y * w1;
       const bool have = alive && lt > 0.f;
       const long long orow = row0 + row;               // = (query head) * n_q + qi
-      const uint32_t o0a = tO[0] + lane_off, o1a = tO[1] + lane_off;
+      const uint32_t o0a = tO(0) + lane_off, o1a = tO(1) + lane_off;
       if (p.nsplit > 1) {
         // partial of this key range: normalised o and its lse2, folded later
         const size_t part = ((size_t)h * p.n_tiles + tile) * p.nsplit + split;

@@ -12,6 +12,7 @@ and use inputs larger than L2 where the kernel streams HBM.
   decode_int2     the same pages demoted to INT2
   decode_int1     the same pages demoted to INT1
   decode_sparse   one layer of the sparse workload: decode over the indexer's selection
+  decode_host     the same decode with the FP8 pool in page-locked host memory (1024 pages per row)
   quantize_fp8    demote 128 Ki 16x128 BF16 units to FP8 (512 MB read)
   quantize_int8   the same to INT8
   quantize_int4   the same to INT4
@@ -19,6 +20,7 @@ and use inputs larger than L2 where the kernel streams HBM.
   quantize_int1   the same to INT1
   select          indexer scores + top-k for one layer of the sparse workload
   prefill         one 131072-token window of the windowed prefill
+  prefill_paged   one 32768-token window of FP8 pages staged through the block table
   fold            fold a 16 x 1024 x 128 fp32 partial into an accumulator
 """
 
@@ -116,6 +118,39 @@ def _decode_sparse(dev):
     return lambda: argus.paged_decode_attn(a, ws)
 
 
+def _decode_host(dev):
+    """The sparse case with its FP8 pool in page-locked host memory: decode reads
+    the selected pages in place over the host link."""
+    B, Hq, Hkv, D, P, NP, K = 8, 32, 4, 128, 64, 1024, 32
+    width = 2 * K + 8
+    g = argus.geom(Hq, Hkv, D, P)
+    ids = torch.arange(NP, dtype=torch.int32, device=dev)
+    pool = argus.Pool.empty(W.FP8_E4M3, B * NP, Hkv, P, D, device=dev)
+    ck = torch.empty((B, NP, Hkv, D), dtype=torch.bfloat16, device=dev)
+    for b in range(B):
+        src = W.normal((NP, 2, Hkv, P, D), W.BF16, W.seed_of("sparse", 0, 1) * 16 + b, device=dev)
+        argus.quantize_pages(g, W.BF16, src, NP, ids, pool, ids + b * NP, NP, ckey_out=ck[b])
+        del src
+    q = W.normal((B, Hq, D), W.BF16, W.seed_of("sparse", 0, 0), device=dev)
+    npg = torch.full((B,), NP, dtype=torch.int32, device=dev)
+    sel = torch.empty((B, Hkv, width), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B, Hkv), dtype=torch.int32, device=dev)
+    sws = torch.empty(argus.select_workspace_bytes(g, B, NP), dtype=torch.uint8, device=dev)
+    argus.select_pages(g, B, q, ck, npg, NP, K, True, sel, cnt, width, None, sws)
+    torch.cuda.synchronize()
+    host = pool.to_host()
+    del pool
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    a = argus.decode_args(g, B, q, [host], torch.full((B, NP), W.FP8_E4M3, dtype=torch.uint8, device=dev),
+                          torch.arange(B * NP, dtype=torch.int32, device=dev).reshape(B, NP),
+                          torch.full((B,), NP * P, dtype=torch.int32, device=dev), NP, W.softmax_scale(D), out=out,
+                          sel_pages=sel, sel_count=cnt, sel_width=width)
+    ws = torch.empty(max(1, argus.decode_workspace_bytes(a)), dtype=torch.uint8, device=dev)
+    fn = lambda: argus.paged_decode_attn(a, ws)
+    fn.keep = (host, a, ws, out)
+    return fn
+
+
 def _select(dev):
     B, Hq, Hkv, D, NP, K = 8, 32, 4, 128, 4096, 32
     g = argus.geom(Hq, Hkv, D, 64)
@@ -142,6 +177,27 @@ def _prefill(dev):
                                              acc_l, 1, ws=ws)
 
 
+def _prefill_paged(dev):
+    """One 32768-token window of FP8 e4m3 pages (64-token pages, random slots)
+    staged through the block table and attended by a 1024-query chunk."""
+    Hq, Hkv, D, P, NQ, WIN = 16, 2, 128, 64, 1024, 32768
+    n_pages = WIN // P
+    g = argus.geom(Hq, Hkv, D, P)
+    src = W.normal((n_pages, 2, Hkv, P, D), W.BF16, W.seed_of("prefill", 0, 1), device=dev)
+    slots = torch.from_numpy(W.permutation(n_pages, W.seed_of("prefill", 0, 4)).astype(np.int32)).to(dev)
+    pool = argus.Pool.empty(W.FP8_E4M3, n_pages, Hkv, P, D, device=dev)
+    argus.quantize_pages(g, W.BF16, src, n_pages, torch.arange(n_pages, dtype=torch.int32, device=dev), pool,
+                         slots, n_pages)
+    del src
+    q = W.normal((Hq, NQ, D), W.BF16, W.seed_of("prefill", 0, 0), device=dev)
+    codec = torch.full((n_pages,), W.FP8_E4M3, dtype=torch.uint8, device=dev)
+    acc_o = torch.zeros((Hq, NQ, D), dtype=torch.float32, device=dev)
+    acc_l = torch.full((Hq, NQ), float("-inf"), device=dev)
+    ws = torch.empty(argus.paged_window_prefill_workspace_bytes(g, NQ, WIN), dtype=torch.uint8, device=dev)
+    return lambda: argus.paged_window_prefill_attn(g, NQ, q, [pool], codec, slots, n_pages, 0, WIN, 1 << 20,
+                                                   W.softmax_scale(D), acc_o, acc_l, 1, ws)
+
+
 def _fold(dev):
     n, D = 16 * 1024, 128
     ao = torch.randn((n, D), device=dev)
@@ -158,6 +214,7 @@ CASES = {
     "decode_int2": lambda d: _decode_batched(d, W.INT2_G32),
     "decode_int1": lambda d: _decode_batched(d, W.INT1_G32),
     "decode_sparse": _decode_sparse,
+    "decode_host": _decode_host,
     "quantize_fp8": lambda d: _quantize(d, W.FP8_E4M3),
     "quantize_int8": lambda d: _quantize(d, W.INT8),
     "quantize_int4": lambda d: _quantize(d, W.INT4_G32),
@@ -165,6 +222,7 @@ CASES = {
     "quantize_int1": lambda d: _quantize(d, W.INT1_G32),
     "select": _select,
     "prefill": _prefill,
+    "prefill_paged": _prefill_paged,
     "fold": _fold,
 }
 
