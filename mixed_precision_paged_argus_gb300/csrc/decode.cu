@@ -49,11 +49,16 @@ constexpr int chunks_per_stage() { return NARROW ? 16 : kChunksPerStage; }
 // (two CTAs per SM; a second chunk in flight per warp hides MMA latency);
 // head_dim 128 runs 8 warps, of one chunk (16-bit layout: the ring fills
 // shared memory) or two chunks (narrow layout) per stage.
+// Producer warps: a warp issues its bulk copies one after another (about 60
+// cycles each, whatever their size), so the narrow ring -- 16 chunks and up
+// to 64 copies per stage -- has two producers taking alternate batches of two
+// stages; 12 warps still fit the register file at the consumers' count.
 template <int D, bool NARROW = false>
 struct Warps {
   static constexpr int kConsumer = (D == 64) ? 4 : 8;
   static constexpr int kNC = chunks_per_stage<NARROW>() / kConsumer;  // chunks per warp and stage
-  static constexpr int kThreads = 32 * (kConsumer + 1);
+  static constexpr int kProducers = NARROW ? 2 : 1;
+  static constexpr int kThreads = 32 * (kConsumer + kProducers);
 };
 constexpr int kMaxG = 8;
 constexpr int kNumCodecs = ARGUS_INT1_G32 + 1;
@@ -627,7 +632,11 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
   ChunkDesc* descs = reinterpret_cast<ChunkDesc*>(smem + L::kDescOff);
   int* misc = reinterpret_cast<int*>(smem + L::kMiscOff);
   volatile int* abort_flag = misc;
-  uint64_t* drained = reinterpret_cast<uint64_t*>(misc + 2);
+  uint64_t* drained = reinterpret_cast<uint64_t*>(misc + 2);   // the issued copies have landed (after a timeout)
+  uint64_t* pdone = reinterpret_cast<uint64_t*>(misc + 4);     // every producer has stopped issuing
+  volatile int* slot_stage = misc + 6;                          // [kStages] last stage issued into each slot
+  int* cons_done = misc + 9;                                    // consumer warps past their stage loop
+  constexpr int kProducers = Warps<D, NARROW>::kProducers;
 
   // Programmatic dependent launch: the next kernel on the stream may start its
   // prologue (block-table walk and K/V prefetch) while this grid finishes; every
@@ -655,8 +664,8 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
   const size_t sel_row = ((size_t)b * Hkv + h) * (size_t)p.sel_width;
   int pf_page = -1, pf_codec = -1;
   long long pf_slot = -1;
-  if (warp == kConsumerWarps) {
-    const int v = (split * p.cps + lane) / cpp;
+  if (warp >= kConsumerWarps) {
+    const int v = (split * p.cps + (warp - kConsumerWarps) * 32 + lane) / cpp;
     if (sparse) {
       pf_page = (v < p.sel_width) ? p.sel_pages[sel_row + v] : -1;
     } else {
@@ -708,24 +717,33 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
       mbar_init(&empty[s], kConsumerWarps);
     }
     misc[0] = 0;  // timeout flag
-    mbar_init(drained, 1);  // the producer's copies have all landed (after a timeout)
+    mbar_init(drained, 1);
+    mbar_init(pdone, kProducers);
+    for (int s = 0; s < L::kStages; ++s) slot_stage[s] = -1;
+    *cons_done = 0;
     fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == kConsumerWarps) {
-    // ------------------------------------------------------------ producer
-    // Chunks are translated 32 at a time, one per lane.  Lookups run one batch
-    // ahead of the copies: while a batch's stages are issued, the next batch's
-    // codec and slot loads and the selection entries of the batch after that
-    // are in flight.  The first batch's lookups were issued before the
-    // sequence length was known.
+  if (warp >= kConsumerWarps) {
+    // ------------------------------------------------------------ producers
+    // Chunks are translated 32 at a time, one per lane; producer pw takes the
+    // batches pw, pw + kProducers, ...  Lookups run one batch ahead of the
+    // copies: while a batch's stages are issued, the warp's next batch's codec
+    // and slot loads and the selection entries of the batch after that are in
+    // flight.  The first batch's lookups were issued before the sequence
+    // length was known.  (A producer's consecutive stages are never more than
+    // kStages apart, so its parity waits on a slot are at most one phase ahead.)
+    const int pw = warp - kConsumerWarps;
+    constexpr int kStride = 32 * kProducers;
+    static_assert(kProducers == 1 || 32 / kChunksPerStage * (kProducers - 1) + 1 <= L::kStages,
+                  "a producer's consecutive stages must stay within the ring");
     int cur_page = pf_page, cur_codec = pf_codec;
     long long cur_slot = pf_slot;
     if (sparse) {
       lookup(cur_page, cur_codec, cur_slot);
     } else if (EXT) {   // the speculative lookup assumed the unwindowed list
-      cur_page = cl.chunk(c_begin + lane) / cpp;
+      cur_page = cl.chunk(c_begin + pw * 32 + lane) / cpp;
       lookup(cur_page, cur_codec, cur_slot);
     }
     auto page_at = [&](int base) -> int {
@@ -734,14 +752,14 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
       const int v = (c_begin + base + lane) / cpp;
       return (v < p.sel_width) ? p.sel_pages[sel_row + v] : -1;
     };
-    int nxt_page = page_at(32);
+    int nxt_page = page_at(pw * 32 + kStride);
     bool stop = false;
-    int withheld = -1, last_issued = -1;  // stages (warp-uniform)
-    for (int base = 0; base < n_local && !stop; base += 32) {
+    int withheld = -1;  // stage (warp-uniform)
+    for (int base = pw * 32; base < n_local && !stop; base += kStride) {
       int nxt_codec = -1;
       long long nxt_slot = -1;
-      if (base + 32 < n_local) lookup(nxt_page, nxt_codec, nxt_slot);
-      const int nn_page = page_at(base + 64);
+      if (base + kStride < n_local) lookup(nxt_page, nxt_codec, nxt_slot);
+      const int nn_page = page_at(base + 2 * kStride);
 
       ChunkDesc d;
       d.codec = -1;
@@ -850,20 +868,22 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
           descs[slot * kChunksPerStage + j] = d;
         }
         __syncwarp();
+        if (lane == 0) slot_stage[slot] = s;
         if (s == p.stall_stage) withheld = s;
         else if (lane == 0) mbar_arrive(&full[slot]);
-        last_issued = s;
       }
       cur_page = nxt_page;
       cur_codec = nxt_codec;
       cur_slot = nxt_slot;
       nxt_page = nn_page;
     }
-    if (!stop && withheld < 0) return;
-    // Wind-down after a timeout.  Bulk copies may still be landing in the
-    // ring, which the consumers reuse for their merge: complete the withheld
-    // arrival (once the consumers have given up on that stage), wait until
-    // the stages issued last have received all their bytes, then release the
+    // Wind-down.  After a timeout bulk copies may still be landing in the
+    // ring, which the consumers reuse for their merge.  A producer that
+    // withheld an arrival completes it once the consumers have given up on
+    // that stage; every producer then reports that it stopped issuing.
+    // Producer 0 stays until the consumers are past their stage loops or a
+    // timeout was raised; in the latter case it waits until the last stage
+    // issued into each slot has received all its bytes, then releases the
     // consumers through `drained`.  Every wait here is bounded as well.
     if (withheld >= 0) {
       const unsigned long long t0 = global_ns();
@@ -872,8 +892,26 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
       while (!*abort_flag && global_ns() - t0 <= 2 * p.wait_ns) __nanosleep(1000);
       if (lane == 0) mbar_arrive(&full[withheld % L::kStages]);
     }
-    for (int s = max(0, last_issued - L::kStages + 1); s <= last_issued; ++s)
-      mbar_wait(&full[s % L::kStages], (s / L::kStages) & 1, nullptr, p.wait_ns);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(pdone);
+    if (pw != 0) return;
+    {
+      const unsigned long long t0 = global_ns();
+      while (!*abort_flag && global_ns() - t0 <= kWaitLimitNs) {
+        if (*reinterpret_cast<volatile int*>(cons_done) >= kConsumerWarps) {
+          __threadfence_block();   // a consumer's flag precedes its count
+          break;
+        }
+        __nanosleep(500);
+      }
+    }
+    if (*abort_flag) {
+      mbar_wait(pdone, 0, nullptr, 3 * p.wait_ns);
+      for (int sl = 0; sl < L::kStages; ++sl) {
+        const int x = slot_stage[sl];
+        if (x >= 0) mbar_wait(&full[sl], (x / L::kStages) & 1, nullptr, 3 * p.wait_ns);
+      }
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(drained);
     return;
@@ -1199,10 +1237,14 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
     l1 += __shfl_xor_sync(0xffffffffu, l1, o);
   }
   if (sigma == 0.f) sigma = 1.f;  // nothing accumulated
+  if (lane == 0) {
+    __threadfence_block();   // this warp's abort flag, if any, before its count
+    atomicAdd(cons_done, 1);
+  }
   // After a timeout the ring may still be receiving copies: wait (bounded)
-  // until the producer reports them landed.  Every warp sees the flag here:
+  // until the producers report them landed.  Every warp sees the flag here:
   // no warp completes all its stages once another has given up.
-  if (*abort_flag) mbar_wait(drained, 0, nullptr, p.wait_ns);
+  if (*abort_flag) mbar_wait(drained, 0, nullptr, 4 * p.wait_ns);
   consumer_bar<kConsumerWarps>();  // every warp is done with the stage ring; reuse it
   float* red_o = reinterpret_cast<float*>(smem);               // [warps][8][D]
   float* red_ml = red_o + kConsumerWarps * kMaxG * D;          // [warps][8][2]

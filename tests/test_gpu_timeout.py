@@ -33,13 +33,20 @@ def _check_against_oracle(c, out32, lse, window=0, sinks=0):
     assert np.all(np.abs(gl[fin] - ref_lse[fin]) <= 1e-4 * np.maximum(1.0, np.abs(ref_lse[fin])))
 
 
-@pytest.mark.parametrize("D,q_dtype,window,stall", [
-    (128, W.FP16, 0, 0),    # wide ring, the stall in the first stage
-    (128, W.BF16, 0, 1),
-    (64, W.FP16, 0, 0),
-    (128, W.FP16, 96, 0),   # the extended kernel (sliding window)
+WIDE = (W.FP16, W.FP8_E4M3, W.INT8, W.INT4_G32)
+NARROW = (W.FP8_E4M3, W.INT8, W.INT4_G32)          # no 16-bit pool: the narrow ring, two producer warps
+
+
+@pytest.mark.parametrize("D,q_dtype,window,stall,tiers", [
+    (128, W.FP16, 0, 0, WIDE),    # wide ring, the stall in the first stage
+    (128, W.BF16, 0, 1, WIDE),
+    (64, W.FP16, 0, 0, WIDE),
+    (128, W.FP16, 96, 0, WIDE),   # the extended kernel (sliding window)
+    (128, W.BF16, 0, 0, NARROW),  # narrow ring: the first producer withholds
+    (128, W.FP16, 0, 2, NARROW),  # narrow ring: the second producer's first stage
+    (128, W.BF16, 0, 3, NARROW + (W.INT2_G32, W.INT1_G32)),   # extended narrow kernel
 ])
-def test_stalled_stage_times_out_and_the_context_stays_usable(D, q_dtype, window, stall):
+def test_stalled_stage_times_out_and_the_context_stays_usable(D, q_dtype, window, stall, tiers):
     Hq, Hkv, P = 8, 2, 16
     # long rows (many stages: the producer meets the abort at its empty wait)
     # and short rows (one stage: the producer has issued everything when the
@@ -47,7 +54,7 @@ def test_stalled_stage_times_out_and_the_context_stays_usable(D, q_dtype, window
     lens = [1024, 16, 40, 0]
     max_pages = 64
     rng = np.random.default_rng(3)
-    pc = rng.choice([W.FP16, W.FP8_E4M3, W.INT8, W.INT4_G32], size=(len(lens), max_pages))
+    pc = rng.choice(list(tiers), size=(len(lens), max_pages))
     if q_dtype == W.BF16:
         pc[pc == W.FP16] = W.BF16
     c = build_case(Hq, Hkv, D, P, lens, pc, q_dtype, seed=41)
