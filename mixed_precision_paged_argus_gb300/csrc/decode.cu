@@ -57,7 +57,8 @@ template <int D, bool NARROW = false>
 struct Warps {
   static constexpr int kConsumer = (D == 64) ? 4 : 8;
   static constexpr int kNC = chunks_per_stage<NARROW>() / kConsumer;  // chunks per warp and stage
-  static constexpr int kProducers = NARROW ? 2 : 1;
+  static constexpr int kProducers = NARROW ? 3 : 1;
+  static constexpr int kBatch = NARROW ? 16 : 32;   // chunks a producer translates per round trip
   static constexpr int kThreads = 32 * (kConsumer + kProducers);
 };
 constexpr int kMaxG = 8;
@@ -665,7 +666,7 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
   int pf_page = -1, pf_codec = -1;
   long long pf_slot = -1;
   if (warp >= kConsumerWarps) {
-    const int v = (split * p.cps + (warp - kConsumerWarps) * 32 + lane) / cpp;
+    const int v = (split * p.cps + (warp - kConsumerWarps) * Warps<D, NARROW>::kBatch + lane) / cpp;
     if (sparse) {
       pf_page = (v < p.sel_width) ? p.sel_pages[sel_row + v] : -1;
     } else {
@@ -735,15 +736,16 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
     // length was known.  (A producer's consecutive stages are never more than
     // kStages apart, so its parity waits on a slot are at most one phase ahead.)
     const int pw = warp - kConsumerWarps;
-    constexpr int kStride = 32 * kProducers;
-    static_assert(kProducers == 1 || 32 / kChunksPerStage * (kProducers - 1) + 1 <= L::kStages,
+    constexpr int kBatch = Warps<D, NARROW>::kBatch;
+    constexpr int kStride = kBatch * kProducers;
+    static_assert(kProducers == 1 || kBatch / kChunksPerStage * (kProducers - 1) + 1 <= L::kStages,
                   "a producer's consecutive stages must stay within the ring");
     int cur_page = pf_page, cur_codec = pf_codec;
     long long cur_slot = pf_slot;
     if (sparse) {
       lookup(cur_page, cur_codec, cur_slot);
     } else if (EXT) {   // the speculative lookup assumed the unwindowed list
-      cur_page = cl.chunk(c_begin + pw * 32 + lane) / cpp;
+      cur_page = cl.chunk(c_begin + pw * kBatch + lane) / cpp;
       lookup(cur_page, cur_codec, cur_slot);
     }
     auto page_at = [&](int base) -> int {
@@ -752,10 +754,10 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
       const int v = (c_begin + base + lane) / cpp;
       return (v < p.sel_width) ? p.sel_pages[sel_row + v] : -1;
     };
-    int nxt_page = page_at(pw * 32 + kStride);
+    int nxt_page = page_at(pw * kBatch + kStride);
     bool stop = false;
     int withheld = -1;  // stage (warp-uniform)
-    for (int base = pw * 32; base < n_local && !stop; base += kStride) {
+    for (int base = pw * kBatch; base < n_local && !stop; base += kStride) {
       int nxt_codec = -1;
       long long nxt_slot = -1;
       if (base + kStride < n_local) lookup(nxt_page, nxt_codec, nxt_slot);
@@ -769,7 +771,7 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
       d.hk = d.hv = d.hmk = d.hmv = nullptr;
       uint32_t kv_bytes = 0, m_bytes = 0;
       const uint8_t *srcK = nullptr, *srcV = nullptr, *srcMK = nullptr, *srcMV = nullptr;
-      if (base + lane < n_local) {
+      if (lane < kBatch && base + lane < n_local) {
         const int ci = (EXT && !sparse) ? cl.chunk(c_begin + base + lane) : c_begin + base + lane;
         const int cip = ci - (ci / cpp) * cpp;
         // anomalies are counted once per page: at its first listed chunk
@@ -828,7 +830,7 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
         }
       }
       const uint32_t my_bytes = 2 * (kv_bytes + m_bytes);
-      const int n_batch_stages = min(32 / kChunksPerStage, (n_local - base + kChunksPerStage - 1) / kChunksPerStage);
+      const int n_batch_stages = min(kBatch / kChunksPerStage, (n_local - base + kChunksPerStage - 1) / kChunksPerStage);
       for (int st = 0; st < n_batch_stages; ++st) {
         const int s = base / kChunksPerStage + st;
         const int slot = s % L::kStages;
