@@ -517,8 +517,10 @@ def leg_sparse(dev, timer, steps, warm, hbm):
     drops = torch.zeros(1, dtype=torch.int32, device=dev)
     sws = torch.empty(argus.select_workspace_bytes(g, B, NP), dtype=torch.uint8, device=dev)
     outs = [torch.empty((B, Hq, D_), dtype=torch.bfloat16, device=dev) for _ in range(L_)]
+    # pdl=2: each decode grid starts during the select's tail and reads the
+    # selection after it completes
     args = [argus.decode_args(g, B, qs[l], [pools[l]], codec, table, lens, NP, W.softmax_scale(D_), out=outs[l],
-                              sel_pages=sel, sel_count=cnt, sel_width=width) for l in range(L_)]
+                              sel_pages=sel, sel_count=cnt, sel_width=width, pdl=2) for l in range(L_)]
     dws = torch.empty(max(argus.decode_workspace_bytes(a) for a in args), dtype=torch.uint8, device=dev)
 
     def step(select=True, decode=True):
@@ -583,7 +585,7 @@ def leg_sparse_host(dev, timer, steps, warm, hbm):
     sws = torch.empty(argus.select_workspace_bytes(g, B, NP), dtype=torch.uint8, device=dev)
     out = torch.empty((B, Hq, D_), dtype=torch.bfloat16, device=dev)
     a = argus.decode_args(g, B, q, [host], codec, table, lens, NP, W.softmax_scale(D_), out=out, sel_pages=sel,
-                          sel_count=cnt, sel_width=width)
+                          sel_count=cnt, sel_width=width, pdl=2)
     dws = torch.zeros(max(16, argus.decode_workspace_bytes(a)), dtype=torch.uint8, device=dev)
 
     def select():

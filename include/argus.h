@@ -215,7 +215,12 @@ typedef struct {
  * sel_count, the pools' codes and meta BEFORE it waits for that predecessor
  * (q is read, and every output written, after the wait).  Set it only when
  * the predecessor does not write those inputs -- for example a previous
- * argus_paged_decode_attn call, layer after layer.  When in doubt, 0. */
+ * argus_paged_decode_attn call, layer after layer.  When in doubt, 0.
+ * args.pdl = 2: the decode grid may start while its stream predecessor is
+ * still running but reads every input after that predecessor completes: always
+ * safe, and it hides the launch behind the predecessor's tail (for example
+ * after argus_select_pages, which writes sel_pages and sel_count).
+ * Other values are ARGUS_E_INVALID. */
 
 /* Workspace needed by argus_paged_decode_attn for these arguments: fp32
  * partial outputs and log2-sum-exp values of the context splits.  Its contents
@@ -274,6 +279,8 @@ argus_status argus_paged_decode_attn_noalloc(const argus_decode_args* args, void
  * [B][max_pages][Hkv][D] in logical page order (q and ckeys 16-byte aligned); n_pages device int32 [B]
  * (values above max_pages are clamped and counted as drops); ws of
  * argus_select_workspace_bytes bytes.  max_pages is at most 65535.
+ * The kernels may start while their stream predecessor is still running
+ * (programmatic dependent launch); every input is read after it completes.
  * ------------------------------------------------------------------------- */
 argus_status argus_select_workspace_bytes(const argus_geom* g, int32_t batch,
                                           int32_t max_pages, size_t* bytes);

@@ -222,7 +222,7 @@ def decode_args(g, batch, q, pools, page_codec, block_table, seq_lens, max_pages
     a.lse2_out = _ptr(lse2_out)
     a.status = _ptr(status)
     a.num_splits = int(num_splits)
-    a.pdl = 1 if pdl else 0
+    a.pdl = int(pdl)   # False / True / 2
     a.window_tokens = int(window_tokens)
     a.sink_tokens = int(sink_tokens)
     # the struct holds raw pointers: keep every tensor it points to alive with it

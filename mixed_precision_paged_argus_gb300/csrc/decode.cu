@@ -89,7 +89,8 @@ struct Params {
   uint32_t* status;
   int cps;         // chunks per split, a multiple of kChunksPerStage
   int num_splits;  // grid.x
-  int pdl;         // launch the decode grid with programmatic stream serialisation
+  int pdl;         // 0: stream order; 1: early start, inputs read before the wait;
+                   // 2: early start, every input read after the wait
   int window;      // > 0: only the newest `window` tokens and the first `sinks` are visible
   int sinks;
   float* part_o;   // [B][Hkv][num_splits][G][D]
@@ -644,6 +645,7 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
   // read of data a predecessor may write (q) and every global write below
   // happens after griddepcontrol.wait.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (p.pdl == 2) asm volatile("griddepcontrol.wait;" ::: "memory");   // nothing is read before it
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hkv = p.Hkv, G = p.G, P = p.P;
@@ -1443,6 +1445,7 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
     return fail(ARGUS_E_INVALID, "decode: n_q_heads %% n_kv_heads != 0");
   const int G = g.n_q_heads / g.n_kv_heads;
   if (G > kMaxG) return fail(ARGUS_E_UNSUPPORTED, "decode: G = %d > 8 query heads per KV head", G);
+  if (a->pdl < 0 || a->pdl > 2) return fail(ARGUS_E_INVALID, "decode: pdl must be 0, 1 or 2");
   if (g.head_dim != 64 && g.head_dim != 128)
     return fail(ARGUS_E_UNSUPPORTED, "decode: head_dim %d (supported: 64, 128)", g.head_dim);
   if (g.page_tokens % kChunk != 0)
@@ -1666,7 +1669,7 @@ static argus_status run(const argus_decode_args* a, const Plan& pl, void* ws, vo
   p.status = a->status;
   p.cps = pl.cps;
   p.num_splits = pl.num_splits;
-  p.pdl = a->pdl ? 1 : 0;
+  p.pdl = a->pdl;
   // at most 2^30 tokens are ever visible (max_pages * page_tokens <= 2^30):
   // larger values mean the same and keep the device arithmetic in range
   p.window = std::min(a->window_tokens, 1 << 30);

@@ -144,6 +144,9 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) score_kernel(i
                                                               uint32_t* __restrict__ emit) {
   // the top-k grid may start its prologue now; it waits for this grid's keys
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // this grid itself may start during its stream predecessor's tail: every
+  // input is read after that predecessor completes
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // shared memory: the range's compressed keys [ppc * Hkv][D] bf16, the
   // G-query sums [Hkv][D] fp32, the range's order keys [ppc][Hkv], mbarriers
   extern __shared__ __align__(128) uint8_t sm_raw[];
@@ -659,12 +662,29 @@ extern "C" argus_status argus_select_pages(const argus_geom* g, int32_t batch, c
   const uint16_t* ck = static_cast<const uint16_t*>(ckeys);
   const bool bf = (q_dtype == ARGUS_BF16);
   const int kn = keep_newest ? 1 : 0;
-  if (g->head_dim == 64) {
-    if (bf) select::score_kernel<64, true><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, (int)ppc, q, ck, n_pages, keys, kn, emit_arg);
-    else select::score_kernel<64, false><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, (int)ppc, q, ck, n_pages, keys, kn, emit_arg);
-  } else {
-    if (bf) select::score_kernel<128, true><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, (int)ppc, q, ck, n_pages, keys, kn, emit_arg);
-    else select::score_kernel<128, false><<<grid1, select::kScoreThreads, sh, s>>>(g->n_kv_heads, G, max_pages, (int)ppc, q, ck, n_pages, keys, kn, emit_arg);
+  {
+    // programmatic dependent launch: the score grid starts during its stream
+    // predecessor's tail and waits for it before reading anything
+    cudaLaunchConfig_t sc = {};
+    sc.gridDim = grid1;
+    sc.blockDim = dim3(select::kScoreThreads);
+    sc.dynamicSmemBytes = sh;
+    sc.stream = s;
+    cudaLaunchAttribute sattr[1];
+    sattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    sattr[0].val.programmaticStreamSerializationAllowed = 1;
+    sc.attrs = sattr;
+    sc.numAttrs = 1;
+    const int Hkv_i = g->n_kv_heads, mp = max_pages, ppc_i = (int)ppc;
+    cudaError_t se;
+    if (g->head_dim == 64) {
+      se = bf ? cudaLaunchKernelEx(&sc, select::score_kernel<64, true>, Hkv_i, G, mp, ppc_i, q, ck, n_pages, keys, kn, emit_arg)
+              : cudaLaunchKernelEx(&sc, select::score_kernel<64, false>, Hkv_i, G, mp, ppc_i, q, ck, n_pages, keys, kn, emit_arg);
+    } else {
+      se = bf ? cudaLaunchKernelEx(&sc, select::score_kernel<128, true>, Hkv_i, G, mp, ppc_i, q, ck, n_pages, keys, kn, emit_arg)
+              : cudaLaunchKernelEx(&sc, select::score_kernel<128, false>, Hkv_i, G, mp, ppc_i, q, ck, n_pages, keys, kn, emit_arg);
+    }
+    if (se != cudaSuccess) return fail(ARGUS_E_LAUNCH, "argus_select_pages (score): %s", cudaGetErrorString(se));
   }
   argus_status st = launch_status("argus_select_pages (score)");
   if (st != ARGUS_OK) return st;

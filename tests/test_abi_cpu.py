@@ -63,6 +63,11 @@ def test_host_validation_without_gpu():
     assert L.argus_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 2
     a.g = argus.geom(8, 2, 128, 24)
     assert L.argus_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 2
+    a.g = argus.geom(8, 2, 128, 16)
+    a.pdl = 3   # 0, 1 or 2
+    assert L.argus_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 1
+    a.pdl = 2
+    assert L.argus_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 0
     g = argus.geom(8, 2, 128, 16)
     assert L.argus_select_workspace_bytes(ctypes.byref(g), 2, 10, ctypes.byref(n)) == 0
     assert n.value == 2 * 2 * 10 * 4 + 2 * 2 * 2 * 4 * 4   # keys, then 4 reported keys of ceil(10 / 8) ranges

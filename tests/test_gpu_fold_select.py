@@ -159,3 +159,66 @@ def test_select_many_ties_and_long_rows(max_pages, n_pages):
         osel, ocnt, odrops = oracle.select_pages(q64, ck, n_pages, Hkv, top_k, True, 2 * top_k + 8)
         assert np.array_equal(cnt, ocnt) and drops == odrops
         assert np.array_equal(sel[:, :, :cnt.max()], osel[:, :, :cnt.max()])
+
+
+def test_select_then_decode_with_early_start():
+    """argus_select_pages (its score grid starts in its predecessor's tail and
+    waits for it) followed by decode with pdl=2 (starts early, reads the
+    selection after the select completes), layer after layer, eagerly and from
+    a CUDA graph: the same bits as stream order, and the oracle's result over
+    the selected pages."""
+    from paged_cases import build_case, tol
+    Hq, Hkv, D, P, NP, B = 16, 2, 128, 16, 96, 2
+    K, width = 8, 24
+    pc = np.full((B, NP), W.FP8_E4M3)
+    c = build_case(Hq, Hkv, D, P, [NP * P, NP * P - 9], pc, W.BF16, q_dtype=W.BF16, seed=900)
+    g = argus.geom(Hq, Hkv, D, P)
+    layers = 3
+    cks = [W.normal((B, NP, Hkv, D), W.BF16, 910 + l).to(DEV) for l in range(layers)]
+    npg = torch.tensor([NP, NP], dtype=torch.int32, device=DEV)
+    sws = torch.empty(argus.select_workspace_bytes(g, B, NP), dtype=torch.uint8, device=DEV)
+
+    def chain(pdl):
+        sels = [torch.full((B, Hkv, width), -7, dtype=torch.int32, device=DEV) for _ in range(layers)]
+        cnts = [torch.zeros((B, Hkv), dtype=torch.int32, device=DEV) for _ in range(layers)]
+        outs = [torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device=DEV) for _ in range(layers)]
+        lses = [torch.full((B, Hq), float("nan"), dtype=torch.float32, device=DEV) for _ in range(layers)]
+        args = [argus.decode_args(c.g, c.B, c.q, c.pools, c.d_codec, c.d_table, c.d_lens, c.max_pages, c.scale,
+                                  out_f32=outs[l], lse2_out=lses[l], sel_pages=sels[l], sel_count=cnts[l],
+                                  sel_width=width, pdl=pdl) for l in range(layers)]
+        ws = torch.empty(max(argus.decode_workspace_bytes(a) for a in args), dtype=torch.uint8, device=DEV)
+
+        def step(stream):
+            for l in range(layers):
+                argus.select_pages(g, B, c.q, cks[l], npg, NP, K, True, sels[l], cnts[l], width, None, sws,
+                                   stream=stream)
+                argus.paged_decode_attn(args[l], ws, stream=stream)
+        return sels, cnts, outs, lses, step
+
+    ref = chain(0)
+    stream = torch.cuda.Stream(device=DEV)
+    with torch.cuda.stream(stream):
+        ref[4](stream)
+    torch.cuda.synchronize()
+    got = chain(2)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            got[4](stream)
+        stream.synchronize()
+        for l in range(layers):
+            for x, y in zip(got[:4], ref[:4]):
+                assert torch.equal(x[l], y[l]), l
+            got[2][l].fill_(float("nan"))
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            got[4](stream)
+        graph.replay()
+    torch.cuda.synchronize()
+    for l in range(layers):
+        assert torch.equal(got[2][l], ref[2][l])
+    # the oracle over the pages the first layer selected
+    sel0, cnt0 = ref[0][0].cpu().numpy(), ref[1][0].cpu().numpy()
+    o, lse, bad = oracle.paged_decode(c.q64, c.Hkv, c.P, c.opools, c.page_codec, c.table, c.lens, c.scale,
+                                      sel_pages=sel0, sel_count=cnt0, sel_width=width)
+    assert bad == 0
+    assert np.abs(ref[2][0].cpu().numpy() - o).max() <= tol(o)
