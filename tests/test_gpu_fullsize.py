@@ -143,7 +143,7 @@ def test_sparse_one_layer_full_size_sampled_sequence():
     assert np.all(diff <= np.abs(C.bf16_bits_to_f64(ock)) * 2.0 ** -7 + (P + 2) * 2.0 ** -24 * 8 + 1e-30)
     q64 = C.bf16_bits_to_f64(W.to_bits(q))[b:b + 1]
     osel, ocnt, _ = oracle.select_pages(q64, ock[None], [NP], Hkv, K, True, width)
-    # the selection is judged on the GPU's own compressed-key slab (the slab is
+    # the selection is checked on the GPU's own compressed-key slab (the slab is
     # select's input): every selected page scores within 1e-5 max|s| of the k-th
     scores = oracle.compressed_key_scores(q64, gck[None], [NP], Hkv)
     gsel = sel[b].cpu().numpy()
