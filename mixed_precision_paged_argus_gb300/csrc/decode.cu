@@ -491,13 +491,15 @@ __device__ __forceinline__ void group_scores(const uint8_t* const* cptr, const C
       for (int c = 0; c < NCG; ++c) mma_f16(sg[c][k / 2], a[c][k][0], a[c][k][1], a[c][k][2], a[c][k][3], qf[k][0], qf[k][1]);
 #pragma unroll
     for (int c = 0; c < NCG; ++c) {
+      // sum_g scale_g * acc_g + zero_g * qsum_g, the two heads of a row in
+      // packed f32x2 multiply-adds
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < D / 32; ++i) {
-        sc[0] += kz[c][0][i][0] * sg[c][i][0] + kz[c][0][i][1] * qgs[i][0];
-        sc[1] += kz[c][0][i][0] * sg[c][i][1] + kz[c][0][i][1] * qgs[i][1];
-        sc[2] += kz[c][1][i][0] * sg[c][i][2] + kz[c][1][i][1] * qgs[i][0];
-        sc[3] += kz[c][1][i][0] * sg[c][i][3] + kz[c][1][i][1] * qgs[i][1];
+        f2_fma(sc[0], sc[1], kz[c][0][i][0], kz[c][0][i][0], sg[c][i][0], sg[c][i][1], sc[0], sc[1]);
+        f2_fma(sc[0], sc[1], kz[c][0][i][1], kz[c][0][i][1], qgs[i][0], qgs[i][1], sc[0], sc[1]);
+        f2_fma(sc[2], sc[3], kz[c][1][i][0], kz[c][1][i][0], sg[c][i][2], sg[c][i][3], sc[2], sc[3]);
+        f2_fma(sc[2], sc[3], kz[c][1][i][1], kz[c][1][i][1], qgs[i][0], qgs[i][1], sc[2], sc[3]);
       }
       const float f0 = scale_log2 * f0h, f1 = scale_log2 * f1h;
       const uint32_t vk = dsc[c].vmask;
