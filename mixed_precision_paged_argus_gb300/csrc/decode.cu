@@ -636,10 +636,8 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
   ChunkDesc* descs = reinterpret_cast<ChunkDesc*>(smem + L::kDescOff);
   int* misc = reinterpret_cast<int*>(smem + L::kMiscOff);
   volatile int* abort_flag = misc;
-  uint64_t* drained = reinterpret_cast<uint64_t*>(misc + 2);   // the issued copies have landed (after a timeout)
   uint64_t* pdone = reinterpret_cast<uint64_t*>(misc + 4);     // every producer has stopped issuing
   volatile int* slot_stage = misc + 6;                          // [kStages] last stage issued into each slot
-  int* cons_done = misc + 9;                                    // consumer warps past their stage loop
   constexpr int kProducers = Warps<D, NARROW>::kProducers;
 
   // Programmatic dependent launch: the next kernel on the stream may start its
@@ -722,10 +720,8 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
       mbar_init(&empty[s], kConsumerWarps);
     }
     misc[0] = 0;  // timeout flag
-    mbar_init(drained, 1);
     mbar_init(pdone, kProducers);
     for (int s = 0; s < L::kStages; ++s) slot_stage[s] = -1;
-    *cons_done = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -883,14 +879,10 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
       cur_slot = nxt_slot;
       nxt_page = nn_page;
     }
-    // Wind-down.  After a timeout bulk copies may still be landing in the
-    // ring, which the consumers reuse for their merge.  A producer that
-    // withheld an arrival completes it once the consumers have given up on
-    // that stage; every producer then reports that it stopped issuing.
-    // Producer 0 stays until the consumers are past their stage loops or a
-    // timeout was raised; in the latter case it waits until the last stage
-    // issued into each slot has received all its bytes, then releases the
-    // consumers through `drained`.  Every wait here is bounded as well.
+    // Wind-down.  A producer that withheld an arrival completes it once the
+    // consumers have given up on that stage; every producer then reports
+    // that it stopped issuing (after a timeout the consumers drain the ring
+    // before reusing it).  Every wait here is bounded as well.
     if (withheld >= 0) {
       const unsigned long long t0 = global_ns();
       // the consumers start their wait on this stage within microseconds of
@@ -900,26 +892,6 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(pdone);
-    if (pw != 0) return;
-    {
-      const unsigned long long t0 = global_ns();
-      while (!*abort_flag && global_ns() - t0 <= kWaitLimitNs) {
-        if (*reinterpret_cast<volatile int*>(cons_done) >= kConsumerWarps) {
-          __threadfence_block();   // a consumer's flag precedes its count
-          break;
-        }
-        __nanosleep(500);
-      }
-    }
-    if (*abort_flag) {
-      mbar_wait(pdone, 0, nullptr, 3 * p.wait_ns);
-      for (int sl = 0; sl < L::kStages; ++sl) {
-        const int x = slot_stage[sl];
-        if (x >= 0) mbar_wait(&full[sl], (x / L::kStages) & 1, nullptr, 3 * p.wait_ns);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(drained);
     return;
   }
 
@@ -1243,14 +1215,17 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
     l1 += __shfl_xor_sync(0xffffffffu, l1, o);
   }
   if (sigma == 0.f) sigma = 1.f;  // nothing accumulated
-  if (lane == 0) {
-    __threadfence_block();   // this warp's abort flag, if any, before its count
-    atomicAdd(cons_done, 1);
+  // After a timeout the ring may still be receiving copies: once every
+  // producer has stopped issuing, wait (bounded) until the last stage issued
+  // into each slot has received all its bytes.  Every warp sees the flag
+  // here: no warp completes all its stages once another has given up.
+  if (*abort_flag) {
+    mbar_wait(pdone, 0, nullptr, 3 * p.wait_ns);
+    for (int sl = 0; sl < L::kStages; ++sl) {
+      const int x = slot_stage[sl];
+      if (x >= 0) mbar_wait(&full[sl], (x / L::kStages) & 1, nullptr, 3 * p.wait_ns);
+    }
   }
-  // After a timeout the ring may still be receiving copies: wait (bounded)
-  // until the producers report them landed.  Every warp sees the flag here:
-  // no warp completes all its stages once another has given up.
-  if (*abort_flag) mbar_wait(drained, 0, nullptr, 4 * p.wait_ns);
   consumer_bar<kConsumerWarps>();  // every warp is done with the stage ring; reuse it
   float* red_o = reinterpret_cast<float*>(smem);               // [warps][8][D]
   float* red_ml = red_o + kConsumerWarps * kMaxG * D;          // [warps][8][2]
