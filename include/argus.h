@@ -186,7 +186,10 @@ typedef struct {
   float* out_f32;             /* device [B][Hq][D] fp32 output (16-byte aligned), or NULL */
   float* lse2_out;            /* device [B][Hq] log2-sum-exp, or NULL */
   uint32_t* status;           /* device uint32 anomaly counter, or NULL */
-  int32_t num_splits;         /* context splits per (b, KV head); 0 = automatic */
+  int32_t num_splits;         /* context splits per (b, KV head); 0 = automatic.
+                                 Dense pages: contiguous chunk ranges.  A selection:
+                                 its entries dealt round-robin (split s takes entries
+                                 s, s + S, ...), at most sel_width splits */
   int32_t pdl;                /* programmatic dependent launch, see below */
   int32_t window_tokens;      /* > 0: sliding window, see below; 0 = every token */
   int32_t sink_tokens;        /* with a window: leading tokens that stay visible */

@@ -87,8 +87,8 @@ struct Params {
   float* out_f32;
   float* lse2_out;
   uint32_t* status;
-  int cps;         // chunks per split, a multiple of kChunksPerStage
-  int num_splits;  // grid.x
+  int cps;         // dense pages: chunks per split, a multiple of kChunksPerStage
+  int num_splits;  // grid.x (a selection's entries are dealt round-robin over the splits)
   int pdl;         // 0: stream order; 1: early start, inputs read before the wait;
                    // 2: early start, every input read after the wait
   int window;      // > 0: only the newest `window` tokens and the first `sinks` are visible
@@ -651,6 +651,11 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
   const int Hkv = p.Hkv, G = p.G, P = p.P;
   const int cpp = P / kChunk;
   const bool sparse = p.sel_pages != nullptr;
+  // A selection's entries are dealt round-robin: split s reads entries s,
+  // s + S, s + 2S, ... (S = num_splits), so the splits of a row get equal
+  // shares of whatever count the row has.  Dense pages: split s reads chunks
+  // [s cps, (s + 1) cps).  sel_entry: the entry of this CTA's local chunk i.
+  auto sel_entry = [&](int i) -> int { return (i / cpp) * p.num_splits + split; };
 
   // Codec and slot of logical page `page` (both -1 outside the table).
   auto lookup = [&](int page, int& codec, long long& slot) {
@@ -668,11 +673,12 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
   int pf_page = -1, pf_codec = -1;
   long long pf_slot = -1;
   if (warp >= kConsumerWarps) {
-    const int v = (split * p.cps + (warp - kConsumerWarps) * Warps<D, NARROW>::kBatch + lane) / cpp;
+    const int i0 = (warp - kConsumerWarps) * Warps<D, NARROW>::kBatch + lane;
     if (sparse) {
+      const int v = sel_entry(i0);
       pf_page = (v < p.sel_width) ? p.sel_pages[sel_row + v] : -1;
     } else {
-      pf_page = v;
+      pf_page = (split * p.cps + i0) / cpp;
       lookup(pf_page, pf_codec, pf_slot);
     }
   }
@@ -680,23 +686,23 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
   int seq_len = p.seq_lens[b];
   seq_len = max(0, min(seq_len, p.max_pages * P));
   const int n_pages_b = (seq_len + P - 1) / P;
-  int n_chunks;
   ChunkList cl{0, 0, 0};
+  const int c_begin = sparse ? 0 : split * p.cps;
+  int n_local, n_active;
   if (!sparse) {
     cl = dense_chunks(seq_len, EXT ? p.window : 0, EXT ? p.sinks : 0);
-    n_chunks = cl.n;
+    n_local = min(cl.n, c_begin + p.cps) - c_begin;
+    n_active = (cl.n + p.cps - 1) / p.cps;
   } else {
     const int cnt = p.sel_count[b * Hkv + h];
     const int n_sel = max(0, min(cnt, p.sel_width));
-    n_chunks = n_sel * cpp;
+    n_local = (n_sel > split) ? (n_sel - split + p.num_splits - 1) / p.num_splits * cpp : 0;
+    n_active = min(n_sel, p.num_splits);
     if (cnt > p.sel_width && split == 0 && threadIdx.x == 0 && p.status) atomicAdd(p.status, 1u);
   }
-  const int c_begin = split * p.cps;
-  const int c_end = min(n_chunks, c_begin + p.cps);
-  const int n_active = (n_chunks + p.cps - 1) / p.cps;
   const size_t row0 = (size_t)b * (Hkv * G) + (size_t)h * G;  // first query head row
 
-  if (c_begin >= c_end) {
+  if (n_local <= 0) {
     if (n_active == 0 && split == 0) {  // empty visible set: o = 0, lse2 = -inf
       asm volatile("griddepcontrol.wait;" ::: "memory");
       for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
@@ -711,7 +717,6 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
     }
     return;
   }
-  const int n_local = c_end - c_begin;
   const int n_stages = (n_local + kChunksPerStage - 1) / kChunksPerStage;
 
   if (threadIdx.x == 0) {
@@ -751,7 +756,7 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
     auto page_at = [&](int base) -> int {
       if (base >= n_local) return -1;
       if (!sparse) return (EXT ? cl.chunk(c_begin + base + lane) : c_begin + base + lane) / cpp;
-      const int v = (c_begin + base + lane) / cpp;
+      const int v = sel_entry(base + lane);
       return (v < p.sel_width) ? p.sel_pages[sel_row + v] : -1;
     };
     int nxt_page = page_at(pw * kBatch + kStride);
@@ -772,7 +777,8 @@ __global__ void __launch_bounds__(Warps<D, NARROW>::kThreads, Layout<D, NARROW>:
       uint32_t kv_bytes = 0, m_bytes = 0;
       const uint8_t *srcK = nullptr, *srcV = nullptr, *srcMK = nullptr, *srcMV = nullptr;
       if (lane < kBatch && base + lane < n_local) {
-        const int ci = (EXT && !sparse) ? cl.chunk(c_begin + base + lane) : c_begin + base + lane;
+        const int ci = sparse ? sel_entry(base + lane) * cpp + (base + lane) % cpp
+                              : (EXT ? cl.chunk(c_begin + base + lane) : c_begin + base + lane);
         const int cip = ci - (ci / cpp) * cpp;
         // anomalies are counted once per page: at its first listed chunk
         const bool first = cip == 0 || (EXT && !sparse && ci == cl.cw && (cl.cs == 0 || (cl.cs - 1) / cpp != ci / cpp));
@@ -1310,13 +1316,11 @@ __global__ void __launch_bounds__(kFoldThreads) decode_fold_kernel(const Params 
   const int hq = blockIdx.x, b = blockIdx.y;
   const int G = p.G, Hkv = p.Hkv;
   const int h = hq / G, g = hq - h * G;
-  const int cpp = p.P / kChunk;
   int seq_len = p.seq_lens[b];
   seq_len = max(0, min(seq_len, p.max_pages * p.P));
-  int n_chunks;
-  if (!p.sel_pages) n_chunks = dense_chunks(seq_len, p.window, p.sinks).n;
-  else n_chunks = max(0, min(p.sel_count[b * Hkv + h], p.sel_width)) * cpp;
-  const int n_active = (n_chunks + p.cps - 1) / p.cps;
+  int n_active;
+  if (!p.sel_pages) n_active = (dense_chunks(seq_len, p.window, p.sinks).n + p.cps - 1) / p.cps;
+  else n_active = min(max(0, min(p.sel_count[b * Hkv + h], p.sel_width)), p.num_splits);
   if (n_active <= 1) return;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const size_t bh = (size_t)b * Hkv + h;
@@ -1486,25 +1490,34 @@ static argus_status plan(const argus_decode_args* a, Plan* pl) {
   if (a->window_tokens > 0)   // sink chunks + window chunks (+1 when the window starts mid-chunk)
     max_chunks = std::min<long long>(max_chunks, ((long long)a->sink_tokens + kChunk - 1) / kChunk +
                                                      ((long long)a->window_tokens + kChunk - 1) / kChunk + 1);
-  long long cps;
-  if (a->num_splits > 0) {
-    cps = (max_chunks + a->num_splits - 1) / a->num_splits;
+  const long long rows = (long long)std::max(a->batch, 1) * g.n_kv_heads;
+  const long long slots = (long long)device_sm_count() * (g.head_dim == 64 ? 2 : 1);
+  if (a->sel_pages) {
+    // Selected pages are dealt round-robin over the splits, so every split of
+    // a row gets an equal share of its actual count, whatever part of the
+    // width it uses.  Each split is a CTA that pays the whole lookup-and-load
+    // latency: automatically, one wave (one CTA per resident slot).
+    long long ns = a->num_splits > 0 ? a->num_splits : std::max<long long>(1, slots / rows);
+    ns = std::min<long long>({ns, (long long)a->sel_width, (long long)kMaxSplits});
+    pl->num_splits = (int)std::max<long long>(1, ns);
+    pl->cps = (int)max_chunks;   // unused by a selection
   } else {
-    // Dense pages: about ten CTAs per SM, so that rows of unequal length
-    // balance.  Selected pages: the list width bounds the work but typically
-    // about half of it is used, and each split is a CTA that pays the whole
-    // lookup-and-load latency; one CTA per resident slot does best there.
-    const long long total = (long long)std::max(a->batch, 1) * g.n_kv_heads * max_chunks;
-    const long long slots = (long long)device_sm_count() * (g.head_dim == 64 ? 2 : 1);
-    // A sliding window gives every row the same bounded work: one wave of
-    // CTAs (about one per SM) beats ten short ones per SM there.
-    const long long target = a->sel_pages ? slots : (a->window_tokens > 0 ? 1LL : 10LL) * device_sm_count();
-    cps = std::max<long long>(cps_unit, (total + target - 1) / target);
+    long long cps;
+    if (a->num_splits > 0) {
+      cps = (max_chunks + a->num_splits - 1) / a->num_splits;
+    } else {
+      // About ten CTAs per SM, so that rows of unequal length balance.  A
+      // sliding window gives every row the same bounded work: one wave of
+      // CTAs (about one per SM) beats ten short ones per SM there.
+      const long long total = rows * max_chunks;
+      const long long target = (a->window_tokens > 0 ? 1LL : 10LL) * device_sm_count();
+      cps = std::max<long long>(cps_unit, (total + target - 1) / target);
+    }
+    cps = std::max<long long>(cps, (max_chunks + kMaxSplits - 1) / kMaxSplits);
+    cps = std::max<long long>(cps_unit, (cps + cps_unit - 1) / cps_unit * cps_unit);
+    pl->cps = (int)cps;
+    pl->num_splits = (int)std::max<long long>(1, (max_chunks + cps - 1) / cps);
   }
-  cps = std::max<long long>(cps, (max_chunks + kMaxSplits - 1) / kMaxSplits);
-  cps = std::max<long long>(cps_unit, (cps + cps_unit - 1) / cps_unit * cps_unit);
-  pl->cps = (int)cps;
-  pl->num_splits = (int)std::max<long long>(1, (max_chunks + cps - 1) / cps);
   if (pl->num_splits > 65535) return fail(ARGUS_E_UNSUPPORTED, "decode: too many splits");
   pl->part_o_bytes = (size_t)std::max(a->batch, 1) * g.n_kv_heads * pl->num_splits * G * g.head_dim * 4;
   pl->ws_bytes = pl->part_o_bytes +

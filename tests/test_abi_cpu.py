@@ -108,6 +108,13 @@ def test_codec_range_window_and_int2_checks_without_gpu():
     a.sel_pages = a.sel_count = ctypes.cast(ctypes.byref(sel), ctypes.c_void_p)
     a.sel_width = 4
     assert L.argus_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 2
+    # a selection's entries are dealt over at most sel_width splits: workspace
+    # = B * Hkv * splits * G * (D + 1) fp32 values
+    a.window_tokens = a.sink_tokens = 0
+    for req, splits in ((3, 3), (4, 4), (100, 4)):
+        a.num_splits = req
+        assert L.argus_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 0
+        assert n.value == 2 * 2 * splits * 4 * (128 + 1) * 4
     del keep
     # quantize: destination codec 7 is rejected before any device work
     g = argus.geom(8, 2, 128, 16)

@@ -103,7 +103,11 @@ def test_ragged_batch_permuted_slots_and_empty_rows():
         assert torch.all(out32[0] == 0) and torch.all(torch.isinf(lse[0]))
 
 
-def test_selected_page_lists_and_invalid_entries():
+@pytest.mark.parametrize("splits", [0, 1, 3, 50])
+def test_selected_page_lists_and_invalid_entries(splits):
+    """Selected entries are dealt round-robin over the splits: split counts
+    that do not divide a row's count, rows with fewer entries than splits, and
+    a request above the list width (clamped to it)."""
     Hq, Hkv, D, P = 32, 4, 128, 64
     maxp = 40
     lens = [40 * 64 - 10, 20 * 64 + 3]
@@ -127,7 +131,7 @@ def test_selected_page_lists_and_invalid_entries():
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     out, out32, lse, _ = run_decode(c, out_dtype=torch.bfloat16,
                                     sel=torch.from_numpy(sel).to(DEV), sel_count=torch.from_numpy(cnt).to(DEV),
-                                    sel_width=width, status=status)
+                                    sel_width=width, status=status, num_splits=splits)
     _check(c, out, out32, lse, sel=sel, cnt=cnt, width=width, expect_bad=2)
     assert int(status.item()) == 2
 
