@@ -283,7 +283,10 @@ argus_status argus_paged_decode_attn_noalloc(const argus_decode_args* args, void
  * (values above max_pages are clamped and counted as drops); ws of
  * argus_select_workspace_bytes bytes.  max_pages is at most 65535.
  * The kernels may start while their stream predecessor is still running
- * (programmatic dependent launch); every input is read after it completes.
+ * (programmatic dependent launch); every input is read after it completes
+ * (before that, the score grid only prefetches its slab ranges and the
+ * queries toward L2, a cache hint that reads nothing into the kernel), and
+ * the top-k grid lets its own successor start early in the same way.
  * ------------------------------------------------------------------------- */
 argus_status argus_select_workspace_bytes(const argus_geom* g, int32_t batch,
                                           int32_t max_pages, size_t* bytes);

@@ -12,18 +12,21 @@
 //   the lower page index; the newest page is always added; ascending order.
 //
 // GB300 design: two launches.  (1) score: the slab is the dominant HBM stream
-// (D bf16 per page and head); one wave of CTAs tiles (batch row, page range),
-// lanes read 16 bytes of a compressed key each, eight rows' loads in flight,
-// and fold eight rows' partial dot products across the head's lanes in one
-// transposed reduction; the G-query sum is formed once per CTA and kept in
-// registers; scores are stored as order-preserving uint32 keys.  Each CTA also
-// reports, per KV head, the 4 largest keys of its own page range.
+// (D bf16 per page and head); one wave of CTAs tiles (batch row, page range).
+// A CTA prefetches its range toward L2 before waiting for its stream
+// predecessor, then streams it into shared memory with bulk copies; lanes
+// read 16 bytes of a compressed key each and fold eight rows' partial dot
+// products across the head's lanes in one transposed reduction; the G-query
+// sum is formed once per CTA and kept in registers; scores are stored as
+// order-preserving uint32 keys.  Each CTA also reports, per KV head, the 4
+// largest keys of its own page range.
 // (2) top-k: one CTA per (batch row, KV head).  The row's k-th largest key T is
 // at least T0, the k-th largest of the reported keys (they are keys of
 // distinct pages of the row), and since the row's top k rarely crowd more than
 // 4 into one range, T0 is T or close to it: only the keys >= T0 -- about k of
 // them -- are searched.  The top-k grid starts behind the score grid with
-// programmatic dependent launch.  They are compacted in page order, one warp finds T
+// programmatic dependent launch, and releases its own successor at once (the
+// next score grid's prefetch then overlaps this top-k).  They are compacted in page order, one warp finds T
 // among them (two bits per round by warp reductions) and writes the chosen
 // pages, ascending, with ties to the lower page index.  Many keys >= T0 (heavy
 // ties) or rows longer than the registers hold take block-wide searches over
@@ -145,7 +148,24 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) score_kernel(i
   // the top-k grid may start its prologue now; it waits for this grid's keys
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // this grid itself may start during its stream predecessor's tail: every
-  // input is read after that predecessor completes
+  // input is read after that predecessor completes.  Before that, the CTA's
+  // slab range and its batch row's queries are prefetched toward L2: a
+  // prefetch only warms the cache (L2 is where the predecessor's writes land
+  // too), so the bulk copies after the wait see the current bytes, sooner.
+  if (threadIdx.x < 32) {
+    const int pb = blockIdx.x * ppc, pe = min(max_pages, pb + ppc);
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(ckeys + (((size_t)blockIdx.y * max_pages + pb) * Hkv) * D);
+    const uint32_t bytes = pb < pe ? (uint32_t)(pe - pb) * Hkv * D * 2 : 0u;
+    for (uint32_t off = threadIdx.x * (uint32_t)kPieceBytes; off < bytes; off += 32u * kPieceBytes)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src + off),
+                   "r"(min((uint32_t)kPieceBytes, bytes - off))
+                   : "memory");
+    if (threadIdx.x == 0 && blockIdx.x == 0)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(static_cast<const uint8_t*>(q) +
+                                                                       (size_t)blockIdx.y * Hkv * G * D * 2),
+                   "r"((uint32_t)(Hkv * G * D * 2))
+                   : "memory");
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // shared memory: the range's compressed keys [ppc * Hkv][D] bf16, the
   // G-query sums [Hkv][D] fp32, the range's order keys [ppc][Hkv], mbarriers
@@ -371,7 +391,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pag
   const int k = max(0, min(k_want, room));
   if (tid == 0) dropped += (uint32_t)(k_want - k);
   // launched behind the score grid with programmatic dependent launch: its
-  // keys are read after this wait
+  // keys are read after this wait.  Its own successor may start now (a decode
+  // or the next score grid waits for this grid before reading its results).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int KPT = kKeysPerThread;
   const bool in_regs = n_cand <= KPT * nthr;
