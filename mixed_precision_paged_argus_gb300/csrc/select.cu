@@ -21,14 +21,16 @@
 // order-preserving uint32 keys.  Each CTA also reports, per KV head, the 4
 // largest keys of its own page range.
 // (2) top-k: one CTA per (batch row, KV head).  The row's k-th largest key T is
-// at least T0, the k-th largest of the reported keys (they are keys of
-// distinct pages of the row), and since the row's top k rarely crowd more than
-// 4 into one range, T0 is T or close to it: only the keys >= T0 -- about k of
-// them -- are searched.  The top-k grid starts behind the score grid with
+// at least the k-th largest of the reported keys (they are keys of distinct
+// pages of the row), and since the row's top k rarely crowd more than 4 into
+// one range, that key is T or close to it.  T0, its top 16 bits (half the
+// search rounds), bounds T from below as well: only the keys >= T0 -- about k
+// of them -- are searched.  The top-k grid starts behind the score grid with
 // programmatic dependent launch, and releases its own successor at once (the
-// next score grid's prefetch then overlaps this top-k).  They are compacted in page order, one warp finds T
-// among them (two bits per round by warp reductions) and writes the chosen
-// pages, ascending, with ties to the lower page index.  Many keys >= T0 (heavy
+// next score grid's prefetch then overlaps this top-k).  They are compacted
+// in page order; one warp ranks them against each other (up to 64, two per
+// lane; beyond that it finds T two bits per round by warp reductions) and
+// writes the chosen pages, ascending, with ties to the lower page index.  Many keys >= T0 (heavy
 // ties) or rows longer than the registers hold take block-wide searches over
 // every key.
 #include <algorithm>
@@ -76,11 +78,14 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 // The kk-th largest of the values a warp holds (nv per lane; empty slots hold
 // 0, which no candidate -- always >= 1 -- counts): two bits per round, the
 // three candidate counts in two warp reductions.  No barrier.  (A key of 0 is
-// the order key of a negative NaN score: NaN scores are unordered.)
-template <int NV>
+// the order key of a negative NaN score: NaN scores are unordered.)  With
+// kLowBit > 0 the bits below kLowBit are left 0: the result is then the
+// largest multiple of 2^kLowBit with at least kk values at or above it, a
+// lower bound of the kk-th largest found in fewer rounds.
+template <int NV, int kLowBit = 0>
 __device__ __forceinline__ uint32_t warp_kth(const uint32_t (&vals)[NV], int kk) {
   uint32_t t = 0u;
-  for (int bb = 30; bb >= 0; bb -= 2) {
+  for (int bb = 30; bb >= kLowBit; bb -= 2) {
     const uint32_t c1 = t | (1u << bb), c2 = t | (2u << bb), c3 = t | (3u << bb);
     uint32_t a = 0u, c = 0u;
 #pragma unroll
@@ -408,9 +413,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pag
       const int pk = KPT * tid + j;
       kr[j] = pk < n_cand ? keys[pk] : 0u;
     }
-    // T0 = the k-th largest of the keys the ranges reported: real keys of
-    // distinct pages, so T0 <= T, the row's k-th largest (0 when the report is
-    // too long to hold, or holds fewer than k keys)
+    // T0 <= the k-th largest of the keys the ranges reported (real keys of
+    // distinct pages), so T0 <= T, the row's k-th largest: its top 16 bits,
+    // which also admits the few keys just below it in the same 16-bit bucket
+    // (0 when the report is too long to hold, or holds fewer than k keys)
     // (warp 0 alone, then one barrier)
     const int n_ranges = min(n_chunks, (n_cand + ppc - 1) / ppc);
     const int n_emit = n_ranges * kEmit;
@@ -424,7 +430,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pag
           const int i = lane + 32 * m;
           ev[m] = i < n_emit ? er[i] : 0u;
         }
-        t0w = warp_kth(ev, k);
+        t0w = warp_kth<8, 16>(ev, k);
       } else if (n_emit >= k && n_emit <= 32 * kSurvivorsPerLane) {
         uint32_t ev[kSurvivorsPerLane];
 #pragma unroll
@@ -432,7 +438,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pag
           const int i = lane + 32 * m;
           ev[m] = i < n_emit ? er[i] : 0u;
         }
-        t0w = warp_kth(ev, k);
+        t0w = warp_kth<kSurvivorsPerLane, 16>(ev, k);
       }
       if (lane == 0) sh_t0 = t0w;
     }
@@ -456,36 +462,54 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pag
       __syncthreads();
       if (warp == 0) {
         // survivor i = lane + 32 m: index order is page order
-        uint32_t cv[kSurvivorsPerLane];
-#pragma unroll
-        for (int m = 0; m < kSurvivorsPerLane; ++m) {
-          const int i = lane + 32 * m;
-          cv[m] = i < M ? sh_cand[i] : 0u;
-        }
-        uint32_t T;
-        if (M <= 64) {   // the usual case: about k survivors, two per lane
-          const uint32_t c2[2] = {cv[0], cv[1]};
-          T = warp_kth(c2, k);
-        } else {
-          T = warp_kth(cv, k);
-        }
-        uint32_t gt = 0u;
-#pragma unroll
-        for (int m = 0; m < kSurvivorsPerLane; ++m) gt += cv[m] > T ? 1u : 0u;
-        gt = __reduce_add_sync(0xffffffffu, gt);
-        const int k_rem = k - (int)gt;   // ties at T taken, lowest pages first
-        int written = 0, ties_seen = 0;
         const uint32_t below = (1u << lane) - 1u;
+        int written = 0;
+        if (M <= 64) {
+          // the usual case, about k survivors, two per lane: each is ranked
+          // against all the others, rank_i = #{j : c_j > c_i} + #{j < i :
+          // c_j == c_i} (a permutation of 0 .. M-1); the k survivors of rank
+          // below k are the row's top k, ties to the lower page
+          const uint32_t x0 = lane < M ? sh_cand[lane] : 0u;
+          const uint32_t x1 = lane + 32 < M ? sh_cand[lane + 32] : 0u;
+          int r0 = 0, r1 = 0;
+#pragma unroll 8
+          for (int src = 0; src < 32; ++src) {
+            const uint32_t y0 = __shfl_sync(0xffffffffu, x0, src);   // survivor src
+            const uint32_t y1 = __shfl_sync(0xffffffffu, x1, src);   // survivor src + 32
+            const bool v0 = src < M, v1 = src + 32 < M;
+            r0 += ((v0 && (y0 > x0 || (y0 == x0 && src < lane))) ? 1 : 0) + ((v1 && y1 > x0) ? 1 : 0);
+            r1 += ((v0 && y0 >= x1) ? 1 : 0) + ((v1 && (y1 > x1 || (y1 == x1 && src < lane))) ? 1 : 0);
+          }
+          const bool take0 = lane < M && r0 < k, take1 = lane + 32 < M && r1 < k;
+          const uint32_t b0 = __ballot_sync(0xffffffffu, take0), b1 = __ballot_sync(0xffffffffu, take1);
+          if (take0) out[__popc(b0 & below)] = sh_page[lane];
+          if (take1) out[__popc(b0) + __popc(b1 & below)] = sh_page[lane + 32];
+          written = __popc(b0) + __popc(b1);
+        } else {
+          uint32_t cv[kSurvivorsPerLane];
 #pragma unroll
-        for (int m = 0; m < kSurvivorsPerLane; ++m) {
-          const int i = lane + 32 * m;
-          const bool tie = i < M && cv[m] == T;
-          const uint32_t tb = __ballot_sync(0xffffffffu, tie);
-          const bool take = (i < M && cv[m] > T) || (tie && ties_seen + __popc(tb & below) < k_rem);
-          const uint32_t kb = __ballot_sync(0xffffffffu, take);
-          if (take) out[written + __popc(kb & below)] = sh_page[i];
-          written += __popc(kb);
-          ties_seen += __popc(tb);
+          for (int m = 0; m < kSurvivorsPerLane; ++m) {
+            const int i = lane + 32 * m;
+            cv[m] = i < M ? sh_cand[i] : 0u;
+          }
+          const uint32_t T = warp_kth(cv, k);
+          uint32_t gt = 0u;
+#pragma unroll
+          for (int m = 0; m < kSurvivorsPerLane; ++m) gt += cv[m] > T ? 1u : 0u;
+          gt = __reduce_add_sync(0xffffffffu, gt);
+          const int k_rem = k - (int)gt;   // ties at T taken, lowest pages first
+          int ties_seen = 0;
+#pragma unroll
+          for (int m = 0; m < kSurvivorsPerLane; ++m) {
+            const int i = lane + 32 * m;
+            const bool tie = i < M && cv[m] == T;
+            const uint32_t tb = __ballot_sync(0xffffffffu, tie);
+            const bool take = (i < M && cv[m] > T) || (tie && ties_seen + __popc(tb & below) < k_rem);
+            const uint32_t kb = __ballot_sync(0xffffffffu, take);
+            if (take) out[written + __popc(kb & below)] = sh_page[i];
+            written += __popc(kb);
+            ties_seen += __popc(tb);
+          }
         }
         // written == k <= room; the newest page (larger than every candidate) last
         int total = written;
