@@ -18,12 +18,13 @@
 // read 16 bytes of a compressed key each and fold eight rows' partial dot
 // products across the head's lanes in one transposed reduction; the G-query
 // sum is formed once per CTA and kept in registers; scores are stored as
-// order-preserving uint32 keys.  Each CTA also reports, per KV head, the 4
+// order-preserving uint32 keys.  Each CTA also reports, per KV head, the 2
 // largest keys of its own page range.
 // (2) top-k: one CTA per (batch row, KV head).  The row's k-th largest key T is
 // at least the k-th largest of the reported keys (they are keys of distinct
-// pages of the row), and since the row's top k rarely crowd more than 4 into
-// one range, that key is T or close to it.  T0, its top 16 bits (half the
+// pages of the row), and since the row's top k rarely crowd more than 2 into
+// one range (k = 32 over 57 ranges of 72 pages in the sparse workload), that
+// key is T or close to it.  T0, its top 16 bits (half the
 // search rounds), bounds T from below as well: only the keys >= T0 -- about k
 // of them -- are searched.  The top-k grid starts behind the score grid with
 // programmatic dependent launch, and releases its own successor at once (the
@@ -47,7 +48,7 @@ constexpr int kKeysPerThread = 8;             // top-k keys held in registers pe
 constexpr int kRowBatch = 8;               // compressed-key loads in flight per lane
 constexpr int kTopkSmemKeys = 40 * 1024;   // rows up to this many pages are staged in shared memory
 constexpr int kMaxPpc = 256;               // pages per score CTA (its keys per head in registers)
-constexpr int kEmit = 4;                   // largest keys each score CTA reports per KV head
+constexpr int kEmit = 2;                   // largest keys each score CTA reports per KV head
 constexpr long long kScoreSmemBytes = 75 * 1024;   // a score CTA's shared memory (3 CTAs per SM)
 constexpr int kPieceBytes = 16384;         // bulk-copy pieces of a score CTA's slab range, one mbarrier each
 constexpr int kMaxPieces = 8;
@@ -423,7 +424,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(int Hkv, int max_pag
     if (warp == 0) {
       uint32_t t0w = 0u;
       const uint32_t* er = emit_g + ((size_t)b * Hkv + h) * n_chunks * kEmit;
-      if (n_emit >= k && n_emit <= 256) {   // eight per lane
+      if (n_emit >= k && n_emit <= 128) {   // four per lane
+        uint32_t ev[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int i = lane + 32 * m;
+          ev[m] = i < n_emit ? er[i] : 0u;
+        }
+        t0w = warp_kth<4, 16>(ev, k);
+      } else if (n_emit >= k && n_emit <= 256) {   // eight per lane
         uint32_t ev[8];
 #pragma unroll
         for (int m = 0; m < 8; ++m) {

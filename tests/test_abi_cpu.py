@@ -70,7 +70,7 @@ def test_host_validation_without_gpu():
     assert L.argus_decode_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 0
     g = argus.geom(8, 2, 128, 16)
     assert L.argus_select_workspace_bytes(ctypes.byref(g), 2, 10, ctypes.byref(n)) == 0
-    assert n.value == 2 * 2 * 10 * 4 + 2 * 2 * 2 * 4 * 4   # keys, then 4 reported keys of ceil(10 / 8) ranges
+    assert n.value == 2 * 2 * 10 * 4 + 2 * 2 * 2 * 2 * 4   # keys, then 2 reported keys of ceil(10 / 8) ranges
 
 
 def test_codec_range_window_and_int2_checks_without_gpu():
