@@ -718,7 +718,8 @@ static argus_status launch3(const QParams& p, cudaStream_t s) {
   const bool small = (long long)p.P * D <= 32 * kRegVecs * 8;
   if (small) {
     const long long blocks_needed = (units + (kCtaThreads / 32) - 1) / (kCtaThreads / 32);
-    const int blocks = (int)std::max<long long>(1, std::min<long long>(blocks_needed, (long long)sms * 4));
+    // one wave: two CTAs per SM are resident at this kernel's register count
+    const int blocks = (int)std::max<long long>(1, std::min<long long>(blocks_needed, (long long)sms * 2));
     if (p.ckey) quantize_small_kernel<D, SBF16, CODEC, true><<<blocks, kCtaThreads, 0, s>>>(p);
     else quantize_small_kernel<D, SBF16, CODEC, false><<<blocks, kCtaThreads, 0, s>>>(p);
   } else {
